@@ -1,0 +1,416 @@
+"""Benchmark: one decode step of split-KV attention on the 128K-context GQA workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
+
+Workload (default): bf16, B=1, Hq=64, Hkv=8 (G=8), d=128, L=131072, contiguous KV
+cache (512 MiB of K+V, four times the L2), split count from the library heuristic.
+A step is one full pass of the hot path: the split-KV partial kernel plus the LSE
+merge kernel, through the C ABI (fd_decode_attention).
+
+Prints ONE JSON line.  ``value`` is the whole-job KV-read throughput (GB/s) over the
+K timed steps (device time, CUDA events, max over ranks); ``ms_per_step`` and
+``us_per_step`` give the step time.  Also reported:
+  roofline      the partial kernel alone: algorithmic KV bytes per launch / its mean
+                CUDA-event duration, against the measured HBM copy bandwidth;
+  e2e           the same metric through the public Python API with the step's inputs
+                copied from pinned host memory and the result read back every step;
+  cpu_baseline  the fp64 oracle timed on the host cores on a bounded sample;
+  clocks        SM clocks and throttle reasons sampled during the timed region.
+
+With N > 1 (torchrun) every rank runs its own full replica of the workload (weak
+scaling, no collective on the data path).  ``--impl reference`` times the fp64 oracle
+instead (rank 0 only; other ranks exit 0 at once).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import datetime
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "decode-step µs and KV-read GB/s (% of GB300 HBM peak), GQA 128K ctx"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
+    ap.add_argument("--config", type=int, default=3, help="workload number (1-5)")
+    ap.add_argument("--num-splits", type=int, default=0, help="0 = library heuristic")
+    ap.add_argument("--path", choices=["auto", "simt", "mma"], default="auto")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy, burst)"
+    except Exception:  # noqa: BLE001
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_attention_05_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            rec = json.load(f)
+        e = rec["entries"][kernel + "|" + workload]
+        if e["source_hash"] != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:  # noqa: BLE001
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi in the background (20 ms period); keeps samples inside a window."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:  # noqa: BLE001
+            self.proc = None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:  # noqa: BLE001
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = []
+        for line in self.out.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.out.name)
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        if not inside and rows:                       # region shorter than the period
+            inside = sorted(rows, key=lambda r: abs(r[0] - 0.5 * (t0 + t1)))[:3]
+        if not inside:
+            return None
+        mhz = sorted(r[1] for r in inside)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": inside[0][2], "reasons": reasons,
+                "samples": len(inside)}
+
+
+def oracle_sample(w, budget_s: float):
+    """Time the fp64 oracle (as it stands) on a bounded sample of the workload.
+
+    The sample is `rows` query heads (spread over the kv heads) over the first
+    `tokens` keys of each row, sized to take roughly `budget_s` seconds.  Returns
+    (KV GB/s in the step's terms, threads used, sample description, seconds)."""
+    import oracle
+    q, k, v, lens, bt, ps = w.oracle_arrays()
+    threads = oracle.max_threads()
+    B, Hq = w.B, w.Hq
+    rows = list(range(0, B * Hq, max(1, (B * Hq) // threads)))[:threads]
+    L = int(lens.max())
+
+    def run(tokens):
+        sl = lens.copy()
+        sl[:] = min(tokens, L)
+        t0 = time.perf_counter()
+        oracle.decode(q, k, v, sl, block_table=bt, page_size=ps, rows=rows)
+        return time.perf_counter() - t0
+
+    probe = min(L, 4096)
+    t_probe = run(probe)
+    tokens = int(min(L, max(probe, probe * budget_s / max(t_probe, 1e-6))))
+    t = run(tokens)
+    # Fraction of one full step this sample covers: rows / (B * Hq) of the rows, and
+    # tokens / L of each row (all rows have length L in the timed workloads).
+    frac = (len(rows) / (B * Hq)) * (tokens / L)
+    step_s = t / frac
+    gbs = w.kv_bytes() / step_s / 1e9
+    desc = "%d of %d query heads x first %d of %d keys (%.4f of a step), %.1f s" % (
+        len(rows), B * Hq, tokens, L, frac, t)
+    return gbs, min(threads, len(rows)), desc, t, step_s
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    w = workloads.CONFIGS[args.config]()
+    import oracle
+    q, k, v, lens, bt, ps = w.oracle_arrays()
+    threads = oracle.max_threads()
+    B, Hq = w.B, w.Hq
+    rows = list(range(0, B * Hq, max(1, (B * Hq) // threads)))[:threads]
+    L = int(lens.max())
+    # Size each step so that warm-up + timed steps end within ~90 s.
+    sl = lens.copy()
+    sl[:] = min(L, 1024)
+    t0 = time.perf_counter()
+    oracle.decode(q, k, v, sl, block_table=bt, page_size=ps, rows=rows)
+    t_probe = time.perf_counter() - t0
+    per_step = 90.0 / max(1, args.steps + args.warmup)
+    tokens = int(max(16, min(L, 1024 * per_step / max(t_probe, 1e-6))))
+    sl[:] = tokens
+    for _ in range(args.warmup):
+        oracle.decode(q, k, v, sl, block_table=bt, page_size=ps, rows=rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode(q, k, v, sl, block_table=bt, page_size=ps, rows=rows)
+    elapsed = time.perf_counter() - t0
+    frac = (len(rows) / (B * Hq)) * (tokens / L)
+    step_s = elapsed / args.steps / frac
+    gbs = w.kv_bytes() / step_s / 1e9
+    sample = "%d of %d query heads x first %d of %d keys per step (%.5f of a step)" % (
+        len(rows), B * Hq, tokens, L, frac)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_s * 1e3, 3), "us_per_step": round(step_s * 1e6, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": min(threads, len(rows)),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_fd(args):
+    world, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import decode_attention_05_gb300 as fd
+    from decode_attention_05_gb300._binding import tensor_desc
+    L = fd.lib()
+    fd.set_path({"auto": fd.FD_PATH_AUTO, "simt": fd.FD_PATH_SIMT, "mma": fd.FD_PATH_MMA}[args.path])
+
+    w_cpu = workloads.CONFIGS[args.config]()
+    w = w_cpu.to("cuda")
+    B, Hq, d, Hkv = w.B, w.Hq, w.d, w.Hkv
+    S = fd.resolve_num_splits(B, Hq, Hkv, d, w.L_cap, args.num_splits or w.num_splits)
+    ws = torch.zeros(fd.workspace_size(B, Hq, Hkv, d, S), dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, Hq, d), dtype=w.out_dtype, device="cuda")
+    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+    dq, dk, dv, dbt, do = (tensor_desc(w.q), tensor_desc(w.k), tensor_desc(w.v),
+                           tensor_desc(w.block_table), tensor_desc(out))
+    bt_ref = None if dbt is None else ctypes.byref(dbt)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream or None
+    ws_bytes = ws.numel()
+    args_step = (ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), w.seq_lens.data_ptr(),
+                 bt_ref, w.page_size, S, ctypes.byref(do), lse.data_ptr(), ws.data_ptr(),
+                 ws_bytes, sh)
+
+    def step():
+        st = L.fd_decode_attention(*args_step)
+        if st:
+            raise fd.FdError(st, L.fd_last_error().decode())
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    kv_bytes = w.kv_bytes()
+    for _ in range(max(3, args.warmup)):
+        step()
+    if fd.read_device_error(ws) != 0:
+        raise RuntimeError("device error flags set during warm-up")
+
+    sampler = ClockSampler(local)
+    time.sleep(0.3)                                   # let nvidia-smi start sampling
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    e1.synchronize()
+    t_wall1 = time.time()
+    barrier()
+    ms = e0.elapsed_time(e1)
+    clocks = sampler.stop(t_wall0, t_wall1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * kv_bytes * args.steps / (ms * 1e-3) / 1e9
+
+    # ---- roofline of the dominant kernel: the partial pass alone, K launches
+    args_partial = (ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), w.seq_lens.data_ptr(),
+                    bt_ref, w.page_size, S, ws.data_ptr(), ws_bytes, sh)
+    for _ in range(3):
+        L.fd_decode_partial(*args_partial)
+    barrier()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.steps):
+        st = L.fd_decode_partial(*args_partial)
+        if st:
+            raise fd.FdError(st, L.fd_last_error().decode())
+    e3.record(stream)
+    e3.synchronize()
+    partial_ms = e2.elapsed_time(e3) / args.steps
+    lse_part, o_part = fd.workspace_partials(ws, B, Hq, d, S)
+    dout = tensor_desc(out)
+    e4, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e4.record(stream)
+    for _ in range(args.steps):
+        L.fd_merge_partials(B, Hq, d, S, lse_part.data_ptr(), o_part.data_ptr(),
+                            ctypes.byref(dout), lse.data_ptr(), sh)
+    e5.record(stream)
+    e5.synchronize()
+    merge_ms = e4.elapsed_time(e5) / args.steps
+    peak, peak_src = measured_peak()
+    achieved = kv_bytes / (partial_ms * 1e-3) / 1e9
+    path_name = "mma" if (args.path == "mma" or (args.path == "auto" and w.q.dtype == torch.bfloat16)) else "simt"
+    kernel = "fd_partial_%s_kernel" % path_name
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kernel, w.name),
+                "kernel": kernel, "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": kv_bytes,
+                "partial_us": round(partial_ms * 1e3, 2), "merge_us": round(merge_ms * 1e3, 2)}
+
+    # ---- end to end through the public API, host buffers, copies inside the timed region
+    pin = lambda t: t.pin_memory()
+    qh, kh, vh, sh_lens = pin(w_cpu.q), pin(w_cpu.k), pin(w_cpu.v), pin(w_cpu.seq_lens)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh, sh_lens))
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def e2e_step():
+        w.q.copy_(qh, non_blocking=True)
+        w.k.copy_(kh, non_blocking=True)
+        w.v.copy_(vh, non_blocking=True)
+        w.seq_lens.copy_(sh_lens, non_blocking=True)
+        fd.decode_attention(w.q, w.k, w.v, w.seq_lens, w.block_table, w.page_size, S, out=out,
+                            lse_out=lse, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e6, e7 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e6.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e7.record(stream)
+    e7.synchronize()
+    e2e_ms = e6.elapsed_time(e7) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": round(e2e_ms, 3)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, cores, desc, _, step_s = oracle_sample(w_cpu, args.cpu_budget_s)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": desc, "step_ms_extrapolated": round(step_s * 1e3, 1)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "us_per_step": round(ms_per_step * 1e3, 2),
+            "hbm_frac_step": round(value / world / peak, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.q.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d,
+                       "L": int(w.seq_lens.max()), "num_splits": S, "path": path_name,
+                       "kv_bytes_per_step": kv_bytes,
+                       "l2": "inputs larger than L2 (KV %d MiB vs 126 MiB L2), no flush" % (kv_bytes >> 20),
+                       "parallelism": "replicas x%d" % world},
+            "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
+            "gpu_launches": 2 * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_fd(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

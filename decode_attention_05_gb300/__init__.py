@@ -1,0 +1,15 @@
+"""Split-KV (Flash-Decoding) single-token decode attention for GB300 (sm_103a).
+
+A thin ctypes binding over ``libfd.so`` (C ABI in ``include/fd.h``).  Every step of
+the computation runs in the library's CUDA kernels; this module only marshals torch
+tensors into ``fd_tensor`` descriptors, passes the current CUDA stream, and turns
+status codes into exceptions.  There is no CPU fallback: if the library is missing
+or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+from ._binding import (  # noqa: F401
+    FD_PATH_AUTO, FD_PATH_MMA, FD_PATH_SIMT, FdError, Plan, decode_attention, decode_partial,
+    get_path, lib, library_path, merge_partials, num_splits_heuristic, read_device_error,
+    resolve_num_splits, set_path, workspace_init, workspace_partials, workspace_size,
+)

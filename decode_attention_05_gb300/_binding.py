@@ -1,0 +1,306 @@
+"""ctypes binding of libfd (see include/fd.h for the meaning of every argument)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+FD_OK = 0
+FD_ERR_DEVICE_FLAG = 5
+FD_F32, FD_BF16, FD_I32 = 0, 1, 2
+FD_PATH_AUTO, FD_PATH_SIMT, FD_PATH_MMA = 0, 1, 2
+
+_STATUS = {0: "FD_OK", 1: "FD_ERR_INVALID_ARG", 2: "FD_ERR_UNSUPPORTED",
+           3: "FD_ERR_WORKSPACE_TOO_SMALL", 4: "FD_ERR_CUDA", 5: "FD_ERR_DEVICE_FLAG"}
+
+
+class FdError(RuntimeError):
+    """A libfd call returned a status other than FD_OK."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (_STATUS.get(status, status), message))
+        self.status = status
+
+
+class FdTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libfd.so (build it first if it is missing or stale).  Raises if that fails."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            if not os.path.exists(path):
+                raise ImportError("libfd.so is missing at %s" % path)
+            L = ctypes.CDLL(path)
+            _declare(L)
+            _lib = L
+    return _lib
+
+
+def _declare(L):
+    P = ctypes.POINTER(FdTensor)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    L.fd_decode_attention.restype = ctypes.c_int
+    L.fd_decode_attention.argtypes = [P, P, P, vp, P, i32, i32, P, vp, vp, sz, vp]
+    L.fd_decode_partial.restype = ctypes.c_int
+    L.fd_decode_partial.argtypes = [P, P, P, vp, P, i32, i32, vp, sz, vp]
+    L.fd_workspace_partials.restype = ctypes.c_int
+    L.fd_workspace_partials.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(vp),
+                                        ctypes.POINTER(vp)]
+    L.fd_merge_partials.restype = ctypes.c_int
+    L.fd_merge_partials.argtypes = [i32, i32, i32, i32, vp, vp, P, vp, vp]
+    L.fd_workspace_size.restype = sz
+    L.fd_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    L.fd_num_splits_heuristic.restype = i32
+    L.fd_num_splits_heuristic.argtypes = [i32, i32, i32, i32, i64, i32]
+    L.fd_resolve_num_splits.restype = i32
+    L.fd_resolve_num_splits.argtypes = [i32, i32, i32, i32, i64, i32]
+    L.fd_workspace_init.restype = ctypes.c_int
+    L.fd_workspace_init.argtypes = [vp, sz, vp]
+    L.fd_read_device_error.restype = ctypes.c_int
+    L.fd_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+    L.fd_plan_create.restype = ctypes.c_int
+    L.fd_plan_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i64, i32]
+    L.fd_plan_num_splits.restype = i32
+    L.fd_plan_num_splits.argtypes = [vp]
+    L.fd_plan_workspace_bytes.restype = sz
+    L.fd_plan_workspace_bytes.argtypes = [vp]
+    L.fd_plan_workspace.restype = vp
+    L.fd_plan_workspace.argtypes = [vp]
+    L.fd_plan_decode.restype = ctypes.c_int
+    L.fd_plan_decode.argtypes = [vp, P, P, P, vp, P, i32, P, vp, vp]
+    L.fd_plan_resize.restype = ctypes.c_int
+    L.fd_plan_resize.argtypes = [vp, i32]
+    L.fd_plan_destroy.restype = None
+    L.fd_plan_destroy.argtypes = [vp]
+    L.fd_set_path.restype = ctypes.c_int
+    L.fd_set_path.argtypes = [i32]
+    L.fd_get_path.restype = i32
+    L.fd_get_path.argtypes = []
+    L.fd_status_string.restype = ctypes.c_char_p
+    L.fd_status_string.argtypes = [ctypes.c_int]
+    L.fd_last_error.restype = ctypes.c_char_p
+    L.fd_last_error.argtypes = []
+    L.fd_version.restype = ctypes.c_char_p
+    L.fd_version.argtypes = []
+
+
+def _check(status: int):
+    if status != FD_OK:
+        raise FdError(status, lib().fd_last_error().decode(errors="replace"))
+
+
+_DTYPES = {torch.float32: FD_F32, torch.bfloat16: FD_BF16, torch.int32: FD_I32}
+
+
+def tensor_desc(t: Optional[torch.Tensor]) -> Optional[FdTensor]:
+    """Describe a torch tensor (up to 4-D) as an fd_tensor; strides in elements."""
+    if t is None:
+        return None
+    if t.dtype not in _DTYPES:
+        raise TypeError("unsupported dtype %s" % t.dtype)
+    if t.dim() > 4:
+        raise ValueError("fd_tensor holds at most 4 dims")
+    d = FdTensor()
+    d.data = t.data_ptr()
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _ref(x):
+    return None if x is None else ctypes.byref(x)
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    h = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return h or None
+
+
+def workspace_size(B: int, Hq: int, Hkv: int, d: int, num_splits: int) -> int:
+    return int(lib().fd_workspace_size(B, Hq, Hkv, d, num_splits))
+
+
+def num_splits_heuristic(B: int, Hq: int, Hkv: int, d: int, L_cap: int, num_sms: int) -> int:
+    return int(lib().fd_num_splits_heuristic(B, Hq, Hkv, d, L_cap, num_sms))
+
+
+def resolve_num_splits(B: int, Hq: int, Hkv: int, d: int, L_cap: int, num_splits: int) -> int:
+    return int(lib().fd_resolve_num_splits(B, Hq, Hkv, d, L_cap, num_splits))
+
+
+def set_path(path: int):
+    _check(lib().fd_set_path(path))
+
+
+def get_path() -> int:
+    return int(lib().fd_get_path())
+
+
+def workspace_init(ws: torch.Tensor, stream=None):
+    _check(lib().fd_workspace_init(ws.data_ptr(), ws.numel() * ws.element_size(),
+                                   _stream_handle(stream)))
+
+
+def read_device_error(ws: torch.Tensor, stream=None) -> int:
+    """Synchronise, return the workspace's device error flags and clear them."""
+    flags = ctypes.c_uint32(0)
+    st = lib().fd_read_device_error(ws.data_ptr(), _stream_handle(stream), ctypes.byref(flags))
+    if st not in (FD_OK, FD_ERR_DEVICE_FLAG):
+        _check(st)
+    return int(flags.value)
+
+
+def _cap(k_cache, block_table, page_size):
+    return k_cache.shape[2] if block_table is None else block_table.shape[1] * page_size
+
+
+def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                     seq_lens: torch.Tensor, block_table: Optional[torch.Tensor] = None,
+                     page_size: int = 0, num_splits: int = 0,
+                     out: Optional[torch.Tensor] = None, lse_out: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None, out_dtype=None,
+                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Run fd_decode_attention on the current CUDA stream; returns (out, lse_out).
+
+    Missing ``out``/``lse_out``/``workspace`` buffers are allocated with torch (a
+    fresh workspace is zero-filled); the library itself allocates nothing.
+    """
+    L = lib()
+    B, Hq, d = q.shape
+    Hkv = k_cache.shape[1]
+    S = resolve_num_splits(B, Hq, Hkv, d, _cap(k_cache, block_table, page_size), num_splits)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=out_dtype or q.dtype, device=q.device)
+    if lse_out is None:
+        lse_out = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.zeros(workspace_size(B, Hq, Hkv, d, S), dtype=torch.uint8,
+                                device=q.device)
+    if seq_lens.dtype != torch.int32:
+        raise TypeError("seq_lens must be int32")
+    dq, dk, dv, dbt, do = (tensor_desc(q), tensor_desc(k_cache), tensor_desc(v_cache),
+                           tensor_desc(block_table), tensor_desc(out))
+    st = L.fd_decode_attention(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv),
+                               seq_lens.data_ptr(), _ref(dbt), page_size, S, ctypes.byref(do),
+                               lse_out.data_ptr(), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(),
+                               _stream_handle(stream))
+    _check(st)
+    return out, lse_out
+
+
+def decode_partial(q, k_cache, v_cache, seq_lens, workspace: torch.Tensor, block_table=None,
+                   page_size: int = 0, num_splits: int = 0, stream=None) -> int:
+    """Partial pass only (fd_decode_partial); returns the split count used."""
+    B, Hq, d = q.shape
+    S = resolve_num_splits(B, Hq, k_cache.shape[1], d, _cap(k_cache, block_table, page_size),
+                           num_splits)
+    dq, dk, dv, dbt = tensor_desc(q), tensor_desc(k_cache), tensor_desc(v_cache), tensor_desc(block_table)
+    _check(lib().fd_decode_partial(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv),
+                                   seq_lens.data_ptr(), _ref(dbt), page_size, S,
+                                   workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                   _stream_handle(stream)))
+    return S
+
+
+def workspace_partials(workspace: torch.Tensor, B: int, Hq: int, d: int, num_splits: int):
+    """Views (lse_part [B, Hq, S], o_part [B, Hq, S, d]) of the partials in a workspace."""
+    lp, op = ctypes.c_void_p(), ctypes.c_void_p()
+    _check(lib().fd_workspace_partials(workspace.data_ptr(), B, Hq, d, num_splits,
+                                       ctypes.byref(lp), ctypes.byref(op)))
+    base = workspace.data_ptr()
+    raw = workspace.view(torch.uint8)
+    lo = (lp.value - base)
+    oo = (op.value - base)
+    lse = raw[lo:lo + B * Hq * num_splits * 4].view(torch.float32).view(B, Hq, num_splits)
+    o = raw[oo:oo + B * Hq * num_splits * d * 4].view(torch.float32).view(B, Hq, num_splits, d)
+    return lse, o
+
+
+def merge_partials(lse_part: torch.Tensor, o_part: torch.Tensor, out: Optional[torch.Tensor] = None,
+                   lse_out: Optional[torch.Tensor] = None, out_dtype=torch.float32, stream=None):
+    """Merge pass only (fd_merge_partials) over [B, Hq, S] LSEs and [B, Hq, S, d] outputs."""
+    B, Hq, S, d = o_part.shape
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=out_dtype, device=o_part.device)
+    if lse_out is None:
+        lse_out = torch.empty((B, Hq), dtype=torch.float32, device=o_part.device)
+    if not (lse_part.is_contiguous() and o_part.is_contiguous()):
+        raise ValueError("lse_part and o_part must be contiguous")
+    do = tensor_desc(out)
+    _check(lib().fd_merge_partials(B, Hq, d, S, lse_part.data_ptr(), o_part.data_ptr(),
+                                   ctypes.byref(do), lse_out.data_ptr(), _stream_handle(stream)))
+    return out, lse_out
+
+
+class Plan:
+    """fd_plan: fixed sizes and split count, owning its workspace and completion event."""
+
+    def __init__(self, B: int, Hq: int, Hkv: int, d: int, L_cap: int, num_splits: int = 0):
+        self._h = ctypes.c_void_p()
+        _check(lib().fd_plan_create(ctypes.byref(self._h), B, Hq, Hkv, d, L_cap, num_splits))
+
+    @property
+    def num_splits(self) -> int:
+        return int(lib().fd_plan_num_splits(self._h))
+
+    @property
+    def workspace_bytes(self) -> int:
+        return int(lib().fd_plan_workspace_bytes(self._h))
+
+    @property
+    def workspace_ptr(self) -> int:
+        return int(lib().fd_plan_workspace(self._h) or 0)
+
+    def decode(self, q, k_cache, v_cache, seq_lens, block_table=None, page_size=0, out=None,
+               lse_out=None, out_dtype=None, stream=None):
+        B, Hq, d = q.shape
+        if out is None:
+            out = torch.empty((B, Hq, d), dtype=out_dtype or q.dtype, device=q.device)
+        if lse_out is None:
+            lse_out = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        dq, dk, dv, dbt, do = (tensor_desc(q), tensor_desc(k_cache), tensor_desc(v_cache),
+                               tensor_desc(block_table), tensor_desc(out))
+        _check(lib().fd_plan_decode(self._h, ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv),
+                                    seq_lens.data_ptr(), _ref(dbt), page_size, ctypes.byref(do),
+                                    lse_out.data_ptr(), _stream_handle(stream)))
+        return out, lse_out
+
+    def resize(self, num_splits: int):
+        _check(lib().fd_plan_resize(self._h, num_splits))
+
+    def close(self):
+        if self._h:
+            lib().fd_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 -- interpreter shutdown
+            pass

@@ -1,0 +1,593 @@
+// fd_api.cu -- the C ABI of libfd (include/fd.h): argument validation, the split-count
+// planner, workspace layout, TMA tensor maps, kernel dispatch, and plans.
+//
+// Host code only (the kernels live in fd_partial_*.cu and fd_combine.cu).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "fd.h"
+#include "fd_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+std::atomic<int> g_path{FD_PATH_AUTO};
+
+fd_status fail(fd_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+constexpr size_t kAlign = 256;
+constexpr size_t kHeaderBytes = 256;
+constexpr int32_t kMaxSplits = 4096;
+constexpr int64_t kMinSplitTokens = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int ilog2(int64_t x) {
+  int r = 0;
+  while ((int64_t{1} << r) < x) ++r;
+  return r;
+}
+
+int esize(int32_t dtype) { return dtype == FD_BF16 ? 2 : 4; }
+
+// Workspace regions for given sizes.
+struct WsLayout {
+  size_t lse_off, o_off, total;
+};
+
+WsLayout ws_layout(int64_t B, int64_t Hq, int64_t d, int64_t S) {
+  WsLayout w;
+  w.lse_off = kHeaderBytes;
+  w.o_off = align_up(w.lse_off + (size_t)(B * Hq * S) * sizeof(float), kAlign);
+  w.total = align_up(w.o_off + (size_t)(B * Hq * S * d) * sizeof(float), kAlign);
+  return w;
+}
+
+// ---- cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda) ----
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+  });
+  return fn;
+}
+
+// A KV cache viewed as 5-D for TMA: {elements of one 128-byte line, lines per row,
+// tokens (L_cap or page_size), kv heads, batch rows (or pages)}, 128-byte swizzle.
+struct MapKey {
+  const void* ptr;
+  int32_t dtype;
+  uint64_t dims[5];
+  uint64_t strides[4];
+  uint32_t box_rows;
+  bool operator==(const MapKey& o) const { return memcmp(this, &o, sizeof *this) == 0; }
+};
+
+struct MapCache {
+  std::mutex mu;
+  std::vector<std::pair<MapKey, CUtensorMap>> entries;   // most recent last
+};
+
+MapCache& map_cache() {
+  static MapCache c;
+  return c;
+}
+
+fd_status make_kv_map(const fd_tensor* t, uint32_t box_rows, CUtensorMap* out) {
+  const int es = esize(t->dtype);
+  const int d = (int)t->shape[3];
+  MapKey key;
+  memset(&key, 0, sizeof key);
+  key.ptr = t->data;
+  key.dtype = t->dtype;
+  key.dims[0] = (uint64_t)(128 / es);
+  key.dims[1] = (uint64_t)(d * es / 128);
+  key.dims[2] = (uint64_t)t->shape[2];
+  key.dims[3] = (uint64_t)t->shape[1];
+  key.dims[4] = (uint64_t)t->shape[0];
+  key.strides[0] = 128;
+  key.strides[1] = (uint64_t)t->stride[2] * es;
+  key.strides[2] = (uint64_t)t->stride[1] * es;
+  key.strides[3] = (uint64_t)t->stride[0] * es;
+  key.box_rows = box_rows;
+  MapCache& c = map_cache();
+  {
+    std::lock_guard<std::mutex> lock(c.mu);
+    for (size_t i = 0; i < c.entries.size(); ++i) {
+      if (c.entries[i].first == key) {
+        *out = c.entries[i].second;
+        return FD_OK;
+      }
+    }
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(FD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint32_t box[5] = {(cuuint32_t)key.dims[0], (cuuint32_t)key.dims[1], box_rows, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUtensorMap m;
+  CUresult r = enc(&m, t->dtype == FD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                   5, t->data, key.dims, key.strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    return fail(FD_ERR_INVALID_ARG, "cuTensorMapEncodeTiled rejected the KV cache view (CUresult %d)",
+                (int)r);
+  }
+  std::lock_guard<std::mutex> lock(c.mu);
+  if (c.entries.size() >= 32) c.entries.erase(c.entries.begin());
+  c.entries.emplace_back(key, m);
+  *out = m;
+  return FD_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fd_version(void) { return "fd 0.1.0 (sm_103a)"; }
+
+const char* fd_last_error(void) { return g_last_error; }
+
+const char* fd_status_string(fd_status s) {
+  switch (s) {
+    case FD_OK: return "FD_OK";
+    case FD_ERR_INVALID_ARG: return "FD_ERR_INVALID_ARG";
+    case FD_ERR_UNSUPPORTED: return "FD_ERR_UNSUPPORTED";
+    case FD_ERR_WORKSPACE_TOO_SMALL: return "FD_ERR_WORKSPACE_TOO_SMALL";
+    case FD_ERR_CUDA: return "FD_ERR_CUDA";
+    case FD_ERR_DEVICE_FLAG: return "FD_ERR_DEVICE_FLAG";
+  }
+  return "FD_ERR_UNKNOWN";
+}
+
+fd_status fd_set_path(int32_t path) {
+  if (path != FD_PATH_AUTO && path != FD_PATH_SIMT && path != FD_PATH_MMA)
+    return fail(FD_ERR_INVALID_ARG, "unknown kernel path %d", path);
+  g_path.store(path);
+  return FD_OK;
+}
+
+int32_t fd_get_path(void) { return g_path.load(); }
+
+size_t fd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_splits) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || num_splits <= 0 || num_splits > kMaxSplits)
+    return 0;
+  return ws_layout(B, Hq, d, num_splits).total;
+}
+
+int32_t fd_num_splits_heuristic(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int64_t L_cap,
+                                int32_t num_sms) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || L_cap <= 0 || num_sms <= 0) return 1;
+  // Work units are (b, kv head) pairs; each split multiplies them.  Aim for two CTAs on
+  // every SM, but never cut a split below kMinSplitTokens tokens: below that the
+  // partial results and the merge cost more than the extra parallelism returns.
+  const int64_t units = (int64_t)B * Hkv;
+  const int64_t target = 2 * (int64_t)num_sms;
+  int64_t S = (target + units - 1) / units;
+  const int64_t max_by_len = (L_cap + kMinSplitTokens - 1) / kMinSplitTokens;
+  if (S > max_by_len) S = max_by_len;
+  if (S > kMaxSplits) S = kMaxSplits;
+  if (S < 1) S = 1;
+  (void)Hq;
+  (void)d;
+  return (int32_t)S;
+}
+
+int32_t fd_resolve_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int64_t L_cap,
+                              int32_t num_splits) {
+  if (num_splits > 0) return num_splits;
+  return fd_num_splits_heuristic(B, Hq, Hkv, d, L_cap, current_sm_count());
+}
+
+fd_status fd_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace) return fail(FD_ERR_INVALID_ARG, "workspace is NULL");
+  cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(FD_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+  return FD_OK;
+}
+
+fd_status fd_read_device_error(void* workspace, void* stream, uint32_t* flags) {
+  if (!workspace) return fail(FD_ERR_INVALID_ARG, "workspace is NULL");
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t f = 0;
+  cudaError_t e = cudaMemcpyAsync(&f, workspace, sizeof f, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && f != 0) e = cudaMemsetAsync(workspace, 0, sizeof f, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(FD_ERR_CUDA, "reading device flags: %s", cudaGetErrorString(e));
+  if (flags) *flags = f;
+  if (f) return fail(FD_ERR_DEVICE_FLAG, "device error flags 0x%x", f);
+  return FD_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Everything a call resolved on the host: kernel parameters, tensor maps and path.
+struct Prepared {
+  fd::Params p;
+  CUtensorMap tk, tv;
+  int path;
+  int32_t dtype;
+};
+
+// Validate a decode call and resolve it.  `out` may be NULL (partial pass only).
+fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor* v_cache,
+                  const int32_t* seq_lens, const fd_tensor* block_table, int32_t page_size,
+                  int32_t num_splits, const fd_tensor* out, float* lse_out, void* workspace,
+                  size_t workspace_bytes, bool need_out, Prepared* pr) {
+  // ---- presence and ranks
+  if (!q || !k_cache || !v_cache || (need_out && !out))
+    return fail(FD_ERR_INVALID_ARG, "q, k_cache, v_cache and out are required");
+  if (!q->data || !k_cache->data || !v_cache->data || (out && !out->data))
+    return fail(FD_ERR_INVALID_ARG, "a tensor has a NULL data pointer");
+  if (!seq_lens) return fail(FD_ERR_INVALID_ARG, "seq_lens is NULL");
+  if (!workspace) return fail(FD_ERR_INVALID_ARG, "workspace is NULL");
+  if (q->ndim != 3 || k_cache->ndim != 4 || v_cache->ndim != 4 || (out && out->ndim != 3))
+    return fail(FD_ERR_INVALID_ARG, "ranks must be q 3, k/v 4, out 3 (got %d, %d, %d, %d)", q->ndim,
+                k_cache->ndim, v_cache->ndim, out ? out->ndim : 3);
+  if (num_splits < 0 || num_splits > kMaxSplits)
+    return fail(FD_ERR_INVALID_ARG, "num_splits must be in [0, %d], got %d", kMaxSplits, num_splits);
+
+  const int64_t B = q->shape[0], Hq = q->shape[1], d = q->shape[2];
+  const int64_t Hkv = k_cache->shape[1];
+  if (B <= 0 || Hq <= 0 || d <= 0 || Hkv <= 0) return fail(FD_ERR_INVALID_ARG, "empty shape");
+  for (int i = 0; i < 4; ++i) {
+    if (k_cache->shape[i] != v_cache->shape[i])
+      return fail(FD_ERR_INVALID_ARG, "k_cache and v_cache shapes differ in dim %d", i);
+  }
+  if (k_cache->shape[3] != d) return fail(FD_ERR_INVALID_ARG, "k/v head dim %lld != q head dim %lld",
+                                          (long long)k_cache->shape[3], (long long)d);
+  if (out && (out->shape[0] != B || out->shape[1] != Hq || out->shape[2] != d))
+    return fail(FD_ERR_INVALID_ARG, "out must be [B, Hq, d]");
+  if (Hq % Hkv != 0) return fail(FD_ERR_INVALID_ARG, "Hq (%lld) is not a multiple of Hkv (%lld)",
+                                 (long long)Hq, (long long)Hkv);
+  // ---- dtypes
+  if (k_cache->dtype != q->dtype || v_cache->dtype != q->dtype)
+    return fail(FD_ERR_INVALID_ARG, "q, k_cache and v_cache must share one dtype");
+  if (q->dtype != FD_BF16 && q->dtype != FD_F32)
+    return fail(FD_ERR_UNSUPPORTED, "q/k/v dtype must be bf16 or f32");
+  if (out && out->dtype != FD_F32 && !(out->dtype == FD_BF16 && q->dtype == FD_BF16))
+    return fail(FD_ERR_UNSUPPORTED, "out must be f32, or bf16 with bf16 inputs");
+  const int64_t G = Hq / Hkv;
+  if (d != 64 && d != 128) return fail(FD_ERR_UNSUPPORTED, "head dim %lld not in {64, 128}", (long long)d);
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+    return fail(FD_ERR_UNSUPPORTED, "group size %lld not in {1, 2, 4, 8, 16}", (long long)G);
+  const int es = esize(q->dtype);
+  // ---- strides and alignment (TMA: 16-byte base and strides; rows contiguous)
+  if (q->stride[2] != 1 || k_cache->stride[3] != 1 || v_cache->stride[3] != 1 ||
+      (out && out->stride[2] != 1))
+    return fail(FD_ERR_INVALID_ARG, "the last dimension of q, k, v and out must be contiguous");
+  if (!aligned16(q->data) || !aligned16(k_cache->data) || !aligned16(v_cache->data))
+    return fail(FD_ERR_INVALID_ARG, "q, k_cache and v_cache must be 16-byte aligned");
+  if ((q->stride[0] * es) % 16 || (q->stride[1] * es) % 16)
+    return fail(FD_ERR_INVALID_ARG, "q strides must be multiples of 16 bytes");
+  for (int i = 0; i < 3; ++i) {
+    if ((k_cache->stride[i] * es) % 16 || (v_cache->stride[i] * es) % 16 || k_cache->stride[i] <= 0 ||
+        v_cache->stride[i] <= 0)
+      return fail(FD_ERR_INVALID_ARG, "k/v strides must be positive multiples of 16 bytes");
+  }
+  if (k_cache->stride[2] < d || v_cache->stride[2] < d)
+    return fail(FD_ERR_INVALID_ARG, "k/v token rows overlap");
+  // ---- contiguous or paged
+  const bool paged = block_table != nullptr;
+  int64_t L_cap = 0;
+  int32_t max_pages = 0;
+  int64_t bt_sb = 0;
+  if (!paged) {
+    if (page_size != 0) return fail(FD_ERR_INVALID_ARG, "page_size must be 0 without a block table");
+    if (k_cache->shape[0] != B) return fail(FD_ERR_INVALID_ARG, "contiguous k_cache must be [B, Hkv, L_cap, d]");
+    L_cap = k_cache->shape[2];
+  } else {
+    if (!block_table->data) return fail(FD_ERR_INVALID_ARG, "block_table has a NULL data pointer");
+    if (block_table->ndim != 2 || block_table->dtype != FD_I32)
+      return fail(FD_ERR_INVALID_ARG, "block_table must be int32 [B, max_pages]");
+    if (block_table->shape[0] != B || block_table->shape[1] <= 0 || block_table->stride[1] != 1)
+      return fail(FD_ERR_INVALID_ARG, "block_table must be [B, max_pages] with contiguous rows");
+    if (!is_pow2(page_size) || page_size < 8 || page_size > 65536)
+      return fail(FD_ERR_INVALID_ARG, "page_size must be a power of two in [8, 65536], got %d", page_size);
+    if (k_cache->shape[2] != page_size)
+      return fail(FD_ERR_INVALID_ARG, "paged k_cache must be [num_pages, Hkv, page_size, d]");
+    max_pages = (int32_t)block_table->shape[1];
+    bt_sb = block_table->stride[0];
+    L_cap = (int64_t)max_pages * page_size;
+  }
+  if (L_cap <= 0 || L_cap >= (int64_t{1} << 31))
+    return fail(FD_ERR_INVALID_ARG, "cache capacity must be in [1, 2^31), got %lld", (long long)L_cap);
+  if (lse_out && ((uintptr_t)lse_out & 3))
+    return fail(FD_ERR_INVALID_ARG, "lse_out must be 4-byte aligned");
+  // ---- splits and workspace
+  int32_t S = num_splits > 0 ? num_splits
+                             : fd_num_splits_heuristic((int32_t)B, (int32_t)Hq, (int32_t)Hkv,
+                                                       (int32_t)d, L_cap, current_sm_count());
+  const WsLayout wl = ws_layout(B, Hq, d, S);
+  if (((uintptr_t)workspace & (kAlign - 1)) != 0)
+    return fail(FD_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (workspace_bytes < wl.total)
+    return fail(FD_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes, got %zu", wl.total, workspace_bytes);
+  if ((int64_t)S * Hkv > 65535 * 65535LL || Hkv > 65535 || B > 65535)
+    return fail(FD_ERR_UNSUPPORTED, "grid too large");
+
+  // ---- path
+  int path = g_path.load();
+  if (path == FD_PATH_AUTO) path = q->dtype == FD_BF16 ? FD_PATH_MMA : FD_PATH_SIMT;
+  if (path == FD_PATH_MMA && q->dtype != FD_BF16)
+    return fail(FD_ERR_UNSUPPORTED, "the tensor-core path needs bf16 inputs");
+
+  // ---- tensor maps (box height: one tile, or one page when pages are shorter)
+  const int TT = fd::tile_tokens((int)d, es);
+  const uint32_t box_rows = (uint32_t)(paged && page_size < TT ? page_size : TT);
+  fd_status st = make_kv_map(k_cache, box_rows, &pr->tk);
+  if (st != FD_OK) return st;
+  st = make_kv_map(v_cache, box_rows, &pr->tv);
+  if (st != FD_OK) return st;
+
+  fd::Params& p = pr->p;
+  memset(&p, 0, sizeof p);
+  p.B = (int32_t)B;
+  p.Hq = (int32_t)Hq;
+  p.Hkv = (int32_t)Hkv;
+  p.d = (int32_t)d;
+  p.G = (int32_t)G;
+  p.L_cap = L_cap;
+  p.S = S;
+  p.split_len = (L_cap + S - 1) / S;
+  p.q = q->data;
+  p.q_sb = q->stride[0];
+  p.q_sh = q->stride[1];
+  p.seq_lens = seq_lens;
+  p.block_table = paged ? static_cast<const int32_t*>(block_table->data) : nullptr;
+  p.bt_sb = bt_sb;
+  p.page_size = paged ? page_size : 0;
+  p.log2_page = paged ? ilog2(page_size) : 0;
+  p.max_pages = max_pages;
+  p.num_pages = paged ? k_cache->shape[0] : 0;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.flags = reinterpret_cast<uint32_t*>(ws);
+  p.lse_part = reinterpret_cast<float*>(ws + wl.lse_off);
+  p.o_part = reinterpret_cast<float*>(ws + wl.o_off);
+  p.out = out ? out->data : nullptr;
+  p.out_sb = out ? out->stride[0] : 0;
+  p.out_sh = out ? out->stride[1] : 0;
+  p.out_bf16 = out && out->dtype == FD_BF16 ? 1 : 0;
+  p.lse_out = lse_out;
+  p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
+
+  pr->path = path;
+  pr->dtype = q->dtype;
+  return FD_OK;
+}
+
+fd_status launch_partial(const Prepared& pr, cudaStream_t s) {
+  cudaError_t e = pr.path == FD_PATH_MMA ? fd::launch_partial_mma(pr.p, pr.tk, pr.tv, s)
+                                         : fd::launch_partial_simt(pr.p, pr.tk, pr.tv, pr.dtype, s);
+  if (e != cudaSuccess) return fail(FD_ERR_CUDA, "partial-pass launch: %s", cudaGetErrorString(e));
+  return FD_OK;
+}
+
+fd_status launch_merge(const fd::Params& p, cudaStream_t s) {
+  cudaError_t e = fd::launch_combine(p, s, /*pdl=*/true);
+  if (e != cudaSuccess) return fail(FD_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
+  return FD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
+                              const fd_tensor* v_cache, const int32_t* seq_lens,
+                              const fd_tensor* block_table, int32_t page_size,
+                              int32_t num_splits, fd_tensor* out, float* lse_out,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  Prepared pr;
+  fd_status st = prepare(q, k_cache, v_cache, seq_lens, block_table, page_size, num_splits, out,
+                         lse_out, workspace, workspace_bytes, true, &pr);
+  if (st != FD_OK) return st;
+  st = launch_partial(pr, (cudaStream_t)stream);
+  if (st != FD_OK) return st;
+  return launch_merge(pr.p, (cudaStream_t)stream);
+}
+
+fd_status fd_decode_partial(const fd_tensor* q, const fd_tensor* k_cache,
+                            const fd_tensor* v_cache, const int32_t* seq_lens,
+                            const fd_tensor* block_table, int32_t page_size, int32_t num_splits,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  Prepared pr;
+  fd_status st = prepare(q, k_cache, v_cache, seq_lens, block_table, page_size, num_splits,
+                         nullptr, nullptr, workspace, workspace_bytes, false, &pr);
+  if (st != FD_OK) return st;
+  return launch_partial(pr, (cudaStream_t)stream);
+}
+
+fd_status fd_workspace_partials(void* workspace, int32_t B, int32_t Hq, int32_t d,
+                                int32_t num_splits, float** lse_part, float** o_part) {
+  if (!workspace || B <= 0 || Hq <= 0 || d <= 0 || num_splits <= 0 || num_splits > kMaxSplits)
+    return fail(FD_ERR_INVALID_ARG, "invalid workspace or sizes");
+  const WsLayout wl = ws_layout(B, Hq, d, num_splits);
+  if (lse_part) *lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + wl.lse_off);
+  if (o_part) *o_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + wl.o_off);
+  return FD_OK;
+}
+
+fd_status fd_merge_partials(int32_t B, int32_t Hq, int32_t d, int32_t num_splits,
+                            const float* lse_part, const float* o_part, fd_tensor* out,
+                            float* lse_out, void* stream) {
+  if (!lse_part || !o_part || !out || !out->data)
+    return fail(FD_ERR_INVALID_ARG, "lse_part, o_part and out are required");
+  if (B <= 0 || Hq <= 0 || num_splits <= 0 || num_splits > kMaxSplits)
+    return fail(FD_ERR_INVALID_ARG, "invalid sizes");
+  if (d != 64 && d != 128) return fail(FD_ERR_UNSUPPORTED, "head dim %d not in {64, 128}", d);
+  if (out->ndim != 3 || out->shape[0] != B || out->shape[1] != Hq || out->shape[2] != d ||
+      out->stride[2] != 1)
+    return fail(FD_ERR_INVALID_ARG, "out must be [B, Hq, d] with a contiguous last dim");
+  if (out->dtype != FD_F32 && out->dtype != FD_BF16)
+    return fail(FD_ERR_UNSUPPORTED, "out must be f32 or bf16");
+  if (((uintptr_t)o_part & 15) || ((uintptr_t)lse_part & 3))
+    return fail(FD_ERR_INVALID_ARG, "o_part must be 16-byte and lse_part 4-byte aligned");
+  if (lse_out && ((uintptr_t)lse_out & 3)) return fail(FD_ERR_INVALID_ARG, "lse_out misaligned");
+  fd::Params p;
+  memset(&p, 0, sizeof p);
+  p.B = B;
+  p.Hq = Hq;
+  p.d = d;
+  p.S = num_splits;
+  p.lse_part = const_cast<float*>(lse_part);
+  p.o_part = const_cast<float*>(o_part);
+  p.out = out->data;
+  p.out_sb = out->stride[0];
+  p.out_sh = out->stride[1];
+  p.out_bf16 = out->dtype == FD_BF16 ? 1 : 0;
+  p.lse_out = lse_out;
+  return launch_merge(p, (cudaStream_t)stream);
+}
+
+
+// ------------------------------------------------------------------------ plans
+struct fd_plan {
+  int32_t B, Hq, Hkv, d;
+  int64_t L_cap;
+  int32_t S;
+  int device;
+  void* ws;
+  size_t ws_bytes;
+  cudaEvent_t done;   // recorded after each decode's merge pass
+};
+
+static fd_status plan_alloc(fd_plan* p, int32_t S) {
+  const size_t bytes = fd_workspace_size(p->B, p->Hq, p->Hkv, p->d, S);
+  if (bytes == 0) return fail(FD_ERR_INVALID_ARG, "invalid plan sizes");
+  void* ws = nullptr;
+  cudaError_t e = cudaMalloc(&ws, bytes);
+  if (e != cudaSuccess) return fail(FD_ERR_CUDA, "cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
+  e = cudaMemset(ws, 0, bytes);
+  if (e != cudaSuccess) {
+    cudaFree(ws);
+    return fail(FD_ERR_CUDA, "cudaMemset: %s", cudaGetErrorString(e));
+  }
+  cudaEvent_t ev;
+  e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    cudaFree(ws);
+    return fail(FD_ERR_CUDA, "cudaEventCreate: %s", cudaGetErrorString(e));
+  }
+  p->ws = ws;
+  p->ws_bytes = bytes;
+  p->done = ev;
+  p->S = S;
+  return FD_OK;
+}
+
+fd_status fd_plan_create(fd_plan** plan, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+                         int64_t L_cap, int32_t num_splits) {
+  if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
+  *plan = nullptr;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || L_cap <= 0 || num_splits < 0 ||
+      num_splits > kMaxSplits || Hq % Hkv != 0)
+    return fail(FD_ERR_INVALID_ARG, "invalid plan sizes");
+  fd_plan* p = new fd_plan();
+  p->B = B;
+  p->Hq = Hq;
+  p->Hkv = Hkv;
+  p->d = d;
+  p->L_cap = L_cap;
+  cudaGetDevice(&p->device);
+  const int32_t S = num_splits > 0 ? num_splits
+                                   : fd_num_splits_heuristic(B, Hq, Hkv, d, L_cap, current_sm_count());
+  fd_status st = plan_alloc(p, S);
+  if (st != FD_OK) {
+    delete p;
+    return st;
+  }
+  *plan = p;
+  return FD_OK;
+}
+
+int32_t fd_plan_num_splits(const fd_plan* plan) { return plan ? plan->S : 0; }
+size_t fd_plan_workspace_bytes(const fd_plan* plan) { return plan ? plan->ws_bytes : 0; }
+void* fd_plan_workspace(const fd_plan* plan) { return plan ? plan->ws : nullptr; }
+
+fd_status fd_plan_decode(fd_plan* plan, const fd_tensor* q, const fd_tensor* k_cache,
+                         const fd_tensor* v_cache, const int32_t* seq_lens,
+                         const fd_tensor* block_table, int32_t page_size, fd_tensor* out,
+                         float* lse_out, void* stream) {
+  if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
+  if (!q || q->ndim != 3 || q->shape[0] != plan->B || q->shape[1] != plan->Hq || q->shape[2] != plan->d ||
+      !k_cache || k_cache->ndim != 4 || k_cache->shape[1] != plan->Hkv)
+    return fail(FD_ERR_INVALID_ARG, "tensor sizes differ from the plan's");
+  fd_status st = fd_decode_attention(q, k_cache, v_cache, seq_lens, block_table, page_size, plan->S,
+                                     out, lse_out, plan->ws, plan->ws_bytes, stream);
+  if (st != FD_OK) return st;
+  cudaError_t e = cudaEventRecord(plan->done, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(FD_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
+  return FD_OK;
+}
+
+fd_status fd_plan_resize(fd_plan* plan, int32_t num_splits) {
+  if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
+  if (num_splits < 0 || num_splits > kMaxSplits) return fail(FD_ERR_INVALID_ARG, "bad num_splits");
+  const int32_t S = num_splits > 0 ? num_splits
+                                   : fd_num_splits_heuristic(plan->B, plan->Hq, plan->Hkv, plan->d,
+                                                             plan->L_cap, current_sm_count());
+  if (S == plan->S) return FD_OK;
+  // The old workspace may still be read by an in-flight merge: wait for it first.
+  cudaError_t e = cudaEventSynchronize(plan->done);
+  if (e != cudaSuccess) return fail(FD_ERR_CUDA, "cudaEventSynchronize: %s", cudaGetErrorString(e));
+  void* old_ws = plan->ws;
+  cudaEvent_t old_ev = plan->done;
+  fd_status st = plan_alloc(plan, S);
+  if (st != FD_OK) return st;   // plan unchanged (old buffers kept)
+  cudaFree(old_ws);
+  cudaEventDestroy(old_ev);
+  return FD_OK;
+}
+
+void fd_plan_destroy(fd_plan* plan) {
+  if (!plan) return;
+  if (plan->done) {
+    cudaEventSynchronize(plan->done);
+    cudaEventDestroy(plan->done);
+  }
+  if (plan->ws) cudaFree(plan->ws);
+  delete plan;
+}
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// fd_internal.h -- parameters shared by the host planner (fd_api.cu) and the kernels.
+//
+// Not part of the public ABI (that is include/fd.h).
+#pragma once
+
+#include <cuda.h>            // CUtensorMap (type only; the driver entry point is looked up)
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fd.h"
+
+namespace fd {
+
+// Device error flag set when a bounded wait gives up (a kernel then writes empty
+// partials for its split and returns; the host sees it via fd_read_device_error).
+constexpr uint32_t kDevFlagTimeout = FD_DEVFLAG_TIMEOUT;
+
+// Bytes of one K (or V) tile in shared memory; the tile height in tokens is
+// kTileBytes / (d * element size): 64 tokens for bf16 d=128.
+constexpr int kTileBytes = 16384;
+
+// Everything one decode call needs on the device, resolved by the host planner.
+struct Params {
+  // sizes
+  int32_t B, Hq, Hkv, d, G;
+  int64_t L_cap;          // tokens of capacity per row
+  int32_t S;              // number of splits
+  int64_t split_len;      // ceil(L_cap / S)
+  // query [B, Hq, d]
+  const void* q;
+  int64_t q_sb, q_sh;     // strides (elements) of batch and head
+  // lengths and paging
+  const int32_t* seq_lens;
+  const int32_t* block_table;   // nullptr -> contiguous
+  int64_t bt_sb;                // batch stride of the block table (elements)
+  int32_t page_size;            // tokens per page (paged), else 0
+  int32_t log2_page;            // log2(page_size)
+  int32_t max_pages;            // block table width
+  int64_t num_pages;            // pages in the pool
+  // workspace
+  uint32_t* flags;        // device error flags (workspace header)
+  float* lse_part;        // [B, Hq, S]     natural-log LSE_i, -inf for an empty split
+  float* o_part;          // [B, Hq, S, d]  normalised partial output O_i
+  // outputs
+  void* out;
+  int64_t out_sb, out_sh;
+  int32_t out_bf16;       // 1: bf16 out, 0: f32 out
+  float* lse_out;         // [B, Hq] or nullptr
+  float scale_log2;       // log2(e) / sqrt(d): scores are kept in base-2 units inside kernels
+};
+
+// Launchers (each returns the launch's cudaError_t).
+cudaError_t launch_partial_simt(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                                int dtype, cudaStream_t stream);
+cudaError_t launch_partial_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                               cudaStream_t stream);
+cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool pdl);
+
+// Tile height (tokens) used by the kernels for a dtype and head dim.
+inline int tile_tokens(int d, int esz) { return kTileBytes / (d * esz); }
+
+}  // namespace fd

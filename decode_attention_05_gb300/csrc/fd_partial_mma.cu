@@ -1,0 +1,362 @@
+// fd_partial_mma.cu -- split-KV partial pass with the GQA group's dot products on the
+// tensor cores (bf16 inputs, f32 accumulation), for G = Hq / Hkv in {1, 2, 4, 8, 16}.
+//
+// Why tensor cores here: with G query heads sharing one KV head, every KV element
+// feeds G multiply-adds for the scores and G for the output, i.e. G FLOP per KV byte.
+// At G = 8 and ~7 TB/s that is ~55 TFLOP/s of FMA work, about 75% of the CUDA-core
+// FP32 rate of a GB300, so the CUDA-core kernel (fd_partial_simt.cuh) is co-limited
+// by arithmetic.  The same work is under 20% of the legacy tensor-core (mma.sync)
+// rate, which leaves the pass bound by HBM, as it should be.
+//
+// Memory side: the TMA producer warp and stage ring of fd_pipeline.cuh (128-byte
+// swizzled K/V tiles).  Compute side, per consumer warp and per 16-token chunk:
+//   S^T[16 tok, 8 heads] = K_chunk[16, d] . Q^T[d, 8]          (tokens in M, heads in N:
+//                                                                G = 8 fills N exactly)
+//   scores -> base-2 logits, mask (-inf), online-softmax max / rescale
+//   P^T = movmatrix.trans(bf16(2^(S - m)))                      (register transpose)
+//   O^T[d, 8] += V_chunk^T[d, 16 tok] . P^T[16 tok, 8 heads]    (V^T via ldmatrix.trans)
+// which is the FlashAttention update of "AI Infra: math and infra optimisation in large
+// models", section 2.6 (S = Q K^T per KV block; rescale the running sum and output by
+// exp(m_old - m_new); add exp(S - m_new) V), run inside one KV split of
+// Flash-Decoding (same section, "Flash-Decoding Split-K").
+#include <cuda_bf16.h>
+
+#include "fd_epilogue.cuh"
+
+namespace fd {
+
+namespace {
+
+template <int D_, int G_>
+struct MmaShape {
+  static constexpr int D = D_;
+  static constexpr int G = G_;
+  static constexpr int NT = G > 8 ? 2 : 1;                 // n-tiles of 8 heads
+  static constexpr int ROW_BYTES = D * 2;
+  static constexpr int TT = kTileBytes / ROW_BYTES;        // 64 (d=128) or 128 (d=64)
+  static constexpr int LINES = ROW_BYTES / 128;
+  static constexpr int NCW = 4;                            // consumer warps
+  static constexpr int ROWS_PER_WARP = TT / NCW;           // 16 or 32
+  static constexpr int CHUNKS = ROWS_PER_WARP / 16;        // 16-token chunks per warp per tile
+  static constexpr int KSTEPS = D / 16;                    // k-steps of the QK^T product
+  static constexpr int MTILES = D / 16;                    // m-tiles of the PV product
+  static constexpr int STAGES = 3;
+  static constexpr int THREADS = (NCW + 1) * 32;
+  static constexpr int MERGE_BYTES = NCW * G * D * 4 + 2 * NCW * G * 4;
+  static_assert(MERGE_BYTES <= STAGES * 2 * kTileBytes, "merge scratch fits the stages");
+  static constexpr size_t SMEM_BYTES =
+      1024 + (size_t)STAGES * 2 * kTileBytes + sizeof(PipeCtl<STAGES>);
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// D = A . B + D, m16n8k16, bf16 inputs, f32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Pack two f32 into a bf16x2 (round to nearest even); `lo` goes to the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <class SH>
+__global__ void __launch_bounds__(SH::THREADS, 2)
+    fd_partial_mma_kernel(const __grid_constant__ CUtensorMap tk,
+                          const __grid_constant__ CUtensorMap tv,
+                          const __grid_constant__ Params p) {
+  constexpr int G = SH::G, NT = SH::NT, TT = SH::TT, STAGES = SH::STAGES;
+  const SplitInfo si = split_info<TT>(p);
+  if (si.n_tiles == 0) {            // empty split: weight 0 in the merge, nothing to load
+    write_empty_split(p, si, threadIdx.x);
+    pdl_trigger();
+    return;
+  }
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  auto* ctl = reinterpret_cast<PipeCtl<STAGES>*>(stages + (size_t)STAGES * 2 * kTileBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_addr(&ctl->full[s]), 1);
+      mbar_init(smem_addr(&ctl->empty[s]), SH::NCW);
+    }
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == SH::NCW) {            // ---------------- producer warp
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+    produce_tiles<TT, STAGES>(p, si, &tk, &tv, stages, ctl, lane);
+    pdl_trigger();
+    return;
+  }
+
+  // ---------------------------------------------------- consumer warps
+  const int qr = lane >> 2;         // "group" row of the mma fragments (0..7)
+  const int qc = (lane & 3) * 2;    // first of the two fragment columns
+
+  // B fragments of Q^T (k = dim, n = head), bf16 as stored: b0 holds dims
+  // 16 kk + qc, +1 of head nt * 8 + qr; b1 the same 8 dims further.  Heads >= G are 0.
+  uint32_t qb[NT][SH::KSTEPS][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = nt * 8 + qr;
+    const int hc = h < G ? h : 0;                     // never address past the group
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        reinterpret_cast<const __nv_bfloat16*>(p.q) + si.b * p.q_sb + (si.g * G + hc) * p.q_sh);
+#pragma unroll
+    for (int kk = 0; kk < SH::KSTEPS; ++kk) {
+      const uint32_t lo = qrow[(kk * 16 + qc) / 2], hi = qrow[(kk * 16 + qc + 8) / 2];
+      qb[nt][kk][0] = h < G ? lo : 0u;
+      qb[nt][kk][1] = h < G ? hi : 0u;
+    }
+  }
+
+  // Per-thread softmax state for heads nt * 8 + qc + {0, 1}; acc = O^T fragments:
+  // acc[nt][mt] = {(dim 16 mt + qr, head qc), (.., qc + 1), (dim + 8, qc), (.., qc + 1)}.
+  float m[NT][2], l[NT][2];
+  float acc[NT][SH::MTILES][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m[nt][0] = m[nt][1] = kNegInf;
+    l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < SH::MTILES; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[nt][mt][e] = 0.f;
+  }
+
+  const int ps = p.page_size;
+  const bool multi_page = ps > 0 && ps < TT;
+  const float sl2 = p.scale_log2;
+  bool aborted = false;
+
+  // ldmatrix row addresses: lane i serves matrix i / 8, row i % 8.
+  const int lm = lane >> 3, lr = lane & 7;
+
+  for (int n = 0; n < si.n_tiles; ++n) {
+    const int stage = n % STAGES;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(smem_addr(&ctl->full[stage]), (n / STAGES) & 1);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) {
+        ctl->abort = 1;
+        atomicOr(p.flags, kDevFlagTimeout);
+      }
+      aborted = true;
+      break;
+    }
+    uint8_t* kt = stages + (size_t)stage * 2 * kTileBytes;
+    uint8_t* vt = kt + kTileBytes;
+    const uint32_t bad = ctl->bad[stage];
+    const int64_t t0 = si.T0 + (int64_t)n * TT;
+    const int r0 = warp * SH::ROWS_PER_WARP;          // this warp's first row in the tile
+
+    // Rows outside [lo, hi) or on an invalid page: their V rows may be stale (NaN) and
+    // 0 * NaN is NaN inside the MMA, so zero them before use.  Only boundary tiles.
+    const bool clean = t0 + r0 >= si.lo && t0 + r0 + SH::ROWS_PER_WARP <= si.hi && bad == 0;
+    if (!clean) {
+      for (int r = 0; r < SH::ROWS_PER_WARP; ++r) {
+        const int row = r0 + r;
+        const int64_t tok = t0 + row;
+        const int pslot = multi_page ? (row >> p.log2_page) : 0;
+        const bool valid = tok >= si.lo && tok < si.hi && !((bad >> pslot) & 1u);
+        if (!valid) {
+          for (int c = lane; c < SH::ROW_BYTES / 16; c += 32)
+            *reinterpret_cast<uint4*>(vt + row * SH::ROW_BYTES + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      // These generic-proxy stores must be ordered before the next TMA write of the stage.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+    }
+
+#pragma unroll
+    for (int ch = 0; ch < SH::CHUNKS; ++ch) {
+      const int rb = r0 + ch * 16;                    // first row of this 16-token chunk
+      // ---- S^T = K . Q^T  (A = K rows rb..rb+15 via ldmatrix, swizzled tile)
+      float s[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      const int arow = rb + lr + (lm & 1) * 8;
+#pragma unroll
+      for (int kk = 0; kk < SH::KSTEPS; ++kk) {
+        const int c16 = kk * 2 + (lm >> 1);           // 16-byte chunk of the row
+        const uint32_t X = (uint32_t)arow * SH::LINES + (c16 >> 3);
+        uint32_t a[4];
+        ldsm_x4(smem_addr(kt) + swz128(X, c16 & 7), a);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16(s[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+      }
+      // ---- mask and scale: element e of s[nt] is (token rb + qr + 8 (e >> 1),
+      //      head nt * 8 + qc + (e & 1)); excluded tokens get -inf.
+      bool vrow[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int row = rb + qr + 8 * hh;
+        const int64_t tok = t0 + row;
+        const int pslot = multi_page ? (row >> p.log2_page) : 0;
+        vrow[hh] = tok >= si.lo && tok < si.hi && !((bad >> pslot) & 1u);
+      }
+      uint32_t pb[NT][2];                             // P^T fragments (b0/b1 of the PV mma)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = vrow[e >> 1] ? s[nt][e] * sl2 : kNegInf;
+        // chunk max per head over the 16 tokens: in-thread pair, then lanes of equal qc
+        float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+        if (mn0 > m[nt][0] || mn1 > m[nt][1]) {       // rescale the running state
+          const float c0 = (mn0 == kNegInf) ? 1.f : ex2(m[nt][0] - mn0);
+          const float c1 = (mn1 == kNegInf) ? 1.f : ex2(m[nt][1] - mn1);
+          l[nt][0] *= c0;
+          l[nt][1] *= c1;
+#pragma unroll
+          for (int mt = 0; mt < SH::MTILES; ++mt) {
+            acc[nt][mt][0] *= c0;
+            acc[nt][mt][1] *= c1;
+            acc[nt][mt][2] *= c0;
+            acc[nt][mt][3] *= c1;
+          }
+          m[nt][0] = mn0;
+          m[nt][1] = mn1;
+        }
+        float pr[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float mh = m[nt][e & 1];
+          pr[e] = (x[e] == kNegInf) ? 0.f : ex2(x[e] - mh);
+        }
+        l[nt][0] += pr[0] + pr[2];
+        l[nt][1] += pr[1] + pr[3];
+        // P rows (tokens qr, qr + 8) x heads (qc, qc + 1) -> transpose to P^T fragments.
+        pb[nt][0] = movmatrix_trans(pack_bf16x2(pr[0], pr[1]));
+        pb[nt][1] = movmatrix_trans(pack_bf16x2(pr[2], pr[3]));
+      }
+      // ---- O^T += V^T . P^T  (A = V^T via ldmatrix.trans: matrix j covers tokens
+      //      rb + 8 (j >> 1) .. +7 and dims 16 mt + 8 (j & 1) .. +7)
+      const int vrow_addr = rb + lr + (lm >> 1) * 8;
+#pragma unroll
+      for (int mt = 0; mt < SH::MTILES; ++mt) {
+        const int c16 = mt * 2 + (lm & 1);
+        const uint32_t X = (uint32_t)vrow_addr * SH::LINES + (c16 >> 3);
+        uint32_t a[4];
+        ldsm_x4_trans(smem_addr(vt) + swz128(X, c16 & 7), a);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[nt][mt], a, pb[nt][0], pb[nt][1]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
+  }
+  pdl_trigger();
+
+  named_bar_sync(1, SH::NCW * 32);
+  if (aborted || *reinterpret_cast<volatile int32_t*>(&ctl->abort)) {
+    if (warp == 0) write_empty_split(p, si, threadIdx.x);
+    return;
+  }
+
+  // l: sum over the 8 lanes that share qc (they saw different tokens).
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
+      l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
+    }
+  float* macc = reinterpret_cast<float*>(stages);                 // [NCW][G][D]
+  float* mm = macc + SH::NCW * G * SH::D;                         // [NCW][G]
+  float* ml = mm + SH::NCW * G;                                   // [NCW][G]
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int h = nt * 8 + qc + e;
+      if (h < G) {
+#pragma unroll
+        for (int mt = 0; mt < SH::MTILES; ++mt) {
+          macc[(warp * G + h) * SH::D + mt * 16 + qr] = acc[nt][mt][e];
+          macc[(warp * G + h) * SH::D + mt * 16 + qr + 8] = acc[nt][mt][2 + e];
+        }
+        if (qr == 0) {
+          mm[warp * G + h] = m[nt][e];
+          ml[warp * G + h] = l[nt][e];
+        }
+      }
+    }
+  }
+  named_bar_sync(1, SH::NCW * 32);
+  merge_warps_and_store<G, SH::D, SH::NCW>(p, si, macc, mm, ml, threadIdx.x);
+}
+
+template <class SH>
+cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                       cudaStream_t stream) {
+  auto kernel = fd_partial_mma_kernel<SH>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SH::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
+  kernel<<<grid, SH::THREADS, SH::SMEM_BYTES, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dispatch_g(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                       cudaStream_t stream) {
+  switch (p.G) {
+    case 1: return launch_mma<MmaShape<D, 1>>(p, tk, tv, stream);
+    case 2: return launch_mma<MmaShape<D, 2>>(p, tk, tv, stream);
+    case 4: return launch_mma<MmaShape<D, 4>>(p, tk, tv, stream);
+    case 8: return launch_mma<MmaShape<D, 8>>(p, tk, tv, stream);
+    case 16: return launch_mma<MmaShape<D, 16>>(p, tk, tv, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_partial_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                               cudaStream_t stream) {
+  if (p.d == 128) return dispatch_g<128>(p, tk, tv, stream);
+  if (p.d == 64) return dispatch_g<64>(p, tk, tv, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fd

@@ -1,0 +1,155 @@
+// fd_pipeline.cuh -- the memory side of the split-KV partial pass: which tokens a CTA
+// owns, and a TMA producer warp that streams K and V tiles of those tokens from HBM
+// into a ring of shared-memory stages guarded by mbarriers.
+//
+// Grid: blockIdx.x = split i, blockIdx.y = kv head g, blockIdx.z = batch row b.  The
+// CTA serves all G = Hq / Hkv query heads of kv head g, so each KV byte of the split is
+// read from HBM exactly once per step ("AI Infra: math and infra optimisation in large
+// models", section 2.6, "Flash-Decoding Split-K": the KV cache is cut along the
+// sequence and the pieces go to different SMs).
+//
+// Split i of row b covers logical tokens [i * split_len, min((i + 1) * split_len, L_b));
+// it is empty when it starts at or past L_b.  Tiles are TT tokens long and aligned to
+// multiples of TT in the logical token space, so a split that starts or ends mid-tile
+// loads that boundary tile and masks the tokens outside its range.
+//
+// Paged caches: logical token t is slot t % ps of page block_table[b][t / ps]; the page
+// ids are read in the table's order ("2kiu.com/news/6053916", section "the split count
+// is a cost account": logical order must not be replaced by physical page numbers).
+#pragma once
+
+#include "fd_device.cuh"
+
+namespace fd {
+
+struct SplitInfo {
+  int b, g, split;
+  int64_t lo, hi;       // valid logical tokens of this split: [lo, hi)
+  int64_t T0;           // start of the first tile (a multiple of TT)
+  int n_tiles;
+  int64_t used_pages;   // pages of row b that hold tokens < L_b (paged)
+};
+
+// Resolve this CTA's split; clamps and flags an out-of-range sequence length.
+template <int TT>
+__device__ __forceinline__ SplitInfo split_info(const Params& p) {
+  SplitInfo si;
+  si.split = blockIdx.x;
+  si.g = blockIdx.y;
+  si.b = blockIdx.z;
+  int64_t L = p.seq_lens[si.b];
+  if (L < 0 || L > p.L_cap) {
+    if (threadIdx.x == 0) atomicOr(p.flags, FD_DEVFLAG_SEQ_LEN);
+    L = L < 0 ? 0 : p.L_cap;
+  }
+  si.lo = (int64_t)si.split * p.split_len;
+  si.hi = min(si.lo + p.split_len, L);
+  si.T0 = (si.lo / TT) * TT;
+  si.n_tiles = si.lo < si.hi ? (int)((si.hi - si.T0 + TT - 1) / TT) : 0;
+  si.used_pages = p.page_size > 0 ? (L + p.page_size - 1) >> p.log2_page : 0;
+  return si;
+}
+
+// Shared-memory control block of the pipeline.
+template <int STAGES>
+struct PipeCtl {
+  uint64_t full[STAGES];    // TMA bytes landed (count 1 + transaction bytes)
+  uint64_t empty[STAGES];   // consumers released the stage (count = consumer warps)
+  uint32_t bad[STAGES];     // bit j: page slot j of the tile had an invalid page id
+  int32_t abort;            // a bounded wait gave up
+};
+
+// Producer warp: streams tiles 0..n_tiles-1 of the split.  All 32 lanes run the loop
+// (they share the page-id cache); lane 0 issues the copies.
+//   stages: base of STAGES * 2 * kTileBytes bytes, 1024-byte aligned; stage s holds the
+//           K tile at s * 2 * kTileBytes and the V tile kTileBytes after it.
+template <int TT, int STAGES>
+__device__ __forceinline__ void produce_tiles(const Params& p, const SplitInfo& si,
+                                              const CUtensorMap* tk, const CUtensorMap* tv,
+                                              uint8_t* stages, PipeCtl<STAGES>* ctl,
+                                              int lane) {
+  const uint64_t pol = policy_evict_first();
+  const bool paged = p.block_table != nullptr;
+  const int ps = p.page_size;
+  const int pages_per_tile = paged ? (ps >= TT ? 1 : TT / ps) : 1;
+  const int box_rows = paged ? (ps >= TT ? TT : ps) : TT;
+  const uint32_t box_bytes = (uint32_t)(kTileBytes / TT) * box_rows;
+  // Page-id cache: lane i holds the table entry of page (cache_base + i), or -2 when
+  // that page holds no token of the row (never read from the table).
+  int64_t cache_base = -64;      // no window loaded yet
+  int32_t cache = -2;
+  int n = 0;
+  for (; n < si.n_tiles; ++n) {
+    const int stage = n % STAGES;
+    if (n >= STAGES) {
+      // Lane 0 waits and tells the warp, so the lanes never disagree about leaving.
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(smem_addr(&ctl->empty[stage]), ((n / STAGES) - 1) & 1);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          ctl->abort = 1;
+          atomicOr(p.flags, kDevFlagTimeout);
+        }
+        break;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int32_t*>(&ctl->abort), 0)) break;
+    const int64_t t0 = si.T0 + (int64_t)n * TT;
+    uint32_t bad = 0;
+    int32_t pid[16];  // pages_per_tile <= TT / 8 <= 16 (page_size >= 8 is enforced)
+    if (paged) {
+      const int64_t pi0 = t0 >> p.log2_page;
+      for (int j = 0; j < pages_per_tile; ++j) {
+        const int64_t pi = pi0 + j;
+        if (pi < cache_base || pi >= cache_base + 32) {          // warp-uniform refill
+          cache_base = pi;
+          const int64_t mine = pi + lane;
+          cache = mine < si.used_pages ? p.block_table[(int64_t)si.b * p.bt_sb + mine] : -2;
+        }
+        int32_t id = __shfl_sync(0xffffffffu, cache, (int)(pi - cache_base));
+        if (id == -2) {
+          id = 0;                          // no token of the row here: any valid page
+        } else if (id < 0 || (int64_t)id >= p.num_pages) {
+          bad |= 1u << j;                  // a used entry out of range: exclude its tokens
+          id = 0;
+        }
+        pid[j] = id;
+      }
+      if (bad && lane == 0) atomicOr(p.flags, FD_DEVFLAG_PAGE);
+    }
+    if (lane == 0) {
+      ctl->bad[stage] = bad;
+      const uint32_t full = smem_addr(&ctl->full[stage]);
+      mbar_arrive_expect_tx(full, 2u * kTileBytes);
+      const uint32_t dk = smem_addr(stages + (size_t)stage * 2 * kTileBytes);
+      const uint32_t dv = dk + kTileBytes;
+      if (!paged) {
+        tma_load_5d(dk, tk, full, 0, 0, (int)t0, si.g, si.b, pol);
+        tma_load_5d(dv, tv, full, 0, 0, (int)t0, si.g, si.b, pol);
+      } else if (ps >= TT) {
+        const int slot = (int)(t0 & (ps - 1));
+        tma_load_5d(dk, tk, full, 0, 0, slot, si.g, pid[0], pol);
+        tma_load_5d(dv, tv, full, 0, 0, slot, si.g, pid[0], pol);
+      } else {
+        for (int j = 0; j < pages_per_tile; ++j) {
+          tma_load_5d(dk + j * box_bytes, tk, full, 0, 0, 0, si.g, pid[j], pol);
+          tma_load_5d(dv + j * box_bytes, tv, full, 0, 0, 0, si.g, pid[j], pol);
+        }
+      }
+    }
+    __syncwarp();
+  }
+  // Never leave with copies in flight: wait (bounded) for the last issued tile of each
+  // stage.  Earlier tiles of a stage completed before the stage was reused.
+  if (lane == 0) {
+    const int first = n > STAGES ? n - STAGES : 0;
+    for (int m = first; m < n; ++m) {
+      if (!mbar_wait(smem_addr(&ctl->full[m % STAGES]), (m / STAGES) & 1)) {
+        atomicOr(p.flags, kDevFlagTimeout);
+      }
+    }
+  }
+}
+
+}  // namespace fd

@@ -1,0 +1,245 @@
+/*
+ * fd.h -- C ABI of libfd: split-KV (Flash-Decoding) single-token decode attention
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * Sources, cited by page title and section throughout this library:
+ *   [AI-Infra]  "AI Infra: math and infra optimisation in large models"
+ *               (gitcode.csdn.net/6a17a6c1662f9a54cb77c20d.html), sections 2.2-2.6.
+ *   [FD-QA]     "FlashDecoding interview notes: how V_i relates to V_j, V_i is the old O,
+ *               is LSE there against overflow?" (gtnt.cn/news/53829), sections one-three.
+ *   [Split-avg] "averaging split outputs is wrong" essay (2kiu.com/news/6053916),
+ *               sections "weight block results with log-sum-exp", "the split count is a
+ *               cost account", "why this counter-example exposes averaging".
+ *
+ * What one call computes ([AI-Infra] 2.6 "Flash-Decoding Split-K"; [FD-QA] one-three):
+ * for every batch row b and query head h, with kv head g = h / G (G = Hq / Hkv,
+ * consecutive grouping), over the keys t < L_b of row b,
+ *     out[b,h,:] = softmax_t( q[b,h,:] . k[b,g,t,:] / sqrt(d) ) @ v[b,g,t,:]
+ *     lse_out[b,h] = log sum_t exp( q[b,h,:] . k[b,g,t,:] / sqrt(d) )   (natural log)
+ * computed as S splits along the KV axis.  Split i covers the logical tokens
+ * [i * split_len, min((i + 1) * split_len, L_b)) with split_len = ceil(L_cap / S); a
+ * split starting at or past L_b is EMPTY.  Each non-empty split writes a normalised
+ * partial output O_i and LSE_i = m_i + log(l_i) (safe-softmax max m_i, shifted exp-sum
+ * l_i; [AI-Infra] 2.3, 2.6 "LSE and online softmax").  A second pass merges the splits
+ * with weights w_i = exp(LSE_i - max_j LSE_j) ([FD-QA] three.2; [Split-avg] "weight
+ * block results with log-sum-exp"); an empty split gets weight 0 and is never read --
+ * it is not a zero-output block with a normal weight.  A row with L_b = 0 gets
+ * out = 0 and lse_out = -infinity.  Decode needs no causal mask: the single query sits
+ * after every cached key ([AI-Infra] 2.5), so only the length mask t < L_b applies,
+ * and stale cache slots at t >= L_b (even NaN) never reach the result.
+ *
+ * Conventions for every entry point:
+ *   - Status: every call returns an fd_status and never aborts; fd_last_error()
+ *     gives a one-line reason for the last failure on the calling thread.
+ *   - Ownership: the caller owns every buffer.  fd_decode_attention allocates no
+ *     device memory.  Only fd_plan_create / fd_plan_resize allocate (the plan's
+ *     workspace), and fd_plan_destroy frees it.
+ *   - Asynchrony: kernels run on the caller's CUDA stream (cudaStream_t passed as
+ *     void*, NULL = the legacy default stream).  Results, and the workspace, become
+ *     valid or reusable only when that stream's work completes ([Split-avg] "the
+ *     split count is a cost account": submission is not completion).
+ *   - Pointers named "device" must be device (or managed) memory of the current
+ *     device; "host" pointers are host memory.
+ */
+#ifndef FD_H_
+#define FD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FD_API __attribute__((visibility("default")))
+#else
+#define FD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FD_OK = 0,
+  FD_ERR_INVALID_ARG = 1,          /* a shape, stride, pointer or size is wrong          */
+  FD_ERR_UNSUPPORTED = 2,          /* valid, but outside what the kernels implement      */
+  FD_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes < fd_workspace_size(...)           */
+  FD_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed                  */
+  FD_ERR_DEVICE_FLAG = 5           /* a kernel flagged bad device-side input (see below) */
+} fd_status;
+
+typedef enum { FD_F32 = 0, FD_BF16 = 1, FD_I32 = 2 } fd_dtype;
+
+/*
+ * A strided tensor view.  Strides are in ELEMENTS; the last dimension must be
+ * contiguous (stride 1) and every other stride a multiple of 16 bytes; data must be
+ * 16-byte aligned.  Unused trailing shape/stride entries are ignored.
+ */
+typedef struct {
+  void* data;
+  int32_t dtype;      /* fd_dtype */
+  int32_t ndim;
+  int64_t shape[4];
+  int64_t stride[4];
+} fd_tensor;
+
+/* Kernel path selection for the partial pass (process-wide setting). */
+typedef enum {
+  FD_PATH_AUTO = 0,   /* tensor-core tile for bf16, CUDA cores otherwise                */
+  FD_PATH_SIMT = 1,   /* CUDA-core dot products for every dtype                          */
+  FD_PATH_MMA = 2     /* tensor-core tile (bf16 only; FD_ERR_UNSUPPORTED for fp32)        */
+} fd_path;
+
+/*
+ * fd_decode_attention -- one decode step of split-KV attention (see the top of file).
+ *
+ *   q            device [B, Hq, d], bf16 or f32.
+ *   k_cache      device, same dtype as q.  Contiguous: [B, Hkv, L_cap, d] (block_table
+ *                NULL).  Paged: [num_pages, Hkv, page_size, d]; logical token t of row
+ *                b is slot t % page_size of page block_table[b][t / page_size] -- the
+ *                table's order is the logical order, never the physical page number
+ *                ([Split-avg] "the split count is a cost account", on masks and paging;
+ *                [AI-Infra] 2.5 on block tables).
+ *   v_cache      device, same shape, strides-pattern and dtype as k_cache.
+ *   seq_lens     device int32 [B]; 0 <= L_b <= L_cap.  Out-of-range values are clamped
+ *                on the device and flagged (FD_DEVFLAG_SEQ_LEN).
+ *   block_table  NULL for a contiguous cache; else a device int32 [B, max_pages] view,
+ *                L_cap = max_pages * page_size.  Entries a row uses must lie in
+ *                [0, num_pages); a bad one is flagged (FD_DEVFLAG_PAGE) and its tokens
+ *                are excluded.  Entries past a row's length are never read.
+ *   page_size    0 for a contiguous cache; else a power of two in [8, 65536].
+ *   num_splits   S >= 1, or 0 to let fd_num_splits_heuristic choose.  S <= 4096.
+ *   out          device [B, Hq, d], bf16 or f32 (bf16 is rounded to nearest even).
+ *   lse_out      device f32 [B, Hq] (contiguous), natural log; may be NULL.
+ *   workspace    device scratch of at least fd_workspace_size(B, Hq, Hkv, d, S) bytes,
+ *                256-byte aligned, zero-filled once before its first use
+ *                (fd_workspace_init).  Calls leave its header as they found it,
+ *                except for device error flags.  Two calls that are in flight at once
+ *                must not share a workspace.
+ *   stream       cudaStream_t (as void*), NULL = legacy default stream.
+ *
+ * Supported: d in {64, 128}; G = Hq / Hkv in {1, 2, 4, 8, 16}; (q, k, v) all bf16
+ * with out bf16 or f32, or all f32 with out f32.  B >= 1, L_cap >= 1.
+ * Errors: FD_ERR_INVALID_ARG for rank/shape/stride/alignment mismatches, Hq % Hkv != 0,
+ * NULL required pointers, num_splits < 0, page_size invalid with a block table;
+ * FD_ERR_UNSUPPORTED for other d, G or dtype combinations; FD_ERR_WORKSPACE_TOO_SMALL;
+ * FD_ERR_CUDA if a launch fails.  On error nothing is launched.
+ */
+FD_API fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
+                              const fd_tensor* v_cache, const int32_t* seq_lens,
+                              const fd_tensor* block_table, int32_t page_size,
+                              int32_t num_splits, fd_tensor* out, float* lse_out,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The two passes of fd_decode_attention as separate calls, for callers that time or
+ * schedule them apart, or that merge partials produced elsewhere (for instance by
+ * another device holding another piece of the sequence: [AI-Infra] 2.6 "Sequence
+ * Parallelism", where only the small LSE metadata travels with each partial output).
+ *
+ * fd_decode_partial: the partial pass only.  Same arguments and checks as
+ * fd_decode_attention without out / lse_out; writes LSE_i and O_i of every split into
+ * the workspace (empty split: LSE_i = -inf, O_i untouched).
+ */
+FD_API fd_status fd_decode_partial(const fd_tensor* q, const fd_tensor* k_cache,
+                            const fd_tensor* v_cache, const int32_t* seq_lens,
+                            const fd_tensor* block_table, int32_t page_size, int32_t num_splits,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Where a workspace keeps the partials of a call with these sizes: *lse_part is
+ * f32 [B, Hq, S] (natural log, -inf for an empty split) and *o_part f32 [B, Hq, S, d].
+ * Host arithmetic only; either output pointer may be NULL.
+ */
+FD_API fd_status fd_workspace_partials(void* workspace, int32_t B, int32_t Hq, int32_t d,
+                                int32_t num_splits, float** lse_part, float** o_part);
+
+/*
+ * fd_merge_partials: the merge pass only.  lse_part device f32 [B, Hq, S] (natural log;
+ * -inf marks a split with no key, which gets weight 0 and whose O_i is never read),
+ * o_part device f32 [B, Hq, S, d] (16-byte aligned), out device [B, Hq, d] bf16 or f32,
+ * lse_out device f32 [B, Hq] or NULL.  d in {64, 128}.  Computes
+ * out = sum_i w_i O_i / sum_i w_i with w_i = exp(LSE_i - max_j LSE_j) and
+ * lse_out = max_j LSE_j + log(sum_i w_i); rows with no non-empty split give out = 0 and
+ * lse_out = -inf ([FD-QA] three.2; [Split-avg] "weight block results with log-sum-exp").
+ */
+FD_API fd_status fd_merge_partials(int32_t B, int32_t Hq, int32_t d, int32_t num_splits,
+                            const float* lse_part, const float* o_part, fd_tensor* out,
+                            float* lse_out, void* stream);
+
+/*
+ * Bytes of workspace a call with these sizes needs: a 256-byte header (device error
+ * flags), the per-split LSE_i [B, Hq, S] f32 and partial outputs O_i [B, Hq, S, d] f32
+ * ([AI-Infra] 2.6 "Flash-Decoding Split-K": each split writes its local O and one LSE
+ * scalar), each region 256-byte aligned.  num_splits must be >= 1 (resolve 0 with
+ * fd_num_splits_heuristic first).  Returns 0 for invalid sizes.
+ */
+FD_API size_t fd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_splits);
+
+/*
+ * Split-count heuristic over batch, heads, head_dim, context and SM count
+ * ([Split-avg] "the split count is a cost account": more splits expose more parallel
+ * work but add partial results, launches and merge cost, which can outweigh the gain
+ * on short contexts; choose by batch, context, head_dim and device).  Returns S >= 1:
+ * enough (b, kv head, split) work units to fill every SM about twice, but no split
+ * shorter than 256 tokens.  Invalid sizes return 1.
+ */
+FD_API int32_t fd_num_splits_heuristic(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int64_t L_cap,
+                                int32_t num_sms);
+
+/* Zero-fill a workspace on `stream` (asynchronous).  Needed once before first use. */
+FD_API fd_status fd_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Device-side error flags kept in the workspace header (bitwise OR). */
+#define FD_DEVFLAG_SEQ_LEN 1u   /* a seq_lens entry was outside [0, L_cap] (clamped)  */
+#define FD_DEVFLAG_PAGE 2u      /* a used block-table entry was outside [0, num_pages) */
+#define FD_DEVFLAG_TIMEOUT 4u   /* a bounded in-kernel wait gave up; that split is empty */
+
+/*
+ * Synchronise `stream`, read the workspace's device error flags into *flags (may be
+ * NULL), clear them, and return FD_ERR_DEVICE_FLAG if any was set, else FD_OK.
+ */
+FD_API fd_status fd_read_device_error(void* workspace, void* stream, uint32_t* flags);
+
+/*
+ * A plan fixes the sizes and the split count, and owns a workspace sized for them and
+ * a completion event.  Changing the split count changes the workspace size, so
+ * fd_plan_resize waits for the plan's last decode to finish (its event) and then
+ * re-sizes workspace and event together ([Split-avg] "the split count is a cost
+ * account": workspace and event count are kept in step by the scheduling layer, and
+ * statistics are not reclaimed before the merge ends).
+ */
+typedef struct fd_plan fd_plan;
+
+/* Create a plan on the current device.  num_splits 0 -> heuristic. */
+FD_API fd_status fd_plan_create(fd_plan** plan, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+                         int64_t L_cap, int32_t num_splits);
+/* The plan's split count and workspace size. */
+FD_API int32_t fd_plan_num_splits(const fd_plan* plan);
+FD_API size_t fd_plan_workspace_bytes(const fd_plan* plan);
+FD_API void* fd_plan_workspace(const fd_plan* plan);
+/* fd_decode_attention with the plan's split count and workspace; records the event. */
+FD_API fd_status fd_plan_decode(fd_plan* plan, const fd_tensor* q, const fd_tensor* k_cache,
+                         const fd_tensor* v_cache, const int32_t* seq_lens,
+                         const fd_tensor* block_table, int32_t page_size, fd_tensor* out,
+                         float* lse_out, void* stream);
+/* Wait for the last decode, then resize workspace and event for a new split count. */
+FD_API fd_status fd_plan_resize(fd_plan* plan, int32_t num_splits);
+FD_API void fd_plan_destroy(fd_plan* plan);
+
+/* Select the partial-pass kernel path for later calls (process-wide). */
+FD_API fd_status fd_set_path(int32_t path);
+FD_API int32_t fd_get_path(void);
+
+/* Split count a call with these sizes and this num_splits argument would use. */
+FD_API int32_t fd_resolve_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int64_t L_cap,
+                              int32_t num_splits);
+
+FD_API const char* fd_status_string(fd_status status);
+/* One-line reason for the last non-FD_OK status returned on this thread. */
+FD_API const char* fd_last_error(void);
+/* Library version string. */
+FD_API const char* fd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FD_H_ */

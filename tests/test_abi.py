@@ -1,0 +1,201 @@
+"""The C-ABI library loads and exports every symbol include/fd.h declares, and its
+host-only entry points (sizes, heuristic, validation) behave -- no GPU needed.
+
+Validation tests pass fake, never-dereferenced device addresses: every case below is
+rejected on the host before the library touches a pointer or calls CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import decode_attention_05_gb300 as fd
+from decode_attention_05_gb300._binding import FdTensor
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fd.h")
+
+INVALID, UNSUPPORTED, WS_SMALL = 1, 2, 3
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^FD_API\s+[\w\s\*]+?\b(fd_\w+)\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("fd_decode_attention", "fd_workspace_size", "fd_num_splits_heuristic",
+                     "fd_plan_create", "fd_plan_resize", "fd_plan_destroy",
+                     "fd_read_device_error", "fd_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = fd.lib()
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_library_exports_nothing_undeclared():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", fd.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = sorted({l.split()[-1] for l in out.splitlines() if " T " in l and "fd_" in l})
+    assert exported == declared_functions()
+
+
+def test_status_strings_and_version():
+    lib = fd.lib()
+    for code, name in [(0, b"FD_OK"), (1, b"FD_ERR_INVALID_ARG"), (2, b"FD_ERR_UNSUPPORTED"),
+                       (3, b"FD_ERR_WORKSPACE_TOO_SMALL"), (4, b"FD_ERR_CUDA"),
+                       (5, b"FD_ERR_DEVICE_FLAG")]:
+        assert lib.fd_status_string(code) == name
+    assert b"sm_103a" in lib.fd_version()
+
+
+def test_workspace_size_layout():
+    # 256-byte header, then LSE_i [B, Hq, S] f32 and O_i [B, Hq, S, d] f32, each
+    # region rounded up to 256 bytes.
+    def expect(B, Hq, d, S):
+        up = lambda x: (x + 255) // 256 * 256
+        lse_end = 256 + B * Hq * S * 4
+        return up(up(lse_end) + B * Hq * S * d * 4)
+    for B, Hq, Hkv, d, S in [(1, 64, 8, 128, 38), (4, 32, 32, 128, 3), (1, 1, 1, 64, 4),
+                             (16, 32, 8, 128, 256), (3, 6, 3, 64, 4096)]:
+        assert fd.workspace_size(B, Hq, Hkv, d, S) == expect(B, Hq, d, S)
+    assert fd.workspace_size(1, 1, 1, 64, 0) == 0
+    assert fd.workspace_size(1, 1, 1, 64, 4097) == 0
+    assert fd.workspace_size(0, 1, 1, 64, 1) == 0
+
+
+def test_heuristic_properties():
+    h = fd.num_splits_heuristic
+    # 128K-context GQA on 152 SMs: enough (b, kv head, split) units for two per SM.
+    S = h(1, 64, 8, 128, 131072, 152)
+    assert 8 * S >= 2 * 152 and S <= 4096
+    # Splits never shorter than 256 tokens: short contexts get few splits.
+    assert h(1, 32, 8, 128, 300, 152) == 2
+    assert h(1, 32, 8, 128, 256, 152) == 1
+    # Enough batch x heads already fills the GPU: one split.
+    assert h(64, 32, 32, 128, 4096, 152) == 1
+    # More SMs -> at least as many splits; longer contexts never fewer.
+    for L in (1024, 8192, 65536, 1 << 20):
+        assert h(1, 64, 8, 128, L, 304) >= h(1, 64, 8, 128, L, 152)
+        assert h(1, 64, 8, 128, 2 * L, 152) >= h(1, 64, 8, 128, L, 152)
+    # Invalid sizes fall back to one split.
+    assert h(0, 64, 8, 128, 1000, 152) == 1
+    assert h(1, 64, 8, 128, 1000, 0) == 1
+
+
+def test_path_setting_round_trip():
+    lib = fd.lib()
+    try:
+        for path in (fd.FD_PATH_SIMT, fd.FD_PATH_MMA, fd.FD_PATH_AUTO):
+            fd.set_path(path)
+            assert fd.get_path() == path
+        with pytest.raises(fd.FdError):
+            fd.set_path(7)
+    finally:
+        lib.fd_set_path(fd.FD_PATH_AUTO)
+
+
+# ---------------------------------------------------------------- host-side validation
+
+FAKE = 0x7f0000000000          # 16-byte aligned, never dereferenced
+
+
+def desc(shape, dtype=1, stride=None, data=FAKE):
+    t = FdTensor()
+    t.data = data
+    t.dtype = dtype
+    t.ndim = len(shape)
+    if stride is None:
+        stride, acc = [], 1
+        for s in reversed(shape):
+            stride.insert(0, acc)
+            acc *= s
+    for i, (s, st) in enumerate(zip(shape, stride)):
+        t.shape[i] = s
+        t.stride[i] = st
+    return t
+
+
+def call(q, k, v, out, *, bt=None, page_size=0, S=4, ws_bytes=1 << 24, ws=FAKE,
+         seq=FAKE, lse=FAKE):
+    lib = fd.lib()
+    r = lambda x: None if x is None else ctypes.byref(x)
+    return lib.fd_decode_attention(r(q), r(k), r(v), seq, r(bt), page_size, S, r(out), lse, ws,
+                                   ws_bytes, None)
+
+
+def good():
+    return (desc([2, 8, 128]), desc([2, 2, 1024, 128]), desc([2, 2, 1024, 128]),
+            desc([2, 8, 128]))
+
+
+@pytest.mark.parametrize("case,expected", [
+    ("null_q", INVALID), ("null_seq", INVALID), ("null_ws", INVALID), ("rank", INVALID),
+    ("hq_not_multiple", INVALID), ("kv_shape_mismatch", INVALID), ("dtype_mix", INVALID),
+    ("head_dim_96", UNSUPPORTED), ("group_3", UNSUPPORTED), ("f32_in_bf16_out", UNSUPPORTED),
+    ("neg_splits", INVALID), ("too_many_splits", INVALID), ("noncontig_last", INVALID),
+    ("misaligned_k", INVALID), ("odd_stride", INVALID), ("page_size_no_table", INVALID),
+    ("page_size_not_pow2", INVALID), ("page_size_small", INVALID), ("table_dtype", INVALID),
+    ("ws_small", WS_SMALL), ("ws_misaligned", INVALID), ("out_shape", INVALID),
+    ("paged_shape", INVALID),
+])
+def test_validation(case, expected):
+    q, k, v, out = good()
+    kw = {}
+    if case == "null_q":
+        q = None
+    elif case == "null_seq":
+        kw["seq"] = None
+    elif case == "null_ws":
+        kw["ws"] = None
+    elif case == "rank":
+        q = desc([2, 8, 128, 1])
+    elif case == "hq_not_multiple":
+        q, out = desc([2, 7, 128]), desc([2, 7, 128])
+    elif case == "kv_shape_mismatch":
+        v = desc([2, 2, 512, 128])
+    elif case == "dtype_mix":
+        k = desc([2, 2, 1024, 128], dtype=0)
+    elif case == "head_dim_96":
+        q, k, v, out = desc([2, 8, 96]), desc([2, 2, 64, 96]), desc([2, 2, 64, 96]), desc([2, 8, 96])
+    elif case == "group_3":
+        q, out = desc([2, 6, 128]), desc([2, 6, 128])
+    elif case == "f32_in_bf16_out":
+        q, k, v = desc([2, 8, 128], 0), desc([2, 2, 1024, 128], 0), desc([2, 2, 1024, 128], 0)
+    elif case == "neg_splits":
+        kw["S"] = -1
+    elif case == "too_many_splits":
+        kw["S"] = 4097
+    elif case == "noncontig_last":
+        k = desc([2, 2, 1024, 128], stride=[2 * 1024 * 256, 1024 * 256, 256, 2])
+    elif case == "misaligned_k":
+        k = desc([2, 2, 1024, 128], data=FAKE + 8)
+    elif case == "odd_stride":
+        k = desc([2, 2, 1024, 128], stride=[2 * 1024 * 130, 1024 * 130, 130, 1])
+    elif case == "page_size_no_table":
+        kw["page_size"] = 16
+    elif case == "page_size_not_pow2":
+        kw["bt"], kw["page_size"] = desc([2, 8], dtype=2), 24
+        k, v = desc([16, 2, 24, 128]), desc([16, 2, 24, 128])
+    elif case == "page_size_small":
+        kw["bt"], kw["page_size"] = desc([2, 8], dtype=2), 4
+        k, v = desc([16, 2, 4, 128]), desc([16, 2, 4, 128])
+    elif case == "table_dtype":
+        kw["bt"], kw["page_size"] = desc([2, 8], dtype=0), 16
+        k, v = desc([16, 2, 16, 128]), desc([16, 2, 16, 128])
+    elif case == "ws_small":
+        kw["ws_bytes"] = 1024
+    elif case == "ws_misaligned":
+        kw["ws"] = FAKE + 16
+    elif case == "out_shape":
+        out = desc([2, 8, 64])
+    elif case == "paged_shape":
+        kw["bt"], kw["page_size"] = desc([2, 8], dtype=2), 16
+        k, v = desc([16, 2, 32, 128]), desc([16, 2, 32, 128])
+    assert call(q, k, v, out, **kw) == expected
+    assert fd.lib().fd_last_error()        # a reason is recorded

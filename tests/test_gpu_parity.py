@@ -1,0 +1,333 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, element by
+element, on the same seeded inputs.
+
+Tolerances (written here, applied to every element):
+  * bf16 inputs (out bf16 or f32):  |got - ref| <= 4e-3 + 8e-3 |ref|
+  * f32 inputs, f32 out:            |got - ref| <= 1e-4
+  * lse_out (natural log):          |got - ref| <= 1e-4 + 1e-5 |ref|
+  * no NaN anywhere; rows with no key give out = 0 and lse = -inf exactly.
+Both kernel paths (CUDA-core and tensor-core) are checked for bf16.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+fd = pytest.importorskip("decode_attention_05_gb300")
+
+PATHS_BF16 = [("simt", 1), ("mma", 2)]
+
+
+@pytest.fixture(autouse=True)
+def _restore_path():
+    yield
+    if torch.cuda.is_available():
+        fd.set_path(fd.FD_PATH_AUTO)
+
+
+_ORACLE_CACHE = {}
+_WORKLOADS = {}
+
+
+def cached(n):
+    """Workload n generated once per session, with its device copy."""
+    if n not in _WORKLOADS:
+        w = workloads.CONFIGS[n]()
+        _WORKLOADS[n] = (w, w.to("cuda"))
+    return _WORKLOADS[n]
+
+
+def ref_for(w, key=None):
+    if key is not None and key in _ORACLE_CACHE:
+        return _ORACLE_CACHE[key]
+    q, k, v, lens, bt, ps = w.oracle_arrays()
+    r = oracle.decode(q, k, v, lens, block_table=bt, page_size=ps)
+    if key is not None:
+        _ORACLE_CACHE[key] = r
+    return r
+
+
+def run(w, num_splits=None, out_dtype=None, path=None, check_flags=True, wd=None):
+    wd = wd if wd is not None else w.to("cuda")
+    if path is not None:
+        fd.set_path(path)
+    S = w.num_splits if num_splits is None else num_splits
+    B, Hq, d = w.q.shape
+    S_res = fd.resolve_num_splits(B, Hq, w.Hkv, d, w.L_cap, S)
+    ws = torch.zeros(fd.workspace_size(B, Hq, w.Hkv, d, S_res), dtype=torch.uint8, device="cuda")
+    out, lse = fd.decode_attention(wd.q, wd.k, wd.v, wd.seq_lens, wd.block_table, wd.page_size,
+                                   S, workspace=ws, out_dtype=out_dtype or w.out_dtype)
+    torch.cuda.synchronize()
+    if check_flags:
+        assert fd.read_device_error(ws) == 0
+    return out.float().cpu().double().numpy(), lse.cpu().double().numpy(), ws, S_res
+
+
+def check(w, got_o, got_l, ref_o, ref_l, rows=None):
+    if rows is not None:
+        flat_o, flat_l = got_o.reshape(-1, got_o.shape[-1]), got_l.reshape(-1)
+        got_o, got_l = flat_o[rows], flat_l[rows]
+        ref_o, ref_l = ref_o.reshape(-1, ref_o.shape[-1])[rows], ref_l.reshape(-1)[rows]
+    assert not np.isnan(got_o).any(), "NaN in out"
+    assert not np.isnan(got_l).any(), "NaN in lse"
+    if w.q.dtype == torch.bfloat16:
+        bound = 4e-3 + 8e-3 * np.abs(ref_o)
+    else:
+        bound = np.full(ref_o.shape, 1e-4)
+    err = np.abs(got_o - ref_o)
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert (err <= bound).all(), "max excess %.3g at %s (got %r, ref %r)" % (
+        (err - bound)[worst], worst, got_o[worst], ref_o[worst])
+    empty = np.isneginf(ref_l)
+    assert np.array_equal(np.isneginf(got_l), empty)
+    assert (got_o[empty] == 0).all()
+    fin = ~empty
+    lerr = np.abs(got_l[fin] - ref_l[fin])
+    assert (lerr <= 1e-4 + 1e-5 * np.abs(ref_l[fin])).all(), "lse max err %.3g" % lerr.max()
+    return float(err.max()) if err.size else 0.0
+
+
+# ------------------------------------------------------------------ pages' example
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_worked_example(dtype):
+    """Scores [0, 0, 10], values [0, 0, 9], split [2 | 1]: the merged output equals the
+    unsplit 9 e^10 / (2 + e^10), and the per-split partials left in the workspace are
+    the blocks' (0, ln 2) and (9, 10), whose naive average 4.5 is far off."""
+    w = workloads.worked_example()
+    if dtype == "bf16":
+        w = workloads.Workload(w.name, w.q.bfloat16(), w.k.bfloat16(), w.v.bfloat16(),
+                               w.seq_lens, num_splits=2, out_dtype=torch.float32)
+    paths = [fd.FD_PATH_SIMT] if dtype == "f32" else [fd.FD_PATH_SIMT, fd.FD_PATH_MMA]
+    exact = 9.0 * math.exp(10.0) / (2.0 + math.exp(10.0))
+    for path in paths:
+        o, l, ws, S = run(w, path=path)
+        assert S == 2
+        tol = 1e-5 if dtype == "f32" else 4e-3 + 8e-3 * exact
+        assert np.abs(o[0, 0] - exact).max() <= tol
+        assert abs(l[0, 0] - math.log(2.0 + math.exp(10.0))) <= 1e-4
+        # Workspace layout: 256-byte header, LSE_i [B, Hq, S], then O_i [B, Hq, S, d].
+        raw = ws.cpu().numpy()
+        lse_parts = raw[256:256 + 2 * 4].view(np.float32)
+        o_off = (256 + 2 * 4 + 255) // 256 * 256
+        o_parts = raw[o_off:o_off + 2 * 64 * 4].view(np.float32).reshape(2, 64)
+        assert abs(lse_parts[0] - math.log(2.0)) < 1e-5 and abs(lse_parts[1] - 10.0) < 1e-5
+        assert np.abs(o_parts[0]).max() < 1e-6 and np.abs(o_parts[1] - 9.0).max() < 1e-5
+        naive = o_parts.mean(axis=0)
+        assert np.abs(naive - exact).min() > 1.0
+
+
+# ------------------------------------------------------------------ the five workloads
+
+def test_config1_tiny_fp32():
+    w = workloads.config1()
+    ref_o, ref_l = ref_for(w, "c1")
+    o, l, _, S = run(w, path=fd.FD_PATH_SIMT)
+    assert S == 4
+    check(w, o, l, ref_o, ref_l)
+    # The tensor-core path does not take fp32 inputs: it says so.
+    with pytest.raises(fd.FdError):
+        run(w, path=fd.FD_PATH_MMA)
+
+
+@pytest.mark.parametrize("name,path", PATHS_BF16)
+@pytest.mark.parametrize("S", [0, 1, 3, 16, 64])
+def test_config2_mha(name, path, S):
+    w, wd = cached(2)
+    ref_o, ref_l = ref_for(w, "c2")
+    o, l, _, _ = run(w, num_splits=S, path=path, wd=wd)
+    check(w, o, l, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("name,path", PATHS_BF16)
+def test_config3_gqa_128k(name, path):
+    w, wd = cached(3)
+    ref_o, ref_l = ref_for(w, "c3")
+    o, l, _, S = run(w, path=path, wd=wd)     # heuristic split count, as bench.py runs it
+    assert 8 * S >= 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    check(w, o, l, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("name,path", PATHS_BF16)
+@pytest.mark.parametrize("S", [0, 7, 64])
+def test_config4_ragged_paged(name, path, S):
+    w, wd = cached(4)
+    ref_o, ref_l = ref_for(w, "c4")
+    o, l, _, S_res = run(w, num_splits=S, path=path, wd=wd)
+    check(w, o, l, ref_o, ref_l)
+    # Row 1 (37 tokens) is shorter than one split: all its other splits are empty.
+    split_len = -(-w.L_cap // S_res)
+    assert int(w.seq_lens[1]) < split_len or S_res == 1
+
+
+@pytest.mark.parametrize("name,path", PATHS_BF16)
+def test_config5_adversarial_error_does_not_grow(name, path):
+    """Spiky scores (~120) in different splits; error must stay within tolerance at every
+    split count and must not grow with it (checked in f32-out mode, no output rounding)."""
+    w, wd = cached(5)
+    ref_o, ref_l = ref_for(w, "c5")
+    errs = {}
+    for S in w.split_sweep:
+        o, l, _, _ = run(w, num_splits=S, path=path, wd=wd)
+        check(w, o, l, ref_o, ref_l)
+        of, lf, _, _ = run(w, num_splits=S, path=path, out_dtype=torch.float32, wd=wd)
+        errs[S] = check(w, of, lf, ref_o, ref_l)
+    for S, e in errs.items():
+        assert e <= 2.0 * errs[1] + 1e-5, errs
+
+
+def test_config5_spikes_dominate():
+    """The spike heads really see scores near 120: their lse is ~120 and their output is
+    close to the spike token's value row."""
+    w, wd = cached(5)
+    ref_o, ref_l = ref_for(w, "c5")
+    spikes = workloads.config5_spikes()
+    G = w.Hq // w.Hkv
+    for b in range(w.B):
+        for g in range(w.Hkv):
+            for j in range(4):
+                h = g * G + j
+                assert 110.0 < ref_l[b, h] < 130.0
+    o, l, _, _ = run(w, num_splits=64, path=fd.FD_PATH_MMA, wd=wd)
+    b, g, j = 3, 5, 2
+    t = int(spikes[b, g, j])
+    vrow = w.v[b, g, t].float().numpy()
+    assert np.abs(o[b, g * G + j] - vrow).max() < 0.05
+
+
+# ------------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("name,path", PATHS_BF16 + [("simt-f32", 1)])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+def test_shapes_ragged_contiguous(name, path, d, G):
+    """Every supported (d, G); ragged rows incl. 0, 1 and tile-boundary lengths; NaN in
+    the stale cache slots past each length; several split counts."""
+    dtype = torch.float32 if name == "simt-f32" else torch.bfloat16
+    Hkv = 2
+    lens = [0, 1, 63, 64, 65, 300, 517]
+    w = workloads.contiguous_case(len(lens), Hkv * G, Hkv, d, 520, lens, seed=7 + d + G,
+                                  dtype=dtype, out_dtype=torch.float32)
+    ref_o, ref_l = ref_for(w)
+    for S in (1, 3, 8, 33):
+        o, l, _, _ = run(w, num_splits=S, path=path)
+        check(w, o, l, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("name,path", PATHS_BF16)
+@pytest.mark.parametrize("ps", [8, 16, 32, 64, 128, 256])
+def test_paged_page_sizes(name, path, ps):
+    lens = [1, 37, 200, 513, 1000, 0, 2048]
+    max_pages = -(-2048 // ps)
+    w = workloads.paged_case(len(lens), 16, 4, 128, ps, max_pages, lens, seed=ps,
+                             extra_pages=3, out_dtype=torch.float32)
+    ref_o, ref_l = ref_for(w)
+    for S in (1, 5, 16):
+        o, l, _, _ = run(w, num_splits=S, path=path)
+        check(w, o, l, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("name,path", PATHS_BF16)
+def test_paged_d64(name, path):
+    lens = [5, 130, 700]
+    w = workloads.paged_case(3, 8, 2, 64, 16, 64, lens, seed=64)
+    ref_o, ref_l = ref_for(w)
+    o, l, _, _ = run(w, num_splits=6, path=path)
+    check(w, o, l, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("name,path", PATHS_BF16)
+def test_many_empty_splits(name, path):
+    """More splits than tiles, up to the 4096 maximum: most splits are empty (weight 0)."""
+    w = workloads.contiguous_case(2, 8, 2, 128, 4096, [3, 4096], seed=11)
+    ref_o, ref_l = ref_for(w)
+    for S in (512, 4096):
+        o, l, _, _ = run(w, num_splits=S, path=path)
+        check(w, o, l, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("name,path", PATHS_BF16)
+def test_strided_views(name, path):
+    """q, k, v and out as strided views of larger buffers (16-byte multiple strides)."""
+    g = torch.Generator().manual_seed(5)
+    big_q = torch.randn(3, 16, 136, generator=g).bfloat16()
+    big_k = torch.randn(3, 4, 700, 136, generator=g).bfloat16()
+    big_v = torch.randn(3, 4, 700, 136, generator=g).bfloat16()
+    q, k, v = big_q[:, ::2, :128], big_k[:, ::2, :600, :128], big_v[:, ::2, :600, :128]
+    lens = torch.tensor([600, 77, 333], dtype=torch.int32)
+    w = workloads.Workload("strided", q, k, v, lens, out_dtype=torch.float32)
+    ref_o, ref_l = ref_for(w)
+    fd.set_path(path)
+    qd, kd, vd = q.cuda(), None, None
+    kd = big_k.cuda()[:, ::2, :600, :128]
+    vd = big_v.cuda()[:, ::2, :600, :128]
+    qd = big_q.cuda()[:, ::2, :128]
+    out_big = torch.zeros(3, 8, 160, dtype=torch.float32, device="cuda")
+    out = out_big[:, :, :128]
+    fd.decode_attention(qd, kd, vd, lens.cuda(), num_splits=4, out=out)
+    torch.cuda.synchronize()
+    o = out.cpu().double().numpy()
+    assert (out_big[:, :, 128:] == 0).all()
+    lse = fd.decode_attention(qd, kd, vd, lens.cuda(), num_splits=4,
+                              out_dtype=torch.float32)[1].cpu().double().numpy()
+    check(w, o, lse, ref_o, ref_l)
+
+
+def test_bad_page_and_length_are_flagged():
+    """A used block-table entry outside the pool and a length beyond capacity are
+    reported through the workspace flags; the outputs stay finite."""
+    lens = [40, 50]
+    w = workloads.paged_case(2, 8, 2, 128, 16, 4, lens, seed=3)
+    wd = w.to("cuda")
+    bt = wd.block_table.clone()
+    bt[0, 1] = 10_000
+    ws = torch.zeros(fd.workspace_size(2, 8, 2, 128, 2), dtype=torch.uint8, device="cuda")
+    out, lse = fd.decode_attention(wd.q, wd.k, wd.v, wd.seq_lens, bt, 16, 2, workspace=ws)
+    torch.cuda.synchronize()
+    assert fd.read_device_error(ws) == 2            # FD_DEVFLAG_PAGE
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    assert fd.read_device_error(ws) == 0            # cleared by the read
+    seq = torch.tensor([40, 65], dtype=torch.int32, device="cuda")   # capacity is 64
+    fd.decode_attention(wd.q, wd.k, wd.v, seq, wd.block_table, 16, 2, workspace=ws)
+    torch.cuda.synchronize()
+    assert fd.read_device_error(ws) & 1             # FD_DEVFLAG_SEQ_LEN
+
+
+def test_plan_resize_keeps_results():
+    w = workloads.contiguous_case(2, 16, 4, 128, 3000, [3000, 1234], seed=21,
+                                  out_dtype=torch.float32)
+    ref_o, ref_l = ref_for(w)
+    wd = w.to("cuda")
+    plan = fd.Plan(2, 16, 4, 128, 3000, 4)
+    try:
+        assert plan.num_splits == 4
+        bytes4 = plan.workspace_bytes
+        o, l = plan.decode(wd.q, wd.k, wd.v, wd.seq_lens, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
+        plan.resize(37)
+        assert plan.num_splits == 37 and plan.workspace_bytes > bytes4
+        o, l = plan.decode(wd.q, wd.k, wd.v, wd.seq_lens, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
+    finally:
+        plan.close()
+
+
+def test_side_stream_and_events():
+    """Work issued on a side stream completes before results are read there."""
+    w = workloads.contiguous_case(1, 8, 8, 128, 2048, seed=31, out_dtype=torch.float32)
+    ref_o, ref_l = ref_for(w)
+    wd = w.to("cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o, l = fd.decode_attention(wd.q, wd.k, wd.v, wd.seq_lens, num_splits=8,
+                                   out_dtype=torch.float32)
+    s.synchronize()
+    check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
