@@ -61,6 +61,8 @@ def _declare(L):
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     L.fd_decode_attention.restype = ctypes.c_int
     L.fd_decode_attention.argtypes = [P, P, P, vp, P, i32, i32, P, vp, vp, sz, vp]
+    L.fd_decode_attention_noalloc.restype = ctypes.c_int
+    L.fd_decode_attention_noalloc.argtypes = [P, P, P, vp, P, i32, i32, P, vp, vp]
     L.fd_decode_partial.restype = ctypes.c_int
     L.fd_decode_partial.argtypes = [P, P, P, vp, P, i32, i32, vp, sz, vp]
     L.fd_workspace_partials.restype = ctypes.c_int
@@ -211,6 +213,20 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
                                workspace.numel() * workspace.element_size(),
                                _stream_handle(stream))
     _check(st)
+    return out, lse_out
+
+
+def decode_attention_noalloc(q, k_cache, v_cache, seq_lens, out: torch.Tensor,
+                             lse_out: Optional[torch.Tensor] = None, block_table=None,
+                             page_size: int = 0, num_splits: int = 0, stream=None):
+    """fd_decode_attention_noalloc: the caller passes every buffer, the library uses
+    its built-in scratch instead of a workspace (see include/fd.h for the limits)."""
+    dq, dk, dv, dbt, do = (tensor_desc(q), tensor_desc(k_cache), tensor_desc(v_cache),
+                           tensor_desc(block_table), tensor_desc(out))
+    _check(lib().fd_decode_attention_noalloc(
+        ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), seq_lens.data_ptr(), _ref(dbt),
+        page_size, num_splits, ctypes.byref(do), None if lse_out is None else lse_out.data_ptr(),
+        _stream_handle(stream)))
     return out, lse_out
 
 

@@ -159,6 +159,11 @@ int current_sm_count() {
 
 }  // namespace
 
+namespace fd {
+// Lets other translation units of the library report a failure through fd_last_error.
+fd_status record_error(fd_status st, const char* message) { return fail(st, "%s", message); }
+}  // namespace fd
+
 extern "C" {
 
 const char* fd_version(void) { return "fd 0.1.0 (sm_103a)"; }

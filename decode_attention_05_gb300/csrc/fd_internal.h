@@ -56,6 +56,9 @@ cudaError_t launch_partial_mma(const Params& p, const CUtensorMap& tk, const CUt
                                cudaStream_t stream);
 cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool pdl);
 
+// Record `message` as the calling thread's fd_last_error() and return `st`.
+fd_status record_error(fd_status st, const char* message);
+
 // Tile height (tokens) used by the kernels for a dtype and head dim.
 inline int tile_tokens(int d, int esz) { return kTileBytes / (d * esz); }
 

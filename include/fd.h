@@ -166,6 +166,28 @@ FD_API fd_status fd_merge_partials(int32_t B, int32_t Hq, int32_t d, int32_t num
                             float* lse_out, void* stream);
 
 /*
+ * fd_decode_attention_noalloc -- fd_decode_attention for callers that cannot allocate
+ * device memory when they run a step and have no workspace to hand over (for instance
+ * a plugin whose host framework owns all device memory, or a loop with a memory budget
+ * fixed at start-up).  The pages have no counterpart: this is a library convenience.
+ *
+ * Same arguments, checks and results as fd_decode_attention, minus the workspace: the
+ * split partials go to a scratch array built into the library (8 MiB per device, held
+ * by every GPU that loads the library until the process exits).  A call that would need
+ * more than 8 MiB (fd_workspace_size of its sizes and resolved split count) returns
+ * FD_ERR_UNSUPPORTED and launches nothing.  All calls on a device share the array:
+ * calls that can overlap on the GPU race and must be ordered by the caller.  The first
+ * call on each device sets the array up (looks up its address and zero-fills it once,
+ * synchronously); make it before any stream capture.  Device-side input flags are not
+ * reported by this entry point.  Allocates nothing (no cudaMalloc / cudaFree).
+ */
+FD_API fd_status fd_decode_attention_noalloc(const fd_tensor* q, const fd_tensor* k_cache,
+                                      const fd_tensor* v_cache, const int32_t* seq_lens,
+                                      const fd_tensor* block_table, int32_t page_size,
+                                      int32_t num_splits, fd_tensor* out, float* lse_out,
+                                      void* stream);
+
+/*
  * Bytes of workspace a call with these sizes needs: a 256-byte header (device error
  * flags), the per-split LSE_i [B, Hq, S] f32 and partial outputs O_i [B, Hq, S, d] f32
  * ([AI-Infra] 2.6 "Flash-Decoding Split-K": each split writes its local O and one LSE
