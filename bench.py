@@ -56,7 +56,7 @@ def parse_args():
     ap.add_argument("--num-splits", type=int, default=0, help="0 = library heuristic")
     ap.add_argument("--path", choices=["auto", "simt", "mma"], default="auto")
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -80,13 +80,21 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {
+    "fd_partial_mma_kernel": ["fd_partial_mma.cu", "fd_pipeline.cuh", "fd_epilogue.cuh",
+                              "fd_device.cuh", "fd_internal.h"],
+    "fd_partial_simt_kernel": ["fd_partial_simt.cu", "fd_partial_simt.cuh", "fd_pipeline.cuh",
+                               "fd_epilogue.cuh", "fd_device.cuh", "fd_internal.h"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the source files that define `kernel` (ties an ncu record to them)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_attention_05_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -97,7 +105,7 @@ def recorded_traffic(kernel: str, workload: str):
         with open(PROFILE_TRAFFIC) as f:
             rec = json.load(f)
         e = rec["entries"][kernel + "|" + workload]
-        if e["source_hash"] != kernel_source_hash():
+        if e["source_hash"] != kernel_source_hash(kernel):
             return None
         return float(e["dram_bytes_per_launch"])
     except Exception:  # noqa: BLE001
@@ -158,35 +166,58 @@ class ClockSampler:
 def oracle_sample(w, budget_s: float):
     """Time the fp64 oracle (as it stands) on a bounded sample of the workload.
 
-    The sample is `rows` query heads (spread over the kv heads) over the first
-    `tokens` keys of each row, sized to take roughly `budget_s` seconds.  Returns
-    (KV GB/s in the step's terms, threads used, sample description, seconds)."""
+    If a whole step fits the budget, whole steps are repeated until about `budget_s`
+    seconds of work are done and the median step is kept.  Otherwise the sample is
+    every query head over the first `tokens` keys (uniform lengths) or a subset of the
+    query heads (ragged lengths), scaled to a step.  Returns (KV GB/s in the step's
+    terms, threads used, sample description, seconds of work, step seconds)."""
+    import statistics
+
     import oracle
     q, k, v, lens, bt, ps = w.oracle_arrays()
     threads = oracle.max_threads()
-    B, Hq = w.B, w.Hq
-    rows = list(range(0, B * Hq, max(1, (B * Hq) // threads)))[:threads]
+    n_rows = w.B * w.Hq
     L = int(lens.max())
+    uniform = int(lens.min()) == L
 
-    def run(tokens):
-        sl = lens.copy()
-        sl[:] = min(tokens, L)
+    def timed(seq, rows=None):
         t0 = time.perf_counter()
-        oracle.decode(q, k, v, sl, block_table=bt, page_size=ps, rows=rows)
+        oracle.decode(q, k, v, seq, block_table=bt, page_size=ps, rows=rows)
         return time.perf_counter() - t0
 
-    probe = min(L, 4096)
-    t_probe = run(probe)
-    tokens = int(min(L, max(probe, probe * budget_s / max(t_probe, 1e-6))))
-    t = run(tokens)
-    # Fraction of one full step this sample covers: rows / (B * Hq) of the rows, and
-    # tokens / L of each row (all rows have length L in the timed workloads).
-    frac = (len(rows) / (B * Hq)) * (tokens / L)
-    step_s = t / frac
+    probe_tokens = min(L, 2048)
+    if uniform:
+        sl = lens.copy()
+        sl[:] = probe_tokens
+        est_step = timed(sl) * L / probe_tokens
+    else:
+        probe_rows = list(range(0, n_rows, max(1, n_rows // threads)))[:threads]
+        est_step = timed(lens, probe_rows) * n_rows / len(probe_rows)
+    if est_step <= budget_s:
+        times = [timed(lens)]
+        while sum(times) < budget_s and len(times) < 100000:
+            times.append(timed(lens))
+        step_s = statistics.median(times)
+        work = sum(times)
+        desc = "whole step (all %d query heads, all keys) x%d, median; %.1f s of work" % (
+            n_rows, len(times), work)
+    elif uniform:
+        tokens = max(probe_tokens, int(L * budget_s / est_step))
+        sl = lens.copy()
+        sl[:] = tokens
+        work = timed(sl)
+        step_s = work * L / tokens
+        desc = "all %d query heads x first %d of %d keys, scaled to a step; %.1f s of work" % (
+            n_rows, tokens, L, work)
+    else:
+        keep = max(1, int(n_rows * budget_s / est_step))
+        rows = list(range(0, n_rows, max(1, n_rows // keep)))[:keep]
+        work = timed(lens, rows)
+        step_s = work * n_rows / len(rows)
+        desc = "%d of %d query heads, all keys, scaled to a step; %.1f s of work" % (
+            len(rows), n_rows, work)
     gbs = w.kv_bytes() / step_s / 1e9
-    desc = "%d of %d query heads x first %d of %d keys (%.4f of a step), %.1f s" % (
-        len(rows), B * Hq, tokens, L, frac, t)
-    return gbs, min(threads, len(rows)), desc, t, step_s
+    return gbs, threads, desc, work, step_s
 
 
 # ----------------------------------------------------------------------------- arms

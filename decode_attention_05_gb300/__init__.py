@@ -11,6 +11,6 @@ from __future__ import annotations
 from ._binding import (  # noqa: F401
     FD_PATH_AUTO, FD_PATH_MMA, FD_PATH_SIMT, FdError, Plan, decode_attention,
     decode_attention_noalloc, decode_partial, get_path, lib, library_path, merge_partials,
-    num_splits_heuristic, read_device_error, resolve_num_splits, set_path, workspace_init,
+    num_splits_for_lengths, num_splits_heuristic, read_device_error, resolve_num_splits, set_path, workspace_init,
     workspace_partials, workspace_size,
 )

@@ -74,6 +74,8 @@ def _declare(L):
     L.fd_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.fd_num_splits_heuristic.restype = i32
     L.fd_num_splits_heuristic.argtypes = [i32, i32, i32, i32, i64, i32]
+    L.fd_num_splits_for_lengths.restype = i32
+    L.fd_num_splits_for_lengths.argtypes = [i32, i32, i32, i32, i64, vp, i32]
     L.fd_resolve_num_splits.restype = i32
     L.fd_resolve_num_splits.argtypes = [i32, i32, i32, i32, i64, i32]
     L.fd_workspace_init.restype = ctypes.c_int
@@ -149,6 +151,15 @@ def workspace_size(B: int, Hq: int, Hkv: int, d: int, num_splits: int) -> int:
 
 def num_splits_heuristic(B: int, Hq: int, Hkv: int, d: int, L_cap: int, num_sms: int) -> int:
     return int(lib().fd_num_splits_heuristic(B, Hq, Hkv, d, L_cap, num_sms))
+
+
+def num_splits_for_lengths(B: int, Hq: int, Hkv: int, d: int, L_cap: int, seq_lens,
+                           num_sms: int) -> int:
+    """fd_num_splits_for_lengths over host lengths (a CPU int32 tensor or a sequence)."""
+    lens = torch.as_tensor(seq_lens, dtype=torch.int32).cpu().contiguous()
+    if lens.numel() != B:
+        raise ValueError("need one length per batch row")
+    return int(lib().fd_num_splits_for_lengths(B, Hq, Hkv, d, L_cap, lens.data_ptr(), num_sms))
 
 
 def resolve_num_splits(B: int, Hq: int, Hkv: int, d: int, L_cap: int, num_splits: int) -> int:

@@ -19,6 +19,7 @@ namespace {
 
 thread_local char g_last_error[512] = "";
 std::atomic<int> g_path{FD_PATH_AUTO};
+std::atomic<uint32_t> g_epoch{0x5eed0001u};   // per-call ticket epochs of the fused merge
 
 fd_status fail(fd_status st, const char* fmt, ...) {
   va_list ap;
@@ -31,7 +32,6 @@ fd_status fail(fd_status st, const char* fmt, ...) {
 constexpr size_t kAlign = 256;
 constexpr size_t kHeaderBytes = 256;
 constexpr int32_t kMaxSplits = 4096;
-constexpr int64_t kMinSplitTokens = 256;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -45,16 +45,20 @@ int ilog2(int64_t x) {
 
 int esize(int32_t dtype) { return dtype == FD_BF16 ? 2 : 4; }
 
-// Workspace regions for given sizes.
+// Workspace regions for given sizes: header (device flags) | LSE_i [B, Hq, S] |
+// O_i [B, Hq, S, d] | ticket counters [B, Hkv] (64-bit) of the fused merge; each region
+// 256-byte aligned.  The counters need no particular initial contents (take_ticket in
+// fd_epilogue.cuh), so one workspace serves calls of any sizes that fit it.
 struct WsLayout {
-  size_t lse_off, o_off, total;
+  size_t lse_off, o_off, cnt_off, total;
 };
 
-WsLayout ws_layout(int64_t B, int64_t Hq, int64_t d, int64_t S) {
+WsLayout ws_layout(int64_t B, int64_t Hq, int64_t Hkv, int64_t d, int64_t S) {
   WsLayout w;
   w.lse_off = kHeaderBytes;
   w.o_off = align_up(w.lse_off + (size_t)(B * Hq * S) * sizeof(float), kAlign);
-  w.total = align_up(w.o_off + (size_t)(B * Hq * S * d) * sizeof(float), kAlign);
+  w.cnt_off = align_up(w.o_off + (size_t)(B * Hq * S * d) * sizeof(float), kAlign);
+  w.total = align_up(w.cnt_off + (size_t)(B * Hkv) * sizeof(unsigned long long), kAlign);
   return w;
 }
 
@@ -79,8 +83,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// A KV cache viewed as 5-D for TMA: {elements of one 128-byte line, lines per row,
-// tokens (L_cap or page_size), kv heads, batch rows (or pages)}, 128-byte swizzle.
+// A KV cache viewed as 5-D for TMA: {elements of one 128-byte line, tokens (L_cap or
+// page_size), 128-byte lines per row, kv heads, batch rows (or pages)}, 128-byte swizzle.
+// The line dimension sits outside the row dimension (its stride, 128 B, is smaller than
+// the row stride) so that a box of R rows lands in shared memory line-slice by
+// line-slice: [line][row][128 B].
 struct MapKey {
   const void* ptr;
   int32_t dtype;
@@ -107,13 +114,13 @@ fd_status make_kv_map(const fd_tensor* t, uint32_t box_rows, CUtensorMap* out) {
   memset(&key, 0, sizeof key);
   key.ptr = t->data;
   key.dtype = t->dtype;
-  key.dims[0] = (uint64_t)(128 / es);
-  key.dims[1] = (uint64_t)(d * es / 128);
-  key.dims[2] = (uint64_t)t->shape[2];
-  key.dims[3] = (uint64_t)t->shape[1];
-  key.dims[4] = (uint64_t)t->shape[0];
-  key.strides[0] = 128;
-  key.strides[1] = (uint64_t)t->stride[2] * es;
+  key.dims[0] = (uint64_t)(128 / es);              // elements of one 128-byte line
+  key.dims[1] = (uint64_t)t->shape[2];              // token rows (L_cap or page_size)
+  key.dims[2] = (uint64_t)(d * es / 128);           // 128-byte lines per row
+  key.dims[3] = (uint64_t)t->shape[1];              // kv heads
+  key.dims[4] = (uint64_t)t->shape[0];              // batch rows or pages
+  key.strides[0] = (uint64_t)t->stride[2] * es;     // next row
+  key.strides[1] = 128;                             // next line of the same row
   key.strides[2] = (uint64_t)t->stride[1] * es;
   key.strides[3] = (uint64_t)t->stride[0] * es;
   key.box_rows = box_rows;
@@ -129,7 +136,9 @@ fd_status make_kv_map(const fd_tensor* t, uint32_t box_rows, CUtensorMap* out) {
   }
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(FD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const cuuint32_t box[5] = {(cuuint32_t)key.dims[0], (cuuint32_t)key.dims[1], box_rows, 1, 1};
+  // One box = `box_rows` token rows, all lines: it lands as [line][row][128 B], so the
+  // lines of one column slice of consecutive rows are consecutive 128-byte lines.
+  const cuuint32_t box[5] = {(cuuint32_t)key.dims[0], box_rows, (cuuint32_t)key.dims[2], 1, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUtensorMap m;
   CUresult r = enc(&m, t->dtype == FD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -194,25 +203,7 @@ int32_t fd_get_path(void) { return g_path.load(); }
 size_t fd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_splits) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || num_splits <= 0 || num_splits > kMaxSplits)
     return 0;
-  return ws_layout(B, Hq, d, num_splits).total;
-}
-
-int32_t fd_num_splits_heuristic(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int64_t L_cap,
-                                int32_t num_sms) {
-  if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || L_cap <= 0 || num_sms <= 0) return 1;
-  // Work units are (b, kv head) pairs; each split multiplies them.  Aim for two CTAs on
-  // every SM, but never cut a split below kMinSplitTokens tokens: below that the
-  // partial results and the merge cost more than the extra parallelism returns.
-  const int64_t units = (int64_t)B * Hkv;
-  const int64_t target = 2 * (int64_t)num_sms;
-  int64_t S = (target + units - 1) / units;
-  const int64_t max_by_len = (L_cap + kMinSplitTokens - 1) / kMinSplitTokens;
-  if (S > max_by_len) S = max_by_len;
-  if (S > kMaxSplits) S = kMaxSplits;
-  if (S < 1) S = 1;
-  (void)Hq;
-  (void)d;
-  return (int32_t)S;
+  return ws_layout(B, Hq, Hkv, d, num_splits).total;
 }
 
 int32_t fd_resolve_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int64_t L_cap,
@@ -343,7 +334,7 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   int32_t S = num_splits > 0 ? num_splits
                              : fd_num_splits_heuristic((int32_t)B, (int32_t)Hq, (int32_t)Hkv,
                                                        (int32_t)d, L_cap, current_sm_count());
-  const WsLayout wl = ws_layout(B, Hq, d, S);
+  const WsLayout wl = ws_layout(B, Hq, Hkv, d, S);
   if (((uintptr_t)workspace & (kAlign - 1)) != 0)
     return fail(FD_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if (workspace_bytes < wl.total)
@@ -383,10 +374,15 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   p.bt_sb = bt_sb;
   p.page_size = paged ? page_size : 0;
   p.log2_page = paged ? ilog2(page_size) : 0;
+  p.log2_box = ilog2(box_rows);
   p.max_pages = max_pages;
   p.num_pages = paged ? k_cache->shape[0] : 0;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.flags = reinterpret_cast<uint32_t*>(ws);
+  p.counters = reinterpret_cast<unsigned long long*>(ws + wl.cnt_off);
+  uint32_t epoch = g_epoch.fetch_add(1u);
+  if (epoch == 0u) epoch = g_epoch.fetch_add(1u);   // 0 would match a zeroed word
+  p.epoch = epoch;
   p.lse_part = reinterpret_cast<float*>(ws + wl.lse_off);
   p.o_part = reinterpret_cast<float*>(ws + wl.o_off);
   p.out = out ? out->data : nullptr;
@@ -427,9 +423,8 @@ fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
   fd_status st = prepare(q, k_cache, v_cache, seq_lens, block_table, page_size, num_splits, out,
                          lse_out, workspace, workspace_bytes, true, &pr);
   if (st != FD_OK) return st;
-  st = launch_partial(pr, (cudaStream_t)stream);
-  if (st != FD_OK) return st;
-  return launch_merge(pr.p, (cudaStream_t)stream);
+  // One launch: the last CTA of each (b, kv head) group merges the group's splits.
+  return launch_partial(pr, (cudaStream_t)stream);
 }
 
 fd_status fd_decode_partial(const fd_tensor* q, const fd_tensor* k_cache,
@@ -440,6 +435,7 @@ fd_status fd_decode_partial(const fd_tensor* q, const fd_tensor* k_cache,
   fd_status st = prepare(q, k_cache, v_cache, seq_lens, block_table, page_size, num_splits,
                          nullptr, nullptr, workspace, workspace_bytes, false, &pr);
   if (st != FD_OK) return st;
+  pr.p.counters = nullptr;          // partials only: the merge is a separate call
   return launch_partial(pr, (cudaStream_t)stream);
 }
 
@@ -447,7 +443,7 @@ fd_status fd_workspace_partials(void* workspace, int32_t B, int32_t Hq, int32_t 
                                 int32_t num_splits, float** lse_part, float** o_part) {
   if (!workspace || B <= 0 || Hq <= 0 || d <= 0 || num_splits <= 0 || num_splits > kMaxSplits)
     return fail(FD_ERR_INVALID_ARG, "invalid workspace or sizes");
-  const WsLayout wl = ws_layout(B, Hq, d, num_splits);
+  const WsLayout wl = ws_layout(B, Hq, 1, d, num_splits);   // partial offsets need no Hkv
   if (lse_part) *lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + wl.lse_off);
   if (o_part) *o_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + wl.o_off);
   return FD_OK;

@@ -128,4 +128,17 @@ __device__ __forceinline__ uint32_t swz128(uint32_t line, uint32_t chunk) {
   return line * 128u + ((chunk ^ (line & 7u)) << 4);
 }
 
+// Byte offset, inside a K or V tile, of 16-byte chunk `c16` (0 .. row bytes / 16 - 1) of
+// token row `r`.  The tile is a sequence of TMA boxes of R = 2^lb rows each (the whole
+// tile, or one page); a box holds its rows line-slice by line-slice, [line][row][128 B],
+// so row r sits in box r >> lb, and its line l is 128-byte line
+// ((r >> lb) * LINES + l) * R + (r mod R) of the tile.  R is a multiple of 8, so the
+// swizzle phase of that line is r mod 8: 8 consecutive rows of one 16-byte column hit 8
+// different bank groups (conflict-free ldmatrix).
+template <int LINES>
+__device__ __forceinline__ uint32_t tile_chunk(uint32_t r, uint32_t c16, uint32_t lb) {
+  const uint32_t X = ((((r >> lb) * LINES) + (c16 >> 3)) << lb) | (r & ((1u << lb) - 1u));
+  return swz128(X, c16 & 7u);
+}
+
 }  // namespace fd

@@ -15,6 +15,8 @@
 // writes LSE_i = -inf and no O_i.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "fd_pipeline.cuh"
 
 namespace fd {
@@ -63,6 +65,126 @@ __device__ __forceinline__ void merge_warps_and_store(const Params& p, const Spl
       p.lse_part[row * p.S + si.split] = kNegInf;
     }
   }
+}
+
+// ---------------------------------------------------------------- fused merge
+//
+// Single-launch decode: every CTA of a (b, kv head) group -- empty splits included --
+// publishes its partials, then takes a ticket on the group's counter; the CTA that
+// draws the last ticket merges the group's G query heads.  No CTA ever waits for
+// another: the last to arrive finds every partial already visible (writers fence, then
+// take their ticket; the last reader fences after it), so there is no second kernel and
+// no grid-wide dependency ("2kiu.com/news/6053916", section "the split count is a cost
+// account": the merge may start only when every partial it needs is visible).
+//
+// Merge of one row (warp w takes heads w, w + NCW, ...; a lane holds D / 32 dims): the
+// splits are folded 16 at a time with a running maximum, the same online rule as inside
+// a split, so all loads of a batch are issued before any result is needed:
+//   M' = max(M, max_s LSE_s),  W = W 2^(M - M') + sum_s 2^(LSE_s - M'),
+//   acc = acc 2^(M - M') + sum_s 2^(LSE_s - M') O_s          (base-2 of the natural LSEs)
+// ending with out = acc / W and lse_out = M + log W.  An empty split (LSE = -inf) has
+// weight 0 and its O_s never reaches the sum (it is selected away, never multiplied:
+// its memory may hold anything).  A row with no non-empty split gives 0 and -inf.
+template <int D, int NCW>
+__device__ __forceinline__ void merge_group(const Params& p, int b, int g, int ctid) {
+  constexpr int VEC = D / 32;
+  constexpr int BATCH = 16;
+  constexpr float kLog2e = 1.4426950408889634f;
+  const int warp = ctid >> 5, lane = ctid & 31;
+  for (int h = warp; h < p.G; h += NCW) {
+    const int64_t row = (int64_t)b * p.Hq + (int64_t)g * p.G + h;
+    const float* lse = p.lse_part + row * p.S;
+    const float* ob = p.o_part + row * p.S * D + lane * VEC;
+    float M = kNegInf, W = 0.f, acc[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+    for (int s0 = 0; s0 < p.S; s0 += BATCH) {
+      float ls[BATCH], v[BATCH][VEC];
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const bool in = s0 + u < p.S;
+        ls[u] = in ? __ldcg(lse + s0 + u) * kLog2e : kNegInf;
+        if constexpr (VEC == 4) {
+          const float4 t = in ? __ldcg(reinterpret_cast<const float4*>(ob + (int64_t)(s0 + u) * D))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+        } else {
+          const float2 t = in ? __ldcg(reinterpret_cast<const float2*>(ob + (int64_t)(s0 + u) * D))
+                              : make_float2(0.f, 0.f);
+          v[u][0] = t.x; v[u][1] = t.y;
+        }
+      }
+      float mb = ls[0];
+#pragma unroll
+      for (int u = 1; u < BATCH; ++u) mb = fmaxf(mb, ls[u]);
+      const float mn = fmaxf(M, mb);
+      if (mn == kNegInf) continue;                    // nothing non-empty yet
+      const float c = (M == kNegInf) ? 0.f : ex2(M - mn);
+      W *= c;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[e] *= c;
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const bool live = ls[u] != kNegInf;
+        const float w = live ? ex2(ls[u] - mn) : 0.f;
+        W += w;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w, live ? v[u][e] : 0.f, acc[e]);
+      }
+      M = mn;
+    }
+    const int hq = g * p.G + h;
+    const int64_t obase = (int64_t)b * p.out_sb + (int64_t)hq * p.out_sh + lane * VEC;
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      const float o = acc[e] * inv;
+      if (p.out_bf16) {
+        reinterpret_cast<__nv_bfloat16*>(p.out)[obase + e] = __float2bfloat16_rn(o);
+      } else {
+        reinterpret_cast<float*>(p.out)[obase + e] = o;
+      }
+    }
+    if (lane == 0 && p.lse_out != nullptr)
+      p.lse_out[row] = W > 0.f ? (M + lg2_approx(W)) * 0.6931471805599453f : kNegInf;
+  }
+}
+
+// Take this CTA's ticket for its (b, kv head) group.  A counter word holds
+// (epoch << 32 | arrivals).  Each call brings a fresh epoch, so the first arrival of a
+// call restarts the count whatever the word held before (a workspace reused with other
+// sizes, stale data); the last arrival also puts the word back to 0, so a launch that
+// is replayed as is starts from a clean count too.  Lock-free: a failed compare-and-swap
+// means another CTA's succeeded.  Returns the arrival number (1 .. S), or 0 if the
+// bounded loop gave up (flagged).
+__device__ __forceinline__ unsigned take_ticket(const Params& p, unsigned long long* c) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(c);
+  for (int it = 0; it < (1 << 20); ++it) {
+    const unsigned long long want =
+        ((unsigned)(cur >> 32) == p.epoch) ? cur + 1ull
+                                           : (((unsigned long long)p.epoch << 32) | 1ull);
+    const unsigned long long prev = atomicCAS(c, cur, want);
+    if (prev == cur) return (unsigned)(want & 0xffffffffull);
+    cur = prev;
+  }
+  atomicOr(p.flags, kDevFlagTimeout);
+  return 0u;
+}
+
+// Called by the NCW * 32 consumer threads of a CTA after it has written its partials
+// (or its empty-split LSE).  `flag` is a shared-memory word.
+template <int D, int NCW>
+__device__ __forceinline__ void arrive_and_merge(const Params& p, const SplitInfo& si, int ctid,
+                                                 int32_t* flag) {
+  unsigned long long* c = &p.counters[(int64_t)si.b * p.Hkv + si.g];
+  __threadfence();                                   // this thread's partial writes first
+  named_bar_sync(1, NCW * 32);
+  if (ctid == 0) *flag = take_ticket(p, c) == (unsigned)p.S ? 1 : 0;
+  named_bar_sync(1, NCW * 32);
+  if (*flag == 0) return;
+  __threadfence();                                   // then everyone else's
+  merge_group<D, NCW>(p, si.b, si.g, ctid);
+  if (ctid == 0) *c = 0ull;                          // clean for a replay of this launch
 }
 
 }  // namespace fd

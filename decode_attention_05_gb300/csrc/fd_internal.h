@@ -35,10 +35,15 @@ struct Params {
   int64_t bt_sb;                // batch stride of the block table (elements)
   int32_t page_size;            // tokens per page (paged), else 0
   int32_t log2_page;            // log2(page_size)
+  int32_t log2_box;             // log2(rows of one TMA box): the tile, or a page if shorter
   int32_t max_pages;            // block table width
   int64_t num_pages;            // pages in the pool
   // workspace
   uint32_t* flags;        // device error flags (workspace header)
+  unsigned long long* counters;   // [B, Hkv] (epoch << 32 | arrivals) per (b, kv head) for
+                                  // the fused merge, or nullptr: the partial pass then
+                                  // leaves the merge to a separate kernel
+  uint32_t epoch;                 // this call's ticket epoch (never 0)
   float* lse_part;        // [B, Hq, S]     natural-log LSE_i, -inf for an empty split
   float* o_part;          // [B, Hq, S, d]  normalised partial output O_i
   // outputs

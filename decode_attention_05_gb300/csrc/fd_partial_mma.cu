@@ -89,17 +89,18 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
                           const __grid_constant__ Params p) {
   constexpr int G = SH::G, NT = SH::NT, TT = SH::TT, STAGES = SH::STAGES;
   const SplitInfo si = split_info<TT>(p);
-  if (si.n_tiles == 0) {            // empty split: weight 0 in the merge, nothing to load
-    write_empty_split(p, si, threadIdx.x);
-    pdl_trigger();
-    return;
-  }
-
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   auto* ctl = reinterpret_cast<PipeCtl<STAGES>*>(stages + (size_t)STAGES * 2 * kTileBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (si.n_tiles == 0) {            // empty split: weight 0 in the merge, nothing to load
+    write_empty_split(p, si, threadIdx.x);
+    pdl_trigger();
+    if (p.counters != nullptr && warp < SH::NCW)
+      arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   const int ps = p.page_size;
   const bool multi_page = ps > 0 && ps < TT;
   const float sl2 = p.scale_log2;
+  const uint32_t lb = (uint32_t)p.log2_box;
   bool aborted = false;
 
   // ldmatrix row addresses: lane i serves matrix i / 8, row i % 8.
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
         const bool valid = tok >= si.lo && tok < si.hi && !((bad >> pslot) & 1u);
         if (!valid) {
           for (int c = lane; c < SH::ROW_BYTES / 16; c += 32)
-            *reinterpret_cast<uint4*>(vt + row * SH::ROW_BYTES + c * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vt + tile_chunk<SH::LINES>(row, c, lb)) = make_uint4(0, 0, 0, 0);
         }
       }
       // These generic-proxy stores must be ordered before the next TMA write of the stage.
@@ -211,9 +213,8 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
 #pragma unroll
       for (int kk = 0; kk < SH::KSTEPS; ++kk) {
         const int c16 = kk * 2 + (lm >> 1);           // 16-byte chunk of the row
-        const uint32_t X = (uint32_t)arow * SH::LINES + (c16 >> 3);
         uint32_t a[4];
-        ldsm_x4(smem_addr(kt) + swz128(X, c16 & 7), a);
+        ldsm_x4(smem_addr(kt) + tile_chunk<SH::LINES>(arow, c16, lb), a);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_bf16(s[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
       }
@@ -274,9 +275,8 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
 #pragma unroll
       for (int mt = 0; mt < SH::MTILES; ++mt) {
         const int c16 = mt * 2 + (lm & 1);
-        const uint32_t X = (uint32_t)vrow_addr * SH::LINES + (c16 >> 3);
         uint32_t a[4];
-        ldsm_x4_trans(smem_addr(vt) + swz128(X, c16 & 7), a);
+        ldsm_x4_trans(smem_addr(vt) + tile_chunk<SH::LINES>(vrow_addr, c16, lb), a);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[nt][mt], a, pb[nt][0], pb[nt][1]);
       }
@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   named_bar_sync(1, SH::NCW * 32);
   if (aborted || *reinterpret_cast<volatile int32_t*>(&ctl->abort)) {
     if (warp == 0) write_empty_split(p, si, threadIdx.x);
+    if (p.counters != nullptr) arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
     return;
   }
 
@@ -323,6 +324,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   }
   named_bar_sync(1, SH::NCW * 32);
   merge_warps_and_store<G, SH::D, SH::NCW>(p, si, macc, mm, ml, threadIdx.x);
+  if (p.counters != nullptr) arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
 }
 
 template <class SH>

@@ -56,11 +56,10 @@ struct SimtShape {
 
 // Load this lane's EPL elements of token row r from a swizzled tile, widened to f32.
 template <class SH>
-__device__ __forceinline__ void load_row_slice(const uint8_t* tile, int r, int li,
+__device__ __forceinline__ void load_row_slice(const uint8_t* tile, int r, int li, uint32_t lb,
                                                float (&f)[SH::EPL]) {
   const int off = li * SH::BPL;                               // byte offset in the row
-  const uint32_t X = (uint32_t)r * SH::LINES + (off >> 7);    // 128-byte line index
-  const uint32_t a = swz128(X, (off >> 4) & 7) + (off & 15);
+  const uint32_t a = tile_chunk<SH::LINES>((uint32_t)r, (uint32_t)(off >> 4), lb) + (off & 15);
   if constexpr (SH::BPL == 16) {
     const uint4 u = *reinterpret_cast<const uint4*>(tile + a);
     if constexpr (SH::ESZ == 2) {
@@ -101,17 +100,18 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   constexpr int G = SH::G, EPL = SH::EPL, LPR = SH::LPR, RPW = SH::RPW, TT = SH::TT;
   constexpr int STAGES = SH::STAGES;
   const SplitInfo si = split_info<TT>(p);
-  if (si.n_tiles == 0) {            // empty split: weight 0 in the merge, nothing to load
-    write_empty_split(p, si, threadIdx.x);
-    pdl_trigger();
-    return;
-  }
-
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   auto* ctl = reinterpret_cast<PipeCtl<STAGES>*>(stages + (size_t)STAGES * 2 * kTileBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (si.n_tiles == 0) {            // empty split: weight 0 in the merge, nothing to load
+    write_empty_split(p, si, threadIdx.x);
+    pdl_trigger();
+    if (p.counters != nullptr && warp < SH::NCW)
+      arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   }
   const int ps = p.page_size;
   const bool multi_page = ps > 0 && ps < TT;
+  const uint32_t lb = (uint32_t)p.log2_box;
   bool aborted = false;
 
   for (int n = 0; n < si.n_tiles; ++n) {
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
         const int pslot = multi_page ? (r >> p.log2_page) : 0;
         valid[st] = tok >= si.lo && tok < si.hi && !((bad >> pslot) & 1u);
         float kf[EPL];
-        load_row_slice<SH>(kt, r, li, kf);
+        load_row_slice<SH>(kt, r, li, lb, kf);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           float a = 0.f;
@@ -233,7 +234,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
       for (int st = 0; st < SH::SB; ++st) {
         const int r = warp * SH::ROWS_PER_WARP + (sb + st) * RPW + rg;
         float vf[EPL];
-        load_row_slice<SH>(vt, r, li, vf);
+        load_row_slice<SH>(vt, r, li, lb, vf);
 #pragma unroll
         for (int e = 0; e < EPL; ++e) vf[e] = valid[st] ? vf[e] : 0.f;   // stale rows may be NaN
 #pragma unroll
@@ -254,6 +255,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   named_bar_sync(1, SH::NCW * 32);
   if (aborted || *reinterpret_cast<volatile int32_t*>(&ctl->abort)) {
     if (warp == 0) write_empty_split(p, si, threadIdx.x);
+    if (p.counters != nullptr) arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
     return;
   }
 
@@ -286,6 +288,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   }
   named_bar_sync(1, SH::NCW * 32);
   merge_warps_and_store<G, SH::D, SH::NCW>(p, si, macc, mm, ml, threadIdx.x);
+  if (p.counters != nullptr) arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
 }
 
 }  // namespace fd

@@ -57,12 +57,16 @@ struct PipeCtl {
   uint64_t empty[STAGES];   // consumers released the stage (count = consumer warps)
   uint32_t bad[STAGES];     // bit j: page slot j of the tile had an invalid page id
   int32_t abort;            // a bounded wait gave up
+  int32_t last;             // this CTA drew its group's last ticket (fused merge)
 };
 
 // Producer warp: streams tiles 0..n_tiles-1 of the split.  All 32 lanes run the loop
 // (they share the page-id cache); lane 0 issues the copies.
 //   stages: base of STAGES * 2 * kTileBytes bytes, 1024-byte aligned; stage s holds the
-//           K tile at s * 2 * kTileBytes and the V tile kTileBytes after it.
+//           K tile at s * 2 * kTileBytes and the V tile kTileBytes after it.  A tile is
+//           one TMA box (contiguous cache, or pages of at least a tile) or one box per
+//           page; each box is laid out [line][row][128 B] (see tile_chunk), 128-byte
+//           swizzled, and 1024-byte aligned (a box is at least 8 rows).
 template <int TT, int STAGES>
 __device__ __forceinline__ void produce_tiles(const Params& p, const SplitInfo& si,
                                               const CUtensorMap* tk, const CUtensorMap* tv,
@@ -73,7 +77,7 @@ __device__ __forceinline__ void produce_tiles(const Params& p, const SplitInfo& 
   const int ps = p.page_size;
   const int pages_per_tile = paged ? (ps >= TT ? 1 : TT / ps) : 1;
   const int box_rows = paged ? (ps >= TT ? TT : ps) : TT;
-  const uint32_t box_bytes = (uint32_t)(kTileBytes / TT) * box_rows;
+  const uint32_t box_bytes = (uint32_t)(kTileBytes / TT) * box_rows;   // all lines of a box
   // Page-id cache: lane i holds the table entry of page (cache_base + i), or -2 when
   // that page holds no token of the row (never read from the table).
   int64_t cache_base = -64;      // no window loaded yet
@@ -124,13 +128,14 @@ __device__ __forceinline__ void produce_tiles(const Params& p, const SplitInfo& 
       mbar_arrive_expect_tx(full, 2u * kTileBytes);
       const uint32_t dk = smem_addr(stages + (size_t)stage * 2 * kTileBytes);
       const uint32_t dv = dk + kTileBytes;
+      // Coordinates: {element 0, token row, line 0, kv head, batch row | page}.
       if (!paged) {
-        tma_load_5d(dk, tk, full, 0, 0, (int)t0, si.g, si.b, pol);
-        tma_load_5d(dv, tv, full, 0, 0, (int)t0, si.g, si.b, pol);
+        tma_load_5d(dk, tk, full, 0, (int)t0, 0, si.g, si.b, pol);
+        tma_load_5d(dv, tv, full, 0, (int)t0, 0, si.g, si.b, pol);
       } else if (ps >= TT) {
         const int slot = (int)(t0 & (ps - 1));
-        tma_load_5d(dk, tk, full, 0, 0, slot, si.g, pid[0], pol);
-        tma_load_5d(dv, tv, full, 0, 0, slot, si.g, pid[0], pol);
+        tma_load_5d(dk, tk, full, 0, slot, 0, si.g, pid[0], pol);
+        tma_load_5d(dv, tv, full, 0, slot, 0, si.g, pid[0], pol);
       } else {
         for (int j = 0; j < pages_per_tile; ++j) {
           tma_load_5d(dk + j * box_bytes, tk, full, 0, 0, 0, si.g, pid[j], pol);

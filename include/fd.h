@@ -16,7 +16,9 @@
  * consecutive grouping), over the keys t < L_b of row b,
  *     out[b,h,:] = softmax_t( q[b,h,:] . k[b,g,t,:] / sqrt(d) ) @ v[b,g,t,:]
  *     lse_out[b,h] = log sum_t exp( q[b,h,:] . k[b,g,t,:] / sqrt(d) )   (natural log)
- * computed as S splits along the KV axis.  Split i covers the logical tokens
+ * computed as S splits along the KV axis, in ONE kernel launch: every CTA writes its
+ * split's partial to the workspace, and the last CTA of each (b, kv head) group to finish
+ * merges that group (a ticket counter; no CTA ever waits on another).  Split i covers the logical tokens
  * [i * split_len, min((i + 1) * split_len, L_b)) with split_len = ceil(L_cap / S); a
  * split starting at or past L_b is EMPTY.  Each non-empty split writes a normalised
  * partial output O_i and LSE_i = m_i + log(l_i) (safe-softmax max m_i, shifted exp-sum
@@ -111,9 +113,10 @@ typedef enum {
  *   lse_out      device f32 [B, Hq] (contiguous), natural log; may be NULL.
  *   workspace    device scratch of at least fd_workspace_size(B, Hq, Hkv, d, S) bytes,
  *                256-byte aligned, zero-filled once before its first use
- *                (fd_workspace_init).  Calls leave its header as they found it,
- *                except for device error flags.  Two calls that are in flight at once
- *                must not share a workspace.
+ *                (fd_workspace_init) so that its device error flags start clear; flags
+ *                stay set until fd_read_device_error clears them.  Nothing else in it
+ *                needs particular contents: one workspace serves calls of any sizes
+ *                that fit it.  Two calls in flight at once must not share a workspace.
  *   stream       cudaStream_t (as void*), NULL = legacy default stream.
  *
  * Supported: d in {64, 128}; G = Hq / Hkv in {1, 2, 4, 8, 16}; (q, k, v) all bf16
@@ -191,8 +194,9 @@ FD_API fd_status fd_decode_attention_noalloc(const fd_tensor* q, const fd_tensor
  * Bytes of workspace a call with these sizes needs: a 256-byte header (device error
  * flags), the per-split LSE_i [B, Hq, S] f32 and partial outputs O_i [B, Hq, S, d] f32
  * ([AI-Infra] 2.6 "Flash-Decoding Split-K": each split writes its local O and one LSE
- * scalar), each region 256-byte aligned.  num_splits must be >= 1 (resolve 0 with
- * fd_num_splits_heuristic first).  Returns 0 for invalid sizes.
+ * scalar), and [B, Hkv] 64-bit ticket counters of the single-launch merge; each region
+ * 256-byte aligned.  num_splits must be >= 1 (resolve 0 with fd_num_splits_heuristic
+ * first).  Returns 0 for invalid sizes.
  */
 FD_API size_t fd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_splits);
 
@@ -200,12 +204,26 @@ FD_API size_t fd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, i
  * Split-count heuristic over batch, heads, head_dim, context and SM count
  * ([Split-avg] "the split count is a cost account": more splits expose more parallel
  * work but add partial results, launches and merge cost, which can outweigh the gain
- * on short contexts; choose by batch, context, head_dim and device).  Returns S >= 1:
- * enough (b, kv head, split) work units to fill every SM about twice, but no split
- * shorter than 256 tokens.  Invalid sizes return 1.
+ * on short contexts; choose by batch, context, head_dim and device).  Plans for full
+ * rows of L_cap tokens: the largest S whose (b, kv head, split) CTAs all fit in one wave
+ * (two per SM), preferring an S whose split_len is a whole number of tiles if that keeps
+ * three quarters of the count; never a split shorter than 256 tokens.  Invalid sizes
+ * return 1.
  */
 FD_API int32_t fd_num_splits_heuristic(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int64_t L_cap,
                                 int32_t num_sms);
+
+/*
+ * Split count for a batch whose row lengths are known on the host (host int32 [B]):
+ * simulates the launch (running CTAs share an HBM bandwidth that grows with their
+ * number up to the device ceiling, plus per-CTA start-up and per-group merge costs) for
+ * candidate counts and returns the fastest.  Ragged batches need it: a heuristic that sees only L_cap cannot tell
+ * that most rows are short ([Split-avg] "the split count is a cost account").  Host
+ * arithmetic only; invalid sizes return 1.
+ */
+FD_API int32_t fd_num_splits_for_lengths(int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+                                         int64_t L_cap, const int32_t* seq_lens,
+                                         int32_t num_sms);
 
 /* Zero-fill a workspace on `stream` (asynchronous).  Needed once before first use. */
 FD_API fd_status fd_workspace_init(void* workspace, size_t workspace_bytes, void* stream);

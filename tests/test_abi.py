@@ -55,37 +55,66 @@ def test_status_strings_and_version():
 
 
 def test_workspace_size_layout():
-    # 256-byte header, then LSE_i [B, Hq, S] f32 and O_i [B, Hq, S, d] f32, each
-    # region rounded up to 256 bytes.
-    def expect(B, Hq, d, S):
-        up = lambda x: (x + 255) // 256 * 256
-        lse_end = 256 + B * Hq * S * 4
-        return up(up(lse_end) + B * Hq * S * d * 4)
+    # 256-byte header, then LSE_i [B, Hq, S] f32, O_i [B, Hq, S, d] f32 and the ticket
+    # counters [B, Hkv] (64-bit) of the single-launch merge, each rounded up to 256 B.
+    up = lambda x: (x + 255) // 256 * 256
+
+    def expect(B, Hq, Hkv, d, S):
+        o_off = up(256 + B * Hq * S * 4)
+        cnt_off = up(o_off + B * Hq * S * d * 4)
+        return up(cnt_off + B * Hkv * 8)
     for B, Hq, Hkv, d, S in [(1, 64, 8, 128, 38), (4, 32, 32, 128, 3), (1, 1, 1, 64, 4),
                              (16, 32, 8, 128, 256), (3, 6, 3, 64, 4096)]:
-        assert fd.workspace_size(B, Hq, Hkv, d, S) == expect(B, Hq, d, S)
+        assert fd.workspace_size(B, Hq, Hkv, d, S) == expect(B, Hq, Hkv, d, S)
     assert fd.workspace_size(1, 1, 1, 64, 0) == 0
     assert fd.workspace_size(1, 1, 1, 64, 4097) == 0
     assert fd.workspace_size(0, 1, 1, 64, 1) == 0
+    # Where the partials live inside a workspace (host arithmetic only).
+    fake = 0x7f0000000000
+    lp, op = ctypes.c_void_p(), ctypes.c_void_p()
+    assert fd.lib().fd_workspace_partials(fake, 1, 64, 128, 38, ctypes.byref(lp),
+                                          ctypes.byref(op)) == 0
+    assert lp.value == fake + 256 and op.value == fake + up(256 + 64 * 38 * 4)
 
 
 def test_heuristic_properties():
     h = fd.num_splits_heuristic
-    # 128K-context GQA on 152 SMs: enough (b, kv head, split) units for two per SM.
-    S = h(1, 64, 8, 128, 131072, 152)
-    assert 8 * S >= 2 * 152 and S <= 4096
-    # Splits never shorter than 256 tokens: short contexts get few splits.
-    assert h(1, 32, 8, 128, 300, 152) == 2
+    # Full rows of 128K tokens, 8 (b, kv head) pairs, 152 SMs: one wave of at most two
+    # CTAs per SM (S <= 38), and split_len a whole number of 64-token tiles -> 32.
+    assert h(1, 64, 8, 128, 131072, 152) == 32
+    assert h(4, 32, 32, 128, 4096, 152) == 2           # 128 pairs: two splits fit a wave
+    assert h(8, 32, 8, 128, 16384, 152) == 4
+    # Never more CTAs than one wave, never splits shorter than 256 tokens.
+    for B, Hkv, L in [(1, 8, 131072), (1, 1, 1 << 20), (3, 4, 5000), (2, 8, 300)]:
+        S = h(B, 4 * Hkv, Hkv, 128, L, 152)
+        assert B * Hkv * S <= 2 * 152 or S == 1
+        assert S == 1 or -(-L // S) >= 64
     assert h(1, 32, 8, 128, 256, 152) == 1
-    # Enough batch x heads already fills the GPU: one split.
+    # Enough (b, kv head) pairs already fill the GPU: one split.
     assert h(64, 32, 32, 128, 4096, 152) == 1
-    # More SMs -> at least as many splits; longer contexts never fewer.
+    # More SMs -> at least as many splits.
     for L in (1024, 8192, 65536, 1 << 20):
         assert h(1, 64, 8, 128, L, 304) >= h(1, 64, 8, 128, L, 152)
-        assert h(1, 64, 8, 128, 2 * L, 152) >= h(1, 64, 8, 128, L, 152)
     # Invalid sizes fall back to one split.
     assert h(0, 64, 8, 128, 1000, 152) == 1
     assert h(1, 64, 8, 128, 1000, 0) == 1
+
+
+def test_length_aware_planner():
+    import workloads
+    f = fd.num_splits_for_lengths
+    # A ragged batch whose capacity is 32K but most rows are far shorter: the planner
+    # splits more than the capacity-only heuristic would.
+    lens = workloads.config4_lens()
+    S = f(16, 32, 8, 128, 32768, lens, 152)
+    assert S > fd.num_splits_heuristic(16, 32, 8, 128, 32768, 152)
+    assert S == f(16, 32, 8, 128, 32768, lens, 152)             # deterministic
+    # Full rows: a single-wave split count, as the capacity-only heuristic plans.
+    S3 = f(1, 64, 8, 128, 131072, [131072], 152)
+    assert 8 * S3 <= 2 * 152 and S3 >= 16
+    # Nothing to read, or invalid sizes: one split.
+    assert f(4, 8, 8, 128, 4096, [0, 0, 0, 0], 152) == 1
+    assert f(0, 8, 8, 128, 4096, [], 152) == 1
 
 
 def test_path_setting_round_trip():

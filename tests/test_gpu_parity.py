@@ -112,11 +112,10 @@ def test_worked_example(dtype):
         tol = 1e-5 if dtype == "f32" else 4e-3 + 8e-3 * exact
         assert np.abs(o[0, 0] - exact).max() <= tol
         assert abs(l[0, 0] - math.log(2.0 + math.exp(10.0))) <= 1e-4
-        # Workspace layout: 256-byte header, LSE_i [B, Hq, S], then O_i [B, Hq, S, d].
-        raw = ws.cpu().numpy()
-        lse_parts = raw[256:256 + 2 * 4].view(np.float32)
-        o_off = (256 + 2 * 4 + 255) // 256 * 256
-        o_parts = raw[o_off:o_off + 2 * 64 * 4].view(np.float32).reshape(2, 64)
+        # The per-split partials the step left in its workspace.
+        lp, op = fd.workspace_partials(ws, 1, 1, 64, 2)
+        lse_parts = lp.cpu().numpy().reshape(2)
+        o_parts = op.cpu().numpy().reshape(2, 64)
         assert abs(lse_parts[0] - math.log(2.0)) < 1e-5 and abs(lse_parts[1] - 10.0) < 1e-5
         assert np.abs(o_parts[0]).max() < 1e-6 and np.abs(o_parts[1] - 9.0).max() < 1e-5
         naive = o_parts.mean(axis=0)
@@ -150,15 +149,19 @@ def test_config3_gqa_128k(name, path):
     w, wd = cached(3)
     ref_o, ref_l = ref_for(w, "c3")
     o, l, _, S = run(w, path=path, wd=wd)     # heuristic split count, as bench.py runs it
-    assert 8 * S >= 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert S == fd.num_splits_heuristic(1, 64, 8, 128, 131072, sms) and S > 1
     check(w, o, l, ref_o, ref_l)
 
 
 @pytest.mark.parametrize("name,path", PATHS_BF16)
-@pytest.mark.parametrize("S", [0, 7, 64])
+@pytest.mark.parametrize("S", [0, -1, 7, 64])
 def test_config4_ragged_paged(name, path, S):
     w, wd = cached(4)
     ref_o, ref_l = ref_for(w, "c4")
+    if S == -1:                                 # the length-aware planner's choice
+        S = fd.num_splits_for_lengths(w.B, w.Hq, w.Hkv, w.d, w.L_cap, w.seq_lens,
+                                      torch.cuda.get_device_properties(0).multi_processor_count)
     o, l, _, S_res = run(w, num_splits=S, path=path, wd=wd)
     check(w, o, l, ref_o, ref_l)
     # Row 1 (37 tokens) is shorter than one split: all its other splits are empty.
@@ -331,3 +334,65 @@ def test_side_stream_and_events():
                                    out_dtype=torch.float32)
     s.synchronize()
     check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
+
+
+@pytest.mark.parametrize("name,path", PATHS_BF16)
+def test_single_launch_equals_two_pass(name, path):
+    """fd_decode_attention (partials + in-kernel merge by the last CTA of each group)
+    against fd_decode_partial followed by fd_merge_partials (separate merge kernel)."""
+    w = workloads.paged_case(5, 32, 8, 128, 16, 256, [4096, 1, 0, 2500, 77], seed=51,
+                             out_dtype=torch.float32)
+    ref_o, ref_l = ref_for(w)
+    wd = w.to("cuda")
+    fd.set_path(path)
+    for S in (1, 6, 40, 64):
+        ws = torch.zeros(fd.workspace_size(5, 32, 8, 128, S), dtype=torch.uint8, device="cuda")
+        o1, l1 = fd.decode_attention(wd.q, wd.k, wd.v, wd.seq_lens, wd.block_table, 16, S,
+                                     workspace=ws, out_dtype=torch.float32)
+        fd.decode_partial(wd.q, wd.k, wd.v, wd.seq_lens, ws, wd.block_table, 16, S)
+        lp, op = fd.workspace_partials(ws, 5, 32, 128, S)
+        o2, l2 = fd.merge_partials(lp, op, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        check(w, o1.cpu().double().numpy(), l1.cpu().double().numpy(), ref_o, ref_l)
+        check(w, o2.cpu().double().numpy(), l2.cpu().double().numpy(), ref_o, ref_l)
+        assert torch.allclose(o1, o2, atol=2e-6, rtol=1e-5)
+
+
+@pytest.mark.parametrize("name,path", PATHS_BF16)
+def test_workspace_reuse_across_calls(name, path):
+    """One workspace, many calls with different inputs and split counts (so the merge
+    tickets move around inside it): every call must still merge exactly once."""
+    fd.set_path(path)
+    cases = [workloads.contiguous_case(3, 16, 4, 128, 2000, [2000, 5, 999], seed=61 + i,
+                                       out_dtype=torch.float32) for i in range(3)]
+    refs = [ref_for(w) for w in cases]
+    ws = torch.zeros(fd.workspace_size(3, 16, 4, 128, 64), dtype=torch.uint8, device="cuda")
+    for rep in range(3):
+        for (w, (ro, rl)), S in zip(zip(cases, refs), (64, 7, 1)):
+            wd = w.to("cuda")
+            o, l = fd.decode_attention(wd.q, wd.k, wd.v, wd.seq_lens, num_splits=S,
+                                       workspace=ws, out_dtype=torch.float32)
+            torch.cuda.synchronize()
+            check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ro, rl)
+    assert fd.read_device_error(ws) == 0
+
+
+@pytest.mark.parametrize("name,path", PATHS_BF16)
+def test_workspace_with_stale_contents(name, path):
+    """Apart from its flag header, a workspace may hold anything (left by calls of other
+    sizes): the merge tickets of each call start from a fresh epoch."""
+    fd.set_path(path)
+    w = workloads.contiguous_case(2, 16, 2, 128, 3000, [3000, 1500], seed=71,
+                                  out_dtype=torch.float32)
+    ref_o, ref_l = ref_for(w)
+    wd = w.to("cuda")
+    n = fd.workspace_size(2, 16, 2, 128, 48)
+    g = torch.Generator(device="cuda").manual_seed(3)
+    ws = torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda", generator=g)
+    ws[:256] = 0
+    for S in (48, 5):
+        o, l = fd.decode_attention(wd.q, wd.k, wd.v, wd.seq_lens, num_splits=S, workspace=ws,
+                                   out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
+    assert fd.read_device_error(ws) == 0
