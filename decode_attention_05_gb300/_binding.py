@@ -14,6 +14,7 @@ FD_OK = 0
 FD_ERR_DEVICE_FLAG = 5
 FD_F32, FD_BF16, FD_I32 = 0, 1, 2
 FD_PATH_AUTO, FD_PATH_SIMT, FD_PATH_MMA = 0, 1, 2
+FD_MERGE_KERNEL, FD_MERGE_IN_KERNEL = 0, 1
 
 _STATUS = {0: "FD_OK", 1: "FD_ERR_INVALID_ARG", 2: "FD_ERR_UNSUPPORTED",
            3: "FD_ERR_WORKSPACE_TOO_SMALL", 4: "FD_ERR_CUDA", 5: "FD_ERR_DEVICE_FLAG"}
@@ -75,7 +76,7 @@ def _declare(L):
     L.fd_num_splits_heuristic.restype = i32
     L.fd_num_splits_heuristic.argtypes = [i32, i32, i32, i32, i64, i32]
     L.fd_num_splits_for_lengths.restype = i32
-    L.fd_num_splits_for_lengths.argtypes = [i32, i32, i32, i32, i64, vp, i32]
+    L.fd_num_splits_for_lengths.argtypes = [i32, i32, i32, i32, i64, vp, i32, i32]
     L.fd_resolve_num_splits.restype = i32
     L.fd_resolve_num_splits.argtypes = [i32, i32, i32, i32, i64, i32]
     L.fd_workspace_init.restype = ctypes.c_int
@@ -98,6 +99,10 @@ def _declare(L):
     L.fd_plan_destroy.argtypes = [vp]
     L.fd_set_path.restype = ctypes.c_int
     L.fd_set_path.argtypes = [i32]
+    L.fd_set_merge_mode.restype = ctypes.c_int
+    L.fd_set_merge_mode.argtypes = [i32]
+    L.fd_get_merge_mode.restype = i32
+    L.fd_get_merge_mode.argtypes = []
     L.fd_get_path.restype = i32
     L.fd_get_path.argtypes = []
     L.fd_status_string.restype = ctypes.c_char_p
@@ -154,12 +159,13 @@ def num_splits_heuristic(B: int, Hq: int, Hkv: int, d: int, L_cap: int, num_sms:
 
 
 def num_splits_for_lengths(B: int, Hq: int, Hkv: int, d: int, L_cap: int, seq_lens,
-                           num_sms: int) -> int:
+                           num_sms: int, page_size: int = 0) -> int:
     """fd_num_splits_for_lengths over host lengths (a CPU int32 tensor or a sequence)."""
     lens = torch.as_tensor(seq_lens, dtype=torch.int32).cpu().contiguous()
     if lens.numel() != B:
         raise ValueError("need one length per batch row")
-    return int(lib().fd_num_splits_for_lengths(B, Hq, Hkv, d, L_cap, lens.data_ptr(), num_sms))
+    return int(lib().fd_num_splits_for_lengths(B, Hq, Hkv, d, L_cap, lens.data_ptr(), page_size,
+                                               num_sms))
 
 
 def resolve_num_splits(B: int, Hq: int, Hkv: int, d: int, L_cap: int, num_splits: int) -> int:
@@ -172,6 +178,14 @@ def set_path(path: int):
 
 def get_path() -> int:
     return int(lib().fd_get_path())
+
+
+def set_merge_mode(mode: int):
+    _check(lib().fd_set_merge_mode(mode))
+
+
+def get_merge_mode() -> int:
+    return int(lib().fd_get_merge_mode())
 
 
 def workspace_init(ws: torch.Tensor, stream=None):

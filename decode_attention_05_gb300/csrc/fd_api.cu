@@ -19,6 +19,7 @@ namespace {
 
 thread_local char g_last_error[512] = "";
 std::atomic<int> g_path{FD_PATH_AUTO};
+std::atomic<int> g_merge{FD_MERGE_KERNEL};
 std::atomic<uint32_t> g_epoch{0x5eed0001u};   // per-call ticket epochs of the fused merge
 
 fd_status fail(fd_status st, const char* fmt, ...) {
@@ -199,6 +200,15 @@ fd_status fd_set_path(int32_t path) {
 }
 
 int32_t fd_get_path(void) { return g_path.load(); }
+
+fd_status fd_set_merge_mode(int32_t mode) {
+  if (mode != FD_MERGE_KERNEL && mode != FD_MERGE_IN_KERNEL)
+    return fail(FD_ERR_INVALID_ARG, "unknown merge mode %d", mode);
+  g_merge.store(mode);
+  return FD_OK;
+}
+
+int32_t fd_get_merge_mode(void) { return g_merge.load(); }
 
 size_t fd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_splits) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || num_splits <= 0 || num_splits > kMaxSplits)
@@ -423,8 +433,14 @@ fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
   fd_status st = prepare(q, k_cache, v_cache, seq_lens, block_table, page_size, num_splits, out,
                          lse_out, workspace, workspace_bytes, true, &pr);
   if (st != FD_OK) return st;
-  // One launch: the last CTA of each (b, kv head) group merges the group's splits.
-  return launch_partial(pr, (cudaStream_t)stream);
+  // FD_MERGE_IN_KERNEL: one launch, the last CTA of each (b, kv head) group merges it.
+  // FD_MERGE_KERNEL (default): the merge is its own kernel over (b, query head) rows,
+  // launched with programmatic dependent launch behind the partial pass.
+  if (g_merge.load() == FD_MERGE_IN_KERNEL) return launch_partial(pr, (cudaStream_t)stream);
+  pr.p.counters = nullptr;
+  st = launch_partial(pr, (cudaStream_t)stream);
+  if (st != FD_OK) return st;
+  return launch_merge(pr.p, (cudaStream_t)stream);
 }
 
 fd_status fd_decode_partial(const fd_tensor* q, const fd_tensor* k_cache,

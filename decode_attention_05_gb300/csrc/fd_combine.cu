@@ -3,11 +3,13 @@
 // Reads the S partials (O_i, LSE_i) of its row and computes
 //   M = max over non-empty splits of LSE_i,   w_i = exp(LSE_i - M)  in (0, 1],
 //   out = sum_i w_i O_i / sum_i w_i,          lse_out = M + log(sum_i w_i)
+// in one pass: the splits are folded with a running maximum (when M grows, what was
+// summed so far is rescaled by exp(M_old - M_new)), so no load waits for a maximum.
 // ("FlashDecoding interview notes" (gtnt.cn/news/53829), section three, point 2: the
 // weights use LSE_i - LSE_global <= 0, so no exponent can overflow; "2kiu.com/news/
 // 6053916", section "weight block results with log-sum-exp": a softmax over the block
 // LSEs weights the block outputs).  An empty split (LSE_i = -inf) has weight 0 and its
-// O_i is never read: it is not a zero-output block with a normal weight.  A row whose
+// O_i never enters the sum: it is not a zero-output block with a normal weight.  A row whose
 // splits are all empty gets out = 0 and lse_out = -inf.
 //
 // Launched with programmatic dependent launch: the CTA waits (griddepcontrol.wait) for
@@ -21,61 +23,85 @@ namespace fd {
 template <int D>
 __global__ void __launch_bounds__(128) fd_combine_kernel(const __grid_constant__ Params p) {
   constexpr int VEC = D / 32;                  // dims per lane: 4 (d=128) or 2 (d=64)
+  constexpr int BATCH = 8;                     // splits whose loads are in flight at once
   constexpr float kLog2e = 1.4426950408889634f;
   constexpr float kLn2 = 0.6931471805599453f;
-  __shared__ float red[4];
-  __shared__ float sw[4];
+  __shared__ float wm[4], ww[4];
   __shared__ __align__(16) float accs[4][D];
   pdl_wait();
 
   const int row = blockIdx.x;                  // b * Hq + h
   const int S = p.S;
   const float* lse = p.lse_part + (int64_t)row * S;
+  const float* ob = p.o_part + (int64_t)row * S * D + (threadIdx.x & 31) * VEC;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  float mx = kNegInf;
-  for (int s = tid; s < S; s += 128) mx = fmaxf(mx, lse[s]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  if (lane == 0) red[warp] = mx;
-  __syncthreads();
-  const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-
-  float acc[VEC];
+  // Warp w folds splits w, w + 4, w + 8, ... with a running maximum (base-2 units): a
+  // batch's loads are all issued before any of them is used.
+  float M = kNegInf, W = 0.f, acc[VEC];
 #pragma unroll
   for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  if (M != kNegInf) {
-    const float* ob = p.o_part + (int64_t)row * S * D + lane * VEC;
-#pragma unroll 4
-    for (int s = warp; s < S; s += 4) {
-      const float ls = lse[s];
-      if (ls == kNegInf) continue;             // empty split: weight 0, O_i never read
-      const float w = ex2((ls - M) * kLog2e);
-      wsum += w;
+  for (int s0 = warp; s0 < S; s0 += 4 * BATCH) {
+    float ls[BATCH], v[BATCH][VEC];
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int s = s0 + 4 * u;
+      const bool in = s < S;
+      ls[u] = in ? lse[s] * kLog2e : kNegInf;
       if constexpr (VEC == 4) {
-        const float4 o = *reinterpret_cast<const float4*>(ob + (int64_t)s * D);
-        acc[0] = fmaf(w, o.x, acc[0]);
-        acc[1] = fmaf(w, o.y, acc[1]);
-        acc[2] = fmaf(w, o.z, acc[2]);
-        acc[3] = fmaf(w, o.w, acc[3]);
+        const float4 t = in ? *reinterpret_cast<const float4*>(ob + (int64_t)s * D)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
       } else {
-        const float2 o = *reinterpret_cast<const float2*>(ob + (int64_t)s * D);
-        acc[0] = fmaf(w, o.x, acc[0]);
-        acc[1] = fmaf(w, o.y, acc[1]);
+        const float2 t = in ? *reinterpret_cast<const float2*>(ob + (int64_t)s * D)
+                            : make_float2(0.f, 0.f);
+        v[u][0] = t.x; v[u][1] = t.y;
       }
     }
+    float mb = ls[0];
+#pragma unroll
+    for (int u = 1; u < BATCH; ++u) mb = fmaxf(mb, ls[u]);
+    const float mn = fmaxf(M, mb);
+    if (mn == kNegInf) continue;               // only empty splits so far
+    const float c = (M == kNegInf) ? 0.f : ex2(M - mn);
+    W *= c;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] *= c;
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      // An empty split (LSE = -inf) has weight 0 and its O_i is selected away, never
+      // multiplied: that memory was not written by this call.
+      const bool live = ls[u] != kNegInf;
+      const float w = live ? ex2(ls[u] - mn) : 0.f;
+      W += w;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w, live ? v[u][e] : 0.f, acc[e]);
+    }
+    M = mn;
   }
 #pragma unroll
   for (int e = 0; e < VEC; ++e) accs[warp][lane * VEC + e] = acc[e];
-  if (lane == 0) sw[warp] = wsum;
+  if (lane == 0) {
+    wm[warp] = M;
+    ww[warp] = W;
+  }
   __syncthreads();
 
+  // Merge the four warps' states with the same rule.
+  const float Mt = fmaxf(fmaxf(wm[0], wm[1]), fmaxf(wm[2], wm[3]));
+  float cw[4], Wt = 0.f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    cw[w] = (wm[w] == kNegInf) ? 0.f : ex2(wm[w] - Mt);
+    Wt = fmaf(ww[w], cw[w], Wt);
+  }
   const int b = row / p.Hq, h = row % p.Hq;
-  const float W = sw[0] + sw[1] + sw[2] + sw[3];
   for (int j = tid; j < D; j += 128) {
     float o = 0.f;
-    if (W > 0.f) o = (accs[0][j] + accs[1][j] + accs[2][j] + accs[3][j]) / W;
+    if (Wt > 0.f) {
+      o = accs[0][j] * cw[0] + accs[1][j] * cw[1] + accs[2][j] * cw[2] + accs[3][j] * cw[3];
+      o /= Wt;
+    }
     const int64_t off = (int64_t)b * p.out_sb + (int64_t)h * p.out_sh + j;
     if (p.out_bf16) {
       reinterpret_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(o);
@@ -85,8 +111,8 @@ __global__ void __launch_bounds__(128) fd_combine_kernel(const __grid_constant__
   }
   if (tid == 0 && p.lse_out != nullptr) {
     float lg;
-    asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(W));
-    p.lse_out[row] = (W > 0.f) ? M + lg * kLn2 : kNegInf;
+    asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(Wt));
+    p.lse_out[row] = (Wt > 0.f) ? (Mt + lg) * kLn2 : kNegInf;
   }
 }
 

@@ -72,8 +72,9 @@ __device__ __forceinline__ void merge_warps_and_store(const Params& p, const Spl
 // Single-launch decode: every CTA of a (b, kv head) group -- empty splits included --
 // publishes its partials, then takes a ticket on the group's counter; the CTA that
 // draws the last ticket merges the group's G query heads.  No CTA ever waits for
-// another: the last to arrive finds every partial already visible (writers fence, then
-// take their ticket; the last reader fences after it), so there is no second kernel and
+// another: the last to arrive finds every partial already visible (each CTA fences
+// once, after a barrier, before its ticket; the last one fences after it), so there is
+// no second kernel and
 // no grid-wide dependency ("2kiu.com/news/6053916", section "the split count is a cost
 // account": the merge may start only when every partial it needs is visible).
 //
@@ -177,12 +178,17 @@ template <int D, int NCW>
 __device__ __forceinline__ void arrive_and_merge(const Params& p, const SplitInfo& si, int ctid,
                                                  int32_t* flag) {
   unsigned long long* c = &p.counters[(int64_t)si.b * p.Hkv + si.g];
-  __threadfence();                                   // this thread's partial writes first
+  // The barrier makes every consumer thread's partial writes visible to thread 0; its
+  // gpu-scope fence then publishes them (cumulatively) before its ticket.
   named_bar_sync(1, NCW * 32);
-  if (ctid == 0) *flag = take_ticket(p, c) == (unsigned)p.S ? 1 : 0;
+  if (ctid == 0) {
+    __threadfence();
+    const bool last = take_ticket(p, c) == (unsigned)p.S;
+    if (last) __threadfence();                       // acquire the other CTAs' partials
+    *flag = last ? 1 : 0;
+  }
   named_bar_sync(1, NCW * 32);
   if (*flag == 0) return;
-  __threadfence();                                   // then everyone else's
   merge_group<D, NCW>(p, si.b, si.g, ctid);
   if (ctid == 0) *c = 0ull;                          // clean for a replay of this launch
 }

@@ -37,34 +37,45 @@ constexpr int64_t kMinSplitTokens = 256;
 constexpr int kCtasPerSm = 2;             // residency of the partial kernels
 
 // Model constants, fitted on GB300 to this library's partial kernel: n CTAs streaming
-// at once reach BW(n) = kHbmBytesPerUs * (1 - exp(-n / kSatCtas)) together (measured
-// 1.7, 3.0, 4.7 TB/s at 32, 64, 128 CTAs; ~62 GB/s for one CTA alone; 7.0 TB/s is the
-// read ceiling), shared equally.
+// at once reach BW(n) = kHbmBytesPerUs * (1 - exp(-n / tau)) together, shared equally.
+// Contiguous caches: tau = 113 (measured 1.8, 3.0, 4.7 TB/s at 32, 64, 128 CTAs; one
+// CTA alone ~72 GB/s; 7.0 TB/s is the read ceiling).  Paged caches issue one TMA box
+// per page, so one CTA streams slower (~55 GB/s with pages of a tile or more, ~27 GB/s
+// with 16-token pages) and tau grows in proportion.
 constexpr double kHbmBytesPerUs = 7.0e6;
-constexpr double kSatCtas = 113.0;
+constexpr double kSatCtasContig = 113.0;
+constexpr double kOneCtaContig = 72.5e3;    // bytes per µs
 constexpr double kCtaFixedUs = 2.0;         // start-up + epilogue of one CTA
-constexpr double kMergeBytesPerUs = 1.0e5;  // last-CTA merge reading partials from L2
+constexpr double kMergeBytesPerUs = 1.0e5;  // merging a group's partials from L2
 
-double rate_per_cta(size_t n) {
-  return kHbmBytesPerUs * (1.0 - std::exp(-(double)n / kSatCtas)) / (double)n;
+// One CTA's streaming rate (bytes per µs) for a page size (0 = contiguous cache).
+double one_cta_rate(int page_size, int tile) {
+  if (page_size <= 0) return kOneCtaContig;
+  if (page_size >= tile) return 55.0e3;
+  return std::min(55.0e3, 27.5e3 * page_size / 16.0);
+}
+
+double rate_per_cta(size_t n, double tau) {
+  return kHbmBytesPerUs * (1.0 - std::exp(-(double)n / tau)) / (double)n;
 }
 
 int tile_tokens_bf16(int d) { return 16384 / (d * 2); }
 
 // Simulated duration (µs) of one partial-pass launch.
 //   work[i]  bytes CTA i streams (launch order), fixed[i] its fixed time (µs).
-double simulate(const std::vector<double>& work, const std::vector<double>& fixed, int slots) {
+double simulate(const std::vector<double>& work, const std::vector<double>& fixed, int slots,
+                double tau) {
   // Every running CTA progresses at the same rate, so track the progress P (in bytes;
   // a CTA's fixed time counts as bytes at the one-CTA rate) at which each one finishes.
   std::priority_queue<double, std::vector<double>, std::greater<double>> heap;
   const size_t n = work.size();
-  const double fixed_rate = rate_per_cta(1);
+  const double fixed_rate = rate_per_cta(1, tau);
   size_t next = 0;
   double t = 0.0, P = 0.0;
   auto push = [&](size_t i) { heap.push(P + work[i] + fixed[i] * fixed_rate); };
   while (next < n && (int)heap.size() < slots) push(next++);
   while (!heap.empty()) {
-    const double rate = rate_per_cta(heap.size());
+    const double rate = rate_per_cta(heap.size(), tau);
     const double f = heap.top();
     heap.pop();
     t += (f - P) / rate;
@@ -77,7 +88,7 @@ double simulate(const std::vector<double>& work, const std::vector<double>& fixe
 // Per-CTA work of one split count: bytes each CTA loads (whole tiles, as the kernels
 // do) and its fixed time, in launch order (split fastest, then kv head, then row).
 double plan_time(int B, int Hq, int Hkv, int d, int64_t L_cap, const int32_t* lens, int S,
-                 int slots) {
+                 int slots, int page_size) {
   const int TT = tile_tokens_bf16(d);
   const int64_t split_len = (L_cap + S - 1) / S;
   const double tok_bytes = 2.0 * d * 2.0;          // K and V rows, bf16
@@ -106,7 +117,8 @@ double plan_time(int B, int Hq, int Hkv, int d, int64_t L_cap, const int32_t* le
       if (last >= 0) fixed[last] += merge_us;
     }
   }
-  return simulate(work, fixed, slots);
+  const double tau = kSatCtasContig * kOneCtaContig / one_cta_rate(page_size, TT);
+  return simulate(work, fixed, slots, tau);
 }
 
 }  // namespace
@@ -132,7 +144,7 @@ int32_t fd_num_splits_heuristic(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, i
 }
 
 int32_t fd_num_splits_for_lengths(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int64_t L_cap,
-                                  const int32_t* seq_lens, int32_t num_sms) {
+                                  const int32_t* seq_lens, int32_t page_size, int32_t num_sms) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || L_cap <= 0 || num_sms <= 0 || !seq_lens ||
       Hq % Hkv != 0)
     return 1;
@@ -148,10 +160,10 @@ int32_t fd_num_splits_for_lengths(int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
   for (int S = 288; S <= 1024; S += 32) cand.push_back(S);
   const int64_t S_cap = std::max<int64_t>(1, (L_cap + kMinSplitTokens - 1) / kMinSplitTokens);
   int best_S = 1;
-  double best_t = plan_time(B, Hq, Hkv, d, L_cap, seq_lens, 1, slots);
+  double best_t = plan_time(B, Hq, Hkv, d, L_cap, seq_lens, 1, slots, page_size);
   for (int S : cand) {
     if (S == 1 || S > S_cap || S > kMaxSplits) continue;
-    const double t = plan_time(B, Hq, Hkv, d, L_cap, seq_lens, S, slots);
+    const double t = plan_time(B, Hq, Hkv, d, L_cap, seq_lens, S, slots, page_size);
     if (t < best_t * 0.995) {                 // a smaller count wins near-ties
       best_t = t;
       best_S = S;

@@ -16,17 +16,19 @@
  * consecutive grouping), over the keys t < L_b of row b,
  *     out[b,h,:] = softmax_t( q[b,h,:] . k[b,g,t,:] / sqrt(d) ) @ v[b,g,t,:]
  *     lse_out[b,h] = log sum_t exp( q[b,h,:] . k[b,g,t,:] / sqrt(d) )   (natural log)
- * computed as S splits along the KV axis, in ONE kernel launch: every CTA writes its
- * split's partial to the workspace, and the last CTA of each (b, kv head) group to finish
- * merges that group (a ticket counter; no CTA ever waits on another).  Split i covers the logical tokens
+ * computed as S splits along the KV axis.  Split i covers the logical tokens
  * [i * split_len, min((i + 1) * split_len, L_b)) with split_len = ceil(L_cap / S); a
  * split starting at or past L_b is EMPTY.  Each non-empty split writes a normalised
  * partial output O_i and LSE_i = m_i + log(l_i) (safe-softmax max m_i, shifted exp-sum
  * l_i; [AI-Infra] 2.3, 2.6 "LSE and online softmax").  A second pass merges the splits
  * with weights w_i = exp(LSE_i - max_j LSE_j) ([FD-QA] three.2; [Split-avg] "weight
  * block results with log-sum-exp"); an empty split gets weight 0 and is never read --
- * it is not a zero-output block with a normal weight.  A row with L_b = 0 gets
- * out = 0 and lse_out = -infinity.  Decode needs no causal mask: the single query sits
+ * it is not a zero-output block with a normal weight.  By default the merge is a
+ * second kernel over (b, query head) rows, launched behind the first with programmatic
+ * dependent launch; with fd_set_merge_mode(FD_MERGE_IN_KERNEL) the step is ONE launch:
+ * every CTA writes its split's partial and the last CTA of each (b, kv head) group to
+ * finish merges it (a ticket counter; no CTA ever waits on another).
+ * A row with L_b = 0 gets out = 0 and lse_out = -infinity.  Decode needs no causal mask: the single query sits
  * after every cached key ([AI-Infra] 2.5), so only the length mask t < L_b applies,
  * and stale cache slots at t >= L_b (even NaN) never reach the result.
  *
@@ -214,7 +216,8 @@ FD_API int32_t fd_num_splits_heuristic(int32_t B, int32_t Hq, int32_t Hkv, int32
                                 int32_t num_sms);
 
 /*
- * Split count for a batch whose row lengths are known on the host (host int32 [B]):
+ * Split count for a batch whose row lengths are known on the host (host int32 [B];
+ * page_size 0 for a contiguous cache):
  * simulates the launch (running CTAs share an HBM bandwidth that grows with their
  * number up to the device ceiling, plus per-CTA start-up and per-group merge costs) for
  * candidate counts and returns the fastest.  Ragged batches need it: a heuristic that sees only L_cap cannot tell
@@ -223,7 +226,7 @@ FD_API int32_t fd_num_splits_heuristic(int32_t B, int32_t Hq, int32_t Hkv, int32
  */
 FD_API int32_t fd_num_splits_for_lengths(int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
                                          int64_t L_cap, const int32_t* seq_lens,
-                                         int32_t num_sms);
+                                         int32_t page_size, int32_t num_sms);
 
 /* Zero-fill a workspace on `stream` (asynchronous).  Needed once before first use. */
 FD_API fd_status fd_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
@@ -264,6 +267,16 @@ FD_API fd_status fd_plan_decode(fd_plan* plan, const fd_tensor* q, const fd_tens
 /* Wait for the last decode, then resize workspace and event for a new split count. */
 FD_API fd_status fd_plan_resize(fd_plan* plan, int32_t num_splits);
 FD_API void fd_plan_destroy(fd_plan* plan);
+
+/*
+ * Where fd_decode_attention merges the splits (process-wide, for later calls).
+ * FD_MERGE_KERNEL: a separate merge kernel (default; on GB300 it is as fast or faster,
+ * since it spreads each group's partials over many SMs).  FD_MERGE_IN_KERNEL: a single
+ * launch, the last CTA of each (b, kv head) group merging it.
+ */
+typedef enum { FD_MERGE_KERNEL = 0, FD_MERGE_IN_KERNEL = 1 } fd_merge_mode;
+FD_API fd_status fd_set_merge_mode(int32_t mode);
+FD_API int32_t fd_get_merge_mode(void);
 
 /* Select the partial-pass kernel path for later calls (process-wide). */
 FD_API fd_status fd_set_path(int32_t path);

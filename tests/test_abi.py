@@ -106,15 +106,27 @@ def test_length_aware_planner():
     # A ragged batch whose capacity is 32K but most rows are far shorter: the planner
     # splits more than the capacity-only heuristic would.
     lens = workloads.config4_lens()
-    S = f(16, 32, 8, 128, 32768, lens, 152)
+    S = f(16, 32, 8, 128, 32768, lens, 152, page_size=16)
     assert S > fd.num_splits_heuristic(16, 32, 8, 128, 32768, 152)
-    assert S == f(16, 32, 8, 128, 32768, lens, 152)             # deterministic
+    assert S == f(16, 32, 8, 128, 32768, lens, 152, page_size=16)             # deterministic
     # Full rows: a single-wave split count, as the capacity-only heuristic plans.
     S3 = f(1, 64, 8, 128, 131072, [131072], 152)
     assert 8 * S3 <= 2 * 152 and S3 >= 16
     # Nothing to read, or invalid sizes: one split.
     assert f(4, 8, 8, 128, 4096, [0, 0, 0, 0], 152) == 1
     assert f(0, 8, 8, 128, 4096, [], 152) == 1
+
+
+def test_merge_mode_round_trip():
+    lib = fd.lib()
+    try:
+        assert fd.get_merge_mode() == fd.FD_MERGE_KERNEL          # the default
+        fd.set_merge_mode(fd.FD_MERGE_IN_KERNEL)
+        assert fd.get_merge_mode() == fd.FD_MERGE_IN_KERNEL
+        with pytest.raises(fd.FdError):
+            fd.set_merge_mode(5)
+    finally:
+        lib.fd_set_merge_mode(fd.FD_MERGE_KERNEL)
 
 
 def test_path_setting_round_trip():

@@ -29,6 +29,10 @@ def _restore_path():
     yield
     if torch.cuda.is_available():
         fd.set_path(fd.FD_PATH_AUTO)
+        fd.set_merge_mode(fd.FD_MERGE_KERNEL)
+
+
+MERGES = [("merge-kernel", 0), ("merge-in-kernel", 1)]
 
 
 _ORACLE_CACHE = {}
@@ -161,7 +165,8 @@ def test_config4_ragged_paged(name, path, S):
     ref_o, ref_l = ref_for(w, "c4")
     if S == -1:                                 # the length-aware planner's choice
         S = fd.num_splits_for_lengths(w.B, w.Hq, w.Hkv, w.d, w.L_cap, w.seq_lens,
-                                      torch.cuda.get_device_properties(0).multi_processor_count)
+                                      torch.cuda.get_device_properties(0).multi_processor_count,
+                                      page_size=w.page_size)
     o, l, _, S_res = run(w, num_splits=S, path=path, wd=wd)
     check(w, o, l, ref_o, ref_l)
     # Row 1 (37 tokens) is shorter than one split: all its other splits are empty.
@@ -338,8 +343,9 @@ def test_side_stream_and_events():
 
 @pytest.mark.parametrize("name,path", PATHS_BF16)
 def test_single_launch_equals_two_pass(name, path):
-    """fd_decode_attention (partials + in-kernel merge by the last CTA of each group)
-    against fd_decode_partial followed by fd_merge_partials (separate merge kernel)."""
+    """fd_decode_attention in single-launch mode (partials + in-kernel merge by the last
+    CTA of each group) against fd_decode_partial followed by fd_merge_partials."""
+    fd.set_merge_mode(fd.FD_MERGE_IN_KERNEL)
     w = workloads.paged_case(5, 32, 8, 128, 16, 256, [4096, 1, 0, 2500, 77], seed=51,
                              out_dtype=torch.float32)
     ref_o, ref_l = ref_for(w)
@@ -358,11 +364,13 @@ def test_single_launch_equals_two_pass(name, path):
         assert torch.allclose(o1, o2, atol=2e-6, rtol=1e-5)
 
 
+@pytest.mark.parametrize("merge,mode", MERGES)
 @pytest.mark.parametrize("name,path", PATHS_BF16)
-def test_workspace_reuse_across_calls(name, path):
+def test_workspace_reuse_across_calls(name, path, merge, mode):
     """One workspace, many calls with different inputs and split counts (so the merge
     tickets move around inside it): every call must still merge exactly once."""
     fd.set_path(path)
+    fd.set_merge_mode(mode)
     cases = [workloads.contiguous_case(3, 16, 4, 128, 2000, [2000, 5, 999], seed=61 + i,
                                        out_dtype=torch.float32) for i in range(3)]
     refs = [ref_for(w) for w in cases]
@@ -377,11 +385,13 @@ def test_workspace_reuse_across_calls(name, path):
     assert fd.read_device_error(ws) == 0
 
 
+@pytest.mark.parametrize("merge,mode", MERGES)
 @pytest.mark.parametrize("name,path", PATHS_BF16)
-def test_workspace_with_stale_contents(name, path):
+def test_workspace_with_stale_contents(name, path, merge, mode):
     """Apart from its flag header, a workspace may hold anything (left by calls of other
     sizes): the merge tickets of each call start from a fresh epoch."""
     fd.set_path(path)
+    fd.set_merge_mode(mode)
     w = workloads.contiguous_case(2, 16, 2, 128, 3000, [3000, 1500], seed=71,
                                   out_dtype=torch.float32)
     ref_o, ref_l = ref_for(w)
