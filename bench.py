@@ -70,6 +70,17 @@ def dist_info():
     return world, rank, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The maximum of `value` over all ranks (the job is as slow as its slowest rank);
+    the value itself when there is no process group."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -329,10 +340,7 @@ def run_fd(args):
     barrier()
     ms = e0.elapsed_time(e1)
     clocks = sampler.stop(t_wall0, t_wall1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, device="cuda")
     ms_per_step = ms / args.steps
     value = world * kv_bytes * args.steps / (ms * 1e-3) / 1e9
 
@@ -399,10 +407,7 @@ def run_fd(args):
     e7.record(stream)
     e7.synchronize()
     e2e_ms = e6.elapsed_time(e7) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, device="cuda")
     e2e = {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": round(e2e_ms, 3)}

@@ -406,3 +406,35 @@ def test_workspace_with_stale_contents(name, path, merge, mode):
         torch.cuda.synchronize()
         check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
     assert fd.read_device_error(ws) == 0
+
+
+@pytest.mark.parametrize("name,path", PATHS_BF16)
+def test_sequence_sharded_merge(name, path):
+    """Context parallelism simulated on one GPU: the KV sequence is cut into 4 shards of
+    uneven length (as 4 devices would hold them), each shard's partials come from
+    fd_decode_partial on that shard alone, and fd_merge_partials over all of them equals
+    the unsharded result -- including a row that ends inside shard 2 and has no key at
+    all in shard 3."""
+    fd.set_path(path)
+    w = workloads.contiguous_case(2, 32, 8, 128, 8192, [8192, 5000], seed=81,
+                                  out_dtype=torch.float32)
+    ref_o, ref_l = ref_for(w)
+    wd = w.to("cuda")
+    cuts = [0, 3000, 4096, 6500, 8192]
+    lse_list, o_list = [], []
+    for r in range(4):
+        lo, hi = cuts[r], cuts[r + 1]
+        k = wd.k[:, :, lo:hi].contiguous()
+        v = wd.v[:, :, lo:hi].contiguous()
+        lens = (wd.seq_lens - lo).clamp(0, hi - lo).to(torch.int32)
+        S = 3
+        ws = torch.zeros(fd.workspace_size(2, 32, 8, 128, S), dtype=torch.uint8, device="cuda")
+        fd.decode_partial(wd.q, k, v, lens, ws, num_splits=S)
+        lp, op = fd.workspace_partials(ws, 2, 32, 128, S)
+        lse_list.append(lp.clone())
+        o_list.append(op.clone())
+    lse_all = torch.cat(lse_list, dim=2).contiguous()
+    o_all = torch.cat(o_list, dim=2).contiguous()
+    o, l = fd.merge_partials(lse_all, o_all, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
