@@ -70,6 +70,15 @@ def load_library(path: Optional[str] = None):
         ctypes.c_void_p, ctypes.c_int64,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
     ]
+    lib.fd_oracle_decode_causal.restype = ctypes.c_int
+    lib.fd_oracle_decode_causal.argtypes = [
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+    ]
     lib.fd_oracle_max_threads.restype = ctypes.c_int
     lib.fd_oracle_max_threads.argtypes = []
     if path is None:
@@ -138,6 +147,44 @@ def decode(q: np.ndarray, k: np.ndarray, v: np.ndarray, seq_lens: np.ndarray,
                               int(num_threads))
     if rc != 0:
         raise ValueError("fd_oracle_decode rejected its arguments (code %d)" % rc)
+    return out, lse
+
+
+def decode_causal(q: np.ndarray, k: np.ndarray, v: np.ndarray, seq_lens: np.ndarray,
+                  block_table: Optional[np.ndarray] = None, page_size: int = 0,
+                  rows: Optional[Iterable[int]] = None, num_threads: int = 0,
+                  lib=None) -> Tuple[np.ndarray, np.ndarray]:
+    """Multi-token decode in fp64: q [B, Q, Hq, d]; query j of row b sees keys
+    t < L_b - Q + 1 + j.  Returns (out [B, Q, Hq, d], lse [B, Q, Hq]); rows not listed
+    in ``rows`` (flat ids (b * Q + j) * Hq + h) are NaN."""
+    lib = lib or load_library()
+    q, dt_q = _as_storage(q)
+    k, dt_k = _as_storage(k)
+    v, dt_v = _as_storage(v)
+    if not (dt_q == dt_k == dt_v):
+        raise TypeError("q, k and v must share one storage dtype")
+    B, Q, Hq, d = q.shape
+    Hkv = k.shape[1]
+    seq = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    if block_table is None:
+        L_cap, bt_ptr, max_pages, ps, num_pages, bt = k.shape[2], None, 0, 0, 0, None
+    else:
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        max_pages, ps, num_pages = bt.shape[1], int(page_size), k.shape[0]
+        L_cap, bt_ptr = max_pages * ps, bt.ctypes.data
+    out = np.full((B, Q, Hq, d), np.nan, dtype=np.float64)
+    lse = np.full((B, Q, Hq), np.nan, dtype=np.float64)
+    if rows is not None:
+        rows_arr = np.ascontiguousarray(np.fromiter(rows, dtype=np.int64))
+        rows_ptr, n_rows = rows_arr.ctypes.data, rows_arr.size
+    else:
+        rows_arr, rows_ptr, n_rows = None, None, 0
+    rc = lib.fd_oracle_decode_causal(B, Q, Hq, Hkv, d, dt_q, q.ctypes.data, k.ctypes.data,
+                                     v.ctypes.data, seq.ctypes.data, L_cap, bt_ptr, max_pages,
+                                     ps, num_pages, rows_ptr, n_rows, out.ctypes.data,
+                                     lse.ctypes.data, int(num_threads))
+    if rc != 0:
+        raise ValueError("fd_oracle_decode_causal rejected its arguments (code %d)" % rc)
     return out, lse
 
 

@@ -174,6 +174,97 @@ int fd_oracle_decode(int B, int Hq, int Hkv, int d, int dtype,
   return failed ? -6 : 0;
 }
 
+/*
+ * fd_oracle_decode_causal: decode with Q query tokens per row (multi-token decode, as in
+ * speculative verification).  The Q tokens are the last Q positions of row b and their
+ * keys and values are already in the cache, so query j (0-based) sits at position
+ * L_b - Q + j and, with the causal mask of "AI Infra: math and infra optimisation in
+ * large models" section 2.5 (a token sees only itself and the past), attends to the
+ * keys t < L_b - Q + 1 + j.  A query that sees no key gets o = 0, lse = -infinity.
+ * Everything else is fd_oracle_decode's plain definition, in fp64.
+ *
+ *   q  [B, Q, Hq, d]   out [B, Q, Hq, d] double   lse [B, Q, Hq] double
+ *   rows: optional flat ids ((b * Q + j) * Hq + h) to compute; NULL = all.
+ * Returns 0, or the error codes of fd_oracle_decode.
+ */
+int fd_oracle_decode_causal(int B, int Q, int Hq, int Hkv, int d, int dtype,
+                            const void* q, const void* k, const void* v,
+                            const int32_t* seq_lens, int64_t L_cap,
+                            const int32_t* block_table, int max_pages, int page_size,
+                            int64_t num_pages, const int64_t* rows, int64_t n_rows,
+                            double* out, double* lse, int num_threads) {
+  if (B < 0 || Q <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || L_cap < 0) return -1;
+  if (Hq % Hkv != 0) return -2;
+  if (dtype != FDO_F32 && dtype != FDO_BF16) return -3;
+  if (block_table != NULL && (page_size <= 0 || max_pages <= 0)) return -1;
+  const int G = Hq / Hkv;
+  for (int b = 0; b < B; ++b) {
+    if (seq_lens[b] < 0 || seq_lens[b] > L_cap) return -4;
+    if (block_table != NULL) {
+      int64_t used = ((int64_t)seq_lens[b] + page_size - 1) / page_size;
+      for (int64_t i = 0; i < used; ++i) {
+        int32_t p = block_table[(int64_t)b * max_pages + i];
+        if (p < 0 || p >= num_pages) return -5;
+      }
+    }
+  }
+  const int64_t total = rows ? n_rows : (int64_t)B * Q * Hq;
+  const double scale = 1.0 / sqrt((double)d);
+  int failed = 0;
+
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+#endif
+  for (int64_t r = 0; r < total; ++r) {
+    const int64_t row = rows ? rows[r] : r;          /* (b * Q + j) * Hq + h */
+    const int h = (int)(row % Hq);
+    const int j = (int)((row / Hq) % Q);
+    const int b = (int)(row / ((int64_t)Hq * Q));
+    const int g = h / G;
+    const int64_t visible = (int64_t)seq_lens[b] - Q + 1 + j;   /* keys t < visible */
+    double* o = out + row * d;
+    if (visible <= 0) {
+      for (int c = 0; c < d; ++c) o[c] = 0.0;
+      lse[row] = -INFINITY;
+      continue;
+    }
+    double* s = (double*)malloc((size_t)visible * sizeof(double));
+    if (s == NULL) {
+      failed |= 1;
+      continue;
+    }
+    for (int64_t t = 0; t < visible; ++t) {
+      double dot = 0.0;
+      for (int c = 0; c < d; ++c) {
+        double qc = fdo_load(q, dtype, row * d + c);
+        double kc = fdo_load(k, dtype, fdo_kv_offset(b, g, t, c, Hkv, d, L_cap, block_table,
+                                                     max_pages, page_size));
+        dot += qc * kc;
+      }
+      s[t] = dot * scale;
+    }
+    double m = s[0];
+    for (int64_t t = 1; t < visible; ++t) {
+      if (s[t] > m) m = s[t];
+    }
+    double l = 0.0;
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (int64_t t = 0; t < visible; ++t) {
+      double p = exp(s[t] - m);
+      l += p;
+      for (int c = 0; c < d; ++c) {
+        o[c] += p * fdo_load(v, dtype, fdo_kv_offset(b, g, t, c, Hkv, d, L_cap, block_table,
+                                                     max_pages, page_size));
+      }
+    }
+    for (int c = 0; c < d; ++c) o[c] /= l;
+    lse[row] = m + log(l);
+    free(s);
+  }
+  return failed ? -6 : 0;
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int fd_oracle_max_threads(void) {
 #ifdef _OPENMP

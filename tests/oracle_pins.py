@@ -339,10 +339,92 @@ def pin_layout_transpose(lib):
             assert abs(lse[b, h] - math.log(2.0 + math.exp(z))) < 1e-13
 
 
+def pin_causal_reduces_to_decode(lib):
+    """One query token: the multi-token oracle is the single-token one, bit for bit."""
+    rng = np.random.default_rng(18)
+    B, Hkv, G, d, L = 2, 2, 3, 8, 17
+    q = rng.standard_normal((B, 1, Hkv * G, d)).astype(np.float32)
+    k = rng.standard_normal((B, Hkv, L, d)).astype(np.float32)
+    v = rng.standard_normal((B, Hkv, L, d)).astype(np.float32)
+    lens = np.array([L, 9], np.int32)
+    o1, l1 = oracle.decode_causal(q, k, v, lens, lib=lib)
+    o2, l2 = oracle.decode(q[:, 0], k, v, lens, lib=lib)
+    assert np.array_equal(o1[:, 0], o2) and np.array_equal(l1[:, 0], l2)
+
+
+def pin_causal_prefix_and_library(lib):
+    """Query j of Q sees exactly the first L - Q + 1 + j keys: it equals single-token decode
+    over that prefix, and torch float64 SDPA with a bottom-right aligned causal mask
+    (keys repeated per query group); queries that see no key give 0 and -inf."""
+    import torch
+    rng = np.random.default_rng(19)
+    B, Q, Hkv, G, d, Lc = 3, 4, 2, 2, 16, 30
+    Hq = Hkv * G
+    q = rng.standard_normal((B, Q, Hq, d)).astype(np.float32)
+    k = rng.standard_normal((B, Hkv, Lc, d)).astype(np.float32)
+    v = rng.standard_normal((B, Hkv, Lc, d)).astype(np.float32)
+    lens = np.array([30, 11, 2], np.int32)             # row 2: only 2 keys for 4 queries
+    o, l = oracle.decode_causal(q, k, v, lens, lib=lib)
+    for j in range(Q):
+        pre = np.maximum(lens - Q + 1 + j, 0).astype(np.int32)
+        oj, lj = oracle.decode(q[:, j], k, v, pre, lib=lib)
+        assert np.allclose(o[:, j], oj, rtol=1e-13, atol=1e-14)
+        assert np.array_equal(np.isneginf(l[:, j]), np.isneginf(lj))
+        fin = ~np.isneginf(lj)
+        assert np.allclose(l[:, j][fin], lj[fin], rtol=1e-13, atol=1e-14)
+    assert np.all(o[2, :2] == 0.0) and np.all(np.isneginf(l[2, :2]))
+    for b in range(B):
+        L = int(lens[b])
+        qt = torch.from_numpy(q[b].astype(np.float64)).permute(1, 0, 2)          # [Hq, Q, d]
+        kt = torch.from_numpy(k[b, :, :L].astype(np.float64)).repeat_interleave(G, dim=0)
+        vt = torch.from_numpy(v[b, :, :L].astype(np.float64)).repeat_interleave(G, dim=0)
+        pos = torch.arange(Q)[:, None] + (L - Q)                                 # query positions
+        mask = torch.arange(L)[None, :] <= pos                                   # [Q, L]
+        live = mask.any(dim=1)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qt[:, live], kt, vt, attn_mask=mask[live])                            # [Hq, Ql, d]
+        got = torch.from_numpy(o[b]).permute(1, 0, 2)[:, live]
+        assert torch.allclose(got, ref, rtol=1e-10, atol=1e-12)
+
+
+def pin_causal_decimal(lib):
+    """40-digit decimal evaluation of the causal rows on a tiny bf16 case."""
+    ctx = decimal.Context(prec=40)
+    rng = np.random.default_rng(20)
+    B, Q, Hkv, G, d, Lc = 2, 3, 1, 2, 4, 6
+    Hq = Hkv * G
+    qb = _bf16_bits(rng.standard_normal((B, Q, Hq, d)).astype(np.float32))
+    kb = _bf16_bits((2 * rng.standard_normal((B, Hkv, Lc, d))).astype(np.float32))
+    vb = _bf16_bits(rng.standard_normal((B, Hkv, Lc, d)).astype(np.float32))
+    qf, kf, vf = _bits_to_f64(qb), _bits_to_f64(kb), _bits_to_f64(vb)
+    lens = np.array([6, 4], np.int32)
+    o, l = oracle.decode_causal(qb, kb, vb, lens, lib=lib)
+    inv = ctx.divide(decimal.Decimal(1), ctx.sqrt(decimal.Decimal(d)))
+    for b in range(B):
+        for j in range(Q):
+            for h in range(Hq):
+                vis = int(lens[b]) - Q + 1 + j
+                ex, num = [], [decimal.Decimal(0)] * d
+                for t in range(vis):
+                    dot = decimal.Decimal(0)
+                    for c in range(d):
+                        dot = ctx.add(dot, ctx.multiply(decimal.Decimal(float(qf[b, j, h, c])),
+                                                        decimal.Decimal(float(kf[b, h // G, t, c]))))
+                    e = ctx.exp(ctx.multiply(dot, inv))
+                    ex.append(e)
+                    for c in range(d):
+                        num[c] = ctx.add(num[c], ctx.multiply(e, decimal.Decimal(float(vf[b, h // G, t, c]))))
+                den = sum(ex, decimal.Decimal(0))
+                assert abs(l[b, j, h] - float(ctx.ln(den))) < 1e-12
+                assert np.allclose(o[b, j, h], [float(ctx.divide(x, den)) for x in num],
+                                   rtol=1e-12, atol=1e-13)
+
+
 ALL_PINS = [
     pin_softmax_examples, pin_worked_example, pin_closed_forms, pin_shift_invariance,
     pin_split_invariance, pin_brute_force_decimal, pin_torch_library,
     pin_paged_permutation, pin_gqa_map, pin_layout_transpose,
+    pin_causal_reduces_to_decode, pin_causal_prefix_and_library, pin_causal_decimal,
 ]
 
 
