@@ -218,15 +218,18 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     fresh workspace is zero-filled); the library itself allocates nothing.
     """
     L = lib()
-    B, Hq, d = q.shape
+    if q.dim() == 4:                                   # [B, Q, Hq, d]: multi-token decode
+        B, Qn, Hq, d = q.shape
+    else:
+        (B, Hq, d), Qn = q.shape, 1
     Hkv = k_cache.shape[1]
     S = resolve_num_splits(B, Hq, Hkv, d, _cap(k_cache, block_table, page_size), num_splits)
     if out is None:
-        out = torch.empty((B, Hq, d), dtype=out_dtype or q.dtype, device=q.device)
+        out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
     if lse_out is None:
-        lse_out = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        lse_out = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     if workspace is None:
-        workspace = torch.zeros(workspace_size(B, Hq, Hkv, d, S), dtype=torch.uint8,
+        workspace = torch.zeros(workspace_size(B, Qn * Hq, Hkv, d, S), dtype=torch.uint8,
                                 device=q.device)
     if seq_lens.dtype != torch.int32:
         raise TypeError("seq_lens must be int32")
@@ -258,7 +261,7 @@ def decode_attention_noalloc(q, k_cache, v_cache, seq_lens, out: torch.Tensor,
 def decode_partial(q, k_cache, v_cache, seq_lens, workspace: torch.Tensor, block_table=None,
                    page_size: int = 0, num_splits: int = 0, stream=None) -> int:
     """Partial pass only (fd_decode_partial); returns the split count used."""
-    B, Hq, d = q.shape
+    B, Hq, d = q.shape[0], q.shape[-2], q.shape[-1]
     S = resolve_num_splits(B, Hq, k_cache.shape[1], d, _cap(k_cache, block_table, page_size),
                            num_splits)
     dq, dk, dv, dbt = tensor_desc(q), tensor_desc(k_cache), tensor_desc(v_cache), tensor_desc(block_table)

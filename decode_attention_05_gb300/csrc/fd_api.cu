@@ -267,13 +267,19 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
     return fail(FD_ERR_INVALID_ARG, "a tensor has a NULL data pointer");
   if (!seq_lens) return fail(FD_ERR_INVALID_ARG, "seq_lens is NULL");
   if (!workspace) return fail(FD_ERR_INVALID_ARG, "workspace is NULL");
-  if (q->ndim != 3 || k_cache->ndim != 4 || v_cache->ndim != 4 || (out && out->ndim != 3))
-    return fail(FD_ERR_INVALID_ARG, "ranks must be q 3, k/v 4, out 3 (got %d, %d, %d, %d)", q->ndim,
-                k_cache->ndim, v_cache->ndim, out ? out->ndim : 3);
+  if ((q->ndim != 3 && q->ndim != 4) || k_cache->ndim != 4 || v_cache->ndim != 4 ||
+      (out && out->ndim != q->ndim))
+    return fail(FD_ERR_INVALID_ARG,
+                "ranks must be q 3 or 4, k/v 4, out as q (got %d, %d, %d, %d)", q->ndim,
+                k_cache->ndim, v_cache->ndim, out ? out->ndim : q->ndim);
   if (num_splits < 0 || num_splits > kMaxSplits)
     return fail(FD_ERR_INVALID_ARG, "num_splits must be in [0, %d], got %d", kMaxSplits, num_splits);
 
-  const int64_t B = q->shape[0], Hq = q->shape[1], d = q->shape[2];
+  // q [B, Hq, d] (one query token per row) or [B, Q, Hq, d] (Q tokens, causal).
+  const bool multi = q->ndim == 4;
+  const int64_t B = q->shape[0], Q = multi ? q->shape[1] : 1;
+  const int64_t Hq = q->shape[multi ? 2 : 1], d = q->shape[multi ? 3 : 2];
+  if (Q <= 0) return fail(FD_ERR_INVALID_ARG, "empty query token dimension");
   const int64_t Hkv = k_cache->shape[1];
   if (B <= 0 || Hq <= 0 || d <= 0 || Hkv <= 0) return fail(FD_ERR_INVALID_ARG, "empty shape");
   for (int i = 0; i < 4; ++i) {
@@ -282,8 +288,11 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   }
   if (k_cache->shape[3] != d) return fail(FD_ERR_INVALID_ARG, "k/v head dim %lld != q head dim %lld",
                                           (long long)k_cache->shape[3], (long long)d);
-  if (out && (out->shape[0] != B || out->shape[1] != Hq || out->shape[2] != d))
-    return fail(FD_ERR_INVALID_ARG, "out must be [B, Hq, d]");
+  if (out) {
+    for (int i = 0; i < q->ndim; ++i) {
+      if (out->shape[i] != q->shape[i]) return fail(FD_ERR_INVALID_ARG, "out must have q's shape");
+    }
+  }
   if (Hq % Hkv != 0) return fail(FD_ERR_INVALID_ARG, "Hq (%lld) is not a multiple of Hkv (%lld)",
                                  (long long)Hq, (long long)Hkv);
   // ---- dtypes
@@ -297,15 +306,19 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   if (d != 64 && d != 128) return fail(FD_ERR_UNSUPPORTED, "head dim %lld not in {64, 128}", (long long)d);
   if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
     return fail(FD_ERR_UNSUPPORTED, "group size %lld not in {1, 2, 4, 8, 16}", (long long)G);
+  if (Q * G > 16)
+    return fail(FD_ERR_UNSUPPORTED, "query tokens x group size = %lld exceeds 16 rows per kv head",
+                (long long)(Q * G));
   const int es = esize(q->dtype);
   // ---- strides and alignment (TMA: 16-byte base and strides; rows contiguous)
-  if (q->stride[2] != 1 || k_cache->stride[3] != 1 || v_cache->stride[3] != 1 ||
-      (out && out->stride[2] != 1))
+  if (q->stride[q->ndim - 1] != 1 || k_cache->stride[3] != 1 || v_cache->stride[3] != 1 ||
+      (out && out->stride[out->ndim - 1] != 1))
     return fail(FD_ERR_INVALID_ARG, "the last dimension of q, k, v and out must be contiguous");
   if (!aligned16(q->data) || !aligned16(k_cache->data) || !aligned16(v_cache->data))
     return fail(FD_ERR_INVALID_ARG, "q, k_cache and v_cache must be 16-byte aligned");
-  if ((q->stride[0] * es) % 16 || (q->stride[1] * es) % 16)
-    return fail(FD_ERR_INVALID_ARG, "q strides must be multiples of 16 bytes");
+  for (int i = 0; i + 1 < q->ndim; ++i) {
+    if ((q->stride[i] * es) % 16) return fail(FD_ERR_INVALID_ARG, "q strides must be multiples of 16 bytes");
+  }
   for (int i = 0; i < 3; ++i) {
     if ((k_cache->stride[i] * es) % 16 || (v_cache->stride[i] * es) % 16 || k_cache->stride[i] <= 0 ||
         v_cache->stride[i] <= 0)
@@ -344,7 +357,7 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   int32_t S = num_splits > 0 ? num_splits
                              : fd_num_splits_heuristic((int32_t)B, (int32_t)Hq, (int32_t)Hkv,
                                                        (int32_t)d, L_cap, current_sm_count());
-  const WsLayout wl = ws_layout(B, Hq, Hkv, d, S);
+  const WsLayout wl = ws_layout(B, Q * Hq, Hkv, d, S);   // partial rows: [B, Q, Hq]
   if (((uintptr_t)workspace & (kAlign - 1)) != 0)
     return fail(FD_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if (workspace_bytes < wl.total)
@@ -377,8 +390,11 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   p.S = S;
   p.split_len = (L_cap + S - 1) / S;
   p.q = q->data;
+  p.Q = (int32_t)Q;
+  p.n_rows = (int32_t)(Q * G);
   p.q_sb = q->stride[0];
-  p.q_sh = q->stride[1];
+  p.q_sj = multi ? q->stride[1] : 0;
+  p.q_sh = q->stride[multi ? 2 : 1];
   p.seq_lens = seq_lens;
   p.block_table = paged ? static_cast<const int32_t*>(block_table->data) : nullptr;
   p.bt_sb = bt_sb;
@@ -397,7 +413,8 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   p.o_part = reinterpret_cast<float*>(ws + wl.o_off);
   p.out = out ? out->data : nullptr;
   p.out_sb = out ? out->stride[0] : 0;
-  p.out_sh = out ? out->stride[1] : 0;
+  p.out_sj = out && multi ? out->stride[1] : 0;
+  p.out_sh = out ? out->stride[multi ? 2 : 1] : 0;
   p.out_bf16 = out && out->dtype == FD_BF16 ? 1 : 0;
   p.lse_out = lse_out;
   p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
@@ -494,6 +511,9 @@ fd_status fd_merge_partials(int32_t B, int32_t Hq, int32_t d, int32_t num_splits
   p.out_sh = out->stride[1];
   p.out_bf16 = out->dtype == FD_BF16 ? 1 : 0;
   p.lse_out = lse_out;
+  p.Q = 1;
+  p.G = 1;
+  p.n_rows = 1;
   return launch_merge(p, (cudaStream_t)stream);
 }
 

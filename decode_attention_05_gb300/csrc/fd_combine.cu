@@ -1,4 +1,5 @@
-// fd_combine.cu -- the merge pass of split-KV decode: one CTA per (b, query head).
+// fd_combine.cu -- the merge pass of split-KV decode: one CTA per (b, query token,
+// query head) row.
 //
 // Reads the S partials (O_i, LSE_i) of its row and computes
 //   M = max over non-empty splits of LSE_i,   w_i = exp(LSE_i - M)  in (0, 1],
@@ -30,7 +31,7 @@ __global__ void __launch_bounds__(128) fd_combine_kernel(const __grid_constant__
   __shared__ __align__(16) float accs[4][D];
   pdl_wait();
 
-  const int row = blockIdx.x;                  // b * Hq + h
+  const int row = blockIdx.x;                  // (b * Q + j) * Hq + h
   const int S = p.S;
   const float* lse = p.lse_part + (int64_t)row * S;
   const float* ob = p.o_part + (int64_t)row * S * D + (threadIdx.x & 31) * VEC;
@@ -95,14 +96,14 @@ __global__ void __launch_bounds__(128) fd_combine_kernel(const __grid_constant__
     cw[w] = (wm[w] == kNegInf) ? 0.f : ex2(wm[w] - Mt);
     Wt = fmaf(ww[w], cw[w], Wt);
   }
-  const int b = row / p.Hq, h = row % p.Hq;
+  const int h = row % p.Hq, bj = row / p.Hq, b = bj / p.Q, qj = bj % p.Q;
   for (int j = tid; j < D; j += 128) {
     float o = 0.f;
     if (Wt > 0.f) {
       o = accs[0][j] * cw[0] + accs[1][j] * cw[1] + accs[2][j] * cw[2] + accs[3][j] * cw[3];
       o /= Wt;
     }
-    const int64_t off = (int64_t)b * p.out_sb + (int64_t)h * p.out_sh + j;
+    const int64_t off = (int64_t)b * p.out_sb + (int64_t)qj * p.out_sj + (int64_t)h * p.out_sh + j;
     if (p.out_bf16) {
       reinterpret_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(o);
     } else {
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(128) fd_combine_kernel(const __grid_constant__
 
 cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.B * p.Hq));
+  cfg.gridDim = dim3((unsigned)((int64_t)p.B * p.Q * p.Hq));
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

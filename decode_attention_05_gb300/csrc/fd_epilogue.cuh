@@ -29,20 +29,17 @@ __device__ __forceinline__ float lg2_approx(float x) {
 
 // Split epilogue for an empty (or aborted) split: LSE_i = -inf for the whole group.
 __device__ __forceinline__ void write_empty_split(const Params& p, const SplitInfo& si, int tid) {
-  if (tid < p.G) {
-    const int64_t row = (int64_t)si.b * p.Hq + (int64_t)si.g * p.G + tid;
-    p.lse_part[row * p.S + si.split] = kNegInf;
-  }
+  if (tid < p.n_rows) p.lse_part[flat_row(p, si.b, si.g, tid) * p.S + si.split] = kNegInf;
 }
 
-// macc [NCW][G][D], mm [NCW][G], ml [NCW][G] in shared memory, filled by every warp;
-// called by all NCW * 32 consumer threads (ctid = 0 .. NCW * 32 - 1) after a barrier.
+// macc [NCW][G][D], mm [NCW][G], ml [NCW][G] in shared memory (G = query rows of the
+// group, a power of two >= p.n_rows), filled by every warp for rows < p.n_rows; called
+// by all NCW * 32 consumer threads (ctid = 0 .. NCW * 32 - 1) after a barrier.
 template <int G, int D, int NCW>
 __device__ __forceinline__ void merge_warps_and_store(const Params& p, const SplitInfo& si,
                                                       const float* macc, const float* mm,
                                                       const float* ml, int ctid) {
-  const int64_t row0 = (int64_t)si.b * p.Hq + (int64_t)si.g * G;
-  for (int idx = ctid; idx < G * D; idx += NCW * 32) {
+  for (int idx = ctid; idx < p.n_rows * D; idx += NCW * 32) {
     const int h = idx / D, j = idx % D;
     float M = kNegInf;
 #pragma unroll
@@ -57,7 +54,7 @@ __device__ __forceinline__ void merge_warps_and_store(const Params& p, const Spl
         O = fmaf(macc[(w * G + h) * D + j], c, O);
       }
     }
-    const int64_t row = row0 + h;
+    const int64_t row = flat_row(p, si.b, si.g, h);
     if (L > 0.f) {
       p.o_part[(row * p.S + si.split) * D + j] = O / L;
       if (j == 0) p.lse_part[row * p.S + si.split] = (M + lg2_approx(L)) * 0.6931471805599453f;
@@ -78,7 +75,7 @@ __device__ __forceinline__ void merge_warps_and_store(const Params& p, const Spl
 // no grid-wide dependency ("2kiu.com/news/6053916", section "the split count is a cost
 // account": the merge may start only when every partial it needs is visible).
 //
-// Merge of one row (warp w takes heads w, w + NCW, ...; a lane holds D / 32 dims): the
+// Merge of one row (warp w takes rows w, w + NCW, ...; a lane holds D / 32 dims): the
 // splits are folded 16 at a time with a running maximum, the same online rule as inside
 // a split, so all loads of a batch are issued before any result is needed:
 //   M' = max(M, max_s LSE_s),  W = W 2^(M - M') + sum_s 2^(LSE_s - M'),
@@ -92,8 +89,8 @@ __device__ __forceinline__ void merge_group(const Params& p, int b, int g, int c
   constexpr int BATCH = 16;
   constexpr float kLog2e = 1.4426950408889634f;
   const int warp = ctid >> 5, lane = ctid & 31;
-  for (int h = warp; h < p.G; h += NCW) {
-    const int64_t row = (int64_t)b * p.Hq + (int64_t)g * p.G + h;
+  for (int rho = warp; rho < p.n_rows; rho += NCW) {
+    const int64_t row = flat_row(p, b, g, rho);
     const float* lse = p.lse_part + row * p.S;
     const float* ob = p.o_part + row * p.S * D + lane * VEC;
     float M = kNegInf, W = 0.f, acc[VEC];
@@ -134,8 +131,9 @@ __device__ __forceinline__ void merge_group(const Params& p, int b, int g, int c
       }
       M = mn;
     }
-    const int hq = g * p.G + h;
-    const int64_t obase = (int64_t)b * p.out_sb + (int64_t)hq * p.out_sh + lane * VEC;
+    const int j = rho / p.G, hq = g * p.G + (rho - j * p.G);
+    const int64_t obase = (int64_t)b * p.out_sb + (int64_t)j * p.out_sj +
+                          (int64_t)hq * p.out_sh + lane * VEC;
     const float inv = W > 0.f ? 1.f / W : 0.f;
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {

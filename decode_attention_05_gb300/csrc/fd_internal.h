@@ -26,9 +26,11 @@ struct Params {
   int64_t L_cap;          // tokens of capacity per row
   int32_t S;              // number of splits
   int64_t split_len;      // ceil(L_cap / S)
-  // query [B, Hq, d]
+  // query [B, Q, Hq, d] (Q = 1: single-token decode)
   const void* q;
-  int64_t q_sb, q_sh;     // strides (elements) of batch and head
+  int64_t q_sb, q_sj, q_sh;   // strides (elements) of batch, query token and head
+  int32_t Q;                  // query tokens per row; query j sees keys t < L_b - Q + 1 + j
+  int32_t n_rows;             // query rows per (b, kv head) = Q * G
   // lengths and paging
   const int32_t* seq_lens;
   const int32_t* block_table;   // nullptr -> contiguous
@@ -44,13 +46,13 @@ struct Params {
                                   // the fused merge, or nullptr: the partial pass then
                                   // leaves the merge to a separate kernel
   uint32_t epoch;                 // this call's ticket epoch (never 0)
-  float* lse_part;        // [B, Hq, S]     natural-log LSE_i, -inf for an empty split
-  float* o_part;          // [B, Hq, S, d]  normalised partial output O_i
+  float* lse_part;        // [B, Q, Hq, S]     natural-log LSE_i, -inf for an empty split
+  float* o_part;          // [B, Q, Hq, S, d]  normalised partial output O_i
   // outputs
-  void* out;
-  int64_t out_sb, out_sh;
+  void* out;                // [B, Q, Hq, d]
+  int64_t out_sb, out_sj, out_sh;
   int32_t out_bf16;       // 1: bf16 out, 0: f32 out
-  float* lse_out;         // [B, Hq] or nullptr
+  float* lse_out;         // [B, Q, Hq] or nullptr
   float scale_log2;       // log2(e) / sqrt(d): scores are kept in base-2 units inside kernels
 };
 
@@ -63,6 +65,14 @@ cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool pdl);
 
 // Record `message` as the calling thread's fd_last_error() and return `st`.
 fd_status record_error(fd_status st, const char* message);
+
+// Kernel instance for n query rows per (b, kv head): the next power of two (1..16), or 0
+// when n exceeds 16.
+inline int rows_template(int n) {
+  int r = 1;
+  while (r < n) r <<= 1;
+  return n >= 1 && r <= 16 ? r : 0;
+}
 
 // Tile height (tokens) used by the kernels for a dtype and head dim.
 inline int tile_tokens(int d, int esz) { return kTileBytes / (d * esz); }

@@ -10,8 +10,10 @@
 //
 // Memory side: the TMA producer warp and stage ring of fd_pipeline.cuh (128-byte
 // swizzled K/V tiles).  Compute side, per consumer warp and per 16-token chunk:
-//   S^T[16 tok, 8 heads] = K_chunk[16, d] . Q^T[d, 8]          (tokens in M, heads in N:
-//                                                                G = 8 fills N exactly)
+//   S^T[16 tok, 8 rows] = K_chunk[16, d] . Q^T[d, 8]           (tokens in M, query rows in
+//                                                                N: G = 8 fills N exactly;
+//                                                                multi-token decode adds
+//                                                                Q x G rows, up to 16)
 //   scores -> base-2 logits, mask (-inf), online-softmax max / rescale
 //   P^T = movmatrix.trans(bf16(2^(S - m)))                      (register transpose)
 //   O^T[d, 8] += V_chunk^T[d, 16 tok] . P^T[16 tok, 8 heads]    (V^T via ldmatrix.trans)
@@ -129,16 +131,24 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   uint32_t qb[NT][SH::KSTEPS][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int h = nt * 8 + qr;
-    const int hc = h < G ? h : 0;                     // never address past the group
+    const int h = nt * 8 + qr;                        // query row of the group
+    const bool live = h < p.n_rows;
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-        reinterpret_cast<const __nv_bfloat16*>(p.q) + si.b * p.q_sb + (si.g * G + hc) * p.q_sh);
+        reinterpret_cast<const __nv_bfloat16*>(p.q) +
+        q_offset(p, si.b, si.g, live ? h : 0));       // never address past the group
 #pragma unroll
     for (int kk = 0; kk < SH::KSTEPS; ++kk) {
       const uint32_t lo = qrow[(kk * 16 + qc) / 2], hi = qrow[(kk * 16 + qc + 8) / 2];
-      qb[nt][kk][0] = h < G ? lo : 0u;
-      qb[nt][kk][1] = h < G ? hi : 0u;
+      qb[nt][kk][0] = live ? lo : 0u;
+      qb[nt][kk][1] = live ? hi : 0u;
     }
+  }
+  // Causal key bound of this thread's two fragment columns (rows nt * 8 + qc + {0, 1}).
+  int64_t lim[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    lim[nt][0] = key_bound(p, si.L, nt * 8 + qc);
+    lim[nt][1] = key_bound(p, si.L, nt * 8 + qc + 1);
   }
 
   // Per-thread softmax state for heads nt * 8 + qc + {0, 1}; acc = O^T fragments:
@@ -221,19 +231,22 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
       // ---- mask and scale: element e of s[nt] is (token rb + qr + 8 (e >> 1),
       //      head nt * 8 + qc + (e & 1)); excluded tokens get -inf.
       bool vrow[2];
+      int64_t vtok[2];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int row = rb + qr + 8 * hh;
         const int64_t tok = t0 + row;
         const int pslot = multi_page ? (row >> p.log2_page) : 0;
         vrow[hh] = tok >= si.lo && tok < si.hi && !((bad >> pslot) & 1u);
+        vtok[hh] = tok;
       }
       uint32_t pb[NT][2];                             // P^T fragments (b0/b1 of the PV mma)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         float x[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] = vrow[e >> 1] ? s[nt][e] * sl2 : kNegInf;
+        for (int e = 0; e < 4; ++e)
+          x[e] = (vrow[e >> 1] && vtok[e >> 1] < lim[nt][e & 1]) ? s[nt][e] * sl2 : kNegInf;
         // chunk max per head over the 16 tokens: in-thread pair, then lanes of equal qc
         float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
@@ -309,7 +322,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int h = nt * 8 + qc + e;
-      if (h < G) {
+      if (h < p.n_rows) {
 #pragma unroll
         for (int mt = 0; mt < SH::MTILES; ++mt) {
           macc[(warp * G + h) * SH::D + mt * 16 + qr] = acc[nt][mt][e];
@@ -342,7 +355,7 @@ cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap
 template <int D>
 cudaError_t dispatch_g(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                        cudaStream_t stream) {
-  switch (p.G) {
+  switch (rows_template(p.n_rows)) {   // query rows per (b, kv head), padded
     case 1: return launch_mma<MmaShape<D, 1>>(p, tk, tv, stream);
     case 2: return launch_mma<MmaShape<D, 2>>(p, tk, tv, stream);
     case 4: return launch_mma<MmaShape<D, 4>>(p, tk, tv, stream);

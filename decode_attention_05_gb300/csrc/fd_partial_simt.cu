@@ -22,7 +22,7 @@ cudaError_t launch_simt(const Params& p, const CUtensorMap& tk, const CUtensorMa
 template <int ESZ, int D>
 cudaError_t dispatch_g(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                        cudaStream_t stream) {
-  switch (p.G) {
+  switch (rows_template(p.n_rows)) {   // query rows per (b, kv head), padded
     case 1: return launch_simt<SimtShape<ESZ, D, 1>>(p, tk, tv, stream);
     case 2: return launch_simt<SimtShape<ESZ, D, 2>>(p, tk, tv, stream);
     case 4: return launch_simt<SimtShape<ESZ, D, 4>>(p, tk, tv, stream);

@@ -1,7 +1,9 @@
 // fd_partial_simt.cuh -- split-KV partial pass with CUDA-core dot products.
 //
-// One CTA = one split of one (batch row b, kv head g) and all G query heads that read
-// kv head g.  Warp 4 is the TMA producer (fd_pipeline.cuh); warps 0-3 consume tiles.
+// One CTA = one split of one (batch row b, kv head g) and all query rows that read kv
+// head g: its G query heads, times Q query tokens in multi-token decode (template G is
+// that row count rounded up to a power of two).  Warp 4 is the TMA producer
+// (fd_pipeline.cuh); warps 0-3 consume tiles.
 //
 // Per tile, each consumer warp takes TT/4 token rows.  A lane owns EPL consecutive
 // dims of a row (LPR lanes cover one row, RPW rows per warp step), keeps the matching
@@ -9,7 +11,8 @@
 // are base-2 logits), and the G x EPL slice of the accumulator.  For a batch of rows:
 //   s[h]   = q_h . k_t / sqrt(d)                 (dot over the lane's dims, then a
 //                                                  butterfly sum across the LPR lanes)
-//   s[h]   = -inf for t outside [lo, hi) or on an invalid page (excluded, not added)
+//   s[h]   = -inf for t outside [lo, hi), on an invalid page, or past row h's causal
+//            bound (excluded, not added)
 //   m_new  = max(m, max_t s)                     (safe-softmax shift)
 //   c      = 2^(m - m_new);  l = l c;  acc = acc c   (only when some m grows)
 //   p      = 2^(s - m_new);  l += p;  acc += p v_t
@@ -134,12 +137,17 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   // ---------------------------------------------------- consumer warps
   const int rg = lane / LPR;        // row within a warp step
   const int li = lane % LPR;        // lane within the row
+  // Row h of the group (query token h / p.G, head h mod p.G); rows past p.n_rows pad
+  // the template size and stay zero.
   float qv[G][EPL];
+  int64_t lim[G];                   // causal key bound of each row
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    load_q_slice<SH>(p.q, si.b * p.q_sb + (si.g * G + h) * p.q_sh + li * EPL, qv[h]);
+    const bool live = h < p.n_rows;
+    load_q_slice<SH>(p.q, q_offset(p, si.b, si.g, live ? h : 0) + li * EPL, qv[h]);
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) qv[h][e] *= p.scale_log2;
+    for (int e = 0; e < EPL; ++e) qv[h][e] = live ? qv[h][e] * p.scale_log2 : 0.f;
+    lim[h] = key_bound(p, si.L, h);
   }
   float m[G], l[G], acc[G][EPL];
 #pragma unroll
@@ -176,10 +184,12 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
     for (int sb = 0; sb < SH::NSTEP; sb += SH::SB) {
       float s[SH::SB][G];
       bool valid[SH::SB];
+      int64_t toks[SH::SB];
 #pragma unroll
       for (int st = 0; st < SH::SB; ++st) {
         const int r = warp * SH::ROWS_PER_WARP + (sb + st) * RPW + rg;
         const int64_t tok = t0 + r;
+        toks[st] = tok;
         const int pslot = multi_page ? (r >> p.log2_page) : 0;
         valid[st] = tok >= si.lo && tok < si.hi && !((bad >> pslot) & 1u);
         float kf[EPL];
@@ -208,7 +218,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
       for (int st = 0; st < SH::SB; ++st)
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          s[st][h] = valid[st] ? s[st][h] : kNegInf;
+          s[st][h] = (valid[st] && toks[st] < lim[h]) ? s[st][h] : kNegInf;
           mx[h] = fmaxf(mx[h], s[st][h]);
         }
       bool grow = false;
@@ -239,7 +249,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
         for (int e = 0; e < EPL; ++e) vf[e] = valid[st] ? vf[e] : 0.f;   // stale rows may be NaN
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float pr = valid[st] ? ex2(s[st][h] - m[h]) : 0.f;
+          const float pr = s[st][h] != kNegInf ? ex2(s[st][h] - m[h]) : 0.f;
           l[h] += pr;
 #pragma unroll
           for (int e = 0; e < EPL; ++e) acc[h][e] = fmaf(pr, vf[e], acc[h][e]);
@@ -276,8 +286,9 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   if (rg == 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h)
+      if (h < p.n_rows)
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) macc[(warp * G + h) * SH::D + li * EPL + e] = acc[h][e];
+        for (int e = 0; e < EPL; ++e) macc[(warp * G + h) * SH::D + li * EPL + e] = acc[h][e];
   }
   if (lane == 0) {
 #pragma unroll

@@ -24,6 +24,7 @@ namespace fd {
 
 struct SplitInfo {
   int b, g, split;
+  int64_t L;            // the row's length (clamped to [0, L_cap])
   int64_t lo, hi;       // valid logical tokens of this split: [lo, hi)
   int64_t T0;           // start of the first tile (a multiple of TT)
   int n_tiles;
@@ -42,12 +43,31 @@ __device__ __forceinline__ SplitInfo split_info(const Params& p) {
     if (threadIdx.x == 0) atomicOr(p.flags, FD_DEVFLAG_SEQ_LEN);
     L = L < 0 ? 0 : p.L_cap;
   }
+  si.L = L;
   si.lo = (int64_t)si.split * p.split_len;
   si.hi = min(si.lo + p.split_len, L);
   si.T0 = (si.lo / TT) * TT;
   si.n_tiles = si.lo < si.hi ? (int)((si.hi - si.T0 + TT - 1) / TT) : 0;
   si.used_pages = p.page_size > 0 ? (L + p.page_size - 1) >> p.log2_page : 0;
   return si;
+}
+
+// Query rows of a (b, kv head) group: row rho (0 .. Q * G - 1) is query token j = rho / G
+// of head h = rho mod G.  Its flat index over [B, Q, Hq] (partials, lse_out), its query
+// vector, and its causal key bound: the Q query tokens are the last Q positions of the
+// row, so token j sees keys t < L_b - Q + 1 + j ("AI Infra: math and infra optimisation
+// in large models", section 2.5: a token sees itself and the past; with Q = 1 this is
+// the plain length mask t < L_b).
+__device__ __forceinline__ int64_t flat_row(const Params& p, int b, int g, int rho) {
+  const int j = rho / p.G, h = rho - j * p.G;
+  return ((int64_t)b * p.Q + j) * p.Hq + (int64_t)g * p.G + h;
+}
+__device__ __forceinline__ int64_t q_offset(const Params& p, int b, int g, int rho) {
+  const int j = rho / p.G, h = rho - j * p.G;
+  return (int64_t)b * p.q_sb + (int64_t)j * p.q_sj + ((int64_t)g * p.G + h) * p.q_sh;
+}
+__device__ __forceinline__ int64_t key_bound(const Params& p, int64_t L, int rho) {
+  return L - p.Q + 1 + rho / p.G;
 }
 
 // Shared-memory control block of the pipeline.

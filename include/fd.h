@@ -95,7 +95,12 @@ typedef enum {
 /*
  * fd_decode_attention -- one decode step of split-KV attention (see the top of file).
  *
- *   q            device [B, Hq, d], bf16 or f32.
+ *   q            device [B, Hq, d], bf16 or f32 -- or [B, Q, Hq, d] for multi-token
+ *                decode (speculative verification): the Q query tokens are the last Q
+ *                positions of row b, their keys and values already in the cache, so
+ *                query j (0-based) attends to the keys t <= L_b - Q + j (the causal mask
+ *                of [AI-Infra] 2.5 applied inside each split); a query that sees no key
+ *                gets out = 0, lse_out = -inf.  Q * G <= 16.
  *   k_cache      device, same dtype as q.  Contiguous: [B, Hkv, L_cap, d] (block_table
  *                NULL).  Paged: [num_pages, Hkv, page_size, d]; logical token t of row
  *                b is slot t % page_size of page block_table[b][t / page_size] -- the
@@ -111,9 +116,9 @@ typedef enum {
  *                are excluded.  Entries past a row's length are never read.
  *   page_size    0 for a contiguous cache; else a power of two in [8, 65536].
  *   num_splits   S >= 1, or 0 to let fd_num_splits_heuristic choose.  S <= 4096.
- *   out          device [B, Hq, d], bf16 or f32 (bf16 is rounded to nearest even).
- *   lse_out      device f32 [B, Hq] (contiguous), natural log; may be NULL.
- *   workspace    device scratch of at least fd_workspace_size(B, Hq, Hkv, d, S) bytes,
+ *   out          device, q's shape, bf16 or f32 (bf16 is rounded to nearest even).
+ *   lse_out      device f32 [B, Hq] or [B, Q, Hq] (contiguous), natural log; may be NULL.
+ *   workspace    device scratch of at least fd_workspace_size(B, Q * Hq, Hkv, d, S) bytes,
  *                256-byte aligned, zero-filled once before its first use
  *                (fd_workspace_init) so that its device error flags start clear; flags
  *                stay set until fd_read_device_error clears them.  Nothing else in it

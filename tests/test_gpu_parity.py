@@ -438,3 +438,49 @@ def test_sequence_sharded_merge(name, path):
     o, l = fd.merge_partials(lse_all, o_all, out_dtype=torch.float32)
     torch.cuda.synchronize()
     check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
+
+
+@pytest.mark.parametrize("name,path", PATHS_BF16)
+@pytest.mark.parametrize("Q,G", [(1, 8), (2, 8), (3, 4), (4, 4), (4, 2), (16, 1)])
+@pytest.mark.parametrize("paged", [False, True])
+def test_multi_token_decode(name, path, Q, G, paged):
+    """q [B, Q, Hq, d]: query j of row b sees keys t <= L_b - Q + j (the causal mask
+    inside each split).  Rows shorter than Q leave their first queries without keys
+    (out 0, lse -inf).  Checked against the fp64 multi-token oracle for several S."""
+    fd.set_path(path)
+    Hkv, d = 2, 128
+    Hq = Hkv * G
+    lens = [1, Q - 1 if Q > 1 else 2, 65, 300, 1000]
+    if paged:
+        w = workloads.paged_case(len(lens), Hq, Hkv, d, 16, 64, lens, seed=90 + Q * 7 + G,
+                                 out_dtype=torch.float32)
+    else:
+        w = workloads.contiguous_case(len(lens), Hq, Hkv, d, 1024, lens, seed=90 + Q * 7 + G,
+                                      out_dtype=torch.float32)
+    q4 = workloads.multi_token_queries(len(lens), Q, Hq, d, seed=190 + Q + G)
+    _, k, v, lens_np, bt, ps = w.oracle_arrays()
+    ref_o, ref_l = oracle.decode_causal(workloads.np_storage(q4), k, v, lens_np,
+                                        block_table=bt, page_size=ps)
+    wd = w.to("cuda")
+    qd = q4.cuda()
+    B = len(lens)
+    for S in (1, 3, 16):
+        ws = torch.zeros(fd.workspace_size(B, Q * Hq, Hkv, d, S), dtype=torch.uint8, device="cuda")
+        o, l = fd.decode_attention(qd, wd.k, wd.v, wd.seq_lens, wd.block_table, w.page_size, S,
+                                   workspace=ws, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert o.shape == (B, Q, Hq, d) and l.shape == (B, Q, Hq)
+        assert fd.read_device_error(ws) == 0
+        got_o = o.cpu().double().numpy().reshape(B * Q, Hq, d)
+        got_l = l.cpu().double().numpy().reshape(B * Q, Hq)
+        mw = workloads.Workload("mt", q4.reshape(B * Q, Hq, d), w.k, w.v, w.seq_lens)
+        check(mw, got_o, got_l, ref_o.reshape(B * Q, Hq, d), ref_l.reshape(B * Q, Hq))
+
+
+def test_multi_token_limits():
+    """More than 16 query rows per kv head is refused on the host."""
+    q = torch.zeros(1, 3, 8, 128, dtype=torch.bfloat16, device="cuda")      # 3 x 8 = 24 rows
+    k = torch.zeros(1, 1, 64, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fd.FdError):
+        fd.decode_attention(q, k, k, torch.tensor([64], dtype=torch.int32, device="cuda"),
+                            num_splits=1)

@@ -147,6 +147,20 @@ def paged_case(B, Hq, Hkv, d, page_size, max_pages, seq_lens, *, seed, dtype=tor
                     page_size, num_splits=num_splits, out_dtype=out_dtype or dtype)
 
 
+def multi_token_queries(B: int, Q: int, Hq: int, d: int, *, seed: int,
+                        dtype=torch.bfloat16) -> torch.Tensor:
+    """Queries for multi-token decode: [B, Q, Hq, d], N(0,1), drawn from their own seed."""
+    return _randn(_gen(seed), (B, Q, Hq, d), dtype)
+
+
+def np_storage(t: torch.Tensor) -> np.ndarray:
+    """A tensor as the oracle reads it: fp32 as float32, bf16 as raw uint16 bits."""
+    t = t.contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
 def worked_example(d: int = 64) -> Workload:
     """The pages' counter-example as one fp32 attention row: q = 80 e_0, k_0 = k_1 = 0,
     k_2 = e_0 (scores [0, 0, 10] at scale 1/8); values 0, 0, 9 in every dim; S = 2,
