@@ -79,6 +79,17 @@ def load_library(path: Optional[str] = None):
         ctypes.c_void_p, ctypes.c_int64,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
     ]
+    lib.fd_oracle_e4m3_to_double.restype = ctypes.c_double
+    lib.fd_oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.fd_oracle_decode_kv8.restype = ctypes.c_int
+    lib.fd_oracle_decode_kv8.argtypes = [
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+    ]
     lib.fd_oracle_max_threads.restype = ctypes.c_int
     lib.fd_oracle_max_threads.argtypes = []
     if path is None:
@@ -185,6 +196,50 @@ def decode_causal(q: np.ndarray, k: np.ndarray, v: np.ndarray, seq_lens: np.ndar
                                      lse.ctypes.data, int(num_threads))
     if rc != 0:
         raise ValueError("fd_oracle_decode_causal rejected its arguments (code %d)" % rc)
+    return out, lse
+
+
+def e4m3_to_double(code: int, lib=None) -> float:
+    """One FP8 E4M3 code widened to double by the oracle's definition-based decoder."""
+    return float((lib or load_library()).fd_oracle_e4m3_to_double(int(code) & 0xFF))
+
+
+def decode_kv8(q: np.ndarray, k_codes: np.ndarray, v_codes: np.ndarray, k_scale: np.ndarray,
+               v_scale: np.ndarray, seq_lens: np.ndarray, block_table: Optional[np.ndarray] = None,
+               page_size: int = 0, rows: Optional[Iterable[int]] = None, num_threads: int = 0,
+               lib=None) -> Tuple[np.ndarray, np.ndarray]:
+    """Decode over an FP8 E4M3 KV cache (uint8 codes) with per-kv-head scales [Hkv]:
+    k = code * k_scale[g], v = code * v_scale[g]; q fp32 or bf16 bits.  fp64 results."""
+    lib = lib or load_library()
+    q, dt_q = _as_storage(q)
+    k = np.ascontiguousarray(k_codes, dtype=np.uint8)
+    v = np.ascontiguousarray(v_codes, dtype=np.uint8)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    B, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if ks.shape != (Hkv,) or vs.shape != (Hkv,):
+        raise ValueError("one scale per kv head")
+    seq = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    if block_table is None:
+        L_cap, bt_ptr, max_pages, ps, num_pages, bt = k.shape[2], None, 0, 0, 0, None
+    else:
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        max_pages, ps, num_pages = bt.shape[1], int(page_size), k.shape[0]
+        L_cap, bt_ptr = max_pages * ps, bt.ctypes.data
+    out = np.full((B, Hq, d), np.nan, dtype=np.float64)
+    lse = np.full((B, Hq), np.nan, dtype=np.float64)
+    if rows is not None:
+        rows_arr = np.ascontiguousarray(np.fromiter(rows, dtype=np.int64))
+        rows_ptr, n_rows = rows_arr.ctypes.data, rows_arr.size
+    else:
+        rows_arr, rows_ptr, n_rows = None, None, 0
+    rc = lib.fd_oracle_decode_kv8(B, Hq, Hkv, d, dt_q, q.ctypes.data, k.ctypes.data,
+                                  v.ctypes.data, ks.ctypes.data, vs.ctypes.data, seq.ctypes.data,
+                                  L_cap, bt_ptr, max_pages, ps, num_pages, rows_ptr, n_rows,
+                                  out.ctypes.data, lse.ctypes.data, int(num_threads))
+    if rc != 0:
+        raise ValueError("fd_oracle_decode_kv8 rejected its arguments (code %d)" % rc)
     return out, lse
 
 

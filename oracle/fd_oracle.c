@@ -265,6 +265,109 @@ int fd_oracle_decode_causal(int B, int Q, int Hq, int Hkv, int d, int dtype,
   return failed ? -6 : 0;
 }
 
+/*
+ * FP8 E4M3 code -> double, from the format's definition: 1 sign bit, 4 exponent bits
+ * (bias 7), 3 mantissa bits; exponent 0 is subnormal (2^-6 * m / 8); the code with all
+ * exponent and mantissa bits set is NaN; there is no infinity.
+ */
+double fd_oracle_e4m3_to_double(uint8_t code) {
+  const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  double mag;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) {
+    mag = ldexp((double)m / 8.0, -6);
+  } else {
+    mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+  }
+  return sign ? -mag : mag;
+}
+
+/*
+ * fd_oracle_decode_kv8: single-token decode over a KV cache stored as FP8 E4M3 codes
+ * with one dequantisation scale per kv head for K and for V: k = code * k_scale[g],
+ * v = code * v_scale[g], widened exactly to double.  q is fp32 or bf16 (q_dtype).  The
+ * attention itself is fd_oracle_decode's plain unsplit definition.
+ *   q [B, Hq, d]; k, v as uint8 codes in fd_oracle_decode's layouts; out [B, Hq, d]
+ *   double; lse [B, Hq] double.  Returns 0 or fd_oracle_decode's error codes.
+ */
+int fd_oracle_decode_kv8(int B, int Hq, int Hkv, int d, int q_dtype, const void* q,
+                         const uint8_t* k, const uint8_t* v, const float* k_scale,
+                         const float* v_scale, const int32_t* seq_lens, int64_t L_cap,
+                         const int32_t* block_table, int max_pages, int page_size,
+                         int64_t num_pages, const int64_t* rows, int64_t n_rows,
+                         double* out, double* lse, int num_threads) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || L_cap < 0) return -1;
+  if (Hq % Hkv != 0) return -2;
+  if (q_dtype != FDO_F32 && q_dtype != FDO_BF16) return -3;
+  if (block_table != NULL && (page_size <= 0 || max_pages <= 0)) return -1;
+  const int G = Hq / Hkv;
+  for (int b = 0; b < B; ++b) {
+    if (seq_lens[b] < 0 || seq_lens[b] > L_cap) return -4;
+    if (block_table != NULL) {
+      int64_t used = ((int64_t)seq_lens[b] + page_size - 1) / page_size;
+      for (int64_t i = 0; i < used; ++i) {
+        int32_t p = block_table[(int64_t)b * max_pages + i];
+        if (p < 0 || p >= num_pages) return -5;
+      }
+    }
+  }
+  const int64_t total = rows ? n_rows : (int64_t)B * Hq;
+  const double scale = 1.0 / sqrt((double)d);
+  int failed = 0;
+
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+#endif
+  for (int64_t r = 0; r < total; ++r) {
+    const int64_t row = rows ? rows[r] : r;
+    const int b = (int)(row / Hq);
+    const int h = (int)(row % Hq);
+    const int g = h / G;
+    const int64_t L = seq_lens[b];
+    const double ks = (double)k_scale[g], vs = (double)v_scale[g];
+    double* o = out + row * d;
+    if (L == 0) {
+      for (int c = 0; c < d; ++c) o[c] = 0.0;
+      lse[row] = -INFINITY;
+      continue;
+    }
+    double* s = (double*)malloc((size_t)L * sizeof(double));
+    if (s == NULL) {
+      failed |= 1;
+      continue;
+    }
+    for (int64_t t = 0; t < L; ++t) {
+      double dot = 0.0;
+      for (int c = 0; c < d; ++c) {
+        const double kc = fd_oracle_e4m3_to_double(
+            k[fdo_kv_offset(b, g, t, c, Hkv, d, L_cap, block_table, max_pages, page_size)]);
+        dot += fdo_load(q, q_dtype, row * d + c) * (kc * ks);
+      }
+      s[t] = dot * scale;
+    }
+    double m = s[0];
+    for (int64_t t = 1; t < L; ++t) {
+      if (s[t] > m) m = s[t];
+    }
+    double l = 0.0;
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (int64_t t = 0; t < L; ++t) {
+      const double p = exp(s[t] - m);
+      l += p;
+      for (int c = 0; c < d; ++c) {
+        const double vc = fd_oracle_e4m3_to_double(
+            v[fdo_kv_offset(b, g, t, c, Hkv, d, L_cap, block_table, max_pages, page_size)]);
+        o[c] += p * (vc * vs);
+      }
+    }
+    for (int c = 0; c < d; ++c) o[c] /= l;
+    lse[row] = m + log(l);
+    free(s);
+  }
+  return failed ? -6 : 0;
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int fd_oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -420,11 +420,51 @@ def pin_causal_decimal(lib):
                                    rtol=1e-12, atol=1e-13)
 
 
+def pin_e4m3_decoding(lib):
+    """Every FP8 E4M3 code against torch's float8_e4m3fn -> float64 conversion (a library
+    routine), plus values fixed by the format: 0x38 = 1, 0x7E = 448 (largest finite),
+    0x01 = 2^-9 (smallest subnormal), 0x08 = 2^-6 (smallest normal), 0x7F = NaN."""
+    import torch
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_double(c, lib=lib) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    fixed = {0x38: 1.0, 0x7E: 448.0, 0x01: 2.0 ** -9, 0x08: 2.0 ** -6, 0xB8: -1.0, 0x00: 0.0}
+    for c, val in fixed.items():
+        assert oracle.e4m3_to_double(c, lib=lib) == val
+    assert math.isnan(oracle.e4m3_to_double(0x7F, lib=lib))
+
+
+def pin_kv8_equals_dequantised(lib):
+    """Decode over FP8 codes with per-head scales equals plain decode over the
+    dequantised cache (codes widened, times the scale, stored exactly in fp32)."""
+    import torch
+    rng = np.random.default_rng(21)
+    B, Hkv, G, d, L = 2, 2, 2, 16, 23
+    Hq = Hkv * G
+    q = rng.standard_normal((B, Hq, d)).astype(np.float32)
+    codes_k = rng.integers(0, 256, (B, Hkv, L, d), dtype=np.uint8)
+    codes_v = rng.integers(0, 256, (B, Hkv, L, d), dtype=np.uint8)
+    for c in (codes_k, codes_v):                       # no NaN codes (0x7F, 0xFF)
+        c[(c & 0x7F) == 0x7F] = 0x38
+    ks = np.array([0.5, 0.125], np.float32)
+    vs = np.array([0.25, 2.0], np.float32)
+    lens = np.array([L, 9], np.int32)
+    o, l = oracle.decode_kv8(q, codes_k, codes_v, ks, vs, lens, lib=lib)
+    deq = lambda c, sc: (torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+                         * sc[None, :, None, None]).astype(np.float32)
+    o2, l2 = oracle.decode(q, deq(codes_k, ks), deq(codes_v, vs), lens, lib=lib)
+    assert np.allclose(o, o2, rtol=1e-13, atol=1e-13) and np.allclose(l, l2, rtol=1e-13, atol=1e-13)
+
+
 ALL_PINS = [
     pin_softmax_examples, pin_worked_example, pin_closed_forms, pin_shift_invariance,
     pin_split_invariance, pin_brute_force_decimal, pin_torch_library,
     pin_paged_permutation, pin_gqa_map, pin_layout_transpose,
     pin_causal_reduces_to_decode, pin_causal_prefix_and_library, pin_causal_decimal,
+    pin_e4m3_decoding, pin_kv8_equals_dequantised,
 ]
 
 

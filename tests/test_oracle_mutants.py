@@ -36,6 +36,11 @@ MUTANTS = [
     ("causal_reversed", "const int64_t visible = (int64_t)seq_lens[b] - Q + 1 + j;",
      "const int64_t visible = (int64_t)seq_lens[b] - j;"),
     ("causal_token_index", "const int j = (int)((row / Hq) % Q);", "const int j = (int)(row % Q);"),
+    # The FP8 decoder and the scaled decode.
+    ("e4m3_bias", "mag = ldexp(1.0 + (double)m / 8.0, e - 7);", "mag = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    ("e4m3_subnormal", "mag = ldexp((double)m / 8.0, -6);", "mag = ldexp((double)m / 8.0, -7);"),
+    ("kv8_v_scale_from_k", "const double ks = (double)k_scale[g], vs = (double)v_scale[g];",
+     "const double ks = (double)k_scale[g], vs = (double)k_scale[g];"),
     ("causal_drops_scale", "      s[t] = dot * scale;\n    }\n    double m = s[0];\n    for (int64_t t = 1; t < visible;",
      "      s[t] = dot;\n    }\n    double m = s[0];\n    for (int64_t t = 1; t < visible;"),
 ]
