@@ -9,8 +9,9 @@ or fails to load, every call raises.
 from __future__ import annotations
 
 from ._binding import (  # noqa: F401
-    FD_MERGE_IN_KERNEL, FD_MERGE_KERNEL, FD_PATH_AUTO, FD_PATH_MMA, FD_PATH_SIMT, FdError, Plan, decode_attention,
-    decode_attention_noalloc, decode_partial, get_merge_mode, get_path, lib, library_path, merge_partials,
-    num_splits_for_lengths, num_splits_heuristic, read_device_error, resolve_num_splits, set_merge_mode, set_path, workspace_init,
-    workspace_partials, workspace_size,
+    FD_MERGE_IN_KERNEL, FD_MERGE_KERNEL, FD_PATH_AUTO, FD_PATH_MMA, FD_PATH_SIMT, FdError,
+    Plan, decode_attention, decode_attention_fp8kv, decode_attention_noalloc,
+    decode_partial, get_merge_mode, get_path, lib, library_path, merge_partials,
+    num_splits_for_lengths, num_splits_heuristic, read_device_error, resolve_num_splits,
+    set_merge_mode, set_path, workspace_init, workspace_partials, workspace_size,
 )

@@ -12,7 +12,7 @@ from . import build as _build
 
 FD_OK = 0
 FD_ERR_DEVICE_FLAG = 5
-FD_F32, FD_BF16, FD_I32 = 0, 1, 2
+FD_F32, FD_BF16, FD_I32, FD_F8E4M3 = 0, 1, 2, 3
 FD_PATH_AUTO, FD_PATH_SIMT, FD_PATH_MMA = 0, 1, 2
 FD_MERGE_KERNEL, FD_MERGE_IN_KERNEL = 0, 1
 
@@ -64,6 +64,8 @@ def _declare(L):
     L.fd_decode_attention.argtypes = [P, P, P, vp, P, i32, i32, P, vp, vp, sz, vp]
     L.fd_decode_attention_noalloc.restype = ctypes.c_int
     L.fd_decode_attention_noalloc.argtypes = [P, P, P, vp, P, i32, i32, P, vp, vp]
+    L.fd_decode_attention_fp8kv.restype = ctypes.c_int
+    L.fd_decode_attention_fp8kv.argtypes = [P, P, P, vp, vp, vp, P, i32, i32, P, vp, vp, sz, vp]
     L.fd_decode_partial.restype = ctypes.c_int
     L.fd_decode_partial.argtypes = [P, P, P, vp, P, i32, i32, vp, sz, vp]
     L.fd_workspace_partials.restype = ctypes.c_int
@@ -118,7 +120,8 @@ def _check(status: int):
         raise FdError(status, lib().fd_last_error().decode(errors="replace"))
 
 
-_DTYPES = {torch.float32: FD_F32, torch.bfloat16: FD_BF16, torch.int32: FD_I32}
+_DTYPES = {torch.float32: FD_F32, torch.bfloat16: FD_BF16, torch.int32: FD_I32,
+           torch.float8_e4m3fn: FD_F8E4M3}
 
 
 def tensor_desc(t: Optional[torch.Tensor]) -> Optional[FdTensor]:
@@ -254,6 +257,40 @@ def decode_attention_noalloc(q, k_cache, v_cache, seq_lens, out: torch.Tensor,
     _check(lib().fd_decode_attention_noalloc(
         ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), seq_lens.data_ptr(), _ref(dbt),
         page_size, num_splits, ctypes.byref(do), None if lse_out is None else lse_out.data_ptr(),
+        _stream_handle(stream)))
+    return out, lse_out
+
+
+def decode_attention_fp8kv(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           k_scale: Optional[torch.Tensor], v_scale: Optional[torch.Tensor],
+                           seq_lens: torch.Tensor, block_table: Optional[torch.Tensor] = None,
+                           page_size: int = 0, num_splits: int = 0,
+                           out: Optional[torch.Tensor] = None,
+                           lse_out: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None, out_dtype=None,
+                           stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """fd_decode_attention_fp8kv: k/v torch.float8_e4m3fn, per-kv-head f32 scales."""
+    L = lib()
+    if q.dim() == 4:
+        B, Qn, Hq, d = q.shape
+    else:
+        (B, Hq, d), Qn = q.shape, 1
+    Hkv = k_cache.shape[1]
+    S = resolve_num_splits(B, Hq, Hkv, d, _cap(k_cache, block_table, page_size), num_splits)
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
+    if lse_out is None:
+        lse_out = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.zeros(workspace_size(B, Qn * Hq, Hkv, d, S), dtype=torch.uint8,
+                                device=q.device)
+    dq, dk, dv, dbt, do = (tensor_desc(q), tensor_desc(k_cache), tensor_desc(v_cache),
+                           tensor_desc(block_table), tensor_desc(out))
+    ptr = lambda t: None if t is None else t.data_ptr()
+    _check(L.fd_decode_attention_fp8kv(
+        ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), ptr(k_scale), ptr(v_scale),
+        seq_lens.data_ptr(), _ref(dbt), page_size, S, ctypes.byref(do), lse_out.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         _stream_handle(stream)))
     return out, lse_out
 

@@ -44,7 +44,7 @@ int ilog2(int64_t x) {
   return r;
 }
 
-int esize(int32_t dtype) { return dtype == FD_BF16 ? 2 : 4; }
+int esize(int32_t dtype) { return dtype == FD_F8E4M3 ? 1 : (dtype == FD_BF16 ? 2 : 4); }
 
 // Workspace regions for given sizes: header (device flags) | LSE_i [B, Hq, S] |
 // O_i [B, Hq, S, d] | ticket counters [B, Hkv] (64-bit) of the fused merge; each region
@@ -142,8 +142,10 @@ fd_status make_kv_map(const fd_tensor* t, uint32_t box_rows, CUtensorMap* out) {
   const cuuint32_t box[5] = {(cuuint32_t)key.dims[0], box_rows, (cuuint32_t)key.dims[2], 1, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUtensorMap m;
-  CUresult r = enc(&m, t->dtype == FD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+  const CUtensorMapDataType ty = t->dtype == FD_BF16     ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : t->dtype == FD_F8E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUresult r = enc(&m, ty,
                    5, t->data, key.dims, key.strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -259,7 +261,9 @@ struct Prepared {
 fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor* v_cache,
                   const int32_t* seq_lens, const fd_tensor* block_table, int32_t page_size,
                   int32_t num_splits, const fd_tensor* out, float* lse_out, void* workspace,
-                  size_t workspace_bytes, bool need_out, Prepared* pr) {
+                  size_t workspace_bytes, bool need_out, Prepared* pr,
+                  bool kv8 = false, const float* k_scale = nullptr,
+                  const float* v_scale = nullptr) {
   // ---- presence and ranks
   if (!q || !k_cache || !v_cache || (need_out && !out))
     return fail(FD_ERR_INVALID_ARG, "q, k_cache, v_cache and out are required");
@@ -296,8 +300,19 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   if (Hq % Hkv != 0) return fail(FD_ERR_INVALID_ARG, "Hq (%lld) is not a multiple of Hkv (%lld)",
                                  (long long)Hq, (long long)Hkv);
   // ---- dtypes
-  if (k_cache->dtype != q->dtype || v_cache->dtype != q->dtype)
-    return fail(FD_ERR_INVALID_ARG, "q, k_cache and v_cache must share one dtype");
+  if (kv8) {
+    if (k_cache->dtype != FD_F8E4M3 || v_cache->dtype != FD_F8E4M3 || q->dtype != FD_BF16)
+      return fail(FD_ERR_INVALID_ARG, "the FP8 KV entry point takes bf16 q and fp8 e4m3 k/v");
+    if (q->shape[q->ndim - 1] != 128)
+      return fail(FD_ERR_UNSUPPORTED, "the FP8 KV cache needs head dim 128");
+    if ((k_scale && ((uintptr_t)k_scale & 3)) || (v_scale && ((uintptr_t)v_scale & 3)))
+      return fail(FD_ERR_INVALID_ARG, "scales must be 4-byte aligned");
+  } else {
+    if (k_cache->dtype == FD_F8E4M3 || v_cache->dtype == FD_F8E4M3)
+      return fail(FD_ERR_INVALID_ARG, "an FP8 KV cache goes through fd_decode_attention_fp8kv");
+    if (k_cache->dtype != q->dtype || v_cache->dtype != q->dtype)
+      return fail(FD_ERR_INVALID_ARG, "q, k_cache and v_cache must share one dtype");
+  }
   if (q->dtype != FD_BF16 && q->dtype != FD_F32)
     return fail(FD_ERR_UNSUPPORTED, "q/k/v dtype must be bf16 or f32");
   if (out && out->dtype != FD_F32 && !(out->dtype == FD_BF16 && q->dtype == FD_BF16))
@@ -309,7 +324,8 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   if (Q * G > 16)
     return fail(FD_ERR_UNSUPPORTED, "query tokens x group size = %lld exceeds 16 rows per kv head",
                 (long long)(Q * G));
-  const int es = esize(q->dtype);
+  const int es = esize(k_cache->dtype);              // KV element size (TMA, tiles)
+  const int qes = esize(q->dtype);
   // ---- strides and alignment (TMA: 16-byte base and strides; rows contiguous)
   if (q->stride[q->ndim - 1] != 1 || k_cache->stride[3] != 1 || v_cache->stride[3] != 1 ||
       (out && out->stride[out->ndim - 1] != 1))
@@ -317,7 +333,7 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   if (!aligned16(q->data) || !aligned16(k_cache->data) || !aligned16(v_cache->data))
     return fail(FD_ERR_INVALID_ARG, "q, k_cache and v_cache must be 16-byte aligned");
   for (int i = 0; i + 1 < q->ndim; ++i) {
-    if ((q->stride[i] * es) % 16) return fail(FD_ERR_INVALID_ARG, "q strides must be multiples of 16 bytes");
+    if ((q->stride[i] * qes) % 16) return fail(FD_ERR_INVALID_ARG, "q strides must be multiples of 16 bytes");
   }
   for (int i = 0; i < 3; ++i) {
     if ((k_cache->stride[i] * es) % 16 || (v_cache->stride[i] * es) % 16 || k_cache->stride[i] <= 0 ||
@@ -370,6 +386,8 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   if (path == FD_PATH_AUTO) path = q->dtype == FD_BF16 ? FD_PATH_MMA : FD_PATH_SIMT;
   if (path == FD_PATH_MMA && q->dtype != FD_BF16)
     return fail(FD_ERR_UNSUPPORTED, "the tensor-core path needs bf16 inputs");
+  if (kv8 && path != FD_PATH_MMA)
+    return fail(FD_ERR_UNSUPPORTED, "the FP8 KV cache runs on the tensor-core path only");
 
   // ---- tensor maps (box height: one tile, or one page when pages are shorter)
   const int TT = fd::tile_tokens((int)d, es);
@@ -418,6 +436,9 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   p.out_bf16 = out && out->dtype == FD_BF16 ? 1 : 0;
   p.lse_out = lse_out;
   p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
+  p.kv_fp8 = kv8 ? 1 : 0;
+  p.k_scale = kv8 ? k_scale : nullptr;
+  p.v_scale = kv8 ? v_scale : nullptr;
 
   pr->path = path;
   pr->dtype = q->dtype;
@@ -470,6 +491,23 @@ fd_status fd_decode_partial(const fd_tensor* q, const fd_tensor* k_cache,
   if (st != FD_OK) return st;
   pr.p.counters = nullptr;          // partials only: the merge is a separate call
   return launch_partial(pr, (cudaStream_t)stream);
+}
+
+fd_status fd_decode_attention_fp8kv(const fd_tensor* q, const fd_tensor* k_cache,
+                                   const fd_tensor* v_cache, const float* k_scale,
+                                   const float* v_scale, const int32_t* seq_lens,
+                                   const fd_tensor* block_table, int32_t page_size,
+                                   int32_t num_splits, fd_tensor* out, float* lse_out,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  Prepared pr;
+  fd_status st = prepare(q, k_cache, v_cache, seq_lens, block_table, page_size, num_splits, out,
+                         lse_out, workspace, workspace_bytes, true, &pr, true, k_scale, v_scale);
+  if (st != FD_OK) return st;
+  if (g_merge.load() == FD_MERGE_IN_KERNEL) return launch_partial(pr, (cudaStream_t)stream);
+  pr.p.counters = nullptr;
+  st = launch_partial(pr, (cudaStream_t)stream);
+  if (st != FD_OK) return st;
+  return launch_merge(pr.p, (cudaStream_t)stream);
 }
 
 fd_status fd_workspace_partials(void* workspace, int32_t B, int32_t Hq, int32_t d,

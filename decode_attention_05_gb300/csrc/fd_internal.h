@@ -54,6 +54,10 @@ struct Params {
   int32_t out_bf16;       // 1: bf16 out, 0: f32 out
   float* lse_out;         // [B, Q, Hq] or nullptr
   float scale_log2;       // log2(e) / sqrt(d): scores are kept in base-2 units inside kernels
+  // FP8 KV cache (E4M3 codes): per-kv-head dequantisation scales [Hkv] (nullptr = 1)
+  int32_t kv_fp8;
+  const float* k_scale;
+  const float* v_scale;
 };
 
 // Launchers (each returns the launch's cudaError_t).

@@ -22,6 +22,7 @@
 // exp(m_old - m_new); add exp(S - m_new) V), run inside one KV split of
 // Flash-Decoding (same section, "Flash-Decoding Split-K").
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "fd_epilogue.cuh"
 
@@ -29,13 +30,14 @@ namespace fd {
 
 namespace {
 
-template <int D_, int G_>
+template <int D_, int G_, bool KV8_ = false>
 struct MmaShape {
   static constexpr int D = D_;
   static constexpr int G = G_;
+  static constexpr bool KV8 = KV8_;                        // K/V stored as FP8 E4M3 codes
   static constexpr int NT = G > 8 ? 2 : 1;                 // n-tiles of 8 heads
-  static constexpr int ROW_BYTES = D * 2;
-  static constexpr int TT = kTileBytes / ROW_BYTES;        // 64 (d=128) or 128 (d=64)
+  static constexpr int ROW_BYTES = D * (KV8 ? 1 : 2);
+  static constexpr int TT = kTileBytes / ROW_BYTES;        // 64 (bf16 d=128), 128 (d=64 or fp8)
   static constexpr int LINES = ROW_BYTES / 128;
   static constexpr int NCW = 4;                            // consumer warps
   static constexpr int ROWS_PER_WARP = TT / NCW;           // 16 or 32
@@ -76,6 +78,37 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D = A . B + D, m16n8k16, f16 inputs, f32 accumulators (the FP8 KV path).
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two FP8 E4M3 codes (low byte -> low half) to an f16x2; exact (every E4M3 value is an
+// f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes_in_low_16) {
+  uint32_t y;
+  const uint16_t x = (uint16_t)(two_codes_in_low_16 & 0xffffu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(y) : "h"(x));
+  return y;
+}
+
+// Byte permute: bytes of {b:a} picked by the selector nibbles (prmt.b32).
+__device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // Pack two f32 into a bf16x2 (round to nearest even); `lo` goes to the low half.
@@ -128,6 +161,10 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
 
   // B fragments of Q^T (k = dim, n = head), bf16 as stored: b0 holds dims
   // 16 kk + qc, +1 of head nt * 8 + qr; b1 the same 8 dims further.  Heads >= G are 0.
+  // FP8 KV: the k index of the QK^T mma is a permutation of the dims (see the K
+  // fragments below): in a 16-dim step, fragment columns (2c, 2c+1) hold dims (4c, 4c+1)
+  // and columns (2c+8, 2c+9) hold dims (4c+2, 4c+3), c = lane % 4.  q is converted to
+  // f16 (exact for bf16 values in f16's range) with the same permutation.
   uint32_t qb[NT][SH::KSTEPS][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -138,7 +175,15 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
         q_offset(p, si.b, si.g, live ? h : 0));       // never address past the group
 #pragma unroll
     for (int kk = 0; kk < SH::KSTEPS; ++kk) {
-      const uint32_t lo = qrow[(kk * 16 + qc) / 2], hi = qrow[(kk * 16 + qc + 8) / 2];
+      uint32_t lo, hi;
+      if constexpr (SH::KV8) {
+        const uint32_t w0 = qrow[(kk * 16 + 2 * qc) / 2], w1 = qrow[(kk * 16 + 2 * qc + 2) / 2];
+        lo = pack_f16x2(bf16lo_to_f32(w0), bf16hi_to_f32(w0));
+        hi = pack_f16x2(bf16lo_to_f32(w1), bf16hi_to_f32(w1));
+      } else {
+        lo = qrow[(kk * 16 + qc) / 2];
+        hi = qrow[(kk * 16 + qc + 8) / 2];
+      }
       qb[nt][kk][0] = live ? lo : 0u;
       qb[nt][kk][1] = live ? hi : 0u;
     }
@@ -167,7 +212,10 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
 
   const int ps = p.page_size;
   const bool multi_page = ps > 0 && ps < TT;
-  const float sl2 = p.scale_log2;
+  // FP8 KV: per-kv-head dequantisation scales fold into the score scale and the output.
+  const float ksc = (SH::KV8 && p.k_scale != nullptr) ? p.k_scale[si.g] : 1.f;
+  const float vsc = (SH::KV8 && p.v_scale != nullptr) ? p.v_scale[si.g] : 1.f;
+  const float sl2 = p.scale_log2 * ksc;
   const uint32_t lb = (uint32_t)p.log2_box;
   bool aborted = false;
 
@@ -220,13 +268,34 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
       const int arow = rb + lr + (lm & 1) * 8;
+      if constexpr (SH::KV8) {
+        // A 16-byte chunk holds 16 dims: one ldmatrix.x4 (chunks c, c + 1, rows 0-7 and
+        // 8-15) feeds two k-steps.  A register holds dims 4c'..4c'+3 of one row; its low
+        // half gives fragment columns (2c', 2c'+1), its high half (2c'+8, 2c'+9).
 #pragma unroll
-      for (int kk = 0; kk < SH::KSTEPS; ++kk) {
-        const int c16 = kk * 2 + (lm >> 1);           // 16-byte chunk of the row
-        uint32_t a[4];
-        ldsm_x4(smem_addr(kt) + tile_chunk<SH::LINES>(arow, c16, lb), a);
+        for (int kk = 0; kk < SH::KSTEPS; kk += 2) {
+          const int c16 = kk + (lm >> 1);
+          uint32_t r[4];
+          ldsm_x4(smem_addr(kt) + tile_chunk<SH::LINES>(arow, c16, lb), r);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16(s[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t rr0 = r[2 * u], rr1 = r[2 * u + 1];
+            const uint32_t a[4] = {e4m3x2_to_f16x2(rr0), e4m3x2_to_f16x2(rr1),
+                                   e4m3x2_to_f16x2(rr0 >> 16), e4m3x2_to_f16x2(rr1 >> 16)};
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma_f16(s[nt], a, qb[nt][kk + u][0], qb[nt][kk + u][1]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < SH::KSTEPS; ++kk) {
+          const int c16 = kk * 2 + (lm >> 1);         // 16-byte chunk of the row
+          uint32_t a[4];
+          ldsm_x4(smem_addr(kt) + tile_chunk<SH::LINES>(arow, c16, lb), a);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16(s[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+        }
       }
       // ---- mask and scale: element e of s[nt] is (token rb + qr + 8 (e >> 1),
       //      head nt * 8 + qc + (e & 1)); excluded tokens get -inf.
@@ -279,19 +348,48 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
         l[nt][0] += pr[0] + pr[2];
         l[nt][1] += pr[1] + pr[3];
         // P rows (tokens qr, qr + 8) x heads (qc, qc + 1) -> transpose to P^T fragments.
-        pb[nt][0] = movmatrix_trans(pack_bf16x2(pr[0], pr[1]));
-        pb[nt][1] = movmatrix_trans(pack_bf16x2(pr[2], pr[3]));
+        if constexpr (SH::KV8) {                      // f16 P for the f16 PV mma
+          pb[nt][0] = movmatrix_trans(pack_f16x2(pr[0], pr[1]));
+          pb[nt][1] = movmatrix_trans(pack_f16x2(pr[2], pr[3]));
+        } else {
+          pb[nt][0] = movmatrix_trans(pack_bf16x2(pr[0], pr[1]));
+          pb[nt][1] = movmatrix_trans(pack_bf16x2(pr[2], pr[3]));
+        }
       }
       // ---- O^T += V^T . P^T  (A = V^T via ldmatrix.trans: matrix j covers tokens
       //      rb + 8 (j >> 1) .. +7 and dims 16 mt + 8 (j & 1) .. +7)
-      const int vrow_addr = rb + lr + (lm >> 1) * 8;
+      if constexpr (SH::KV8) {
+        // ldmatrix.trans over 16-bit pairs of codes: matrix j covers tokens
+        // rb + 8 (j & 1) .. +7 of chunk (m-tile) mt + (j >> 1); a register holds tokens
+        // (qc, qc+1) x dims (2 qr, 2 qr + 1).  Regrouped by dim (prmt) and widened, it
+        // gives the A fragment of V^T with m-row qr <-> dim 2 qr and m-row qr + 8 <->
+        // dim 2 qr + 1 of the 16-dim tile (undone when the output is written).
+        const int vtok_addr = rb + lr + (lm & 1) * 8;
 #pragma unroll
-      for (int mt = 0; mt < SH::MTILES; ++mt) {
-        const int c16 = mt * 2 + (lm & 1);
-        uint32_t a[4];
-        ldsm_x4_trans(smem_addr(vt) + tile_chunk<SH::LINES>(vrow_addr, c16, lb), a);
+        for (int mt = 0; mt < SH::MTILES; mt += 2) {
+          const int c16 = mt + (lm >> 1);
+          uint32_t r[4];
+          ldsm_x4_trans(smem_addr(vt) + tile_chunk<SH::LINES>(vtok_addr, c16, lb), r);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[nt][mt], a, pb[nt][0], pb[nt][1]);
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t x0 = byte_perm(r[2 * u], 0u, 0x3120u);       // tokens 0-7
+            const uint32_t x1 = byte_perm(r[2 * u + 1], 0u, 0x3120u);   // tokens 8-15
+            const uint32_t a[4] = {e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x0 >> 16),
+                                   e4m3x2_to_f16x2(x1), e4m3x2_to_f16x2(x1 >> 16)};
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16(acc[nt][mt + u], a, pb[nt][0], pb[nt][1]);
+          }
+        }
+      } else {
+        const int vrow_addr = rb + lr + (lm >> 1) * 8;
+#pragma unroll
+        for (int mt = 0; mt < SH::MTILES; ++mt) {
+          const int c16 = mt * 2 + (lm & 1);
+          uint32_t a[4];
+          ldsm_x4_trans(smem_addr(vt) + tile_chunk<SH::LINES>(vrow_addr, c16, lb), a);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[nt][mt], a, pb[nt][0], pb[nt][1]);
+        }
       }
     }
     __syncwarp();
@@ -325,8 +423,11 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
       if (h < p.n_rows) {
 #pragma unroll
         for (int mt = 0; mt < SH::MTILES; ++mt) {
-          macc[(warp * G + h) * SH::D + mt * 16 + qr] = acc[nt][mt][e];
-          macc[(warp * G + h) * SH::D + mt * 16 + qr + 8] = acc[nt][mt][2 + e];
+          // m-rows qr, qr + 8 of tile mt are dims 16 mt + (qr, qr + 8), or with FP8 KV
+          // dims 16 mt + (2 qr, 2 qr + 1); the V scale applies to the whole output.
+          const int d0 = SH::KV8 ? 2 * qr : qr, d1 = SH::KV8 ? 2 * qr + 1 : qr + 8;
+          macc[(warp * G + h) * SH::D + mt * 16 + d0] = acc[nt][mt][e] * vsc;
+          macc[(warp * G + h) * SH::D + mt * 16 + d1] = acc[nt][mt][2 + e] * vsc;
         }
         if (qr == 0) {
           mm[warp * G + h] = m[nt][e];
@@ -352,15 +453,15 @@ cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool KV8>
 cudaError_t dispatch_g(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                        cudaStream_t stream) {
   switch (rows_template(p.n_rows)) {   // query rows per (b, kv head), padded
-    case 1: return launch_mma<MmaShape<D, 1>>(p, tk, tv, stream);
-    case 2: return launch_mma<MmaShape<D, 2>>(p, tk, tv, stream);
-    case 4: return launch_mma<MmaShape<D, 4>>(p, tk, tv, stream);
-    case 8: return launch_mma<MmaShape<D, 8>>(p, tk, tv, stream);
-    case 16: return launch_mma<MmaShape<D, 16>>(p, tk, tv, stream);
+    case 1: return launch_mma<MmaShape<D, 1, KV8>>(p, tk, tv, stream);
+    case 2: return launch_mma<MmaShape<D, 2, KV8>>(p, tk, tv, stream);
+    case 4: return launch_mma<MmaShape<D, 4, KV8>>(p, tk, tv, stream);
+    case 8: return launch_mma<MmaShape<D, 8, KV8>>(p, tk, tv, stream);
+    case 16: return launch_mma<MmaShape<D, 16, KV8>>(p, tk, tv, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -369,8 +470,9 @@ cudaError_t dispatch_g(const Params& p, const CUtensorMap& tk, const CUtensorMap
 
 cudaError_t launch_partial_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream) {
-  if (p.d == 128) return dispatch_g<128>(p, tk, tv, stream);
-  if (p.d == 64) return dispatch_g<64>(p, tk, tv, stream);
+  if (p.kv_fp8) return p.d == 128 ? dispatch_g<128, true>(p, tk, tv, stream) : cudaErrorInvalidValue;
+  if (p.d == 128) return dispatch_g<128, false>(p, tk, tv, stream);
+  if (p.d == 64) return dispatch_g<64, false>(p, tk, tv, stream);
   return cudaErrorInvalidValue;
 }
 

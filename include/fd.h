@@ -70,7 +70,7 @@ typedef enum {
   FD_ERR_DEVICE_FLAG = 5           /* a kernel flagged bad device-side input (see below) */
 } fd_status;
 
-typedef enum { FD_F32 = 0, FD_BF16 = 1, FD_I32 = 2 } fd_dtype;
+typedef enum { FD_F32 = 0, FD_BF16 = 1, FD_I32 = 2, FD_F8E4M3 = 3 } fd_dtype;
 
 /*
  * A strided tensor view.  Strides are in ELEMENTS; the last dimension must be
@@ -138,6 +138,25 @@ FD_API fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cach
                               const fd_tensor* block_table, int32_t page_size,
                               int32_t num_splits, fd_tensor* out, float* lse_out,
                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fd_decode_attention_fp8kv -- fd_decode_attention over a KV cache stored as FP8 E4M3
+ * codes (fd_dtype FD_F8E4M3, one byte per element, same layouts), which halves the bytes
+ * a step reads.  The pages only name KV quantisation ([AI-Infra] 04 "summary": KV Quant
+ * among the KV-cache optimisations); the format read here: each kv head g has one fp32
+ * dequantisation scale for K and one for V, and an element's value is code * scale.
+ *   k_scale, v_scale  device f32 [Hkv] (4-byte aligned), or NULL for 1.0.
+ *   q bf16 [B, Hq, 128] or [B, Q, Hq, 128]; out bf16 or f32; head dim 128 only; runs on
+ *   the tensor-core path (FP8 pairs widened exactly to f16, q converted to f16, P fed as
+ *   f16, f32 accumulation).  Everything else as fd_decode_attention, merge mode included.
+ */
+FD_API fd_status fd_decode_attention_fp8kv(const fd_tensor* q, const fd_tensor* k_cache,
+                                           const fd_tensor* v_cache, const float* k_scale,
+                                           const float* v_scale, const int32_t* seq_lens,
+                                           const fd_tensor* block_table, int32_t page_size,
+                                           int32_t num_splits, fd_tensor* out, float* lse_out,
+                                           void* workspace, size_t workspace_bytes,
+                                           void* stream);
 
 /*
  * The two passes of fd_decode_attention as separate calls, for callers that time or

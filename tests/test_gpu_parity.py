@@ -484,3 +484,64 @@ def test_multi_token_limits():
     with pytest.raises(fd.FdError):
         fd.decode_attention(q, k, k, torch.tensor([64], dtype=torch.int32, device="cuda"),
                             num_splits=1)
+
+
+def _fp8_views(codes):
+    return codes.view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("case", ["contiguous", "paged16", "paged256", "gqa16"])
+def test_fp8_kv_cache(case):
+    """FP8 E4M3 KV cache with per-kv-head scales against the fp64 FP8 oracle (stale
+    slots hold NaN codes), several split counts, both merge modes."""
+    if case == "contiguous":
+        w = workloads.contiguous_case(4, 32, 8, 128, 3000, [3000, 1, 777, 2048], seed=301)
+    elif case == "gqa16":
+        w = workloads.contiguous_case(2, 32, 2, 128, 2000, [2000, 1500], seed=302)
+    else:
+        ps = 16 if case == "paged16" else 256
+        w = workloads.paged_case(4, 32, 8, 128, ps, 4096 // ps, [1, 37, 2500, 4096], seed=303)
+    kc, vc, ks, vs = workloads.fp8_quantize(w)
+    q, _, _, lens, bt, ps = w.oracle_arrays()
+    ref_o, ref_l = oracle.decode_kv8(q, _fp8_views(kc), _fp8_views(vc), ks.numpy(), vs.numpy(),
+                                     lens, block_table=bt, page_size=ps)
+    wd = w.to("cuda")
+    kcd, vcd, ksd, vsd = kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda()
+    for mode in (fd.FD_MERGE_KERNEL, fd.FD_MERGE_IN_KERNEL):
+        fd.set_merge_mode(mode)
+        for S in (1, 5, 32):
+            ws = torch.zeros(fd.workspace_size(w.B, w.Hq, w.Hkv, 128, S), dtype=torch.uint8,
+                             device="cuda")
+            o, l = fd.decode_attention_fp8kv(wd.q, kcd, vcd, ksd, vsd, wd.seq_lens,
+                                             wd.block_table, w.page_size, S, workspace=ws)
+            torch.cuda.synchronize()
+            assert fd.read_device_error(ws) == 0
+            check(w, o.float().cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
+
+
+def test_fp8_kv_multi_token():
+    """FP8 KV with multi-token queries: power-of-two scales make the dequantised cache
+    exact in fp32, so the fp64 multi-token oracle over it is the reference."""
+    Q = 2
+    w = workloads.contiguous_case(3, 32, 4, 128, 1500, [1500, 1, 900], seed=311)
+    kc, vc, ks, vs = workloads.fp8_quantize(w, power_of_two_scales=True)
+    deq = lambda c, s: (c.float() * s.view(1, -1, 1, 1)).numpy()
+    q4 = workloads.multi_token_queries(3, Q, 32, 128, seed=312)
+    ref_o, ref_l = oracle.decode_causal(q4.float().numpy(), deq(kc, ks), deq(vc, vs),
+                                        w.seq_lens.numpy())      # bf16 q is exact in fp32
+    o, l = fd.decode_attention_fp8kv(q4.cuda(), kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda(),
+                                     w.seq_lens.cuda(), num_splits=4, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    mw = workloads.Workload("mt8", q4.reshape(3 * Q, 32, 128), w.k, w.v, w.seq_lens)
+    check(mw, o.cpu().double().numpy().reshape(3 * Q, 32, 128), l.cpu().double().numpy().reshape(3 * Q, 32),
+          ref_o.reshape(3 * Q, 32, 128), ref_l.reshape(3 * Q, 32))
+
+
+def test_fp8_kv_is_refused_by_the_bf16_entry_point():
+    w = workloads.contiguous_case(1, 8, 1, 128, 64, seed=5).to("cuda")
+    kc = w.k.float().to(torch.float8_e4m3fn)
+    with pytest.raises(fd.FdError):
+        fd.decode_attention(w.q, kc, kc, w.seq_lens, num_splits=1)
+    with pytest.raises(fd.FdError):                   # CUDA-core path has no FP8 tile
+        fd.set_path(fd.FD_PATH_SIMT)
+        fd.decode_attention_fp8kv(w.q, kc, kc, None, None, w.seq_lens, num_splits=1)

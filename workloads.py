@@ -161,6 +161,28 @@ def np_storage(t: torch.Tensor) -> np.ndarray:
     return t.numpy()
 
 
+def fp8_quantize(w: Workload, power_of_two_scales: bool = False):
+    """An FP8 E4M3 copy of a workload's K and V with one scale per kv head for each:
+    scale = amax(|x|) of that head / 448 (the largest E4M3 value), codes = x / scale
+    rounded to E4M3 by torch.  NaN stale slots stay NaN codes.  With
+    `power_of_two_scales` the scales are rounded up to powers of two, so that
+    code * scale is exact in fp32.  Returns (k_codes, v_codes, k_scale, v_scale)."""
+    def quant(x):
+        x = x.float()
+        head_dim = 1                                   # [B|P, Hkv, rows, d]
+        amax = torch.nan_to_num(x.abs(), nan=0.0).amax(dim=(0, 2, 3)).clamp_min(1e-12)
+        scale = amax / 448.0
+        if power_of_two_scales:
+            scale = torch.exp2(torch.ceil(torch.log2(scale)))
+        shape = [1] * x.dim()
+        shape[head_dim] = -1
+        codes = (x / scale.view(shape)).to(torch.float8_e4m3fn)
+        return codes, scale.to(torch.float32)
+    kc, ks = quant(w.k)
+    vc, vs = quant(w.v)
+    return kc, vc, ks, vs
+
+
 def worked_example(d: int = 64) -> Workload:
     """The pages' counter-example as one fp32 attention row: q = 80 e_0, k_0 = k_1 = 0,
     k_2 = e_0 (scores [0, 0, 10] at scale 1/8); values 0, 0, 9 in every dim; S = 2,
