@@ -3,7 +3,8 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
 
 Workload (default): bf16, B=1, Hq=64, Hkv=8 (G=8), d=128, L=131072, contiguous KV
-cache (512 MiB of K+V, four times the L2), split count from the library heuristic.
+cache (512 MiB of K+V, four times the L2), split count from the library's length-aware
+planner (fd_num_splits_for_lengths).
 A step is one full pass of the hot path: the split-KV partial kernel plus the LSE
 merge kernel, through the C ABI (fd_decode_attention).
 
@@ -295,7 +296,11 @@ def run_fd(args):
     w_cpu = workloads.CONFIGS[args.config]()
     w = w_cpu.to("cuda")
     B, Hq, d, Hkv = w.B, w.Hq, w.d, w.Hkv
-    S = fd.resolve_num_splits(B, Hq, Hkv, d, w.L_cap, args.num_splits or w.num_splits)
+    S = args.num_splits or w.num_splits
+    if S == 0:          # the lengths are known here: plan with them
+        sms = torch.cuda.get_device_properties(local).multi_processor_count
+        S = fd.num_splits_for_lengths(B, Hq, Hkv, d, w.L_cap, w_cpu.seq_lens, sms,
+                                      page_size=w.page_size)
     ws = torch.zeros(fd.workspace_size(B, Hq, Hkv, d, S), dtype=torch.uint8, device="cuda")
     out = torch.empty((B, Hq, d), dtype=w.out_dtype, device="cuda")
     lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")

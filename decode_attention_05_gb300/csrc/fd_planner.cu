@@ -38,15 +38,17 @@ constexpr int kCtasPerSm = 2;             // residency of the partial kernels
 
 // Model constants, fitted on GB300 to this library's partial kernel: n CTAs streaming
 // at once reach BW(n) = kHbmBytesPerUs * (1 - exp(-n / tau)) together, shared equally.
-// Contiguous caches: tau = 113 (measured 1.8, 3.0, 4.7 TB/s at 32, 64, 128 CTAs; one
-// CTA alone ~72 GB/s; 7.0 TB/s is the read ceiling).  Paged caches issue one TMA box
+// Contiguous caches: tau = 95 (fitted to 32, 64 and 128 CTAs streaming 2048, 1024 and
+// 512 tokens each once their fixed time is taken out; one CTA alone ~72 GB/s; 7.0 TB/s
+// is the read ceiling).  Paged caches issue one TMA box
 // per page, so one CTA streams slower (~55 GB/s with pages of a tile or more, ~27 GB/s
 // with 16-token pages) and tau grows in proportion.
 constexpr double kHbmBytesPerUs = 7.0e6;
-constexpr double kSatCtasContig = 113.0;
+constexpr double kSatCtasContig = 95.0;
 constexpr double kOneCtaContig = 72.5e3;    // bytes per µs
 constexpr double kCtaFixedUs = 2.0;         // start-up + epilogue of one CTA
 constexpr double kMergeBytesPerUs = 1.0e5;  // merging a group's partials from L2
+constexpr double kMisalignedPenalty = 1.04;
 
 // One CTA's streaming rate (bytes per µs) for a page size (0 = contiguous cache).
 double one_cta_rate(int page_size, int tile) {
@@ -161,9 +163,14 @@ int32_t fd_num_splits_for_lengths(int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
   const int64_t S_cap = std::max<int64_t>(1, (L_cap + kMinSplitTokens - 1) / kMinSplitTokens);
   int best_S = 1;
   double best_t = plan_time(B, Hq, Hkv, d, L_cap, seq_lens, 1, slots, page_size);
+  if (L_cap % tile_tokens_bf16(d) != 0) best_t *= kMisalignedPenalty;
   for (int S : cand) {
     if (S == 1 || S > S_cap || S > kMaxSplits) continue;
-    const double t = plan_time(B, Hq, Hkv, d, L_cap, seq_lens, S, slots, page_size);
+    double t = plan_time(B, Hq, Hkv, d, L_cap, seq_lens, S, slots, page_size);
+    // A split that ends mid-tile makes two CTAs load its boundary tile and breaks the
+    // tiles' alignment; measured on the 128K workload it costs ~4% beyond the extra
+    // bytes the model already counts (S = 38: 83.3 us against 79.9 us at S = 32).
+    if (((L_cap + S - 1) / S) % tile_tokens_bf16(d) != 0) t *= kMisalignedPenalty;
     if (t < best_t * 0.995) {                 // a smaller count wins near-ties
       best_t = t;
       best_S = S;
