@@ -15,6 +15,7 @@ FD_ERR_DEVICE_FLAG = 5
 FD_F32, FD_BF16, FD_I32, FD_F8E4M3 = 0, 1, 2, 3
 FD_PATH_AUTO, FD_PATH_SIMT, FD_PATH_MMA = 0, 1, 2
 FD_MERGE_KERNEL, FD_MERGE_IN_KERNEL = 0, 1
+FD_SCHEDULE_AUTO, FD_SCHEDULE_GRID, FD_SCHEDULE_PERSISTENT, FD_SCHEDULE_HEAD_GROUPS = 0, 1, 2, 3
 
 _STATUS = {0: "FD_OK", 1: "FD_ERR_INVALID_ARG", 2: "FD_ERR_UNSUPPORTED",
            3: "FD_ERR_WORKSPACE_TOO_SMALL", 4: "FD_ERR_CUDA", 5: "FD_ERR_DEVICE_FLAG"}
@@ -105,6 +106,10 @@ def _declare(L):
     L.fd_set_merge_mode.argtypes = [i32]
     L.fd_get_merge_mode.restype = i32
     L.fd_get_merge_mode.argtypes = []
+    L.fd_set_schedule.restype = ctypes.c_int
+    L.fd_set_schedule.argtypes = [i32]
+    L.fd_get_schedule.restype = i32
+    L.fd_get_schedule.argtypes = []
     L.fd_get_path.restype = i32
     L.fd_get_path.argtypes = []
     L.fd_status_string.restype = ctypes.c_char_p
@@ -189,6 +194,14 @@ def set_merge_mode(mode: int):
 
 def get_merge_mode() -> int:
     return int(lib().fd_get_merge_mode())
+
+
+def set_schedule(schedule: int):
+    _check(lib().fd_set_schedule(schedule))
+
+
+def get_schedule() -> int:
+    return int(lib().fd_get_schedule())
 
 
 def workspace_init(ws: torch.Tensor, stream=None):

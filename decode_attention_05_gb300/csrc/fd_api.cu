@@ -20,6 +20,7 @@ namespace {
 thread_local char g_last_error[512] = "";
 std::atomic<int> g_path{FD_PATH_AUTO};
 std::atomic<int> g_merge{FD_MERGE_KERNEL};
+std::atomic<int> g_schedule{FD_SCHEDULE_AUTO};
 std::atomic<uint32_t> g_epoch{0x5eed0001u};   // per-call ticket epochs of the fused merge
 
 fd_status fail(fd_status st, const char* fmt, ...) {
@@ -31,7 +32,11 @@ fd_status fail(fd_status st, const char* fmt, ...) {
 }
 
 constexpr size_t kAlign = 256;
+// Header: device error flags (u32 at 0), the persistent schedule's item queue and
+// done counter (u64 at kQueueOff, kDoneOff; epoch-tagged like the merge tickets, so
+// they need no particular contents either).
 constexpr size_t kHeaderBytes = 256;
+constexpr size_t kQueueOff = 64, kDoneOff = 128;
 constexpr int32_t kMaxSplits = 4096;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -46,7 +51,7 @@ int ilog2(int64_t x) {
 
 int esize(int32_t dtype) { return dtype == FD_F8E4M3 ? 1 : (dtype == FD_BF16 ? 2 : 4); }
 
-// Workspace regions for given sizes: header (device flags) | LSE_i [B, Hq, S] |
+// Workspace regions for given sizes: header | LSE_i [B, Hq, S] |
 // O_i [B, Hq, S, d] | ticket counters [B, Hkv] (64-bit) of the fused merge; each region
 // 256-byte aligned.  The counters need no particular initial contents (take_ticket in
 // fd_epilogue.cuh), so one workspace serves calls of any sizes that fit it.
@@ -94,7 +99,7 @@ struct MapKey {
   int32_t dtype;
   uint64_t dims[5];
   uint64_t strides[4];
-  uint32_t box_rows;
+  uint32_t box_rows, box_heads;
   bool operator==(const MapKey& o) const { return memcmp(this, &o, sizeof *this) == 0; }
 };
 
@@ -108,7 +113,8 @@ MapCache& map_cache() {
   return c;
 }
 
-fd_status make_kv_map(const fd_tensor* t, uint32_t box_rows, CUtensorMap* out) {
+fd_status make_kv_map(const fd_tensor* t, uint32_t box_rows, uint32_t box_heads,
+                      CUtensorMap* out) {
   const int es = esize(t->dtype);
   const int d = (int)t->shape[3];
   MapKey key;
@@ -125,6 +131,7 @@ fd_status make_kv_map(const fd_tensor* t, uint32_t box_rows, CUtensorMap* out) {
   key.strides[2] = (uint64_t)t->stride[1] * es;
   key.strides[3] = (uint64_t)t->stride[0] * es;
   key.box_rows = box_rows;
+  key.box_heads = box_heads;
   MapCache& c = map_cache();
   {
     std::lock_guard<std::mutex> lock(c.mu);
@@ -137,9 +144,11 @@ fd_status make_kv_map(const fd_tensor* t, uint32_t box_rows, CUtensorMap* out) {
   }
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(FD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  // One box = `box_rows` token rows, all lines: it lands as [line][row][128 B], so the
-  // lines of one column slice of consecutive rows are consecutive 128-byte lines.
-  const cuuint32_t box[5] = {(cuuint32_t)key.dims[0], box_rows, (cuuint32_t)key.dims[2], 1, 1};
+  // One box = `box_rows` token rows, all lines, of `box_heads` consecutive kv heads: it
+  // lands as [head][line][row][128 B], so the lines of one column slice of consecutive
+  // rows are consecutive 128-byte lines.
+  const cuuint32_t box[5] = {(cuuint32_t)key.dims[0], box_rows, (cuuint32_t)key.dims[2],
+                             box_heads, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUtensorMap m;
   const CUtensorMapDataType ty = t->dtype == FD_BF16     ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -212,6 +221,16 @@ fd_status fd_set_merge_mode(int32_t mode) {
 
 int32_t fd_get_merge_mode(void) { return g_merge.load(); }
 
+fd_status fd_set_schedule(int32_t schedule) {
+  if (schedule != FD_SCHEDULE_AUTO && schedule != FD_SCHEDULE_GRID &&
+      schedule != FD_SCHEDULE_PERSISTENT && schedule != FD_SCHEDULE_HEAD_GROUPS)
+    return fail(FD_ERR_INVALID_ARG, "unknown schedule %d", schedule);
+  g_schedule.store(schedule);
+  return FD_OK;
+}
+
+int32_t fd_get_schedule(void) { return g_schedule.load(); }
+
 size_t fd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_splits) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || num_splits <= 0 || num_splits > kMaxSplits)
     return 0;
@@ -255,6 +274,7 @@ struct Prepared {
   CUtensorMap tk, tv;
   int path;
   int32_t dtype;
+  bool fused;   // the last CTA of each group merges it (FD_MERGE_IN_KERNEL with an output)
 };
 
 // Validate a decode call and resolve it.  `out` may be NULL (partial pass only).
@@ -389,12 +409,27 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   if (kv8 && path != FD_PATH_MMA)
     return fail(FD_ERR_UNSUPPORTED, "the FP8 KV cache runs on the tensor-core path only");
 
-  // ---- tensor maps (box height: one tile, or one page when pages are shorter)
+  // ---- schedule (fd_set_schedule).  The persistent and head-group kernels write only
+  // partials, so neither runs under the single-launch merge.
+  const bool fused = need_out && g_merge.load() == FD_MERGE_IN_KERNEL;
+  const int sched = g_schedule.load();
+  const int64_t items = (int64_t)S * Hkv * B;
+  const bool head_ok = path == FD_PATH_MMA && !kv8 && d == 128 && paged &&
+                       (page_size == 16 || page_size == 32) && Hkv % fd::kHeadGroup == 0 &&
+                       !fused;
+  const bool heads = head_ok && (sched == FD_SCHEDULE_AUTO || sched == FD_SCHEDULE_HEAD_GROUPS);
+  const bool persistent = !heads && path == FD_PATH_MMA && !fused &&
+                          (sched == FD_SCHEDULE_PERSISTENT);
+  (void)items;
+
+  // ---- tensor maps (box height: one tile, or one page when pages are shorter; with head
+  // groups 16 rows of kHeadGroup heads)
   const int TT = fd::tile_tokens((int)d, es);
-  const uint32_t box_rows = (uint32_t)(paged && page_size < TT ? page_size : TT);
-  fd_status st = make_kv_map(k_cache, box_rows, &pr->tk);
+  const uint32_t box_rows = heads ? 16u : (uint32_t)(paged && page_size < TT ? page_size : TT);
+  const uint32_t box_heads = heads ? (uint32_t)fd::kHeadGroup : 1u;
+  fd_status st = make_kv_map(k_cache, box_rows, box_heads, &pr->tk);
   if (st != FD_OK) return st;
-  st = make_kv_map(v_cache, box_rows, &pr->tv);
+  st = make_kv_map(v_cache, box_rows, box_heads, &pr->tv);
   if (st != FD_OK) return st;
 
   fd::Params& p = pr->p;
@@ -424,6 +459,8 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.flags = reinterpret_cast<uint32_t*>(ws);
   p.counters = reinterpret_cast<unsigned long long*>(ws + wl.cnt_off);
+  p.item_queue = reinterpret_cast<unsigned long long*>(ws + kQueueOff);
+  p.ctas_done = reinterpret_cast<unsigned long long*>(ws + kDoneOff);
   uint32_t epoch = g_epoch.fetch_add(1u);
   if (epoch == 0u) epoch = g_epoch.fetch_add(1u);   // 0 would match a zeroed word
   p.epoch = epoch;
@@ -440,8 +477,12 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   p.k_scale = kv8 ? k_scale : nullptr;
   p.v_scale = kv8 ? v_scale : nullptr;
 
+  p.persistent = persistent ? 1 : 0;
+  p.head_group = heads ? fd::kHeadGroup : 0;
+
   pr->path = path;
   pr->dtype = q->dtype;
+  pr->fused = fused;
   return FD_OK;
 }
 
@@ -474,7 +515,7 @@ fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
   // FD_MERGE_IN_KERNEL: one launch, the last CTA of each (b, kv head) group merges it.
   // FD_MERGE_KERNEL (default): the merge is its own kernel over (b, query head) rows,
   // launched with programmatic dependent launch behind the partial pass.
-  if (g_merge.load() == FD_MERGE_IN_KERNEL) return launch_partial(pr, (cudaStream_t)stream);
+  if (pr.fused) return launch_partial(pr, (cudaStream_t)stream);
   pr.p.counters = nullptr;
   st = launch_partial(pr, (cudaStream_t)stream);
   if (st != FD_OK) return st;
@@ -503,7 +544,7 @@ fd_status fd_decode_attention_fp8kv(const fd_tensor* q, const fd_tensor* k_cache
   fd_status st = prepare(q, k_cache, v_cache, seq_lens, block_table, page_size, num_splits, out,
                          lse_out, workspace, workspace_bytes, true, &pr, true, k_scale, v_scale);
   if (st != FD_OK) return st;
-  if (g_merge.load() == FD_MERGE_IN_KERNEL) return launch_partial(pr, (cudaStream_t)stream);
+  if (pr.fused) return launch_partial(pr, (cudaStream_t)stream);
   pr.p.counters = nullptr;
   st = launch_partial(pr, (cudaStream_t)stream);
   if (st != FD_OK) return st;

@@ -149,27 +149,6 @@ __device__ __forceinline__ void merge_group(const Params& p, int b, int g, int c
   }
 }
 
-// Take this CTA's ticket for its (b, kv head) group.  A counter word holds
-// (epoch << 32 | arrivals).  Each call brings a fresh epoch, so the first arrival of a
-// call restarts the count whatever the word held before (a workspace reused with other
-// sizes, stale data); the last arrival also puts the word back to 0, so a launch that
-// is replayed as is starts from a clean count too.  Lock-free: a failed compare-and-swap
-// means another CTA's succeeded.  Returns the arrival number (1 .. S), or 0 if the
-// bounded loop gave up (flagged).
-__device__ __forceinline__ unsigned take_ticket(const Params& p, unsigned long long* c) {
-  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(c);
-  for (int it = 0; it < (1 << 20); ++it) {
-    const unsigned long long want =
-        ((unsigned)(cur >> 32) == p.epoch) ? cur + 1ull
-                                           : (((unsigned long long)p.epoch << 32) | 1ull);
-    const unsigned long long prev = atomicCAS(c, cur, want);
-    if (prev == cur) return (unsigned)(want & 0xffffffffull);
-    cur = prev;
-  }
-  atomicOr(p.flags, kDevFlagTimeout);
-  return 0u;
-}
-
 // Called by the NCW * 32 consumer threads of a CTA after it has written its partials
 // (or its empty-split LSE).  `flag` is a shared-memory word.
 template <int D, int NCW>

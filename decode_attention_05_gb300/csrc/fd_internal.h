@@ -18,6 +18,8 @@ constexpr uint32_t kDevFlagTimeout = FD_DEVFLAG_TIMEOUT;
 // Bytes of one K (or V) tile in shared memory; the tile height in tokens is
 // kTileBytes / (d * element size): 64 tokens for bf16 d=128.
 constexpr int kTileBytes = 16384;
+// kv heads per CTA (and per TMA box) in the head-group tiling; one per consumer warp
+constexpr int kHeadGroup = 4;
 
 // Everything one decode call needs on the device, resolved by the host planner.
 struct Params {
@@ -46,6 +48,14 @@ struct Params {
                                   // the fused merge, or nullptr: the partial pass then
                                   // leaves the merge to a separate kernel
   uint32_t epoch;                 // this call's ticket epoch (never 0)
+  // Persistent schedule: work items (split, kv head, row) handed out by a queue word and
+  // a finished-CTA word in the workspace header (zero between launches, 64-bit)
+  int32_t persistent;
+  // Head-group tiles (kHeadGroup): a CTA serves kHeadGroup kv heads of a split and a
+  // tile is 16 tokens of one page x kHeadGroup heads, one TMA box; 0 = one head per CTA
+  int32_t head_group;
+  unsigned long long* item_queue;
+  unsigned long long* ctas_done;
   float* lse_part;        // [B, Q, Hq, S]     natural-log LSE_i, -inf for an empty split
   float* o_part;          // [B, Q, Hq, S, d]  normalised partial output O_i
   // outputs

@@ -30,7 +30,7 @@ namespace fd {
 
 namespace {
 
-template <int D_, int G_, bool KV8_ = false>
+template <int D_, int G_, bool KV8_ = false, bool PERSIST_ = false>
 struct MmaShape {
   static constexpr int D = D_;
   static constexpr int G = G_;
@@ -44,12 +44,20 @@ struct MmaShape {
   static constexpr int CHUNKS = ROWS_PER_WARP / 16;        // 16-token chunks per warp per tile
   static constexpr int KSTEPS = D / 16;                    // k-steps of the QK^T product
   static constexpr int MTILES = D / 16;                    // m-tiles of the PV product
+  // Persistent schedule: the same two CTAs per SM, each taking items from a queue; an
+  // item's epilogue uses the ring stage of its last tile as merge scratch (the other
+  // stages, and the other CTA of the SM, keep streaming meanwhile).
+  static constexpr bool PERSIST = PERSIST_;
   static constexpr int STAGES = 3;
   static constexpr int THREADS = (NCW + 1) * 32;
   static constexpr int MERGE_BYTES = NCW * G * D * 4 + 2 * NCW * G * 4;
   static_assert(MERGE_BYTES <= STAGES * 2 * kTileBytes, "merge scratch fits the stages");
+  static_assert(NCW * G * D * 4 <= 2 * kTileBytes && NCW * G <= 64,
+                "persistent merge scratch fits one stage and the control block");
+  static constexpr size_t RING_BYTES = (size_t)STAGES * 2 * kTileBytes;
   static constexpr size_t SMEM_BYTES =
-      1024 + (size_t)STAGES * 2 * kTileBytes + sizeof(PipeCtl<STAGES>);
+      1024 + RING_BYTES + (PERSIST ? sizeof(PersistCtl<STAGES>) : sizeof(PipeCtl<STAGES>));
+  static_assert(2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -117,139 +125,83 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// Per-consumer-warp state and tile math of the tensor-core partial pass: the query
+// fragments of one (b, kv head) group, the online-softmax state (m, l) and the O^T
+// accumulator of this warp's share of the tokens.  Used per split by the grid and
+// head-group kernels and per work item by the persistent kernel.
 template <class SH>
-__global__ void __launch_bounds__(SH::THREADS, 2)
-    fd_partial_mma_kernel(const __grid_constant__ CUtensorMap tk,
-                          const __grid_constant__ CUtensorMap tv,
-                          const __grid_constant__ Params p) {
-  constexpr int G = SH::G, NT = SH::NT, TT = SH::TT, STAGES = SH::STAGES;
-  const SplitInfo si = split_info<TT>(p);
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* stages = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  auto* ctl = reinterpret_cast<PipeCtl<STAGES>*>(stages + (size_t)STAGES * 2 * kTileBytes);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (si.n_tiles == 0) {            // empty split: weight 0 in the merge, nothing to load
-    write_empty_split(p, si, threadIdx.x);
-    pdl_trigger();
-    if (p.counters != nullptr && warp < SH::NCW)
-      arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
-    return;
-  }
+struct Consumer {
+  static constexpr int NT = SH::NT;
+  uint32_t qb[NT][SH::KSTEPS][2];  // Q^T B-fragments
+  int64_t lim[NT][2];              // causal key bound of this thread's two columns per n-tile
+  float m[NT][2], l[NT][2];        // per column (query row nt * 8 + qc + {0, 1})
+  float acc[NT][SH::MTILES][4];    // O^T fragments
+  float sl2, vsc;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_addr(&ctl->full[s]), 1);
-      mbar_init(smem_addr(&ctl->empty[s]), SH::NCW);
-    }
-    ctl->abort = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (warp == SH::NCW) {            // ---------------- producer warp
-    prefetch_tensormap(&tk);
-    prefetch_tensormap(&tv);
-    produce_tiles<TT, STAGES>(p, si, &tk, &tv, stages, ctl, lane);
-    pdl_trigger();
-    return;
-  }
-
-  // ---------------------------------------------------- consumer warps
-  const int qr = lane >> 2;         // "group" row of the mma fragments (0..7)
-  const int qc = (lane & 3) * 2;    // first of the two fragment columns
-
-  // B fragments of Q^T (k = dim, n = head), bf16 as stored: b0 holds dims
-  // 16 kk + qc, +1 of head nt * 8 + qr; b1 the same 8 dims further.  Heads >= G are 0.
-  // FP8 KV: the k index of the QK^T mma is a permutation of the dims (see the K
-  // fragments below): in a 16-dim step, fragment columns (2c, 2c+1) hold dims (4c, 4c+1)
-  // and columns (2c+8, 2c+9) hold dims (4c+2, 4c+3), c = lane % 4.  q is converted to
-  // f16 (exact for bf16 values in f16's range) with the same permutation.
-  uint32_t qb[NT][SH::KSTEPS][2];
+  // Load the group's query fragments and reset the state.
+  //   B fragments of Q^T (k = dim, n = row), bf16 as stored: b0 holds dims 16 kk + qc,
+  //   +1 of row nt * 8 + qr; b1 the same 8 dims further.  Rows >= n_rows are 0.
+  //   FP8 KV: the k index of the QK^T mma is a permutation of the dims (see tile()): in
+  //   a 16-dim step, fragment columns (2c, 2c+1) hold dims (4c, 4c+1) and columns
+  //   (2c+8, 2c+9) hold dims (4c+2, 4c+3), c = lane % 4.  q is converted to f16 (exact
+  //   for bf16 values in f16's range) with the same permutation.
+  __device__ __forceinline__ void start(const Params& p, int b, int g, int64_t L, int lane) {
+    const int qr = lane >> 2, qc = (lane & 3) * 2;
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int h = nt * 8 + qr;                        // query row of the group
-    const bool live = h < p.n_rows;
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-        reinterpret_cast<const __nv_bfloat16*>(p.q) +
-        q_offset(p, si.b, si.g, live ? h : 0));       // never address past the group
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = nt * 8 + qr;
+      const bool live = h < p.n_rows;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          reinterpret_cast<const __nv_bfloat16*>(p.q) +
+          q_offset(p, b, g, live ? h : 0));           // never address past the group
 #pragma unroll
-    for (int kk = 0; kk < SH::KSTEPS; ++kk) {
-      uint32_t lo, hi;
-      if constexpr (SH::KV8) {
-        const uint32_t w0 = qrow[(kk * 16 + 2 * qc) / 2], w1 = qrow[(kk * 16 + 2 * qc + 2) / 2];
-        lo = pack_f16x2(bf16lo_to_f32(w0), bf16hi_to_f32(w0));
-        hi = pack_f16x2(bf16lo_to_f32(w1), bf16hi_to_f32(w1));
-      } else {
-        lo = qrow[(kk * 16 + qc) / 2];
-        hi = qrow[(kk * 16 + qc + 8) / 2];
+      for (int kk = 0; kk < SH::KSTEPS; ++kk) {
+        uint32_t lo, hi;
+        if constexpr (SH::KV8) {
+          const uint32_t w0 = qrow[(kk * 16 + 2 * qc) / 2], w1 = qrow[(kk * 16 + 2 * qc + 2) / 2];
+          lo = pack_f16x2(bf16lo_to_f32(w0), bf16hi_to_f32(w0));
+          hi = pack_f16x2(bf16lo_to_f32(w1), bf16hi_to_f32(w1));
+        } else {
+          lo = qrow[(kk * 16 + qc) / 2];
+          hi = qrow[(kk * 16 + qc + 8) / 2];
+        }
+        qb[nt][kk][0] = live ? lo : 0u;
+        qb[nt][kk][1] = live ? hi : 0u;
       }
-      qb[nt][kk][0] = live ? lo : 0u;
-      qb[nt][kk][1] = live ? hi : 0u;
+      lim[nt][0] = key_bound(p, L, nt * 8 + qc);
+      lim[nt][1] = key_bound(p, L, nt * 8 + qc + 1);
+      m[nt][0] = m[nt][1] = kNegInf;
+      l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < SH::MTILES; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][mt][e] = 0.f;
     }
-  }
-  // Causal key bound of this thread's two fragment columns (rows nt * 8 + qc + {0, 1}).
-  int64_t lim[NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    lim[nt][0] = key_bound(p, si.L, nt * 8 + qc);
-    lim[nt][1] = key_bound(p, si.L, nt * 8 + qc + 1);
+    // FP8 KV: per-kv-head dequantisation scales fold into the score scale and output.
+    const float ksc = (SH::KV8 && p.k_scale != nullptr) ? p.k_scale[g] : 1.f;
+    vsc = (SH::KV8 && p.v_scale != nullptr) ? p.v_scale[g] : 1.f;
+    sl2 = p.scale_log2 * ksc;
   }
 
-  // Per-thread softmax state for heads nt * 8 + qc + {0, 1}; acc = O^T fragments:
-  // acc[nt][mt] = {(dim 16 mt + qr, head qc), (.., qc + 1), (dim + 8, qc), (.., qc + 1)}.
-  float m[NT][2], l[NT][2];
-  float acc[NT][SH::MTILES][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    m[nt][0] = m[nt][1] = kNegInf;
-    l[nt][0] = l[nt][1] = 0.f;
-#pragma unroll
-    for (int mt = 0; mt < SH::MTILES; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[nt][mt][e] = 0.f;
-  }
-
-  const int ps = p.page_size;
-  const bool multi_page = ps > 0 && ps < TT;
-  // FP8 KV: per-kv-head dequantisation scales fold into the score scale and the output.
-  const float ksc = (SH::KV8 && p.k_scale != nullptr) ? p.k_scale[si.g] : 1.f;
-  const float vsc = (SH::KV8 && p.v_scale != nullptr) ? p.v_scale[si.g] : 1.f;
-  const float sl2 = p.scale_log2 * ksc;
-  const uint32_t lb = (uint32_t)p.log2_box;
-  bool aborted = false;
-
-  // ldmatrix row addresses: lane i serves matrix i / 8, row i % 8.
-  const int lm = lane >> 3, lr = lane & 7;
-
-  for (int n = 0; n < si.n_tiles; ++n) {
-    const int stage = n % STAGES;
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(smem_addr(&ctl->full[stage]), (n / STAGES) & 1);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) {
-      if (lane == 0) {
-        ctl->abort = 1;
-        atomicOr(p.flags, kDevFlagTimeout);
-      }
-      aborted = true;
-      break;
-    }
-    uint8_t* kt = stages + (size_t)stage * 2 * kTileBytes;
-    uint8_t* vt = kt + kTileBytes;
-    const uint32_t bad = ctl->bad[stage];
-    const int64_t t0 = si.T0 + (int64_t)n * TT;
+  // One K/V tile in shared memory: this warp's ROWS_PER_WARP token rows of it.
+  // Valid tokens are [lo, hi) minus invalid pages (`bad`); each query row also keeps
+  // only keys below its causal bound.
+  __device__ __forceinline__ void tile(const Params& p, uint8_t* kt, uint8_t* vt, int64_t t0,
+                                       int64_t lo, int64_t hi, uint32_t bad, int warp, int lane,
+                                       uint32_t lb, bool multi_page) {
+    const int qr = lane >> 2;
+    const int lm = lane >> 3, lr = lane & 7;          // ldmatrix: matrix i / 8, row i % 8
     const int r0 = warp * SH::ROWS_PER_WARP;          // this warp's first row in the tile
 
     // Rows outside [lo, hi) or on an invalid page: their V rows may be stale (NaN) and
     // 0 * NaN is NaN inside the MMA, so zero them before use.  Only boundary tiles.
-    const bool clean = t0 + r0 >= si.lo && t0 + r0 + SH::ROWS_PER_WARP <= si.hi && bad == 0;
+    const bool clean = t0 + r0 >= lo && t0 + r0 + SH::ROWS_PER_WARP <= hi && bad == 0;
     if (!clean) {
       for (int r = 0; r < SH::ROWS_PER_WARP; ++r) {
         const int row = r0 + r;
         const int64_t tok = t0 + row;
         const int pslot = multi_page ? (row >> p.log2_page) : 0;
-        const bool valid = tok >= si.lo && tok < si.hi && !((bad >> pslot) & 1u);
+        const bool valid = tok >= lo && tok < hi && !((bad >> pslot) & 1u);
         if (!valid) {
           for (int c = lane; c < SH::ROW_BYTES / 16; c += 32)
             *reinterpret_cast<uint4*>(vt + tile_chunk<SH::LINES>(row, c, lb)) = make_uint4(0, 0, 0, 0);
@@ -298,7 +250,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
         }
       }
       // ---- mask and scale: element e of s[nt] is (token rb + qr + 8 (e >> 1),
-      //      head nt * 8 + qc + (e & 1)); excluded tokens get -inf.
+      //      row nt * 8 + qc + (e & 1)); excluded tokens get -inf.
       bool vrow[2];
       int64_t vtok[2];
 #pragma unroll
@@ -306,7 +258,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
         const int row = rb + qr + 8 * hh;
         const int64_t tok = t0 + row;
         const int pslot = multi_page ? (row >> p.log2_page) : 0;
-        vrow[hh] = tok >= si.lo && tok < si.hi && !((bad >> pslot) & 1u);
+        vrow[hh] = tok >= lo && tok < hi && !((bad >> pslot) & 1u);
         vtok[hh] = tok;
       }
       uint32_t pb[NT][2];                             // P^T fragments (b0/b1 of the PV mma)
@@ -316,7 +268,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           x[e] = (vrow[e >> 1] && vtok[e >> 1] < lim[nt][e & 1]) ? s[nt][e] * sl2 : kNegInf;
-        // chunk max per head over the 16 tokens: in-thread pair, then lanes of equal qc
+        // chunk max per column over the 16 tokens: in-thread pair, then lanes of equal qc
         float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -347,7 +299,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
         }
         l[nt][0] += pr[0] + pr[2];
         l[nt][1] += pr[1] + pr[3];
-        // P rows (tokens qr, qr + 8) x heads (qc, qc + 1) -> transpose to P^T fragments.
+        // P rows (tokens qr, qr + 8) x columns (qc, qc + 1) -> transpose to P^T fragments.
         if constexpr (SH::KV8) {                      // f16 P for the f16 PV mma
           pb[nt][0] = movmatrix_trans(pack_f16x2(pr[0], pr[1]));
           pb[nt][1] = movmatrix_trans(pack_f16x2(pr[2], pr[3]));
@@ -356,8 +308,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
           pb[nt][1] = movmatrix_trans(pack_bf16x2(pr[2], pr[3]));
         }
       }
-      // ---- O^T += V^T . P^T  (A = V^T via ldmatrix.trans: matrix j covers tokens
-      //      rb + 8 (j >> 1) .. +7 and dims 16 mt + 8 (j & 1) .. +7)
+      // ---- O^T += V^T . P^T
       if constexpr (SH::KV8) {
         // ldmatrix.trans over 16-bit pairs of codes: matrix j covers tokens
         // rb + 8 (j & 1) .. +7 of chunk (m-tile) mt + (j >> 1); a register holds tokens
@@ -381,6 +332,8 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
           }
         }
       } else {
+        // A = V^T via ldmatrix.trans: matrix j covers tokens rb + 8 (j >> 1) .. +7 and
+        // dims 16 mt + 8 (j & 1) .. +7.
         const int vrow_addr = rb + lr + (lm >> 1) * 8;
 #pragma unroll
         for (int mt = 0; mt < SH::MTILES; ++mt) {
@@ -392,6 +345,144 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
         }
       }
     }
+  }
+
+  // End of a split: sum l over the 8 lanes that share a column (they saw different
+  // tokens) and write this warp's (m, l, acc) into the merge scratch
+  // macc [NCW][G][D], mm [NCW][G], ml [NCW][G].
+  __device__ __forceinline__ void store(const Params& p, float* macc, float* mm, float* ml,
+                                        int warp, int lane) {
+    constexpr int G = SH::G;
+    const int qr = lane >> 2, qc = (lane & 3) * 2;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
+        l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
+      }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int h = nt * 8 + qc + e;
+        if (h < p.n_rows) {
+#pragma unroll
+          for (int mt = 0; mt < SH::MTILES; ++mt) {
+            // m-rows qr, qr + 8 of tile mt are dims 16 mt + (qr, qr + 8), or with FP8 KV
+            // dims 16 mt + (2 qr, 2 qr + 1); the V scale applies to the whole output.
+            const int d0 = SH::KV8 ? 2 * qr : qr, d1 = SH::KV8 ? 2 * qr + 1 : qr + 8;
+            macc[(warp * G + h) * SH::D + mt * 16 + d0] = acc[nt][mt][e] * vsc;
+            macc[(warp * G + h) * SH::D + mt * 16 + d1] = acc[nt][mt][2 + e] * vsc;
+          }
+          if (qr == 0) {
+            mm[warp * G + h] = m[nt][e];
+            ml[warp * G + h] = l[nt][e];
+          }
+        }
+      }
+    }
+  }
+
+  // End of a split when this warp alone saw all of it (head-group tiles: one warp per kv
+  // head): write O_i = acc / l and LSE_i = (m + log2 l) ln 2 of the warp's rows directly,
+  // the single-warp case of merge_warps_and_store.
+  __device__ __forceinline__ void store_own(const Params& p, int b, int g, int split, int lane) {
+    const int qr = lane >> 2, qc = (lane & 3) * 2;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
+        l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
+      }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int h = nt * 8 + qc + e;
+        if (h >= p.n_rows) continue;
+        const int64_t row = flat_row(p, b, g, h);
+        const float L = l[nt][e];
+        if (L > 0.f) {
+          float* o = p.o_part + (row * p.S + split) * SH::D;
+#pragma unroll
+          for (int mt = 0; mt < SH::MTILES; ++mt) {
+            const int d0 = SH::KV8 ? 2 * qr : qr, d1 = SH::KV8 ? 2 * qr + 1 : qr + 8;
+            o[mt * 16 + d0] = acc[nt][mt][e] * vsc / L;
+            o[mt * 16 + d1] = acc[nt][mt][2 + e] * vsc / L;
+          }
+          if (qr == 0) p.lse_part[row * p.S + split] = (m[nt][e] + lg2_approx(L)) * 0.6931471805599453f;
+        } else if (qr == 0) {
+          p.lse_part[row * p.S + split] = kNegInf;
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------- grid schedule
+// One CTA per (split, kv head, row); two CTAs per SM.
+template <class SH>
+__global__ void __launch_bounds__(SH::THREADS, 2)
+    fd_partial_mma_kernel(const __grid_constant__ CUtensorMap tk,
+                          const __grid_constant__ CUtensorMap tv,
+                          const __grid_constant__ Params p) {
+  constexpr int G = SH::G, TT = SH::TT, STAGES = SH::STAGES;
+  const SplitInfo si = split_info<TT>(p);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  auto* ctl = reinterpret_cast<PipeCtl<STAGES>*>(stages + SH::RING_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (si.n_tiles == 0) {            // empty split: weight 0 in the merge, nothing to load
+    write_empty_split(p, si, threadIdx.x);
+    pdl_trigger();
+    if (p.counters != nullptr && warp < SH::NCW)
+      arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_addr(&ctl->full[s]), 1);
+      mbar_init(smem_addr(&ctl->empty[s]), SH::NCW);
+    }
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == SH::NCW) {            // ---------------- producer warp
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+    produce_tiles<TT, STAGES>(p, si, &tk, &tv, stages, ctl, lane);
+    pdl_trigger();
+    return;
+  }
+
+  // ---------------------------------------------------- consumer warps
+  Consumer<SH> c;
+  c.start(p, si.b, si.g, si.L, lane);
+  const bool multi_page = p.page_size > 0 && p.page_size < TT;
+  const uint32_t lb = (uint32_t)p.log2_box;
+  bool aborted = false;
+  for (int n = 0; n < si.n_tiles; ++n) {
+    const int stage = n % STAGES;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(smem_addr(&ctl->full[stage]), (n / STAGES) & 1);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) {
+        ctl->abort = 1;
+        atomicOr(p.flags, kDevFlagTimeout);
+      }
+      aborted = true;
+      break;
+    }
+    uint8_t* kt = stages + (size_t)stage * 2 * kTileBytes;
+    c.tile(p, kt, kt + kTileBytes, si.T0 + (int64_t)n * TT, si.lo, si.hi, ctl->bad[stage], warp,
+           lane, lb, multi_page);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
   }
@@ -403,77 +494,266 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
     if (p.counters != nullptr) arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
     return;
   }
-
-  // l: sum over the 8 lanes that share qc (they saw different tokens).
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
-      l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
-    }
-  float* macc = reinterpret_cast<float*>(stages);                 // [NCW][G][D]
+  float* macc = reinterpret_cast<float*>(stages);                 // [NCW][G][D], ring drained
   float* mm = macc + SH::NCW * G * SH::D;                         // [NCW][G]
   float* ml = mm + SH::NCW * G;                                   // [NCW][G]
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int h = nt * 8 + qc + e;
-      if (h < p.n_rows) {
-#pragma unroll
-        for (int mt = 0; mt < SH::MTILES; ++mt) {
-          // m-rows qr, qr + 8 of tile mt are dims 16 mt + (qr, qr + 8), or with FP8 KV
-          // dims 16 mt + (2 qr, 2 qr + 1); the V scale applies to the whole output.
-          const int d0 = SH::KV8 ? 2 * qr : qr, d1 = SH::KV8 ? 2 * qr + 1 : qr + 8;
-          macc[(warp * G + h) * SH::D + mt * 16 + d0] = acc[nt][mt][e] * vsc;
-          macc[(warp * G + h) * SH::D + mt * 16 + d1] = acc[nt][mt][2 + e] * vsc;
-        }
-        if (qr == 0) {
-          mm[warp * G + h] = m[nt][e];
-          ml[warp * G + h] = l[nt][e];
-        }
-      }
-    }
-  }
+  c.store(p, macc, mm, ml, warp, lane);
   named_bar_sync(1, SH::NCW * 32);
   merge_warps_and_store<G, SH::D, SH::NCW>(p, si, macc, mm, ml, threadIdx.x);
   if (p.counters != nullptr) arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
 }
 
+// ---------------------------------------------------------------- head-group tiles
+// One CTA per (split, group of kHeadGroup kv heads, row).  A tile is 16 tokens of one
+// page for the group's kHeadGroup heads: one TMA box of 16 rows x kHeadGroup heads
+// (16 KB) per K and V, laid out [head][line][row][128 B] -- the same shared-memory
+// layout as kHeadGroup page boxes of 16 rows, so the consumer's addressing is
+// unchanged: consumer warp w reads tile rows 16 w .. 16 w + 15, which are head
+// g0 + w's 16 tokens.  Each warp therefore sees every token of its own head in the
+// split and writes that head's partial itself; no cross-warp merge.
+template <class SH>
+__global__ void __launch_bounds__(SH::THREADS, 2)
+    fd_partial_heads_kernel(const __grid_constant__ CUtensorMap tk,
+                            const __grid_constant__ CUtensorMap tv,
+                            const __grid_constant__ Params p) {
+  constexpr int STAGES = SH::STAGES, TOK = 16;
+  static_assert(SH::ROWS_PER_WARP == TOK && SH::CHUNKS == 1 && SH::NCW == kHeadGroup,
+                "one 16-token page slice per consumer warp");
+  SplitInfo si = split_info<TOK>(p);
+  si.g = blockIdx.y * kHeadGroup;                 // first kv head of the group
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  auto* ctl = reinterpret_cast<PipeCtl<STAGES>*>(stages + SH::RING_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (si.n_tiles == 0) {            // empty split for every head of the group
+    for (int i = threadIdx.x; i < kHeadGroup * p.n_rows; i += blockDim.x)
+      p.lse_part[flat_row(p, si.b, si.g + i / p.n_rows, i % p.n_rows) * p.S + si.split] = kNegInf;
+    pdl_trigger();
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_addr(&ctl->full[s]), 1);
+      mbar_init(smem_addr(&ctl->empty[s]), SH::NCW);
+    }
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == SH::NCW) {            // producer: one 16-row box of the group per K and V
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+    produce_tiles<TOK, STAGES>(p, si, &tk, &tv, stages, ctl, lane);
+    pdl_trigger();
+    return;
+  }
+
+  const int g = si.g + warp;        // this warp's kv head
+  Consumer<SH> c;
+  c.start(p, si.b, g, si.L, lane);
+  const int r0 = warp * TOK;
+  bool aborted = false;
+  for (int n = 0; n < si.n_tiles; ++n) {
+    const int stage = n % STAGES;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(smem_addr(&ctl->full[stage]), (n / STAGES) & 1);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) {
+        ctl->abort = 1;
+        atomicOr(p.flags, kDevFlagTimeout);
+      }
+      aborted = true;
+      break;
+    }
+    uint8_t* kt = stages + (size_t)stage * 2 * kTileBytes;
+    // Row r0 + i of the tile is token t0 + i of head g: pass the row-0 token as t0 - r0.
+    const int64_t t0 = si.T0 + (int64_t)n * TOK;
+    c.tile(p, kt, kt + kTileBytes, t0 - r0, si.lo, si.hi, ctl->bad[stage], warp, lane,
+           (uint32_t)p.log2_box, false);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
+  }
+  pdl_trigger();
+  if (aborted || *reinterpret_cast<volatile int32_t*>(&ctl->abort)) {
+    if (lane < p.n_rows) p.lse_part[flat_row(p, si.b, g, lane) * p.S + si.split] = kNegInf;
+    return;
+  }
+  c.store_own(p, si.b, g, si.split, lane);
+}
+
+// ---------------------------------------------------------------- persistent schedule
+// Two CTAs per SM for the whole pass.  The producer warp takes (split, kv head, row)
+// items from a queue in the workspace and streams their tiles back to back; the
+// consumers follow the tiles' metadata, restart their state at an item's first tile and,
+// at its last, merge the four warps' states in that tile's stage before releasing it.
+// No per-item CTA launch, pipeline fill or partial last wave.
+template <class SH>
+__global__ void __launch_bounds__(SH::THREADS, 2)
+    fd_partial_persist_kernel(const __grid_constant__ CUtensorMap tk,
+                              const __grid_constant__ CUtensorMap tv,
+                              const __grid_constant__ Params p) {
+  constexpr int G = SH::G, TT = SH::TT, STAGES = SH::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  auto* ctl = reinterpret_cast<PersistCtl<STAGES>*>(stages + SH::RING_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_addr(&ctl->full[s]), 1);
+      mbar_init(smem_addr(&ctl->empty[s]), SH::NCW);
+    }
+    mbar_init(smem_addr(&ctl->epi[0]), SH::NCW);
+    mbar_init(smem_addr(&ctl->epi[1]), SH::NCW);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == SH::NCW) {
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+    produce_items<TT, STAGES>(p, &tk, &tv, stages, ctl, lane);
+    pdl_trigger();
+    return;
+  }
+
+  // The consumer warps meet around each item's epilogue on mbarriers with bounded waits
+  // rather than a hardware barrier: a warp that gave up on a stalled stage must not
+  // leave the others blocked.
+  uint32_t epi_phase = 0;
+  auto meet = [&](int which) -> bool {
+    __syncwarp();
+    int ok = 1;
+    if (lane == 0) {
+      mbar_arrive(smem_addr(&ctl->epi[which]));
+      ok = mbar_wait(smem_addr(&ctl->epi[which]), epi_phase & 1);
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
+  auto give_up = [&]() {
+    if (lane == 0) {
+      ctl->abort = 1;
+      atomicOr(p.flags, kDevFlagTimeout);
+    }
+  };
+
+  Consumer<SH> c;
+  const bool multi_page = p.page_size > 0 && p.page_size < TT;
+  const uint32_t lb = (uint32_t)p.log2_box;
+  for (int n = 0;; ++n) {
+    const int stage = n % STAGES;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(smem_addr(&ctl->full[stage]), (n / STAGES) & 1);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      give_up();
+      break;
+    }
+    const TileMeta mt = ctl->meta[stage];
+    if (mt.flags & kMetaDone) break;
+    if (mt.flags & kMetaFirst) c.start(p, mt.b, mt.g, mt.L, lane);
+    uint8_t* kt = stages + (size_t)stage * 2 * kTileBytes;
+    c.tile(p, kt, kt + kTileBytes, mt.t0, mt.lo, mt.hi, mt.bad, warp, lane, lb, multi_page);
+    if (mt.flags & kMetaLast) {
+      // The stage becomes the merge scratch macc [NCW][G][D] once every warp is done
+      // with its K/V rows; mm, ml [NCW][G] live in the control block.
+      if (!meet(0)) {
+        give_up();
+        break;
+      }
+      float* macc = reinterpret_cast<float*>(kt);
+      c.store(p, macc, ctl->mm, ctl->ml, warp, lane);
+      if (!meet(1)) {
+        give_up();
+        break;
+      }
+      SplitInfo si{};
+      si.b = mt.b;
+      si.g = mt.g;
+      si.split = mt.split;
+      merge_warps_and_store<G, SH::D, SH::NCW>(p, si, macc, ctl->mm, ctl->ml, threadIdx.x);
+      ++epi_phase;
+      // Generic-proxy use of the stage ends before its next TMA fill.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
+  }
+  pdl_trigger();
+}
+
 template <class SH>
 cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                        cudaStream_t stream) {
-  auto kernel = fd_partial_mma_kernel<SH>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SH::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
-  kernel<<<grid, SH::THREADS, SH::SMEM_BYTES, stream>>>(tk, tv, p);
+  cudaError_t e;
+  if constexpr (SH::PERSIST) {
+    auto kernel = fd_partial_persist_kernel<SH>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SH::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t items = (int64_t)p.S * p.Hkv * p.B;
+    const unsigned grid = (unsigned)(items < 2 * sms ? items : 2 * sms);
+    kernel<<<grid, SH::THREADS, SH::SMEM_BYTES, stream>>>(tk, tv, p);
+  } else if (p.head_group) {
+    if constexpr (SH::D == 128 && !SH::KV8) {
+      auto kernel = fd_partial_heads_kernel<SH>;
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)SH::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      dim3 grid((unsigned)p.S, (unsigned)(p.Hkv / kHeadGroup), (unsigned)p.B);
+      kernel<<<grid, SH::THREADS, SH::SMEM_BYTES, stream>>>(tk, tv, p);
+    } else {
+      return cudaErrorInvalidValue;   // the host enables head groups for bf16 d = 128 only
+    }
+  } else {
+    auto kernel = fd_partial_mma_kernel<SH>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SH::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
+    kernel<<<grid, SH::THREADS, SH::SMEM_BYTES, stream>>>(tk, tv, p);
+  }
   return cudaGetLastError();
 }
 
-template <int D, bool KV8>
+template <int D, bool KV8, bool PERSIST>
 cudaError_t dispatch_g(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                        cudaStream_t stream) {
   switch (rows_template(p.n_rows)) {   // query rows per (b, kv head), padded
-    case 1: return launch_mma<MmaShape<D, 1, KV8>>(p, tk, tv, stream);
-    case 2: return launch_mma<MmaShape<D, 2, KV8>>(p, tk, tv, stream);
-    case 4: return launch_mma<MmaShape<D, 4, KV8>>(p, tk, tv, stream);
-    case 8: return launch_mma<MmaShape<D, 8, KV8>>(p, tk, tv, stream);
-    case 16: return launch_mma<MmaShape<D, 16, KV8>>(p, tk, tv, stream);
+    case 1: return launch_mma<MmaShape<D, 1, KV8, PERSIST>>(p, tk, tv, stream);
+    case 2: return launch_mma<MmaShape<D, 2, KV8, PERSIST>>(p, tk, tv, stream);
+    case 4: return launch_mma<MmaShape<D, 4, KV8, PERSIST>>(p, tk, tv, stream);
+    case 8: return launch_mma<MmaShape<D, 8, KV8, PERSIST>>(p, tk, tv, stream);
+    case 16: return launch_mma<MmaShape<D, 16, KV8, PERSIST>>(p, tk, tv, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+template <bool PERSIST>
+cudaError_t dispatch_kind(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                          cudaStream_t stream) {
+  if (p.kv_fp8) return p.d == 128 ? dispatch_g<128, true, PERSIST>(p, tk, tv, stream) : cudaErrorInvalidValue;
+  if (p.d == 128) return dispatch_g<128, false, PERSIST>(p, tk, tv, stream);
+  if (p.d == 64) return dispatch_g<64, false, PERSIST>(p, tk, tv, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_partial_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream) {
-  if (p.kv_fp8) return p.d == 128 ? dispatch_g<128, true>(p, tk, tv, stream) : cudaErrorInvalidValue;
-  if (p.d == 128) return dispatch_g<128, false>(p, tk, tv, stream);
-  if (p.d == 64) return dispatch_g<64, false>(p, tk, tv, stream);
-  return cudaErrorInvalidValue;
+  return p.persistent ? dispatch_kind<true>(p, tk, tv, stream)
+                      : dispatch_kind<false>(p, tk, tv, stream);
 }
 
 }  // namespace fd

@@ -70,6 +70,28 @@ __device__ __forceinline__ int64_t key_bound(const Params& p, int64_t L, int rho
   return L - p.Q + 1 + rho / p.G;
 }
 
+// Take a ticket on an epoch-tagged counter word (the fused merge's per-group arrivals,
+// the persistent schedule's work queue).  A counter word holds
+// (epoch << 32 | arrivals).  Each call brings a fresh epoch, so the first arrival of a
+// call restarts the count whatever the word held before (a workspace reused with other
+// sizes, stale data); the last arrival also puts the word back to 0, so a launch that
+// is replayed as is starts from a clean count too.  Lock-free: a failed compare-and-swap
+// means another CTA's succeeded.  Returns the arrival number (1 .. S), or 0 if the
+// bounded loop gave up (flagged).
+__device__ __forceinline__ unsigned take_ticket(const Params& p, unsigned long long* c) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(c);
+  for (int it = 0; it < (1 << 20); ++it) {
+    const unsigned long long want =
+        ((unsigned)(cur >> 32) == p.epoch) ? cur + 1ull
+                                           : (((unsigned long long)p.epoch << 32) | 1ull);
+    const unsigned long long prev = atomicCAS(c, cur, want);
+    if (prev == cur) return (unsigned)(want & 0xffffffffull);
+    cur = prev;
+  }
+  atomicOr(p.flags, kDevFlagTimeout);
+  return 0u;
+}
+
 // Shared-memory control block of the pipeline.
 template <int STAGES>
 struct PipeCtl {
@@ -79,6 +101,178 @@ struct PipeCtl {
   int32_t abort;            // a bounded wait gave up
   int32_t last;             // this CTA drew its group's last ticket (fused merge)
 };
+
+// ---------------------------------------------------------------- persistent schedule
+//
+// Work item x (0 .. S * Hkv * B - 1) is split S - 1 - x / (Hkv * B) of kv head
+// x mod Hkv of row (x / Hkv) mod B: the highest split indices, which only the longest
+// rows have, go first, and the many short or empty items fill in at the end.
+struct TileMeta {
+  int32_t b, g, split, flags;   // flags: kFirst | kLast | kDone
+  int64_t t0, lo, hi, L;        // tile start, the item's valid range, the row's length
+  uint32_t bad;
+};
+constexpr int32_t kMetaFirst = 1, kMetaLast = 2, kMetaDone = 4;
+
+template <int STAGES>
+struct PersistCtl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t epi[2];              // consumer warps meet here around an item's epilogue
+  TileMeta meta[STAGES];
+  float mm[4 * 16], ml[4 * 16]; // per-warp running max and exp-sum of the item's rows
+  int32_t abort;
+};
+
+// Producer warp of the persistent kernel: takes items from the queue and streams their
+// tiles into the ring without a break between items; publishes a kDone stage at the
+// end.  Empty items get their LSE_i = -inf written here and never reach the consumers.
+template <int TT, int STAGES>
+__device__ __forceinline__ void produce_items(const Params& p, const CUtensorMap* tk,
+                                              const CUtensorMap* tv, uint8_t* stages,
+                                              PersistCtl<STAGES>* ctl, int lane) {
+  const uint64_t pol = policy_evict_first();
+  const bool paged = p.block_table != nullptr;
+  const int ps = p.page_size;
+  const int pages_per_tile = paged ? (ps >= TT ? 1 : TT / ps) : 1;
+  const int box_rows = paged ? (ps >= TT ? TT : ps) : TT;
+  const uint32_t box_bytes = (uint32_t)(kTileBytes / TT) * box_rows;
+  const int64_t n_items = (int64_t)p.S * p.Hkv * p.B;
+  int n = 0;                        // tiles published so far (ring position)
+  bool aborted = false;
+
+  // Acquire ring slot n (lane 0 waits, the warp agrees).
+  auto acquire = [&](int slot_n) -> bool {
+    if (slot_n < STAGES) return true;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(smem_addr(&ctl->empty[slot_n % STAGES]), ((slot_n / STAGES) - 1) & 1);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok && lane == 0) {
+      ctl->abort = 1;
+      atomicOr(p.flags, kDevFlagTimeout);
+    }
+    return ok != 0;
+  };
+
+  // Items come from a plain fetch-and-add on the queue word (zero at launch: a fresh
+  // workspace header is zero and the last CTA of every launch puts it back).  The next
+  // item's ticket is taken when an item starts, so its latency hides behind the item.
+  unsigned long long ticket = 0;
+  if (lane == 0) ticket = atomicAdd(p.item_queue, 1ull);
+  while (!aborted) {
+    if (__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int32_t*>(&ctl->abort), 0)) break;
+    const int64_t item = (int64_t)__shfl_sync(0xffffffffu, ticket, 0);
+    if (item >= n_items) break;
+    if (lane == 0) ticket = atomicAdd(p.item_queue, 1ull);
+    const int64_t per_split = (int64_t)p.Hkv * p.B;
+    const int split = p.S - 1 - (int)(item / per_split);
+    const int g = (int)((item % per_split) % p.Hkv);
+    const int b = (int)((item % per_split) / p.Hkv);
+    int64_t L = p.seq_lens[b];
+    if (L < 0 || L > p.L_cap) {
+      if (lane == 0) atomicOr(p.flags, FD_DEVFLAG_SEQ_LEN);
+      L = L < 0 ? 0 : p.L_cap;
+    }
+    const int64_t lo = (int64_t)split * p.split_len;
+    const int64_t hi = min(lo + p.split_len, L);
+    if (lo >= hi) {                 // empty split: weight 0 in the merge
+      if (lane < p.n_rows) p.lse_part[flat_row(p, b, g, lane) * p.S + split] = kNegInf;
+      continue;
+    }
+    const int64_t T0 = lo / TT * TT;
+    const int n_tiles = (int)((hi - T0 + TT - 1) / TT);
+    const int64_t used_pages = paged ? (L + ps - 1) >> p.log2_page : 0;
+    int64_t cache_base = -64;
+    int32_t cache = -2;
+    for (int t = 0; t < n_tiles; ++t, ++n) {
+      if (!acquire(n)) {
+        aborted = true;
+        break;
+      }
+      const int stage = n % STAGES;
+      const int64_t t0 = T0 + (int64_t)t * TT;
+      uint32_t bad = 0;
+      int32_t pid[16];
+      if (paged) {
+        const int64_t pi0 = t0 >> p.log2_page;
+        for (int j = 0; j < pages_per_tile; ++j) {
+          const int64_t pi = pi0 + j;
+          if (pi < cache_base || pi >= cache_base + 32) {
+            cache_base = pi;
+            const int64_t mine = pi + lane;
+            cache = mine < used_pages ? p.block_table[(int64_t)b * p.bt_sb + mine] : -2;
+          }
+          int32_t id = __shfl_sync(0xffffffffu, cache, (int)(pi - cache_base));
+          if (id == -2) {
+            id = 0;
+          } else if (id < 0 || (int64_t)id >= p.num_pages) {
+            bad |= 1u << j;
+            id = 0;
+          }
+          pid[j] = id;
+        }
+        if (bad && lane == 0) atomicOr(p.flags, FD_DEVFLAG_PAGE);
+      }
+      if (lane == 0) {
+        TileMeta& m = ctl->meta[stage];
+        m.b = b;
+        m.g = g;
+        m.split = split;
+        m.flags = (t == 0 ? kMetaFirst : 0) | (t == n_tiles - 1 ? kMetaLast : 0);
+        m.t0 = t0;
+        m.lo = lo;
+        m.hi = hi;
+        m.L = L;
+        m.bad = bad;
+        const uint32_t full = smem_addr(&ctl->full[stage]);
+        mbar_arrive_expect_tx(full, 2u * kTileBytes);
+        const uint32_t dk = smem_addr(stages + (size_t)stage * 2 * kTileBytes);
+        const uint32_t dv = dk + kTileBytes;
+        if (!paged) {
+          tma_load_5d(dk, tk, full, 0, (int)t0, 0, g, b, pol);
+          tma_load_5d(dv, tv, full, 0, (int)t0, 0, g, b, pol);
+        } else if (ps >= TT) {
+          const int slot = (int)(t0 & (ps - 1));
+          tma_load_5d(dk, tk, full, 0, slot, 0, g, pid[0], pol);
+          tma_load_5d(dv, tv, full, 0, slot, 0, g, pid[0], pol);
+        } else {
+          for (int j = 0; j < pages_per_tile; ++j) {
+            tma_load_5d(dk + j * box_bytes, tk, full, 0, 0, 0, g, pid[j], pol);
+            tma_load_5d(dv + j * box_bytes, tv, full, 0, 0, 0, g, pid[j], pol);
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+  // Tell the consumers there is nothing more (a stage with kDone, completed by a plain
+  // arrive), unless the ring is stuck.
+  if (!aborted && acquire(n)) {
+    if (lane == 0) {
+      ctl->meta[n % STAGES].flags = kMetaDone;
+      mbar_arrive(smem_addr(&ctl->full[n % STAGES]));
+    }
+    __syncwarp();
+    ++n;
+  }
+  // Never leave with copies in flight (bounded waits on the last issued stages).
+  if (lane == 0) {
+    const int first = n > STAGES ? n - STAGES : 0;
+    for (int m = first; m < n; ++m) {
+      if (!mbar_wait(smem_addr(&ctl->full[m % STAGES]), (m / STAGES) & 1))
+        atomicOr(p.flags, kDevFlagTimeout);
+    }
+    // The last CTA to finish puts the queue words back to zero, so that a launch that
+    // is replayed as is starts from a clean queue too.  The fences order this CTA's
+    // last queue ticket before its done ticket, and every done ticket before the reset.
+    __threadfence();
+    if (atomicAdd(p.ctas_done, 1ull) == gridDim.x - 1ull) {
+      __threadfence();
+      *p.item_queue = 0ull;
+      *p.ctas_done = 0ull;
+    }
+  }
+}
 
 // Producer warp: streams tiles 0..n_tiles-1 of the split.  All 32 lanes run the loop
 // (they share the page-id cache); lane 0 issues the copies.

@@ -18,7 +18,9 @@
 // up; the running CTAs share an aggregate bandwidth that grows with their number and
 // saturates at the HBM ceiling; each CTA also pays a fixed start-up and finish time, and
 // the last CTA of a group pays for the merge -- and picks the split count with the
-// shortest simulated step.
+// shortest simulated step.  It plans for the default schedule: where head-group tiles
+// apply (d = 128 with 16- or 32-token pages and Hkv a multiple of 4) a CTA streams one
+// split of four kv heads in 16-token tiles, one 16 KB box per K and V.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -35,6 +37,7 @@ namespace {
 constexpr int32_t kMaxSplits = 4096;
 constexpr int64_t kMinSplitTokens = 256;
 constexpr int kCtasPerSm = 2;             // residency of the partial kernels
+constexpr int kHeadGroup = 4;             // kv heads per CTA with head-group tiles
 
 // Model constants, fitted on GB300 to this library's partial kernel: n CTAs streaming
 // at once reach BW(n) = kHbmBytesPerUs * (1 - exp(-n / tau)) together, shared equally.
@@ -87,20 +90,28 @@ double simulate(const std::vector<double>& work, const std::vector<double>& fixe
   return t;
 }
 
+// Whether the default schedule runs head-group tiles for these sizes (bf16 assumed).
+bool head_groups(int Hkv, int d, int page_size) {
+  return d == 128 && (page_size == 16 || page_size == 32) && Hkv % kHeadGroup == 0;
+}
+
 // Per-CTA work of one split count: bytes each CTA loads (whole tiles, as the kernels
-// do) and its fixed time, in launch order (split fastest, then kv head, then row).
+// do) and its fixed time, in launch order (split fastest, then kv head or head group,
+// then row).
 double plan_time(int B, int Hq, int Hkv, int d, int64_t L_cap, const int32_t* lens, int S,
                  int slots, int page_size) {
-  const int TT = tile_tokens_bf16(d);
+  const bool heads = head_groups(Hkv, d, page_size);
+  const int TT = heads ? 16 : tile_tokens_bf16(d);
+  const int per_cta = heads ? kHeadGroup : 1;      // kv heads a CTA streams
   const int64_t split_len = (L_cap + S - 1) / S;
-  const double tok_bytes = 2.0 * d * 2.0;          // K and V rows, bf16
+  const double tok_bytes = 2.0 * d * 2.0 * per_cta;   // K and V rows, bf16
   const int G = Hq / Hkv;
   std::vector<double> work, fixed;
   work.reserve((size_t)B * Hkv * S);
   fixed.reserve((size_t)B * Hkv * S);
   for (int b = 0; b < B; ++b) {
     const int64_t L = std::min<int64_t>(std::max<int64_t>(lens ? lens[b] : L_cap, 0), L_cap);
-    for (int g = 0; g < Hkv; ++g) {
+    for (int g = 0; g < Hkv; g += per_cta) {
       int last = -1;
       for (int i = 0; i < S; ++i) {
         const int64_t lo = (int64_t)i * split_len, hi = std::min(lo + split_len, L);
@@ -115,11 +126,13 @@ double plan_time(int B, int Hq, int Hkv, int d, int64_t L_cap, const int32_t* le
         }
       }
       // The group's merge reads G rows of S partials (d + 1 floats each).
-      const double merge_us = (double)G * S * (d + 1) * 4.0 / kMergeBytesPerUs;
+      const double merge_us = (double)per_cta * G * S * (d + 1) * 4.0 / kMergeBytesPerUs;
       if (last >= 0) fixed[last] += merge_us;
     }
   }
-  const double tau = kSatCtasContig * kOneCtaContig / one_cta_rate(page_size, TT);
+  // Head-group tiles are one 16 KB box per K and V, like a contiguous cache's.
+  const double tau =
+      heads ? kSatCtasContig : kSatCtasContig * kOneCtaContig / one_cta_rate(page_size, TT);
   return simulate(work, fixed, slots, tau);
 }
 
@@ -161,16 +174,17 @@ int32_t fd_num_splits_for_lengths(int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
   for (int S = 72; S <= 256; S += 8) cand.push_back(S);
   for (int S = 288; S <= 1024; S += 32) cand.push_back(S);
   const int64_t S_cap = std::max<int64_t>(1, (L_cap + kMinSplitTokens - 1) / kMinSplitTokens);
+  const int TT = head_groups(Hkv, d, page_size) ? 16 : tile_tokens_bf16(d);
   int best_S = 1;
   double best_t = plan_time(B, Hq, Hkv, d, L_cap, seq_lens, 1, slots, page_size);
-  if (L_cap % tile_tokens_bf16(d) != 0) best_t *= kMisalignedPenalty;
+  if (L_cap % TT != 0) best_t *= kMisalignedPenalty;
   for (int S : cand) {
     if (S == 1 || S > S_cap || S > kMaxSplits) continue;
     double t = plan_time(B, Hq, Hkv, d, L_cap, seq_lens, S, slots, page_size);
     // A split that ends mid-tile makes two CTAs load its boundary tile and breaks the
     // tiles' alignment; measured on the 128K workload it costs ~4% beyond the extra
     // bytes the model already counts (S = 38: 83.3 us against 79.9 us at S = 32).
-    if (((L_cap + S - 1) / S) % tile_tokens_bf16(d) != 0) t *= kMisalignedPenalty;
+    if (((L_cap + S - 1) / S) % TT != 0) t *= kMisalignedPenalty;
     if (t < best_t * 0.995) {                 // a smaller count wins near-ties
       best_t = t;
       best_S = S;

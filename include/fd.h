@@ -306,6 +306,32 @@ FD_API int32_t fd_get_merge_mode(void);
 FD_API fd_status fd_set_path(int32_t path);
 FD_API int32_t fd_get_path(void);
 
+/*
+ * How the tensor-core partial pass assigns work items -- one (split, kv head, row) of
+ * [FD-interview] section two's split loop -- to CTAs (process-wide, for later calls).
+ * FD_SCHEDULE_GRID: one CTA per item, two per SM; items beyond one wave wait for a
+ * slot, and each CTA fills and drains its own copy pipeline.
+ * FD_SCHEDULE_PERSISTENT: two CTAs per SM take items from a queue in the workspace
+ * header and stream their tiles back to back.  Same partials as FD_SCHEDULE_GRID, bit
+ * for bit (the per-item arithmetic is shared).
+ * FD_SCHEDULE_HEAD_GROUPS: one CTA per (split, group of 4 kv heads, row); a tile is 16
+ * tokens of one page for all 4 heads, loaded as one 16 KB TMA box instead of four 4 KB
+ * ones, and each consumer warp keeps one head's state.  For paged bf16 caches with
+ * d = 128, 16- or 32-token pages and Hkv a multiple of 4; other calls run the grid
+ * schedule.  Same results up to rounding order.
+ * FD_SCHEDULE_AUTO (default): head groups where they apply, else grid.
+ * The persistent and head-group schedules run only with FD_MERGE_KERNEL (or
+ * fd_decode_partial) and on the tensor-core path; otherwise the grid schedule runs.
+ */
+typedef enum {
+  FD_SCHEDULE_AUTO = 0,
+  FD_SCHEDULE_GRID = 1,
+  FD_SCHEDULE_PERSISTENT = 2,
+  FD_SCHEDULE_HEAD_GROUPS = 3
+} fd_schedule;
+FD_API fd_status fd_set_schedule(int32_t schedule);
+FD_API int32_t fd_get_schedule(void);
+
 /* Split count a call with these sizes and this num_splits argument would use. */
 FD_API int32_t fd_resolve_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int64_t L_cap,
                               int32_t num_splits);

@@ -134,6 +134,21 @@ def test_merge_mode_round_trip():
         lib.fd_set_merge_mode(fd.FD_MERGE_KERNEL)
 
 
+def test_schedule_round_trip():
+    lib = fd.lib()
+    try:
+        assert fd.get_schedule() == fd.FD_SCHEDULE_AUTO            # the default
+        for sched in (fd.FD_SCHEDULE_GRID, fd.FD_SCHEDULE_PERSISTENT,
+                      fd.FD_SCHEDULE_HEAD_GROUPS, fd.FD_SCHEDULE_AUTO):
+            fd.set_schedule(sched)
+            assert fd.get_schedule() == sched
+        with pytest.raises(fd.FdError):
+            fd.set_schedule(4)
+        assert fd.get_schedule() == fd.FD_SCHEDULE_AUTO            # unchanged on error
+    finally:
+        lib.fd_set_schedule(fd.FD_SCHEDULE_AUTO)
+
+
 def test_path_setting_round_trip():
     lib = fd.lib()
     try:

@@ -30,6 +30,7 @@ def _restore_path():
     if torch.cuda.is_available():
         fd.set_path(fd.FD_PATH_AUTO)
         fd.set_merge_mode(fd.FD_MERGE_KERNEL)
+        fd.set_schedule(fd.FD_SCHEDULE_AUTO)
 
 
 MERGES = [("merge-kernel", 0), ("merge-in-kernel", 1)]
@@ -344,8 +345,10 @@ def test_side_stream_and_events():
 @pytest.mark.parametrize("name,path", PATHS_BF16)
 def test_single_launch_equals_two_pass(name, path):
     """fd_decode_attention in single-launch mode (partials + in-kernel merge by the last
-    CTA of each group) against fd_decode_partial followed by fd_merge_partials."""
+    CTA of each group) against fd_decode_partial followed by fd_merge_partials, both with
+    one kv head per CTA (the same partials, so only the merge order differs)."""
     fd.set_merge_mode(fd.FD_MERGE_IN_KERNEL)
+    fd.set_schedule(fd.FD_SCHEDULE_GRID)
     w = workloads.paged_case(5, 32, 8, 128, 16, 256, [4096, 1, 0, 2500, 77], seed=51,
                              out_dtype=torch.float32)
     ref_o, ref_l = ref_for(w)
