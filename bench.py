@@ -95,6 +95,10 @@ def measured_peak():
 KERNEL_SOURCES = {
     "fd_partial_mma_kernel": ["fd_partial_mma.cu", "fd_pipeline.cuh", "fd_epilogue.cuh",
                               "fd_device.cuh", "fd_internal.h"],
+    "fd_partial_heads_kernel": ["fd_partial_mma.cu", "fd_pipeline.cuh", "fd_epilogue.cuh",
+                                "fd_device.cuh", "fd_internal.h"],
+    "fd_partial_persist_kernel": ["fd_partial_mma.cu", "fd_pipeline.cuh", "fd_epilogue.cuh",
+                                  "fd_device.cuh", "fd_internal.h"],
     "fd_partial_simt_kernel": ["fd_partial_simt.cu", "fd_partial_simt.cuh", "fd_pipeline.cuh",
                                "fd_epilogue.cuh", "fd_device.cuh", "fd_internal.h"],
 }
@@ -377,7 +381,7 @@ def run_fd(args):
     peak, peak_src = measured_peak()
     achieved = kv_bytes / (partial_ms * 1e-3) / 1e9
     path_name = "mma" if (args.path == "mma" or (args.path == "auto" and w.q.dtype == torch.bfloat16)) else "simt"
-    kernel = "fd_partial_%s_kernel" % path_name
+    kernel = fd.partial_kernel_name(w.q.dtype, w.k.dtype, d, w.Hkv, w.page_size)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kernel, w.name),
                 "kernel": kernel, "peak_source": peak_src,

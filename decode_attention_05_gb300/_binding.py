@@ -110,6 +110,8 @@ def _declare(L):
     L.fd_set_schedule.argtypes = [i32]
     L.fd_get_schedule.restype = i32
     L.fd_get_schedule.argtypes = []
+    L.fd_partial_kernel_name.restype = ctypes.c_char_p
+    L.fd_partial_kernel_name.argtypes = [i32, i32, i32, i32, i32, i32]
     L.fd_get_path.restype = i32
     L.fd_get_path.argtypes = []
     L.fd_status_string.restype = ctypes.c_char_p
@@ -202,6 +204,14 @@ def set_schedule(schedule: int):
 
 def get_schedule() -> int:
     return int(lib().fd_get_schedule())
+
+
+def partial_kernel_name(dtype, kv_dtype, d: int, Hkv: int, page_size: int = 0,
+                        with_output: bool = True) -> Optional[str]:
+    """The partial-pass kernel a call with these sizes would launch (torch dtypes)."""
+    name = lib().fd_partial_kernel_name(_DTYPES[dtype], _DTYPES[kv_dtype], d, Hkv, page_size,
+                                        1 if with_output else 0)
+    return name.decode() if name else None
 
 
 def workspace_init(ws: torch.Tensor, stream=None):

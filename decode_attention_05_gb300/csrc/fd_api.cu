@@ -23,6 +23,30 @@ std::atomic<int> g_merge{FD_MERGE_KERNEL};
 std::atomic<int> g_schedule{FD_SCHEDULE_AUTO};
 std::atomic<uint32_t> g_epoch{0x5eed0001u};   // per-call ticket epochs of the fused merge
 
+// Which partial-pass kernel runs, from the process settings and the call's sizes.  The
+// persistent and head-group kernels write only partials, so neither runs under the
+// single-launch merge.
+struct Schedule {
+  bool heads, persistent;
+};
+
+Schedule choose_schedule(int path, bool kv8, int64_t d, int64_t Hkv, int32_t page_size,
+                         bool fused) {
+  const int sched = g_schedule.load();
+  const bool head_ok = path == FD_PATH_MMA && !kv8 && d == 128 &&
+                       (page_size == 16 || page_size == 32) && Hkv % fd::kHeadGroup == 0 &&
+                       !fused;
+  Schedule sc;
+  sc.heads = head_ok && (sched == FD_SCHEDULE_AUTO || sched == FD_SCHEDULE_HEAD_GROUPS);
+  sc.persistent = !sc.heads && path == FD_PATH_MMA && !fused && sched == FD_SCHEDULE_PERSISTENT;
+  return sc;
+}
+
+int resolve_path(int32_t q_dtype) {
+  const int path = g_path.load();
+  return path == FD_PATH_AUTO ? (q_dtype == FD_BF16 ? FD_PATH_MMA : FD_PATH_SIMT) : path;
+}
+
 fd_status fail(fd_status st, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -231,6 +255,22 @@ fd_status fd_set_schedule(int32_t schedule) {
 
 int32_t fd_get_schedule(void) { return g_schedule.load(); }
 
+const char* fd_partial_kernel_name(int32_t dtype, int32_t kv_dtype, int32_t d, int32_t Hkv,
+                                   int32_t page_size, int32_t with_output) {
+  const bool kv8 = kv_dtype == FD_F8E4M3;
+  if ((dtype != FD_BF16 && dtype != FD_F32) || (!kv8 && kv_dtype != dtype) ||
+      (kv8 && dtype != FD_BF16) || d <= 0 || Hkv <= 0 || page_size < 0)
+    return nullptr;
+  const int path = resolve_path(dtype);
+  if ((path == FD_PATH_MMA && dtype != FD_BF16) || (kv8 && path != FD_PATH_MMA)) return nullptr;
+  if (path == FD_PATH_SIMT) return "fd_partial_simt_kernel";
+  const bool fused = with_output && g_merge.load() == FD_MERGE_IN_KERNEL;
+  const Schedule sc = choose_schedule(path, kv8, d, Hkv, page_size, fused);
+  if (sc.heads) return "fd_partial_heads_kernel";
+  if (sc.persistent) return "fd_partial_persist_kernel";
+  return "fd_partial_mma_kernel";
+}
+
 size_t fd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_splits) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || num_splits <= 0 || num_splits > kMaxSplits)
     return 0;
@@ -402,25 +442,16 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
     return fail(FD_ERR_UNSUPPORTED, "grid too large");
 
   // ---- path
-  int path = g_path.load();
-  if (path == FD_PATH_AUTO) path = q->dtype == FD_BF16 ? FD_PATH_MMA : FD_PATH_SIMT;
+  const int path = resolve_path(q->dtype);
   if (path == FD_PATH_MMA && q->dtype != FD_BF16)
     return fail(FD_ERR_UNSUPPORTED, "the tensor-core path needs bf16 inputs");
   if (kv8 && path != FD_PATH_MMA)
     return fail(FD_ERR_UNSUPPORTED, "the FP8 KV cache runs on the tensor-core path only");
 
-  // ---- schedule (fd_set_schedule).  The persistent and head-group kernels write only
-  // partials, so neither runs under the single-launch merge.
+  // ---- schedule (fd_set_schedule)
   const bool fused = need_out && g_merge.load() == FD_MERGE_IN_KERNEL;
-  const int sched = g_schedule.load();
-  const int64_t items = (int64_t)S * Hkv * B;
-  const bool head_ok = path == FD_PATH_MMA && !kv8 && d == 128 && paged &&
-                       (page_size == 16 || page_size == 32) && Hkv % fd::kHeadGroup == 0 &&
-                       !fused;
-  const bool heads = head_ok && (sched == FD_SCHEDULE_AUTO || sched == FD_SCHEDULE_HEAD_GROUPS);
-  const bool persistent = !heads && path == FD_PATH_MMA && !fused &&
-                          (sched == FD_SCHEDULE_PERSISTENT);
-  (void)items;
+  const Schedule sc = choose_schedule(path, kv8, d, Hkv, paged ? page_size : 0, fused);
+  const bool heads = sc.heads, persistent = sc.persistent;
 
   // ---- tensor maps (box height: one tile, or one page when pages are shorter; with head
   // groups 16 rows of kHeadGroup heads)

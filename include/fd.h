@@ -332,6 +332,17 @@ typedef enum {
 FD_API fd_status fd_set_schedule(int32_t schedule);
 FD_API int32_t fd_get_schedule(void);
 
+/*
+ * Name of the partial-pass kernel a call would launch under the current process
+ * settings (path, merge mode, schedule): "fd_partial_mma_kernel",
+ * "fd_partial_heads_kernel", "fd_partial_persist_kernel" or "fd_partial_simt_kernel".
+ * dtype is q's fd_dtype, kv_dtype the cache's; page_size 0 for a contiguous cache;
+ * with_output 1 for fd_decode_attention, 0 for fd_decode_partial.  NULL for a
+ * combination no entry point accepts.  Static string; host only.
+ */
+FD_API const char* fd_partial_kernel_name(int32_t dtype, int32_t kv_dtype, int32_t d, int32_t Hkv,
+                                          int32_t page_size, int32_t with_output);
+
 /* Split count a call with these sizes and this num_splits argument would use. */
 FD_API int32_t fd_resolve_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int64_t L_cap,
                               int32_t num_splits);

@@ -149,6 +149,39 @@ def test_schedule_round_trip():
         lib.fd_set_schedule(fd.FD_SCHEDULE_AUTO)
 
 
+def test_partial_kernel_name_follows_settings():
+    """Which partial kernel a call would launch, from the sizes and process settings."""
+    import torch
+    bf, f32, f8 = torch.bfloat16, torch.float32, torch.float8_e4m3fn
+    name = fd.partial_kernel_name
+    lib = fd.lib()
+    try:
+        assert name(bf, bf, 128, 8) == "fd_partial_mma_kernel"                 # contiguous
+        assert name(bf, bf, 128, 8, 16) == "fd_partial_heads_kernel"           # small pages
+        assert name(bf, bf, 128, 8, 32) == "fd_partial_heads_kernel"
+        assert name(bf, bf, 128, 8, 64) == "fd_partial_mma_kernel"
+        assert name(bf, bf, 128, 6, 16) == "fd_partial_mma_kernel"             # Hkv % 4
+        assert name(bf, bf, 64, 8, 16) == "fd_partial_mma_kernel"              # d = 64
+        assert name(bf, f8, 128, 8, 16) == "fd_partial_mma_kernel"             # FP8 KV
+        assert name(f32, f32, 128, 8) == "fd_partial_simt_kernel"
+        assert name(f32, f8, 128, 8) is None
+        fd.set_merge_mode(fd.FD_MERGE_IN_KERNEL)                              # single launch
+        assert name(bf, bf, 128, 8, 16) == "fd_partial_mma_kernel"
+        assert name(bf, bf, 128, 8, 16, with_output=False) == "fd_partial_heads_kernel"
+        fd.set_merge_mode(fd.FD_MERGE_KERNEL)
+        fd.set_schedule(fd.FD_SCHEDULE_GRID)
+        assert name(bf, bf, 128, 8, 16) == "fd_partial_mma_kernel"
+        fd.set_schedule(fd.FD_SCHEDULE_PERSISTENT)
+        assert name(bf, bf, 128, 8, 16) == "fd_partial_persist_kernel"
+        assert name(bf, bf, 128, 8) == "fd_partial_persist_kernel"
+        fd.set_path(fd.FD_PATH_SIMT)
+        assert name(bf, bf, 128, 8) == "fd_partial_simt_kernel"
+    finally:
+        lib.fd_set_schedule(fd.FD_SCHEDULE_AUTO)
+        lib.fd_set_merge_mode(fd.FD_MERGE_KERNEL)
+        lib.fd_set_path(fd.FD_PATH_AUTO)
+
+
 def test_path_setting_round_trip():
     lib = fd.lib()
     try:
