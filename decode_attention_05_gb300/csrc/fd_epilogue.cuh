@@ -32,36 +32,66 @@ __device__ __forceinline__ void write_empty_split(const Params& p, const SplitIn
   if (tid < p.n_rows) p.lse_part[flat_row(p, si.b, si.g, tid) * p.S + si.split] = kNegInf;
 }
 
-// macc [NCW][G][D], mm [NCW][G], ml [NCW][G] in shared memory (G = query rows of the
-// group, a power of two >= p.n_rows), filled by every warp for rows < p.n_rows; called
-// by all NCW * 32 consumer threads (ctid = 0 .. NCW * 32 - 1) after a barrier.
-template <int G, int D, int NCW>
-__device__ __forceinline__ void merge_warps_and_store(const Params& p, const SplitInfo& si,
-                                                      const float* macc, const float* mm,
-                                                      const float* ml, int ctid) {
-  for (int idx = ctid; idx < p.n_rows * D; idx += NCW * 32) {
-    const int h = idx / D, j = idx % D;
+// Index of (warp w, row h, dim j) in the merge scratch macc [NCW][G][D].  The dims of
+// a row are XOR-swizzled by 8 x ((h / 2) mod 4): the tensor-core epilogue's lanes write
+// rows 2 apart at the same dims, which then fall in different banks; groups of 4
+// consecutive dims stay together (16-byte reads).
+template <int G, int D>
+__device__ __forceinline__ int macc_index(int w, int h, int j) {
+  static_assert(D % 32 == 0, "the swizzle needs 32 dims per row");
+  return (w * G + h) * D + (j ^ (((h >> 1) & 3) << 3));
+}
+
+// macc [NCW][G][D] (macc_index), mm [NCW][G], ml [NCW][G] in shared memory (G = query
+// rows of the group, a power of two >= p.n_rows), filled by every warp for rows
+// < p.n_rows; called by all NCW * 32 consumer threads (ctid = 0 .. NCW * 32 - 1) after
+// they are visible.  One thread per row turns the warps' maxima into weights
+// w_w = 2^(m_w - M) / L (kept in mm; L in ml[h]) and writes LSE_i; `sync` makes them
+// visible to all (it returns false if the threads could not meet; nothing more is
+// written then); every thread then forms 4 output dims at a time.  Returns sync's
+// answer.
+template <int G, int D, int NCW, class Sync>
+__device__ __forceinline__ bool merge_warps_and_store(const Params& p, const SplitInfo& si,
+                                                      const float* macc, float* mm, float* ml,
+                                                      int ctid, Sync&& sync) {
+  if (ctid < p.n_rows) {
+    const int h = ctid;
     float M = kNegInf;
 #pragma unroll
     for (int w = 0; w < NCW; ++w) M = fmaxf(M, mm[w * G + h]);
-    float L = 0.f, O = 0.f;
-    if (M != kNegInf) {
+    float c[NCW], L = 0.f;
 #pragma unroll
-      for (int w = 0; w < NCW; ++w) {
-        const float mw = mm[w * G + h];
-        const float c = (mw == kNegInf) ? 0.f : ex2(mw - M);
-        L = fmaf(ml[w * G + h], c, L);
-        O = fmaf(macc[(w * G + h) * D + j], c, O);
-      }
+    for (int w = 0; w < NCW; ++w) {
+      const float mw = mm[w * G + h];
+      c[w] = (M == kNegInf || mw == kNegInf) ? 0.f : ex2(mw - M);
+      L = fmaf(ml[w * G + h], c[w], L);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) mm[w * G + h] = c[w] * inv;
+    ml[h] = L;
+    const int64_t row = flat_row(p, si.b, si.g, h);
+    p.lse_part[row * p.S + si.split] = L > 0.f ? (M + lg2_approx(L)) * 0.6931471805599453f : kNegInf;
+  }
+  if (!sync()) return false;
+  constexpr int D4 = D / 4;
+  for (int idx = ctid; idx < p.n_rows * D4; idx += NCW * 32) {
+    const int h = idx / D4, j = (idx - h * D4) * 4;
+    if (!(ml[h] > 0.f)) continue;                   // no key in the split: no O_i
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) {
+      const float f = mm[w * G + h];
+      const float4 a = *reinterpret_cast<const float4*>(macc + macc_index<G, D>(w, h, j));
+      o.x = fmaf(a.x, f, o.x);
+      o.y = fmaf(a.y, f, o.y);
+      o.z = fmaf(a.z, f, o.z);
+      o.w = fmaf(a.w, f, o.w);
     }
     const int64_t row = flat_row(p, si.b, si.g, h);
-    if (L > 0.f) {
-      p.o_part[(row * p.S + si.split) * D + j] = O / L;
-      if (j == 0) p.lse_part[row * p.S + si.split] = (M + lg2_approx(L)) * 0.6931471805599453f;
-    } else if (j == 0) {
-      p.lse_part[row * p.S + si.split] = kNegInf;
-    }
+    *reinterpret_cast<float4*>(p.o_part + (row * p.S + si.split) * D + j) = o;
   }
+  return true;
 }
 
 // ---------------------------------------------------------------- fused merge

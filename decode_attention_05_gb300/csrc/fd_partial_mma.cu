@@ -137,6 +137,7 @@ struct Consumer {
   float m[NT][2], l[NT][2];        // per column (query row nt * 8 + qc + {0, 1})
   float acc[NT][SH::MTILES][4];    // O^T fragments
   float sl2, vsc;
+  int64_t kmin;                    // smallest causal key bound of the group's rows
 
   // Load the group's query fragments and reset the state.
   //   B fragments of Q^T (k = dim, n = row), bf16 as stored: b0 holds dims 16 kk + qc,
@@ -177,6 +178,7 @@ struct Consumer {
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[nt][mt][e] = 0.f;
     }
+    kmin = key_bound(p, L, 0);
     // FP8 KV: per-kv-head dequantisation scales fold into the score scale and output.
     const float ksc = (SH::KV8 && p.k_scale != nullptr) ? p.k_scale[g] : 1.f;
     vsc = (SH::KV8 && p.v_scale != nullptr) ? p.v_scale[g] : 1.f;
@@ -212,13 +214,19 @@ struct Consumer {
       __syncwarp();
     }
 
+    // The warp's CHUNKS 16-token chunks go through the online softmax together: all
+    // QK^T products first (independent mma chains), one max and one rescale for the
+    // warp's rows of the tile, then all PV products.
+    // A row needs masking only on a boundary tile (split range, invalid page) or where
+    // a query's causal bound falls inside the warp's rows; kmin is the smallest bound.
+    const bool full = clean && t0 + r0 + SH::ROWS_PER_WARP <= kmin;
+    float s[SH::CHUNKS][NT][4];
 #pragma unroll
     for (int ch = 0; ch < SH::CHUNKS; ++ch) {
       const int rb = r0 + ch * 16;                    // first row of this 16-token chunk
       // ---- S^T = K . Q^T  (A = K rows rb..rb+15 via ldmatrix, swizzled tile)
-      float s[NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      for (int nt = 0; nt < NT; ++nt) s[ch][nt][0] = s[ch][nt][1] = s[ch][nt][2] = s[ch][nt][3] = 0.f;
       const int arow = rb + lr + (lm & 1) * 8;
       if constexpr (SH::KV8) {
         // A 16-byte chunk holds 16 dims: one ldmatrix.x4 (chunks c, c + 1, rows 0-7 and
@@ -236,7 +244,7 @@ struct Consumer {
                                    e4m3x2_to_f16x2(rr0 >> 16), e4m3x2_to_f16x2(rr1 >> 16)};
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
-              mma_f16(s[nt], a, qb[nt][kk + u][0], qb[nt][kk + u][1]);
+              mma_f16(s[ch][nt], a, qb[nt][kk + u][0], qb[nt][kk + u][1]);
           }
         }
       } else {
@@ -246,69 +254,99 @@ struct Consumer {
           uint32_t a[4];
           ldsm_x4(smem_addr(kt) + tile_chunk<SH::LINES>(arow, c16, lb), a);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16(s[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+          for (int nt = 0; nt < NT; ++nt) mma_bf16(s[ch][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
         }
       }
-      // ---- mask and scale: element e of s[nt] is (token rb + qr + 8 (e >> 1),
-      //      row nt * 8 + qc + (e & 1)); excluded tokens get -inf.
-      bool vrow[2];
-      int64_t vtok[2];
+    }
+
+    // ---- mask and scale: element e of s[ch][nt] is (token rb + qr + 8 (e >> 1),
+    //      row nt * 8 + qc + (e & 1)); excluded tokens get -inf.
+    if (full) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int row = rb + qr + 8 * hh;
-        const int64_t tok = t0 + row;
-        const int pslot = multi_page ? (row >> p.log2_page) : 0;
-        vrow[hh] = tok >= lo && tok < hi && !((bad >> pslot) & 1u);
-        vtok[hh] = tok;
+      for (int ch = 0; ch < SH::CHUNKS; ++ch)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[ch][nt][e] *= sl2;
+    } else {
+#pragma unroll
+      for (int ch = 0; ch < SH::CHUNKS; ++ch) {
+        const int rb = r0 + ch * 16;
+        bool vrow[2];
+        int64_t vtok[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int row = rb + qr + 8 * hh;
+          const int64_t tok = t0 + row;
+          const int pslot = multi_page ? (row >> p.log2_page) : 0;
+          vrow[hh] = tok >= lo && tok < hi && !((bad >> pslot) & 1u);
+          vtok[hh] = tok;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            s[ch][nt][e] = (vrow[e >> 1] && vtok[e >> 1] < lim[nt][e & 1]) ? s[ch][nt][e] * sl2
+                                                                             : kNegInf;
       }
-      uint32_t pb[NT][2];                             // P^T fragments (b0/b1 of the PV mma)
+    }
+
+    uint32_t pb[SH::CHUNKS][NT][2];                   // P^T fragments (b0/b1 of the PV mma)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float x[4];
+    for (int nt = 0; nt < NT; ++nt) {
+      // max per column over the warp's rows: in-thread, then lanes of equal qc
+      float mx0 = kNegInf, mx1 = kNegInf;
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          x[e] = (vrow[e >> 1] && vtok[e >> 1] < lim[nt][e & 1]) ? s[nt][e] * sl2 : kNegInf;
-        // chunk max per column over the 16 tokens: in-thread pair, then lanes of equal qc
-        float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+      for (int ch = 0; ch < SH::CHUNKS; ++ch) {
+        mx0 = fmaxf(mx0, fmaxf(s[ch][nt][0], s[ch][nt][2]));
+        mx1 = fmaxf(mx1, fmaxf(s[ch][nt][1], s[ch][nt][3]));
+      }
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+      if (mn0 > m[nt][0] || mn1 > m[nt][1]) {         // rescale the running state
+        const float c0 = (mn0 == kNegInf) ? 1.f : ex2(m[nt][0] - mn0);
+        const float c1 = (mn1 == kNegInf) ? 1.f : ex2(m[nt][1] - mn1);
+        l[nt][0] *= c0;
+        l[nt][1] *= c1;
+#pragma unroll
+        for (int mt = 0; mt < SH::MTILES; ++mt) {
+          acc[nt][mt][0] *= c0;
+          acc[nt][mt][1] *= c1;
+          acc[nt][mt][2] *= c0;
+          acc[nt][mt][3] *= c1;
         }
-        const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-        if (mn0 > m[nt][0] || mn1 > m[nt][1]) {       // rescale the running state
-          const float c0 = (mn0 == kNegInf) ? 1.f : ex2(m[nt][0] - mn0);
-          const float c1 = (mn1 == kNegInf) ? 1.f : ex2(m[nt][1] - mn1);
-          l[nt][0] *= c0;
-          l[nt][1] *= c1;
+        m[nt][0] = mn0;
+        m[nt][1] = mn1;
+      }
 #pragma unroll
-          for (int mt = 0; mt < SH::MTILES; ++mt) {
-            acc[nt][mt][0] *= c0;
-            acc[nt][mt][1] *= c1;
-            acc[nt][mt][2] *= c0;
-            acc[nt][mt][3] *= c1;
-          }
-          m[nt][0] = mn0;
-          m[nt][1] = mn1;
-        }
+      for (int ch = 0; ch < SH::CHUNKS; ++ch) {
         float pr[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float mh = m[nt][e & 1];
-          pr[e] = (x[e] == kNegInf) ? 0.f : ex2(x[e] - mh);
+          const float x = s[ch][nt][e];
+          pr[e] = (x == kNegInf) ? 0.f : ex2(x - m[nt][e & 1]);
         }
         l[nt][0] += pr[0] + pr[2];
         l[nt][1] += pr[1] + pr[3];
         // P rows (tokens qr, qr + 8) x columns (qc, qc + 1) -> transpose to P^T fragments.
         if constexpr (SH::KV8) {                      // f16 P for the f16 PV mma
-          pb[nt][0] = movmatrix_trans(pack_f16x2(pr[0], pr[1]));
-          pb[nt][1] = movmatrix_trans(pack_f16x2(pr[2], pr[3]));
+          pb[ch][nt][0] = movmatrix_trans(pack_f16x2(pr[0], pr[1]));
+          pb[ch][nt][1] = movmatrix_trans(pack_f16x2(pr[2], pr[3]));
         } else {
-          pb[nt][0] = movmatrix_trans(pack_bf16x2(pr[0], pr[1]));
-          pb[nt][1] = movmatrix_trans(pack_bf16x2(pr[2], pr[3]));
+          pb[ch][nt][0] = movmatrix_trans(pack_bf16x2(pr[0], pr[1]));
+          pb[ch][nt][1] = movmatrix_trans(pack_bf16x2(pr[2], pr[3]));
         }
       }
-      // ---- O^T += V^T . P^T
+    }
+
+    // ---- O^T += V^T . P^T
+#pragma unroll
+    for (int ch = 0; ch < SH::CHUNKS; ++ch) {
+      const int rb = r0 + ch * 16;
       if constexpr (SH::KV8) {
         // ldmatrix.trans over 16-bit pairs of codes: matrix j covers tokens
         // rb + 8 (j & 1) .. +7 of chunk (m-tile) mt + (j >> 1); a register holds tokens
@@ -328,7 +366,8 @@ struct Consumer {
             const uint32_t a[4] = {e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x0 >> 16),
                                    e4m3x2_to_f16x2(x1), e4m3x2_to_f16x2(x1 >> 16)};
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_f16(acc[nt][mt + u], a, pb[nt][0], pb[nt][1]);
+            for (int nt = 0; nt < NT; ++nt)
+              mma_f16(acc[nt][mt + u], a, pb[ch][nt][0], pb[ch][nt][1]);
           }
         }
       } else {
@@ -341,7 +380,8 @@ struct Consumer {
           uint32_t a[4];
           ldsm_x4_trans(smem_addr(vt) + tile_chunk<SH::LINES>(vrow_addr, c16, lb), a);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[nt][mt], a, pb[nt][0], pb[nt][1]);
+          for (int nt = 0; nt < NT; ++nt)
+            mma_bf16(acc[nt][mt], a, pb[ch][nt][0], pb[ch][nt][1]);
         }
       }
     }
@@ -349,7 +389,7 @@ struct Consumer {
 
   // End of a split: sum l over the 8 lanes that share a column (they saw different
   // tokens) and write this warp's (m, l, acc) into the merge scratch
-  // macc [NCW][G][D], mm [NCW][G], ml [NCW][G].
+  // macc [NCW][G][D] (macc_index), mm [NCW][G], ml [NCW][G].
   __device__ __forceinline__ void store(const Params& p, float* macc, float* mm, float* ml,
                                         int warp, int lane) {
     constexpr int G = SH::G;
@@ -372,8 +412,8 @@ struct Consumer {
             // m-rows qr, qr + 8 of tile mt are dims 16 mt + (qr, qr + 8), or with FP8 KV
             // dims 16 mt + (2 qr, 2 qr + 1); the V scale applies to the whole output.
             const int d0 = SH::KV8 ? 2 * qr : qr, d1 = SH::KV8 ? 2 * qr + 1 : qr + 8;
-            macc[(warp * G + h) * SH::D + mt * 16 + d0] = acc[nt][mt][e] * vsc;
-            macc[(warp * G + h) * SH::D + mt * 16 + d1] = acc[nt][mt][2 + e] * vsc;
+            macc[macc_index<G, SH::D>(warp, h, mt * 16 + d0)] = acc[nt][mt][e] * vsc;
+            macc[macc_index<G, SH::D>(warp, h, mt * 16 + d1)] = acc[nt][mt][2 + e] * vsc;
           }
           if (qr == 0) {
             mm[warp * G + h] = m[nt][e];
@@ -499,7 +539,10 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   float* ml = mm + SH::NCW * G;                                   // [NCW][G]
   c.store(p, macc, mm, ml, warp, lane);
   named_bar_sync(1, SH::NCW * 32);
-  merge_warps_and_store<G, SH::D, SH::NCW>(p, si, macc, mm, ml, threadIdx.x);
+  merge_warps_and_store<G, SH::D, SH::NCW>(p, si, macc, mm, ml, threadIdx.x, [] {
+    named_bar_sync(1, SH::NCW * 32);
+    return true;
+  });
   if (p.counters != nullptr) arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
 }
 
@@ -608,8 +651,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
       mbar_init(smem_addr(&ctl->full[s]), 1);
       mbar_init(smem_addr(&ctl->empty[s]), SH::NCW);
     }
-    mbar_init(smem_addr(&ctl->epi[0]), SH::NCW);
-    mbar_init(smem_addr(&ctl->epi[1]), SH::NCW);
+    for (int i = 0; i < 3; ++i) mbar_init(smem_addr(&ctl->epi[i]), SH::NCW);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -677,7 +719,11 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
       si.b = mt.b;
       si.g = mt.g;
       si.split = mt.split;
-      merge_warps_and_store<G, SH::D, SH::NCW>(p, si, macc, ctl->mm, ctl->ml, threadIdx.x);
+      if (!merge_warps_and_store<G, SH::D, SH::NCW>(p, si, macc, ctl->mm, ctl->ml, threadIdx.x,
+                                                    [&] { return meet(2); })) {
+        give_up();
+        break;
+      }
       ++epi_phase;
       // Generic-proxy use of the stage ends before its next TMA fill.
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

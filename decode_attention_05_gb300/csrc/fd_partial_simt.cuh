@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
     }
   }
   // Intra-CTA merge of the four warps' (m, l, acc), through the drained stage buffers.
-  float* macc = reinterpret_cast<float*>(stages);                 // [NCW][G][D]
+  float* macc = reinterpret_cast<float*>(stages);                 // [NCW][G][D], swizzled
   float* mm = macc + SH::NCW * G * SH::D;                         // [NCW][G]
   float* ml = mm + SH::NCW * G;                                   // [NCW][G]
   if (rg == 0) {
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
     for (int h = 0; h < G; ++h)
       if (h < p.n_rows)
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) macc[(warp * G + h) * SH::D + li * EPL + e] = acc[h][e];
+        for (int e = 0; e < EPL; ++e) macc[macc_index<G, SH::D>(warp, h, li * EPL + e)] = acc[h][e];
   }
   if (lane == 0) {
 #pragma unroll
@@ -298,7 +298,10 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
     }
   }
   named_bar_sync(1, SH::NCW * 32);
-  merge_warps_and_store<G, SH::D, SH::NCW>(p, si, macc, mm, ml, threadIdx.x);
+  merge_warps_and_store<G, SH::D, SH::NCW>(p, si, macc, mm, ml, threadIdx.x, [] {
+    named_bar_sync(1, SH::NCW * 32);
+    return true;
+  });
   if (p.counters != nullptr) arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
 }
 

@@ -118,7 +118,7 @@ template <int STAGES>
 struct PersistCtl {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t epi[2];              // consumer warps meet here around an item's epilogue
+  uint64_t epi[3];              // consumer warps meet here around an item's epilogue
   TileMeta meta[STAGES];
   float mm[4 * 16], ml[4 * 16]; // per-warp running max and exp-sum of the item's rows
   int32_t abort;
