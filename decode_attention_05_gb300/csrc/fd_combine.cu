@@ -14,7 +14,8 @@
 // splits are all empty gets out = 0 and lse_out = -inf.
 //
 // Launched with programmatic dependent launch: the CTA waits (griddepcontrol.wait) for
-// the partial pass's memory to be visible before it reads the workspace.
+// the partial pass's memory to be visible before it reads the workspace, and lets the
+// next kernel of the stream start launching at once (that kernel waits in turn).
 #include <cuda_bf16.h>
 
 #include "fd_device.cuh"
@@ -29,6 +30,7 @@ __global__ void __launch_bounds__(128) fd_combine_kernel(const __grid_constant__
   constexpr float kLn2 = 0.6931471805599453f;
   __shared__ float wm[4], ww[4];
   __shared__ __align__(16) float accs[4][D];
+  pdl_trigger();                               // the next step's partial pass may launch
   pdl_wait();
 
   const int row = blockIdx.x;                  // (b * Q + j) * Hq + h

@@ -77,6 +77,26 @@ cudaError_t launch_partial_mma(const Params& p, const CUtensorMap& tk, const CUt
                                cudaStream_t stream);
 cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool pdl);
 
+// Launch a partial-pass kernel with programmatic dependent launch: its CTAs may be
+// scheduled while the previous kernel in the stream finishes; the kernel waits
+// (griddepcontrol.wait) before its first global memory access.
+template <class Kernel>
+cudaError_t launch_partial_kernel(Kernel kernel, dim3 grid, int threads, size_t smem,
+                                  cudaStream_t stream, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, const Params& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tk, tv, p);
+}
+
 // Record `message` as the calling thread's fd_last_error() and return `st`.
 fd_status record_error(fd_status st, const char* message);
 

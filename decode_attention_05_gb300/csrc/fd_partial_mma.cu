@@ -469,6 +469,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
                           const __grid_constant__ CUtensorMap tv,
                           const __grid_constant__ Params p) {
   constexpr int G = SH::G, TT = SH::TT, STAGES = SH::STAGES;
+  pdl_wait();                       // inputs of this step are visible
   const SplitInfo si = split_info<TT>(p);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>(
@@ -562,6 +563,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   constexpr int STAGES = SH::STAGES, TOK = 16;
   static_assert(SH::ROWS_PER_WARP == TOK && SH::CHUNKS == 1 && SH::NCW == kHeadGroup,
                 "one 16-token page slice per consumer warp");
+  pdl_wait();                       // inputs of this step are visible
   SplitInfo si = split_info<TOK>(p);
   si.g = blockIdx.y * kHeadGroup;                 // first kv head of the group
   extern __shared__ uint8_t smem_raw[];
@@ -640,6 +642,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
                               const __grid_constant__ CUtensorMap tv,
                               const __grid_constant__ Params p) {
   constexpr int G = SH::G, TT = SH::TT, STAGES = SH::STAGES;
+  pdl_wait();                       // inputs of this step are visible
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -749,7 +752,7 @@ cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap
     if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)p.S * p.Hkv * p.B;
     const unsigned grid = (unsigned)(items < 2 * sms ? items : 2 * sms);
-    kernel<<<grid, SH::THREADS, SH::SMEM_BYTES, stream>>>(tk, tv, p);
+    e = launch_partial_kernel(kernel, dim3(grid), SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
   } else if (p.head_group) {
     if constexpr (SH::D == 128 && !SH::KV8) {
       auto kernel = fd_partial_heads_kernel<SH>;
@@ -757,7 +760,7 @@ cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap
                                (int)SH::SMEM_BYTES);
       if (e != cudaSuccess) return e;
       dim3 grid((unsigned)p.S, (unsigned)(p.Hkv / kHeadGroup), (unsigned)p.B);
-      kernel<<<grid, SH::THREADS, SH::SMEM_BYTES, stream>>>(tk, tv, p);
+      e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
     } else {
       return cudaErrorInvalidValue;   // the host enables head groups for bf16 d = 128 only
     }
@@ -767,8 +770,9 @@ cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap
                              (int)SH::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
-    kernel<<<grid, SH::THREADS, SH::SMEM_BYTES, stream>>>(tk, tv, p);
+    e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

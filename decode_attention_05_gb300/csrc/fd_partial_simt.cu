@@ -15,7 +15,8 @@ cudaError_t launch_simt(const Params& p, const CUtensorMap& tk, const CUtensorMa
                                        (int)SH::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
-  kernel<<<grid, SH::THREADS, SH::SMEM_BYTES, stream>>>(tk, tv, p);
+  e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

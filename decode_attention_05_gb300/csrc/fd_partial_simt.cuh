@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
                            const __grid_constant__ Params p) {
   constexpr int G = SH::G, EPL = SH::EPL, LPR = SH::LPR, RPW = SH::RPW, TT = SH::TT;
   constexpr int STAGES = SH::STAGES;
+  pdl_wait();                       // inputs of this step are visible
   const SplitInfo si = split_info<TT>(p);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>(
