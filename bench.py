@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="issue every timed call from Python instead of replaying CUDA graphs")
     return ap.parse_args()
 
 
@@ -323,6 +325,44 @@ def run_fd(args):
         if st:
             raise fd.FdError(st, L.fd_last_error().decode())
 
+    # Timed loops replay a CUDA graph of GRAPH_CHUNK back-to-back calls (as a decode loop
+    # would run them), so that the host's per-call cost stays out of the device time;
+    # exactly n calls are issued either way.  call(stream_handle) issues one call.
+    GRAPH_CHUNK = 100
+
+    def checked(st):
+        if st:
+            raise fd.FdError(st, L.fd_last_error().decode())
+
+    def make_graph(call, chunk):
+        if args.no_graph:
+            return None
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            for _ in range(2):
+                call(cap.cuda_stream)
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for _ in range(chunk):
+                call(cap.cuda_stream)
+        torch.cuda.synchronize()
+        return g
+
+    def issue(call, graph, n):
+        if graph is None:
+            for _ in range(n):
+                call(sh)
+            return
+        for _ in range(n // GRAPH_CHUNK):
+            graph.replay()
+        for _ in range(n % GRAPH_CHUNK):
+            call(sh)
+
+    step_call = lambda s: checked(L.fd_decode_attention(*args_step[:-1], s))
+
     def barrier():
         torch.cuda.synchronize()
         if world > 1:
@@ -332,6 +372,9 @@ def run_fd(args):
     kv_bytes = w.kv_bytes()
     for _ in range(max(3, args.warmup)):
         step()
+    step_graph = make_graph(step_call, GRAPH_CHUNK)
+    if step_graph is not None:
+        step_graph.replay()
     if fd.read_device_error(ws) != 0:
         raise RuntimeError("device error flags set during warm-up")
 
@@ -341,8 +384,7 @@ def run_fd(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
     e0.record(stream)
-    for _ in range(args.steps):
-        step()
+    issue(step_call, step_graph, args.steps)
     e1.record(stream)
     e1.synchronize()
     t_wall1 = time.time()
@@ -355,26 +397,28 @@ def run_fd(args):
 
     # ---- roofline of the dominant kernel: the partial pass alone, K launches
     args_partial = (ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), w.seq_lens.data_ptr(),
-                    bt_ref, w.page_size, S, ws.data_ptr(), ws_bytes, sh)
+                    bt_ref, w.page_size, S, ws.data_ptr(), ws_bytes)
+    partial_call = lambda s: checked(L.fd_decode_partial(*args_partial, s))
     for _ in range(3):
-        L.fd_decode_partial(*args_partial)
+        partial_call(sh)
+    partial_graph = make_graph(partial_call, GRAPH_CHUNK)
     barrier()
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2.record(stream)
-    for _ in range(args.steps):
-        st = L.fd_decode_partial(*args_partial)
-        if st:
-            raise fd.FdError(st, L.fd_last_error().decode())
+    issue(partial_call, partial_graph, args.steps)
     e3.record(stream)
     e3.synchronize()
     partial_ms = e2.elapsed_time(e3) / args.steps
     lse_part, o_part = fd.workspace_partials(ws, B, Hq, d, S)
     dout = tensor_desc(out)
+    merge_call = lambda s: checked(L.fd_merge_partials(B, Hq, d, S, lse_part.data_ptr(),
+                                                       o_part.data_ptr(), ctypes.byref(dout),
+                                                       lse.data_ptr(), s))
+    merge_graph = make_graph(merge_call, GRAPH_CHUNK)
+    barrier()
     e4, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e4.record(stream)
-    for _ in range(args.steps):
-        L.fd_merge_partials(B, Hq, d, S, lse_part.data_ptr(), o_part.data_ptr(),
-                            ctypes.byref(dout), lse.data_ptr(), sh)
+    issue(merge_call, merge_graph, args.steps)
     e5.record(stream)
     e5.synchronize()
     merge_ms = e4.elapsed_time(e5) / args.steps
@@ -439,7 +483,10 @@ def run_fd(args):
                        "L": int(w.seq_lens.max()), "num_splits": S, "path": path_name,
                        "kv_bytes_per_step": kv_bytes,
                        "l2": "inputs larger than L2 (KV %d MiB vs 126 MiB L2), no flush" % (kv_bytes >> 20),
-                       "parallelism": "replicas x%d" % world},
+                       "parallelism": "replicas x%d" % world,
+                       "launch": ("direct calls" if args.no_graph else
+                                  "CUDA graphs of %d back-to-back decode calls, replayed"
+                                  % GRAPH_CHUNK)},
             "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
             "gpu_launches": 2 * args.steps,
         }
