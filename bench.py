@@ -26,6 +26,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import dataclasses
 import datetime
 import hashlib
 import json
@@ -59,6 +60,9 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="KV cache storage: the workload's own, or FP8 E4M3 codes with "
+                         "per-kv-head scales (decode over the quantised cache)")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue every timed call from Python instead of replaying CUDA graphs")
     return ap.parse_args()
@@ -181,7 +185,34 @@ class ClockSampler:
                 "samples": len(inside)}
 
 
-def oracle_sample(w, budget_s: float):
+def fp8_variant(w):
+    """The workload with its K/V cache quantised to FP8 E4M3 codes (per-kv-head scales);
+    returns (workload, k_scale, v_scale)."""
+    kc, vc, ks, vs = workloads.fp8_quantize(w)
+    w8 = dataclasses.replace(w, name=w.name + ", FP8 E4M3 KV", k=kc, v=vc)
+    return w8, ks, vs
+
+
+def oracle_decoder(w, scales=None):
+    """(decode(seq_lens, rows), seq_lens) running the oracle on the workload's stored
+    values: the bf16/f32 decode, or the FP8 one when scales are given."""
+    import oracle
+    if scales is None:
+        q, k, v, lens, bt, ps = w.oracle_arrays()
+        return (lambda seq, rows=None: oracle.decode(q, k, v, seq, block_table=bt,
+                                                      page_size=ps, rows=rows)), lens
+    q = workloads.np_storage(w.q)
+    kc = w.k.view(torch.uint8).numpy()
+    vc = w.v.view(torch.uint8).numpy()
+    ks, vs = scales[0].numpy(), scales[1].numpy()
+    lens = w.seq_lens.numpy()
+    bt = None if w.block_table is None else w.block_table.numpy()
+    ps = w.page_size
+    return (lambda seq, rows=None: oracle.decode_kv8(q, kc, vc, ks, vs, seq, block_table=bt,
+                                                      page_size=ps, rows=rows)), lens
+
+
+def oracle_sample(w, budget_s: float, scales=None):
     """Time the fp64 oracle (as it stands) on a bounded sample of the workload.
 
     If a whole step fits the budget, whole steps are repeated until about `budget_s`
@@ -192,7 +223,7 @@ def oracle_sample(w, budget_s: float):
     import statistics
 
     import oracle
-    q, k, v, lens, bt, ps = w.oracle_arrays()
+    run, lens = oracle_decoder(w, scales)
     threads = oracle.max_threads()
     n_rows = w.B * w.Hq
     L = int(lens.max())
@@ -200,7 +231,7 @@ def oracle_sample(w, budget_s: float):
 
     def timed(seq, rows=None):
         t0 = time.perf_counter()
-        oracle.decode(q, k, v, seq, block_table=bt, page_size=ps, rows=rows)
+        run(seq, rows)
         return time.perf_counter() - t0
 
     probe_tokens = min(L, 2048)
@@ -245,8 +276,12 @@ def run_reference(args):
     if rank != 0:
         return 0
     w = workloads.CONFIGS[args.config]()
+    scales = None
+    if args.kv == "fp8":
+        w, ks, vs = fp8_variant(w)
+        scales = (ks, vs)
     import oracle
-    q, k, v, lens, bt, ps = w.oracle_arrays()
+    run, lens = oracle_decoder(w, scales)
     threads = oracle.max_threads()
     B, Hq = w.B, w.Hq
     rows = list(range(0, B * Hq, max(1, (B * Hq) // threads)))[:threads]
@@ -255,16 +290,16 @@ def run_reference(args):
     sl = lens.copy()
     sl[:] = min(L, 1024)
     t0 = time.perf_counter()
-    oracle.decode(q, k, v, sl, block_table=bt, page_size=ps, rows=rows)
+    run(sl, rows)
     t_probe = time.perf_counter() - t0
     per_step = 90.0 / max(1, args.steps + args.warmup)
     tokens = int(max(16, min(L, 1024 * per_step / max(t_probe, 1e-6))))
     sl[:] = tokens
     for _ in range(args.warmup):
-        oracle.decode(q, k, v, sl, block_table=bt, page_size=ps, rows=rows)
+        run(sl, rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.decode(q, k, v, sl, block_table=bt, page_size=ps, rows=rows)
+        run(sl, rows)
     elapsed = time.perf_counter() - t0
     frac = (len(rows) / (B * Hq)) * (tokens / L)
     step_s = elapsed / args.steps / frac
@@ -300,7 +335,12 @@ def run_fd(args):
     fd.set_path({"auto": fd.FD_PATH_AUTO, "simt": fd.FD_PATH_SIMT, "mma": fd.FD_PATH_MMA}[args.path])
 
     w_cpu = workloads.CONFIGS[args.config]()
+    scales_cpu = None
+    if args.kv == "fp8":
+        w_cpu, ks, vs = fp8_variant(w_cpu)
+        scales_cpu = (ks, vs)
     w = w_cpu.to("cuda")
+    scales = None if scales_cpu is None else tuple(t.cuda() for t in scales_cpu)
     B, Hq, d, Hkv = w.B, w.Hq, w.d, w.Hkv
     S = args.num_splits or w.num_splits
     if S == 0:          # the lengths are known here: plan with them
@@ -316,12 +356,18 @@ def run_fd(args):
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream or None
     ws_bytes = ws.numel()
-    args_step = (ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), w.seq_lens.data_ptr(),
-                 bt_ref, w.page_size, S, ctypes.byref(do), lse.data_ptr(), ws.data_ptr(),
-                 ws_bytes, sh)
+    if scales is None:
+        decode_fn, partial_fn = L.fd_decode_attention, L.fd_decode_partial
+        kv_args = (ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv))
+    else:
+        decode_fn, partial_fn = L.fd_decode_attention_fp8kv, L.fd_decode_partial_fp8kv
+        kv_args = (ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), scales[0].data_ptr(),
+                   scales[1].data_ptr())
+    args_step = kv_args + (w.seq_lens.data_ptr(), bt_ref, w.page_size, S, ctypes.byref(do),
+                           lse.data_ptr(), ws.data_ptr(), ws_bytes, sh)
 
     def step():
-        st = L.fd_decode_attention(*args_step)
+        st = decode_fn(*args_step)
         if st:
             raise fd.FdError(st, L.fd_last_error().decode())
 
@@ -361,7 +407,7 @@ def run_fd(args):
         for _ in range(n % GRAPH_CHUNK):
             call(sh)
 
-    step_call = lambda s: checked(L.fd_decode_attention(*args_step[:-1], s))
+    step_call = lambda s: checked(decode_fn(*args_step[:-1], s))
 
     def barrier():
         torch.cuda.synchronize()
@@ -396,9 +442,9 @@ def run_fd(args):
     value = world * kv_bytes * args.steps / (ms * 1e-3) / 1e9
 
     # ---- roofline of the dominant kernel: the partial pass alone, K launches
-    args_partial = (ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), w.seq_lens.data_ptr(),
-                    bt_ref, w.page_size, S, ws.data_ptr(), ws_bytes)
-    partial_call = lambda s: checked(L.fd_decode_partial(*args_partial, s))
+    args_partial = kv_args + (w.seq_lens.data_ptr(), bt_ref, w.page_size, S, ws.data_ptr(),
+                              ws_bytes)
+    partial_call = lambda s: checked(partial_fn(*args_partial, s))
     for _ in range(3):
         partial_call(sh)
     partial_graph = make_graph(partial_call, GRAPH_CHUNK)
@@ -435,9 +481,10 @@ def run_fd(args):
     # ---- end to end through the public API, host buffers, copies inside the timed region
     pin = lambda t: t.pin_memory()
     qh, kh, vh, sh_lens = pin(w_cpu.q), pin(w_cpu.k), pin(w_cpu.v), pin(w_cpu.seq_lens)
+    scales_h = () if scales_cpu is None else tuple(pin(t) for t in scales_cpu)
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh, sh_lens))
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh, sh_lens) + scales_h)
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
 
     def e2e_step():
@@ -445,8 +492,15 @@ def run_fd(args):
         w.k.copy_(kh, non_blocking=True)
         w.v.copy_(vh, non_blocking=True)
         w.seq_lens.copy_(sh_lens, non_blocking=True)
-        fd.decode_attention(w.q, w.k, w.v, w.seq_lens, w.block_table, w.page_size, S, out=out,
-                            lse_out=lse, workspace=ws)
+        if scales is None:
+            fd.decode_attention(w.q, w.k, w.v, w.seq_lens, w.block_table, w.page_size, S,
+                                out=out, lse_out=lse, workspace=ws)
+        else:
+            for dst, src in zip(scales, scales_h):
+                dst.copy_(src, non_blocking=True)
+            fd.decode_attention_fp8kv(w.q, w.k, w.v, scales[0], scales[1], w.seq_lens,
+                                      w.block_table, w.page_size, S, out=out, lse_out=lse,
+                                      workspace=ws)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
 
@@ -467,7 +521,7 @@ def run_fd(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, cores, desc, _, step_s = oracle_sample(w_cpu, args.cpu_budget_s)
+        gbs, cores, desc, _, step_s = oracle_sample(w_cpu, args.cpu_budget_s, scales_cpu)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": desc, "step_ms_extrapolated": round(step_s * 1e3, 1)}
 
@@ -478,7 +532,9 @@ def run_fd(args):
             "us_per_step": round(ms_per_step * 1e3, 2),
             "hbm_frac_step": round(value / world / peak, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if w.q.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+            "dtype": ("bf16" if w.q.dtype == torch.bfloat16 else "f32") +
+                     ("+e4m3 KV" if scales is not None else ""),
+            "data": "synthetic",
             "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d,
                        "L": int(w.seq_lens.max()), "num_splits": S, "path": path_name,
                        "kv_bytes_per_step": kv_bytes,

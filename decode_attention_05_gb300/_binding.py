@@ -69,6 +69,8 @@ def _declare(L):
     L.fd_decode_attention_fp8kv.argtypes = [P, P, P, vp, vp, vp, P, i32, i32, P, vp, vp, sz, vp]
     L.fd_decode_partial.restype = ctypes.c_int
     L.fd_decode_partial.argtypes = [P, P, P, vp, P, i32, i32, vp, sz, vp]
+    L.fd_decode_partial_fp8kv.restype = ctypes.c_int
+    L.fd_decode_partial_fp8kv.argtypes = [P, P, P, vp, vp, vp, P, i32, i32, vp, sz, vp]
     L.fd_workspace_partials.restype = ctypes.c_int
     L.fd_workspace_partials.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(vp),
                                         ctypes.POINTER(vp)]
@@ -329,6 +331,22 @@ def decode_partial(q, k_cache, v_cache, seq_lens, workspace: torch.Tensor, block
                                    seq_lens.data_ptr(), _ref(dbt), page_size, S,
                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                    _stream_handle(stream)))
+    return S
+
+
+def decode_partial_fp8kv(q, k_cache, v_cache, k_scale, v_scale, seq_lens,
+                         workspace: torch.Tensor, block_table=None, page_size: int = 0,
+                         num_splits: int = 0, stream=None) -> int:
+    """Partial pass over an FP8 E4M3 cache (fd_decode_partial_fp8kv); returns S."""
+    B, Hq, d = q.shape[0], q.shape[-2], q.shape[-1]
+    S = resolve_num_splits(B, Hq, k_cache.shape[1], d, _cap(k_cache, block_table, page_size),
+                           num_splits)
+    dq, dk, dv, dbt = tensor_desc(q), tensor_desc(k_cache), tensor_desc(v_cache), tensor_desc(block_table)
+    ptr = lambda t: None if t is None else t.data_ptr()
+    _check(lib().fd_decode_partial_fp8kv(
+        ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), ptr(k_scale), ptr(v_scale),
+        seq_lens.data_ptr(), _ref(dbt), page_size, S, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream)))
     return S
 
 

@@ -582,6 +582,21 @@ fd_status fd_decode_attention_fp8kv(const fd_tensor* q, const fd_tensor* k_cache
   return launch_merge(pr.p, (cudaStream_t)stream);
 }
 
+fd_status fd_decode_partial_fp8kv(const fd_tensor* q, const fd_tensor* k_cache,
+                                 const fd_tensor* v_cache, const float* k_scale,
+                                 const float* v_scale, const int32_t* seq_lens,
+                                 const fd_tensor* block_table, int32_t page_size,
+                                 int32_t num_splits, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  Prepared pr;
+  fd_status st = prepare(q, k_cache, v_cache, seq_lens, block_table, page_size, num_splits,
+                         nullptr, nullptr, workspace, workspace_bytes, false, &pr, true, k_scale,
+                         v_scale);
+  if (st != FD_OK) return st;
+  pr.p.counters = nullptr;          // partials only: the merge is a separate call
+  return launch_partial(pr, (cudaStream_t)stream);
+}
+
 fd_status fd_workspace_partials(void* workspace, int32_t B, int32_t Hq, int32_t d,
                                 int32_t num_splits, float** lse_part, float** o_part) {
   if (!workspace || B <= 0 || Hq <= 0 || d <= 0 || num_splits <= 0 || num_splits > kMaxSplits)

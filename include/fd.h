@@ -174,6 +174,18 @@ FD_API fd_status fd_decode_partial(const fd_tensor* q, const fd_tensor* k_cache,
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fd_decode_partial_fp8kv: the partial pass over an FP8 E4M3 KV cache, with the
+ * arguments and checks of fd_decode_attention_fp8kv without out / lse_out; writes the
+ * same workspace partials as fd_decode_partial (merge them with fd_merge_partials).
+ */
+FD_API fd_status fd_decode_partial_fp8kv(const fd_tensor* q, const fd_tensor* k_cache,
+                                         const fd_tensor* v_cache, const float* k_scale,
+                                         const float* v_scale, const int32_t* seq_lens,
+                                         const fd_tensor* block_table, int32_t page_size,
+                                         int32_t num_splits, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
+/*
  * Where a workspace keeps the partials of a call with these sizes: *lse_part is
  * f32 [B, Hq, S] (natural log, -inf for an empty split) and *o_part f32 [B, Hq, S, d].
  * Host arithmetic only; either output pointer may be NULL.

@@ -548,3 +548,26 @@ def test_fp8_kv_is_refused_by_the_bf16_entry_point():
     with pytest.raises(fd.FdError):                   # CUDA-core path has no FP8 tile
         fd.set_path(fd.FD_PATH_SIMT)
         fd.decode_attention_fp8kv(w.q, kc, kc, None, None, w.seq_lens, num_splits=1)
+
+
+def test_fp8_kv_partials_then_merge():
+    """fd_decode_partial_fp8kv followed by fd_merge_partials gives what the one-call FP8
+    decode gives (same partial kernel, same merge kernel), and matches the oracle."""
+    w = workloads.paged_case(3, 32, 8, 128, 16, 128, [2048, 37, 1500], seed=321)
+    kc, vc, ks, vs = workloads.fp8_quantize(w)
+    q, _, _, lens, bt, ps = w.oracle_arrays()
+    ref_o, ref_l = oracle.decode_kv8(q, _fp8_views(kc), _fp8_views(vc), ks.numpy(), vs.numpy(),
+                                     lens, block_table=bt, page_size=ps)
+    wd = w.to("cuda")
+    kcd, vcd, ksd, vsd = kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda()
+    S = 7
+    ws = torch.zeros(fd.workspace_size(3, 32, 8, 128, S), dtype=torch.uint8, device="cuda")
+    fd.decode_partial_fp8kv(wd.q, kcd, vcd, ksd, vsd, wd.seq_lens, ws, wd.block_table, 16, S)
+    lp, op = fd.workspace_partials(ws, 3, 32, 128, S)
+    o2, l2 = fd.merge_partials(lp, op, out_dtype=torch.float32)
+    o1, l1 = fd.decode_attention_fp8kv(wd.q, kcd, vcd, ksd, vsd, wd.seq_lens, wd.block_table,
+                                       16, S, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fd.read_device_error(ws) == 0
+    check(w, o2.cpu().double().numpy(), l2.cpu().double().numpy(), ref_o, ref_l)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
