@@ -96,7 +96,9 @@ __device__ __forceinline__ void load_q_slice(const void* q, int64_t off, float (
 }
 
 template <class SH>
-__global__ void __launch_bounds__(SH::THREADS, 2)
+// Two CTAs of 160 threads per SM leave 204 registers per thread; __launch_bounds__ would
+// budget for 192-thread CTAs and cap at 168, which spills the wide GQA accumulators.
+__global__ void __maxnreg__(200)
     fd_partial_simt_kernel(const __grid_constant__ CUtensorMap tk,
                            const __grid_constant__ CUtensorMap tv,
                            const __grid_constant__ Params p) {
