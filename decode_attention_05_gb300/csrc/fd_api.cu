@@ -57,8 +57,8 @@ fd_status fail(fd_status st, const char* fmt, ...) {
 
 constexpr size_t kAlign = 256;
 // Header: device error flags (u32 at 0), the persistent schedule's item queue and
-// done counter (u64 at kQueueOff, kDoneOff; epoch-tagged like the merge tickets, so
-// they need no particular contents either).
+// done counter (u64 at kQueueOff, kDoneOff: plain fetch-add counters, zero between
+// launches -- a fresh header is zero and the last CTA of each launch resets them).
 constexpr size_t kHeaderBytes = 256;
 constexpr size_t kQueueOff = 64, kDoneOff = 128;
 constexpr int32_t kMaxSplits = 4096;

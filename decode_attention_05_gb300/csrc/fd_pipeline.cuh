@@ -70,8 +70,8 @@ __device__ __forceinline__ int64_t key_bound(const Params& p, int64_t L, int rho
   return L - p.Q + 1 + rho / p.G;
 }
 
-// Take a ticket on an epoch-tagged counter word (the fused merge's per-group arrivals,
-// the persistent schedule's work queue).  A counter word holds
+// Take a ticket on an epoch-tagged counter word (the fused merge's per-group
+// arrivals).  A counter word holds
 // (epoch << 32 | arrivals).  Each call brings a fresh epoch, so the first arrival of a
 // call restarts the count whatever the word held before (a workspace reused with other
 // sizes, stale data); the last arrival also puts the word back to 0, so a launch that

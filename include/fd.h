@@ -120,10 +120,12 @@ typedef enum {
  *   lse_out      device f32 [B, Hq] or [B, Q, Hq] (contiguous), natural log; may be NULL.
  *   workspace    device scratch of at least fd_workspace_size(B, Q * Hq, Hkv, d, S) bytes,
  *                256-byte aligned, zero-filled once before its first use
- *                (fd_workspace_init) so that its device error flags start clear; flags
- *                stay set until fd_read_device_error clears them.  Nothing else in it
- *                needs particular contents: one workspace serves calls of any sizes
- *                that fit it.  Two calls in flight at once must not share a workspace.
+ *                (fd_workspace_init) so that its 256-byte header starts clear: the
+ *                device error flags (they stay set until fd_read_device_error clears
+ *                them) and the persistent schedule's queue words (every launch leaves
+ *                them zero).  Nothing else in it needs particular contents: one
+ *                workspace serves calls of any sizes that fit it.  Two calls in flight
+ *                at once must not share a workspace.
  *   stream       cudaStream_t (as void*), NULL = legacy default stream.
  *
  * Supported: d in {64, 128}; G = Hq / Hkv in {1, 2, 4, 8, 16}; (q, k, v) all bf16
