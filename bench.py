@@ -110,13 +110,23 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source without comments and with whitespace runs collapsed, so that an
+    ncu record stays tied to the code and not to its comments."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel: str) -> str:
-    """Hash of the source files that define `kernel` (ties an ncu record to them)."""
+    """Hash of the code of the source files that define `kernel` (ties an ncu record to
+    them; comments and layout do not count)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_attention_05_gb300", "csrc")
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
