@@ -45,6 +45,7 @@ import workloads  # noqa: E402
 
 METRIC = "decode-step µs and KV-read GB/s (% of GB300 HBM peak), GQA 128K ctx"
 FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 126 << 20          # GB300 L2 as the runtime reports it
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -366,18 +367,31 @@ def run_fd(args):
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream or None
     ws_bytes = ws.numel()
+    # A cache smaller than three L2s is streamed from alternating copies, so that no
+    # step finds the previous step's KV in L2.
+    kv_bytes = w.kv_bytes()
+    n_sets = 2 if kv_bytes < 3 * L2_BYTES else 1
+    kv_sets = [(w.k, w.v)] + [(w.k.clone(), w.v.clone()) for _ in range(n_sets - 1)]
+    kv_descs = [(tensor_desc(k), tensor_desc(v)) for k, v in kv_sets]
     if scales is None:
         decode_fn, partial_fn = L.fd_decode_attention, L.fd_decode_partial
-        kv_args = (ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv))
+        kv_args = [(ctypes.byref(dq), ctypes.byref(dk_), ctypes.byref(dv_))
+                   for dk_, dv_ in kv_descs]
     else:
         decode_fn, partial_fn = L.fd_decode_attention_fp8kv, L.fd_decode_partial_fp8kv
-        kv_args = (ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), scales[0].data_ptr(),
-                   scales[1].data_ptr())
-    args_step = kv_args + (w.seq_lens.data_ptr(), bt_ref, w.page_size, S, ctypes.byref(do),
-                           lse.data_ptr(), ws.data_ptr(), ws_bytes, sh)
+        kv_args = [(ctypes.byref(dq), ctypes.byref(dk_), ctypes.byref(dv_), scales[0].data_ptr(),
+                    scales[1].data_ptr()) for dk_, dv_ in kv_descs]
+    step_args = [a + (w.seq_lens.data_ptr(), bt_ref, w.page_size, S, ctypes.byref(do),
+                      lse.data_ptr(), ws.data_ptr(), ws_bytes) for a in kv_args]
+    turn = [0]
+
+    def next_set():
+        i = turn[0] % n_sets
+        turn[0] += 1
+        return i
 
     def step():
-        st = decode_fn(*args_step)
+        st = decode_fn(*step_args[next_set()], sh)
         if st:
             raise fd.FdError(st, L.fd_last_error().decode())
 
@@ -417,7 +431,7 @@ def run_fd(args):
         for _ in range(n % GRAPH_CHUNK):
             call(sh)
 
-    step_call = lambda s: checked(decode_fn(*args_step[:-1], s))
+    step_call = lambda s: checked(decode_fn(*step_args[next_set()], s))
 
     def barrier():
         torch.cuda.synchronize()
@@ -425,7 +439,6 @@ def run_fd(args):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    kv_bytes = w.kv_bytes()
     for _ in range(max(3, args.warmup)):
         step()
     step_graph = make_graph(step_call, GRAPH_CHUNK)
@@ -452,9 +465,9 @@ def run_fd(args):
     value = world * kv_bytes * args.steps / (ms * 1e-3) / 1e9
 
     # ---- roofline of the dominant kernel: the partial pass alone, K launches
-    args_partial = kv_args + (w.seq_lens.data_ptr(), bt_ref, w.page_size, S, ws.data_ptr(),
-                              ws_bytes)
-    partial_call = lambda s: checked(partial_fn(*args_partial, s))
+    partial_args = [a + (w.seq_lens.data_ptr(), bt_ref, w.page_size, S, ws.data_ptr(), ws_bytes)
+                    for a in kv_args]
+    partial_call = lambda s: checked(partial_fn(*partial_args[next_set()], s))
     for _ in range(3):
         partial_call(sh)
     partial_graph = make_graph(partial_call, GRAPH_CHUNK)
@@ -548,7 +561,10 @@ def run_fd(args):
             "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d,
                        "L": int(w.seq_lens.max()), "num_splits": S, "path": path_name,
                        "kv_bytes_per_step": kv_bytes,
-                       "l2": "inputs larger than L2 (KV %d MiB vs 126 MiB L2), no flush" % (kv_bytes >> 20),
+                       "l2": ("inputs larger than L2 (KV %d MiB vs 126 MiB L2), no flush" %
+                              (kv_bytes >> 20) if n_sets == 1 else
+                              "KV %d MiB < 3 x 126 MiB L2: steps alternate between %d copies "
+                              "of the cache, no flush" % (kv_bytes >> 20, n_sets)),
                        "parallelism": "replicas x%d" % world,
                        "launch": ("direct calls" if args.no_graph else
                                   "CUDA graphs of %d back-to-back decode calls, replayed"
