@@ -571,3 +571,45 @@ def test_fp8_kv_partials_then_merge():
     assert fd.read_device_error(ws) == 0
     check(w, o2.cpu().double().numpy(), l2.cpu().double().numpy(), ref_o, ref_l)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_bench_launch_configuration():
+    """The 128K GQA workload run the way bench.py times it: planned split count, a CUDA
+    graph of back-to-back decode calls (programmatic dependent launch between them)
+    replayed several times, then the partial pass alone the same way followed by one
+    merge.  Every output against the oracle."""
+    w, wd = cached(3)
+    ref_o, ref_l = ref_for(w, "c3")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    S = fd.num_splits_for_lengths(1, 64, 8, 128, 131072, w.seq_lens.tolist(), sms)
+    ws = torch.zeros(fd.workspace_size(1, 64, 8, 128, S), dtype=torch.uint8, device="cuda")
+    out = torch.empty(1, 64, 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(1, 64, dtype=torch.float32, device="cuda")
+    step = lambda: fd.decode_attention(wd.q, wd.k, wd.v, wd.seq_lens, None, 0, S, out=out,
+                                       lse_out=lse, workspace=ws)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(20):
+            step()
+    out.zero_()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert fd.read_device_error(ws) == 0
+    check(w, out.float().cpu().double().numpy(), lse.cpu().double().numpy(), ref_o, ref_l)
+    # partial pass back to back, then the merge of the last one's partials
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2):
+        for _ in range(10):
+            fd.decode_partial(wd.q, wd.k, wd.v, wd.seq_lens, ws, None, 0, S)
+    g2.replay()
+    lp, op = fd.workspace_partials(ws, 1, 64, 128, S)
+    o2, l2 = fd.merge_partials(lp, op, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    check(w, o2.cpu().double().numpy(), l2.cpu().double().numpy(), ref_o, ref_l)
