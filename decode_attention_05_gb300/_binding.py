@@ -112,6 +112,8 @@ def _declare(L):
     L.fd_set_schedule.argtypes = [i32]
     L.fd_get_schedule.restype = i32
     L.fd_get_schedule.argtypes = []
+    L.fd_selftest_bounded_wait.restype = ctypes.c_int
+    L.fd_selftest_bounded_wait.argtypes = [vp, ctypes.c_uint32, vp]
     L.fd_partial_kernel_name.restype = ctypes.c_char_p
     L.fd_partial_kernel_name.argtypes = [i32, i32, i32, i32, i32, i32]
     L.fd_get_path.restype = i32
@@ -206,6 +208,12 @@ def set_schedule(schedule: int):
 
 def get_schedule() -> int:
     return int(lib().fd_get_schedule())
+
+
+def selftest_bounded_wait(workspace: torch.Tensor, limit_us: int = 50000, stream=None):
+    """fd_selftest_bounded_wait: a kernel whose wait runs out must flag a timeout."""
+    _check(lib().fd_selftest_bounded_wait(workspace.data_ptr(), limit_us,
+                                          _stream_handle(stream)))
 
 
 def partial_kernel_name(dtype, kv_dtype, d: int, Hkv: int, page_size: int = 0,

@@ -269,6 +269,17 @@ FD_API int32_t fd_num_splits_for_lengths(int32_t B, int32_t Hq, int32_t Hkv, int
 /* Zero-fill a workspace on `stream` (asynchronous).  Needed once before first use. */
 FD_API fd_status fd_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Self-test of the failure path (no counterpart on the pages): launches one CTA that
+ * waits, with the kernels' own bounded wait, on an mbarrier that nothing completes.
+ * After limit_us microseconds (1 .. 2,000,000) the wait gives up and raises
+ * FD_DEVFLAG_TIMEOUT in the workspace header, as a partial kernel does when its copy
+ * ring stalls.  Read it with fd_read_device_error; the context stays usable.
+ * Asynchronous on `stream`.  FD_ERR_INVALID_ARG for a NULL workspace or a limit out of
+ * range.
+ */
+FD_API fd_status fd_selftest_bounded_wait(void* workspace, uint32_t limit_us, void* stream);
+
 /* Device-side error flags kept in the workspace header (bitwise OR). */
 #define FD_DEVFLAG_SEQ_LEN 1u   /* a seq_lens entry was outside [0, L_cap] (clamped)  */
 #define FD_DEVFLAG_PAGE 2u      /* a used block-table entry was outside [0, num_pages) */
