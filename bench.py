@@ -1,6 +1,7 @@
 """Benchmark: one decode step of split-KV attention on the 128K-context GQA workload.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
+                    [--config 1-5] [--kv bf16|fp8] [--num-splits S] [--no-graph]
 
 Workload (default): bf16, B=1, Hq=64, Hkv=8 (G=8), d=128, L=131072, contiguous KV
 cache (512 MiB of K+V, four times the L2), split count from the library's length-aware
@@ -10,7 +11,10 @@ merge kernel, through the C ABI (fd_decode_attention).
 
 Prints ONE JSON line.  ``value`` is the whole-job KV-read throughput (GB/s) over the
 K timed steps (device time, CUDA events, max over ranks); ``ms_per_step`` and
-``us_per_step`` give the step time.  Also reported:
+``us_per_step`` give the step time.  The timed loops replay CUDA graphs of 100
+back-to-back calls (``--no-graph``: one call at a time from Python); a cache smaller
+than three L2s is streamed from two alternating copies.  ``--kv fp8`` runs the same
+workload over its FP8 E4M3 quantisation (per-kv-head scales).  Also reported:
   roofline      the partial kernel alone: algorithmic KV bytes per launch / its mean
                 CUDA-event duration, against the measured HBM copy bandwidth;
   e2e           the same metric through the public Python API with the step's inputs
