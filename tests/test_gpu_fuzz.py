@@ -1,8 +1,8 @@
 """Seeded random parity cases: shapes, layouts, lengths, split counts, query tokens,
 cache formats and schedules drawn together, each checked element by element against
 the fp64 oracle with the tolerances of test_gpu_parity.  Sizes stay small, so the
-oracle finishes each case in well under a second; every case prints its draw when it
-fails, and the seed of case i is 7000 + i."""
+oracle finishes each case in about a second at most; every case prints its draw when
+it fails, and the seed of case i is 7000 + i (medium cases: i = 100000 + j)."""
 import random
 
 import numpy as np
@@ -29,7 +29,7 @@ def _restore_settings():
         fd.set_merge_mode(fd.FD_MERGE_KERNEL)
 
 
-def draw(i):
+def draw(i, medium=False):
     r = random.Random(7000 + i)
     d = r.choice([64, 128, 128])
     fp8 = d == 128 and r.random() < 0.2
@@ -41,10 +41,13 @@ def draw(i):
     paged = r.random() < 0.5
     ps = r.choice([8, 16, 32, 64, 128]) if paged else 0
     cap = r.choice([64, 200, 1000, 2048, 3000])
+    if medium:                      # multi-wave grids, page-table windows past 32 pages
+        cap = r.choice([8192, 20000, 32768])
+        B = r.randint(1, 8)
     if paged:
         cap = -(-cap // ps) * ps
     lens = [r.choice([0, 1, r.randint(1, cap), cap, r.randint(cap // 2, cap)]) for _ in range(B)]
-    S = r.choice([0, 1, 2, 5, 16, 64])
+    S = r.choice([0, 1, 2, 5, 16, 64] + ([128, 300, 512] if medium else []))
     sched = r.choice([fd.FD_SCHEDULE_AUTO, fd.FD_SCHEDULE_GRID, fd.FD_SCHEDULE_PERSISTENT,
                       fd.FD_SCHEDULE_HEAD_GROUPS])
     merge = r.choice([fd.FD_MERGE_KERNEL, fd.FD_MERGE_KERNEL, fd.FD_MERGE_IN_KERNEL])
@@ -53,9 +56,21 @@ def draw(i):
                 sched=sched, merge=merge, path=path)
 
 
+N_MEDIUM = 40
+
+
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_random_case(i):
-    c = draw(i)
+    run_case(i, draw(i))
+
+
+@pytest.mark.parametrize("i", range(N_MEDIUM))
+def test_random_medium_case(i):
+    """Longer caches (8K to 32K tokens), more rows and up to 512 splits."""
+    run_case(100000 + i, draw(100000 + i, medium=True))
+
+
+def run_case(i, c):
     dtype = torch.float32 if c["f32"] else torch.bfloat16
     Hq = c["Hkv"] * c["G"]
     if c["ps"]:
