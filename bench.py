@@ -498,7 +498,8 @@ def run_fd(args):
     peak, peak_src = measured_peak()
     achieved = kv_bytes / (partial_ms * 1e-3) / 1e9
     path_name = "mma" if (args.path == "mma" or (args.path == "auto" and w.q.dtype == torch.bfloat16)) else "simt"
-    kernel = fd.partial_kernel_name(w.q.dtype, w.k.dtype, d, w.Hkv, w.page_size)
+    kernel = fd.partial_kernel_name(w.q.dtype, w.k.dtype, d, w.Hkv, w.page_size,
+                                    rows=Hq // Hkv)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kernel, w.name),
                 "kernel": kernel, "peak_source": peak_src,

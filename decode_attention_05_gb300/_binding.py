@@ -115,7 +115,7 @@ def _declare(L):
     L.fd_selftest_bounded_wait.restype = ctypes.c_int
     L.fd_selftest_bounded_wait.argtypes = [vp, ctypes.c_uint32, vp]
     L.fd_partial_kernel_name.restype = ctypes.c_char_p
-    L.fd_partial_kernel_name.argtypes = [i32, i32, i32, i32, i32, i32]
+    L.fd_partial_kernel_name.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     L.fd_get_path.restype = i32
     L.fd_get_path.argtypes = []
     L.fd_status_string.restype = ctypes.c_char_p
@@ -217,10 +217,11 @@ def selftest_bounded_wait(workspace: torch.Tensor, limit_us: int = 50000, stream
 
 
 def partial_kernel_name(dtype, kv_dtype, d: int, Hkv: int, page_size: int = 0,
-                        with_output: bool = True) -> Optional[str]:
-    """The partial-pass kernel a call with these sizes would launch (torch dtypes)."""
+                        with_output: bool = True, rows: int = 8) -> Optional[str]:
+    """The partial-pass kernel a call with these sizes would launch (torch dtypes);
+    rows = query rows per kv head (query tokens x Hq / Hkv)."""
     name = lib().fd_partial_kernel_name(_DTYPES[dtype], _DTYPES[kv_dtype], d, Hkv, page_size,
-                                        1 if with_output else 0)
+                                        rows, 1 if with_output else 0)
     return name.decode() if name else None
 
 

@@ -30,15 +30,19 @@ struct Schedule {
   bool heads, persistent;
 };
 
+// rows: query rows per (b, kv head) group (Q x G); groups above kMaxNarrowRows always
+// run the wide grid kernel.
 Schedule choose_schedule(int path, bool kv8, int64_t d, int64_t Hkv, int32_t page_size,
-                         bool fused) {
+                         bool fused, int64_t rows) {
   const int sched = g_schedule.load();
+  const bool narrow = rows <= fd::kMaxNarrowRows;
   const bool head_ok = path == FD_PATH_MMA && !kv8 && d == 128 &&
                        (page_size == 16 || page_size == 32) && Hkv % fd::kHeadGroup == 0 &&
-                       !fused;
+                       !fused && narrow;
   Schedule sc;
   sc.heads = head_ok && (sched == FD_SCHEDULE_AUTO || sched == FD_SCHEDULE_HEAD_GROUPS);
-  sc.persistent = !sc.heads && path == FD_PATH_MMA && !fused && sched == FD_SCHEDULE_PERSISTENT;
+  sc.persistent = !sc.heads && path == FD_PATH_MMA && !fused && narrow &&
+                  sched == FD_SCHEDULE_PERSISTENT;
   return sc;
 }
 
@@ -256,16 +260,19 @@ fd_status fd_set_schedule(int32_t schedule) {
 int32_t fd_get_schedule(void) { return g_schedule.load(); }
 
 const char* fd_partial_kernel_name(int32_t dtype, int32_t kv_dtype, int32_t d, int32_t Hkv,
-                                   int32_t page_size, int32_t with_output) {
+                                   int32_t page_size, int32_t rows, int32_t with_output) {
   const bool kv8 = kv_dtype == FD_F8E4M3;
   if ((dtype != FD_BF16 && dtype != FD_F32) || (!kv8 && kv_dtype != dtype) ||
-      (kv8 && dtype != FD_BF16) || d <= 0 || Hkv <= 0 || page_size < 0)
+      (kv8 && dtype != FD_BF16) || d <= 0 || Hkv <= 0 || page_size < 0 || rows < 1 ||
+      rows > fd::kMaxRows)
     return nullptr;
   const int path = resolve_path(dtype);
   if ((path == FD_PATH_MMA && dtype != FD_BF16) || (kv8 && path != FD_PATH_MMA)) return nullptr;
+  if (rows > fd::kMaxNarrowRows && (path != FD_PATH_MMA || kv8)) return nullptr;
   if (path == FD_PATH_SIMT) return "fd_partial_simt_kernel";
+  if (rows > fd::kMaxNarrowRows) return "fd_partial_wide_kernel";
   const bool fused = with_output && g_merge.load() == FD_MERGE_IN_KERNEL;
-  const Schedule sc = choose_schedule(path, kv8, d, Hkv, page_size, fused);
+  const Schedule sc = choose_schedule(path, kv8, d, Hkv, page_size, fused, rows);
   if (sc.heads) return "fd_partial_heads_kernel";
   if (sc.persistent) return "fd_partial_persist_kernel";
   return "fd_partial_mma_kernel";
@@ -379,11 +386,11 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
     return fail(FD_ERR_UNSUPPORTED, "out must be f32, or bf16 with bf16 inputs");
   const int64_t G = Hq / Hkv;
   if (d != 64 && d != 128) return fail(FD_ERR_UNSUPPORTED, "head dim %lld not in {64, 128}", (long long)d);
-  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
-    return fail(FD_ERR_UNSUPPORTED, "group size %lld not in {1, 2, 4, 8, 16}", (long long)G);
-  if (Q * G > 16)
-    return fail(FD_ERR_UNSUPPORTED, "query tokens x group size = %lld exceeds 16 rows per kv head",
-                (long long)(Q * G));
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16 && G != 32 && G != 64)
+    return fail(FD_ERR_UNSUPPORTED, "group size %lld not in {1, 2, 4, 8, 16, 32, 64}", (long long)G);
+  if (Q * G > fd::kMaxRows)
+    return fail(FD_ERR_UNSUPPORTED, "query tokens x group size = %lld exceeds %d rows per kv head",
+                (long long)(Q * G), fd::kMaxRows);
   const int es = esize(k_cache->dtype);              // KV element size (TMA, tiles)
   const int qes = esize(q->dtype);
   // ---- strides and alignment (TMA: 16-byte base and strides; rows contiguous)
@@ -447,10 +454,14 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
     return fail(FD_ERR_UNSUPPORTED, "the tensor-core path needs bf16 inputs");
   if (kv8 && path != FD_PATH_MMA)
     return fail(FD_ERR_UNSUPPORTED, "the FP8 KV cache runs on the tensor-core path only");
+  if (Q * G > fd::kMaxNarrowRows && (path != FD_PATH_MMA || kv8))
+    return fail(FD_ERR_UNSUPPORTED,
+                "more than %d query rows per kv head (%lld) run on the bf16 tensor-core path only",
+                fd::kMaxNarrowRows, (long long)(Q * G));
 
   // ---- schedule (fd_set_schedule)
   const bool fused = need_out && g_merge.load() == FD_MERGE_IN_KERNEL;
-  const Schedule sc = choose_schedule(path, kv8, d, Hkv, paged ? page_size : 0, fused);
+  const Schedule sc = choose_schedule(path, kv8, d, Hkv, paged ? page_size : 0, fused, Q * G);
   const bool heads = sc.heads, persistent = sc.persistent;
 
   // ---- tensor maps (box height: one tile, or one page when pages are shorter; with head

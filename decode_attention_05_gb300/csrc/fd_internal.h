@@ -102,10 +102,14 @@ fd_status record_error(fd_status st, const char* message);
 
 // Kernel instance for n query rows per (b, kv head): the next power of two (1..16), or 0
 // when n exceeds 16.
+// Query rows per (b, kv head) group padded to the kernels' template size: a power of two
+// up to kMaxRows (groups above kMaxNarrowRows run the wide tensor-core kernel only).
+constexpr int kMaxNarrowRows = 16;
+constexpr int kMaxRows = 64;
 inline int rows_template(int n) {
   int r = 1;
   while (r < n) r <<= 1;
-  return n >= 1 && r <= 16 ? r : 0;
+  return n >= 1 && r <= kMaxRows ? r : 0;
 }
 
 // Tile height (tokens) used by the kernels for a dtype and head dim.

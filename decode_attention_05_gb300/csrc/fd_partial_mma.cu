@@ -30,18 +30,25 @@ namespace fd {
 
 namespace {
 
-template <int D_, int G_, bool KV8_ = false, bool PERSIST_ = false>
+// G: query rows a consumer warp works on (the whole group, padded to a power of two;
+// with WIDE, the warp's quarter of a group of 32 or 64 rows).  WIDE: each consumer warp
+// takes all tokens of every tile for its own rows, instead of a quarter of the tokens
+// for all rows.
+template <int D_, int G_, bool KV8_ = false, bool PERSIST_ = false, bool WIDE_ = false>
 struct MmaShape {
   static constexpr int D = D_;
   static constexpr int G = G_;
   static constexpr bool KV8 = KV8_;                        // K/V stored as FP8 E4M3 codes
+  static constexpr bool WIDE = WIDE_;
+  static_assert(!(WIDE && (KV8 || PERSIST_)), "wide groups: bf16 grid schedule only");
   static constexpr int NT = G > 8 ? 2 : 1;                 // n-tiles of 8 heads
   static constexpr int ROW_BYTES = D * (KV8 ? 1 : 2);
   static constexpr int TT = kTileBytes / ROW_BYTES;        // 64 (bf16 d=128), 128 (d=64 or fp8)
   static constexpr int LINES = ROW_BYTES / 128;
   static constexpr int NCW = 4;                            // consumer warps
-  static constexpr int ROWS_PER_WARP = TT / NCW;           // 16 or 32
+  static constexpr int ROWS_PER_WARP = WIDE ? TT : TT / NCW;   // token rows of a warp per tile
   static constexpr int CHUNKS = ROWS_PER_WARP / 16;        // 16-token chunks per warp per tile
+  static constexpr int JOINT = CHUNKS < 2 ? CHUNKS : 2;    // chunks sharing one softmax update
   static constexpr int KSTEPS = D / 16;                    // k-steps of the QK^T product
   static constexpr int MTILES = D / 16;                    // m-tiles of the PV product
   // Persistent schedule: the same two CTAs per SM, each taking items from a queue; an
@@ -137,7 +144,8 @@ struct Consumer {
   float m[NT][2], l[NT][2];        // per column (query row nt * 8 + qc + {0, 1})
   float acc[NT][SH::MTILES][4];    // O^T fragments
   float sl2, vsc;
-  int64_t kmin;                    // smallest causal key bound of the group's rows
+  int64_t kmin;                    // smallest causal key bound of the warp's rows
+  int row0;                        // first query row of the group this warp works on
 
   // Load the group's query fragments and reset the state.
   //   B fragments of Q^T (k = dim, n = row), bf16 as stored: b0 holds dims 16 kk + qc,
@@ -146,11 +154,13 @@ struct Consumer {
   //   a 16-dim step, fragment columns (2c, 2c+1) hold dims (4c, 4c+1) and columns
   //   (2c+8, 2c+9) hold dims (4c+2, 4c+3), c = lane % 4.  q is converted to f16 (exact
   //   for bf16 values in f16's range) with the same permutation.
-  __device__ __forceinline__ void start(const Params& p, int b, int g, int64_t L, int lane) {
+  __device__ __forceinline__ void start(const Params& p, int b, int g, int64_t L, int lane,
+                                        int first_row = 0) {
     const int qr = lane >> 2, qc = (lane & 3) * 2;
+    row0 = first_row;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int h = nt * 8 + qr;
+      const int h = row0 + nt * 8 + qr;
       const bool live = h < p.n_rows;
       const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
           reinterpret_cast<const __nv_bfloat16*>(p.q) +
@@ -169,8 +179,8 @@ struct Consumer {
         qb[nt][kk][0] = live ? lo : 0u;
         qb[nt][kk][1] = live ? hi : 0u;
       }
-      lim[nt][0] = key_bound(p, L, nt * 8 + qc);
-      lim[nt][1] = key_bound(p, L, nt * 8 + qc + 1);
+      lim[nt][0] = key_bound(p, L, row0 + nt * 8 + qc);
+      lim[nt][1] = key_bound(p, L, row0 + nt * 8 + qc + 1);
       m[nt][0] = m[nt][1] = kNegInf;
       l[nt][0] = l[nt][1] = 0.f;
 #pragma unroll
@@ -178,27 +188,29 @@ struct Consumer {
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[nt][mt][e] = 0.f;
     }
-    kmin = key_bound(p, L, 0);
+    kmin = key_bound(p, L, row0);
     // FP8 KV: per-kv-head dequantisation scales fold into the score scale and output.
     const float ksc = (SH::KV8 && p.k_scale != nullptr) ? p.k_scale[g] : 1.f;
     vsc = (SH::KV8 && p.v_scale != nullptr) ? p.v_scale[g] : 1.f;
     sl2 = p.scale_log2 * ksc;
   }
 
-  // One K/V tile in shared memory: this warp's ROWS_PER_WARP token rows of it.
-  // Valid tokens are [lo, hi) minus invalid pages (`bad`); each query row also keeps
-  // only keys below its causal bound.
+  // One K/V tile in shared memory: this warp's ROWS_PER_WARP token rows of it (all of
+  // them with WIDE).  Valid tokens are [lo, hi) minus invalid pages (`bad`); each query
+  // row also keeps only keys below its causal bound.
   __device__ __forceinline__ void tile(const Params& p, uint8_t* kt, uint8_t* vt, int64_t t0,
                                        int64_t lo, int64_t hi, uint32_t bad, int warp, int lane,
                                        uint32_t lb, bool multi_page) {
     const int qr = lane >> 2;
     const int lm = lane >> 3, lr = lane & 7;          // ldmatrix: matrix i / 8, row i % 8
-    const int r0 = warp * SH::ROWS_PER_WARP;          // this warp's first row in the tile
+    const int r0 = SH::WIDE ? 0 : warp * SH::ROWS_PER_WARP;   // warp's first row in the tile
 
     // Rows outside [lo, hi) or on an invalid page: their V rows may be stale (NaN) and
-    // 0 * NaN is NaN inside the MMA, so zero them before use.  Only boundary tiles.
+    // 0 * NaN is NaN inside the MMA, so they must read as 0.  Only boundary tiles.  A
+    // warp that owns its rows zeroes them in shared memory; with WIDE every warp reads
+    // every row, so the V fragments are masked in registers instead (below).
     const bool clean = t0 + r0 >= lo && t0 + r0 + SH::ROWS_PER_WARP <= hi && bad == 0;
-    if (!clean) {
+    if (!SH::WIDE && !clean) {
       for (int r = 0; r < SH::ROWS_PER_WARP; ++r) {
         const int row = r0 + r;
         const int64_t tok = t0 + row;
@@ -214,16 +226,18 @@ struct Consumer {
       __syncwarp();
     }
 
-    // The warp's CHUNKS 16-token chunks go through the online softmax together: all
-    // QK^T products first (independent mma chains), one max and one rescale for the
-    // warp's rows of the tile, then all PV products.
+    // JOINT 16-token chunks at a time go through the online softmax together: all their
+    // QK^T products first (independent mma chains), one max and one rescale, then all
+    // their PV products.
     // A row needs masking only on a boundary tile (split range, invalid page) or where
     // a query's causal bound falls inside the warp's rows; kmin is the smallest bound.
     const bool full = clean && t0 + r0 + SH::ROWS_PER_WARP <= kmin;
-    float s[SH::CHUNKS][NT][4];
 #pragma unroll
-    for (int ch = 0; ch < SH::CHUNKS; ++ch) {
-      const int rb = r0 + ch * 16;                    // first row of this 16-token chunk
+    for (int cg = 0; cg < SH::CHUNKS; cg += SH::JOINT) {
+    float s[SH::JOINT][NT][4];
+#pragma unroll
+    for (int ch = 0; ch < SH::JOINT; ++ch) {
+      const int rb = r0 + (cg + ch) * 16;             // first row of this 16-token chunk
       // ---- S^T = K . Q^T  (A = K rows rb..rb+15 via ldmatrix, swizzled tile)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) s[ch][nt][0] = s[ch][nt][1] = s[ch][nt][2] = s[ch][nt][3] = 0.f;
@@ -263,15 +277,15 @@ struct Consumer {
     //      row nt * 8 + qc + (e & 1)); excluded tokens get -inf.
     if (full) {
 #pragma unroll
-      for (int ch = 0; ch < SH::CHUNKS; ++ch)
+      for (int ch = 0; ch < SH::JOINT; ++ch)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) s[ch][nt][e] *= sl2;
     } else {
 #pragma unroll
-      for (int ch = 0; ch < SH::CHUNKS; ++ch) {
-        const int rb = r0 + ch * 16;
+      for (int ch = 0; ch < SH::JOINT; ++ch) {
+        const int rb = r0 + (cg + ch) * 16;
         bool vrow[2];
         int64_t vtok[2];
 #pragma unroll
@@ -291,13 +305,13 @@ struct Consumer {
       }
     }
 
-    uint32_t pb[SH::CHUNKS][NT][2];                   // P^T fragments (b0/b1 of the PV mma)
+    uint32_t pb[SH::JOINT][NT][2];                    // P^T fragments (b0/b1 of the PV mma)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      // max per column over the warp's rows: in-thread, then lanes of equal qc
+      // max per column over the chunks' rows: in-thread, then lanes of equal qc
       float mx0 = kNegInf, mx1 = kNegInf;
 #pragma unroll
-      for (int ch = 0; ch < SH::CHUNKS; ++ch) {
+      for (int ch = 0; ch < SH::JOINT; ++ch) {
         mx0 = fmaxf(mx0, fmaxf(s[ch][nt][0], s[ch][nt][2]));
         mx1 = fmaxf(mx1, fmaxf(s[ch][nt][1], s[ch][nt][3]));
       }
@@ -323,7 +337,7 @@ struct Consumer {
         m[nt][1] = mn1;
       }
 #pragma unroll
-      for (int ch = 0; ch < SH::CHUNKS; ++ch) {
+      for (int ch = 0; ch < SH::JOINT; ++ch) {
         float pr[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -345,8 +359,8 @@ struct Consumer {
 
     // ---- O^T += V^T . P^T
 #pragma unroll
-    for (int ch = 0; ch < SH::CHUNKS; ++ch) {
-      const int rb = r0 + ch * 16;
+    for (int ch = 0; ch < SH::JOINT; ++ch) {
+      const int rb = r0 + (cg + ch) * 16;
       if constexpr (SH::KV8) {
         // ldmatrix.trans over 16-bit pairs of codes: matrix j covers tokens
         // rb + 8 (j & 1) .. +7 of chunk (m-tile) mt + (j >> 1); a register holds tokens
@@ -372,19 +386,42 @@ struct Consumer {
         }
       } else {
         // A = V^T via ldmatrix.trans: matrix j covers tokens rb + 8 (j >> 1) .. +7 and
-        // dims 16 mt + 8 (j & 1) .. +7.
+        // dims 16 mt + 8 (j & 1) .. +7; a register holds tokens rb + 8 (j >> 1) + 2 c and
+        // + 1 (low, high half), c = lane % 4, at one dim.
         const int vrow_addr = rb + lr + (lm >> 1) * 8;
+        uint32_t vmask[2] = {0xffffffffu, 0xffffffffu};   // tokens +0/+1 and +8/+9
+        if (SH::WIDE && !clean) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t mk = 0u;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int row = rb + 8 * hh + 2 * (lane & 3) + u;
+              const int64_t tok = t0 + row;
+              const int pslot = multi_page ? (row >> p.log2_page) : 0;
+              if (tok >= lo && tok < hi && !((bad >> pslot) & 1u)) mk |= 0xffffu << (16 * u);
+            }
+            vmask[hh] = mk;
+          }
+        }
 #pragma unroll
         for (int mt = 0; mt < SH::MTILES; ++mt) {
           const int c16 = mt * 2 + (lm & 1);
           uint32_t a[4];
           ldsm_x4_trans(smem_addr(vt) + tile_chunk<SH::LINES>(vrow_addr, c16, lb), a);
+          if (SH::WIDE && !clean) {
+            a[0] &= vmask[0];
+            a[1] &= vmask[0];
+            a[2] &= vmask[1];
+            a[3] &= vmask[1];
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
             mma_bf16(acc[nt][mt], a, pb[ch][nt][0], pb[ch][nt][1]);
         }
       }
     }
+    }                                                  // chunk groups
   }
 
   // End of a split: sum l over the 8 lanes that share a column (they saw different
@@ -440,7 +477,7 @@ struct Consumer {
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int h = nt * 8 + qc + e;
+        const int h = row0 + nt * 8 + qc + e;
         if (h >= p.n_rows) continue;
         const int64_t row = flat_row(p, b, g, h);
         const float L = l[nt][e];
@@ -544,6 +581,89 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
     named_bar_sync(1, SH::NCW * 32);
     return true;
   });
+  if (p.counters != nullptr) arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
+}
+
+// ---------------------------------------------------------------- wide groups
+// Query groups of 17 to 64 rows (Q query tokens x G heads of a kv head, or G > 16):
+// one CTA per (split, kv head, row) as in the grid schedule, but consumer warp w works
+// on rows w G .. w G + G - 1 (G = 8 or 16 here) over every token of each tile, so a
+// warp's state covers its rows for the whole split and it writes their partials itself
+// (no cross-warp merge).  Each K/V tile is read from shared memory by all four warps.
+// Two CTAs of 160 threads per SM leave 204 registers per thread; __launch_bounds__
+// would budget for 192-thread CTAs and cap at 168, which spills the wide accumulators.
+template <class SH>
+__global__ void __maxnreg__(200)
+    fd_partial_wide_kernel(const __grid_constant__ CUtensorMap tk,
+                           const __grid_constant__ CUtensorMap tv,
+                           const __grid_constant__ Params p) {
+  constexpr int TT = SH::TT, STAGES = SH::STAGES;
+  static_assert(SH::WIDE, "wide shape");
+  pdl_wait();                       // inputs of this step are visible
+  const SplitInfo si = split_info<TT>(p);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  auto* ctl = reinterpret_cast<PipeCtl<STAGES>*>(stages + SH::RING_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (si.n_tiles == 0) {            // empty split: weight 0 in the merge, nothing to load
+    write_empty_split(p, si, threadIdx.x);
+    pdl_trigger();
+    if (p.counters != nullptr && warp < SH::NCW)
+      arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_addr(&ctl->full[s]), 1);
+      mbar_init(smem_addr(&ctl->empty[s]), SH::NCW);
+    }
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == SH::NCW) {            // ---------------- producer warp
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+    produce_tiles<TT, STAGES>(p, si, &tk, &tv, stages, ctl, lane);
+    pdl_trigger();
+    return;
+  }
+
+  Consumer<SH> c;
+  c.start(p, si.b, si.g, si.L, lane, warp * SH::G);
+  const bool multi_page = p.page_size > 0 && p.page_size < TT;
+  const uint32_t lb = (uint32_t)p.log2_box;
+  bool aborted = false;
+  for (int n = 0; n < si.n_tiles; ++n) {
+    const int stage = n % STAGES;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(smem_addr(&ctl->full[stage]), (n / STAGES) & 1);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) {
+        ctl->abort = 1;
+        atomicOr(p.flags, kDevFlagTimeout);
+      }
+      aborted = true;
+      break;
+    }
+    uint8_t* kt = stages + (size_t)stage * 2 * kTileBytes;
+    c.tile(p, kt, kt + kTileBytes, si.T0 + (int64_t)n * TT, si.lo, si.hi, ctl->bad[stage], warp,
+           lane, lb, multi_page);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
+  }
+  pdl_trigger();
+  if (aborted) {                    // this warp's rows of the split: weight 0
+    const int h = warp * SH::G + lane;
+    if (lane < SH::G && h < p.n_rows)
+      p.lse_part[flat_row(p, si.b, si.g, h) * p.S + si.split] = kNegInf;
+  } else {
+    c.store_own(p, si.b, si.g, si.split, lane);
+  }
   if (p.counters != nullptr) arrive_and_merge<SH::D, SH::NCW>(p, si, threadIdx.x, &ctl->last);
 }
 
@@ -753,6 +873,13 @@ cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap
     const int64_t items = (int64_t)p.S * p.Hkv * p.B;
     const unsigned grid = (unsigned)(items < 2 * sms ? items : 2 * sms);
     e = launch_partial_kernel(kernel, dim3(grid), SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
+  } else if constexpr (SH::WIDE) {
+    auto kernel = fd_partial_wide_kernel<SH>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SH::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
+    e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
   } else if (p.head_group) {
     if constexpr (SH::D == 128 && !SH::KV8) {
       auto kernel = fd_partial_heads_kernel<SH>;
@@ -785,6 +912,12 @@ cudaError_t dispatch_g(const Params& p, const CUtensorMap& tk, const CUtensorMap
     case 4: return launch_mma<MmaShape<D, 4, KV8, PERSIST>>(p, tk, tv, stream);
     case 8: return launch_mma<MmaShape<D, 8, KV8, PERSIST>>(p, tk, tv, stream);
     case 16: return launch_mma<MmaShape<D, 16, KV8, PERSIST>>(p, tk, tv, stream);
+    case 32:   // wide groups: four warps of 8 rows
+      if constexpr (!KV8 && !PERSIST) return launch_mma<MmaShape<D, 8, false, false, true>>(p, tk, tv, stream);
+      else return cudaErrorInvalidValue;
+    case 64:   // four warps of 16 rows
+      if constexpr (!KV8 && !PERSIST) return launch_mma<MmaShape<D, 16, false, false, true>>(p, tk, tv, stream);
+      else return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }

@@ -100,7 +100,8 @@ typedef enum {
  *                positions of row b, their keys and values already in the cache, so
  *                query j (0-based) attends to the keys t <= L_b - Q + j (the causal mask
  *                of [AI-Infra] 2.5 applied inside each split); a query that sees no key
- *                gets out = 0, lse_out = -inf.  Q * G <= 16.
+ *                gets out = 0, lse_out = -inf.  Q * G <= 64 (above 16 rows per kv
+ *                head: bf16 tensor-core path only).
  *   k_cache      device, same dtype as q.  Contiguous: [B, Hkv, L_cap, d] (block_table
  *                NULL).  Paged: [num_pages, Hkv, page_size, d]; logical token t of row
  *                b is slot t % page_size of page block_table[b][t / page_size] -- the
@@ -128,8 +129,9 @@ typedef enum {
  *                at once must not share a workspace.
  *   stream       cudaStream_t (as void*), NULL = legacy default stream.
  *
- * Supported: d in {64, 128}; G = Hq / Hkv in {1, 2, 4, 8, 16}; (q, k, v) all bf16
- * with out bf16 or f32, or all f32 with out f32.  B >= 1, L_cap >= 1.
+ * Supported: d in {64, 128}; G = Hq / Hkv in {1, 2, 4, 8, 16, 32, 64} with Q * G <= 64
+ * (more than 16 rows per kv head on the bf16 tensor-core path only); (q, k, v) all
+ * bf16 with out bf16 or f32, or all f32 with out f32.  B >= 1, L_cap >= 1.
  * Errors: FD_ERR_INVALID_ARG for rank/shape/stride/alignment mismatches, Hq % Hkv != 0,
  * NULL required pointers, num_splits < 0, page_size invalid with a block table;
  * FD_ERR_UNSUPPORTED for other d, G or dtype combinations; FD_ERR_WORKSPACE_TOO_SMALL;
@@ -360,13 +362,14 @@ FD_API int32_t fd_get_schedule(void);
 /*
  * Name of the partial-pass kernel a call would launch under the current process
  * settings (path, merge mode, schedule): "fd_partial_mma_kernel",
- * "fd_partial_heads_kernel", "fd_partial_persist_kernel" or "fd_partial_simt_kernel".
- * dtype is q's fd_dtype, kv_dtype the cache's; page_size 0 for a contiguous cache;
- * with_output 1 for fd_decode_attention, 0 for fd_decode_partial.  NULL for a
+ * "fd_partial_heads_kernel", "fd_partial_wide_kernel", "fd_partial_persist_kernel" or
+ * "fd_partial_simt_kernel".  dtype is q's fd_dtype, kv_dtype the cache's; page_size 0
+ * for a contiguous cache; rows the query rows per kv head (Q x Hq / Hkv); with_output
+ * 1 for fd_decode_attention, 0 for fd_decode_partial.  NULL for a
  * combination no entry point accepts.  Static string; host only.
  */
 FD_API const char* fd_partial_kernel_name(int32_t dtype, int32_t kv_dtype, int32_t d, int32_t Hkv,
-                                          int32_t page_size, int32_t with_output);
+                                          int32_t page_size, int32_t rows, int32_t with_output);
 
 /* Split count a call with these sizes and this num_splits argument would use. */
 FD_API int32_t fd_resolve_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int64_t L_cap,

@@ -165,6 +165,11 @@ def test_partial_kernel_name_follows_settings():
         assert name(bf, f8, 128, 8, 16) == "fd_partial_mma_kernel"             # FP8 KV
         assert name(f32, f32, 128, 8) == "fd_partial_simt_kernel"
         assert name(f32, f8, 128, 8) is None
+        assert name(bf, bf, 128, 8, rows=32) == "fd_partial_wide_kernel"      # Q x G > 16
+        assert name(bf, bf, 128, 8, 16, rows=64) == "fd_partial_wide_kernel"
+        assert name(bf, f8, 128, 8, rows=32) is None                          # bf16 only
+        assert name(f32, f32, 128, 8, rows=32) is None
+        assert name(bf, bf, 128, 8, rows=65) is None
         fd.set_merge_mode(fd.FD_MERGE_IN_KERNEL)                              # single launch
         assert name(bf, bf, 128, 8, 16) == "fd_partial_mma_kernel"
         assert name(bf, bf, 128, 8, 16, with_output=False) == "fd_partial_heads_kernel"

@@ -481,12 +481,63 @@ def test_multi_token_decode(name, path, Q, G, paged):
 
 
 def test_multi_token_limits():
-    """More than 16 query rows per kv head is refused on the host."""
-    q = torch.zeros(1, 3, 8, 128, dtype=torch.bfloat16, device="cuda")      # 3 x 8 = 24 rows
+    """Up to 64 query rows per kv head on the bf16 tensor-core path; more rows, or more
+    than 16 on the CUDA-core path or with an FP8 cache, are refused on the host."""
+    seq = torch.tensor([64], dtype=torch.int32, device="cuda")
     k = torch.zeros(1, 1, 64, 128, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(1, 5, 16, 128, dtype=torch.bfloat16, device="cuda")     # 5 x 16 = 80 rows
     with pytest.raises(fd.FdError):
-        fd.decode_attention(q, k, k, torch.tensor([64], dtype=torch.int32, device="cuda"),
-                            num_splits=1)
+        fd.decode_attention(q, k, k, seq, num_splits=1)
+    q = torch.zeros(1, 3, 8, 128, dtype=torch.bfloat16, device="cuda")      # 24 rows
+    fd.set_path(fd.FD_PATH_SIMT)
+    with pytest.raises(fd.FdError):
+        fd.decode_attention(q, k, k, seq, num_splits=1)
+    fd.set_path(fd.FD_PATH_AUTO)
+    k8 = k.float().to(torch.float8_e4m3fn)
+    with pytest.raises(fd.FdError):
+        fd.decode_attention_fp8kv(q, k8, k8, None, None, seq, num_splits=1)
+    o, l = fd.decode_attention(q, k, k, seq, num_splits=1)                   # accepted
+    torch.cuda.synchronize()
+    assert o.shape == (1, 3, 8, 128)
+
+
+@pytest.mark.parametrize("merge,mode", MERGES)
+@pytest.mark.parametrize("Q,G,Hkv,d,paged", [
+    (3, 8, 2, 128, False), (4, 8, 2, 128, True), (8, 8, 1, 128, False), (2, 16, 2, 128, True),
+    (4, 16, 1, 128, False), (1, 32, 2, 128, False), (1, 64, 1, 128, True), (5, 4, 2, 128, False),
+    (3, 16, 1, 64, False), (8, 8, 2, 64, True)])
+def test_wide_groups(Q, G, Hkv, d, paged, merge, mode):
+    """17 to 64 query rows per kv head (multi-token decode on GQA groups, or groups of 32
+    and 64 heads): the wide kernel, each warp on its own rows over every token, against
+    the fp64 causal oracle; rows shorter than Q leave their first queries keyless."""
+    fd.set_merge_mode(mode)
+    Hq = Hkv * G
+    lens = [1, max(Q - 1, 1), 70, 333, 1500, 2048]
+    if paged:
+        w = workloads.paged_case(len(lens), Hq, Hkv, d, 16, 128, lens, seed=900 + Q * 11 + G + d,
+                                 out_dtype=torch.float32)
+    else:
+        w = workloads.contiguous_case(len(lens), Hq, Hkv, d, 2048, lens, seed=900 + Q * 11 + G + d,
+                                      out_dtype=torch.float32)
+    q4 = workloads.multi_token_queries(len(lens), Q, Hq, d, seed=950 + Q + G + d)
+    _, k, v, lens_np, bt, ps = w.oracle_arrays()
+    ref_o, ref_l = oracle.decode_causal(workloads.np_storage(q4), k, v, lens_np,
+                                        block_table=bt, page_size=ps)
+    wd = w.to("cuda")
+    B = len(lens)
+    qd = q4.cuda() if Q > 1 else q4[:, 0].contiguous().cuda()
+    assert fd.partial_kernel_name(torch.bfloat16, torch.bfloat16, d, Hkv, w.page_size,
+                                  rows=Q * G) == "fd_partial_wide_kernel"
+    for S in (1, 5, 16):
+        ws = torch.zeros(fd.workspace_size(B, Q * Hq, Hkv, d, S), dtype=torch.uint8, device="cuda")
+        o, l = fd.decode_attention(qd, wd.k, wd.v, wd.seq_lens, wd.block_table, w.page_size, S,
+                                   workspace=ws, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert fd.read_device_error(ws) == 0
+        mw = workloads.Workload("wide", q4.reshape(B * Q, Hq, d), w.k, w.v, w.seq_lens)
+        check(mw, o.cpu().double().numpy().reshape(B * Q, Hq, d),
+              l.cpu().double().numpy().reshape(B * Q, Hq),
+              ref_o.reshape(B * Q, Hq, d), ref_l.reshape(B * Q, Hq))
 
 
 def _fp8_views(codes):
