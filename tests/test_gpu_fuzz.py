@@ -34,8 +34,9 @@ def draw(i, medium=False):
     d = r.choice([64, 128, 128])
     fp8 = d == 128 and r.random() < 0.2
     f32 = not fp8 and r.random() < 0.15
-    Q = r.choice([1, 1, 1, 2, 3, 4])
-    G = r.choice([g for g in (1, 2, 4, 8, 16) if Q * g <= 16])
+    Q = r.choice([1, 1, 1, 2, 3, 4, 8])
+    wide_ok = not fp8 and not f32          # above 16 rows: bf16 tensor-core path only
+    G = r.choice([g for g in (1, 2, 4, 8, 16, 32, 64) if Q * g <= (64 if wide_ok else 16)])
     Hkv = r.choice([1, 2, 3, 4, 8])
     B = r.randint(1, 5)
     paged = r.random() < 0.5
@@ -51,7 +52,8 @@ def draw(i, medium=False):
     sched = r.choice([fd.FD_SCHEDULE_AUTO, fd.FD_SCHEDULE_GRID, fd.FD_SCHEDULE_PERSISTENT,
                       fd.FD_SCHEDULE_HEAD_GROUPS])
     merge = r.choice([fd.FD_MERGE_KERNEL, fd.FD_MERGE_KERNEL, fd.FD_MERGE_IN_KERNEL])
-    path = fd.FD_PATH_SIMT if (f32 or (not fp8 and r.random() < 0.2)) else fd.FD_PATH_MMA
+    path = fd.FD_PATH_SIMT if (f32 or (not fp8 and Q * G <= 16 and r.random() < 0.2)) \
+        else fd.FD_PATH_MMA
     return dict(d=d, fp8=fp8, f32=f32, Q=Q, G=G, Hkv=Hkv, B=B, ps=ps, cap=cap, lens=lens, S=S,
                 sched=sched, merge=merge, path=path)
 
