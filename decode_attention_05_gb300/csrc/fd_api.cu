@@ -32,10 +32,11 @@ struct Schedule {
 
 // rows: query rows per (b, kv head) group (Q x G); groups above kMaxNarrowRows always
 // run the wide grid kernel.
-Schedule choose_schedule(int path, bool kv8, int64_t d, int64_t Hkv, int32_t page_size,
-                         bool fused, int64_t rows) {
+// f32 inputs on the tensor-core path run on the grid schedule only.
+Schedule choose_schedule(int path, bool kv8, bool f32, int64_t d, int64_t Hkv,
+                         int32_t page_size, bool fused, int64_t rows) {
   const int sched = g_schedule.load();
-  const bool narrow = rows <= fd::kMaxNarrowRows;
+  const bool narrow = rows <= fd::kMaxNarrowRows && !f32;
   const bool head_ok = path == FD_PATH_MMA && !kv8 && d == 128 &&
                        (page_size == 16 || page_size == 32) && Hkv % fd::kHeadGroup == 0 &&
                        !fused && narrow;
@@ -46,9 +47,12 @@ Schedule choose_schedule(int path, bool kv8, int64_t d, int64_t Hkv, int32_t pag
   return sc;
 }
 
-int resolve_path(int32_t q_dtype) {
+// Automatic choice: the tensor-core path for bf16, and for f32 groups of up to
+// kMaxF32MmaRows query rows per kv head; the CUDA-core path for larger f32 groups.
+int resolve_path(int32_t q_dtype, int64_t rows) {
   const int path = g_path.load();
-  return path == FD_PATH_AUTO ? (q_dtype == FD_BF16 ? FD_PATH_MMA : FD_PATH_SIMT) : path;
+  if (path != FD_PATH_AUTO) return path;
+  return q_dtype == FD_BF16 || rows <= fd::kMaxF32MmaRows ? FD_PATH_MMA : FD_PATH_SIMT;
 }
 
 fd_status fail(fd_status st, const char* fmt, ...) {
@@ -266,13 +270,15 @@ const char* fd_partial_kernel_name(int32_t dtype, int32_t kv_dtype, int32_t d, i
       (kv8 && dtype != FD_BF16) || d <= 0 || Hkv <= 0 || page_size < 0 || rows < 1 ||
       rows > fd::kMaxRows)
     return nullptr;
-  const int path = resolve_path(dtype);
-  if ((path == FD_PATH_MMA && dtype != FD_BF16) || (kv8 && path != FD_PATH_MMA)) return nullptr;
+  const int path = resolve_path(dtype, rows);
+  if ((path == FD_PATH_MMA && dtype == FD_F32 && rows > fd::kMaxF32MmaRows) ||
+      (kv8 && path != FD_PATH_MMA))
+    return nullptr;
   if (rows > fd::kMaxNarrowRows && (path != FD_PATH_MMA || kv8)) return nullptr;
   if (path == FD_PATH_SIMT) return "fd_partial_simt_kernel";
   if (rows > fd::kMaxNarrowRows) return "fd_partial_wide_kernel";
   const bool fused = with_output && g_merge.load() == FD_MERGE_IN_KERNEL;
-  const Schedule sc = choose_schedule(path, kv8, d, Hkv, page_size, fused, rows);
+  const Schedule sc = choose_schedule(path, kv8, dtype == FD_F32, d, Hkv, page_size, fused, rows);
   if (sc.heads) return "fd_partial_heads_kernel";
   if (sc.persistent) return "fd_partial_persist_kernel";
   return "fd_partial_mma_kernel";
@@ -449,9 +455,11 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
     return fail(FD_ERR_UNSUPPORTED, "grid too large");
 
   // ---- path
-  const int path = resolve_path(q->dtype);
-  if (path == FD_PATH_MMA && q->dtype != FD_BF16)
-    return fail(FD_ERR_UNSUPPORTED, "the tensor-core path needs bf16 inputs");
+  const int path = resolve_path(q->dtype, Q * G);
+  if (path == FD_PATH_MMA && q->dtype == FD_F32 && Q * G > fd::kMaxF32MmaRows)
+    return fail(FD_ERR_UNSUPPORTED,
+                "the tensor-core path takes f32 inputs for up to %d query rows per kv head",
+                fd::kMaxF32MmaRows);
   if (kv8 && path != FD_PATH_MMA)
     return fail(FD_ERR_UNSUPPORTED, "the FP8 KV cache runs on the tensor-core path only");
   if (Q * G > fd::kMaxNarrowRows && (path != FD_PATH_MMA || kv8))
@@ -461,7 +469,8 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
 
   // ---- schedule (fd_set_schedule)
   const bool fused = need_out && g_merge.load() == FD_MERGE_IN_KERNEL;
-  const Schedule sc = choose_schedule(path, kv8, d, Hkv, paged ? page_size : 0, fused, Q * G);
+  const Schedule sc = choose_schedule(path, kv8, q->dtype == FD_F32, d, Hkv,
+                                     paged ? page_size : 0, fused, Q * G);
   const bool heads = sc.heads, persistent = sc.persistent;
 
   // ---- tensor maps (box height: one tile, or one page when pages are shorter; with head
@@ -516,6 +525,7 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   p.lse_out = lse_out;
   p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
   p.kv_fp8 = kv8 ? 1 : 0;
+  p.in_f32 = q->dtype == FD_F32 ? 1 : 0;
   p.k_scale = kv8 ? k_scale : nullptr;
   p.v_scale = kv8 ? v_scale : nullptr;
 

@@ -66,6 +66,7 @@ struct Params {
   float scale_log2;       // log2(e) / sqrt(d): scores are kept in base-2 units inside kernels
   // FP8 KV cache (E4M3 codes): per-kv-head dequantisation scales [Hkv] (nullptr = 1)
   int32_t kv_fp8;
+  int32_t in_f32;         // 1: q, K and V are f32 (tensor-core path: 3xTF32 products)
   const float* k_scale;
   const float* v_scale;
 };
@@ -100,12 +101,12 @@ cudaError_t launch_partial_kernel(Kernel kernel, dim3 grid, int threads, size_t 
 // Record `message` as the calling thread's fd_last_error() and return `st`.
 fd_status record_error(fd_status st, const char* message);
 
-// Kernel instance for n query rows per (b, kv head): the next power of two (1..16), or 0
-// when n exceeds 16.
 // Query rows per (b, kv head) group padded to the kernels' template size: a power of two
 // up to kMaxRows (groups above kMaxNarrowRows run the wide tensor-core kernel only).
 constexpr int kMaxNarrowRows = 16;
 constexpr int kMaxRows = 64;
+// f32 inputs run on the tensor cores (3xTF32) for groups of up to this many rows.
+constexpr int kMaxF32MmaRows = 8;
 inline int rows_template(int n) {
   int r = 1;
   while (r < n) r <<= 1;

@@ -34,22 +34,30 @@ namespace {
 // with WIDE, the warp's quarter of a group of 32 or 64 rows).  WIDE: each consumer warp
 // takes all tokens of every tile for its own rows, instead of a quarter of the tokens
 // for all rows.
-template <int D_, int G_, bool KV8_ = false, bool PERSIST_ = false, bool WIDE_ = false>
+// F32: q, K and V stored as f32, multiplied on the tensor cores as three TF32 products
+// (see split_tf32), for groups of up to 8 rows.
+template <int D_, int G_, bool KV8_ = false, bool PERSIST_ = false, bool WIDE_ = false,
+          bool F32_ = false>
 struct MmaShape {
   static constexpr int D = D_;
   static constexpr int G = G_;
   static constexpr bool KV8 = KV8_;                        // K/V stored as FP8 E4M3 codes
   static constexpr bool WIDE = WIDE_;
+  static constexpr bool F32 = F32_;
   static_assert(!(WIDE && (KV8 || PERSIST_)), "wide groups: bf16 grid schedule only");
+  static_assert(!(F32 && (KV8 || PERSIST_ || WIDE_ || G_ > 8)),
+                "f32 inputs: grid schedule, up to 8 rows");
   static constexpr int NT = G > 8 ? 2 : 1;                 // n-tiles of 8 heads
-  static constexpr int ROW_BYTES = D * (KV8 ? 1 : 2);
-  static constexpr int TT = kTileBytes / ROW_BYTES;        // 64 (bf16 d=128), 128 (d=64 or fp8)
+  static constexpr int ROW_BYTES = D * (F32 ? 4 : (KV8 ? 1 : 2));
+  static constexpr int TT = kTileBytes / ROW_BYTES;        // 64 (bf16 d=128), 128 (d=64 or
+                                                           // fp8), 32 (f32 d=128)
   static constexpr int LINES = ROW_BYTES / 128;
-  static constexpr int NCW = 4;                            // consumer warps
+  static constexpr int NCW = F32 ? TT / 16 : 4;            // consumer warps (f32 d=128: 2)
   static constexpr int ROWS_PER_WARP = WIDE ? TT : TT / NCW;   // token rows of a warp per tile
   static constexpr int CHUNKS = ROWS_PER_WARP / 16;        // 16-token chunks per warp per tile
   static constexpr int JOINT = CHUNKS < 2 ? CHUNKS : 2;    // chunks sharing one softmax update
-  static constexpr int KSTEPS = D / 16;                    // k-steps of the QK^T product
+  static constexpr int KSTEPS = F32 ? D / 8 : D / 16;     // k-steps of the QK^T product
+  static constexpr int QLO = F32 ? KSTEPS : 1;             // TF32 residual fragments of q
   static constexpr int MTILES = D / 16;                    // m-tiles of the PV product
   // Persistent schedule: the same two CTAs per SM, each taking items from a queue; an
   // item's epilogue uses the ring stage of its last tile as merge scratch (the other
@@ -93,6 +101,30 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D = A . B + D, m16n8k8, TF32 inputs, f32 accumulators (the f32 path).
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// An f32 value as a TF32 pair hi + lo: hi = x rounded to TF32 (10 mantissa bits), lo =
+// the residual x - hi rounded to TF32.  With a = ah + al and b = bh + bl, ah bh + ah bl +
+// al bh carries about 21 bits of each product (al bl, ~2^-22 relative, is dropped):
+// f32 accuracy for this pass from three TF32 tensor-core products.
+__device__ __forceinline__ uint32_t cvt_tf32(float x) {
+  uint32_t y;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = cvt_tf32(x);
+  lo = cvt_tf32(x - __uint_as_float(hi));
 }
 
 // D = A . B + D, m16n8k16, f16 inputs, f32 accumulators (the FP8 KV path).
@@ -139,7 +171,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <class SH>
 struct Consumer {
   static constexpr int NT = SH::NT;
-  uint32_t qb[NT][SH::KSTEPS][2];  // Q^T B-fragments
+  uint32_t qb[NT][SH::KSTEPS][2];  // Q^T B-fragments (f32 path: the TF32 high parts)
+  uint32_t qlo[NT][SH::QLO][2];    // f32 path: the TF32 residuals
   int64_t lim[NT][2];              // causal key bound of this thread's two columns per n-tile
   float m[NT][2], l[NT][2];        // per column (query row nt * 8 + qc + {0, 1})
   float acc[NT][SH::MTILES][4];    // O^T fragments
@@ -154,6 +187,8 @@ struct Consumer {
   //   a 16-dim step, fragment columns (2c, 2c+1) hold dims (4c, 4c+1) and columns
   //   (2c+8, 2c+9) hold dims (4c+2, 4c+3), c = lane % 4.  q is converted to f16 (exact
   //   for bf16 values in f16's range) with the same permutation.
+  //   F32: m16n8k8 B fragments, b0 = dim 8 kk + c, b1 = dim 8 kk + c + 4 of row qr, each
+  //   split into TF32 high part (qb) and residual (qlo).
   __device__ __forceinline__ void start(const Params& p, int b, int g, int64_t L, int lane,
                                         int first_row = 0) {
     const int qr = lane >> 2, qc = (lane & 3) * 2;
@@ -162,6 +197,15 @@ struct Consumer {
     for (int nt = 0; nt < NT; ++nt) {
       const int h = row0 + nt * 8 + qr;
       const bool live = h < p.n_rows;
+      if constexpr (SH::F32) {
+        const float* qf = reinterpret_cast<const float*>(p.q) + q_offset(p, b, g, live ? h : 0);
+        const int c = lane & 3;
+#pragma unroll
+        for (int kk = 0; kk < SH::KSTEPS; ++kk) {
+          split_tf32(live ? qf[kk * 8 + c] : 0.f, qb[nt][kk][0], qlo[nt][kk][0]);
+          split_tf32(live ? qf[kk * 8 + c + 4] : 0.f, qb[nt][kk][1], qlo[nt][kk][1]);
+        }
+      } else {
       const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
           reinterpret_cast<const __nv_bfloat16*>(p.q) +
           q_offset(p, b, g, live ? h : 0));           // never address past the group
@@ -178,6 +222,7 @@ struct Consumer {
         }
         qb[nt][kk][0] = live ? lo : 0u;
         qb[nt][kk][1] = live ? hi : 0u;
+      }
       }
       lim[nt][0] = key_bound(p, L, row0 + nt * 8 + qc);
       lim[nt][1] = key_bound(p, L, row0 + nt * 8 + qc + 1);
@@ -261,6 +306,42 @@ struct Consumer {
               mma_f16(s[ch][nt], a, qb[nt][kk + u][0], qb[nt][kk + u][1]);
           }
         }
+      } else if constexpr (SH::F32) {
+        // A 16-byte chunk holds 4 dims: ldmatrix.x4 over chunks 2 kk, 2 kk + 1 and rows
+        // 0-7, 8-15 gives exactly the m16n8k8 A fragment (a register is one f32 of row
+        // qr or qr + 8 at dim 8 kk + c or + 4).  K . Q^T = Kh Qh + Kh Ql + Kl Qh.  Each
+        // product and each parity of kk has its own accumulator (six independent mma
+        // chains of KSTEPS / 2), summed at the end.
+        float sp[3][2][NT][4];
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) sp[j][u][nt][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < SH::KSTEPS; ++kk) {
+          const int c16 = kk * 2 + (lm >> 1);
+          uint32_t r[4], ah[4], al[4];
+          ldsm_x4(smem_addr(kt) + tile_chunk<SH::LINES>(arow, c16, lb), r);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) split_tf32(__uint_as_float(r[i]), ah[i], al[i]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_tf32(sp[0][kk & 1][nt], ah, qlo[nt][kk][0], qlo[nt][kk][1]);
+            mma_tf32(sp[1][kk & 1][nt], al, qb[nt][kk][0], qb[nt][kk][1]);
+            mma_tf32(sp[2][kk & 1][nt], ah, qb[nt][kk][0], qb[nt][kk][1]);
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            s[ch][nt][e] = ((sp[0][0][nt][e] + sp[0][1][nt][e]) +
+                            (sp[1][0][nt][e] + sp[1][1][nt][e])) +
+                           (sp[2][0][nt][e] + sp[2][1][nt][e]);
       } else {
 #pragma unroll
         for (int kk = 0; kk < SH::KSTEPS; ++kk) {
@@ -306,6 +387,9 @@ struct Consumer {
     }
 
     uint32_t pb[SH::JOINT][NT][2];                    // P^T fragments (b0/b1 of the PV mma)
+    // F32: m16n8k8 P^T fragments per 8-token half kk of the chunk, TF32 high parts and
+    // residuals.  The PV k index t <-> token 2t, t + 4 <-> token 2t + 1 of the half.
+    uint32_t pf[SH::F32 ? SH::JOINT : 1][NT][2][2], pfl[SH::F32 ? SH::JOINT : 1][NT][2][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       // max per column over the chunks' rows: in-thread, then lanes of equal qc
@@ -347,7 +431,21 @@ struct Consumer {
         l[nt][0] += pr[0] + pr[2];
         l[nt][1] += pr[1] + pr[3];
         // P rows (tokens qr, qr + 8) x columns (qc, qc + 1) -> transpose to P^T fragments.
-        if constexpr (SH::KV8) {                      // f16 P for the f16 PV mma
+        if constexpr (SH::F32) {
+          // b0 of lane (g, c) is P[token 8 kk + 2c][row g], held by lane 8c + g / 2 as its
+          // element 2 kk + (g & 1); b1 is token 2c + 1, held by lane 8c + 4 + g / 2.
+          const int src0 = 8 * (lane & 3) + (qr >> 1);
+          const bool odd = qr & 1;
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const float x0 = __shfl_sync(0xffffffffu, pr[2 * kk], src0 + 4 * j);
+              const float x1 = __shfl_sync(0xffffffffu, pr[2 * kk + 1], src0 + 4 * j);
+              split_tf32(odd ? x1 : x0, pf[ch][nt][kk][j], pfl[ch][nt][kk][j]);
+            }
+          }
+        } else if constexpr (SH::KV8) {                      // f16 P for the f16 PV mma
           pb[ch][nt][0] = movmatrix_trans(pack_f16x2(pr[0], pr[1]));
           pb[ch][nt][1] = movmatrix_trans(pack_f16x2(pr[2], pr[3]));
         } else {
@@ -361,7 +459,36 @@ struct Consumer {
 #pragma unroll
     for (int ch = 0; ch < SH::JOINT; ++ch) {
       const int rb = r0 + (cg + ch) * 16;
-      if constexpr (SH::KV8) {
+      if constexpr (SH::F32) {
+        // m16n8k8 A fragment of V^T from two 8-byte loads: m-row qr <-> dim 16 mt + 2 qr,
+        // m-row qr + 8 <-> dim 16 mt + 2 qr + 1 (undone when the output is written), k
+        // index c <-> token 2c and c + 4 <-> token 2c + 1.  A half-warp's 16 loads cover
+        // 16 distinct 8-byte slots of the swizzled rows: no bank conflicts.
+        const int c = lane & 3;
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const int row = rb + 8 * kk + 2 * c;
+#pragma unroll
+          for (int mt = 0; mt < SH::MTILES; ++mt) {
+            const int dim = mt * 16 + 2 * qr;
+            const uint32_t off = (uint32_t)(dim & 3) * 4u;
+            const uint2 x = *reinterpret_cast<const uint2*>(
+                vt + tile_chunk<SH::LINES>(row, dim >> 2, lb) + off);
+            const uint2 y = *reinterpret_cast<const uint2*>(
+                vt + tile_chunk<SH::LINES>(row + 1, dim >> 2, lb) + off);
+            const uint32_t a[4] = {x.x, x.y, y.x, y.y};
+            uint32_t ah[4], al[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) split_tf32(__uint_as_float(a[i]), ah[i], al[i]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_tf32(acc[nt][mt], ah, pfl[ch][nt][kk][0], pfl[ch][nt][kk][1]);
+              mma_tf32(acc[nt][mt], al, pf[ch][nt][kk][0], pf[ch][nt][kk][1]);
+              mma_tf32(acc[nt][mt], ah, pf[ch][nt][kk][0], pf[ch][nt][kk][1]);
+            }
+          }
+        }
+      } else if constexpr (SH::KV8) {
         // ldmatrix.trans over 16-bit pairs of codes: matrix j covers tokens
         // rb + 8 (j & 1) .. +7 of chunk (m-tile) mt + (j >> 1); a register holds tokens
         // (qc, qc+1) x dims (2 qr, 2 qr + 1).  Regrouped by dim (prmt) and widened, it
@@ -447,8 +574,9 @@ struct Consumer {
 #pragma unroll
           for (int mt = 0; mt < SH::MTILES; ++mt) {
             // m-rows qr, qr + 8 of tile mt are dims 16 mt + (qr, qr + 8), or with FP8 KV
-            // dims 16 mt + (2 qr, 2 qr + 1); the V scale applies to the whole output.
-            const int d0 = SH::KV8 ? 2 * qr : qr, d1 = SH::KV8 ? 2 * qr + 1 : qr + 8;
+            // or f32 dims 16 mt + (2 qr, 2 qr + 1); the V scale applies to the whole output.
+            constexpr bool PAIRED = SH::KV8 || SH::F32;
+            const int d0 = PAIRED ? 2 * qr : qr, d1 = PAIRED ? 2 * qr + 1 : qr + 8;
             macc[macc_index<G, SH::D>(warp, h, mt * 16 + d0)] = acc[nt][mt][e] * vsc;
             macc[macc_index<G, SH::D>(warp, h, mt * 16 + d1)] = acc[nt][mt][2 + e] * vsc;
           }
@@ -485,7 +613,8 @@ struct Consumer {
           float* o = p.o_part + (row * p.S + split) * SH::D;
 #pragma unroll
           for (int mt = 0; mt < SH::MTILES; ++mt) {
-            const int d0 = SH::KV8 ? 2 * qr : qr, d1 = SH::KV8 ? 2 * qr + 1 : qr + 8;
+            constexpr bool PAIRED = SH::KV8 || SH::F32;
+            const int d0 = PAIRED ? 2 * qr : qr, d1 = PAIRED ? 2 * qr + 1 : qr + 8;
             o[mt * 16 + d0] = acc[nt][mt][e] * vsc / L;
             o[mt * 16 + d1] = acc[nt][mt][2 + e] * vsc / L;
           }
@@ -881,7 +1010,7 @@ cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap
     dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
     e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
   } else if (p.head_group) {
-    if constexpr (SH::D == 128 && !SH::KV8) {
+    if constexpr (SH::D == 128 && !SH::KV8 && !SH::F32) {
       auto kernel = fd_partial_heads_kernel<SH>;
       e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)SH::SMEM_BYTES);
@@ -922,9 +1051,27 @@ cudaError_t dispatch_g(const Params& p, const CUtensorMap& tk, const CUtensorMap
   }
 }
 
+template <int D>
+cudaError_t dispatch_f32(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                         cudaStream_t stream) {
+  switch (rows_template(p.n_rows)) {
+    case 1: return launch_mma<MmaShape<D, 1, false, false, false, true>>(p, tk, tv, stream);
+    case 2: return launch_mma<MmaShape<D, 2, false, false, false, true>>(p, tk, tv, stream);
+    case 4: return launch_mma<MmaShape<D, 4, false, false, false, true>>(p, tk, tv, stream);
+    case 8: return launch_mma<MmaShape<D, 8, false, false, false, true>>(p, tk, tv, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <bool PERSIST>
 cudaError_t dispatch_kind(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                           cudaStream_t stream) {
+  if (p.in_f32) {   // the host runs f32 inputs here on the grid schedule only
+    if constexpr (PERSIST) return cudaErrorInvalidValue;
+    else if (p.head_group) return cudaErrorInvalidValue;
+    else return p.d == 128 ? dispatch_f32<128>(p, tk, tv, stream)
+                           : p.d == 64 ? dispatch_f32<64>(p, tk, tv, stream) : cudaErrorInvalidValue;
+  }
   if (p.kv_fp8) return p.d == 128 ? dispatch_g<128, true, PERSIST>(p, tk, tv, stream) : cudaErrorInvalidValue;
   if (p.d == 128) return dispatch_g<128, false, PERSIST>(p, tk, tv, stream);
   if (p.d == 64) return dispatch_g<64, false, PERSIST>(p, tk, tv, stream);

@@ -163,7 +163,9 @@ def test_partial_kernel_name_follows_settings():
         assert name(bf, bf, 128, 6, 16) == "fd_partial_mma_kernel"             # Hkv % 4
         assert name(bf, bf, 64, 8, 16) == "fd_partial_mma_kernel"              # d = 64
         assert name(bf, f8, 128, 8, 16) == "fd_partial_mma_kernel"             # FP8 KV
-        assert name(f32, f32, 128, 8) == "fd_partial_simt_kernel"
+        assert name(f32, f32, 128, 8) == "fd_partial_mma_kernel"               # 3xTF32
+        assert name(f32, f32, 64, 8, 16, rows=4) == "fd_partial_mma_kernel"    # grid only
+        assert name(f32, f32, 128, 8, rows=16) == "fd_partial_simt_kernel"     # > 8 rows
         assert name(f32, f8, 128, 8) is None
         assert name(bf, bf, 128, 8, rows=32) == "fd_partial_wide_kernel"      # Q x G > 16
         assert name(bf, bf, 128, 8, 16, rows=64) == "fd_partial_wide_kernel"
@@ -179,7 +181,11 @@ def test_partial_kernel_name_follows_settings():
         fd.set_schedule(fd.FD_SCHEDULE_PERSISTENT)
         assert name(bf, bf, 128, 8, 16) == "fd_partial_persist_kernel"
         assert name(bf, bf, 128, 8) == "fd_partial_persist_kernel"
+        assert name(f32, f32, 128, 8) == "fd_partial_mma_kernel"
+        fd.set_path(fd.FD_PATH_MMA)
+        assert name(f32, f32, 128, 8, rows=16) is None
         fd.set_path(fd.FD_PATH_SIMT)
+        assert name(f32, f32, 128, 8) == "fd_partial_simt_kernel"
         assert name(bf, bf, 128, 8) == "fd_partial_simt_kernel"
     finally:
         lib.fd_set_schedule(fd.FD_SCHEDULE_AUTO)

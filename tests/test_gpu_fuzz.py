@@ -52,8 +52,11 @@ def draw(i, medium=False):
     sched = r.choice([fd.FD_SCHEDULE_AUTO, fd.FD_SCHEDULE_GRID, fd.FD_SCHEDULE_PERSISTENT,
                       fd.FD_SCHEDULE_HEAD_GROUPS])
     merge = r.choice([fd.FD_MERGE_KERNEL, fd.FD_MERGE_KERNEL, fd.FD_MERGE_IN_KERNEL])
-    path = fd.FD_PATH_SIMT if (f32 or (not fp8 and Q * G <= 16 and r.random() < 0.2)) \
-        else fd.FD_PATH_MMA
+    if f32:     # the tensor-core path takes up to 8 f32 rows
+        path = fd.FD_PATH_MMA if Q * G <= 8 and r.random() < 0.7 else fd.FD_PATH_SIMT
+    else:
+        path = fd.FD_PATH_SIMT if (not fp8 and Q * G <= 16 and r.random() < 0.2) \
+            else fd.FD_PATH_MMA
     return dict(d=d, fp8=fp8, f32=f32, Q=Q, G=G, Hkv=Hkv, B=B, ps=ps, cap=cap, lens=lens, S=S,
                 sched=sched, merge=merge, path=path)
 

@@ -6,7 +6,8 @@ Tolerances (written here, applied to every element):
   * f32 inputs, f32 out:            |got - ref| <= 1e-4
   * lse_out (natural log):          |got - ref| <= 1e-4 + 1e-5 |ref|
   * no NaN anywhere; rows with no key give out = 0 and lse = -inf exactly.
-Both kernel paths (CUDA-core and tensor-core) are checked for bf16.
+Both kernel paths (CUDA-core and tensor-core) are checked for bf16; the f32 tensor-core
+path has its own file (test_gpu_f32.py).
 """
 import math
 
@@ -109,7 +110,7 @@ def test_worked_example(dtype):
     if dtype == "bf16":
         w = workloads.Workload(w.name, w.q.bfloat16(), w.k.bfloat16(), w.v.bfloat16(),
                                w.seq_lens, num_splits=2, out_dtype=torch.float32)
-    paths = [fd.FD_PATH_SIMT] if dtype == "f32" else [fd.FD_PATH_SIMT, fd.FD_PATH_MMA]
+    paths = [fd.FD_PATH_SIMT, fd.FD_PATH_MMA]
     exact = 9.0 * math.exp(10.0) / (2.0 + math.exp(10.0))
     for path in paths:
         o, l, ws, S = run(w, path=path)
@@ -132,12 +133,10 @@ def test_worked_example(dtype):
 def test_config1_tiny_fp32():
     w = workloads.config1()
     ref_o, ref_l = ref_for(w, "c1")
-    o, l, _, S = run(w, path=fd.FD_PATH_SIMT)
-    assert S == 4
-    check(w, o, l, ref_o, ref_l)
-    # The tensor-core path does not take fp32 inputs: it says so.
-    with pytest.raises(fd.FdError):
-        run(w, path=fd.FD_PATH_MMA)
+    for path in (fd.FD_PATH_SIMT, fd.FD_PATH_MMA, fd.FD_PATH_AUTO):   # AUTO: tensor cores
+        o, l, _, S = run(w, path=path)
+        assert S == 4
+        check(w, o, l, ref_o, ref_l)
 
 
 @pytest.mark.parametrize("name,path", PATHS_BF16)
