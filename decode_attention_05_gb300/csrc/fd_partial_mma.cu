@@ -55,7 +55,8 @@ struct MmaShape {
   static constexpr int NCW = F32 ? TT / 16 : 4;            // consumer warps (f32 d=128: 2)
   static constexpr int ROWS_PER_WARP = WIDE ? TT : TT / NCW;   // token rows of a warp per tile
   static constexpr int CHUNKS = ROWS_PER_WARP / 16;        // 16-token chunks per warp per tile
-  static constexpr int JOINT = CHUNKS < 2 ? CHUNKS : 2;    // chunks sharing one softmax update
+  // chunks sharing one softmax update (wide groups of 8 rows a warp: the whole tile)
+  static constexpr int JOINT = (WIDE && NT == 1) ? CHUNKS : (CHUNKS < 2 ? CHUNKS : 2);
   static constexpr int KSTEPS = F32 ? D / 8 : D / 16;     // k-steps of the QK^T product
   static constexpr int QLO = F32 ? KSTEPS : 1;             // TF32 residual fragments of q
   static constexpr int MTILES = D / 16;                    // m-tiles of the PV product
@@ -113,18 +114,18 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// An f32 value as a TF32 pair hi + lo: hi = x rounded to TF32 (10 mantissa bits), lo =
-// the residual x - hi rounded to TF32.  With a = ah + al and b = bh + bl, ah bh + ah bl +
-// al bh carries about 21 bits of each product (al bl, ~2^-22 relative, is dropped):
-// f32 accuracy for this pass from three TF32 tensor-core products.
-__device__ __forceinline__ uint32_t cvt_tf32(float x) {
-  uint32_t y;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
-  return y;
-}
+// An f32 value as a TF32 pair hi + lo.  hi: x rounded to the nearest TF32 value (10
+// mantissa bits, ties away from zero), by adding half a TF32 unit to the bit pattern and
+// clearing the 13 low bits (a carry into the exponent is the correct rounding up to the
+// next binade).  lo = x - hi, exact in f32 and at most half a TF32 unit of x (2^-11 |x|);
+// the mma reads it as TF32 (its low 13 bits do not take part), an error below 2^-21 |x|.  With a = ah + al and b = bh + bl, ah bh + ah bl + al bh then carries about
+// 21 bits of each product (al bl, ~2^-22 relative, is dropped): f32 accuracy for this
+// pass from three TF32 tensor-core products, at three integer/float ops per split.
+// Non-finite inputs only occur in masked slots, whose scores are replaced by -inf and
+// whose V rows are zeroed before use.
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  hi = cvt_tf32(x);
-  lo = cvt_tf32(x - __uint_as_float(hi));
+  hi = (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
+  lo = __float_as_uint(x - __uint_as_float(hi));
 }
 
 // D = A . B + D, m16n8k16, f16 inputs, f32 accumulators (the FP8 KV path).
