@@ -61,7 +61,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
     ap.add_argument("--config", type=int, default=3, help="workload number (1-5)")
     ap.add_argument("--num-splits", type=int, default=0, help="0 = library heuristic")
-    ap.add_argument("--path", choices=["auto", "simt", "mma"], default="auto")
+    ap.add_argument("--path", choices=["auto", "simt", "mma", "tcgen05"], default="auto")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -112,6 +112,10 @@ KERNEL_SOURCES = {
                                   "fd_device.cuh", "fd_internal.h"],
     "fd_partial_simt_kernel": ["fd_partial_simt.cu", "fd_partial_simt.cuh", "fd_pipeline.cuh",
                                "fd_epilogue.cuh", "fd_device.cuh", "fd_internal.h"],
+    "fd_partial_wide_kernel": ["fd_partial_mma.cu", "fd_pipeline.cuh", "fd_epilogue.cuh",
+                               "fd_device.cuh", "fd_internal.h"],
+    "fd_partial_tc_kernel": ["fd_partial_tc.cu", "fd_pipeline.cuh", "fd_epilogue.cuh",
+                             "fd_device.cuh", "fd_internal.h"],
 }
 
 
@@ -347,7 +351,8 @@ def run_fd(args):
     import decode_attention_05_gb300 as fd
     from decode_attention_05_gb300._binding import tensor_desc
     L = fd.lib()
-    fd.set_path({"auto": fd.FD_PATH_AUTO, "simt": fd.FD_PATH_SIMT, "mma": fd.FD_PATH_MMA}[args.path])
+    fd.set_path({"auto": fd.FD_PATH_AUTO, "simt": fd.FD_PATH_SIMT, "mma": fd.FD_PATH_MMA,
+                 "tcgen05": fd.FD_PATH_TCGEN05}[args.path])
 
     w_cpu = workloads.CONFIGS[args.config]()
     scales_cpu = None
@@ -497,9 +502,9 @@ def run_fd(args):
     merge_ms = e4.elapsed_time(e5) / args.steps
     peak, peak_src = measured_peak()
     achieved = kv_bytes / (partial_ms * 1e-3) / 1e9
-    path_name = "mma" if (args.path == "mma" or (args.path == "auto" and w.q.dtype == torch.bfloat16)) else "simt"
     kernel = fd.partial_kernel_name(w.q.dtype, w.k.dtype, d, w.Hkv, w.page_size,
                                     rows=Hq // Hkv)
+    path_name = {"fd_partial_simt_kernel": "simt", "fd_partial_tc_kernel": "tcgen05"}.get(kernel, "mma")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kernel, w.name),
                 "kernel": kernel, "peak_source": peak_src,

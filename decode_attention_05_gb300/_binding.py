@@ -13,7 +13,7 @@ from . import build as _build
 FD_OK = 0
 FD_ERR_DEVICE_FLAG = 5
 FD_F32, FD_BF16, FD_I32, FD_F8E4M3 = 0, 1, 2, 3
-FD_PATH_AUTO, FD_PATH_SIMT, FD_PATH_MMA = 0, 1, 2
+FD_PATH_AUTO, FD_PATH_SIMT, FD_PATH_MMA, FD_PATH_TCGEN05 = 0, 1, 2, 3
 FD_MERGE_KERNEL, FD_MERGE_IN_KERNEL = 0, 1
 FD_SCHEDULE_AUTO, FD_SCHEDULE_GRID, FD_SCHEDULE_PERSISTENT, FD_SCHEDULE_HEAD_GROUPS = 0, 1, 2, 3
 

@@ -47,11 +47,21 @@ Schedule choose_schedule(int path, bool kv8, bool f32, int64_t d, int64_t Hkv,
   return sc;
 }
 
-// Automatic choice: the tensor-core path for bf16, and for f32 groups of up to
-// kMaxF32MmaRows query rows per kv head; the CUDA-core path for larger f32 groups.
-int resolve_path(int32_t q_dtype, int64_t rows) {
+// Whether the tcgen05 kernel takes a call: bf16 q/K/V, d = 128, contiguous or pages of
+// at least 16 tokens (its per-page products need N >= 16), up to kMaxRows rows.
+bool tc_takes(int32_t q_dtype, bool kv8, int64_t d, int32_t page_size, int64_t rows) {
+  return q_dtype == FD_BF16 && !kv8 && d == 128 && (page_size == 0 || page_size >= 16) &&
+         rows >= 1 && rows <= fd::kMaxRows;
+}
+
+// Automatic choice: groups above kMaxNarrowRows rows go to the tcgen05 kernel where it
+// applies; otherwise the mma.sync path for bf16 and for f32 groups of up to
+// kMaxF32MmaRows rows, and the CUDA-core path for larger f32 groups.
+int resolve_path(int32_t q_dtype, bool kv8, int64_t d, int32_t page_size, int64_t rows) {
   const int path = g_path.load();
   if (path != FD_PATH_AUTO) return path;
+  if (rows > fd::kMaxNarrowRows && tc_takes(q_dtype, kv8, d, page_size, rows))
+    return FD_PATH_TCGEN05;
   return q_dtype == FD_BF16 || rows <= fd::kMaxF32MmaRows ? FD_PATH_MMA : FD_PATH_SIMT;
 }
 
@@ -236,7 +246,8 @@ const char* fd_status_string(fd_status s) {
 }
 
 fd_status fd_set_path(int32_t path) {
-  if (path != FD_PATH_AUTO && path != FD_PATH_SIMT && path != FD_PATH_MMA)
+  if (path != FD_PATH_AUTO && path != FD_PATH_SIMT && path != FD_PATH_MMA &&
+      path != FD_PATH_TCGEN05)
     return fail(FD_ERR_INVALID_ARG, "unknown kernel path %d", path);
   g_path.store(path);
   return FD_OK;
@@ -270,10 +281,12 @@ const char* fd_partial_kernel_name(int32_t dtype, int32_t kv_dtype, int32_t d, i
       (kv8 && dtype != FD_BF16) || d <= 0 || Hkv <= 0 || page_size < 0 || rows < 1 ||
       rows > fd::kMaxRows)
     return nullptr;
-  const int path = resolve_path(dtype, rows);
+  const int path = resolve_path(dtype, kv8, d, page_size, rows);
   if ((path == FD_PATH_MMA && dtype == FD_F32 && rows > fd::kMaxF32MmaRows) ||
       (kv8 && path != FD_PATH_MMA))
     return nullptr;
+  if (path == FD_PATH_TCGEN05)
+    return tc_takes(dtype, kv8, d, page_size, rows) ? "fd_partial_tc_kernel" : nullptr;
   if (rows > fd::kMaxNarrowRows && (path != FD_PATH_MMA || kv8)) return nullptr;
   if (path == FD_PATH_SIMT) return "fd_partial_simt_kernel";
   if (rows > fd::kMaxNarrowRows) return "fd_partial_wide_kernel";
@@ -455,16 +468,21 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
     return fail(FD_ERR_UNSUPPORTED, "grid too large");
 
   // ---- path
-  const int path = resolve_path(q->dtype, Q * G);
+  const int path = resolve_path(q->dtype, kv8, d, paged ? page_size : 0, Q * G);
+  if (path == FD_PATH_TCGEN05 && !tc_takes(q->dtype, kv8, d, paged ? page_size : 0, Q * G))
+    return fail(FD_ERR_UNSUPPORTED,
+                "the tcgen05 kernel takes bf16 q/K/V with d = 128, up to %d query rows per kv "
+                "head and pages of at least 16 tokens",
+                fd::kMaxRows);
   if (path == FD_PATH_MMA && q->dtype == FD_F32 && Q * G > fd::kMaxF32MmaRows)
     return fail(FD_ERR_UNSUPPORTED,
                 "the tensor-core path takes f32 inputs for up to %d query rows per kv head",
                 fd::kMaxF32MmaRows);
   if (kv8 && path != FD_PATH_MMA)
     return fail(FD_ERR_UNSUPPORTED, "the FP8 KV cache runs on the tensor-core path only");
-  if (Q * G > fd::kMaxNarrowRows && (path != FD_PATH_MMA || kv8))
+  if (Q * G > fd::kMaxNarrowRows && (path == FD_PATH_SIMT || kv8))
     return fail(FD_ERR_UNSUPPORTED,
-                "more than %d query rows per kv head (%lld) run on the bf16 tensor-core path only",
+                "more than %d query rows per kv head (%lld) run on the bf16 tensor-core paths only",
                 fd::kMaxNarrowRows, (long long)(Q * G));
 
   // ---- schedule (fd_set_schedule)
@@ -539,8 +557,9 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
 }
 
 fd_status launch_partial(const Prepared& pr, cudaStream_t s) {
-  cudaError_t e = pr.path == FD_PATH_MMA ? fd::launch_partial_mma(pr.p, pr.tk, pr.tv, s)
-                                         : fd::launch_partial_simt(pr.p, pr.tk, pr.tv, pr.dtype, s);
+  cudaError_t e = pr.path == FD_PATH_MMA      ? fd::launch_partial_mma(pr.p, pr.tk, pr.tv, s)
+                  : pr.path == FD_PATH_TCGEN05 ? fd::launch_partial_tc(pr.p, pr.tk, pr.tv, s)
+                                               : fd::launch_partial_simt(pr.p, pr.tk, pr.tv, pr.dtype, s);
   if (e != cudaSuccess) return fail(FD_ERR_CUDA, "partial-pass launch: %s", cudaGetErrorString(e));
   return FD_OK;
 }

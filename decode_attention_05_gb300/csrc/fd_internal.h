@@ -72,6 +72,11 @@ struct Params {
 };
 
 // Launchers (each returns the launch's cudaError_t).
+// tcgen05 kernel (fd_partial_tc.cu): bf16 q/K/V, d = 128, 1..64 query rows per kv head,
+// contiguous caches or pages of at least 16 tokens, grid schedule.
+bool partial_tc_supported(const Params& p);
+cudaError_t launch_partial_tc(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                              cudaStream_t stream);
 cudaError_t launch_partial_simt(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                 int dtype, cudaStream_t stream);
 cudaError_t launch_partial_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,

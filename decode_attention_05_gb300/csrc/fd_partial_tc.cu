@@ -1,0 +1,566 @@
+// fd_partial_tc.cu -- split-KV partial pass on the 5th-generation tensor cores
+// (tcgen05.mma, accumulators in tensor memory), for groups of up to 64 query rows per
+// kv head: multi-token decode on GQA groups (Q query tokens x G heads), or groups of
+// 32 and 64 heads.  bf16 inputs, d = 128.
+//
+// Per tile of TT = 64 tokens of one kv head (the TMA tiles of fd_pipeline.cuh, used as
+// the mma operands in place):
+//   S[128, TT]  = Q[128, d] . K_tile^T          tcgen05.mma, M = 128 (query rows 0..R-1,
+//                                               the rest padding), N = TT, into TMEM
+//   one thread per query row reads its row of S from TMEM (tcgen05.ld), masks it, keeps
+//   the running max m and sum l, and writes P = bf16(2^(S - m)) to shared memory
+//   O[128, d]  += P[128, TT] . V_tile[TT, d]    tcgen05.mma, V read as an MN-major
+//                                               operand, O kept in TMEM
+// This is the FlashAttention block update of "AI Infra: math and infra optimisation in
+// large models", section 2.6, inside one split of Flash-Decoding (same section, Split-K):
+// S = Q K^T per KV block; rescale the running sum and output by exp(m_old - m_new); add
+// exp(S - m_new) V.  The running max only moves (and O in TMEM is rescaled) when a
+// tile's max exceeds it by more than 8 in base-2 units: every 2^(S - m) then stays at
+// most 2^8, and since l and O use the same m throughout, the result is unchanged.
+//
+// Why: with R query rows per kv head each KV byte feeds R flops, and past 16 rows the
+// mma.sync kernels become bound by issue latency and by every warp re-reading the tile
+// from shared memory.  Here one thread issues each tile's products as a few large
+// instructions that read the tile once, and the other warps only do the softmax.
+//
+// Warps: 0-7 softmax in two groups of four, 8 the TMA producer, 9 the mma issuer (one
+// thread).  Group g takes the tiles n = g mod 2 with its own S buffer, P buffer and O
+// accumulator, so the two groups' per-tile handoffs (scores ready, P written, product
+// done) overlap.  The 128 rows of the products are the R query rows repeated 128 / R
+// times (Q is stored that way): TMEM lane L holds query row L mod R, and its thread
+// takes the slice L / R of each tile's tokens (TT R / 128 of them), with its own running
+// max and sum (P is zero outside the slice).  The 2 x 128 / R partial states of a row
+// are merged at the end of the split, like the warps of the mma.sync kernel.  One CTA
+// per SM: 5 stages of K + V (160 KB), Q (32 KB), two P buffers (2 x 16 KB), 512 TMEM
+// columns (S 2 x 64, O 2 x 128).
+#include <cuda_bf16.h>
+
+#include "fd_epilogue.cuh"
+
+namespace fd {
+namespace {
+
+constexpr int kTcD = 128;
+constexpr int kTcTT = 64;                    // tokens per tile (16 KB of K, 16 KB of V)
+constexpr int kTcStages = 5;
+constexpr int kTcThreads = 320;
+constexpr int kTcSoftThreads = 256;          // two groups of four warps
+constexpr uint32_t kTcCols = 512;            // TMEM columns: S 2 x 64, O 2 x 128
+constexpr uint32_t kTcOCol = 128;            // O of group g at kTcOCol + 128 g
+// Shared memory, from a 1024-byte aligned base: the ring, Q (two 64-dim slabs of 128
+// rows, K-major, 128-byte swizzled), two P buffers (128 rows x 64 tokens, K-major,
+// swizzled), the control block.
+constexpr uint32_t kTcQOff = kTcStages * 2 * kTileBytes;    // 160 KB
+constexpr uint32_t kTcSlab = 128 * 128;                     // one 64-dim slab of 128 rows
+constexpr uint32_t kTcPOff = kTcQOff + 2 * kTcSlab;
+constexpr uint32_t kTcPBytes = 128 * 128;
+constexpr uint32_t kTcCtlOff = kTcPOff + 2 * kTcPBytes;
+
+struct TcCtl {
+  PipeCtl<kTcStages> pipe;   // TMA ring (empty: released by the mma issuer's commit)
+  uint64_t s_full[2];        // S buffer b holds a finished Q K^T (tcgen05.commit)
+  uint64_t s_free[2];        // the softmax warps have read S buffer b
+  uint64_t p_full[2];        // P of tile n (and its zeroed V rows) is in place, n % 2 = b
+                             // (two barriers: the softmax may finish tile n + 1 before
+                             // the issuer has seen tile n, and a parity wait must never
+                             // be two phases behind its barrier)
+  uint64_t pv_done[2];       // the P V product reading P buffer b has completed
+  uint64_t mma_done;         // every product this CTA issued has completed
+  uint32_t tmem;             // TMEM base address (tcgen05.alloc)
+};
+constexpr size_t kTcSmemBytes = 1024 + kTcCtlOff + ((sizeof(TcCtl) + 127) / 128) * 128;
+static_assert(kTcSmemBytes <= 227 * 1024, "one CTA per SM");
+
+// ---------------------------------------------------------------- tcgen05 wrappers
+__device__ __forceinline__ void tc_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+               :: "r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D (TMEM) = A . B (+ D when accumulate != 0); A, B described in shared memory.
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+// Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               :: "r"(bar) : "memory");
+}
+// TMEM -> registers: 32 consecutive f32 columns of this thread's lane (a warp reads
+// lanes 32 (warp % 4) .. + 31), with the wait inside the same asm statement so that no
+// use of the registers can be scheduled before the data has arrived.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Registers -> TMEM (32 columns of the lane), complete before the statement ends.
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;"
+      :: "r"(taddr), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+         "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]),
+         "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]),
+         "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory operand descriptor, 128-byte swizzle: start address, leading and stride
+// byte offsets (16-byte units), descriptor version 1, layout 2 = SWIZZLE_128B.
+//   K-major operand (rows of 128 bytes = 64 bf16 along K): stride = 1024 (one 8-row
+//   swizzle atom to the next along M/N); the leading offset is not used.  A k-step of 16
+//   elements inside the atom advances the start address by 32 bytes.
+//   MN-major operand (the V tile: a row is one token, 128 bytes = 64 dims along N):
+//   leading = bytes from one 64-dim slab to the next, stride = 1024 (8 tokens).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lead, uint32_t stride) {
+  return (uint64_t)((addr >> 4) & 0x3fffu) | ((uint64_t)((lead >> 4) & 0x3fffu) << 16) |
+         ((uint64_t)((stride >> 4) & 0x3fffu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of kind::f16: f32 accumulator, bf16 A and B, A K-major, B
+// K-major (b_mn = 0) or MN-major (1), N >> 3 and M >> 4.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Byte offset of 16-byte chunk c of row r in a K-major, 128-byte swizzled operand.
+__device__ __forceinline__ uint32_t kmajor_chunk(uint32_t r, uint32_t c) {
+  return (r >> 3) * 1024u + (r & 7u) * 128u + ((c ^ (r & 7u)) << 4);
+}
+
+// A bounded wait whose outcome every lane of the warp shares.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(bar, parity);
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void set_abort(const Params& p, TcCtl* ctl) {
+  *reinterpret_cast<volatile int32_t*>(&ctl->pipe.abort) = 1;
+  atomicOr(p.flags, kDevFlagTimeout);
+}
+__device__ __forceinline__ bool aborted(TcCtl* ctl) {
+  return *reinterpret_cast<volatile int32_t*>(&ctl->pipe.abort) != 0;
+}
+
+// ---------------------------------------------------------------- mma issuer
+// Non-blocking probe of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Probe that may suspend the thread for up to `hint_ns` while the phase is incomplete.
+__device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// One thread, event-driven: it issues each tile's scores S(j) = Q K(j)^T as soon as the
+// tile has landed and its S buffer is free (up to two tiles ahead), and each tile's
+// P V product as soon as its P is in place.  The product of tile n never waits for a
+// later tile to land, so a stage is released as early as its own work allows.
+__device__ void issue_products(const Params& p, const SplitInfo& si, uint8_t* stages,
+                               uint8_t* qs, uint8_t* ps, TcCtl* ctl, uint32_t tmem) {
+  const bool multi_page = p.block_table != nullptr && p.page_size < kTcTT;
+  const int box = multi_page ? p.page_size : kTcTT;     // token rows of one TMA box
+  const int nbox = kTcTT / box;
+  const uint32_t box_bytes = 2u * (uint32_t)box * 128u;  // [line][row][128 B], 2 lines
+  const uint32_t id_s = instr_desc(128, box, 0), id_pv = instr_desc(128, kTcD, 1);
+  const uint32_t qa = smem_addr(qs), pa = smem_addr(ps);
+  const int N = si.n_tiles;
+  auto s_ready = [&](int j) -> bool {
+    return mbar_test(smem_addr(&ctl->pipe.full[j % kTcStages]), (j / kTcStages) & 1) &&
+           (j < 2 || mbar_test(smem_addr(&ctl->s_free[j & 1]), ((j >> 1) - 1) & 1));
+  };
+  auto issue_s = [&](int j) {
+    tc_fence_after();
+    const uint32_t kb = smem_addr(stages + (size_t)(j % kTcStages) * 2 * kTileBytes);
+    for (int bx = 0; bx < nbox; ++bx) {
+#pragma unroll
+      for (int ks = 0; ks < kTcD / 16; ++ks) {
+        const uint64_t a = smem_desc(qa + (ks >> 2) * kTcSlab + (ks & 3) * 32u, 0, 1024);
+        const uint64_t b = smem_desc(kb + bx * box_bytes + (ks >> 2) * (uint32_t)box * 128u +
+                                         (ks & 3) * 32u, 0, 1024);
+        tc_mma(tmem + (j & 1) * kTcTT + bx * box, a, b, id_s, ks > 0);
+      }
+    }
+    tc_commit(smem_addr(&ctl->s_full[j & 1]));
+  };
+  bool ok = true;
+  int ns = 0;                                  // next tile whose scores are to be issued
+  for (int n = 0; ok && n < N; ++n) {
+    const uint64_t t0 = global_ns();
+    for (;;) {
+      if (ns < N && ns <= n + 2 && s_ready(ns)) {
+        issue_s(ns++);
+        continue;
+      }
+      if (ns > n && mbar_probe(smem_addr(&ctl->p_full[n & 1]), (n >> 1) & 1, 200u)) break;
+      if (aborted(ctl) || global_ns() - t0 > kWaitLimitNs) {
+        ok = false;
+        break;
+      }
+    }
+    if (!ok) break;
+    tc_fence_after();
+    const int st = n % kTcStages;
+    const uint32_t vb = smem_addr(stages + (size_t)st * 2 * kTileBytes + kTileBytes);
+    const uint32_t pn = pa + (uint32_t)(n & 1) * kTcPBytes;
+#pragma unroll
+    for (int ks = 0; ks < kTcTT / 16; ++ks) {
+      const int tok = ks * 16, bx = tok / box, rr = tok % box;
+      const uint64_t a = smem_desc(pn + ks * 32u, 0, 1024);
+      const uint64_t b = smem_desc(vb + bx * box_bytes + (uint32_t)rr * 128u,
+                                   (uint32_t)box * 128u, 1024);
+      tc_mma(tmem + kTcOCol + (uint32_t)(n & 1) * kTcD, a, b, id_pv, (n > 1 || ks > 0) ? 1u : 0u);
+    }
+    tc_commit(smem_addr(&ctl->pv_done[n & 1]));
+    tc_commit(smem_addr(&ctl->pipe.empty[st]));
+  }
+  if (!ok) set_abort(p, ctl);
+  // Never leave (or free TMEM) with products in flight.
+  tc_commit(smem_addr(&ctl->mma_done));
+  if (!mbar_wait(smem_addr(&ctl->mma_done), 0)) atomicOr(p.flags, kDevFlagTimeout);
+}
+
+// ---------------------------------------------------------------- softmax warps
+// Thread t (0..255): group g = t / 128 takes tiles n = g mod 2; within it, TMEM lane
+// tg = t mod 128 holds query row h = tg mod R and the token slice tg / R of each tile.
+// Returns false if a bounded wait gave up.
+template <int R>
+__device__ bool softmax_rows(const Params& p, const SplitInfo& si, uint8_t* stages,
+                             uint8_t* ps, TcCtl* ctl, uint32_t tmem, int t, float& m_out,
+                             float& l_out) {
+  constexpr int SLICE = kTcTT * R / 128;             // tokens of a tile per lane: 32 or 16
+  const int grp = t >> 7, tg = t & 127;
+  const int warp = tg >> 5, lane = t & 31;
+  const int h = tg % R, slice = tg / R;
+  const int64_t kb = key_bound(p, si.L, h);          // causal bound of row h
+  const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+  const bool multi_page = p.block_table != nullptr && p.page_size < kTcTT;
+  const uint32_t lb = (uint32_t)p.log2_box;
+  const float sl2 = p.scale_log2;
+  const int j0 = slice * SLICE;                      // first token of the slice in a tile
+  const uint32_t prow = (uint32_t)(tg >> 3) * 1024u + (uint32_t)(tg & 7) * 128u;
+  const uint32_t ocol = kTcOCol + (uint32_t)grp * kTcD;
+  float m = kNegInf, l = 0.f;
+  for (int n = grp; n < si.n_tiles; n += 2) {
+    const int st = n % kTcStages;
+    // The tile has landed (for its page-validity bits) and its scores are complete.
+    if (!warp_wait(smem_addr(&ctl->pipe.full[st]), (n / kTcStages) & 1, lane)) return false;
+    if (!warp_wait(smem_addr(&ctl->s_full[n & 1]), (n >> 1) & 1, lane)) return false;
+    tc_fence_after();
+    float s[SLICE];
+    if constexpr (SLICE == 32) tc_ld32(tl + (n & 1) * kTcTT + j0, s);
+    else tc_ld16(tl + (n & 1) * kTcTT + j0, s);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&ctl->s_free[n & 1]));
+
+    const int64_t t0 = si.T0 + (int64_t)n * kTcTT;
+    const uint32_t bad = ctl->pipe.bad[st];
+    const bool clean = t0 >= si.lo && t0 + kTcTT <= si.hi && bad == 0;
+    float mt = kNegInf;
+    if (clean && t0 + j0 + SLICE <= kb) {
+#pragma unroll
+      for (int j = 0; j < SLICE; ++j) {
+        s[j] *= sl2;
+        mt = fmaxf(mt, s[j]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < SLICE; ++j) {
+        const int64_t tok = t0 + j0 + j;
+        const int pslot = multi_page ? ((j0 + j) >> p.log2_page) : 0;
+        const bool valid = tok >= si.lo && tok < si.hi && !((bad >> pslot) & 1u) && tok < kb;
+        s[j] = valid ? s[j] * sl2 : kNegInf;
+        mt = fmaxf(mt, s[j]);
+      }
+    }
+    const float mn = fmaxf(m, mt);
+    const bool resc = n > 1 && m != kNegInf && mn > m + 8.f;
+    const float mu = (m == kNegInf || resc) ? mn : m;
+    const float c = resc ? ex2(m - mn) : 1.f;
+    float sum = 0.f;
+    uint32_t pk[SLICE / 2];
+#pragma unroll
+    for (int j = 0; j < SLICE / 2; ++j) {
+      const float p0 = s[2 * j] == kNegInf ? 0.f : ex2(s[2 * j] - mu);
+      const float p1 = s[2 * j + 1] == kNegInf ? 0.f : ex2(s[2 * j + 1] - mu);
+      sum += p0 + p1;
+      pk[j] = pack_bf16(p0, p1);
+    }
+    l = l * c + sum;
+    m = mu;
+
+    // The group's previous product (tile n - 2) has completed: its P buffer is free and
+    // its O stable (tile n's product is not issued before this warp arrives on p_full).
+    if (n >= 2 && !warp_wait(smem_addr(&ctl->pv_done[n & 1]), ((n >> 1) - 1) & 1, lane))
+      return false;
+    tc_fence_after();
+    if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+      for (int q = 0; q < kTcD / 32; ++q) {
+        float o[32];
+        tc_ld32(tl + ocol + q * 32, o);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] *= c;
+        tc_st32(tl + ocol + q * 32, o);
+      }
+    }
+    // This lane's slice of its P row (the rest of the row stays zero).
+    uint8_t* pr = ps + (n & 1) * kTcPBytes + prow;
+#pragma unroll
+    for (int cc = 0; cc < SLICE / 8; ++cc) {
+      const uint32_t chunk = (uint32_t)(j0 / 8 + cc);
+      *reinterpret_cast<uint4*>(pr + ((chunk ^ (uint32_t)(tg & 7)) << 4)) =
+          make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+    }
+    // Boundary tile: the V rows of tokens outside [lo, hi) or on an invalid page may hold
+    // stale values (NaN), and 0 * NaN would poison the product: zero them.
+    if (!clean && tg < kTcTT) {
+      const int64_t tok = t0 + tg;
+      const int pslot = multi_page ? (tg >> p.log2_page) : 0;
+      if (!(tok >= si.lo && tok < si.hi && !((bad >> pslot) & 1u))) {
+        uint8_t* vt = stages + (size_t)st * 2 * kTileBytes + kTileBytes;
+#pragma unroll
+        for (int c16 = 0; c16 < kTcD * 2 / 16; ++c16)
+          *reinterpret_cast<uint4*>(vt + tile_chunk<2>((uint32_t)tg, (uint32_t)c16, lb)) =
+              make_uint4(0, 0, 0, 0);
+      }
+    }
+    fence_proxy_async_smem();       // P and V stores -> the tensor core's reads
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&ctl->p_full[n & 1]));   // one per softmax warp
+  }
+  const int last = si.n_tiles - 1 - ((si.n_tiles - 1 - grp) & 1);   // group's last tile
+  if (last >= 0 && !warp_wait(smem_addr(&ctl->pv_done[grp]), (last >> 1) & 1, lane))
+    return false;
+  m_out = m;
+  l_out = l;
+  return true;
+}
+
+template <int R>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    fd_partial_tc_kernel(const __grid_constant__ CUtensorMap tk,
+                         const __grid_constant__ CUtensorMap tv,
+                         const __grid_constant__ Params p) {
+  static_assert(R == 32 || R == 64, "32 or 64 query rows");
+  constexpr int DUP = 128 / R;      // token slices (copies of each query row) per group
+  constexpr int NPART = 2 * DUP;    // partial states per query row
+  pdl_wait();                       // inputs of this step are visible
+  const SplitInfo si = split_info<kTcTT>(p);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = base;
+  uint8_t* qs = base + kTcQOff;
+  uint8_t* ps = base + kTcPOff;
+  auto* ctl = reinterpret_cast<TcCtl*>(base + kTcCtlOff);
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  if (si.n_tiles == 0) {            // empty split: weight 0 in the merge, nothing to load
+    write_empty_split(p, si, t);
+    pdl_trigger();
+    if (p.counters != nullptr && warp < 8) arrive_and_merge<kTcD, 8>(p, si, t, &ctl->pipe.last);
+    return;
+  }
+
+  if (t == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(smem_addr(&ctl->pipe.full[s]), 1);
+      mbar_init(smem_addr(&ctl->pipe.empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&ctl->s_full[b]), 1);
+      mbar_init(smem_addr(&ctl->s_free[b]), 4);
+      mbar_init(smem_addr(&ctl->pv_done[b]), 1);
+      mbar_init(smem_addr(&ctl->p_full[b]), 4);     // the four warps of group b
+    }
+    mbar_init(smem_addr(&ctl->mma_done), 1);
+    ctl->pipe.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc_alloc(smem_addr(&ctl->tmem), kTcCols);
+    tc_relinquish();
+  }
+  if (warp < 8) {
+    // Q rows -> K-major swizzled slabs, row L holding query row L mod R (rows past the
+    // group are zero); both P buffers start zero (each lane later writes only its slice).
+    for (int i = t; i < 128 * (kTcD / 2); i += kTcSoftThreads) {
+      const int row = i / (kTcD / 2), w = i % (kTcD / 2);   // word w: dims 2w, 2w + 1
+      const int h = row % R;
+      uint32_t v = 0u;
+      if (h < p.n_rows)
+        v = reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                                              q_offset(p, si.b, si.g, h))[w];
+      const int dim = 2 * w;
+      *reinterpret_cast<uint32_t*>(qs + (dim >> 6) * kTcSlab +
+                                   kmajor_chunk((uint32_t)row, (uint32_t)((dim & 63) >> 3)) +
+                                   (dim & 7) * 2) = v;
+    }
+    for (int i = t; i < (int)(2 * kTcPBytes / 16); i += kTcSoftThreads)
+      reinterpret_cast<uint4*>(ps)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+
+  float m = kNegInf, l = 0.f;
+  if (warp == 8) {                  // ---------------- TMA producer
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+    produce_tiles<kTcTT, kTcStages>(p, si, &tk, &tv, stages, &ctl->pipe, lane);
+  } else if (warp == 9) {           // ---------------- mma issuer
+    if (lane == 0) issue_products(p, si, stages, qs, ps, ctl, tmem);
+    __syncwarp();
+  } else {                          // ---------------- softmax
+    if (!softmax_rows<R>(p, si, stages, ps, ctl, tmem, t, m, l) && lane == 0) set_abort(p, ctl);
+  }
+  pdl_trigger();
+  tc_fence_before();
+  __syncthreads();                  // ring drained, every product complete
+  tc_fence_after();
+
+  if (warp < 8) {
+    const bool bad = aborted(ctl);
+    float* macc = reinterpret_cast<float*>(stages);      // [NPART][R][D] (macc_index)
+    float* mm = macc + kTcSoftThreads * kTcD;             // [NPART][R]
+    float* ml = mm + kTcSoftThreads;                      // [NPART][R]
+    if (!bad) {
+      // Partial state t: group t / 128, slice (t mod 128) / R, row t mod R -- i.e. index
+      // t / R, row t mod R of the merge scratch.  A group without tiles (a one-tile split)
+      // has an O that was never written: it contributes zeros with weight 0.
+      const int h = t % R, part = t / R, grp = t >> 7;
+      const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+      const bool has = grp < si.n_tiles;
+#pragma unroll 1
+      for (int q = 0; q < kTcD / 32; ++q) {
+        float o[32];
+        if (has) {
+          tc_ld32(tl + kTcOCol + (uint32_t)grp * kTcD + q * 32, o);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(macc + macc_index<R, kTcD>(part, h, q * 32 + j)) =
+              make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+      }
+      mm[t] = m;
+      ml[t] = l;
+    }
+    named_bar_sync(1, kTcSoftThreads);
+    if (bad) {
+      write_empty_split(p, si, t);
+    } else if (t < NPART * 32) {
+      merge_warps_and_store<R, kTcD, NPART>(p, si, macc, mm, ml, t, [] {
+        named_bar_sync(3, NPART * 32);
+        return true;
+      });
+    }
+    if (p.counters != nullptr) arrive_and_merge<kTcD, 8>(p, si, t, &ctl->pipe.last);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tc_dealloc(tmem, kTcCols);
+  }
+}
+
+template <int R>
+cudaError_t launch_tc(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                      cudaStream_t stream) {
+  auto kernel = fd_partial_tc_kernel<R>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kTcSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
+  e = launch_partial_kernel(kernel, grid, kTcThreads, kTcSmemBytes, stream, tk, tv, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool partial_tc_supported(const Params& p) {
+  return p.d == kTcD && !p.kv_fp8 && !p.in_f32 && p.n_rows >= 1 && p.n_rows <= 64 &&
+         p.head_group == 0 && !p.persistent &&
+         (p.block_table == nullptr || p.page_size >= 16);
+}
+
+cudaError_t launch_partial_tc(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                              cudaStream_t stream) {
+  if (!partial_tc_supported(p)) return cudaErrorInvalidValue;
+  return p.n_rows <= 32 ? launch_tc<32>(p, tk, tv, stream) : launch_tc<64>(p, tk, tv, stream);
+}
+
+}  // namespace fd

@@ -167,8 +167,10 @@ def test_partial_kernel_name_follows_settings():
         assert name(f32, f32, 64, 8, 16, rows=4) == "fd_partial_mma_kernel"    # grid only
         assert name(f32, f32, 128, 8, rows=16) == "fd_partial_simt_kernel"     # > 8 rows
         assert name(f32, f8, 128, 8) is None
-        assert name(bf, bf, 128, 8, rows=32) == "fd_partial_wide_kernel"      # Q x G > 16
-        assert name(bf, bf, 128, 8, 16, rows=64) == "fd_partial_wide_kernel"
+        assert name(bf, bf, 128, 8, rows=32) == "fd_partial_tc_kernel"        # Q x G > 16
+        assert name(bf, bf, 128, 8, 16, rows=64) == "fd_partial_tc_kernel"
+        assert name(bf, bf, 128, 8, 8, rows=64) == "fd_partial_wide_kernel"   # 8-token pages
+        assert name(bf, bf, 64, 8, rows=32) == "fd_partial_wide_kernel"       # d = 64
         assert name(bf, f8, 128, 8, rows=32) is None                          # bf16 only
         assert name(f32, f32, 128, 8, rows=32) is None
         assert name(bf, bf, 128, 8, rows=65) is None
@@ -184,6 +186,14 @@ def test_partial_kernel_name_follows_settings():
         assert name(f32, f32, 128, 8) == "fd_partial_mma_kernel"
         fd.set_path(fd.FD_PATH_MMA)
         assert name(f32, f32, 128, 8, rows=16) is None
+        assert name(bf, bf, 128, 8, rows=32) == "fd_partial_wide_kernel"
+        fd.set_path(fd.FD_PATH_TCGEN05)
+        assert name(bf, bf, 128, 8) == "fd_partial_tc_kernel"                 # any group size
+        assert name(bf, bf, 128, 8, 32, rows=64) == "fd_partial_tc_kernel"
+        assert name(bf, bf, 128, 8, 8) is None
+        assert name(bf, bf, 64, 8) is None
+        assert name(f32, f32, 128, 8) is None
+        assert name(bf, f8, 128, 8) is None
         fd.set_path(fd.FD_PATH_SIMT)
         assert name(f32, f32, 128, 8) == "fd_partial_simt_kernel"
         assert name(bf, bf, 128, 8) == "fd_partial_simt_kernel"
@@ -196,7 +206,7 @@ def test_partial_kernel_name_follows_settings():
 def test_path_setting_round_trip():
     lib = fd.lib()
     try:
-        for path in (fd.FD_PATH_SIMT, fd.FD_PATH_MMA, fd.FD_PATH_AUTO):
+        for path in (fd.FD_PATH_SIMT, fd.FD_PATH_MMA, fd.FD_PATH_TCGEN05, fd.FD_PATH_AUTO):
             fd.set_path(path)
             assert fd.get_path() == path
         with pytest.raises(fd.FdError):
