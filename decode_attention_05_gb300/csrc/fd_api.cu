@@ -54,13 +54,13 @@ bool tc_takes(int32_t q_dtype, bool kv8, int64_t d, int32_t page_size, int64_t r
          rows >= 1 && rows <= fd::kMaxRows;
 }
 
-// Automatic choice: groups above kMaxNarrowRows rows go to the tcgen05 kernel where it
-// applies; otherwise the mma.sync path for bf16 and for f32 groups of up to
+// Automatic choice: groups of kTcAutoMinRows rows or more go to the tcgen05 kernel where
+// it applies; otherwise the mma.sync path for bf16 and for f32 groups of up to
 // kMaxF32MmaRows rows, and the CUDA-core path for larger f32 groups.
 int resolve_path(int32_t q_dtype, bool kv8, int64_t d, int32_t page_size, int64_t rows) {
   const int path = g_path.load();
   if (path != FD_PATH_AUTO) return path;
-  if (rows > fd::kMaxNarrowRows && tc_takes(q_dtype, kv8, d, page_size, rows))
+  if (rows >= fd::kTcAutoMinRows && tc_takes(q_dtype, kv8, d, page_size, rows))
     return FD_PATH_TCGEN05;
   return q_dtype == FD_BF16 || rows <= fd::kMaxF32MmaRows ? FD_PATH_MMA : FD_PATH_SIMT;
 }

@@ -110,6 +110,11 @@ fd_status record_error(fd_status st, const char* message);
 // up to kMaxRows (groups above kMaxNarrowRows run the wide tensor-core kernel only).
 constexpr int kMaxNarrowRows = 16;
 constexpr int kMaxRows = 64;
+// The automatic path sends groups of at least this many rows to the tcgen05 kernel
+// (where it applies); smaller wide groups stay on the mma.sync wide kernel, which is as
+// fast up to 32 rows (GQA 128K cache: 32 rows 132 us mma.sync vs 134 us tcgen05; 64 rows
+// 228 us vs 141 us).
+constexpr int kTcAutoMinRows = 33;
 // f32 inputs run on the tensor cores (3xTF32) for groups of up to this many rows.
 constexpr int kMaxF32MmaRows = 8;
 inline int rows_template(int n) {

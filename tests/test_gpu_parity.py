@@ -507,9 +507,11 @@ def test_multi_token_limits():
     (3, 16, 1, 64, False), (8, 8, 2, 64, True)])
 def test_wide_groups(Q, G, Hkv, d, paged, merge, mode):
     """17 to 64 query rows per kv head (multi-token decode on GQA groups, or groups of 32
-    and 64 heads): the wide kernel, each warp on its own rows over every token, against
-    the fp64 causal oracle; rows shorter than Q leave their first queries keyless."""
+    and 64 heads): the mma.sync wide kernel (FD_PATH_MMA; the tcgen05 kernel has its own
+    tests), each warp on its own rows over every token, against the fp64 causal oracle;
+    rows shorter than Q leave their first queries keyless."""
     fd.set_merge_mode(mode)
+    fd.set_path(fd.FD_PATH_MMA)
     Hq = Hkv * G
     lens = [1, max(Q - 1, 1), 70, 333, 1500, 2048]
     if paged:
