@@ -5,12 +5,12 @@
 //
 // Per tile of TT = 64 tokens of one kv head (the TMA tiles of fd_pipeline.cuh, used as
 // the mma operands in place):
-//   S[128, TT]  = Q[128, d] . K_tile^T          tcgen05.mma, M = 128 (query rows 0..R-1,
-//                                               the rest padding), N = TT, into TMEM
-//   one thread per query row reads its row of S from TMEM (tcgen05.ld), masks it, keeps
-//   the running max m and sum l, and writes P = bf16(2^(S - m)) to shared memory
-//   O[128, d]  += P[128, TT] . V_tile[TT, d]    tcgen05.mma, V read as an MN-major
-//                                               operand, O kept in TMEM
+//   S[128, TT]  = Q[128, d] . K_tile^T          tcgen05.mma, Q in TMEM, K the tile in
+//                                               shared memory, M = 128, N = TT, into TMEM
+//   one thread per TMEM lane reads its row of S (tcgen05.ld), masks it, keeps the
+//   running max m and sum l, and writes P = bf16(2^(S - m)) back to TMEM (tcgen05.st)
+//   O[128, d]  += P[128, TT] . V_tile[TT, d]    tcgen05.mma, P in TMEM, V read from the
+//                                               tile as an MN-major operand, O in TMEM
 // This is the FlashAttention block update of "AI Infra: math and infra optimisation in
 // large models", section 2.6, inside one split of Flash-Decoding (same section, Split-K):
 // S = Q K^T per KV block; rescale the running sum and output by exp(m_old - m_new); add
@@ -18,7 +18,7 @@
 // tile's max exceeds it by more than 8 in base-2 units: every 2^(S - m) then stays at
 // most 2^8, and since l and O use the same m throughout, the result is unchanged.
 //
-// Why: with R query rows per kv head each KV byte feeds R flops, and past 16 rows the
+// Why: with R query rows per kv head each KV byte feeds R flops, and past 32 rows the
 // mma.sync kernels become bound by issue latency and by every warp re-reading the tile
 // from shared memory.  Here one thread issues each tile's products as a few large
 // instructions that read the tile once, and the other warps only do the softmax.
@@ -31,8 +31,9 @@
 // takes the slice L / R of each tile's tokens (TT R / 128 of them), with its own running
 // max and sum (P is zero outside the slice).  The 2 x 128 / R partial states of a row
 // are merged at the end of the split, like the warps of the mma.sync kernel.  One CTA
-// per SM: 5 stages of K + V (160 KB), Q (32 KB), two P buffers (2 x 16 KB), 512 TMEM
-// columns (S 2 x 64, O 2 x 128).
+// per SM: 7 stages of K + V (224 KB) in shared memory; 512 TMEM columns: S 2 x 64,
+// O 2 x 128, Q 64 (128 dims as bf16 pairs), P 2 x 32.  With Q and P in TMEM, shared
+// memory carries only the K and V operands (each read once per tile).
 #include <cuda_bf16.h>
 
 #include "fd_epilogue.cuh"
@@ -42,19 +43,15 @@ namespace {
 
 constexpr int kTcD = 128;
 constexpr int kTcTT = 64;                    // tokens per tile (16 KB of K, 16 KB of V)
-constexpr int kTcStages = 5;
+constexpr int kTcStages = 7;
 constexpr int kTcThreads = 320;
 constexpr int kTcSoftThreads = 256;          // two groups of four warps
-constexpr uint32_t kTcCols = 512;            // TMEM columns: S 2 x 64, O 2 x 128
-constexpr uint32_t kTcOCol = 128;            // O of group g at kTcOCol + 128 g
-// Shared memory, from a 1024-byte aligned base: the ring, Q (two 64-dim slabs of 128
-// rows, K-major, 128-byte swizzled), two P buffers (128 rows x 64 tokens, K-major,
-// swizzled), the control block.
-constexpr uint32_t kTcQOff = kTcStages * 2 * kTileBytes;    // 160 KB
-constexpr uint32_t kTcSlab = 128 * 128;                     // one 64-dim slab of 128 rows
-constexpr uint32_t kTcPOff = kTcQOff + 2 * kTcSlab;
-constexpr uint32_t kTcPBytes = 128 * 128;
-constexpr uint32_t kTcCtlOff = kTcPOff + 2 * kTcPBytes;
+constexpr uint32_t kTcCols = 512;            // TMEM columns:
+constexpr uint32_t kTcOCol = 128;            //   S 0..127, O of group g at 128 + 128 g,
+constexpr uint32_t kTcQCol = 384;            //   Q (bf16 pairs along d),
+constexpr uint32_t kTcPCol = 448;            //   P of group g at 448 + 32 g (bf16 pairs)
+// Shared memory, from a 1024-byte aligned base: the ring, then the control block.
+constexpr uint32_t kTcCtlOff = kTcStages * 2 * kTileBytes;  // 224 KB
 
 struct TcCtl {
   PipeCtl<kTcStages> pipe;   // TMA ring (empty: released by the mma issuer's commit)
@@ -89,13 +86,13 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// D (TMEM) = A . B (+ D when accumulate != 0); A, B described in shared memory.
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
+// D (TMEM) = A . B (+ D), A in TMEM (lane = row, K packed two bf16 per column).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      :: "r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
 }
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -144,23 +141,41 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const float* v) {
          "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
       : "memory");
 }
+// Registers -> TMEM, 16 or 8 columns of packed words, complete before the statement ends.
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
+      "%10, %11, %12, %13, %14, %15, %16};\n\t"
+      "tcgen05.wait::st.sync.aligned;"
+      :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+         "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+         "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tc_st8(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n\t"
+      "tcgen05.wait::st.sync.aligned;"
+      :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Shared-memory operand descriptor, 128-byte swizzle: start address, leading and stride
 // byte offsets (16-byte units), descriptor version 1, layout 2 = SWIZZLE_128B.
-//   K-major operand (rows of 128 bytes = 64 bf16 along K): stride = 1024 (one 8-row
-//   swizzle atom to the next along M/N); the leading offset is not used.  A k-step of 16
-//   elements inside the atom advances the start address by 32 bytes.
+//   K-major operand (the K tile: rows of 128 bytes = 64 bf16 along K): stride = 1024
+//   (one 8-row swizzle atom to the next along N); the leading offset is not used.  A
+//   k-step of 16 elements inside the atom advances the start address by 32 bytes.
 //   MN-major operand (the V tile: a row is one token, 128 bytes = 64 dims along N):
 //   leading = bytes from one 64-dim slab to the next, stride = 1024 (8 tokens).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lead, uint32_t stride) {
   return (uint64_t)((addr >> 4) & 0x3fffu) | ((uint64_t)((lead >> 4) & 0x3fffu) << 16) |
          ((uint64_t)((stride >> 4) & 0x3fffu) << 32) | (1ull << 46) | (2ull << 61);
 }
-// Instruction descriptor of kind::f16: f32 accumulator, bf16 A and B, A K-major, B
-// K-major (b_mn = 0) or MN-major (1), N >> 3 and M >> 4.
+// Instruction descriptor of kind::f16: f32 accumulator, bf16 A and B, A K-major (here A
+// is always in TMEM), B K-major (b_mn = 0) or MN-major (1), N >> 3 and M >> 4.
 __host__ __device__ constexpr uint32_t instr_desc(int M, int N, int b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -169,11 +184,6 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, int b_mn) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-// Byte offset of 16-byte chunk c of row r in a K-major, 128-byte swizzled operand.
-__device__ __forceinline__ uint32_t kmajor_chunk(uint32_t r, uint32_t c) {
-  return (r >> 3) * 1024u + (r & 7u) * 128u + ((c ^ (r & 7u)) << 4);
 }
 
 // A bounded wait whose outcome every lane of the warp shares.
@@ -222,13 +232,12 @@ __device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity, uint32
 // P V product as soon as its P is in place.  The product of tile n never waits for a
 // later tile to land, so a stage is released as early as its own work allows.
 __device__ void issue_products(const Params& p, const SplitInfo& si, uint8_t* stages,
-                               uint8_t* qs, uint8_t* ps, TcCtl* ctl, uint32_t tmem) {
+                               TcCtl* ctl, uint32_t tmem) {
   const bool multi_page = p.block_table != nullptr && p.page_size < kTcTT;
   const int box = multi_page ? p.page_size : kTcTT;     // token rows of one TMA box
   const int nbox = kTcTT / box;
   const uint32_t box_bytes = 2u * (uint32_t)box * 128u;  // [line][row][128 B], 2 lines
   const uint32_t id_s = instr_desc(128, box, 0), id_pv = instr_desc(128, kTcD, 1);
-  const uint32_t qa = smem_addr(qs), pa = smem_addr(ps);
   const int N = si.n_tiles;
   auto s_ready = [&](int j) -> bool {
     return mbar_test(smem_addr(&ctl->pipe.full[j % kTcStages]), (j / kTcStages) & 1) &&
@@ -240,10 +249,9 @@ __device__ void issue_products(const Params& p, const SplitInfo& si, uint8_t* st
     for (int bx = 0; bx < nbox; ++bx) {
 #pragma unroll
       for (int ks = 0; ks < kTcD / 16; ++ks) {
-        const uint64_t a = smem_desc(qa + (ks >> 2) * kTcSlab + (ks & 3) * 32u, 0, 1024);
         const uint64_t b = smem_desc(kb + bx * box_bytes + (ks >> 2) * (uint32_t)box * 128u +
                                          (ks & 3) * 32u, 0, 1024);
-        tc_mma(tmem + (j & 1) * kTcTT + bx * box, a, b, id_s, ks > 0);
+        tc_mma_ts(tmem + (j & 1) * kTcTT + bx * box, tmem + kTcQCol + ks * 8, b, id_s, ks > 0);
       }
     }
     tc_commit(smem_addr(&ctl->s_full[j & 1]));
@@ -267,14 +275,14 @@ __device__ void issue_products(const Params& p, const SplitInfo& si, uint8_t* st
     tc_fence_after();
     const int st = n % kTcStages;
     const uint32_t vb = smem_addr(stages + (size_t)st * 2 * kTileBytes + kTileBytes);
-    const uint32_t pn = pa + (uint32_t)(n & 1) * kTcPBytes;
+    const uint32_t pt = tmem + kTcPCol + (uint32_t)(n & 1) * (kTcTT / 2);
 #pragma unroll
     for (int ks = 0; ks < kTcTT / 16; ++ks) {
       const int tok = ks * 16, bx = tok / box, rr = tok % box;
-      const uint64_t a = smem_desc(pn + ks * 32u, 0, 1024);
       const uint64_t b = smem_desc(vb + bx * box_bytes + (uint32_t)rr * 128u,
                                    (uint32_t)box * 128u, 1024);
-      tc_mma(tmem + kTcOCol + (uint32_t)(n & 1) * kTcD, a, b, id_pv, (n > 1 || ks > 0) ? 1u : 0u);
+      tc_mma_ts(tmem + kTcOCol + (uint32_t)(n & 1) * kTcD, pt + ks * 8, b, id_pv,
+                (n > 1 || ks > 0) ? 1u : 0u);
     }
     tc_commit(smem_addr(&ctl->pv_done[n & 1]));
     tc_commit(smem_addr(&ctl->pipe.empty[st]));
@@ -291,8 +299,7 @@ __device__ void issue_products(const Params& p, const SplitInfo& si, uint8_t* st
 // Returns false if a bounded wait gave up.
 template <int R>
 __device__ bool softmax_rows(const Params& p, const SplitInfo& si, uint8_t* stages,
-                             uint8_t* ps, TcCtl* ctl, uint32_t tmem, int t, float& m_out,
-                             float& l_out) {
+                             TcCtl* ctl, uint32_t tmem, int t, float& m_out, float& l_out) {
   constexpr int SLICE = kTcTT * R / 128;             // tokens of a tile per lane: 32 or 16
   const int grp = t >> 7, tg = t & 127;
   const int warp = tg >> 5, lane = t & 31;
@@ -303,8 +310,8 @@ __device__ bool softmax_rows(const Params& p, const SplitInfo& si, uint8_t* stag
   const uint32_t lb = (uint32_t)p.log2_box;
   const float sl2 = p.scale_log2;
   const int j0 = slice * SLICE;                      // first token of the slice in a tile
-  const uint32_t prow = (uint32_t)(tg >> 3) * 1024u + (uint32_t)(tg & 7) * 128u;
   const uint32_t ocol = kTcOCol + (uint32_t)grp * kTcD;
+  const uint32_t pcol = kTcPCol + (uint32_t)grp * (kTcTT / 2) + (uint32_t)(j0 / 2);
   float m = kNegInf, l = 0.f;
   for (int n = grp; n < si.n_tiles; n += 2) {
     const int st = n % kTcStages;
@@ -370,14 +377,10 @@ __device__ bool softmax_rows(const Params& p, const SplitInfo& si, uint8_t* stag
         tc_st32(tl + ocol + q * 32, o);
       }
     }
-    // This lane's slice of its P row (the rest of the row stays zero).
-    uint8_t* pr = ps + (n & 1) * kTcPBytes + prow;
-#pragma unroll
-    for (int cc = 0; cc < SLICE / 8; ++cc) {
-      const uint32_t chunk = (uint32_t)(j0 / 8 + cc);
-      *reinterpret_cast<uint4*>(pr + ((chunk ^ (uint32_t)(tg & 7)) << 4)) =
-          make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-    }
+    // This lane's slice of its P row, into the group's P columns in TMEM (the rest of
+    // the row stays zero).
+    if constexpr (SLICE == 32) tc_st16(tl + pcol, pk);
+    else tc_st8(tl + pcol, pk);
     // Boundary tile: the V rows of tokens outside [lo, hi) or on an invalid page may hold
     // stale values (NaN), and 0 * NaN would poison the product: zero them.
     if (!clean && tg < kTcTT) {
@@ -418,8 +421,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* stages = base;
-  uint8_t* qs = base + kTcQOff;
-  uint8_t* ps = base + kTcPOff;
   auto* ctl = reinterpret_cast<TcCtl*>(base + kTcCtlOff);
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   if (si.n_tiles == 0) {            // empty split: weight 0 in the merge, nothing to load
@@ -448,29 +449,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_alloc(smem_addr(&ctl->tmem), kTcCols);
     tc_relinquish();
   }
-  if (warp < 8) {
-    // Q rows -> K-major swizzled slabs, row L holding query row L mod R (rows past the
-    // group are zero); both P buffers start zero (each lane later writes only its slice).
-    for (int i = t; i < 128 * (kTcD / 2); i += kTcSoftThreads) {
-      const int row = i / (kTcD / 2), w = i % (kTcD / 2);   // word w: dims 2w, 2w + 1
-      const int h = row % R;
-      uint32_t v = 0u;
-      if (h < p.n_rows)
-        v = reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                                              q_offset(p, si.b, si.g, h))[w];
-      const int dim = 2 * w;
-      *reinterpret_cast<uint32_t*>(qs + (dim >> 6) * kTcSlab +
-                                   kmajor_chunk((uint32_t)row, (uint32_t)((dim & 63) >> 3)) +
-                                   (dim & 7) * 2) = v;
-    }
-    for (int i = t; i < (int)(2 * kTcPBytes / 16); i += kTcSoftThreads)
-      reinterpret_cast<uint4*>(ps)[i] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
+  if (warp < 8) {
+    // Lane L = t mod 128 of TMEM: group 0 writes its Q row (query row L mod R, as bf16
+    // pairs along d; rows past the group are zero), each group zeroes its P columns
+    // (each lane later writes only its slice of them).
+    const int L = t & 127;
+    const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    uint32_t v[32];
+    if (t < 128) {
+      const int h = L % R;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          reinterpret_cast<const __nv_bfloat16*>(p.q) +
+          q_offset(p, si.b, si.g, h < p.n_rows ? h : 0));
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v[c] = h < p.n_rows ? qrow[half * 32 + c] : 0u;
+        tc_st32(tl + kTcQCol + half * 32, reinterpret_cast<const float*>(v));
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 32; ++c) v[c] = 0u;
+    tc_st32(tl + kTcPCol + (uint32_t)(t >> 7) * (kTcTT / 2), reinterpret_cast<const float*>(v));
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   float m = kNegInf, l = 0.f;
   if (warp == 8) {                  // ---------------- TMA producer
@@ -478,10 +486,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefetch_tensormap(&tv);
     produce_tiles<kTcTT, kTcStages>(p, si, &tk, &tv, stages, &ctl->pipe, lane);
   } else if (warp == 9) {           // ---------------- mma issuer
-    if (lane == 0) issue_products(p, si, stages, qs, ps, ctl, tmem);
+    if (lane == 0) issue_products(p, si, stages, ctl, tmem);
     __syncwarp();
   } else {                          // ---------------- softmax
-    if (!softmax_rows<R>(p, si, stages, ps, ctl, tmem, t, m, l) && lane == 0) set_abort(p, ctl);
+    if (!softmax_rows<R>(p, si, stages, ctl, tmem, t, m, l) && lane == 0) set_abort(p, ctl);
   }
   pdl_trigger();
   tc_fence_before();
