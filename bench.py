@@ -68,6 +68,9 @@ def parse_args():
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="KV cache storage: the workload's own, or FP8 E4M3 codes with "
                          "per-kv-head scales (decode over the quantised cache)")
+    ap.add_argument("--query-tokens", type=int, default=1,
+                    help="Q > 1: multi-token decode (speculative verification) of Q query "
+                         "tokens per row over the same cache, causal inside the split")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue every timed call from Python instead of replaying CUDA graphs")
     return ap.parse_args()
@@ -212,14 +215,25 @@ def fp8_variant(w):
     return w8, ks, vs
 
 
+def with_query_tokens(w, Q: int):
+    """The workload with Q query tokens per row (multi-token decode): q [B, Q, Hq, d]
+    drawn from its own seed; the cache is unchanged."""
+    if Q <= 1:
+        return w
+    q4 = workloads.multi_token_queries(w.B, Q, w.Hq, w.d, seed=4242, dtype=w.q.dtype)
+    return dataclasses.replace(w, q=q4, name="%s, %d query tokens" % (w.name, Q))
+
+
 def oracle_decoder(w, scales=None):
     """(decode(seq_lens, rows), seq_lens) running the oracle on the workload's stored
-    values: the bf16/f32 decode, or the FP8 one when scales are given."""
+    values: the bf16/f32 decode (causal for multi-token queries), or the FP8 one when
+    scales are given."""
     import oracle
     if scales is None:
         q, k, v, lens, bt, ps = w.oracle_arrays()
-        return (lambda seq, rows=None: oracle.decode(q, k, v, seq, block_table=bt,
-                                                      page_size=ps, rows=rows)), lens
+        fn = oracle.decode_causal if w.Q > 1 else oracle.decode
+        return (lambda seq, rows=None: fn(q, k, v, seq, block_table=bt, page_size=ps,
+                                          rows=rows)), lens
     q = workloads.np_storage(w.q)
     kc = w.k.view(torch.uint8).numpy()
     vc = w.v.view(torch.uint8).numpy()
@@ -244,7 +258,7 @@ def oracle_sample(w, budget_s: float, scales=None):
     import oracle
     run, lens = oracle_decoder(w, scales)
     threads = oracle.max_threads()
-    n_rows = w.B * w.Hq
+    n_rows = w.B * w.Q * w.Hq
     L = int(lens.max())
     uniform = int(lens.min()) == L
 
@@ -294,7 +308,7 @@ def run_reference(args):
     world, rank, _ = dist_info()
     if rank != 0:
         return 0
-    w = workloads.CONFIGS[args.config]()
+    w = with_query_tokens(workloads.CONFIGS[args.config](), args.query_tokens)
     scales = None
     if args.kv == "fp8":
         w, ks, vs = fp8_variant(w)
@@ -302,7 +316,7 @@ def run_reference(args):
     import oracle
     run, lens = oracle_decoder(w, scales)
     threads = oracle.max_threads()
-    B, Hq = w.B, w.Hq
+    B, Hq = w.B, w.Q * w.Hq                      # query rows: B x Q x Hq
     rows = list(range(0, B * Hq, max(1, (B * Hq) // threads)))[:threads]
     L = int(lens.max())
     # Size each step so that warm-up + timed steps end within ~90 s.
@@ -354,22 +368,32 @@ def run_fd(args):
     fd.set_path({"auto": fd.FD_PATH_AUTO, "simt": fd.FD_PATH_SIMT, "mma": fd.FD_PATH_MMA,
                  "tcgen05": fd.FD_PATH_TCGEN05}[args.path])
 
-    w_cpu = workloads.CONFIGS[args.config]()
+    w_cpu = with_query_tokens(workloads.CONFIGS[args.config](), args.query_tokens)
     scales_cpu = None
     if args.kv == "fp8":
+        if w_cpu.Q > 1:
+            raise SystemExit("--kv fp8 takes single-token decode only")
         w_cpu, ks, vs = fp8_variant(w_cpu)
         scales_cpu = (ks, vs)
     w = w_cpu.to("cuda")
     scales = None if scales_cpu is None else tuple(t.cuda() for t in scales_cpu)
-    B, Hq, d, Hkv = w.B, w.Hq, w.d, w.Hkv
+    B, Hq, d, Hkv, Qt = w.B, w.Hq, w.d, w.Hkv, w.Q
+    rows = Qt * (Hq // Hkv)                           # query rows per (b, kv head)
+    kernel = fd.partial_kernel_name(w.q.dtype, w.k.dtype, d, Hkv, w.page_size, rows=rows)
     S = args.num_splits or w.num_splits
     if S == 0:          # the lengths are known here: plan with them
         sms = torch.cuda.get_device_properties(local).multi_processor_count
-        S = fd.num_splits_for_lengths(B, Hq, Hkv, d, w.L_cap, w_cpu.seq_lens, sms,
-                                      page_size=w.page_size)
-    ws = torch.zeros(fd.workspace_size(B, Hq, Hkv, d, S), dtype=torch.uint8, device="cuda")
-    out = torch.empty((B, Hq, d), dtype=w.out_dtype, device="cuda")
-    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+        # The planner models the single-token kernels (two CTAs per SM, bound by HBM).  The
+        # kernels of wide groups are bound by their tile math and do best with one CTA's
+        # worth of splits per SM (the tcgen05 kernel holds one CTA per SM; the mma.sync
+        # wide kernel measured 132 us at 19 splits against 156 us at 32 on the 128K cache).
+        wide = kernel in ("fd_partial_tc_kernel", "fd_partial_wide_kernel")
+        S = fd.num_splits_for_lengths(B, Hq, Hkv, d, w.L_cap, w_cpu.seq_lens,
+                                      sms // 2 if wide else sms, page_size=w.page_size)
+    ws = torch.zeros(fd.workspace_size(B, Qt * Hq, Hkv, d, S), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty(tuple(w.q.shape), dtype=w.out_dtype, device="cuda")
+    lse = torch.empty(tuple(w.q.shape[:-1]), dtype=torch.float32, device="cuda")
     dq, dk, dv, dbt, do = (tensor_desc(w.q), tensor_desc(w.k), tensor_desc(w.v),
                            tensor_desc(w.block_table), tensor_desc(out))
     bt_ref = None if dbt is None else ctypes.byref(dbt)
@@ -487,9 +511,9 @@ def run_fd(args):
     e3.record(stream)
     e3.synchronize()
     partial_ms = e2.elapsed_time(e3) / args.steps
-    lse_part, o_part = fd.workspace_partials(ws, B, Hq, d, S)
-    dout = tensor_desc(out)
-    merge_call = lambda s: checked(L.fd_merge_partials(B, Hq, d, S, lse_part.data_ptr(),
+    lse_part, o_part = fd.workspace_partials(ws, B * Qt, Hq, d, S)
+    dout = tensor_desc(out.view(B * Qt, Hq, d))
+    merge_call = lambda s: checked(L.fd_merge_partials(B * Qt, Hq, d, S, lse_part.data_ptr(),
                                                        o_part.data_ptr(), ctypes.byref(dout),
                                                        lse.data_ptr(), s))
     merge_graph = make_graph(merge_call, GRAPH_CHUNK)
@@ -502,8 +526,6 @@ def run_fd(args):
     merge_ms = e4.elapsed_time(e5) / args.steps
     peak, peak_src = measured_peak()
     achieved = kv_bytes / (partial_ms * 1e-3) / 1e9
-    kernel = fd.partial_kernel_name(w.q.dtype, w.k.dtype, d, w.Hkv, w.page_size,
-                                    rows=Hq // Hkv)
     path_name = {"fd_partial_simt_kernel": "simt", "fd_partial_tc_kernel": "tcgen05"}.get(kernel, "mma")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kernel, w.name),
@@ -569,6 +591,7 @@ def run_fd(args):
                      ("+e4m3 KV" if scales is not None else ""),
             "data": "synthetic",
             "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d,
+                       "query_tokens": Qt,
                        "L": int(w.seq_lens.max()), "num_splits": S, "path": path_name,
                        "kv_bytes_per_step": kv_bytes,
                        "l2": ("inputs larger than L2 (KV %d MiB vs 126 MiB L2), no flush" %

@@ -36,7 +36,7 @@ import torch
 @dataclasses.dataclass
 class Workload:
     name: str
-    q: torch.Tensor                     # [B, Hq, d] storage dtype, CPU
+    q: torch.Tensor                     # [B, Hq, d] (or [B, Q, Hq, d]: Q query tokens) CPU
     k: torch.Tensor                     # contiguous [B, Hkv, L_cap, d] | paged [P, Hkv, ps, d]
     v: torch.Tensor
     seq_lens: torch.Tensor              # int32 [B]
@@ -52,11 +52,16 @@ class Workload:
 
     @property
     def Hq(self) -> int:
-        return self.q.shape[1]
+        return self.q.shape[-2]
 
     @property
     def d(self) -> int:
-        return self.q.shape[2]
+        return self.q.shape[-1]
+
+    @property
+    def Q(self) -> int:
+        """Query tokens per row (multi-token decode), 1 for single-token decode."""
+        return self.q.shape[1] if self.q.dim() == 4 else 1
 
     @property
     def Hkv(self) -> int:
