@@ -111,10 +111,10 @@ fd_status record_error(fd_status st, const char* message);
 constexpr int kMaxNarrowRows = 16;
 constexpr int kMaxRows = 64;
 // The automatic path sends groups of at least this many rows to the tcgen05 kernel
-// (where it applies); smaller wide groups stay on the mma.sync wide kernel, which is as
-// fast up to 32 rows (GQA 128K cache: 32 rows 132 us mma.sync vs 134 us tcgen05; 64 rows
-// 228 us vs 141 us).
-constexpr int kTcAutoMinRows = 33;
+// (where it applies).  GQA 128K cache, one CTA's worth of splits per SM: 32 rows 91 us
+// (tcgen05) vs 132 us (mma.sync wide kernel), 64 rows 93 us vs 228 us; up to 16 rows the
+// mma.sync kernels stay at the HBM rate (79-82 us).
+constexpr int kTcAutoMinRows = 17;
 // f32 inputs run on the tensor cores (3xTF32) for groups of up to this many rows.
 constexpr int kMaxF32MmaRows = 8;
 inline int rows_template(int n) {

@@ -23,8 +23,8 @@
 // from shared memory.  Here one thread issues each tile's products as a few large
 // instructions that read the tile once, and the other warps only do the softmax.
 //
-// Warps: 0-7 softmax in two groups of four, 8 the TMA producer, 9 the mma issuer (one
-// thread).  Group g takes the tiles n = g mod 2 with its own S buffer, P buffer and O
+// Warps: 0-7 softmax in two groups of four, 8 the TMA producer, 9 and 10 the issuers of
+// the score and output products (one thread each).  Group g takes the tiles n = g mod 2 with its own S buffer, P buffer and O
 // accumulator, so the two groups' per-tile handoffs (scores ready, P written, product
 // done) overlap.  The 128 rows of the products are the R query rows repeated 128 / R
 // times (Q is stored that way): TMEM lane L holds query row L mod R, and its thread
@@ -44,7 +44,7 @@ namespace {
 constexpr int kTcD = 128;
 constexpr int kTcTT = 64;                    // tokens per tile (16 KB of K, 16 KB of V)
 constexpr int kTcStages = 7;
-constexpr int kTcThreads = 320;
+constexpr int kTcThreads = 352;
 constexpr int kTcSoftThreads = 256;          // two groups of four warps
 constexpr uint32_t kTcCols = 512;            // TMEM columns:
 constexpr uint32_t kTcOCol = 128;            //   S 0..127, O of group g at 128 + 128 g,
@@ -62,7 +62,7 @@ struct TcCtl {
                              // the issuer has seen tile n, and a parity wait must never
                              // be two phases behind its barrier)
   uint64_t pv_done[2];       // the P V product reading P buffer b has completed
-  uint64_t mma_done;         // every product this CTA issued has completed
+  uint64_t mma_done;         // every product this CTA issued has completed (both issuers)
   uint32_t tmem;             // TMEM base address (tcgen05.alloc)
 };
 constexpr size_t kTcSmemBytes = 1024 + kTcCtlOff + ((sizeof(TcCtl) + 127) / 128) * 128;
@@ -202,18 +202,6 @@ __device__ __forceinline__ bool aborted(TcCtl* ctl) {
 }
 
 // ---------------------------------------------------------------- mma issuer
-// Non-blocking probe of an mbarrier phase.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 // Probe that may suspend the thread for up to `hint_ns` while the phase is incomplete.
 __device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
@@ -227,23 +215,36 @@ __device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity, uint32
   return ok != 0;
 }
 
-// One thread, event-driven: it issues each tile's scores S(j) = Q K(j)^T as soon as the
-// tile has landed and its S buffer is free (up to two tiles ahead), and each tile's
-// P V product as soon as its P is in place.  The product of tile n never waits for a
-// later tile to land, so a stage is released as early as its own work allows.
-__device__ void issue_products(const Params& p, const SplitInfo& si, uint8_t* stages,
-                               TcCtl* ctl, uint32_t tmem) {
+// A bounded wait that also gives up as soon as another role has aborted the split.
+__device__ __forceinline__ bool wait_or_abort(TcCtl* ctl, uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_probe(bar, parity, 200u)) {
+    if (aborted(ctl) || global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// The products are issued by two threads in two warps, each in tile order: one issues
+// the scores S(j) = Q K(j)^T as soon as tile j has landed and its S buffer has been read
+// (the softmax of tile j - 2), the other the products P(n) V(n) as soon as P(n) is in
+// place.  They write disjoint TMEM columns and read different operands, so neither
+// waits for the other's instruction stream; a stage is released by the second's commit
+// after P(n) V(n), which implies S(n) has completed (the softmax read it before writing
+// P(n)).  Each thread finishes by waiting for all of its products.
+__device__ void issue_scores(const Params& p, const SplitInfo& si, uint8_t* stages,
+                             TcCtl* ctl, uint32_t tmem) {
   const bool multi_page = p.block_table != nullptr && p.page_size < kTcTT;
   const int box = multi_page ? p.page_size : kTcTT;     // token rows of one TMA box
   const int nbox = kTcTT / box;
   const uint32_t box_bytes = 2u * (uint32_t)box * 128u;  // [line][row][128 B], 2 lines
-  const uint32_t id_s = instr_desc(128, box, 0), id_pv = instr_desc(128, kTcD, 1);
-  const int N = si.n_tiles;
-  auto s_ready = [&](int j) -> bool {
-    return mbar_test(smem_addr(&ctl->pipe.full[j % kTcStages]), (j / kTcStages) & 1) &&
-           (j < 2 || mbar_test(smem_addr(&ctl->s_free[j & 1]), ((j >> 1) - 1) & 1));
-  };
-  auto issue_s = [&](int j) {
+  const uint32_t id_s = instr_desc(128, box, 0);
+  bool ok = true;
+  for (int j = 0; j < si.n_tiles; ++j) {
+    if (!wait_or_abort(ctl, smem_addr(&ctl->pipe.full[j % kTcStages]), (j / kTcStages) & 1) ||
+        (j >= 2 && !wait_or_abort(ctl, smem_addr(&ctl->s_free[j & 1]), ((j >> 1) - 1) & 1))) {
+      ok = false;
+      break;
+    }
     tc_fence_after();
     const uint32_t kb = smem_addr(stages + (size_t)(j % kTcStages) * 2 * kTileBytes);
     for (int bx = 0; bx < nbox; ++bx) {
@@ -255,23 +256,24 @@ __device__ void issue_products(const Params& p, const SplitInfo& si, uint8_t* st
       }
     }
     tc_commit(smem_addr(&ctl->s_full[j & 1]));
-  };
+  }
+  if (!ok) set_abort(p, ctl);
+  tc_commit(smem_addr(&ctl->mma_done));      // never leave with products in flight
+  if (!mbar_wait(smem_addr(&ctl->mma_done), 0)) atomicOr(p.flags, kDevFlagTimeout);
+}
+
+__device__ void issue_outputs(const Params& p, const SplitInfo& si, uint8_t* stages,
+                              TcCtl* ctl, uint32_t tmem) {
+  const bool multi_page = p.block_table != nullptr && p.page_size < kTcTT;
+  const int box = multi_page ? p.page_size : kTcTT;
+  const uint32_t box_bytes = 2u * (uint32_t)box * 128u;
+  const uint32_t id_pv = instr_desc(128, kTcD, 1);
   bool ok = true;
-  int ns = 0;                                  // next tile whose scores are to be issued
-  for (int n = 0; ok && n < N; ++n) {
-    const uint64_t t0 = global_ns();
-    for (;;) {
-      if (ns < N && ns <= n + 2 && s_ready(ns)) {
-        issue_s(ns++);
-        continue;
-      }
-      if (ns > n && mbar_probe(smem_addr(&ctl->p_full[n & 1]), (n >> 1) & 1, 200u)) break;
-      if (aborted(ctl) || global_ns() - t0 > kWaitLimitNs) {
-        ok = false;
-        break;
-      }
+  for (int n = 0; n < si.n_tiles; ++n) {
+    if (!wait_or_abort(ctl, smem_addr(&ctl->p_full[n & 1]), (n >> 1) & 1)) {
+      ok = false;
+      break;
     }
-    if (!ok) break;
     tc_fence_after();
     const int st = n % kTcStages;
     const uint32_t vb = smem_addr(stages + (size_t)st * 2 * kTileBytes + kTileBytes);
@@ -288,7 +290,6 @@ __device__ void issue_products(const Params& p, const SplitInfo& si, uint8_t* st
     tc_commit(smem_addr(&ctl->pipe.empty[st]));
   }
   if (!ok) set_abort(p, ctl);
-  // Never leave (or free TMEM) with products in flight.
   tc_commit(smem_addr(&ctl->mma_done));
   if (!mbar_wait(smem_addr(&ctl->mma_done), 0)) atomicOr(p.flags, kDevFlagTimeout);
 }
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(smem_addr(&ctl->pv_done[b]), 1);
       mbar_init(smem_addr(&ctl->p_full[b]), 4);     // the four warps of group b
     }
-    mbar_init(smem_addr(&ctl->mma_done), 1);
+    mbar_init(smem_addr(&ctl->mma_done), 2);
     ctl->pipe.abort = 0;
     fence_mbar_init();
   }
@@ -485,8 +486,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefetch_tensormap(&tk);
     prefetch_tensormap(&tv);
     produce_tiles<kTcTT, kTcStages>(p, si, &tk, &tv, stages, &ctl->pipe, lane);
-  } else if (warp == 9) {           // ---------------- mma issuer
-    if (lane == 0) issue_products(p, si, stages, ctl, tmem);
+  } else if (warp == 9) {           // ---------------- score products
+    if (lane == 0) issue_scores(p, si, stages, ctl, tmem);
+    __syncwarp();
+  } else if (warp == 10) {          // ---------------- output products
+    if (lane == 0) issue_outputs(p, si, stages, ctl, tmem);
     __syncwarp();
   } else {                          // ---------------- softmax
     if (!softmax_rows<R>(p, si, stages, ctl, tmem, t, m, l) && lane == 0) set_abort(p, ctl);

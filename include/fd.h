@@ -88,7 +88,7 @@ typedef struct {
 /* Kernel path selection for the partial pass (process-wide setting). */
 typedef enum {
   FD_PATH_AUTO = 0,    /* the fastest kernel for the call: FD_PATH_TCGEN05 for bf16 groups
-                          of 33 to 64 query rows per kv head that it takes, FD_PATH_MMA
+                          of 17 to 64 query rows per kv head that it takes, FD_PATH_MMA
                           for other bf16 groups and f32 groups of up to 8 rows, CUDA
                           cores otherwise                                                */
   FD_PATH_SIMT = 1,    /* CUDA-core dot products for every dtype                         */

@@ -167,8 +167,9 @@ def test_partial_kernel_name_follows_settings():
         assert name(f32, f32, 64, 8, 16, rows=4) == "fd_partial_mma_kernel"    # grid only
         assert name(f32, f32, 128, 8, rows=16) == "fd_partial_simt_kernel"     # > 8 rows
         assert name(f32, f8, 128, 8) is None
-        assert name(bf, bf, 128, 8, rows=32) == "fd_partial_wide_kernel"      # Q x G > 16
-        assert name(bf, bf, 128, 8, rows=33) == "fd_partial_tc_kernel"        # Q x G > 32
+        assert name(bf, bf, 128, 8, rows=16) == "fd_partial_mma_kernel"       # Q x G <= 16
+        assert name(bf, bf, 128, 8, rows=17) == "fd_partial_tc_kernel"        # Q x G > 16
+        assert name(bf, bf, 128, 8, rows=32) == "fd_partial_tc_kernel"
         assert name(bf, bf, 128, 8, 16, rows=64) == "fd_partial_tc_kernel"
         assert name(bf, bf, 128, 8, 8, rows=64) == "fd_partial_wide_kernel"   # 8-token pages
         assert name(bf, bf, 64, 8, rows=32) == "fd_partial_wide_kernel"       # d = 64

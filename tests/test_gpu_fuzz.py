@@ -54,9 +54,10 @@ def draw(i, medium=False):
     merge = r.choice([fd.FD_MERGE_KERNEL, fd.FD_MERGE_KERNEL, fd.FD_MERGE_IN_KERNEL])
     if f32:     # the tensor-core path takes up to 8 f32 rows
         path = fd.FD_PATH_MMA if Q * G <= 8 and r.random() < 0.7 else fd.FD_PATH_SIMT
-    else:
-        path = fd.FD_PATH_SIMT if (not fp8 and Q * G <= 16 and r.random() < 0.2) \
-            else fd.FD_PATH_MMA
+    elif not fp8 and Q * G <= 16 and r.random() < 0.2:
+        path = fd.FD_PATH_SIMT
+    else:       # AUTO runs the tcgen05 kernel for bf16 groups above 16 rows at d = 128
+        path = fd.FD_PATH_AUTO if r.random() < 0.5 else fd.FD_PATH_MMA
     return dict(d=d, fp8=fp8, f32=f32, Q=Q, G=G, Hkv=Hkv, B=B, ps=ps, cap=cap, lens=lens, S=S,
                 sched=sched, merge=merge, path=path)
 

@@ -57,8 +57,8 @@ def decode(w, q4, S):
     (3, 8, 2, 0), (4, 8, 2, 0), (8, 8, 1, 0), (2, 16, 2, 16), (4, 16, 1, 32), (1, 32, 2, 0),
     (1, 64, 1, 64), (5, 4, 2, 128), (3, 16, 1, 0), (8, 8, 2, 16), (6, 4, 2, 0)])
 def test_tc_wide_groups(Q, G, Hkv, ps, merge):
-    """17 to 64 rows per kv head (the automatic choice from 33 rows): ragged rows, rows
-    shorter than Q (keyless queries), NaN tails, tile and page boundaries, several split
+    """17 to 64 rows per kv head (the automatic choice there): ragged rows, rows shorter
+    than Q (keyless queries), NaN tails, tile and page boundaries, several split
     counts."""
     fd.set_merge_mode(merge)
     fd.set_path(fd.FD_PATH_TCGEN05)
