@@ -24,14 +24,15 @@
 // instructions that read the tile once, and the other warps only do the softmax.
 //
 // Warps: 0-7 softmax in two groups of four, 8 the TMA producer, 9 and 10 the issuers of
-// the score and output products (one thread each).  Group g takes the tiles n = g mod 2 with its own S buffer, P buffer and O
+// the even and odd tiles' score products, 11 the issuer of the output products (one
+// thread each).  Group g takes the tiles n = g mod 2 with its own S buffer, P buffer and O
 // accumulator, so the two groups' per-tile handoffs (scores ready, P written, product
 // done) overlap.  The 128 rows of the products are the R query rows repeated 128 / R
 // times (Q is stored that way): TMEM lane L holds query row L mod R, and its thread
 // takes the slice L / R of each tile's tokens (TT R / 128 of them), with its own running
 // max and sum (P is zero outside the slice).  The 2 x 128 / R partial states of a row
 // are merged at the end of the split, like the warps of the mma.sync kernel.  One CTA
-// per SM: 7 stages of K + V (224 KB) in shared memory; 512 TMEM columns: S 2 x 64,
+// per SM: 6 stages of K + V (192 KB) in shared memory; 512 TMEM columns: S 2 x 64,
 // O 2 x 128, Q 64 (128 dims as bf16 pairs), P 2 x 32.  With Q and P in TMEM, shared
 // memory carries only the K and V operands (each read once per tile).
 #include <cuda_bf16.h>
@@ -43,15 +44,19 @@ namespace {
 
 constexpr int kTcD = 128;
 constexpr int kTcTT = 64;                    // tokens per tile (16 KB of K, 16 KB of V)
-constexpr int kTcStages = 7;
-constexpr int kTcThreads = 352;
+// An even number of stages: stage st then only ever holds tiles of parity st % 2, so the
+// roles that take one parity of tiles (a softmax group, a score issuer) see every phase
+// of the stage's barrier -- a parity wait is only exact for a waiter that never skips one.
+constexpr int kTcStages = 6;
+static_assert(kTcStages % 2 == 0, "stages hold tiles of one parity");
+constexpr int kTcThreads = 384;
 constexpr int kTcSoftThreads = 256;          // two groups of four warps
 constexpr uint32_t kTcCols = 512;            // TMEM columns:
 constexpr uint32_t kTcOCol = 128;            //   S 0..127, O of group g at 128 + 128 g,
 constexpr uint32_t kTcQCol = 384;            //   Q (bf16 pairs along d),
 constexpr uint32_t kTcPCol = 448;            //   P of group g at 448 + 32 g (bf16 pairs)
 // Shared memory, from a 1024-byte aligned base: the ring, then the control block.
-constexpr uint32_t kTcCtlOff = kTcStages * 2 * kTileBytes;  // 224 KB
+constexpr uint32_t kTcCtlOff = kTcStages * 2 * kTileBytes;  // 192 KB
 
 struct TcCtl {
   PipeCtl<kTcStages> pipe;   // TMA ring (empty: released by the mma issuer's commit)
@@ -62,7 +67,7 @@ struct TcCtl {
                              // the issuer has seen tile n, and a parity wait must never
                              // be two phases behind its barrier)
   uint64_t pv_done[2];       // the P V product reading P buffer b has completed
-  uint64_t mma_done;         // every product this CTA issued has completed (both issuers)
+  uint64_t mma_done;         // every product this CTA issued has completed (three issuers)
   uint32_t tmem;             // TMEM base address (tcgen05.alloc)
 };
 constexpr size_t kTcSmemBytes = 1024 + kTcCtlOff + ((sizeof(TcCtl) + 127) / 128) * 128;
@@ -224,22 +229,23 @@ __device__ __forceinline__ bool wait_or_abort(TcCtl* ctl, uint32_t bar, uint32_t
   return true;
 }
 
-// The products are issued by two threads in two warps, each in tile order: one issues
-// the scores S(j) = Q K(j)^T as soon as tile j has landed and its S buffer has been read
-// (the softmax of tile j - 2), the other the products P(n) V(n) as soon as P(n) is in
-// place.  They write disjoint TMEM columns and read different operands, so neither
-// waits for the other's instruction stream; a stage is released by the second's commit
-// after P(n) V(n), which implies S(n) has completed (the softmax read it before writing
-// P(n)).  Each thread finishes by waiting for all of its products.
+// The products are issued by three threads in three warps: two issue the scores
+// S(j) = Q K(j)^T of the even and of the odd tiles, each as soon as tile j has landed
+// and its S buffer has been read (the softmax of tile j - 2); the third issues the
+// products P(n) V(n) of all tiles in order, each as soon as P(n) is in place.  They
+// write disjoint TMEM columns and read different operands, so none waits for another's
+// instruction stream; a stage is released by the third's commit after P(n) V(n), which
+// implies S(n) has completed (the softmax read it before writing P(n)).  Each thread
+// finishes by waiting for all of its products.
 __device__ void issue_scores(const Params& p, const SplitInfo& si, uint8_t* stages,
-                             TcCtl* ctl, uint32_t tmem) {
+                             TcCtl* ctl, uint32_t tmem, int parity) {
   const bool multi_page = p.block_table != nullptr && p.page_size < kTcTT;
   const int box = multi_page ? p.page_size : kTcTT;     // token rows of one TMA box
   const int nbox = kTcTT / box;
   const uint32_t box_bytes = 2u * (uint32_t)box * 128u;  // [line][row][128 B], 2 lines
   const uint32_t id_s = instr_desc(128, box, 0);
   bool ok = true;
-  for (int j = 0; j < si.n_tiles; ++j) {
+  for (int j = parity; j < si.n_tiles; j += 2) {
     if (!wait_or_abort(ctl, smem_addr(&ctl->pipe.full[j % kTcStages]), (j / kTcStages) & 1) ||
         (j >= 2 && !wait_or_abort(ctl, smem_addr(&ctl->s_free[j & 1]), ((j >> 1) - 1) & 1))) {
       ok = false;
@@ -442,7 +448,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(smem_addr(&ctl->pv_done[b]), 1);
       mbar_init(smem_addr(&ctl->p_full[b]), 4);     // the four warps of group b
     }
-    mbar_init(smem_addr(&ctl->mma_done), 2);
+    mbar_init(smem_addr(&ctl->mma_done), 3);
     ctl->pipe.abort = 0;
     fence_mbar_init();
   }
@@ -486,10 +492,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefetch_tensormap(&tk);
     prefetch_tensormap(&tv);
     produce_tiles<kTcTT, kTcStages>(p, si, &tk, &tv, stages, &ctl->pipe, lane);
-  } else if (warp == 9) {           // ---------------- score products
-    if (lane == 0) issue_scores(p, si, stages, ctl, tmem);
+  } else if (warp == 9 || warp == 10) {   // ---------- score products, even / odd tiles
+    if (lane == 0) issue_scores(p, si, stages, ctl, tmem, warp - 9);
     __syncwarp();
-  } else if (warp == 10) {          // ---------------- output products
+  } else if (warp == 11) {          // ---------------- output products
     if (lane == 0) issue_outputs(p, si, stages, ctl, tmem);
     __syncwarp();
   } else {                          // ---------------- softmax
