@@ -84,6 +84,8 @@ def _declare(L):
     L.fd_num_splits_for_lengths.argtypes = [i32, i32, i32, i32, i64, vp, i32, i32]
     L.fd_resolve_num_splits.restype = i32
     L.fd_resolve_num_splits.argtypes = [i32, i32, i32, i32, i64, i32]
+    L.fd_resolve_num_splits_q.restype = i32
+    L.fd_resolve_num_splits_q.argtypes = [i32, i32, i32, i32, i32, i64, i32]
     L.fd_workspace_init.restype = ctypes.c_int
     L.fd_workspace_init.argtypes = [vp, sz, vp]
     L.fd_read_device_error.restype = ctypes.c_int
@@ -182,8 +184,10 @@ def num_splits_for_lengths(B: int, Hq: int, Hkv: int, d: int, L_cap: int, seq_le
                                                num_sms))
 
 
-def resolve_num_splits(B: int, Hq: int, Hkv: int, d: int, L_cap: int, num_splits: int) -> int:
-    return int(lib().fd_resolve_num_splits(B, Hq, Hkv, d, L_cap, num_splits))
+def resolve_num_splits(B: int, Hq: int, Hkv: int, d: int, L_cap: int, num_splits: int,
+                       Q: int = 1) -> int:
+    """Split count a call would use (Q query tokens per row; see fd_resolve_num_splits_q)."""
+    return int(lib().fd_resolve_num_splits_q(B, Q, Hq, Hkv, d, L_cap, num_splits))
 
 
 def set_path(path: int):
@@ -260,7 +264,8 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     else:
         (B, Hq, d), Qn = q.shape, 1
     Hkv = k_cache.shape[1]
-    S = resolve_num_splits(B, Hq, Hkv, d, _cap(k_cache, block_table, page_size), num_splits)
+    S = resolve_num_splits(B, Hq, Hkv, d, _cap(k_cache, block_table, page_size), num_splits,
+                           Q=Qn)
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
     if lse_out is None:
@@ -310,7 +315,8 @@ def decode_attention_fp8kv(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     else:
         (B, Hq, d), Qn = q.shape, 1
     Hkv = k_cache.shape[1]
-    S = resolve_num_splits(B, Hq, Hkv, d, _cap(k_cache, block_table, page_size), num_splits)
+    S = resolve_num_splits(B, Hq, Hkv, d, _cap(k_cache, block_table, page_size), num_splits,
+                           Q=Qn)
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
     if lse_out is None:

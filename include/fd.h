@@ -378,9 +378,16 @@ FD_API int32_t fd_get_schedule(void);
 FD_API const char* fd_partial_kernel_name(int32_t dtype, int32_t kv_dtype, int32_t d, int32_t Hkv,
                                           int32_t page_size, int32_t rows, int32_t with_output);
 
-/* Split count a call with these sizes and this num_splits argument would use. */
+/* Split count a single-token call with these sizes and this num_splits argument would use. */
 FD_API int32_t fd_resolve_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int64_t L_cap,
                               int32_t num_splits);
+/* The same for Q query tokens per row (q [B, Q, Hq, d]; Q = 1 gives fd_resolve_num_splits).
+ * With num_splits = 0, groups of more than 16 query rows per kv head (Q * Hq / Hkv) run
+ * the wide kernels, which are bound by their tile math: the count is then one CTA's worth
+ * of splits per SM, and never more than fd_resolve_num_splits returns for the same sizes
+ * (a workspace sized with that count suffices either way). */
+FD_API int32_t fd_resolve_num_splits_q(int32_t B, int32_t Q, int32_t Hq, int32_t Hkv, int32_t d,
+                                       int64_t L_cap, int32_t num_splits);
 
 FD_API const char* fd_status_string(fd_status status);
 /* One-line reason for the last non-FD_OK status returned on this thread. */

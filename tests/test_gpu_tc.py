@@ -154,3 +154,25 @@ def test_tc_long_splits(Q, G):
     for S in (1, 4):
         o, l = decode(w, q4, S)
         check(mw, o, l, ref_o.reshape(B * Q, Hq, 128), ref_l.reshape(B * Q, Hq))
+
+
+def test_tc_default_split_count():
+    """num_splits = 0 on a wide group: one CTA's worth of splits per SM, never more than
+    the single-token plan (so workspaces sized by the single-token count suffice), and
+    the call with the planned count matches the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    one = fd.resolve_num_splits(1, 64, 8, 128, 131072, 0)
+    wide = fd.resolve_num_splits(1, 64, 8, 128, 131072, 0, Q=8)
+    assert wide == min(one, max(1, sms // 8)), (one, wide)
+    assert fd.resolve_num_splits(1, 64, 8, 128, 131072, 0, Q=2) == one      # 16 rows
+    assert fd.resolve_num_splits(1, 64, 8, 128, 131072, 7, Q=8) == 7        # explicit
+    lens = [3000, 2047, 5]
+    w, q4, ref_o, ref_l = multi_token(4, 8, 2, lens, 0, seed=1600, cap=3072)
+    wd = w.to("cuda")
+    o, l = fd.decode_attention(q4.cuda(), wd.k, wd.v, wd.seq_lens, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    B, Hq = len(lens), 16
+    mw = workloads.Workload("tc", q4.reshape(B * 4, Hq, 128), w.k, w.v, w.seq_lens)
+    check(mw, o.cpu().double().numpy().reshape(B * 4, Hq, 128),
+          l.cpu().double().numpy().reshape(B * 4, Hq), ref_o.reshape(B * 4, Hq, 128),
+          ref_l.reshape(B * 4, Hq))
