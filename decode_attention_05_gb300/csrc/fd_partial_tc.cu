@@ -59,14 +59,14 @@ constexpr uint32_t kTcPCol = 448;            //   P of group g at 448 + 32 g (bf
 constexpr uint32_t kTcCtlOff = kTcStages * 2 * kTileBytes;  // 192 KB
 
 struct TcCtl {
-  PipeCtl<kTcStages> pipe;   // TMA ring (empty: released by the mma issuer's commit)
+  PipeCtl<kTcStages> pipe;   // TMA ring (empty: released by the output issuer's commit)
   uint64_t s_full[2];        // S buffer b holds a finished Q K^T (tcgen05.commit)
   uint64_t s_free[2];        // the softmax warps have read S buffer b
   uint64_t p_full[2];        // P of tile n (and its zeroed V rows) is in place, n % 2 = b
                              // (two barriers: the softmax may finish tile n + 1 before
-                             // the issuer has seen tile n, and a parity wait must never
-                             // be two phases behind its barrier)
-  uint64_t pv_done[2];       // the P V product reading P buffer b has completed
+                             // the output issuer has seen tile n, and a parity wait must
+                             // never be two phases behind its barrier)
+  uint64_t pv_done[2];       // the P V product of a tile of parity b has completed
   uint64_t mma_done;         // every product this CTA issued has completed (three issuers)
   uint32_t tmem;             // TMEM base address (tcgen05.alloc)
 };
