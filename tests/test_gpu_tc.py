@@ -176,3 +176,29 @@ def test_tc_default_split_count():
     check(mw, o.cpu().double().numpy().reshape(B * 4, Hq, 128),
           l.cpu().double().numpy().reshape(B * 4, Hq), ref_o.reshape(B * 4, Hq, 128),
           ref_l.reshape(B * 4, Hq))
+
+
+@pytest.mark.parametrize("ps", [16, 64])
+def test_tc_bad_page_is_flagged_and_contained(ps):
+    """A used table entry outside the pool in row 0 (several pages per tile at 16-token
+    pages, one page per tile at 64): flagged, every output finite, and row 1 (a clean
+    table) still equals the causal oracle."""
+    Q, G, Hkv = 4, 8, 2
+    lens = [300, 290]
+    w, q4, ref_o, ref_l = multi_token(Q, G, Hkv, lens, ps, seed=1700 + ps, cap=512)
+    wd = w.to("cuda")
+    bt = wd.block_table.clone()
+    bt[0, 1] = 10_000
+    fd.set_path(fd.FD_PATH_TCGEN05)
+    B, Hq = len(lens), Hkv * G
+    ws = torch.zeros(fd.workspace_size(B, Q * Hq, Hkv, 128, 3), dtype=torch.uint8,
+                     device="cuda")
+    o, l = fd.decode_attention(q4.cuda(), wd.k, wd.v, wd.seq_lens, bt, ps, 3, workspace=ws,
+                               out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fd.read_device_error(ws) == 2            # FD_DEVFLAG_PAGE
+    assert torch.isfinite(o).all() and torch.isfinite(l).all()
+    mw = workloads.Workload("tc", q4.reshape(B * Q, Hq, 128), w.k, w.v, w.seq_lens)
+    check(mw, o.cpu().double().numpy().reshape(B * Q, Hq, 128),
+          l.cpu().double().numpy().reshape(B * Q, Hq), ref_o.reshape(B * Q, Hq, 128),
+          ref_l.reshape(B * Q, Hq), rows=np.arange(Q * Hq, 2 * Q * Hq))
