@@ -1,5 +1,7 @@
 // fd_partial_mma.cu -- split-KV partial pass with the GQA group's dot products on the
-// tensor cores (bf16 inputs, f32 accumulation), for G = Hq / Hkv in {1, 2, 4, 8, 16}.
+// tensor cores through mma.sync (f32 accumulation): bf16 inputs for groups of up to 64
+// query rows per kv head (above 16: the wide kernel), FP8 E4M3 caches (widened to f16)
+// and f32 inputs (three TF32 products per f32 product) for groups of up to 16 and 8 rows.
 //
 // Why tensor cores here: with G query heads sharing one KV head, every KV element
 // feeds G multiply-adds for the scores and G for the output, i.e. G FLOP per KV byte.
