@@ -108,7 +108,7 @@ typedef enum {
  *                query j (0-based) attends to the keys t <= L_b - Q + j (the causal mask
  *                of [AI-Infra] 2.5 applied inside each split); a query that sees no key
  *                gets out = 0, lse_out = -inf.  Q * G <= 64 (above 16 rows per kv
- *                head: bf16 tensor-core path only).
+ *                head: bf16 on the tensor-core paths only).
  *   k_cache      device, same dtype as q.  Contiguous: [B, Hkv, L_cap, d] (block_table
  *                NULL).  Paged: [num_pages, Hkv, page_size, d]; logical token t of row
  *                b is slot t % page_size of page block_table[b][t / page_size] -- the
@@ -123,7 +123,9 @@ typedef enum {
  *                [0, num_pages); a bad one is flagged (FD_DEVFLAG_PAGE) and its tokens
  *                are excluded.  Entries past a row's length are never read.
  *   page_size    0 for a contiguous cache; else a power of two in [8, 65536].
- *   num_splits   S >= 1, or 0 to let fd_num_splits_heuristic choose.  S <= 4096.
+ *   num_splits   S >= 1, or 0 for the count fd_resolve_num_splits_q reports (the
+ *                capacity heuristic; one CTA's worth per SM for more than 16 rows per
+ *                kv head).  S <= 4096.
  *   out          device, q's shape, bf16 or f32 (bf16 is rounded to nearest even).
  *   lse_out      device f32 [B, Hq] or [B, Q, Hq] (contiguous), natural log; may be NULL.
  *   workspace    device scratch of at least fd_workspace_size(B, Q * Hq, Hkv, d, S) bytes,
@@ -137,8 +139,9 @@ typedef enum {
  *   stream       cudaStream_t (as void*), NULL = legacy default stream.
  *
  * Supported: d in {64, 128}; G = Hq / Hkv in {1, 2, 4, 8, 16, 32, 64} with Q * G <= 64
- * (more than 16 rows per kv head on the bf16 tensor-core path only); (q, k, v) all
- * bf16 with out bf16 or f32, or all f32 with out f32.  B >= 1, L_cap >= 1.
+ * (more than 16 rows per kv head: bf16 on the tensor-core paths only; f32 on the
+ * tensor cores up to 8 rows, on CUDA cores up to 16); (q, k, v) all bf16 with out bf16
+ * or f32, or all f32 with out f32.  B >= 1, L_cap >= 1.
  * Errors: FD_ERR_INVALID_ARG for rank/shape/stride/alignment mismatches, Hq % Hkv != 0,
  * NULL required pointers, num_splits < 0, page_size invalid with a block table;
  * FD_ERR_UNSUPPORTED for other d, G or dtype combinations; FD_ERR_WORKSPACE_TOO_SMALL;
