@@ -304,7 +304,14 @@ def oracle_sample(w, budget_s: float, scales=None):
 
 # ----------------------------------------------------------------------------- arms
 
+REFERENCE_BUDGET_S = 240.0     # the whole reference arm (warm-up + timed steps)
+
+
 def run_reference(args):
+    """The oracle as the reference arm: whole steps of the workload (every query row,
+    every key) when warm-up + timed steps fit REFERENCE_BUDGET_S, else each step is a
+    bounded sample (a subset of the query rows, and of the keys if need be) scaled to a
+    step."""
     world, rank, _ = dist_info()
     if rank != 0:
         return 0
@@ -316,37 +323,46 @@ def run_reference(args):
     import oracle
     run, lens = oracle_decoder(w, scales)
     threads = oracle.max_threads()
-    B, Hq = w.B, w.Q * w.Hq                      # query rows: B x Q x Hq
-    rows = list(range(0, B * Hq, max(1, (B * Hq) // threads)))[:threads]
+    n_rows = w.B * w.Q * w.Hq                    # query rows: B x Q x Hq
     L = int(lens.max())
-    # Size each step so that warm-up + timed steps end within ~90 s.
-    sl = lens.copy()
-    sl[:] = min(L, 1024)
+    calls = args.steps + args.warmup
     t0 = time.perf_counter()
-    run(sl, rows)
-    t_probe = time.perf_counter() - t0
-    per_step = 90.0 / max(1, args.steps + args.warmup)
-    tokens = int(max(16, min(L, 1024 * per_step / max(t_probe, 1e-6))))
-    sl[:] = tokens
-    for _ in range(args.warmup):
+    run(lens)                                    # one whole step, also the first warm-up
+    est_step = time.perf_counter() - t0
+    if calls * est_step <= REFERENCE_BUDGET_S:
+        sl, rows, frac = lens, None, 1.0
+        sample = "whole step (all %d query rows, all keys)" % n_rows
+        same = True
+    else:
+        per_step = REFERENCE_BUDGET_S / calls
+        keep = max(1, min(n_rows, int(n_rows * per_step / est_step)))
+        rows = list(range(0, n_rows, max(1, n_rows // keep)))[:keep]
+        row_frac = len(rows) / n_rows
+        tokens = L
+        if est_step * row_frac > per_step:       # even one row per thread is too long
+            tokens = int(max(16, min(L, L * per_step / (est_step * row_frac))))
+        sl = lens.copy()
+        sl[:] = [min(int(x), tokens) for x in lens]
+        frac = row_frac * (tokens / L)
+        sample = "%d of %d query rows x first %d of %d keys per step (%.5f of a step)" % (
+            len(rows), n_rows, tokens, L, frac)
+        same = False
+    for _ in range(max(0, args.warmup - 1)):
         run(sl, rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         run(sl, rows)
     elapsed = time.perf_counter() - t0
-    frac = (len(rows) / (B * Hq)) * (tokens / L)
     step_s = elapsed / args.steps / frac
     gbs = w.kv_bytes() / step_s / 1e9
-    sample = "%d of %d query heads x first %d of %d keys per step (%.5f of a step)" % (
-        len(rows), B * Hq, tokens, L, frac)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(step_s * 1e3, 3), "us_per_step": round(step_s * 1e6, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.name, "sample": sample},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": min(threads, len(rows)),
+        "config": {"workload": w.name, "sample": sample, "same_config": same},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -437,6 +453,9 @@ def run_fd(args):
         if st:
             raise fd.FdError(st, L.fd_last_error().decode())
 
+    # A run shorter than GRAPH_CHUNK steps replays one graph of exactly `steps` calls.
+    chunk = max(1, min(GRAPH_CHUNK, args.steps))
+
     def make_graph(call, chunk):
         if args.no_graph:
             return None
@@ -459,10 +478,20 @@ def run_fd(args):
             for _ in range(n):
                 call(sh)
             return
-        for _ in range(n // GRAPH_CHUNK):
+        for _ in range(n // chunk):
             graph.replay()
-        for _ in range(n % GRAPH_CHUNK):
+        for _ in range(n % chunk):
             call(sh)
+
+    def launch_label(n):
+        """What issue(call, graph, n) does, in words."""
+        if args.no_graph:
+            return "%d direct calls from Python (no CUDA graph)" % n
+        text = "CUDA graph of %d back-to-back decode calls, replayed %d time%s" % (
+            chunk, n // chunk, "" if n // chunk == 1 else "s")
+        if n % chunk:
+            text += ", then %d direct calls" % (n % chunk)
+        return text
 
     step_call = lambda s: checked(decode_fn(*step_args[next_set()], s))
 
@@ -474,7 +503,7 @@ def run_fd(args):
 
     for _ in range(max(3, args.warmup)):
         step()
-    step_graph = make_graph(step_call, GRAPH_CHUNK)
+    step_graph = make_graph(step_call, chunk)
     if step_graph is not None:
         step_graph.replay()
     if fd.read_device_error(ws) != 0:
@@ -503,7 +532,7 @@ def run_fd(args):
     partial_call = lambda s: checked(partial_fn(*partial_args[next_set()], s))
     for _ in range(3):
         partial_call(sh)
-    partial_graph = make_graph(partial_call, GRAPH_CHUNK)
+    partial_graph = make_graph(partial_call, chunk)
     barrier()
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2.record(stream)
@@ -516,7 +545,7 @@ def run_fd(args):
     merge_call = lambda s: checked(L.fd_merge_partials(B * Qt, Hq, d, S, lse_part.data_ptr(),
                                                        o_part.data_ptr(), ctypes.byref(dout),
                                                        lse.data_ptr(), s))
-    merge_graph = make_graph(merge_call, GRAPH_CHUNK)
+    merge_graph = make_graph(merge_call, chunk)
     barrier()
     e4, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e4.record(stream)
@@ -531,7 +560,8 @@ def run_fd(args):
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kernel, w.name),
                 "kernel": kernel, "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": kv_bytes,
-                "partial_us": round(partial_ms * 1e3, 2), "merge_us": round(merge_ms * 1e3, 2)}
+                "partial_us": round(partial_ms * 1e3, 2), "merge_us": round(merge_ms * 1e3, 2),
+                "launch": launch_label(args.steps)}
 
     # ---- end to end through the public API, host buffers, copies inside the timed region
     pin = lambda t: t.pin_memory()
@@ -599,9 +629,7 @@ def run_fd(args):
                               "KV %d MiB < 3 x 126 MiB L2: steps alternate between %d copies "
                               "of the cache, no flush" % (kv_bytes >> 20, n_sets)),
                        "parallelism": "replicas x%d" % world,
-                       "launch": ("direct calls" if args.no_graph else
-                                  "CUDA graphs of %d back-to-back decode calls, replayed"
-                                  % GRAPH_CHUNK)},
+                       "launch": launch_label(args.steps)},
             "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
             "gpu_launches": 2 * args.steps,
         }

@@ -16,6 +16,7 @@ FD_F32, FD_BF16, FD_I32, FD_F8E4M3 = 0, 1, 2, 3
 FD_PATH_AUTO, FD_PATH_SIMT, FD_PATH_MMA, FD_PATH_TCGEN05 = 0, 1, 2, 3
 FD_MERGE_KERNEL, FD_MERGE_IN_KERNEL = 0, 1
 FD_SCHEDULE_AUTO, FD_SCHEDULE_GRID, FD_SCHEDULE_PERSISTENT, FD_SCHEDULE_HEAD_GROUPS = 0, 1, 2, 3
+FD_FROM_PROCESS = -1
 
 _STATUS = {0: "FD_OK", 1: "FD_ERR_INVALID_ARG", 2: "FD_ERR_UNSUPPORTED",
            3: "FD_ERR_WORKSPACE_TOO_SMALL", 4: "FD_ERR_CUDA", 5: "FD_ERR_DEVICE_FLAG"}
@@ -32,6 +33,21 @@ class FdError(RuntimeError):
 class FdTensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
                 ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class FdOptions(ctypes.Structure):
+    """fd_options: path, merge mode and schedule of one call (FD_FROM_PROCESS = the
+    process-wide setting)."""
+    _fields_ = [("path", ctypes.c_int32), ("merge_mode", ctypes.c_int32),
+                ("schedule", ctypes.c_int32)]
+
+
+def options(path: Optional[int] = None, merge_mode: Optional[int] = None,
+            schedule: Optional[int] = None) -> FdOptions:
+    """An fd_options for one call or plan; a field left as None takes the process-wide
+    setting at the time of the call."""
+    pick = lambda v: FD_FROM_PROCESS if v is None else int(v)
+    return FdOptions(pick(path), pick(merge_mode), pick(schedule))
 
 
 _lock = threading.Lock()
@@ -63,6 +79,13 @@ def _declare(L):
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     L.fd_decode_attention.restype = ctypes.c_int
     L.fd_decode_attention.argtypes = [P, P, P, vp, P, i32, i32, P, vp, vp, sz, vp]
+    O = ctypes.POINTER(FdOptions)
+    L.fd_decode_attention_ex.restype = ctypes.c_int
+    L.fd_decode_attention_ex.argtypes = [P, P, P, vp, vp, vp, P, i32, i32, P, vp, vp, sz, vp, O]
+    L.fd_plan_set_options.restype = ctypes.c_int
+    L.fd_plan_set_options.argtypes = [vp, O]
+    L.fd_partial_kernel_name_ex.restype = ctypes.c_char_p
+    L.fd_partial_kernel_name_ex.argtypes = [O, i32, i32, i32, i32, i32, i32, i32]
     L.fd_decode_attention_noalloc.restype = ctypes.c_int
     L.fd_decode_attention_noalloc.argtypes = [P, P, P, vp, P, i32, i32, P, vp, vp]
     L.fd_decode_attention_fp8kv.restype = ctypes.c_int
@@ -221,11 +244,15 @@ def selftest_bounded_wait(workspace: torch.Tensor, limit_us: int = 50000, stream
 
 
 def partial_kernel_name(dtype, kv_dtype, d: int, Hkv: int, page_size: int = 0,
-                        with_output: bool = True, rows: int = 8) -> Optional[str]:
+                        with_output: bool = True, rows: int = 8,
+                        options: Optional[FdOptions] = None) -> Optional[str]:
     """The partial-pass kernel a call with these sizes would launch (torch dtypes);
-    rows = query rows per kv head (query tokens x Hq / Hkv)."""
-    name = lib().fd_partial_kernel_name(_DTYPES[dtype], _DTYPES[kv_dtype], d, Hkv, page_size,
-                                        rows, 1 if with_output else 0)
+    rows = query rows per kv head (query tokens x Hq / Hkv); options as for the call."""
+    args = (_DTYPES[dtype], _DTYPES[kv_dtype], d, Hkv, page_size, rows, 1 if with_output else 0)
+    if options is None:
+        name = lib().fd_partial_kernel_name(*args)
+    else:
+        name = lib().fd_partial_kernel_name_ex(ctypes.byref(options), *args)
     return name.decode() if name else None
 
 
@@ -252,11 +279,14 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
                      page_size: int = 0, num_splits: int = 0,
                      out: Optional[torch.Tensor] = None, lse_out: Optional[torch.Tensor] = None,
                      workspace: Optional[torch.Tensor] = None, out_dtype=None,
-                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+                     stream=None, options: Optional[FdOptions] = None
+                     ) -> Tuple[torch.Tensor, torch.Tensor]:
     """Run fd_decode_attention on the current CUDA stream; returns (out, lse_out).
 
     Missing ``out``/``lse_out``/``workspace`` buffers are allocated with torch (a
-    fresh workspace is zero-filled); the library itself allocates nothing.
+    fresh workspace is zero-filled); the library itself allocates nothing.  With
+    ``options`` (see ``options()``) the call goes through fd_decode_attention_ex with
+    its own path, merge mode and schedule.
     """
     L = lib()
     if q.dim() == 4:                                   # [B, Q, Hq, d]: multi-token decode
@@ -277,11 +307,17 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         raise TypeError("seq_lens must be int32")
     dq, dk, dv, dbt, do = (tensor_desc(q), tensor_desc(k_cache), tensor_desc(v_cache),
                            tensor_desc(block_table), tensor_desc(out))
-    st = L.fd_decode_attention(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv),
-                               seq_lens.data_ptr(), _ref(dbt), page_size, S, ctypes.byref(do),
-                               lse_out.data_ptr(), workspace.data_ptr(),
-                               workspace.numel() * workspace.element_size(),
-                               _stream_handle(stream))
+    ws_args = (workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+               _stream_handle(stream))
+    if options is None:
+        st = L.fd_decode_attention(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv),
+                                   seq_lens.data_ptr(), _ref(dbt), page_size, S,
+                                   ctypes.byref(do), lse_out.data_ptr(), *ws_args)
+    else:
+        st = L.fd_decode_attention_ex(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv),
+                                      None, None, seq_lens.data_ptr(), _ref(dbt), page_size, S,
+                                      ctypes.byref(do), lse_out.data_ptr(), *ws_args,
+                                      ctypes.byref(options))
     _check(st)
     return out, lse_out
 
@@ -430,6 +466,11 @@ class Plan:
 
     def resize(self, num_splits: int):
         _check(lib().fd_plan_resize(self._h, num_splits))
+
+    def set_options(self, opts: Optional[FdOptions]):
+        """fd_plan_set_options: path, merge mode and schedule of this plan's decodes
+        (None = the process-wide settings)."""
+        _check(lib().fd_plan_set_options(self._h, None if opts is None else ctypes.byref(opts)))
 
     def close(self):
         if self._h:

@@ -24,9 +24,32 @@ std::atomic<int> g_merge{FD_MERGE_KERNEL};
 std::atomic<int> g_schedule{FD_SCHEDULE_AUTO};
 std::atomic<uint32_t> g_epoch{0x5eed0001u};   // per-call ticket epochs of the fused merge
 
-// Which partial-pass kernel runs, from the process settings and the call's sizes.  The
-// persistent and head-group kernels write only partials, so neither runs under the
-// single-launch merge.
+// The path, merge mode and schedule one call runs with: its fd_options, with the
+// process-wide settings in the fields marked FD_FROM_PROCESS (or all of them for NULL).
+struct Settings {
+  int path, merge, schedule;
+};
+
+bool valid_path(int v) {
+  return v == FD_PATH_AUTO || v == FD_PATH_SIMT || v == FD_PATH_MMA || v == FD_PATH_TCGEN05;
+}
+bool valid_merge(int v) { return v == FD_MERGE_KERNEL || v == FD_MERGE_IN_KERNEL; }
+bool valid_schedule(int v) {
+  return v == FD_SCHEDULE_AUTO || v == FD_SCHEDULE_GRID || v == FD_SCHEDULE_PERSISTENT ||
+         v == FD_SCHEDULE_HEAD_GROUPS;
+}
+
+// False if a field holds neither FD_FROM_PROCESS nor one of its enum values.
+bool resolve_settings(const fd_options* o, Settings* s) {
+  s->path = (!o || o->path == FD_FROM_PROCESS) ? g_path.load() : o->path;
+  s->merge = (!o || o->merge_mode == FD_FROM_PROCESS) ? g_merge.load() : o->merge_mode;
+  s->schedule = (!o || o->schedule == FD_FROM_PROCESS) ? g_schedule.load() : o->schedule;
+  return valid_path(s->path) && valid_merge(s->merge) && valid_schedule(s->schedule);
+}
+
+// Which partial-pass kernel runs, from the call's settings and sizes.  The persistent
+// and head-group kernels write only partials, so neither runs under the single-launch
+// merge.
 struct Schedule {
   bool heads, persistent;
 };
@@ -34,9 +57,8 @@ struct Schedule {
 // rows: query rows per (b, kv head) group (Q x G); groups above kMaxNarrowRows always
 // run the wide grid kernel.
 // f32 inputs on the tensor-core path run on the grid schedule only.
-Schedule choose_schedule(int path, bool kv8, bool f32, int64_t d, int64_t Hkv,
+Schedule choose_schedule(int sched, int path, bool kv8, bool f32, int64_t d, int64_t Hkv,
                          int32_t page_size, bool fused, int64_t rows) {
-  const int sched = g_schedule.load();
   const bool narrow = rows <= fd::kMaxNarrowRows && !f32;
   const bool head_ok = path == FD_PATH_MMA && !kv8 && d == 128 &&
                        (page_size == 16 || page_size == 32) && Hkv % fd::kHeadGroup == 0 &&
@@ -58,8 +80,8 @@ bool tc_takes(int32_t q_dtype, bool kv8, int64_t d, int32_t page_size, int64_t r
 // Automatic choice: groups of kTcAutoMinRows rows or more go to the tcgen05 kernel where
 // it applies; otherwise the mma.sync path for bf16 and for f32 groups of up to
 // kMaxF32MmaRows rows, and the CUDA-core path for larger f32 groups.
-int resolve_path(int32_t q_dtype, bool kv8, int64_t d, int32_t page_size, int64_t rows) {
-  const int path = g_path.load();
+int resolve_path(int path, int32_t q_dtype, bool kv8, int64_t d, int32_t page_size,
+                 int64_t rows) {
   if (path != FD_PATH_AUTO) return path;
   if (rows >= fd::kTcAutoMinRows && tc_takes(q_dtype, kv8, d, page_size, rows))
     return FD_PATH_TCGEN05;
@@ -215,12 +237,7 @@ fd_status make_kv_map(const fd_tensor* t, uint32_t box_rows, uint32_t box_heads,
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-int current_sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n;
-}
+int current_sm_count() { return fd::sm_count(); }
 
 // Split count for num_splits = 0.  Single-token groups (up to kMaxNarrowRows query rows
 // per kv head) take fd_num_splits_heuristic.  Wider groups run the tcgen05 or mma.sync
@@ -243,6 +260,21 @@ int32_t heuristic_splits(int32_t B, int32_t Q, int32_t Hq, int32_t Hkv, int32_t 
 namespace fd {
 // Lets other translation units of the library report a failure through fd_last_error.
 fd_status record_error(fd_status st, const char* message) { return fail(st, "%s", message); }
+
+// SM count of the current device, queried once per device (0 if it cannot be read).
+int sm_count() {
+  constexpr int kDevices = 64;
+  static std::atomic<int> cached[kDevices];
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kDevices) {
+    n = cached[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+  }
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kDevices && n > 0) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
 }  // namespace fd
 
 extern "C" {
@@ -264,9 +296,7 @@ const char* fd_status_string(fd_status s) {
 }
 
 fd_status fd_set_path(int32_t path) {
-  if (path != FD_PATH_AUTO && path != FD_PATH_SIMT && path != FD_PATH_MMA &&
-      path != FD_PATH_TCGEN05)
-    return fail(FD_ERR_INVALID_ARG, "unknown kernel path %d", path);
+  if (!valid_path(path)) return fail(FD_ERR_INVALID_ARG, "unknown kernel path %d", path);
   g_path.store(path);
   return FD_OK;
 }
@@ -274,8 +304,7 @@ fd_status fd_set_path(int32_t path) {
 int32_t fd_get_path(void) { return g_path.load(); }
 
 fd_status fd_set_merge_mode(int32_t mode) {
-  if (mode != FD_MERGE_KERNEL && mode != FD_MERGE_IN_KERNEL)
-    return fail(FD_ERR_INVALID_ARG, "unknown merge mode %d", mode);
+  if (!valid_merge(mode)) return fail(FD_ERR_INVALID_ARG, "unknown merge mode %d", mode);
   g_merge.store(mode);
   return FD_OK;
 }
@@ -283,9 +312,7 @@ fd_status fd_set_merge_mode(int32_t mode) {
 int32_t fd_get_merge_mode(void) { return g_merge.load(); }
 
 fd_status fd_set_schedule(int32_t schedule) {
-  if (schedule != FD_SCHEDULE_AUTO && schedule != FD_SCHEDULE_GRID &&
-      schedule != FD_SCHEDULE_PERSISTENT && schedule != FD_SCHEDULE_HEAD_GROUPS)
-    return fail(FD_ERR_INVALID_ARG, "unknown schedule %d", schedule);
+  if (!valid_schedule(schedule)) return fail(FD_ERR_INVALID_ARG, "unknown schedule %d", schedule);
   g_schedule.store(schedule);
   return FD_OK;
 }
@@ -294,12 +321,21 @@ int32_t fd_get_schedule(void) { return g_schedule.load(); }
 
 const char* fd_partial_kernel_name(int32_t dtype, int32_t kv_dtype, int32_t d, int32_t Hkv,
                                    int32_t page_size, int32_t rows, int32_t with_output) {
+  return fd_partial_kernel_name_ex(nullptr, dtype, kv_dtype, d, Hkv, page_size, rows,
+                                   with_output);
+}
+
+const char* fd_partial_kernel_name_ex(const fd_options* options, int32_t dtype,
+                                      int32_t kv_dtype, int32_t d, int32_t Hkv,
+                                      int32_t page_size, int32_t rows, int32_t with_output) {
+  Settings cfg;
+  if (!resolve_settings(options, &cfg)) return nullptr;
   const bool kv8 = kv_dtype == FD_F8E4M3;
   if ((dtype != FD_BF16 && dtype != FD_F32) || (!kv8 && kv_dtype != dtype) ||
       (kv8 && dtype != FD_BF16) || d <= 0 || Hkv <= 0 || page_size < 0 || rows < 1 ||
       rows > fd::kMaxRows)
     return nullptr;
-  const int path = resolve_path(dtype, kv8, d, page_size, rows);
+  const int path = resolve_path(cfg.path, dtype, kv8, d, page_size, rows);
   if ((path == FD_PATH_MMA && dtype == FD_F32 && rows > fd::kMaxF32MmaRows) ||
       (kv8 && path != FD_PATH_MMA))
     return nullptr;
@@ -308,8 +344,9 @@ const char* fd_partial_kernel_name(int32_t dtype, int32_t kv_dtype, int32_t d, i
   if (rows > fd::kMaxNarrowRows && (path != FD_PATH_MMA || kv8)) return nullptr;
   if (path == FD_PATH_SIMT) return "fd_partial_simt_kernel";
   if (rows > fd::kMaxNarrowRows) return "fd_partial_wide_kernel";
-  const bool fused = with_output && g_merge.load() == FD_MERGE_IN_KERNEL;
-  const Schedule sc = choose_schedule(path, kv8, dtype == FD_F32, d, Hkv, page_size, fused, rows);
+  const bool fused = with_output && cfg.merge == FD_MERGE_IN_KERNEL;
+  const Schedule sc = choose_schedule(cfg.schedule, path, kv8, dtype == FD_F32, d, Hkv,
+                                      page_size, fused, rows);
   if (sc.heads) return "fd_partial_heads_kernel";
   if (sc.persistent) return "fd_partial_persist_kernel";
   return "fd_partial_mma_kernel";
@@ -371,7 +408,7 @@ struct Prepared {
 fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor* v_cache,
                   const int32_t* seq_lens, const fd_tensor* block_table, int32_t page_size,
                   int32_t num_splits, const fd_tensor* out, float* lse_out, void* workspace,
-                  size_t workspace_bytes, bool need_out, Prepared* pr,
+                  size_t workspace_bytes, bool need_out, const Settings& cfg, Prepared* pr,
                   bool kv8 = false, const float* k_scale = nullptr,
                   const float* v_scale = nullptr) {
   // ---- presence and ranks
@@ -492,7 +529,7 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
     return fail(FD_ERR_UNSUPPORTED, "grid too large");
 
   // ---- path
-  const int path = resolve_path(q->dtype, kv8, d, paged ? page_size : 0, Q * G);
+  const int path = resolve_path(cfg.path, q->dtype, kv8, d, paged ? page_size : 0, Q * G);
   if (path == FD_PATH_TCGEN05 && !tc_takes(q->dtype, kv8, d, paged ? page_size : 0, Q * G))
     return fail(FD_ERR_UNSUPPORTED,
                 "the tcgen05 kernel takes bf16 q/K/V with d = 128, up to %d query rows per kv "
@@ -509,9 +546,9 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
                 "more than %d query rows per kv head (%lld) run on the bf16 tensor-core paths only",
                 fd::kMaxNarrowRows, (long long)(Q * G));
 
-  // ---- schedule (fd_set_schedule)
-  const bool fused = need_out && g_merge.load() == FD_MERGE_IN_KERNEL;
-  const Schedule sc = choose_schedule(path, kv8, q->dtype == FD_F32, d, Hkv,
+  // ---- schedule (fd_set_schedule or the call's options)
+  const bool fused = need_out && cfg.merge == FD_MERGE_IN_KERNEL;
+  const Schedule sc = choose_schedule(cfg.schedule, path, kv8, q->dtype == FD_F32, d, Hkv,
                                      paged ? page_size : 0, fused, Q * G);
   const bool heads = sc.heads, persistent = sc.persistent;
 
@@ -594,6 +631,41 @@ fd_status launch_merge(const fd::Params& p, cudaStream_t s) {
   return FD_OK;
 }
 
+// Which cache format an entry point takes: bf16 / f32 only, FP8 E4M3 only, or whichever
+// k_cache's dtype says (fd_decode_attention_ex).
+enum class CacheKind { kPlain, kFp8, kByDtype };
+
+// One decode call: resolve the settings, validate and plan, then launch the partial pass
+// and, with an output, the merge (its own kernel, or inside the partial pass for
+// FD_MERGE_IN_KERNEL).  need_out false: the partial pass only.
+fd_status run_decode(CacheKind kind, const fd_tensor* q, const fd_tensor* k_cache,
+                     const fd_tensor* v_cache, const float* k_scale, const float* v_scale,
+                     const int32_t* seq_lens, const fd_tensor* block_table, int32_t page_size,
+                     int32_t num_splits, fd_tensor* out, float* lse_out, void* workspace,
+                     size_t workspace_bytes, void* stream, const fd_options* options,
+                     bool need_out) {
+  Settings cfg;
+  if (!resolve_settings(options, &cfg))
+    return fail(FD_ERR_INVALID_ARG, "fd_options holds an unknown path, merge mode or schedule");
+  bool kv8 = kind == CacheKind::kFp8;
+  if (kind == CacheKind::kByDtype) {
+    kv8 = k_cache != nullptr && k_cache->dtype == FD_F8E4M3;
+    if (!kv8 && (k_scale || v_scale))
+      return fail(FD_ERR_INVALID_ARG, "k_scale / v_scale belong to an FP8 E4M3 cache only");
+  }
+  Prepared pr;
+  fd_status st = prepare(q, k_cache, v_cache, seq_lens, block_table, page_size, num_splits,
+                         need_out ? out : nullptr, need_out ? lse_out : nullptr, workspace,
+                         workspace_bytes, need_out, cfg, &pr, kv8, k_scale, v_scale);
+  if (st != FD_OK) return st;
+  const cudaStream_t s = (cudaStream_t)stream;
+  if (need_out && pr.fused) return launch_partial(pr, s);   // one launch merges in-kernel
+  pr.p.counters = nullptr;          // the merge, if any, is a separate kernel
+  st = launch_partial(pr, s);
+  if (st != FD_OK || !need_out) return st;
+  return launch_merge(pr.p, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -603,30 +675,18 @@ fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
                               const fd_tensor* block_table, int32_t page_size,
                               int32_t num_splits, fd_tensor* out, float* lse_out,
                               void* workspace, size_t workspace_bytes, void* stream) {
-  Prepared pr;
-  fd_status st = prepare(q, k_cache, v_cache, seq_lens, block_table, page_size, num_splits, out,
-                         lse_out, workspace, workspace_bytes, true, &pr);
-  if (st != FD_OK) return st;
-  // FD_MERGE_IN_KERNEL: one launch, the last CTA of each (b, kv head) group merges it.
-  // FD_MERGE_KERNEL (default): the merge is its own kernel over (b, query head) rows,
-  // launched with programmatic dependent launch behind the partial pass.
-  if (pr.fused) return launch_partial(pr, (cudaStream_t)stream);
-  pr.p.counters = nullptr;
-  st = launch_partial(pr, (cudaStream_t)stream);
-  if (st != FD_OK) return st;
-  return launch_merge(pr.p, (cudaStream_t)stream);
+  return run_decode(CacheKind::kPlain, q, k_cache, v_cache, nullptr, nullptr, seq_lens,
+                    block_table, page_size, num_splits, out, lse_out, workspace,
+                    workspace_bytes, stream, nullptr, true);
 }
 
 fd_status fd_decode_partial(const fd_tensor* q, const fd_tensor* k_cache,
                             const fd_tensor* v_cache, const int32_t* seq_lens,
                             const fd_tensor* block_table, int32_t page_size, int32_t num_splits,
                             void* workspace, size_t workspace_bytes, void* stream) {
-  Prepared pr;
-  fd_status st = prepare(q, k_cache, v_cache, seq_lens, block_table, page_size, num_splits,
-                         nullptr, nullptr, workspace, workspace_bytes, false, &pr);
-  if (st != FD_OK) return st;
-  pr.p.counters = nullptr;          // partials only: the merge is a separate call
-  return launch_partial(pr, (cudaStream_t)stream);
+  return run_decode(CacheKind::kPlain, q, k_cache, v_cache, nullptr, nullptr, seq_lens,
+                    block_table, page_size, num_splits, nullptr, nullptr, workspace,
+                    workspace_bytes, stream, nullptr, false);
 }
 
 fd_status fd_decode_attention_fp8kv(const fd_tensor* q, const fd_tensor* k_cache,
@@ -635,15 +695,9 @@ fd_status fd_decode_attention_fp8kv(const fd_tensor* q, const fd_tensor* k_cache
                                    const fd_tensor* block_table, int32_t page_size,
                                    int32_t num_splits, fd_tensor* out, float* lse_out,
                                    void* workspace, size_t workspace_bytes, void* stream) {
-  Prepared pr;
-  fd_status st = prepare(q, k_cache, v_cache, seq_lens, block_table, page_size, num_splits, out,
-                         lse_out, workspace, workspace_bytes, true, &pr, true, k_scale, v_scale);
-  if (st != FD_OK) return st;
-  if (pr.fused) return launch_partial(pr, (cudaStream_t)stream);
-  pr.p.counters = nullptr;
-  st = launch_partial(pr, (cudaStream_t)stream);
-  if (st != FD_OK) return st;
-  return launch_merge(pr.p, (cudaStream_t)stream);
+  return run_decode(CacheKind::kFp8, q, k_cache, v_cache, k_scale, v_scale, seq_lens,
+                    block_table, page_size, num_splits, out, lse_out, workspace,
+                    workspace_bytes, stream, nullptr, true);
 }
 
 fd_status fd_decode_partial_fp8kv(const fd_tensor* q, const fd_tensor* k_cache,
@@ -652,13 +706,21 @@ fd_status fd_decode_partial_fp8kv(const fd_tensor* q, const fd_tensor* k_cache,
                                  const fd_tensor* block_table, int32_t page_size,
                                  int32_t num_splits, void* workspace, size_t workspace_bytes,
                                  void* stream) {
-  Prepared pr;
-  fd_status st = prepare(q, k_cache, v_cache, seq_lens, block_table, page_size, num_splits,
-                         nullptr, nullptr, workspace, workspace_bytes, false, &pr, true, k_scale,
-                         v_scale);
-  if (st != FD_OK) return st;
-  pr.p.counters = nullptr;          // partials only: the merge is a separate call
-  return launch_partial(pr, (cudaStream_t)stream);
+  return run_decode(CacheKind::kFp8, q, k_cache, v_cache, k_scale, v_scale, seq_lens,
+                    block_table, page_size, num_splits, nullptr, nullptr, workspace,
+                    workspace_bytes, stream, nullptr, false);
+}
+
+fd_status fd_decode_attention_ex(const fd_tensor* q, const fd_tensor* k_cache,
+                                 const fd_tensor* v_cache, const float* k_scale,
+                                 const float* v_scale, const int32_t* seq_lens,
+                                 const fd_tensor* block_table, int32_t page_size,
+                                 int32_t num_splits, fd_tensor* out, float* lse_out,
+                                 void* workspace, size_t workspace_bytes, void* stream,
+                                 const fd_options* options) {
+  return run_decode(CacheKind::kByDtype, q, k_cache, v_cache, k_scale, v_scale, seq_lens,
+                    block_table, page_size, num_splits, out, lse_out, workspace,
+                    workspace_bytes, stream, options, out != nullptr);
 }
 
 fd_status fd_workspace_partials(void* workspace, int32_t B, int32_t Hq, int32_t d,
@@ -716,6 +778,7 @@ struct fd_plan {
   void* ws;
   size_t ws_bytes;
   cudaEvent_t done;   // recorded after each decode's merge pass
+  fd_options opts;    // fd_plan_set_options (every field FD_FROM_PROCESS by default)
 };
 
 static fd_status plan_alloc(fd_plan* p, int32_t S) {
@@ -750,6 +813,7 @@ fd_status fd_plan_create(fd_plan** plan, int32_t B, int32_t Hq, int32_t Hkv, int
       num_splits > kMaxSplits || Hq % Hkv != 0)
     return fail(FD_ERR_INVALID_ARG, "invalid plan sizes");
   fd_plan* p = new fd_plan();
+  p->opts.path = p->opts.merge_mode = p->opts.schedule = FD_FROM_PROCESS;
   p->B = B;
   p->Hq = Hq;
   p->Hkv = Hkv;
@@ -779,11 +843,24 @@ fd_status fd_plan_decode(fd_plan* plan, const fd_tensor* q, const fd_tensor* k_c
   if (!q || q->ndim != 3 || q->shape[0] != plan->B || q->shape[1] != plan->Hq || q->shape[2] != plan->d ||
       !k_cache || k_cache->ndim != 4 || k_cache->shape[1] != plan->Hkv)
     return fail(FD_ERR_INVALID_ARG, "tensor sizes differ from the plan's");
-  fd_status st = fd_decode_attention(q, k_cache, v_cache, seq_lens, block_table, page_size, plan->S,
-                                     out, lse_out, plan->ws, plan->ws_bytes, stream);
+  fd_status st = run_decode(CacheKind::kPlain, q, k_cache, v_cache, nullptr, nullptr, seq_lens,
+                            block_table, page_size, plan->S, out, lse_out, plan->ws,
+                            plan->ws_bytes, stream, &plan->opts, true);
   if (st != FD_OK) return st;
   cudaError_t e = cudaEventRecord(plan->done, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(FD_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
+  return FD_OK;
+}
+
+fd_status fd_plan_set_options(fd_plan* plan, const fd_options* options) {
+  if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
+  fd_options o;
+  o.path = o.merge_mode = o.schedule = FD_FROM_PROCESS;
+  if (options) o = *options;
+  Settings cfg;
+  if (!resolve_settings(&o, &cfg))
+    return fail(FD_ERR_INVALID_ARG, "fd_options holds an unknown path, merge mode or schedule");
+  plan->opts = o;
   return FD_OK;
 }
 

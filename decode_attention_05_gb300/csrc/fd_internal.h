@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "fd.h"
 
 namespace fd {
@@ -105,6 +107,27 @@ cudaError_t launch_partial_kernel(Kernel kernel, dim3 grid, int threads, size_t 
 
 // Record `message` as the calling thread's fd_last_error() and return `st`.
 fd_status record_error(fd_status st, const char* message);
+
+// SM count of the current device, queried once per device (0 if it cannot be read).
+int sm_count();
+
+// The opt-in dynamic shared-memory size is a per-kernel, per-device attribute: each
+// launcher keeps one of these (a function-local static per kernel instantiation) and
+// sets the attribute the first time it launches on a device, not on every call.
+struct SmemOptIn {
+  std::atomic<uint64_t> done{0};   // bit i: set on device i (devices 0..63)
+  template <class Kernel>
+  cudaError_t apply(Kernel kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t{1} << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+};
 
 // Query rows per (b, kv head) group padded to the kernels' template size: a power of two
 // up to kMaxRows (groups above kMaxNarrowRows run the wide tensor-core kernel only).

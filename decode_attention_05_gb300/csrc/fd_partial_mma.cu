@@ -995,28 +995,26 @@ cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap
   cudaError_t e;
   if constexpr (SH::PERSIST) {
     auto kernel = fd_partial_persist_kernel<SH>;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SH::SMEM_BYTES);
+    static SmemOptIn opt_in;
+    e = opt_in.apply(kernel, (int)SH::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0;
-    e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
     const int64_t items = (int64_t)p.S * p.Hkv * p.B;
     const unsigned grid = (unsigned)(items < 2 * sms ? items : 2 * sms);
     e = launch_partial_kernel(kernel, dim3(grid), SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
   } else if constexpr (SH::WIDE) {
     auto kernel = fd_partial_wide_kernel<SH>;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SH::SMEM_BYTES);
+    static SmemOptIn opt_in;
+    e = opt_in.apply(kernel, (int)SH::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
     e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
   } else if (p.head_group) {
     if constexpr (SH::D == 128 && !SH::KV8 && !SH::F32) {
       auto kernel = fd_partial_heads_kernel<SH>;
-      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)SH::SMEM_BYTES);
+      static SmemOptIn opt_in;
+      e = opt_in.apply(kernel, (int)SH::SMEM_BYTES);
       if (e != cudaSuccess) return e;
       dim3 grid((unsigned)p.S, (unsigned)(p.Hkv / kHeadGroup), (unsigned)p.B);
       e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
@@ -1025,8 +1023,8 @@ cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap
     }
   } else {
     auto kernel = fd_partial_mma_kernel<SH>;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SH::SMEM_BYTES);
+    static SmemOptIn opt_in;
+    e = opt_in.apply(kernel, (int)SH::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
     e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);

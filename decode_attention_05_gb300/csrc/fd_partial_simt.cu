@@ -9,10 +9,8 @@ template <class SH>
 cudaError_t launch_simt(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                         cudaStream_t stream) {
   auto kernel = fd_partial_simt_kernel<SH>;
-  // The opt-in shared-memory size is a per-function attribute; setting it is cheap and
-  // idempotent, so it is set on every launch (any current device).
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SH::SMEM_BYTES);
+  static SmemOptIn opt_in;          // set once per device
+  cudaError_t e = opt_in.apply(kernel, (int)SH::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
   e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);

@@ -558,8 +558,8 @@ template <int R>
 cudaError_t launch_tc(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                       cudaStream_t stream) {
   auto kernel = fd_partial_tc_kernel<R>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kTcSmemBytes);
+  static SmemOptIn opt_in;          // set once per device
+  cudaError_t e = opt_in.apply(kernel, (int)kTcSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
   e = launch_partial_kernel(kernel, grid, kTcThreads, kTcSmemBytes, stream, tk, tv, p);

@@ -229,12 +229,16 @@ FD_API fd_status fd_merge_partials(int32_t B, int32_t Hq, int32_t d, int32_t num
  * Same arguments, checks and results as fd_decode_attention, minus the workspace: the
  * split partials go to a scratch array built into the library (8 MiB per device, held
  * by every GPU that loads the library until the process exits).  A call that would need
- * more than 8 MiB (fd_workspace_size of its sizes and resolved split count) returns
- * FD_ERR_UNSUPPORTED and launches nothing.  All calls on a device share the array:
- * calls that can overlap on the GPU race and must be ordered by the caller.  The first
- * call on each device sets the array up (looks up its address and zero-fills it once,
- * synchronously); make it before any stream capture.  Device-side input flags are not
- * reported by this entry point.  Allocates nothing (no cudaMalloc / cudaFree).
+ * more than 8 MiB -- fd_workspace_size(B, Q * Hq, Hkv, d, S) with Q the query tokens per
+ * row (1 for a 3-D q) and S = fd_resolve_num_splits_q(...) of its arguments -- returns
+ * FD_ERR_UNSUPPORTED and launches nothing.  All calls on a device share the array and it
+ * keeps what the last call left: calls that can overlap on the GPU race and must be
+ * ordered by the caller.  The first call on each device sets the array up: it looks up
+ * the array's address, zero-fills it and waits for the device to finish
+ * (cudaDeviceSynchronize), so the fill is complete before any stream -- non-blocking
+ * ones included -- runs this call's kernels; make that first call before any stream
+ * capture.  Device-side input flags are not reported by this entry point.  Allocates
+ * nothing (no cudaMalloc / cudaFree).
  */
 FD_API fd_status fd_decode_attention_noalloc(const fd_tensor* q, const fd_tensor* k_cache,
                                       const fd_tensor* v_cache, const int32_t* seq_lens,
@@ -320,7 +324,8 @@ FD_API fd_status fd_plan_create(fd_plan** plan, int32_t B, int32_t Hq, int32_t H
 FD_API int32_t fd_plan_num_splits(const fd_plan* plan);
 FD_API size_t fd_plan_workspace_bytes(const fd_plan* plan);
 FD_API void* fd_plan_workspace(const fd_plan* plan);
-/* fd_decode_attention with the plan's split count and workspace; records the event. */
+/* fd_decode_attention with the plan's split count, workspace and options
+ * (fd_plan_set_options); records the event. */
 FD_API fd_status fd_plan_decode(fd_plan* plan, const fd_tensor* q, const fd_tensor* k_cache,
                          const fd_tensor* v_cache, const int32_t* seq_lens,
                          const fd_tensor* block_table, int32_t page_size, fd_tensor* out,
@@ -345,7 +350,7 @@ FD_API int32_t fd_get_path(void);
 
 /*
  * How the tensor-core partial pass assigns work items -- one (split, kv head, row) of
- * [FD-interview] section two's split loop -- to CTAs (process-wide, for later calls).
+ * [FD-QA] section two's split loop -- to CTAs (process-wide, for later calls).
  * FD_SCHEDULE_GRID: one CTA per item, two per SM; items beyond one wave wait for a
  * slot, and each CTA fills and drains its own copy pipeline.
  * FD_SCHEDULE_PERSISTENT: two CTAs per SM take items from a queue in the workspace
@@ -370,6 +375,51 @@ FD_API fd_status fd_set_schedule(int32_t schedule);
 FD_API int32_t fd_get_schedule(void);
 
 /*
+ * Per-call (or per-plan) choice of path, merge mode and schedule.  fd_set_path,
+ * fd_set_merge_mode and fd_set_schedule change the process-wide settings, which every
+ * thread and every other user of the library in the process sees; a caller that wants
+ * its own choice without affecting anyone else passes an fd_options to
+ * fd_decode_attention_ex or fd_plan_set_options instead.  A field set to
+ * FD_FROM_PROCESS takes the process-wide setting at the time of the call; any other
+ * value must be one of the field's enum values (else FD_ERR_INVALID_ARG).  A NULL
+ * options pointer means every field FD_FROM_PROCESS.  The library keeps no pointer to
+ * the struct past the call.
+ */
+#define FD_FROM_PROCESS (-1)
+typedef struct {
+  int32_t path;         /* fd_path, or FD_FROM_PROCESS       */
+  int32_t merge_mode;   /* fd_merge_mode, or FD_FROM_PROCESS */
+  int32_t schedule;     /* fd_schedule, or FD_FROM_PROCESS   */
+} fd_options;
+
+/*
+ * fd_decode_attention_ex -- every decode entry point in one call, with per-call
+ * options.  Arguments as fd_decode_attention, plus:
+ *   k_scale, v_scale  for an FP8 E4M3 cache (k_cache / v_cache dtype FD_F8E4M3): as
+ *                     fd_decode_attention_fp8kv.  Must be NULL for bf16 / f32 caches.
+ *   out               NULL runs the partial pass only (fd_decode_partial /
+ *                     fd_decode_partial_fp8kv: partials in the workspace, lse_out
+ *                     ignored); otherwise the whole step.
+ *   options           path, merge mode and schedule for this call only (see fd_options);
+ *                     NULL = the process-wide settings.
+ * Checks, errors and results are those of the entry point the call stands for.
+ */
+FD_API fd_status fd_decode_attention_ex(const fd_tensor* q, const fd_tensor* k_cache,
+                                        const fd_tensor* v_cache, const float* k_scale,
+                                        const float* v_scale, const int32_t* seq_lens,
+                                        const fd_tensor* block_table, int32_t page_size,
+                                        int32_t num_splits, fd_tensor* out, float* lse_out,
+                                        void* workspace, size_t workspace_bytes, void* stream,
+                                        const fd_options* options);
+
+/*
+ * Options that fd_plan_decode uses for this plan's later decodes (copied; NULL = the
+ * process-wide settings, which is also a new plan's state).  FD_ERR_INVALID_ARG for an
+ * unknown value, and the plan keeps its previous options.
+ */
+FD_API fd_status fd_plan_set_options(fd_plan* plan, const fd_options* options);
+
+/*
  * Name of the partial-pass kernel a call would launch under the current process
  * settings (path, merge mode, schedule): "fd_partial_mma_kernel",
  * "fd_partial_heads_kernel", "fd_partial_wide_kernel", "fd_partial_persist_kernel" or
@@ -380,6 +430,12 @@ FD_API int32_t fd_get_schedule(void);
  */
 FD_API const char* fd_partial_kernel_name(int32_t dtype, int32_t kv_dtype, int32_t d, int32_t Hkv,
                                           int32_t page_size, int32_t rows, int32_t with_output);
+/* The same under `options` (NULL = the process-wide settings); NULL for unknown option
+ * values too. */
+FD_API const char* fd_partial_kernel_name_ex(const fd_options* options, int32_t dtype,
+                                             int32_t kv_dtype, int32_t d, int32_t Hkv,
+                                             int32_t page_size, int32_t rows,
+                                             int32_t with_output);
 
 /* Split count a single-token call with these sizes and this num_splits argument would use. */
 FD_API int32_t fd_resolve_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int64_t L_cap,

@@ -316,3 +316,63 @@ def test_validation(case, expected):
         k, v = desc([16, 2, 32, 128]), desc([16, 2, 32, 128])
     assert call(q, k, v, out, **kw) == expected
     assert fd.lib().fd_last_error()        # a reason is recorded
+
+
+# ---------------------------------------------------------------- per-call options
+
+def test_options_choose_the_kernel_per_call():
+    """fd_options override the process-wide settings for one query (and one call) and
+    leave those settings as they were; FD_FROM_PROCESS fields follow them."""
+    import torch
+    bf = torch.bfloat16
+    name = fd.partial_kernel_name
+    lib = fd.lib()
+    try:
+        fd.set_path(fd.FD_PATH_SIMT)
+        fd.set_schedule(fd.FD_SCHEDULE_PERSISTENT)
+        assert name(bf, bf, 128, 8) == "fd_partial_simt_kernel"
+        o = fd.options(path=fd.FD_PATH_MMA, schedule=fd.FD_SCHEDULE_GRID)
+        assert name(bf, bf, 128, 8, options=o) == "fd_partial_mma_kernel"
+        assert name(bf, bf, 128, 8, options=fd.options(path=fd.FD_PATH_MMA)) == \
+            "fd_partial_persist_kernel"                        # schedule from the process
+        assert name(bf, bf, 128, 8, options=fd.options()) == "fd_partial_simt_kernel"
+        assert name(bf, bf, 128, 8, 16, options=fd.options(
+            path=fd.FD_PATH_AUTO, schedule=fd.FD_SCHEDULE_AUTO)) == "fd_partial_heads_kernel"
+        assert name(bf, bf, 128, 8, 16, options=fd.options(
+            path=fd.FD_PATH_AUTO, schedule=fd.FD_SCHEDULE_AUTO,
+            merge_mode=fd.FD_MERGE_IN_KERNEL)) == "fd_partial_mma_kernel"
+        assert name(bf, bf, 128, 8, options=fd.options(path=fd.FD_PATH_TCGEN05)) == \
+            "fd_partial_tc_kernel"
+        for bad in (fd.options(path=9), fd.options(merge_mode=2), fd.options(schedule=-2)):
+            assert name(bf, bf, 128, 8, options=bad) is None
+        assert fd.get_path() == fd.FD_PATH_SIMT                # process settings untouched
+        assert fd.get_schedule() == fd.FD_SCHEDULE_PERSISTENT
+    finally:
+        lib.fd_set_schedule(fd.FD_SCHEDULE_AUTO)
+        lib.fd_set_merge_mode(fd.FD_MERGE_KERNEL)
+        lib.fd_set_path(fd.FD_PATH_AUTO)
+
+
+def call_ex(q, k, v, out, opts, *, k_scale=None, v_scale=None, S=4):
+    lib = fd.lib()
+    r = lambda x: None if x is None else ctypes.byref(x)
+    return lib.fd_decode_attention_ex(r(q), r(k), r(v), k_scale, v_scale, FAKE, None, 0, S,
+                                      r(out), FAKE, FAKE, 1 << 24, None, r(opts))
+
+
+def test_decode_ex_validation():
+    q, k, v, out = good()
+    assert call_ex(q, k, v, out, fd.options(path=9)) == INVALID
+    assert call_ex(q, k, v, out, fd.options(merge_mode=3)) == INVALID
+    assert call_ex(q, k, v, out, fd.options(schedule=7)) == INVALID
+    # Scales belong to an FP8 cache only.
+    assert call_ex(q, k, v, out, None, k_scale=FAKE) == INVALID
+    # An FP8 cache takes bf16 q and head dim 128; the checks of the FP8 entry point apply.
+    k8, v8 = desc([2, 2, 1024, 64], dtype=3), desc([2, 2, 1024, 64], dtype=3)
+    q64, out64 = desc([2, 8, 64]), desc([2, 8, 64])
+    assert call_ex(q64, k8, v8, out64, None) == UNSUPPORTED
+    # The partial pass alone (out NULL) still validates every input.
+    assert call_ex(desc([2, 7, 128]), k, v, None, None) == INVALID
+    # An FP8 cache through the plain entry point is refused, as before.
+    assert call(q, desc([2, 2, 1024, 128], dtype=3), desc([2, 2, 1024, 128], dtype=3), out) \
+        == INVALID

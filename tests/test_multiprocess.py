@@ -124,3 +124,31 @@ def test_reference_arm_under_torchrun():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
+
+
+def _splits_worker(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    from decode_attention_05_gb300 import sequence_parallel as sp
+    _init(rank, world, port)
+    try:
+        # Shards of different capacities resolve different local counts; every rank must
+        # use the largest (the gather needs one count everywhere).
+        sp.fd.resolve_num_splits = lambda B, Hq, Hkv, d, cap, n: 3 + 5 * rank
+        q.put((rank, sp.shard_num_splits(1, 8, 1, 128, 1000 * (rank + 1), 0),
+               sp.shard_num_splits(1, 8, 1, 128, 1000, 7)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_shard_split_count_agrees_across_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_splits_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert got == [(0, 8, 7), (1, 8, 7)]
