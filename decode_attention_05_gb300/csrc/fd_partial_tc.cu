@@ -121,6 +121,26 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// Two 32-column TMEM loads (columns taddr0.., taddr1..) with a single wait.
+__device__ __forceinline__ void tc_ld32x2(uint32_t taddr0, uint32_t taddr1, float* v) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr0), "r"(taddr1)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
   uint32_t r[16];
   asm volatile(
@@ -144,6 +164,17 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const float* v) {
          "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]),
          "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]),
          "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+// Registers -> TMEM, 32 columns of raw words (bf16 pairs), complete before the statement ends.
+__device__ __forceinline__ void tc_st32w(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;"
+      :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+         "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+         "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+         "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
 // Registers -> TMEM, 16 or 8 columns of packed words, complete before the statement ends.
@@ -222,6 +253,7 @@ __device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity, uint32
 
 // A bounded wait that also gives up as soon as another role has aborted the split.
 __device__ __forceinline__ bool wait_or_abort(TcCtl* ctl, uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;     // the common case reads no timer
   const uint64_t t0 = global_ns();
   while (!mbar_probe(bar, parity, 200u)) {
     if (aborted(ctl) || global_ns() - t0 > kWaitLimitNs) return false;
@@ -414,6 +446,34 @@ __device__ bool softmax_rows(const Params& p, const SplitInfo& si, uint8_t* stag
   return true;
 }
 
+// Epilogue scratch in the ring.  When a softmax group has seen the product of its last
+// tile, every product up to that tile has completed (one issuing thread, in order) and
+// no copy is left to land: the only stage still in use is the one holding the split's
+// last tile, which the other group may still be working on.  So the scratch avoids that
+// stage: partial state q (R rows x D floats, 32 KB for R = 64, 16 KB for R = 32) sits in
+// stage (last + 1 + q / PER) mod STAGES, PER = 32 KB / its size, and the per-state
+// statistics in stage (last + 5) mod STAGES -- 5 of the 6 stages, none of them `last`.
+// A group can then write its states as soon as it is done, while the other finishes.
+template <int R>
+__device__ __forceinline__ float* o_state(uint8_t* stages, int last_stage, int q) {
+  constexpr int PER = 64 / R;                        // states per 32 KB stage
+  const int st = (last_stage + 1 + q / PER) % kTcStages;
+  return reinterpret_cast<float*>(stages + (size_t)st * 2 * kTileBytes +
+                                  (size_t)(q % PER) * R * kTcD * sizeof(float));
+}
+__device__ __forceinline__ float* o_stats(uint8_t* stages, int last_stage) {
+  return reinterpret_cast<float*>(stages + (size_t)((last_stage + 5) % kTcStages) * 2 * kTileBytes);
+}
+// Float offset of dims 4 c4 .. 4 c4 + 3 of query row h inside one state's R x D block.
+// Within each 128-byte segment of a row the 16-byte chunks are XOR-swizzled by h mod 8:
+// 32 lanes writing the same dims of 32 consecutive rows then cover all 8 chunk
+// positions (4 wavefronts per 512 bytes, no bank conflict), and a warp reading the 32
+// chunks of one row is conflict-free as well.
+__device__ __forceinline__ int o_index(int h, int c4) {
+  return h * kTcD + (((c4 & ~7) | ((c4 & 7) ^ (h & 7))) << 2);
+}
+static_assert(kTcStages == 6, "the epilogue scratch takes 5 of 6 stages");
+
 template <int R>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fd_partial_tc_kernel(const __grid_constant__ CUtensorMap tk,
@@ -452,105 +512,167 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     ctl->pipe.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
-    tc_alloc(smem_addr(&ctl->tmem), kTcCols);
-    tc_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = ctl->tmem;
-  if (warp < 8) {
-    // Lane L = t mod 128 of TMEM: group 0 writes its Q row (query row L mod R, as bf16
-    // pairs along d; rows past the group are zero), each group zeroes its P columns
-    // (each lane later writes only its slice of them).
-    const int L = t & 127;
-    const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    uint32_t v[32];
-    if (t < 128) {
-      const int h = L % R;
-      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-          reinterpret_cast<const __nv_bfloat16*>(p.q) +
-          q_offset(p, si.b, si.g, h < p.n_rows ? h : 0));
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) v[c] = h < p.n_rows ? qrow[half * 32 + c] : 0u;
-        tc_st32(tl + kTcQCol + half * 32, reinterpret_cast<const float*>(v));
-      }
-    }
-#pragma unroll
-    for (int c = 0; c < 32; ++c) v[c] = 0u;
-    tc_st32(tl + kTcPCol + (uint32_t)(t >> 7) * (kTcTT / 2), reinterpret_cast<const float*>(v));
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  __syncthreads();                  // barriers initialised
 
   float m = kNegInf, l = 0.f;
-  if (warp == 8) {                  // ---------------- TMA producer
-    prefetch_tensormap(&tk);
+  if (warp == 8) {                  // ---------------- TMA producer, from the start: the
+    prefetch_tensormap(&tk);        // first tiles load while the other warps set up
     prefetch_tensormap(&tv);
     produce_tiles<kTcTT, kTcStages>(p, si, &tk, &tv, stages, &ctl->pipe, lane);
-  } else if (warp == 9 || warp == 10) {   // ---------- score products, even / odd tiles
-    if (lane == 0) issue_scores(p, si, stages, ctl, tmem, warp - 9);
-    __syncwarp();
-  } else if (warp == 11) {          // ---------------- output products
-    if (lane == 0) issue_outputs(p, si, stages, ctl, tmem);
-    __syncwarp();
-  } else {                          // ---------------- softmax
-    if (!softmax_rows<R>(p, si, stages, ctl, tmem, t, m, l) && lane == 0) set_abort(p, ctl);
+  } else {
+    // Set-up of the MMA operands (every warp but the producer): tensor memory, Q and the
+    // zeroed P columns.
+    if (warp == 0) {
+      tc_alloc(smem_addr(&ctl->tmem), kTcCols);
+      tc_relinquish();
+    }
+    tc_fence_before();
+    named_bar_sync(2, kTcThreads - 32);
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem;
+    if (warp < 8) {
+      // Lane L = t mod 128 of TMEM: group 0 writes its Q row (query row L mod R, as bf16
+      // pairs along d; rows past the group are zero), each group zeroes its P columns
+      // (each lane later writes only its slice of them).
+      const int L = t & 127;
+      const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+      if (t < 128) {
+        const int h = L % R;
+        const bool live = h < p.n_rows;
+        const uint4* qrow = reinterpret_cast<const uint4*>(
+            reinterpret_cast<const __nv_bfloat16*>(p.q) + q_offset(p, si.b, si.g, live ? h : 0));
+        uint32_t qw[kTcD / 2];                         // the row: 16 loads of 16 bytes
+#pragma unroll
+        for (int c = 0; c < kTcD / 8; ++c) {
+          const uint4 x = live ? qrow[c] : make_uint4(0, 0, 0, 0);
+          qw[4 * c] = x.x;
+          qw[4 * c + 1] = x.y;
+          qw[4 * c + 2] = x.z;
+          qw[4 * c + 3] = x.w;
+        }
+        tc_st32w(tl + kTcQCol, qw);
+        tc_st32w(tl + kTcQCol + 32, qw + 32);
+      }
+      float z[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) z[c] = 0.f;
+      tc_st32(tl + kTcPCol + (uint32_t)(t >> 7) * (kTcTT / 2), z);
+    }
+    tc_fence_before();
+    named_bar_sync(2, kTcThreads - 32);
+    tc_fence_after();
+
+    if (warp == 9 || warp == 10) {    // ---------- score products, even / odd tiles
+      if (lane == 0) issue_scores(p, si, stages, ctl, tmem, warp - 9);
+      __syncwarp();
+    } else if (warp == 11) {          // ---------------- output products
+      if (lane == 0) issue_outputs(p, si, stages, ctl, tmem);
+      __syncwarp();
+    } else {                          // ---------------- softmax
+      if (!softmax_rows<R>(p, si, stages, ctl, tmem, t, m, l) && lane == 0) set_abort(p, ctl);
+    }
   }
   pdl_trigger();
-  tc_fence_before();
-  __syncthreads();                  // ring drained, every product complete
-  tc_fence_after();
 
   if (warp < 8) {
-    const bool bad = aborted(ctl);
-    float* macc = reinterpret_cast<float*>(stages);      // [NPART][R][D] (macc_index)
-    float* mm = macc + kTcSoftThreads * kTcD;             // [NPART][R]
-    float* ml = mm + kTcSoftThreads;                      // [NPART][R]
-    if (!bad) {
-      // Partial state t: group t / 128, slice (t mod 128) / R, row t mod R -- i.e. index
-      // t / R, row t mod R of the merge scratch.  A group without tiles (a one-tile split)
-      // has an O that was never written: it contributes zeros with weight 0.
-      const int h = t % R, part = t / R, grp = t >> 7;
-      const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    // Split epilogue of the softmax warps.  Each group writes its partial states (O from
+    // tensor memory, m, l) into the scratch as soon as it has seen its last product (see
+    // o_state), then all 256 threads merge them.
+    const int h = t % R, part = t / R, grp = t >> 7;
+    const int last_stage = (si.n_tiles - 1) % kTcStages;
+    float* stats = o_stats(stages, last_stage);
+    float* mm = stats;                                       // [NPART][R]: m, then weights
+    float* ml = mm + kTcSoftThreads;                         // [NPART][R]: l
+    float* lrow = ml + kTcSoftThreads;                       // [R]: the row's merged sum
+    if (!aborted(ctl)) {
+      // Partial state t: group t / 128, slice (t mod 128) / R, row t mod R.  A group
+      // without tiles (a one-tile split) has an O that was never written: it
+      // contributes zeros with weight 0.
+      tc_fence_after();
+      const uint32_t tl = ctl->tmem + ((uint32_t)((warp & 3) * 32) << 16) + kTcOCol +
+                          (uint32_t)grp * kTcD;
       const bool has = grp < si.n_tiles;
+      float* mine = o_state<R>(stages, last_stage, part);
 #pragma unroll 1
-      for (int q = 0; q < kTcD / 32; ++q) {
-        float o[32];
+      for (int q = 0; q < 2; ++q) {
+        float o[64];
         if (has) {
-          tc_ld32(tl + kTcOCol + (uint32_t)grp * kTcD + q * 32, o);
+          tc_ld32x2(tl + q * 64, tl + q * 64 + 32, o);
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = 0.f;
+          for (int j = 0; j < 64; ++j) o[j] = 0.f;
         }
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(macc + macc_index<R, kTcD>(part, h, q * 32 + j)) =
+        for (int j = 0; j < 64; j += 4)
+          *reinterpret_cast<float4*>(mine + o_index(h, q * 16 + j / 4)) =
               make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
       }
       mm[t] = m;
       ml[t] = l;
     }
+    tc_fence_before();
     named_bar_sync(1, kTcSoftThreads);
+    const bool bad = aborted(ctl);
     if (bad) {
       write_empty_split(p, si, t);
-    } else if (t < NPART * 32) {
-      merge_warps_and_store<R, kTcD, NPART>(p, si, macc, mm, ml, t, [] {
-        named_bar_sync(3, NPART * 32);
-        return true;
-      });
+    } else {
+      // Weights of a row's NPART partial states, merged as the warps of the mma.sync
+      // kernel are (M = max m, c = 2^(m - M), L = sum c l, O = sum c O_part / L).
+      if (t < p.n_rows) {
+        float M = kNegInf;
+#pragma unroll
+        for (int q = 0; q < NPART; ++q) M = fmaxf(M, mm[q * R + t]);
+        float c[NPART], L = 0.f;
+#pragma unroll
+        for (int q = 0; q < NPART; ++q) {
+          const float mq = mm[q * R + t];
+          c[q] = (M == kNegInf || mq == kNegInf) ? 0.f : ex2(mq - M);
+          L = fmaf(ml[q * R + t], c[q], L);
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+        for (int q = 0; q < NPART; ++q) mm[q * R + t] = c[q] * inv;
+        lrow[t] = L;
+        const int64_t row = flat_row(p, si.b, si.g, t);
+        p.lse_part[row * p.S + si.split] =
+            L > 0.f ? (M + lg2_approx(L)) * 0.6931471805599453f : kNegInf;
+      }
+      named_bar_sync(1, kTcSoftThreads);
+      // All 256 threads write O_i: thread t takes dims 4 (t mod 32) .. + 3 of the rows
+      // t / 32 + 8 k.  Row rho is query token rho / G of head g G + rho mod G (G a power
+      // of two).
+      const int c4 = t & 31;
+      const int lgG = 31 - __clz(p.G);
+      const int64_t ostride = (int64_t)p.S * kTcD;
+      float* obase = p.o_part + (int64_t)si.split * kTcD + c4 * 4;
+#pragma unroll
+      for (int k = 0; k < R / 8; ++k) {
+        const int hr = (t >> 5) + 8 * k;
+        if (hr < p.n_rows && lrow[hr] > 0.f) {        // no key in the split: no O_i
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int q = 0; q < NPART; ++q) {
+            const float f = mm[q * R + hr];
+            const float4 a = *reinterpret_cast<const float4*>(
+                o_state<R>(stages, last_stage, q) + o_index(hr, c4));
+            acc.x = fmaf(a.x, f, acc.x);
+            acc.y = fmaf(a.y, f, acc.y);
+            acc.z = fmaf(a.z, f, acc.z);
+            acc.w = fmaf(a.w, f, acc.w);
+          }
+          const int64_t row = ((int64_t)si.b * p.Q + (hr >> lgG)) * p.Hq +
+                              (int64_t)si.g * p.G + (hr & (p.G - 1));
+          *reinterpret_cast<float4*>(obase + row * ostride) = acc;
+        }
+      }
     }
     if (p.counters != nullptr) arrive_and_merge<kTcD, 8>(p, si, t, &ctl->pipe.last);
   }
   tc_fence_before();
-  __syncthreads();
+  __syncthreads();                  // every role done; every product complete
   if (warp == 0) {
     tc_fence_after();
-    tc_dealloc(tmem, kTcCols);
+    tc_dealloc(ctl->tmem, kTcCols);
   }
 }
 
