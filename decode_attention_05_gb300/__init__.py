@@ -11,7 +11,7 @@ from __future__ import annotations
 from ._binding import (  # noqa: F401
     FD_MERGE_IN_KERNEL, FD_MERGE_KERNEL, FD_PATH_AUTO, FD_PATH_MMA, FD_PATH_SIMT, FD_PATH_TCGEN05,
     FD_FROM_PROCESS, FD_SCHEDULE_AUTO, FD_SCHEDULE_GRID, FD_SCHEDULE_HEAD_GROUPS,
-    FD_SCHEDULE_PERSISTENT, FdError, FdOptions,
+    FD_SCHEDULE_PERSISTENT, FD_SCHEDULE_TAIL_SHARING, FdError, FdOptions,
     Plan, decode_attention, decode_attention_fp8kv, decode_attention_noalloc,
     decode_partial, decode_partial_fp8kv, get_merge_mode, get_path, get_schedule, lib, library_path, merge_partials,
     num_splits_for_lengths, num_splits_heuristic, options, partial_kernel_name, read_device_error,

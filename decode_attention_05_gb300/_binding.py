@@ -16,6 +16,7 @@ FD_F32, FD_BF16, FD_I32, FD_F8E4M3 = 0, 1, 2, 3
 FD_PATH_AUTO, FD_PATH_SIMT, FD_PATH_MMA, FD_PATH_TCGEN05 = 0, 1, 2, 3
 FD_MERGE_KERNEL, FD_MERGE_IN_KERNEL = 0, 1
 FD_SCHEDULE_AUTO, FD_SCHEDULE_GRID, FD_SCHEDULE_PERSISTENT, FD_SCHEDULE_HEAD_GROUPS = 0, 1, 2, 3
+FD_SCHEDULE_TAIL_SHARING = 4
 FD_FROM_PROCESS = -1
 
 _STATUS = {0: "FD_OK", 1: "FD_ERR_INVALID_ARG", 2: "FD_ERR_UNSUPPORTED",

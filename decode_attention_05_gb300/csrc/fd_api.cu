@@ -36,7 +36,7 @@ bool valid_path(int v) {
 bool valid_merge(int v) { return v == FD_MERGE_KERNEL || v == FD_MERGE_IN_KERNEL; }
 bool valid_schedule(int v) {
   return v == FD_SCHEDULE_AUTO || v == FD_SCHEDULE_GRID || v == FD_SCHEDULE_PERSISTENT ||
-         v == FD_SCHEDULE_HEAD_GROUPS;
+         v == FD_SCHEDULE_HEAD_GROUPS || v == FD_SCHEDULE_TAIL_SHARING;
 }
 
 // False if a field holds neither FD_FROM_PROCESS nor one of its enum values.
@@ -51,7 +51,7 @@ bool resolve_settings(const fd_options* o, Settings* s) {
 // and head-group kernels write only partials, so neither runs under the single-launch
 // merge.
 struct Schedule {
-  bool heads, persistent;
+  bool heads, persistent, tail_share;
 };
 
 // rows: query rows per (b, kv head) group (Q x G); groups above kMaxNarrowRows always
@@ -67,6 +67,9 @@ Schedule choose_schedule(int sched, int path, bool kv8, bool f32, int64_t d, int
   sc.heads = head_ok && (sched == FD_SCHEDULE_AUTO || sched == FD_SCHEDULE_HEAD_GROUPS);
   sc.persistent = !sc.heads && path == FD_PATH_MMA && !fused && narrow &&
                   sched == FD_SCHEDULE_PERSISTENT;
+  // Tail sharing: the tcgen05 kernel, when asked for (measured slower than the plain
+  // grid on GB300: the owners' claim round trips cost more than the tail it recovers).
+  sc.tail_share = path == FD_PATH_TCGEN05 && sched == FD_SCHEDULE_TAIL_SHARING;
   return sc;
 }
 
@@ -118,11 +121,13 @@ int esize(int32_t dtype) { return dtype == FD_F8E4M3 ? 1 : (dtype == FD_BF16 ? 2
 
 
 // Workspace regions for given sizes: header | LSE_i [B, Hq, S] |
-// O_i [B, Hq, S, d] | ticket counters [B, Hkv] (64-bit) of the fused merge; each region
-// 256-byte aligned.  The counters need no particular initial contents (take_ticket in
-// fd_epilogue.cuh), so one workspace serves calls of any sizes that fit it.
+// O_i [B, Hq, S, d] | ticket counters [B, Hkv] (64-bit) of the fused merge | claim words
+// [B, Hkv, S] (16 bytes) of tail sharing; each region 256-byte aligned.  Neither the
+// counters nor the claim words need particular initial contents (take_ticket and
+// produce_tiles_shared in fd_pipeline.cuh), so one workspace serves calls of any sizes
+// that fit it.
 struct WsLayout {
-  size_t lse_off, o_off, cnt_off, total;
+  size_t lse_off, o_off, cnt_off, steal_off, total;
 };
 
 WsLayout ws_layout(int64_t B, int64_t Hq, int64_t Hkv, int64_t d, int64_t S) {
@@ -130,7 +135,8 @@ WsLayout ws_layout(int64_t B, int64_t Hq, int64_t Hkv, int64_t d, int64_t S) {
   w.lse_off = kHeaderBytes;
   w.o_off = align_up(w.lse_off + (size_t)(B * Hq * S) * sizeof(float), kAlign);
   w.cnt_off = align_up(w.o_off + (size_t)(B * Hq * S * d) * sizeof(float), kAlign);
-  w.total = align_up(w.cnt_off + (size_t)(B * Hkv) * sizeof(unsigned long long), kAlign);
+  w.steal_off = align_up(w.cnt_off + (size_t)(B * Hkv) * sizeof(unsigned long long), kAlign);
+  w.total = align_up(w.steal_off + (size_t)(B * Hkv * S) * sizeof(fd::StealWord), kAlign);
   return w;
 }
 
@@ -610,6 +616,8 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
 
   p.persistent = persistent ? 1 : 0;
   p.head_group = heads ? fd::kHeadGroup : 0;
+  p.steal = reinterpret_cast<fd::StealWord*>(ws + wl.steal_off);
+  p.tail_share = sc.tail_share ? 1 : 0;
 
   pr->path = path;
   pr->dtype = q->dtype;

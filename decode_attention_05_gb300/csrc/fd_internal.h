@@ -23,6 +23,15 @@ constexpr int kTileBytes = 16384;
 // kv heads per CTA (and per TMA box) in the head-group tiling; one per consumer warp
 constexpr int kHeadGroup = 4;
 
+// Claim word of one work item (b, kv head, split) for tail sharing, in the workspace:
+// claim = back << 32 | front, the item's tiles [front, back) that nobody has claimed yet;
+// epoch = the call that opened it (its owner writes the claim, then the epoch).
+struct StealWord {
+  unsigned long long claim;
+  uint32_t epoch;
+  uint32_t pad;
+};
+
 // Everything one decode call needs on the device, resolved by the host planner.
 struct Params {
   // sizes
@@ -58,6 +67,10 @@ struct Params {
   int32_t head_group;
   unsigned long long* item_queue;
   unsigned long long* ctas_done;
+  // Tail sharing: claim words [B, Hkv, S] of the items (see fd_pipeline.cuh), and
+  // whether this launch shares (0: every CTA streams exactly its own split)
+  StealWord* steal;
+  int32_t tail_share;
   float* lse_part;        // [B, Q, Hq, S]     natural-log LSE_i, -inf for an empty split
   float* o_part;          // [B, Q, Hq, S, d]  normalised partial output O_i
   // outputs

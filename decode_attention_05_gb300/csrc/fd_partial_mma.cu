@@ -38,6 +38,14 @@ namespace {
 // for all rows.
 // F32: q, K and V stored as f32, multiplied on the tensor cores as three TF32 products
 // (see split_tf32), for groups of up to 8 rows.
+// Tiles of its split a CTA prefetches into L2 before it may read its inputs
+// (prefetch_first_tiles), and how many tiles before the end of its loop the consumers
+// let the next kernel of the stream launch.  Measured on the 128K GQA workload (graphs
+// of back-to-back steps): no prefetch 78.5 us, 4 tiles 75.5 us, 8 tiles 75.0 us,
+// 12 tiles 76.1 us; the early trigger helps the short MHA step (40.1 -> 38.8 us).
+constexpr int kPrefetchTiles = 8;
+constexpr int kTriggerTiles = 4;
+
 template <int D_, int G_, bool KV8_ = false, bool PERSIST_ = false, bool WIDE_ = false,
           bool F32_ = false>
 struct MmaShape {
@@ -638,6 +646,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
                           const __grid_constant__ CUtensorMap tv,
                           const __grid_constant__ Params p) {
   constexpr int G = SH::G, TT = SH::TT, STAGES = SH::STAGES;
+  if (threadIdx.x == SH::NCW * 32) prefetch_first_tiles<TT>(p, &tk, &tv, kPrefetchTiles);
   pdl_wait();                       // inputs of this step are visible
   const SplitInfo si = split_info<TT>(p);
   extern __shared__ uint8_t smem_raw[];
@@ -677,7 +686,12 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   const bool multi_page = p.page_size > 0 && p.page_size < TT;
   const uint32_t lb = (uint32_t)p.log2_box;
   bool aborted = false;
-  for (int n = 0; n < si.n_tiles; ++n) {
+  // The next kernel of the stream may launch once kTriggerTiles tiles are left: its CTAs
+  // take free slots and prefetch their first tiles while this split finishes.
+  const int trigger_at = si.n_tiles > kTriggerTiles ? si.n_tiles - kTriggerTiles : 0;
+  int n = 0;
+  for (; n < si.n_tiles; ++n) {
+    if (n == trigger_at) pdl_trigger();
     const int stage = n % STAGES;
     int ok = 1;
     if (lane == 0) ok = mbar_wait(smem_addr(&ctl->full[stage]), (n / STAGES) & 1);
@@ -696,7 +710,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
   }
-  pdl_trigger();
+  if (n < trigger_at) pdl_trigger();    // the loop ended before the trigger (an abort)
 
   named_bar_sync(1, SH::NCW * 32);
   if (aborted || *reinterpret_cast<volatile int32_t*>(&ctl->abort)) {
@@ -731,6 +745,7 @@ __global__ void __maxnreg__(200)
                            const __grid_constant__ Params p) {
   constexpr int TT = SH::TT, STAGES = SH::STAGES;
   static_assert(SH::WIDE, "wide shape");
+  if (threadIdx.x == SH::NCW * 32) prefetch_first_tiles<TT>(p, &tk, &tv, kPrefetchTiles);
   pdl_wait();                       // inputs of this step are visible
   const SplitInfo si = split_info<TT>(p);
   extern __shared__ uint8_t smem_raw[];

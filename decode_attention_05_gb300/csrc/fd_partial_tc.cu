@@ -261,6 +261,11 @@ __device__ __forceinline__ bool wait_or_abort(TcCtl* ctl, uint32_t bar, uint32_t
   return true;
 }
 
+// Whether ring slot n (landed) carries the end of the tile sequence rather than a tile.
+__device__ __forceinline__ bool tile_done(TcCtl* ctl, int n) {
+  return *reinterpret_cast<volatile int32_t*>(&ctl->pipe.done[n % kTcStages]) != 0;
+}
+
 // The products are issued by three threads in three warps: two issue the scores
 // S(j) = Q K(j)^T of the even and of the odd tiles, each as soon as tile j has landed
 // and its S buffer has been read (the softmax of tile j - 2); the third issues the
@@ -277,9 +282,13 @@ __device__ void issue_scores(const Params& p, const SplitInfo& si, uint8_t* stag
   const uint32_t box_bytes = 2u * (uint32_t)box * 128u;  // [line][row][128 B], 2 lines
   const uint32_t id_s = instr_desc(128, box, 0);
   bool ok = true;
-  for (int j = parity; j < si.n_tiles; j += 2) {
-    if (!wait_or_abort(ctl, smem_addr(&ctl->pipe.full[j % kTcStages]), (j / kTcStages) & 1) ||
-        (j >= 2 && !wait_or_abort(ctl, smem_addr(&ctl->s_free[j & 1]), ((j >> 1) - 1) & 1))) {
+  for (int j = parity;; j += 2) {
+    if (!wait_or_abort(ctl, smem_addr(&ctl->pipe.full[j % kTcStages]), (j / kTcStages) & 1)) {
+      ok = false;
+      break;
+    }
+    if (tile_done(ctl, j)) break;           // no tile j: the sequence has ended
+    if (j >= 2 && !wait_or_abort(ctl, smem_addr(&ctl->s_free[j & 1]), ((j >> 1) - 1) & 1)) {
       ok = false;
       break;
     }
@@ -307,7 +316,12 @@ __device__ void issue_outputs(const Params& p, const SplitInfo& si, uint8_t* sta
   const uint32_t box_bytes = 2u * (uint32_t)box * 128u;
   const uint32_t id_pv = instr_desc(128, kTcD, 1);
   bool ok = true;
-  for (int n = 0; n < si.n_tiles; ++n) {
+  for (int n = 0;; ++n) {
+    if (!wait_or_abort(ctl, smem_addr(&ctl->pipe.full[n % kTcStages]), (n / kTcStages) & 1)) {
+      ok = false;
+      break;
+    }
+    if (tile_done(ctl, n)) break;           // no tile n: the sequence has ended
     if (!wait_or_abort(ctl, smem_addr(&ctl->p_full[n & 1]), (n >> 1) & 1)) {
       ok = false;
       break;
@@ -338,7 +352,8 @@ __device__ void issue_outputs(const Params& p, const SplitInfo& si, uint8_t* sta
 // Returns false if a bounded wait gave up.
 template <int R>
 __device__ bool softmax_rows(const Params& p, const SplitInfo& si, uint8_t* stages,
-                             TcCtl* ctl, uint32_t tmem, int t, float& m_out, float& l_out) {
+                             TcCtl* ctl, uint32_t tmem, int t, float& m_out, float& l_out,
+                             int& n_total) {
   constexpr int SLICE = kTcTT * R / 128;             // tokens of a tile per lane: 32 or 16
   const int grp = t >> 7, tg = t & 127;
   const int warp = tg >> 5, lane = t & 31;
@@ -352,10 +367,17 @@ __device__ bool softmax_rows(const Params& p, const SplitInfo& si, uint8_t* stag
   const uint32_t ocol = kTcOCol + (uint32_t)grp * kTcD;
   const uint32_t pcol = kTcPCol + (uint32_t)grp * (kTcTT / 2) + (uint32_t)(j0 / 2);
   float m = kNegInf, l = 0.f;
-  for (int n = grp; n < si.n_tiles; n += 2) {
+  int last = -1;                                     // the group's last tile
+  for (int n = grp;; n += 2) {
     const int st = n % kTcStages;
-    // The tile has landed (for its page-validity bits) and its scores are complete.
+    // The tile has landed (for its range and page-validity bits) and its scores are
+    // complete -- or the slot carries the end of the sequence.
     if (!warp_wait(smem_addr(&ctl->pipe.full[st]), (n / kTcStages) & 1, lane)) return false;
+    if (tile_done(ctl, n)) {
+      n_total = *reinterpret_cast<volatile int32_t*>(&ctl->pipe.n_total);
+      break;
+    }
+    last = n;
     if (!warp_wait(smem_addr(&ctl->s_full[n & 1]), (n >> 1) & 1, lane)) return false;
     tc_fence_after();
     float s[SLICE];
@@ -365,9 +387,11 @@ __device__ bool softmax_rows(const Params& p, const SplitInfo& si, uint8_t* stag
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&ctl->s_free[n & 1]));
 
-    const int64_t t0 = si.T0 + (int64_t)n * kTcTT;
+    // The tile's first token and the valid range of the split it belongs to (its own
+    // split, or one it took from, with tail sharing).
+    const int64_t t0 = ctl->pipe.t0[st], lo = ctl->pipe.lo[st], hi = ctl->pipe.hi[st];
     const uint32_t bad = ctl->pipe.bad[st];
-    const bool clean = t0 >= si.lo && t0 + kTcTT <= si.hi && bad == 0;
+    const bool clean = t0 >= lo && t0 + kTcTT <= hi && bad == 0;
     float mt = kNegInf;
     if (clean && t0 + j0 + SLICE <= kb) {
 #pragma unroll
@@ -380,7 +404,7 @@ __device__ bool softmax_rows(const Params& p, const SplitInfo& si, uint8_t* stag
       for (int j = 0; j < SLICE; ++j) {
         const int64_t tok = t0 + j0 + j;
         const int pslot = multi_page ? ((j0 + j) >> p.log2_page) : 0;
-        const bool valid = tok >= si.lo && tok < si.hi && !((bad >> pslot) & 1u) && tok < kb;
+        const bool valid = tok >= lo && tok < hi && !((bad >> pslot) & 1u) && tok < kb;
         s[j] = valid ? s[j] * sl2 : kNegInf;
         mt = fmaxf(mt, s[j]);
       }
@@ -425,7 +449,7 @@ __device__ bool softmax_rows(const Params& p, const SplitInfo& si, uint8_t* stag
     if (!clean && tg < kTcTT) {
       const int64_t tok = t0 + tg;
       const int pslot = multi_page ? (tg >> p.log2_page) : 0;
-      if (!(tok >= si.lo && tok < si.hi && !((bad >> pslot) & 1u))) {
+      if (!(tok >= lo && tok < hi && !((bad >> pslot) & 1u))) {
         uint8_t* vt = stages + (size_t)st * 2 * kTileBytes + kTileBytes;
 #pragma unroll
         for (int c16 = 0; c16 < kTcD * 2 / 16; ++c16)
@@ -438,7 +462,6 @@ __device__ bool softmax_rows(const Params& p, const SplitInfo& si, uint8_t* stag
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&ctl->p_full[n & 1]));   // one per softmax warp
   }
-  const int last = si.n_tiles - 1 - ((si.n_tiles - 1 - grp) & 1);   // group's last tile
   if (last >= 0 && !warp_wait(smem_addr(&ctl->pv_done[grp]), (last >> 1) & 1, lane))
     return false;
   m_out = m;
@@ -482,6 +505,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   static_assert(R == 32 || R == 64, "32 or 64 query rows");
   constexpr int DUP = 128 / R;      // token slices (copies of each query row) per group
   constexpr int NPART = 2 * DUP;    // partial states per query row
+  // The first ring's worth of tiles into L2 before the wait (prefetch_first_tiles;
+  // measured best at the ring depth: 6 tiles 86.5 us, 8 tiles 86.8 us, none 88.9 us at
+  // 8 query tokens on the 128K GQA workload).
+  if (threadIdx.x == 8 * 32) prefetch_first_tiles<kTcTT>(p, &tk, &tv, kTcStages);
   pdl_wait();                       // inputs of this step are visible
   const SplitInfo si = split_info<kTcTT>(p);
   extern __shared__ uint8_t smem_raw[];
@@ -510,15 +537,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(smem_addr(&ctl->mma_done), 3);
     ctl->pipe.abort = 0;
+    ctl->pipe.n_total = 0;
     fence_mbar_init();
   }
   __syncthreads();                  // barriers initialised
 
   float m = kNegInf, l = 0.f;
+  int n_total = 0;                  // tiles this CTA streamed (softmax warps)
   if (warp == 8) {                  // ---------------- TMA producer, from the start: the
     prefetch_tensormap(&tk);        // first tiles load while the other warps set up
     prefetch_tensormap(&tv);
-    produce_tiles<kTcTT, kTcStages>(p, si, &tk, &tv, stages, &ctl->pipe, lane);
+    produce_tiles_shared<kTcTT, kTcStages>(p, si, &tk, &tv, stages, &ctl->pipe, lane,
+                                           p.tail_share != 0);
   } else {
     // Set-up of the MMA operands (every warp but the producer): tensor memory, Q and the
     // zeroed P columns.
@@ -569,7 +599,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) issue_outputs(p, si, stages, ctl, tmem);
       __syncwarp();
     } else {                          // ---------------- softmax
-      if (!softmax_rows<R>(p, si, stages, ctl, tmem, t, m, l) && lane == 0) set_abort(p, ctl);
+      if (!softmax_rows<R>(p, si, stages, ctl, tmem, t, m, l, n_total) && lane == 0)
+        set_abort(p, ctl);
     }
   }
   pdl_trigger();
@@ -579,7 +610,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // tensor memory, m, l) into the scratch as soon as it has seen its last product (see
     // o_state), then all 256 threads merge them.
     const int h = t % R, part = t / R, grp = t >> 7;
-    const int last_stage = (si.n_tiles - 1) % kTcStages;
+    const int last_stage = (max(n_total, 1) - 1) % kTcStages;
     float* stats = o_stats(stages, last_stage);
     float* mm = stats;                                       // [NPART][R]: m, then weights
     float* ml = mm + kTcSoftThreads;                         // [NPART][R]: l
@@ -591,7 +622,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       const uint32_t tl = ctl->tmem + ((uint32_t)((warp & 3) * 32) << 16) + kTcOCol +
                           (uint32_t)grp * kTcD;
-      const bool has = grp < si.n_tiles;
+      const bool has = grp < n_total;
       float* mine = o_state<R>(stages, last_stage, part);
 #pragma unroll 1
       for (int q = 0; q < 2; ++q) {

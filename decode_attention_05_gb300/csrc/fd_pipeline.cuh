@@ -52,6 +52,37 @@ __device__ __forceinline__ SplitInfo split_info(const Params& p) {
   return si;
 }
 
+// L2 prefetch of the first `count` tiles of this CTA's split (contiguous caches; grid
+// blockIdx = (split, kv head, batch row)), issued BEFORE griddepcontrol.wait.  Where a
+// split starts depends only on the launch's sizes (split_len, L_cap), and a prefetch is
+// only a hint: L2 is the point of coherence, so the loads after the wait still see
+// whatever the previous kernel of the stream wrote.  The row's length, which that kernel
+// may still be changing, is read relaxed and only bounds how much is prefetched (a
+// split past it prefetches nothing).  A CTA that becomes resident while the previous
+// decode step finishes (programmatic dependent launch) thus has its first tiles on the
+// way to L2 before it may read them, and the tail of the previous step's bandwidth is
+// not left idle.
+__device__ __forceinline__ int32_t ld_relaxed_s32(const int32_t* a) {
+  int32_t v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+template <int TT>
+__device__ __forceinline__ void prefetch_first_tiles(const Params& p, const CUtensorMap* tk,
+                                                     const CUtensorMap* tv, int count) {
+  if (p.block_table != nullptr) return;
+  const int64_t L = min((int64_t)ld_relaxed_s32(p.seq_lens + blockIdx.z), p.L_cap);
+  const int64_t lo = (int64_t)blockIdx.x * p.split_len;
+  const int64_t hi = min(lo + p.split_len, L);
+  const int64_t T0 = lo / TT * TT;
+  for (int k = 0; k < count; ++k) {
+    const int64_t t0 = T0 + (int64_t)k * TT;
+    if (t0 >= hi) break;
+    tma_prefetch_5d(tk, 0, (int)t0, 0, (int)blockIdx.y, (int)blockIdx.z);
+    tma_prefetch_5d(tv, 0, (int)t0, 0, (int)blockIdx.y, (int)blockIdx.z);
+  }
+}
+
 // Query rows of a (b, kv head) group: row rho (0 .. Q * G - 1) is query token j = rho / G
 // of head h = rho mod G.  Its flat index over [B, Q, Hq] (partials, lse_out), its query
 // vector, and its causal key bound: the Q query tokens are the last Q positions of the
@@ -98,6 +129,12 @@ struct PipeCtl {
   uint64_t full[STAGES];    // TMA bytes landed (count 1 + transaction bytes)
   uint64_t empty[STAGES];   // consumers released the stage (count = consumer warps)
   uint32_t bad[STAGES];     // bit j: page slot j of the tile had an invalid page id
+  // Tile descriptors published by produce_tiles_shared with each stage: the tile's first
+  // logical token, the valid range [lo, hi) of the split it belongs to, and done = 1 for
+  // a stage that carries no tile but the end of the sequence (n_total tiles in all).
+  int64_t t0[STAGES], lo[STAGES], hi[STAGES];
+  int32_t done[STAGES];
+  int32_t n_total;
   int32_t abort;            // a bounded wait gave up
   int32_t last;             // this CTA drew its group's last ticket (fused merge)
 };
@@ -274,93 +311,99 @@ __device__ __forceinline__ void produce_items(const Params& p, const CUtensorMap
   }
 }
 
-// Producer warp: streams tiles 0..n_tiles-1 of the split.  All 32 lanes run the loop
-// (they share the page-id cache); lane 0 issues the copies.
+// Page-id window of a producer warp (paged caches): lane i holds the block-table entry
+// of page (base + i) of the row, or -2 when that page holds no token of the row (never
+// read from the table).
+struct PageWindow {
+  int64_t base = -64;            // no window loaded yet
+  int32_t id = -2;
+};
+
+// Issue the K and V copies of the tile whose first logical token is t0 (row si.b, kv
+// head si.g) into `stage`, completing on its full barrier.  All 32 lanes resolve page
+// ids (they share the window); lane 0 records the invalid-page bits and issues.
 //   stages: base of STAGES * 2 * kTileBytes bytes, 1024-byte aligned; stage s holds the
 //           K tile at s * 2 * kTileBytes and the V tile kTileBytes after it.  A tile is
 //           one TMA box (contiguous cache, or pages of at least a tile) or one box per
 //           page; each box is laid out [line][row][128 B] (see tile_chunk), 128-byte
 //           swizzled, and 1024-byte aligned (a box is at least 8 rows).
 template <int TT, int STAGES>
-__device__ __forceinline__ void produce_tiles(const Params& p, const SplitInfo& si,
-                                              const CUtensorMap* tk, const CUtensorMap* tv,
-                                              uint8_t* stages, PipeCtl<STAGES>* ctl,
-                                              int lane) {
-  const uint64_t pol = policy_evict_first();
+__device__ __forceinline__ void issue_tile(const Params& p, const SplitInfo& si, int64_t t0,
+                                           const CUtensorMap* tk, const CUtensorMap* tv,
+                                           uint8_t* stages, PipeCtl<STAGES>* ctl, int stage,
+                                           PageWindow& win, uint64_t pol, int lane) {
   const bool paged = p.block_table != nullptr;
   const int ps = p.page_size;
   const int pages_per_tile = paged ? (ps >= TT ? 1 : TT / ps) : 1;
   const int box_rows = paged ? (ps >= TT ? TT : ps) : TT;
   const uint32_t box_bytes = (uint32_t)(kTileBytes / TT) * box_rows;   // all lines of a box
-  // Page-id cache: lane i holds the table entry of page (cache_base + i), or -2 when
-  // that page holds no token of the row (never read from the table).
-  int64_t cache_base = -64;      // no window loaded yet
-  int32_t cache = -2;
-  int n = 0;
-  for (; n < si.n_tiles; ++n) {
-    const int stage = n % STAGES;
-    if (n >= STAGES) {
-      // Lane 0 waits and tells the warp, so the lanes never disagree about leaving.
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(smem_addr(&ctl->empty[stage]), ((n / STAGES) - 1) & 1);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        if (lane == 0) {
-          ctl->abort = 1;
-          atomicOr(p.flags, kDevFlagTimeout);
-        }
-        break;
+  uint32_t bad = 0;
+  int32_t pid[16];  // pages_per_tile <= TT / 8 <= 16 (page_size >= 8 is enforced)
+  if (paged) {
+    const int64_t pi0 = t0 >> p.log2_page;
+    for (int j = 0; j < pages_per_tile; ++j) {
+      const int64_t pi = pi0 + j;
+      if (pi < win.base || pi >= win.base + 32) {             // warp-uniform refill
+        win.base = pi;
+        const int64_t mine = pi + lane;
+        win.id = mine < si.used_pages ? p.block_table[(int64_t)si.b * p.bt_sb + mine] : -2;
       }
-    }
-    if (__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int32_t*>(&ctl->abort), 0)) break;
-    const int64_t t0 = si.T0 + (int64_t)n * TT;
-    uint32_t bad = 0;
-    int32_t pid[16];  // pages_per_tile <= TT / 8 <= 16 (page_size >= 8 is enforced)
-    if (paged) {
-      const int64_t pi0 = t0 >> p.log2_page;
-      for (int j = 0; j < pages_per_tile; ++j) {
-        const int64_t pi = pi0 + j;
-        if (pi < cache_base || pi >= cache_base + 32) {          // warp-uniform refill
-          cache_base = pi;
-          const int64_t mine = pi + lane;
-          cache = mine < si.used_pages ? p.block_table[(int64_t)si.b * p.bt_sb + mine] : -2;
-        }
-        int32_t id = __shfl_sync(0xffffffffu, cache, (int)(pi - cache_base));
-        if (id == -2) {
-          id = 0;                          // no token of the row here: any valid page
-        } else if (id < 0 || (int64_t)id >= p.num_pages) {
-          bad |= 1u << j;                  // a used entry out of range: exclude its tokens
-          id = 0;
-        }
-        pid[j] = id;
+      int32_t id = __shfl_sync(0xffffffffu, win.id, (int)(pi - win.base));
+      if (id == -2) {
+        id = 0;                          // no token of the row here: any valid page
+      } else if (id < 0 || (int64_t)id >= p.num_pages) {
+        bad |= 1u << j;                  // a used entry out of range: exclude its tokens
+        id = 0;
       }
-      if (bad && lane == 0) atomicOr(p.flags, FD_DEVFLAG_PAGE);
+      pid[j] = id;
     }
-    if (lane == 0) {
-      ctl->bad[stage] = bad;
-      const uint32_t full = smem_addr(&ctl->full[stage]);
-      mbar_arrive_expect_tx(full, 2u * kTileBytes);
-      const uint32_t dk = smem_addr(stages + (size_t)stage * 2 * kTileBytes);
-      const uint32_t dv = dk + kTileBytes;
-      // Coordinates: {element 0, token row, line 0, kv head, batch row | page}.
-      if (!paged) {
-        tma_load_5d(dk, tk, full, 0, (int)t0, 0, si.g, si.b, pol);
-        tma_load_5d(dv, tv, full, 0, (int)t0, 0, si.g, si.b, pol);
-      } else if (ps >= TT) {
-        const int slot = (int)(t0 & (ps - 1));
-        tma_load_5d(dk, tk, full, 0, slot, 0, si.g, pid[0], pol);
-        tma_load_5d(dv, tv, full, 0, slot, 0, si.g, pid[0], pol);
-      } else {
-        for (int j = 0; j < pages_per_tile; ++j) {
-          tma_load_5d(dk + j * box_bytes, tk, full, 0, 0, 0, si.g, pid[j], pol);
-          tma_load_5d(dv + j * box_bytes, tv, full, 0, 0, 0, si.g, pid[j], pol);
-        }
-      }
-    }
-    __syncwarp();
+    if (bad && lane == 0) atomicOr(p.flags, FD_DEVFLAG_PAGE);
   }
-  // Never leave with copies in flight: wait (bounded) for the last issued tile of each
-  // stage.  Earlier tiles of a stage completed before the stage was reused.
+  if (lane == 0) {
+    ctl->bad[stage] = bad;
+    const uint32_t full = smem_addr(&ctl->full[stage]);
+    mbar_arrive_expect_tx(full, 2u * kTileBytes);
+    const uint32_t dk = smem_addr(stages + (size_t)stage * 2 * kTileBytes);
+    const uint32_t dv = dk + kTileBytes;
+    // Coordinates: {element 0, token row, line 0, kv head, batch row | page}.
+    if (!paged) {
+      tma_load_5d(dk, tk, full, 0, (int)t0, 0, si.g, si.b, pol);
+      tma_load_5d(dv, tv, full, 0, (int)t0, 0, si.g, si.b, pol);
+    } else if (ps >= TT) {
+      const int slot = (int)(t0 & (ps - 1));
+      tma_load_5d(dk, tk, full, 0, slot, 0, si.g, pid[0], pol);
+      tma_load_5d(dv, tv, full, 0, slot, 0, si.g, pid[0], pol);
+    } else {
+      for (int j = 0; j < pages_per_tile; ++j) {
+        tma_load_5d(dk + j * box_bytes, tk, full, 0, 0, 0, si.g, pid[j], pol);
+        tma_load_5d(dv + j * box_bytes, tv, full, 0, 0, 0, si.g, pid[j], pol);
+      }
+    }
+  }
+}
+
+// Acquire ring slot n for the producer warp: wait (lane 0, bounded) until the consumers
+// have released the tile that used the stage before; on a timeout the split is aborted
+// and flagged.  Every lane returns the same answer.
+template <int STAGES>
+__device__ __forceinline__ bool acquire_slot(const Params& p, PipeCtl<STAGES>* ctl, int n,
+                                             int lane) {
+  if (n < STAGES) return true;
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(smem_addr(&ctl->empty[n % STAGES]), ((n / STAGES) - 1) & 1);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok && lane == 0) {
+    ctl->abort = 1;
+    atomicOr(p.flags, kDevFlagTimeout);
+  }
+  return ok != 0;
+}
+
+// Never leave with copies in flight: wait (bounded) for the last issued use of each
+// stage (n slots issued in all).  Earlier uses of a stage completed before it was reused.
+template <int STAGES>
+__device__ __forceinline__ void drain_ring(const Params& p, PipeCtl<STAGES>* ctl, int n,
+                                           int lane) {
   if (lane == 0) {
     const int first = n > STAGES ? n - STAGES : 0;
     for (int m = first; m < n; ++m) {
@@ -369,6 +412,232 @@ __device__ __forceinline__ void produce_tiles(const Params& p, const SplitInfo& 
       }
     }
   }
+}
+
+// Producer warp: streams tiles 0..n_tiles-1 of the split.  All 32 lanes run the loop
+// (they share the page-id window); lane 0 issues the copies.
+template <int TT, int STAGES>
+__device__ __forceinline__ void produce_tiles(const Params& p, const SplitInfo& si,
+                                              const CUtensorMap* tk, const CUtensorMap* tv,
+                                              uint8_t* stages, PipeCtl<STAGES>* ctl,
+                                              int lane) {
+  const uint64_t pol = policy_evict_first();
+  PageWindow win;
+  int n = 0;
+  for (; n < si.n_tiles; ++n) {
+    if (!acquire_slot(p, ctl, n, lane)) break;
+    if (__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int32_t*>(&ctl->abort), 0)) break;
+    issue_tile<TT, STAGES>(p, si, si.T0 + (int64_t)n * TT, tk, tv, stages, ctl, n % STAGES,
+                           win, pol, lane);
+    __syncwarp();
+  }
+  drain_ring(p, ctl, n, lane);
+}
+
+// ---------------------------------------------------------------- tail sharing
+//
+// CTAs stream at rates that differ by a few percent (which memory channels their
+// addresses hit), so with one split per CTA the last splits finish well after the
+// average one.  Tail sharing lets a CTA that has finished its own split continue with
+// tiles of a split of the SAME (b, kv head) that is still in progress: same query rows,
+// so the extra keys simply join the helper's own running maximum, sum and accumulator,
+// and its partial (O_i, LSE_i) then covers its split plus the stolen tiles.  Every key
+// is still counted exactly once over the row's partials, and the LSE-weighted merge of
+// "2kiu.com/news/6053916" (section "weight block results with log-sum-exp") is exact
+// whatever keys each partial holds.  Each CTA's stream stays contiguous: the owner takes
+// its tiles from the front of its split in chunks of kClaimChunk (fetch-and-add on the
+// split's claim word), a helper takes the back half of the largest unclaimed remainder
+// (compare-and-swap), so no address interleaving between CTAs arises.
+constexpr uint32_t kClaimChunk = 2;   // tiles an owner claims at a time
+constexpr int kClaimAhead = 2;        // an owner's claims in flight
+constexpr uint32_t kMinSteal = 2;     // a helper takes half of at least this many tiles
+
+__device__ __forceinline__ unsigned long long claim_pack(uint32_t front, uint32_t back) {
+  return ((unsigned long long)back << 32) | front;
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* a) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* a) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t* a, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
+// The split of the helper's (b, kv head) group with the most unclaimed tiles (at least
+// kMinSteal), whose back half the helper then claims.  Only splits whose owner has
+// published this call's epoch are considered.  On success the piece is tiles [cur, end)
+// of that split (relative to its first tile T0) with valid range [lo, hi).  Bounded: a
+// lost compare-and-swap is retried a fixed number of times.
+template <int TT>
+__device__ __forceinline__ bool steal_piece(const Params& p, const SplitInfo& si,
+                                            StealWord* group, int lane, int64_t& T0,
+                                            int64_t& lo, int64_t& hi, uint32_t& cur,
+                                            uint32_t& end) {
+  for (int attempt = 0; attempt < 64; ++attempt) {
+    uint32_t best_rem = 0;
+    int best = -1;
+    unsigned long long best_w = 0;
+    for (int s = lane; s < p.S; s += 32) {
+      if (ld_acquire_u32(&group[s].epoch) != p.epoch) continue;
+      const unsigned long long w = ld_relaxed_u64(&group[s].claim);
+      const uint32_t f = (uint32_t)w, bk = (uint32_t)(w >> 32);
+      const uint32_t rem = bk > f ? bk - f : 0u;
+      if (rem > best_rem) {
+        best_rem = rem;
+        best = s;
+        best_w = w;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {      // arg-max over (remainder, split)
+      const uint32_t r2 = __shfl_xor_sync(0xffffffffu, best_rem, off);
+      const int s2 = __shfl_xor_sync(0xffffffffu, best, off);
+      const unsigned long long w2 = __shfl_xor_sync(0xffffffffu, best_w, off);
+      if (r2 > best_rem || (r2 == best_rem && s2 > best)) {
+        best_rem = r2;
+        best = s2;
+        best_w = w2;
+      }
+    }
+    if (best_rem < kMinSteal) return false;
+    const uint32_t f = (uint32_t)best_w, bk = (uint32_t)(best_w >> 32);
+    const uint32_t k = best_rem / 2;
+    int ok = 0;
+    if (lane == 0) ok = atomicCAS(&group[best].claim, best_w, claim_pack(f, bk - k)) == best_w;
+    if (__shfl_sync(0xffffffffu, ok, 0)) {
+      lo = (int64_t)best * p.split_len;
+      hi = min(lo + p.split_len, si.L);
+      T0 = lo / TT * TT;
+      cur = bk - k;
+      end = bk;
+      return true;
+    }
+  }
+  return false;
+}
+
+// One fetch-and-add claim of kClaimChunk tiles on an owner's word, into ticket slot
+// `slot` (lane 0; the tickets live in separate registers that are never copied, so a
+// claim in flight stalls nothing until its own slot is read).
+__device__ __forceinline__ void claim_into(int slot, unsigned long long* word,
+                                           unsigned long long& t0, unsigned long long& t1,
+                                           unsigned long long& t2) {
+  const unsigned long long add = (unsigned long long)kClaimChunk;
+  if (slot == 0) t0 = atomicAdd(word, add);
+  else if (slot == 1) t1 = atomicAdd(word, add);
+  else t2 = atomicAdd(word, add);
+}
+__device__ __forceinline__ unsigned long long ticket_of(int slot, unsigned long long t0,
+                                                        unsigned long long t1,
+                                                        unsigned long long t2) {
+  return __shfl_sync(0xffffffffu, slot == 0 ? t0 : (slot == 1 ? t1 : t2), 0);
+}
+
+// Producer warp of the kernels whose consumers read the tile descriptors (t0, lo, hi,
+// done) of each stage: streams the CTA's own split and, with `share`, tiles taken from
+// other splits of the same (b, kv head) afterwards (see above); then publishes two done
+// stages (one for each tile parity: some consumers take every other tile) carrying
+// n_total.  Without `share` the sequence is exactly the split's tiles, in order.
+// The owner keeps kClaimAhead claims in flight, so their round trips stay off its path
+// while it streams; a helper looks for a piece when the current one is exhausted (the
+// ring still holds the tiles it has issued).
+template <int TT, int STAGES>
+__device__ __forceinline__ void produce_tiles_shared(const Params& p, const SplitInfo& si,
+                                                     const CUtensorMap* tk,
+                                                     const CUtensorMap* tv, uint8_t* stages,
+                                                     PipeCtl<STAGES>* ctl, int lane,
+                                                     bool share) {
+  static_assert(kClaimAhead >= 1 && kClaimAhead <= 3, "one to three claims in flight");
+  const uint64_t pol = policy_evict_first();
+  PageWindow win;
+  const uint32_t n_own = (uint32_t)si.n_tiles;
+  StealWord* group = share ? p.steal + ((int64_t)si.b * p.Hkv + si.g) * p.S : nullptr;
+  StealWord* mine = share ? group + si.split : nullptr;
+  // The piece being streamed: tiles [cur, end) of a split whose first tile starts at
+  // logical token T0, valid range [lo, hi).  First the own split.
+  int64_t T0 = si.T0, lo = si.lo, hi = si.hi;
+  uint32_t cur = 0, end = share ? min(kClaimChunk, n_own) : n_own;
+  // Own claims in flight: ticket slots used round robin, oldest at `head`.
+  unsigned long long t0r = 0, t1r = 0, t2r = 0;
+  int head = 0, live = 0;
+  uint32_t next_f = end;                   // the front the next claim is expected to see
+  bool own = true;
+  if (share) {
+    if (lane == 0) {
+      // Publish the split's unclaimed range [end, n_own); the epoch (written last) tells
+      // helpers that the word belongs to this call.
+      atomicExch(&mine->claim, claim_pack(end, n_own));
+      __threadfence();
+      st_release_u32(&mine->epoch, p.epoch);
+    }
+    for (; next_f < n_own && live < kClaimAhead; next_f += kClaimChunk, ++live) {
+      if (lane == 0) claim_into((head + live) % kClaimAhead, &mine->claim, t0r, t1r, t2r);
+    }
+  }
+  int n = 0;
+  bool aborted = false;
+  for (;;) {
+    if (cur >= end && own && live > 0) {       // the next chunk of the own split
+      const unsigned long long old = ticket_of(head, t0r, t1r, t2r);
+      const uint32_t f = (uint32_t)old, bk = (uint32_t)(old >> 32);
+      head = (head + 1) % kClaimAhead;
+      --live;
+      cur = f;
+      end = f < bk ? min(f + kClaimChunk, bk) : f;
+      if (end >= bk) {
+        live = 0;                              // the rest come back empty
+      } else if (next_f < bk) {
+        if (lane == 0) claim_into((head + live) % kClaimAhead, &mine->claim, t0r, t1r, t2r);
+        ++live;
+        next_f += kClaimChunk;
+      }
+    }
+    if (cur >= end) {                          // the current piece is exhausted
+      own = false;
+      if (!share || !steal_piece<TT>(p, si, group, lane, T0, lo, hi, cur, end)) break;
+    }
+    if (!acquire_slot(p, ctl, n, lane) ||
+        __shfl_sync(0xffffffffu, *reinterpret_cast<volatile int32_t*>(&ctl->abort), 0)) {
+      aborted = true;
+      break;
+    }
+    const int stage = n % STAGES;
+    const int64_t t0 = T0 + (int64_t)cur * TT;
+    if (lane == 0) {
+      ctl->t0[stage] = t0;
+      ctl->lo[stage] = lo;
+      ctl->hi[stage] = hi;
+      ctl->done[stage] = 0;
+    }
+    issue_tile<TT, STAGES>(p, si, t0, tk, tv, stages, ctl, stage, win, pol, lane);
+    __syncwarp();
+    ++cur;
+    ++n;
+  }
+  const int n_total = n;
+  if (!aborted) {
+    for (int k = 0; k < 2; ++k) {            // the end, for each tile parity
+      if (!acquire_slot(p, ctl, n, lane)) break;
+      if (lane == 0) {
+        const int stage = n % STAGES;
+        ctl->done[stage] = 1;
+        ctl->n_total = n_total;
+        mbar_arrive(smem_addr(&ctl->full[stage]));
+      }
+      __syncwarp();
+      ++n;
+    }
+  }
+  // Close the own split's word: nothing more can be taken from it in this call or, for
+  // a launch that is replayed as is, before its owner opens it again.
+  if (share && lane == 0) atomicExch(&mine->claim, claim_pack(0x7fffffffu, 0u));
+  drain_ring(p, ctl, n, lane);
 }
 
 }  // namespace fd

@@ -250,8 +250,9 @@ FD_API fd_status fd_decode_attention_noalloc(const fd_tensor* q, const fd_tensor
  * Bytes of workspace a call with these sizes needs: a 256-byte header (device error
  * flags), the per-split LSE_i [B, Hq, S] f32 and partial outputs O_i [B, Hq, S, d] f32
  * ([AI-Infra] 2.6 "Flash-Decoding Split-K": each split writes its local O and one LSE
- * scalar), and [B, Hkv] 64-bit ticket counters of the single-launch merge; each region
- * 256-byte aligned.  num_splits must be >= 1 (resolve 0 with fd_num_splits_heuristic
+ * scalar), [B, Hkv] 64-bit ticket counters of the single-launch merge, and [B, Hkv, S]
+ * 16-byte claim words of tail sharing (FD_SCHEDULE_TAIL_SHARING); each region 256-byte
+ * aligned.  num_splits must be >= 1 (resolve 0 with fd_num_splits_heuristic
  * first).  Returns 0 for invalid sizes.
  */
 FD_API size_t fd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_splits);
@@ -361,15 +362,26 @@ FD_API int32_t fd_get_path(void);
  * ones, and each consumer warp keeps one head's state.  For paged bf16 caches with
  * d = 128, 16- or 32-token pages and Hkv a multiple of 4; other calls run the grid
  * schedule.  Same results up to rounding order.
+ * FD_SCHEDULE_TAIL_SHARING: the grid schedule, and a CTA that has finished its own
+ * split goes on with tiles taken from the back of a split of the same (b, kv head)
+ * that is still in progress (claim words in the workspace; each CTA's stream stays
+ * contiguous).  Every key still enters exactly one partial, so the merge is unchanged
+ * ([Split-avg] "weight block results with log-sum-exp": the LSE-weighted merge is exact
+ * whatever keys each partial holds); only which partial holds a key varies from run to
+ * run, so results are equal up to rounding order.  The tcgen05 kernel only; measured
+ * slower than the grid schedule on GB300 (the owners' claims cost more than the tail
+ * they recover), so it is never chosen automatically.
  * FD_SCHEDULE_AUTO (default): head groups where they apply, else grid.
  * The persistent and head-group schedules run only with FD_MERGE_KERNEL (or
- * fd_decode_partial) and on the tensor-core path; otherwise the grid schedule runs.
+ * fd_decode_partial) and on the mma.sync path; otherwise the grid schedule runs (with
+ * tail sharing on the tcgen05 kernel under FD_SCHEDULE_TAIL_SHARING).
  */
 typedef enum {
   FD_SCHEDULE_AUTO = 0,
   FD_SCHEDULE_GRID = 1,
   FD_SCHEDULE_PERSISTENT = 2,
-  FD_SCHEDULE_HEAD_GROUPS = 3
+  FD_SCHEDULE_HEAD_GROUPS = 3,
+  FD_SCHEDULE_TAIL_SHARING = 4
 } fd_schedule;
 FD_API fd_status fd_set_schedule(int32_t schedule);
 FD_API int32_t fd_get_schedule(void);

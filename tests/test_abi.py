@@ -55,14 +55,16 @@ def test_status_strings_and_version():
 
 
 def test_workspace_size_layout():
-    # 256-byte header, then LSE_i [B, Hq, S] f32, O_i [B, Hq, S, d] f32 and the ticket
-    # counters [B, Hkv] (64-bit) of the single-launch merge, each rounded up to 256 B.
+    # 256-byte header, then LSE_i [B, Hq, S] f32, O_i [B, Hq, S, d] f32, the ticket
+    # counters [B, Hkv] (64-bit) of the single-launch merge and the claim words
+    # [B, Hkv, S] (16 bytes) of tail sharing, each rounded up to 256 B.
     up = lambda x: (x + 255) // 256 * 256
 
     def expect(B, Hq, Hkv, d, S):
         o_off = up(256 + B * Hq * S * 4)
         cnt_off = up(o_off + B * Hq * S * d * 4)
-        return up(cnt_off + B * Hkv * 8)
+        steal_off = up(cnt_off + B * Hkv * 8)
+        return up(steal_off + B * Hkv * S * 16)
     for B, Hq, Hkv, d, S in [(1, 64, 8, 128, 38), (4, 32, 32, 128, 3), (1, 1, 1, 64, 4),
                              (16, 32, 8, 128, 256), (3, 6, 3, 64, 4096)]:
         assert fd.workspace_size(B, Hq, Hkv, d, S) == expect(B, Hq, Hkv, d, S)
@@ -139,11 +141,12 @@ def test_schedule_round_trip():
     try:
         assert fd.get_schedule() == fd.FD_SCHEDULE_AUTO            # the default
         for sched in (fd.FD_SCHEDULE_GRID, fd.FD_SCHEDULE_PERSISTENT,
-                      fd.FD_SCHEDULE_HEAD_GROUPS, fd.FD_SCHEDULE_AUTO):
+                      fd.FD_SCHEDULE_HEAD_GROUPS, fd.FD_SCHEDULE_TAIL_SHARING,
+                      fd.FD_SCHEDULE_AUTO):
             fd.set_schedule(sched)
             assert fd.get_schedule() == sched
         with pytest.raises(fd.FdError):
-            fd.set_schedule(4)
+            fd.set_schedule(5)
         assert fd.get_schedule() == fd.FD_SCHEDULE_AUTO            # unchanged on error
     finally:
         lib.fd_set_schedule(fd.FD_SCHEDULE_AUTO)
