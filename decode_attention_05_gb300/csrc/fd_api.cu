@@ -618,6 +618,10 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   p.head_group = heads ? fd::kHeadGroup : 0;
   p.steal = reinterpret_cast<fd::StealWord*>(ws + wl.steal_off);
   p.tail_share = sc.tail_share ? 1 : 0;
+  // The tcgen05 kernel gives a tile that straddles two splits to the lower one, so no
+  // tile is read twice (split_len need not be a whole number of tiles: 128K tokens over
+  // 19 splits, one CTA per SM, read 0.9% more bytes otherwise).
+  p.tile_owned = path == FD_PATH_TCGEN05 ? 1 : 0;
 
   pr->path = path;
   pr->dtype = q->dtype;

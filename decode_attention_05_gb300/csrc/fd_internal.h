@@ -71,6 +71,9 @@ struct Params {
   // whether this launch shares (0: every CTA streams exactly its own split)
   StealWord* steal;
   int32_t tail_share;
+  // 1: split i covers its range with both ends rounded up to whole tiles (split_range in
+  // fd_pipeline.cuh): no tile is loaded by two CTAs (the tcgen05 kernel)
+  int32_t tile_owned;
   float* lse_part;        // [B, Q, Hq, S]     natural-log LSE_i, -inf for an empty split
   float* o_part;          // [B, Q, Hq, S, d]  normalised partial output O_i
   // outputs

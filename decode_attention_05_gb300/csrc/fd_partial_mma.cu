@@ -44,6 +44,9 @@ namespace {
 // of back-to-back steps): no prefetch 78.5 us, 4 tiles 75.5 us, 8 tiles 75.0 us,
 // 12 tiles 76.1 us; the early trigger helps the short MHA step (40.1 -> 38.8 us).
 constexpr int kPrefetchTiles = 8;
+// Head-group tiles (16 tokens x 4 kv heads, 32 KB), paged: ragged paged workload (16-token
+// pages) 135.6 us without, 134.7 us with 8, 133.6 us with 4.
+constexpr int kPrefetchHeadTiles = 4;
 constexpr int kTriggerTiles = 4;
 
 template <int D_, int G_, bool KV8_ = false, bool PERSIST_ = false, bool WIDE_ = false,
@@ -646,7 +649,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
                           const __grid_constant__ CUtensorMap tv,
                           const __grid_constant__ Params p) {
   constexpr int G = SH::G, TT = SH::TT, STAGES = SH::STAGES;
-  if (threadIdx.x == SH::NCW * 32) prefetch_first_tiles<TT>(p, &tk, &tv, kPrefetchTiles);
+  if (threadIdx.x == SH::NCW * 32) prefetch_first_tiles<TT>(p, &tk, &tv, kPrefetchTiles, (int)blockIdx.y);
   pdl_wait();                       // inputs of this step are visible
   const SplitInfo si = split_info<TT>(p);
   extern __shared__ uint8_t smem_raw[];
@@ -745,7 +748,7 @@ __global__ void __maxnreg__(200)
                            const __grid_constant__ Params p) {
   constexpr int TT = SH::TT, STAGES = SH::STAGES;
   static_assert(SH::WIDE, "wide shape");
-  if (threadIdx.x == SH::NCW * 32) prefetch_first_tiles<TT>(p, &tk, &tv, kPrefetchTiles);
+  if (threadIdx.x == SH::NCW * 32) prefetch_first_tiles<TT>(p, &tk, &tv, kPrefetchTiles, (int)blockIdx.y);
   pdl_wait();                       // inputs of this step are visible
   const SplitInfo si = split_info<TT>(p);
   extern __shared__ uint8_t smem_raw[];
@@ -830,6 +833,11 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   constexpr int STAGES = SH::STAGES, TOK = 16;
   static_assert(SH::ROWS_PER_WARP == TOK && SH::CHUNKS == 1 && SH::NCW == kHeadGroup,
                 "one 16-token page slice per consumer warp");
+  // (Not with 16 query rows per kv head: there its registers would spill.)
+  if constexpr (SH::G <= 8) {
+    if (threadIdx.x == SH::NCW * 32)
+      prefetch_first_pages<TOK>(p, &tk, &tv, kPrefetchHeadTiles, (int)blockIdx.y * kHeadGroup);
+  }
   pdl_wait();                       // inputs of this step are visible
   SplitInfo si = split_info<TOK>(p);
   si.g = blockIdx.y * kHeadGroup;                 // first kv head of the group

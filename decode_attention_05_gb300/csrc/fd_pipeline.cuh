@@ -31,6 +31,23 @@ struct SplitInfo {
   int64_t used_pages;   // pages of row b that hold tokens < L_b (paged)
 };
 
+// Logical tokens [lo, hi) that split `split` of a row of length L covers in this
+// launch: [i split_len, (i + 1) split_len) clipped to L -- or, with p.tile_owned, the same
+// with both ends rounded up to whole TT-token tiles, so that every tile belongs to exactly
+// one split and is loaded once (the keys of a tile that straddles a boundary go to the
+// lower split; every key still enters exactly one partial, so the merge is unchanged).
+template <int TT>
+__device__ __forceinline__ void split_range(const Params& p, int split, int64_t L, int64_t& lo,
+                                            int64_t& hi) {
+  lo = (int64_t)split * p.split_len;
+  hi = lo + p.split_len;
+  if (p.tile_owned) {
+    lo = (lo + TT - 1) / TT * TT;
+    hi = (hi + TT - 1) / TT * TT;
+  }
+  hi = min(hi, L);
+}
+
 // Resolve this CTA's split; clamps and flags an out-of-range sequence length.
 template <int TT>
 __device__ __forceinline__ SplitInfo split_info(const Params& p) {
@@ -44,24 +61,24 @@ __device__ __forceinline__ SplitInfo split_info(const Params& p) {
     L = L < 0 ? 0 : p.L_cap;
   }
   si.L = L;
-  si.lo = (int64_t)si.split * p.split_len;
-  si.hi = min(si.lo + p.split_len, L);
+  split_range<TT>(p, si.split, L, si.lo, si.hi);
   si.T0 = (si.lo / TT) * TT;
   si.n_tiles = si.lo < si.hi ? (int)((si.hi - si.T0 + TT - 1) / TT) : 0;
   si.used_pages = p.page_size > 0 ? (L + p.page_size - 1) >> p.log2_page : 0;
   return si;
 }
 
-// L2 prefetch of the first `count` tiles of this CTA's split (contiguous caches; grid
-// blockIdx = (split, kv head, batch row)), issued BEFORE griddepcontrol.wait.  Where a
-// split starts depends only on the launch's sizes (split_len, L_cap), and a prefetch is
-// only a hint: L2 is the point of coherence, so the loads after the wait still see
-// whatever the previous kernel of the stream wrote.  The row's length, which that kernel
-// may still be changing, is read relaxed and only bounds how much is prefetched (a
-// split past it prefetches nothing).  A CTA that becomes resident while the previous
-// decode step finishes (programmatic dependent launch) thus has its first tiles on the
-// way to L2 before it may read them, and the tail of the previous step's bandwidth is
-// not left idle.
+// L2 prefetch of the first `count` tiles of this CTA's split, contiguous caches (grid
+// blockIdx = (split, kv head or head group, batch row); `head` = the first kv head of
+// the CTA's TMA boxes), issued BEFORE griddepcontrol.wait.  Where a split starts depends only on the launch's
+// sizes (split_len), and a prefetch is only a hint: L2 is the point of coherence, so the
+// loads after the wait still see whatever the previous kernel of the stream wrote.  The
+// inputs that kernel may still be changing -- the row's length, and for a paged cache
+// the block-table entries -- are read relaxed and only steer the prefetch: a split past
+// the length prefetches nothing, and a page id outside [0, num_pages) is skipped.  A CTA
+// that becomes resident while the previous decode step finishes (programmatic dependent
+// launch) thus has its first tiles on the way to L2 before it may read them, and the
+// tail of the previous step's bandwidth is not left idle.
 __device__ __forceinline__ int32_t ld_relaxed_s32(const int32_t* a) {
   int32_t v;
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
@@ -69,17 +86,45 @@ __device__ __forceinline__ int32_t ld_relaxed_s32(const int32_t* a) {
 }
 template <int TT>
 __device__ __forceinline__ void prefetch_first_tiles(const Params& p, const CUtensorMap* tk,
-                                                     const CUtensorMap* tv, int count) {
-  if (p.block_table != nullptr) return;
-  const int64_t L = min((int64_t)ld_relaxed_s32(p.seq_lens + blockIdx.z), p.L_cap);
-  const int64_t lo = (int64_t)blockIdx.x * p.split_len;
-  const int64_t hi = min(lo + p.split_len, L);
+                                                     const CUtensorMap* tv, int count, int head) {
+  if (p.block_table != nullptr) return;       // paged caches: prefetch_first_pages
+  const int b = (int)blockIdx.z;
+  const int64_t L = min((int64_t)ld_relaxed_s32(p.seq_lens + b), p.L_cap);
+  int64_t lo, hi;
+  split_range<TT>(p, (int)blockIdx.x, L, lo, hi);
   const int64_t T0 = lo / TT * TT;
+#pragma unroll 1
   for (int k = 0; k < count; ++k) {
     const int64_t t0 = T0 + (int64_t)k * TT;
     if (t0 >= hi) break;
-    tma_prefetch_5d(tk, 0, (int)t0, 0, (int)blockIdx.y, (int)blockIdx.z);
-    tma_prefetch_5d(tv, 0, (int)t0, 0, (int)blockIdx.y, (int)blockIdx.z);
+    tma_prefetch_5d(tk, 0, (int)t0, 0, head, b);
+    tma_prefetch_5d(tv, 0, (int)t0, 0, head, b);
+  }
+}
+
+// The same for a paged cache whose boxes are TT rows of one page (TT <= page_size):
+// the page ids of the split's first tiles come from the block table, read relaxed; a
+// page id outside [0, num_pages) is skipped.  Kept apart from prefetch_first_tiles: in
+// the kernels with 16 query rows per kv head its extra registers spill (measured 7%
+// slower there), and only the head-group kernel, always paged, needs it.
+template <int TT>
+__device__ __forceinline__ void prefetch_first_pages(const Params& p, const CUtensorMap* tk,
+                                                     const CUtensorMap* tv, int count, int head) {
+  const int b = (int)blockIdx.z;
+  const int64_t L = min(max((int64_t)ld_relaxed_s32(p.seq_lens + b), (int64_t)0), p.L_cap);
+  const int64_t lo = (int64_t)blockIdx.x * p.split_len;
+  const int64_t hi = min(lo + p.split_len, L);
+  const int64_t T0 = lo / TT * TT;
+#pragma unroll 1
+  for (int k = 0; k < count; ++k) {
+    const int64_t t0 = T0 + (int64_t)k * TT;
+    if (t0 >= hi) break;
+    const int64_t pi = t0 >> p.log2_page;
+    const int32_t id = ld_relaxed_s32(p.block_table + (int64_t)b * p.bt_sb + pi);
+    if (id < 0 || (int64_t)id >= p.num_pages) continue;
+    const int slot = (int)(t0 & (p.page_size - 1));
+    tma_prefetch_5d(tk, 0, slot, 0, head, id);
+    tma_prefetch_5d(tv, 0, slot, 0, head, id);
   }
 }
 
@@ -511,8 +556,7 @@ __device__ __forceinline__ bool steal_piece(const Params& p, const SplitInfo& si
     int ok = 0;
     if (lane == 0) ok = atomicCAS(&group[best].claim, best_w, claim_pack(f, bk - k)) == best_w;
     if (__shfl_sync(0xffffffffu, ok, 0)) {
-      lo = (int64_t)best * p.split_len;
-      hi = min(lo + p.split_len, si.L);
+      split_range<TT>(p, best, si.L, lo, hi);
       T0 = lo / TT * TT;
       cur = bk - k;
       end = bk;

@@ -180,7 +180,11 @@ FD_API fd_status fd_decode_attention_fp8kv(const fd_tensor* q, const fd_tensor* 
  *
  * fd_decode_partial: the partial pass only.  Same arguments and checks as
  * fd_decode_attention without out / lse_out; writes LSE_i and O_i of every split into
- * the workspace (empty split: LSE_i = -inf, O_i untouched).
+ * the workspace (empty split: LSE_i = -inf, O_i untouched).  On the tcgen05 kernel
+ * (FD_PATH_TCGEN05, or the automatic path for wide query groups) both ends of a split's
+ * range are rounded up to whole 64-token tiles, so a tile that straddles two splits is
+ * read once, by the lower split: its keys past the boundary then sit in that split's
+ * partial.  Every key still enters exactly one partial, so the merged result is the same.
  */
 FD_API fd_status fd_decode_partial(const fd_tensor* q, const fd_tensor* k_cache,
                             const fd_tensor* v_cache, const int32_t* seq_lens,
