@@ -83,6 +83,9 @@ def _declare(L):
     O = ctypes.POINTER(FdOptions)
     L.fd_decode_attention_ex.restype = ctypes.c_int
     L.fd_decode_attention_ex.argtypes = [P, P, P, vp, vp, vp, P, i32, i32, P, vp, vp, sz, vp, O]
+    L.fd_selftest_stalled_decode.restype = ctypes.c_int
+    L.fd_selftest_stalled_decode.argtypes = [P, P, P, vp, vp, vp, P, i32, i32, P, vp, vp, sz,
+                                             vp, O, i32]
     L.fd_plan_set_options.restype = ctypes.c_int
     L.fd_plan_set_options.argtypes = [vp, O]
     L.fd_partial_kernel_name_ex.restype = ctypes.c_char_p
@@ -255,6 +258,29 @@ def partial_kernel_name(dtype, kv_dtype, d: int, Hkv: int, page_size: int = 0,
     else:
         name = lib().fd_partial_kernel_name_ex(ctypes.byref(options), *args)
     return name.decode() if name else None
+
+
+def selftest_stalled_decode(q, k_cache, v_cache, seq_lens, workspace: torch.Tensor,
+                            stall_tile: int, out: torch.Tensor, lse_out: torch.Tensor,
+                            block_table=None, page_size: int = 0, num_splits: int = 0,
+                            k_scale=None, v_scale=None, options: Optional["FdOptions"] = None,
+                            stream=None):
+    """fd_selftest_stalled_decode: a decode whose first CTA's producer stops before tile
+    `stall_tile`, so that CTA's bounded waits run out (see include/fd.h)."""
+    if q.dim() == 4:
+        B, Qn, Hq, d = q.shape
+    else:
+        (B, Hq, d), Qn = q.shape, 1
+    S = resolve_num_splits(B, Hq, k_cache.shape[1], d, _cap(k_cache, block_table, page_size),
+                           num_splits, Q=Qn)
+    dq, dk, dv, dbt, do = (tensor_desc(q), tensor_desc(k_cache), tensor_desc(v_cache),
+                           tensor_desc(block_table), tensor_desc(out))
+    ptr = lambda t: None if t is None else t.data_ptr()
+    _check(lib().fd_selftest_stalled_decode(
+        ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), ptr(k_scale), ptr(v_scale),
+        seq_lens.data_ptr(), _ref(dbt), page_size, S, ctypes.byref(do), lse_out.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream), None if options is None else ctypes.byref(options), stall_tile))
 
 
 def workspace_init(ws: torch.Tensor, stream=None):

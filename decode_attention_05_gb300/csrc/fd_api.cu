@@ -655,7 +655,7 @@ fd_status run_decode(CacheKind kind, const fd_tensor* q, const fd_tensor* k_cach
                      const int32_t* seq_lens, const fd_tensor* block_table, int32_t page_size,
                      int32_t num_splits, fd_tensor* out, float* lse_out, void* workspace,
                      size_t workspace_bytes, void* stream, const fd_options* options,
-                     bool need_out) {
+                     bool need_out, int32_t selftest_stall = 0) {
   Settings cfg;
   if (!resolve_settings(options, &cfg))
     return fail(FD_ERR_INVALID_ARG, "fd_options holds an unknown path, merge mode or schedule");
@@ -670,6 +670,7 @@ fd_status run_decode(CacheKind kind, const fd_tensor* q, const fd_tensor* k_cach
                          need_out ? out : nullptr, need_out ? lse_out : nullptr, workspace,
                          workspace_bytes, need_out, cfg, &pr, kv8, k_scale, v_scale);
   if (st != FD_OK) return st;
+  pr.p.selftest_stall = selftest_stall;
   const cudaStream_t s = (cudaStream_t)stream;
   if (need_out && pr.fused) return launch_partial(pr, s);   // one launch merges in-kernel
   pr.p.counters = nullptr;          // the merge, if any, is a separate kernel
@@ -733,6 +734,19 @@ fd_status fd_decode_attention_ex(const fd_tensor* q, const fd_tensor* k_cache,
   return run_decode(CacheKind::kByDtype, q, k_cache, v_cache, k_scale, v_scale, seq_lens,
                     block_table, page_size, num_splits, out, lse_out, workspace,
                     workspace_bytes, stream, options, out != nullptr);
+}
+
+fd_status fd_selftest_stalled_decode(const fd_tensor* q, const fd_tensor* k_cache,
+                                     const fd_tensor* v_cache, const float* k_scale,
+                                     const float* v_scale, const int32_t* seq_lens,
+                                     const fd_tensor* block_table, int32_t page_size,
+                                     int32_t num_splits, fd_tensor* out, float* lse_out,
+                                     void* workspace, size_t workspace_bytes, void* stream,
+                                     const fd_options* options, int32_t stall_tile) {
+  if (stall_tile < 0) return fail(FD_ERR_INVALID_ARG, "stall_tile must be >= 0");
+  return run_decode(CacheKind::kByDtype, q, k_cache, v_cache, k_scale, v_scale, seq_lens,
+                    block_table, page_size, num_splits, out, lse_out, workspace,
+                    workspace_bytes, stream, options, out != nullptr, stall_tile + 1);
 }
 
 fd_status fd_workspace_partials(void* workspace, int32_t B, int32_t Hq, int32_t d,

@@ -74,6 +74,10 @@ struct Params {
   // 1: split i covers its range with both ends rounded up to whole tiles (split_range in
   // fd_pipeline.cuh): no tile is loaded by two CTAs (the tcgen05 kernel)
   int32_t tile_owned;
+  // Failure-path self-test only (fd_selftest_stalled_decode; 0 otherwise): n > 0 makes the
+  // producer of CTA (0, 0, 0) stop before its tile n - 1 and publish nothing more, as if
+  // those copies never arrived, so the CTA's bounded waits run out
+  int32_t selftest_stall;
   float* lse_part;        // [B, Q, Hq, S]     natural-log LSE_i, -inf for an empty split
   float* o_part;          // [B, Q, Hq, S, d]  normalised partial output O_i
   // outputs

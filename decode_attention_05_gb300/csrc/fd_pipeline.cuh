@@ -459,6 +459,13 @@ __device__ __forceinline__ void drain_ring(const Params& p, PipeCtl<STAGES>* ctl
   }
 }
 
+// Failure-path self-test (Params::selftest_stall): whether the producer of this CTA stops
+// before its ring slot n.  Never true outside fd_selftest_stalled_decode.
+__device__ __forceinline__ bool selftest_stops(const Params& p, int n) {
+  return p.selftest_stall > 0 && n == p.selftest_stall - 1 && blockIdx.x == 0 &&
+         blockIdx.y == 0 && blockIdx.z == 0;
+}
+
 // Producer warp: streams tiles 0..n_tiles-1 of the split.  All 32 lanes run the loop
 // (they share the page-id window); lane 0 issues the copies.
 template <int TT, int STAGES>
@@ -470,6 +477,7 @@ __device__ __forceinline__ void produce_tiles(const Params& p, const SplitInfo& 
   PageWindow win;
   int n = 0;
   for (; n < si.n_tiles; ++n) {
+    if (selftest_stops(p, n)) break;
     if (!acquire_slot(p, ctl, n, lane)) break;
     if (__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int32_t*>(&ctl->abort), 0)) break;
     issue_tile<TT, STAGES>(p, si, si.T0 + (int64_t)n * TT, tk, tv, stages, ctl, n % STAGES,
@@ -646,7 +654,7 @@ __device__ __forceinline__ void produce_tiles_shared(const Params& p, const Spli
       own = false;
       if (!share || !steal_piece<TT>(p, si, group, lane, T0, lo, hi, cur, end)) break;
     }
-    if (!acquire_slot(p, ctl, n, lane) ||
+    if (selftest_stops(p, n) || !acquire_slot(p, ctl, n, lane) ||
         __shfl_sync(0xffffffffu, *reinterpret_cast<volatile int32_t*>(&ctl->abort), 0)) {
       aborted = true;
       break;

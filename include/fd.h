@@ -436,6 +436,28 @@ FD_API fd_status fd_decode_attention_ex(const fd_tensor* q, const fd_tensor* k_c
 FD_API fd_status fd_plan_set_options(fd_plan* plan, const fd_options* options);
 
 /*
+ * Self-test of the partial kernels' own failure paths (no counterpart on the pages):
+ * fd_decode_attention_ex, except that the producer warp of CTA (split 0, kv head 0, row 0)
+ * stops before its tile `stall_tile` (0-based) and publishes nothing more, as if those
+ * copies never arrived.  That CTA's consumers then wait on a stage nothing fills; their
+ * bounded waits give up after ~2 s, raise FD_DEVFLAG_TIMEOUT, drain the copies in flight
+ * (and, on the tcgen05 kernel, every issued product before tensor memory is freed) and
+ * write an empty split; every other CTA runs normally.  The outputs of rows that split
+ * touches are therefore wrong; read the flags with fd_read_device_error.  The context
+ * and workspace stay usable.  stall_tile >= 0 (FD_ERR_INVALID_ARG otherwise); a stall
+ * past the CTA's last tile changes nothing.  Not for production use: it exists so that
+ * tests can make the real kernels' waits run out without a fault.
+ */
+FD_API fd_status fd_selftest_stalled_decode(const fd_tensor* q, const fd_tensor* k_cache,
+                                            const fd_tensor* v_cache, const float* k_scale,
+                                            const float* v_scale, const int32_t* seq_lens,
+                                            const fd_tensor* block_table, int32_t page_size,
+                                            int32_t num_splits, fd_tensor* out,
+                                            float* lse_out, void* workspace,
+                                            size_t workspace_bytes, void* stream,
+                                            const fd_options* options, int32_t stall_tile);
+
+/*
  * Name of the partial-pass kernel a call would launch under the current process
  * settings (path, merge mode, schedule): "fd_partial_mma_kernel",
  * "fd_partial_heads_kernel", "fd_partial_wide_kernel", "fd_partial_persist_kernel" or

@@ -42,3 +42,99 @@ def test_selftest_argument_checks():
         fd.selftest_bounded_wait(ws, limit_us=0)
     with pytest.raises(fd.FdError):
         fd.selftest_bounded_wait(ws, limit_us=3_000_000)
+
+
+# ------------------------------------------------------------------ the kernels' own waits
+# fd_selftest_stalled_decode: the producer of CTA (0, 0, 0) stops before one of its tiles,
+# so that CTA's consumers wait on a stage nothing fills.  Their bounded waits (2 s) must
+# give up, flag FD_DEVFLAG_TIMEOUT, drain what is in flight and end the CTA normally; the
+# same context and workspace must then decode correctly.  One case per kernel family.
+
+def _stalled_case(kind):
+    Q = 1
+    opts = None
+    if kind == "mma":
+        w = workloads.contiguous_case(2, 16, 2, 128, 4096, [4096, 2000], seed=811,
+                                      out_dtype=torch.float32)
+        S, stall = 4, 1
+    elif kind == "mma_fused":
+        w = workloads.contiguous_case(2, 16, 2, 128, 4096, [4096, 2000], seed=812,
+                                      out_dtype=torch.float32)
+        S, stall = 4, 2
+        opts = fd.options(merge_mode=fd.FD_MERGE_IN_KERNEL)
+    elif kind == "heads":
+        w = workloads.paged_case(2, 16, 4, 128, 16, 256, [4096, 1000], seed=813,
+                                 out_dtype=torch.float32)
+        S, stall = 4, 1
+    elif kind == "simt":
+        w = workloads.contiguous_case(2, 16, 2, 128, 4096, [4096, 2000], seed=814,
+                                      out_dtype=torch.float32)
+        S, stall = 4, 1
+        opts = fd.options(path=fd.FD_PATH_SIMT)
+    elif kind in ("tc", "tc_shared"):
+        w = workloads.contiguous_case(2, 16, 2, 128, 4096, [4096, 3000], seed=815,
+                                      out_dtype=torch.float32)
+        Q, S, stall = 4, 3, 2
+        opts = fd.options(schedule=fd.FD_SCHEDULE_TAIL_SHARING) if kind == "tc_shared" else None
+    elif kind == "wide":                     # d = 64, 32 rows per kv head
+        w = workloads.contiguous_case(2, 16, 2, 64, 4096, [4096, 2000], seed=816,
+                                      out_dtype=torch.float32)
+        Q, S, stall = 4, 4, 1
+    else:
+        raise ValueError(kind)
+    return w, Q, S, stall, opts
+
+
+@pytest.mark.parametrize("kind", ["mma", "mma_fused", "heads", "simt", "tc", "tc_shared", "wide"])
+def test_real_kernel_wait_runs_out_and_context_survives(kind):
+    import numpy as np
+    import oracle
+    w, Q, S, stall, opts = _stalled_case(kind)
+    wd = w.to("cuda")
+    q = wd.q
+    if Q > 1:
+        q = workloads.multi_token_queries(w.B, Q, w.Hq, w.d, seed=820).cuda()
+    expected = {"mma": "fd_partial_mma_kernel", "mma_fused": "fd_partial_mma_kernel",
+                "heads": "fd_partial_heads_kernel", "simt": "fd_partial_simt_kernel",
+                "tc": "fd_partial_tc_kernel", "tc_shared": "fd_partial_tc_kernel",
+                "wide": "fd_partial_wide_kernel"}[kind]
+    assert fd.partial_kernel_name(torch.bfloat16, torch.bfloat16, w.d, w.Hkv, w.page_size,
+                                  rows=Q * (w.Hq // w.Hkv), options=opts) == expected
+    ws = torch.zeros(fd.workspace_size(w.B, Q * w.Hq, w.Hkv, w.d, S), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty(tuple(q.shape), dtype=torch.float32, device="cuda")
+    lse = torch.empty(tuple(q.shape[:-1]), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    fd.selftest_stalled_decode(q, wd.k, wd.v, wd.seq_lens, ws, stall, out, lse,
+                               block_table=wd.block_table, page_size=w.page_size,
+                               num_splits=S, options=opts)
+    flags = fd.read_device_error(ws)                        # synchronises, then clears
+    elapsed = time.perf_counter() - t0
+    assert flags == 4                                       # FD_DEVFLAG_TIMEOUT
+    assert 1.5 <= elapsed < 60.0                            # the 2 s waits ran out, then ended
+    # The same context and workspace decode correctly afterwards.
+    o, l = fd.decode_attention(q, wd.k, wd.v, wd.seq_lens, wd.block_table, w.page_size, S,
+                               workspace=ws, out_dtype=torch.float32, options=opts)
+    torch.cuda.synchronize()
+    assert fd.read_device_error(ws) == 0
+    qn, k, v, lens, bt, ps = w.oracle_arrays()
+    if Q > 1:
+        ref_o, ref_l = oracle.decode_causal(workloads.np_storage(q.cpu()), k, v, lens,
+                                            block_table=bt, page_size=ps)
+        o = o.reshape(w.B * Q, w.Hq, w.d)
+        l = l.reshape(w.B * Q, w.Hq)
+        ref_o = ref_o.reshape(w.B * Q, w.Hq, w.d)
+        ref_l = ref_l.reshape(w.B * Q, w.Hq)
+    else:
+        ref_o, ref_l = oracle.decode(qn, k, v, lens, block_table=bt, page_size=ps)
+    check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
+
+
+def test_stalled_decode_argument_check():
+    w = workloads.contiguous_case(1, 8, 1, 128, 256, seed=830).to("cuda")
+    ws = torch.zeros(fd.workspace_size(1, 8, 1, 128, 2), dtype=torch.uint8, device="cuda")
+    out = torch.empty(1, 8, 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(1, 8, dtype=torch.float32, device="cuda")
+    with pytest.raises(fd.FdError):
+        fd.selftest_stalled_decode(w.q, w.k, w.v, w.seq_lens, ws, -1, out, lse, num_splits=2)

@@ -50,7 +50,7 @@ def draw(i, medium=False):
     lens = [r.choice([0, 1, r.randint(1, cap), cap, r.randint(cap // 2, cap)]) for _ in range(B)]
     S = r.choice([0, 1, 2, 5, 16, 64] + ([128, 300, 512] if medium else []))
     sched = r.choice([fd.FD_SCHEDULE_AUTO, fd.FD_SCHEDULE_GRID, fd.FD_SCHEDULE_PERSISTENT,
-                      fd.FD_SCHEDULE_HEAD_GROUPS])
+                      fd.FD_SCHEDULE_HEAD_GROUPS, fd.FD_SCHEDULE_TAIL_SHARING])
     merge = r.choice([fd.FD_MERGE_KERNEL, fd.FD_MERGE_KERNEL, fd.FD_MERGE_IN_KERNEL])
     if f32:     # the tensor-core path takes up to 8 f32 rows
         path = fd.FD_PATH_MMA if Q * G <= 8 and r.random() < 0.7 else fd.FD_PATH_SIMT
