@@ -508,6 +508,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // The first ring's worth of tiles into L2 before the wait (prefetch_first_tiles;
   // measured best at the ring depth: 6 tiles 86.5 us, 8 tiles 86.8 us, none 88.9 us at
   // 8 query tokens on the 128K GQA workload).
+  // Contiguous caches only: with 64-token pages the page-id prefetch measured slower on
+  // this kernel (97.8 against 95.9 us, 4 query tokens on the 128K GQA workload).
   if (threadIdx.x == 8 * 32) prefetch_first_tiles<kTcTT>(p, &tk, &tv, kTcStages, (int)blockIdx.y);
   pdl_wait();                       // inputs of this step are visible
   const SplitInfo si = split_info<kTcTT>(p);

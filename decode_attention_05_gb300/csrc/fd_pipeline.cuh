@@ -102,11 +102,12 @@ __device__ __forceinline__ void prefetch_first_tiles(const Params& p, const CUte
   }
 }
 
-// The same for a paged cache whose boxes are TT rows of one page (TT <= page_size):
+// The same for a paged cache whose boxes are TT rows of one page (TT <= page_size; the
+// caller checks):
 // the page ids of the split's first tiles come from the block table, read relaxed; a
-// page id outside [0, num_pages) is skipped.  Kept apart from prefetch_first_tiles: in
-// the kernels with 16 query rows per kv head its extra registers spill (measured 7%
-// slower there), and only the head-group kernel, always paged, needs it.
+// page id outside [0, num_pages) is skipped.  Kept apart from prefetch_first_tiles, and
+// left out of the kernels with 16 query rows per kv head: there its extra registers
+// spill (measured 7% slower).
 template <int TT>
 __device__ __forceinline__ void prefetch_first_pages(const Params& p, const CUtensorMap* tk,
                                                      const CUtensorMap* tv, int count, int head) {
