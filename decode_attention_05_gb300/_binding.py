@@ -119,6 +119,10 @@ def _declare(L):
     L.fd_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     L.fd_plan_create.restype = ctypes.c_int
     L.fd_plan_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i64, i32]
+    L.fd_plan_create_q.restype = ctypes.c_int
+    L.fd_plan_create_q.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32, i64, i32]
+    L.fd_plan_decode_ex.restype = ctypes.c_int
+    L.fd_plan_decode_ex.argtypes = [vp, P, P, P, vp, vp, vp, P, i32, P, vp, vp]
     L.fd_plan_num_splits.restype = i32
     L.fd_plan_num_splits.argtypes = [vp]
     L.fd_plan_workspace_bytes.restype = sz
@@ -459,11 +463,18 @@ def merge_partials(lse_part: torch.Tensor, o_part: torch.Tensor, out: Optional[t
 
 
 class Plan:
-    """fd_plan: fixed sizes and split count, owning its workspace and completion event."""
+    """fd_plan: fixed sizes and split count, owning its workspace and completion event.
+    Q > 1: a plan for multi-token decode (q [B, Q, Hq, d])."""
 
-    def __init__(self, B: int, Hq: int, Hkv: int, d: int, L_cap: int, num_splits: int = 0):
+    def __init__(self, B: int, Hq: int, Hkv: int, d: int, L_cap: int, num_splits: int = 0,
+                 Q: int = 1):
         self._h = ctypes.c_void_p()
-        _check(lib().fd_plan_create(ctypes.byref(self._h), B, Hq, Hkv, d, L_cap, num_splits))
+        self.Q = Q
+        if Q == 1:
+            _check(lib().fd_plan_create(ctypes.byref(self._h), B, Hq, Hkv, d, L_cap, num_splits))
+        else:
+            _check(lib().fd_plan_create_q(ctypes.byref(self._h), B, Q, Hq, Hkv, d, L_cap,
+                                          num_splits))
 
     @property
     def num_splits(self) -> int:
@@ -478,17 +489,26 @@ class Plan:
         return int(lib().fd_plan_workspace(self._h) or 0)
 
     def decode(self, q, k_cache, v_cache, seq_lens, block_table=None, page_size=0, out=None,
-               lse_out=None, out_dtype=None, stream=None):
-        B, Hq, d = q.shape
+               lse_out=None, out_dtype=None, stream=None, k_scale=None, v_scale=None):
+        """fd_plan_decode (or fd_plan_decode_ex for a 4-D q or an FP8 cache)."""
         if out is None:
-            out = torch.empty((B, Hq, d), dtype=out_dtype or q.dtype, device=q.device)
+            out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
         if lse_out is None:
-            lse_out = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+            lse_out = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
         dq, dk, dv, dbt, do = (tensor_desc(q), tensor_desc(k_cache), tensor_desc(v_cache),
                                tensor_desc(block_table), tensor_desc(out))
-        _check(lib().fd_plan_decode(self._h, ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv),
-                                    seq_lens.data_ptr(), _ref(dbt), page_size, ctypes.byref(do),
-                                    lse_out.data_ptr(), _stream_handle(stream)))
+        ptr = lambda t: None if t is None else t.data_ptr()
+        if q.dim() == 3 and k_cache.dtype != torch.float8_e4m3fn:
+            _check(lib().fd_plan_decode(self._h, ctypes.byref(dq), ctypes.byref(dk),
+                                        ctypes.byref(dv), seq_lens.data_ptr(), _ref(dbt),
+                                        page_size, ctypes.byref(do), lse_out.data_ptr(),
+                                        _stream_handle(stream)))
+        else:
+            _check(lib().fd_plan_decode_ex(self._h, ctypes.byref(dq), ctypes.byref(dk),
+                                           ctypes.byref(dv), ptr(k_scale), ptr(v_scale),
+                                           seq_lens.data_ptr(), _ref(dbt), page_size,
+                                           ctypes.byref(do), lse_out.data_ptr(),
+                                           _stream_handle(stream)))
         return out, lse_out
 
     def resize(self, num_splits: int):

@@ -797,7 +797,7 @@ fd_status fd_merge_partials(int32_t B, int32_t Hq, int32_t d, int32_t num_splits
 
 // ------------------------------------------------------------------------ plans
 struct fd_plan {
-  int32_t B, Hq, Hkv, d;
+  int32_t B, Q, Hq, Hkv, d;   // Q query tokens per row (1: single-token decode)
   int64_t L_cap;
   int32_t S;
   int device;
@@ -808,7 +808,9 @@ struct fd_plan {
 };
 
 static fd_status plan_alloc(fd_plan* p, int32_t S) {
-  const size_t bytes = fd_workspace_size(p->B, p->Hq, p->Hkv, p->d, S);
+  const int64_t rows = (int64_t)p->Q * p->Hq;
+  const size_t bytes = rows <= INT32_MAX ? fd_workspace_size(p->B, (int32_t)rows, p->Hkv, p->d, S)
+                                         : 0;
   if (bytes == 0) return fail(FD_ERR_INVALID_ARG, "invalid plan sizes");
   void* ws = nullptr;
   cudaError_t e = cudaMalloc(&ws, bytes);
@@ -833,21 +835,26 @@ static fd_status plan_alloc(fd_plan* p, int32_t S) {
 
 fd_status fd_plan_create(fd_plan** plan, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
                          int64_t L_cap, int32_t num_splits) {
+  return fd_plan_create_q(plan, B, 1, Hq, Hkv, d, L_cap, num_splits);
+}
+
+fd_status fd_plan_create_q(fd_plan** plan, int32_t B, int32_t Q, int32_t Hq, int32_t Hkv,
+                           int32_t d, int64_t L_cap, int32_t num_splits) {
   if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
   *plan = nullptr;
-  if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || L_cap <= 0 || num_splits < 0 ||
+  if (B <= 0 || Q <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || L_cap <= 0 || num_splits < 0 ||
       num_splits > kMaxSplits || Hq % Hkv != 0)
     return fail(FD_ERR_INVALID_ARG, "invalid plan sizes");
   fd_plan* p = new fd_plan();
   p->opts.path = p->opts.merge_mode = p->opts.schedule = FD_FROM_PROCESS;
+  p->Q = Q;
   p->B = B;
   p->Hq = Hq;
   p->Hkv = Hkv;
   p->d = d;
   p->L_cap = L_cap;
   cudaGetDevice(&p->device);
-  const int32_t S = num_splits > 0 ? num_splits
-                                   : fd_num_splits_heuristic(B, Hq, Hkv, d, L_cap, current_sm_count());
+  const int32_t S = num_splits > 0 ? num_splits : heuristic_splits(B, Q, Hq, Hkv, d, L_cap);
   fd_status st = plan_alloc(p, S);
   if (st != FD_OK) {
     delete p;
@@ -861,21 +868,48 @@ int32_t fd_plan_num_splits(const fd_plan* plan) { return plan ? plan->S : 0; }
 size_t fd_plan_workspace_bytes(const fd_plan* plan) { return plan ? plan->ws_bytes : 0; }
 void* fd_plan_workspace(const fd_plan* plan) { return plan ? plan->ws : nullptr; }
 
-fd_status fd_plan_decode(fd_plan* plan, const fd_tensor* q, const fd_tensor* k_cache,
-                         const fd_tensor* v_cache, const int32_t* seq_lens,
-                         const fd_tensor* block_table, int32_t page_size, fd_tensor* out,
-                         float* lse_out, void* stream) {
+// Whether q and the cache have the plan's sizes: q [B, Hq, d] for a plan of one query
+// token per row, [B, Q, Hq, d] for Q > 1 (a 4-D q with Q = 1 is accepted too).
+static bool plan_fits(const fd_plan* plan, const fd_tensor* q, const fd_tensor* k_cache) {
+  if (!q || !k_cache || k_cache->ndim != 4 || k_cache->shape[1] != plan->Hkv) return false;
+  if (q->ndim == 3)
+    return plan->Q == 1 && q->shape[0] == plan->B && q->shape[1] == plan->Hq &&
+           q->shape[2] == plan->d;
+  return q->ndim == 4 && q->shape[0] == plan->B && q->shape[1] == plan->Q &&
+         q->shape[2] == plan->Hq && q->shape[3] == plan->d;
+}
+
+static fd_status plan_run(fd_plan* plan, CacheKind kind, const fd_tensor* q,
+                          const fd_tensor* k_cache, const fd_tensor* v_cache,
+                          const float* k_scale, const float* v_scale, const int32_t* seq_lens,
+                          const fd_tensor* block_table, int32_t page_size, fd_tensor* out,
+                          float* lse_out, void* stream) {
   if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
-  if (!q || q->ndim != 3 || q->shape[0] != plan->B || q->shape[1] != plan->Hq || q->shape[2] != plan->d ||
-      !k_cache || k_cache->ndim != 4 || k_cache->shape[1] != plan->Hkv)
-    return fail(FD_ERR_INVALID_ARG, "tensor sizes differ from the plan's");
-  fd_status st = run_decode(CacheKind::kPlain, q, k_cache, v_cache, nullptr, nullptr, seq_lens,
-                            block_table, page_size, plan->S, out, lse_out, plan->ws,
-                            plan->ws_bytes, stream, &plan->opts, true);
+  if (!plan_fits(plan, q, k_cache)) return fail(FD_ERR_INVALID_ARG, "tensor sizes differ from the plan's");
+  fd_status st = run_decode(kind, q, k_cache, v_cache, k_scale, v_scale, seq_lens, block_table,
+                            page_size, plan->S, out, lse_out, plan->ws, plan->ws_bytes, stream,
+                            &plan->opts, true);
   if (st != FD_OK) return st;
   cudaError_t e = cudaEventRecord(plan->done, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(FD_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
   return FD_OK;
+}
+
+fd_status fd_plan_decode(fd_plan* plan, const fd_tensor* q, const fd_tensor* k_cache,
+                         const fd_tensor* v_cache, const int32_t* seq_lens,
+                         const fd_tensor* block_table, int32_t page_size, fd_tensor* out,
+                         float* lse_out, void* stream) {
+  return plan_run(plan, CacheKind::kPlain, q, k_cache, v_cache, nullptr, nullptr, seq_lens,
+                  block_table, page_size, out, lse_out, stream);
+}
+
+fd_status fd_plan_decode_ex(fd_plan* plan, const fd_tensor* q, const fd_tensor* k_cache,
+                            const fd_tensor* v_cache, const float* k_scale, const float* v_scale,
+                            const int32_t* seq_lens, const fd_tensor* block_table,
+                            int32_t page_size, fd_tensor* out, float* lse_out, void* stream) {
+  if (!out) return fail(FD_ERR_INVALID_ARG, "out is required");
+  return plan_run(plan, CacheKind::kByDtype, q, k_cache, v_cache, k_scale, v_scale, seq_lens,
+                  block_table, page_size, out, lse_out, stream);
 }
 
 fd_status fd_plan_set_options(fd_plan* plan, const fd_options* options) {
@@ -894,8 +928,8 @@ fd_status fd_plan_resize(fd_plan* plan, int32_t num_splits) {
   if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
   if (num_splits < 0 || num_splits > kMaxSplits) return fail(FD_ERR_INVALID_ARG, "bad num_splits");
   const int32_t S = num_splits > 0 ? num_splits
-                                   : fd_num_splits_heuristic(plan->B, plan->Hq, plan->Hkv, plan->d,
-                                                             plan->L_cap, current_sm_count());
+                                   : heuristic_splits(plan->B, plan->Q, plan->Hq, plan->Hkv,
+                                                      plan->d, plan->L_cap);
   if (S == plan->S) return FD_OK;
   // The old workspace may still be read by an in-flight merge: wait for it first.
   cudaError_t e = cudaEventSynchronize(plan->done);

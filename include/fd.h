@@ -325,6 +325,11 @@ typedef struct fd_plan fd_plan;
 /* Create a plan on the current device.  num_splits 0 -> heuristic. */
 FD_API fd_status fd_plan_create(fd_plan** plan, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
                          int64_t L_cap, int32_t num_splits);
+/* The same for Q >= 1 query tokens per row (multi-token decode, q [B, Q, Hq, d]): the
+ * workspace holds B * Q * Hq partial rows and num_splits 0 resolves as
+ * fd_resolve_num_splits_q does.  fd_plan_create is fd_plan_create_q with Q = 1. */
+FD_API fd_status fd_plan_create_q(fd_plan** plan, int32_t B, int32_t Q, int32_t Hq, int32_t Hkv,
+                                  int32_t d, int64_t L_cap, int32_t num_splits);
 /* The plan's split count and workspace size. */
 FD_API int32_t fd_plan_num_splits(const fd_plan* plan);
 FD_API size_t fd_plan_workspace_bytes(const fd_plan* plan);
@@ -335,6 +340,15 @@ FD_API fd_status fd_plan_decode(fd_plan* plan, const fd_tensor* q, const fd_tens
                          const fd_tensor* v_cache, const int32_t* seq_lens,
                          const fd_tensor* block_table, int32_t page_size, fd_tensor* out,
                          float* lse_out, void* stream);
+/* fd_plan_decode for every cache and query form of fd_decode_attention_ex: q [B, Hq, d]
+ * (plans of one query token per row) or [B, Q, Hq, d] (the plan's Q); an FP8 E4M3 cache
+ * (dtype FD_F8E4M3) with its k_scale / v_scale, which must be NULL for bf16 / f32 caches;
+ * out required.  Uses the plan's split count, workspace and options; records the event. */
+FD_API fd_status fd_plan_decode_ex(fd_plan* plan, const fd_tensor* q, const fd_tensor* k_cache,
+                                   const fd_tensor* v_cache, const float* k_scale,
+                                   const float* v_scale, const int32_t* seq_lens,
+                                   const fd_tensor* block_table, int32_t page_size,
+                                   fd_tensor* out, float* lse_out, void* stream);
 /* Wait for the last decode, then resize workspace and event for a new split count. */
 FD_API fd_status fd_plan_resize(fd_plan* plan, int32_t num_splits);
 FD_API void fd_plan_destroy(fd_plan* plan);

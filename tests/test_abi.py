@@ -379,3 +379,16 @@ def test_decode_ex_validation():
     # An FP8 cache through the plain entry point is refused, as before.
     assert call(q, desc([2, 2, 1024, 128], dtype=3), desc([2, 2, 1024, 128], dtype=3), out) \
         == INVALID
+
+
+def test_plan_argument_checks():
+    """Invalid plan sizes are refused on the host, before any allocation."""
+    lib = fd.lib()
+    h = ctypes.c_void_p()
+    assert lib.fd_plan_create_q(ctypes.byref(h), 1, 0, 8, 1, 128, 1024, 0) == INVALID   # Q = 0
+    assert lib.fd_plan_create_q(ctypes.byref(h), 1, 2, 6, 4, 128, 1024, 0) == INVALID   # Hq % Hkv
+    assert lib.fd_plan_create_q(ctypes.byref(h), 1, 2, 8, 1, 128, 1024, 4097) == INVALID
+    assert lib.fd_plan_create(ctypes.byref(h), 0, 8, 1, 128, 1024, 0) == INVALID
+    assert not h.value
+    assert lib.fd_plan_decode_ex(None, None, None, None, None, None, None, None, 0, None, None,
+                                 None) == INVALID

@@ -166,3 +166,46 @@ def test_swapping_kv_buffers_of_one_shape():
                                out_dtype=torch.float32)
     torch.cuda.synchronize()
     _within_oracle(o, l, *refs["a"])
+
+
+def test_plan_for_multi_token_decode_and_resize():
+    # 4 query tokens x G = 8 = 32 rows per kv head (the tcgen05 kernel), planned split count.
+    w_cpu = workloads.contiguous_case(2, 16, 2, 128, 4096, [4096, 1500], seed=65,
+                                      out_dtype=torch.float32)
+    q4 = workloads.multi_token_queries(2, 4, 16, 128, seed=66)
+    _, k, v, lens, _, _ = w_cpu.oracle_arrays()
+    ref_o, ref_l = oracle.decode_causal(workloads.np_storage(q4), k, v, lens)
+    w = w_cpu.to("cuda")
+    qd = q4.cuda()
+    plan = fd.Plan(2, 16, 2, 128, 4096, 0, Q=4)
+    try:
+        assert plan.num_splits == fd.resolve_num_splits(2, 16, 2, 128, 4096, 0, Q=4)
+        assert plan.workspace_bytes >= fd.workspace_size(2, 4 * 16, 2, 128, plan.num_splits)
+        for S in (None, 7):
+            if S is not None:
+                plan.resize(S)
+                assert plan.num_splits == 7
+            o, l = plan.decode(qd, w.k, w.v, w.seq_lens, out_dtype=torch.float32)
+            torch.cuda.synchronize()
+            _within_oracle(o.reshape(8, 16, 128), l.reshape(8, 16), ref_o.reshape(8, 16, 128),
+                           ref_l.reshape(8, 16))
+        with pytest.raises(fd.FdError):                     # a 3-D q does not fit a Q = 4 plan
+            plan.decode(w.q, w.k, w.v, w.seq_lens)
+    finally:
+        plan.close()
+
+
+def test_plan_over_an_fp8_cache():
+    w_cpu = workloads.contiguous_case(2, 32, 4, 128, 3072, [3072, 999], seed=67)
+    kc, vc, ks, vs = workloads.fp8_quantize(w_cpu)
+    q = workloads.np_storage(w_cpu.q)
+    ref_o, ref_l = oracle.decode_kv8(q, kc.view(torch.uint8).numpy(), vc.view(torch.uint8).numpy(),
+                                     ks.numpy(), vs.numpy(), w_cpu.seq_lens.numpy())
+    plan = fd.Plan(2, 32, 4, 128, 3072, 4)
+    try:
+        o, l = plan.decode(w_cpu.q.cuda(), kc.cuda(), vc.cuda(), w_cpu.seq_lens.cuda(),
+                           k_scale=ks.cuda(), v_scale=vs.cuda(), out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        _within_oracle(o, l, ref_o, ref_l)
+    finally:
+        plan.close()
