@@ -576,8 +576,9 @@ __device__ __forceinline__ bool steal_piece(const Params& p, const SplitInfo& si
 }
 
 // One fetch-and-add claim of kClaimChunk tiles on an owner's word, into ticket slot
-// `slot` (lane 0; the tickets live in separate registers that are never copied, so a
-// claim in flight stalls nothing until its own slot is read).
+// `slot` (lane 0 holds the tickets in separate registers).  Measured: the claims cost the
+// producer 0.16-0.4 us each whatever the number in flight (1 to 3), so how long a claim
+// takes to come back is not the whole cost.
 __device__ __forceinline__ void claim_into(int slot, unsigned long long* word,
                                            unsigned long long& t0, unsigned long long& t1,
                                            unsigned long long& t2) {
@@ -597,9 +598,8 @@ __device__ __forceinline__ unsigned long long ticket_of(int slot, unsigned long 
 // other splits of the same (b, kv head) afterwards (see above); then publishes two done
 // stages (one for each tile parity: some consumers take every other tile) carrying
 // n_total.  Without `share` the sequence is exactly the split's tiles, in order.
-// The owner keeps kClaimAhead claims in flight, so their round trips stay off its path
-// while it streams; a helper looks for a piece when the current one is exhausted (the
-// ring still holds the tiles it has issued).
+// The owner keeps kClaimAhead claims in flight; a helper looks for a piece when the
+// current one is exhausted (the ring still holds the tiles it has issued).
 template <int TT, int STAGES>
 __device__ __forceinline__ void produce_tiles_shared(const Params& p, const SplitInfo& si,
                                                      const CUtensorMap* tk,
