@@ -1,5 +1,5 @@
 // fd_combine.cu -- the merge pass of split-KV decode: one CTA per (b, query token,
-// query head) row.
+// query head) row, or, for calls with many rows, one warp per row.
 //
 // Reads the S partials (O_i, LSE_i) of its row and computes
 //   M = max over non-empty splits of LSE_i,   w_i = exp(LSE_i - M)  in (0, 1],
@@ -19,6 +19,7 @@
 #include <cuda_bf16.h>
 
 #include "fd_device.cuh"
+#include "fd_epilogue.cuh"
 
 namespace fd {
 
@@ -119,10 +120,29 @@ __global__ void __launch_bounds__(128) fd_combine_kernel(const __grid_constant__
   }
 }
 
+// Many rows: one warp per row, kRowWarps rows per CTA (merge_row, the same fold with
+// the splits of a row in one warp).  A CTA of four warps per row spreads a row's splits
+// but lives only as long as one row's loads; with thousands of rows (large batches,
+// usually with few splits each) the launch of those short CTAs, not their memory
+// traffic, set the pass's time.
+constexpr int kRowWarps = 8;
+constexpr int64_t kRowsPerWarpMin = 1024;   // rows from which the warp-per-row form runs
+
+template <int D>
+__global__ void __launch_bounds__(kRowWarps * 32) fd_combine_rows_kernel(const __grid_constant__ Params p) {
+  pdl_trigger();                               // the next step's partial pass may launch
+  pdl_wait();
+  const int64_t row = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (row >= (int64_t)p.B * p.Q * p.Hq) return;
+  merge_row<D, 8>(p, row, threadIdx.x & 31);
+}
+
 cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool pdl) {
+  const int64_t rows = (int64_t)p.B * p.Q * p.Hq;
+  const bool by_rows = rows >= kRowsPerWarpMin;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((int64_t)p.B * p.Q * p.Hq));
-  cfg.blockDim = dim3(128);
+  cfg.gridDim = dim3((unsigned)(by_rows ? (rows + kRowWarps - 1) / kRowWarps : rows));
+  cfg.blockDim = dim3(by_rows ? kRowWarps * 32 : 128);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -130,6 +150,10 @@ cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  if (by_rows) {
+    if (p.d == 128) return cudaLaunchKernelEx(&cfg, fd_combine_rows_kernel<128>, p);
+    return cudaLaunchKernelEx(&cfg, fd_combine_rows_kernel<64>, p);
+  }
   if (p.d == 128) return cudaLaunchKernelEx(&cfg, fd_combine_kernel<128>, p);
   return cudaLaunchKernelEx(&cfg, fd_combine_kernel<64>, p);
 }

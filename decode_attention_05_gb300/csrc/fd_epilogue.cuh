@@ -105,78 +105,84 @@ __device__ __forceinline__ bool merge_warps_and_store(const Params& p, const Spl
 // no grid-wide dependency ("2kiu.com/news/6053916", section "the split count is a cost
 // account": the merge may start only when every partial it needs is visible).
 //
-// Merge of one row (warp w takes rows w, w + NCW, ...; a lane holds D / 32 dims): the
-// splits are folded 16 at a time with a running maximum, the same online rule as inside
-// a split, so all loads of a batch are issued before any result is needed:
+// Merge of one output row by one warp (a lane holds D / 32 dims): the splits are
+// folded BATCH at a time with a running maximum, the same online rule as inside a
+// split, so all loads of a batch are issued before any result is needed:
 //   M' = max(M, max_s LSE_s),  W = W 2^(M - M') + sum_s 2^(LSE_s - M'),
 //   acc = acc 2^(M - M') + sum_s 2^(LSE_s - M') O_s          (base-2 of the natural LSEs)
 // ending with out = acc / W and lse_out = M + log W.  An empty split (LSE = -inf) has
 // weight 0 and its O_s never reaches the sum (it is selected away, never multiplied:
 // its memory may hold anything).  A row with no non-empty split gives 0 and -inf.
+// Row index: (b * Q + j) * Hq + h.  Loads bypass L1 (partials of the running grid).
+template <int D, int BATCH>
+__device__ __forceinline__ void merge_row(const Params& p, int64_t row, int lane) {
+  constexpr int VEC = D / 32;
+  constexpr float kLog2e = 1.4426950408889634f;
+  const float* lse = p.lse_part + row * p.S;
+  const float* ob = p.o_part + row * p.S * D + lane * VEC;
+  float M = kNegInf, W = 0.f, acc[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+  for (int s0 = 0; s0 < p.S; s0 += BATCH) {
+    float ls[BATCH], v[BATCH][VEC];
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const bool in = s0 + u < p.S;
+      ls[u] = in ? __ldcg(lse + s0 + u) * kLog2e : kNegInf;
+      if constexpr (VEC == 4) {
+        const float4 t = in ? __ldcg(reinterpret_cast<const float4*>(ob + (int64_t)(s0 + u) * D))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+      } else {
+        const float2 t = in ? __ldcg(reinterpret_cast<const float2*>(ob + (int64_t)(s0 + u) * D))
+                            : make_float2(0.f, 0.f);
+        v[u][0] = t.x; v[u][1] = t.y;
+      }
+    }
+    float mb = ls[0];
+#pragma unroll
+    for (int u = 1; u < BATCH; ++u) mb = fmaxf(mb, ls[u]);
+    const float mn = fmaxf(M, mb);
+    if (mn == kNegInf) continue;                    // nothing non-empty yet
+    const float c = (M == kNegInf) ? 0.f : ex2(M - mn);
+    W *= c;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] *= c;
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const bool live = ls[u] != kNegInf;
+      const float w = live ? ex2(ls[u] - mn) : 0.f;
+      W += w;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w, live ? v[u][e] : 0.f, acc[e]);
+    }
+    M = mn;
+  }
+  const int64_t bj = row / p.Hq;
+  const int hq = (int)(row - bj * p.Hq);
+  const int64_t b = bj / p.Q;
+  const int j = (int)(bj - b * p.Q);
+  const int64_t obase = b * p.out_sb + (int64_t)j * p.out_sj + (int64_t)hq * p.out_sh + lane * VEC;
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) {
+    const float o = acc[e] * inv;
+    if (p.out_bf16) {
+      reinterpret_cast<__nv_bfloat16*>(p.out)[obase + e] = __float2bfloat16_rn(o);
+    } else {
+      reinterpret_cast<float*>(p.out)[obase + e] = o;
+    }
+  }
+  if (lane == 0 && p.lse_out != nullptr)
+    p.lse_out[row] = W > 0.f ? (M + lg2_approx(W)) * 0.6931471805599453f : kNegInf;
+}
+
+// The merge of a (b, kv head) group's rows inside the partial pass: warp w of the NCW
+// consumer warps takes rows w, w + NCW, ...
 template <int D, int NCW>
 __device__ __forceinline__ void merge_group(const Params& p, int b, int g, int ctid) {
-  constexpr int VEC = D / 32;
-  constexpr int BATCH = 16;
-  constexpr float kLog2e = 1.4426950408889634f;
   const int warp = ctid >> 5, lane = ctid & 31;
-  for (int rho = warp; rho < p.n_rows; rho += NCW) {
-    const int64_t row = flat_row(p, b, g, rho);
-    const float* lse = p.lse_part + row * p.S;
-    const float* ob = p.o_part + row * p.S * D + lane * VEC;
-    float M = kNegInf, W = 0.f, acc[VEC];
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
-    for (int s0 = 0; s0 < p.S; s0 += BATCH) {
-      float ls[BATCH], v[BATCH][VEC];
-#pragma unroll
-      for (int u = 0; u < BATCH; ++u) {
-        const bool in = s0 + u < p.S;
-        ls[u] = in ? __ldcg(lse + s0 + u) * kLog2e : kNegInf;
-        if constexpr (VEC == 4) {
-          const float4 t = in ? __ldcg(reinterpret_cast<const float4*>(ob + (int64_t)(s0 + u) * D))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
-        } else {
-          const float2 t = in ? __ldcg(reinterpret_cast<const float2*>(ob + (int64_t)(s0 + u) * D))
-                              : make_float2(0.f, 0.f);
-          v[u][0] = t.x; v[u][1] = t.y;
-        }
-      }
-      float mb = ls[0];
-#pragma unroll
-      for (int u = 1; u < BATCH; ++u) mb = fmaxf(mb, ls[u]);
-      const float mn = fmaxf(M, mb);
-      if (mn == kNegInf) continue;                    // nothing non-empty yet
-      const float c = (M == kNegInf) ? 0.f : ex2(M - mn);
-      W *= c;
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) acc[e] *= c;
-#pragma unroll
-      for (int u = 0; u < BATCH; ++u) {
-        const bool live = ls[u] != kNegInf;
-        const float w = live ? ex2(ls[u] - mn) : 0.f;
-        W += w;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w, live ? v[u][e] : 0.f, acc[e]);
-      }
-      M = mn;
-    }
-    const int j = rho / p.G, hq = g * p.G + (rho - j * p.G);
-    const int64_t obase = (int64_t)b * p.out_sb + (int64_t)j * p.out_sj +
-                          (int64_t)hq * p.out_sh + lane * VEC;
-    const float inv = W > 0.f ? 1.f / W : 0.f;
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-      const float o = acc[e] * inv;
-      if (p.out_bf16) {
-        reinterpret_cast<__nv_bfloat16*>(p.out)[obase + e] = __float2bfloat16_rn(o);
-      } else {
-        reinterpret_cast<float*>(p.out)[obase + e] = o;
-      }
-    }
-    if (lane == 0 && p.lse_out != nullptr)
-      p.lse_out[row] = W > 0.f ? (M + lg2_approx(W)) * 0.6931471805599453f : kNegInf;
-  }
+  for (int rho = warp; rho < p.n_rows; rho += NCW) merge_row<D, 16>(p, flat_row(p, b, g, rho), lane);
 }
 
 // Called by the NCW * 32 consumer threads of a CTA after it has written its partials

@@ -442,6 +442,47 @@ def test_sequence_sharded_merge(name, path):
     check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
 
 
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("S", [0, 1, 3])
+def test_large_batch_merge(d, S):
+    """Batches of 1024 query rows or more are merged one warp per row (not one CTA per
+    row): 48 rows x 32 heads of ragged lengths -- empty rows, one-key rows, rows that end
+    inside a split and splits with no key -- against the oracle, with the planner's split
+    count (one split here), one and three splits."""
+    import random
+    rnd = random.Random(1000 + d)
+    lens = [0, 1, 600, 599, 65] + [rnd.randint(0, 600) for _ in range(43)]
+    w = workloads.contiguous_case(48, 32, 8, d, 600, lens, seed=1000 + d,
+                                  out_dtype=torch.float32)
+    assert 48 * 32 >= 1024
+    ref_o, ref_l = ref_for(w, key=("large-batch", d))
+    o, l, ws, S_res = run(w, num_splits=S)
+    check(w, o, l, ref_o, ref_l)
+
+
+def test_large_batch_external_merge():
+    """fd_merge_partials over 1280 rows (the warp-per-row merge) of partials computed in
+    two sequence shards equals the unsharded oracle."""
+    w = workloads.contiguous_case(40, 32, 8, 128, 1000, [1000, 0, 400, 401] + [777] * 36,
+                                  seed=1010, out_dtype=torch.float32)
+    ref_o, ref_l = ref_for(w)
+    wd = w.to("cuda")
+    lse_list, o_list = [], []
+    for lo, hi in ((0, 400), (400, 1000)):
+        k = wd.k[:, :, lo:hi].contiguous()
+        v = wd.v[:, :, lo:hi].contiguous()
+        lens = (wd.seq_lens - lo).clamp(0, hi - lo).to(torch.int32)
+        ws = torch.zeros(fd.workspace_size(40, 32, 8, 128, 2), dtype=torch.uint8, device="cuda")
+        fd.decode_partial(wd.q, k, v, lens, ws, num_splits=2)
+        lp, op = fd.workspace_partials(ws, 40, 32, 128, 2)
+        lse_list.append(lp.clone())
+        o_list.append(op.clone())
+    o, l = fd.merge_partials(torch.cat(lse_list, dim=2).contiguous(),
+                             torch.cat(o_list, dim=2).contiguous(), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
+
+
 @pytest.mark.parametrize("name,path", PATHS_BF16)
 @pytest.mark.parametrize("Q,G", [(1, 8), (2, 8), (3, 4), (4, 4), (4, 2), (16, 1)])
 @pytest.mark.parametrize("paged", [False, True])
