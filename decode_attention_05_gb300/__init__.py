@@ -14,7 +14,8 @@ from ._binding import (  # noqa: F401
     FD_SCHEDULE_PERSISTENT, FD_SCHEDULE_TAIL_SHARING, FdError, FdOptions,
     Plan, decode_attention, decode_attention_fp8kv, decode_attention_noalloc,
     decode_partial, decode_partial_fp8kv, get_merge_mode, get_path, get_schedule, lib, library_path, merge_partials,
-    num_splits_for_lengths, num_splits_heuristic, options, partial_kernel_name, read_device_error,
+    num_splits_for_lengths, num_splits_heuristic, options, partial_kernel_name, partial_kernel_name_for,
+    read_device_error,
     resolve_num_splits, selftest_bounded_wait, selftest_stalled_decode,
     set_merge_mode, set_path, set_schedule, workspace_init, workspace_partials, workspace_size,
 )

@@ -90,6 +90,9 @@ def _declare(L):
     L.fd_plan_set_options.argtypes = [vp, O]
     L.fd_partial_kernel_name_ex.restype = ctypes.c_char_p
     L.fd_partial_kernel_name_ex.argtypes = [O, i32, i32, i32, i32, i32, i32, i32]
+    L.fd_partial_kernel_name_for.restype = ctypes.c_char_p
+    L.fd_partial_kernel_name_for.argtypes = [O, i32, i32, i32, i32, i32, i32, i32, i32,
+                                             ctypes.c_int64, i32, i32]
     L.fd_decode_attention_noalloc.restype = ctypes.c_int
     L.fd_decode_attention_noalloc.argtypes = [P, P, P, vp, P, i32, i32, P, vp, vp]
     L.fd_decode_attention_fp8kv.restype = ctypes.c_int
@@ -249,6 +252,18 @@ def selftest_bounded_wait(workspace: torch.Tensor, limit_us: int = 50000, stream
     """fd_selftest_bounded_wait: a kernel whose wait runs out must flag a timeout."""
     _check(lib().fd_selftest_bounded_wait(workspace.data_ptr(), limit_us,
                                           _stream_handle(stream)))
+
+
+def partial_kernel_name_for(dtype, kv_dtype, B: int, Q: int, Hq: int, Hkv: int, d: int,
+                            page_size: int, L_cap: int, num_splits: int = 0,
+                            with_output: bool = True,
+                            options: Optional[FdOptions] = None) -> Optional[str]:
+    """The partial-pass kernel a call with exactly these sizes would launch (torch
+    dtypes): fd_partial_kernel_name_for."""
+    name = lib().fd_partial_kernel_name_for(
+        None if options is None else ctypes.byref(options), _DTYPES[dtype], _DTYPES[kv_dtype],
+        B, Q, Hq, Hkv, d, page_size, L_cap, num_splits, 1 if with_output else 0)
+    return name.decode() if name else None
 
 
 def partial_kernel_name(dtype, kv_dtype, d: int, Hkv: int, page_size: int = 0,

@@ -55,16 +55,33 @@ struct Schedule {
 };
 
 // rows: query rows per (b, kv head) group (Q x G); groups above kMaxNarrowRows always
-// run the wide grid kernel.
+// run the wide grid kernel.  pairs: the call's (b, kv head) pairs, B x Hkv (0: not
+// known -- the name-only queries).
 // f32 inputs on the tensor-core path run on the grid schedule only.
+//
+// Automatic head groups: always for 16- and 32-token pages (four 4 KB page boxes become
+// one 16 KB box); for contiguous caches and larger pages once the batch holds
+// kHeadsMinPairsPerSm (b, kv head) pairs per SM, with up to 8 query rows per kv head.
+// There one CTA streams four kv heads of a row without a cross-warp merge, and the grid
+// schedule's many short CTAs lose a start-up and an epilogue each.  Measured on GB300
+// (bf16, d = 128, 32 heads over 8 kv heads, one split, a step over 256-512 MiB of KV):
+// 128 rows of 512 tokens 50.0 -> 39.8 us, 256 x 512 92.1 -> 77.8, 512 x 256 101.6 ->
+// 84.8, 1024 x 128 127.7 -> 90.0, 96 x 1024 64.0 -> 60.1; below the threshold the grid
+// wins (64 x 1024: 42.0 against 49.6, whose 128 CTAs leave SMs idle).
+constexpr int64_t kHeadsMinPairsPerSm = 5;
+
 Schedule choose_schedule(int sched, int path, bool kv8, bool f32, int64_t d, int64_t Hkv,
-                         int32_t page_size, bool fused, int64_t rows) {
+                         int32_t page_size, bool fused, int64_t rows, int64_t pairs) {
   const bool narrow = rows <= fd::kMaxNarrowRows && !f32;
   const bool head_ok = path == FD_PATH_MMA && !kv8 && d == 128 &&
-                       (page_size == 16 || page_size == 32) && Hkv % fd::kHeadGroup == 0 &&
-                       !fused && narrow;
+                       (page_size == 0 || page_size >= 16) &&
+                       Hkv % fd::kHeadGroup == 0 && !fused && narrow;
+  const bool small_pages = page_size == 16 || page_size == 32;
+  const int sms = rows <= 8 && pairs > 0 ? fd::sm_count() : 0;   // 0: no device
+  const bool big_batch = sms > 0 && pairs >= kHeadsMinPairsPerSm * sms;
   Schedule sc;
-  sc.heads = head_ok && (sched == FD_SCHEDULE_AUTO || sched == FD_SCHEDULE_HEAD_GROUPS);
+  sc.heads = head_ok && ((sched == FD_SCHEDULE_AUTO && (small_pages || big_batch)) ||
+                         sched == FD_SCHEDULE_HEAD_GROUPS);
   sc.persistent = !sc.heads && path == FD_PATH_MMA && !fused && narrow &&
                   sched == FD_SCHEDULE_PERSISTENT;
   // Tail sharing: the tcgen05 kernel, when asked for (measured slower than the plain
@@ -89,6 +106,34 @@ int resolve_path(int path, int32_t q_dtype, bool kv8, int64_t d, int32_t page_si
   if (rows >= fd::kTcAutoMinRows && tc_takes(q_dtype, kv8, d, page_size, rows))
     return FD_PATH_TCGEN05;
   return q_dtype == FD_BF16 || rows <= fd::kMaxF32MmaRows ? FD_PATH_MMA : FD_PATH_SIMT;
+}
+
+// The partial-pass kernel a call runs (fd_partial_kernel_name*); pairs = B x Hkv and S
+// the split count, or 0 when not known (then a call of few pairs and several splits).
+const char* kernel_name(const Settings& cfg, int32_t dtype, int32_t kv_dtype, int32_t d,
+                        int32_t Hkv, int32_t page_size, int32_t rows, int32_t with_output,
+                        int64_t pairs, int32_t S) {
+  const bool kv8 = kv_dtype == FD_F8E4M3;
+  if ((dtype != FD_BF16 && dtype != FD_F32) || (!kv8 && kv_dtype != dtype) ||
+      (kv8 && dtype != FD_BF16) || d <= 0 || Hkv <= 0 || page_size < 0 || rows < 1 ||
+      rows > fd::kMaxRows)
+    return nullptr;
+  const int path = resolve_path(cfg.path, dtype, kv8, d, page_size, rows);
+  if ((path == FD_PATH_MMA && dtype == FD_F32 && rows > fd::kMaxF32MmaRows) ||
+      (kv8 && path != FD_PATH_MMA))
+    return nullptr;
+  if (path == FD_PATH_TCGEN05)
+    return tc_takes(dtype, kv8, d, page_size, rows) ? "fd_partial_tc_kernel" : nullptr;
+  if (rows > fd::kMaxNarrowRows && (path != FD_PATH_MMA || kv8)) return nullptr;
+  if (path == FD_PATH_SIMT) return "fd_partial_simt_kernel";
+  if (rows > fd::kMaxNarrowRows) return "fd_partial_wide_kernel";
+  // One split with an output writes the output from the partial pass: no in-kernel merge.
+  const bool fused = with_output && S != 1 && cfg.merge == FD_MERGE_IN_KERNEL;
+  const Schedule sc = choose_schedule(cfg.schedule, path, kv8, dtype == FD_F32, d, Hkv,
+                                      page_size, fused, rows, pairs);
+  if (sc.heads) return "fd_partial_heads_kernel";
+  if (sc.persistent) return "fd_partial_persist_kernel";
+  return "fd_partial_mma_kernel";
 }
 
 fd_status fail(fd_status st, const char* fmt, ...) {
@@ -336,26 +381,22 @@ const char* fd_partial_kernel_name_ex(const fd_options* options, int32_t dtype,
                                       int32_t page_size, int32_t rows, int32_t with_output) {
   Settings cfg;
   if (!resolve_settings(options, &cfg)) return nullptr;
-  const bool kv8 = kv_dtype == FD_F8E4M3;
-  if ((dtype != FD_BF16 && dtype != FD_F32) || (!kv8 && kv_dtype != dtype) ||
-      (kv8 && dtype != FD_BF16) || d <= 0 || Hkv <= 0 || page_size < 0 || rows < 1 ||
-      rows > fd::kMaxRows)
+  return kernel_name(cfg, dtype, kv_dtype, d, Hkv, page_size, rows, with_output, 0, 0);
+}
+
+const char* fd_partial_kernel_name_for(const fd_options* options, int32_t dtype,
+                                       int32_t kv_dtype, int32_t B, int32_t Q, int32_t Hq,
+                                       int32_t Hkv, int32_t d, int32_t page_size, int64_t L_cap,
+                                       int32_t num_splits, int32_t with_output) {
+  Settings cfg;
+  if (!resolve_settings(options, &cfg) || B <= 0 || Q <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 ||
+      Hq % Hkv != 0 || L_cap <= 0 || num_splits < 0 || num_splits > kMaxSplits)
     return nullptr;
-  const int path = resolve_path(cfg.path, dtype, kv8, d, page_size, rows);
-  if ((path == FD_PATH_MMA && dtype == FD_F32 && rows > fd::kMaxF32MmaRows) ||
-      (kv8 && path != FD_PATH_MMA))
-    return nullptr;
-  if (path == FD_PATH_TCGEN05)
-    return tc_takes(dtype, kv8, d, page_size, rows) ? "fd_partial_tc_kernel" : nullptr;
-  if (rows > fd::kMaxNarrowRows && (path != FD_PATH_MMA || kv8)) return nullptr;
-  if (path == FD_PATH_SIMT) return "fd_partial_simt_kernel";
-  if (rows > fd::kMaxNarrowRows) return "fd_partial_wide_kernel";
-  const bool fused = with_output && cfg.merge == FD_MERGE_IN_KERNEL;
-  const Schedule sc = choose_schedule(cfg.schedule, path, kv8, dtype == FD_F32, d, Hkv,
-                                      page_size, fused, rows);
-  if (sc.heads) return "fd_partial_heads_kernel";
-  if (sc.persistent) return "fd_partial_persist_kernel";
-  return "fd_partial_mma_kernel";
+  const int64_t rows = (int64_t)Q * (Hq / Hkv);
+  if (rows > fd::kMaxRows) return nullptr;
+  const int32_t S = num_splits > 0 ? num_splits : heuristic_splits(B, Q, Hq, Hkv, d, L_cap);
+  return kernel_name(cfg, dtype, kv_dtype, d, Hkv, page_size, (int32_t)rows, with_output,
+                     (int64_t)B * Hkv, S);
 }
 
 size_t fd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_splits) {
@@ -552,10 +593,12 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
                 "more than %d query rows per kv head (%lld) run on the bf16 tensor-core paths only",
                 fd::kMaxNarrowRows, (long long)(Q * G));
 
-  // ---- schedule (fd_set_schedule or the call's options)
-  const bool fused = need_out && cfg.merge == FD_MERGE_IN_KERNEL;
+  // ---- schedule (fd_set_schedule or the call's options).  One split with an output:
+  // the partial pass writes the output itself (Params::direct) and nothing merges.
+  const bool direct = need_out && S == 1;
+  const bool fused = need_out && !direct && cfg.merge == FD_MERGE_IN_KERNEL;
   const Schedule sc = choose_schedule(cfg.schedule, path, kv8, q->dtype == FD_F32, d, Hkv,
-                                     paged ? page_size : 0, fused, Q * G);
+                                     paged ? page_size : 0, fused, Q * G, B * Hkv);
   const bool heads = sc.heads, persistent = sc.persistent;
 
   // ---- tensor maps (box height: one tile, or one page when pages are shorter; with head
@@ -608,6 +651,7 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   p.out_sh = out ? out->stride[multi ? 2 : 1] : 0;
   p.out_bf16 = out && out->dtype == FD_BF16 ? 1 : 0;
   p.lse_out = lse_out;
+  p.direct = 0;                     // set below, once the kernel is known
   p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
   p.kv_fp8 = kv8 ? 1 : 0;
   p.in_f32 = q->dtype == FD_F32 ? 1 : 0;
@@ -622,6 +666,7 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   // tile is read twice (split_len need not be a whole number of tiles: 128K tokens over
   // 19 splits, one CTA per SM, read 0.9% more bytes otherwise).
   p.tile_owned = path == FD_PATH_TCGEN05 ? 1 : 0;
+  p.direct = direct && (path != FD_PATH_MMA || fd::mma_writes_direct(p)) ? 1 : 0;
 
   pr->path = path;
   pr->dtype = q->dtype;
@@ -675,7 +720,7 @@ fd_status run_decode(CacheKind kind, const fd_tensor* q, const fd_tensor* k_cach
   if (need_out && pr.fused) return launch_partial(pr, s);   // one launch merges in-kernel
   pr.p.counters = nullptr;          // the merge, if any, is a separate kernel
   st = launch_partial(pr, s);
-  if (st != FD_OK || !need_out) return st;
+  if (st != FD_OK || !need_out || pr.p.direct) return st;   // direct: out is written
   return launch_merge(pr.p, s);
 }
 

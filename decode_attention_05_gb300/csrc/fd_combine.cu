@@ -120,12 +120,15 @@ __global__ void __launch_bounds__(128) fd_combine_kernel(const __grid_constant__
   }
 }
 
-// Many rows: one warp per row, kRowWarps rows per CTA (merge_row, the same fold with
-// the splits of a row in one warp).  A CTA of four warps per row spreads a row's splits
-// but lives only as long as one row's loads; with thousands of rows (large batches,
-// usually with few splits each) the launch of those short CTAs, not their memory
-// traffic, set the pass's time.
+// Many rows with few splits: one warp per row, kRowWarps rows per CTA (merge_row, the
+// same fold with the splits of a row in one warp, all kRowSplits loads in flight at
+// once).  A CTA of four warps per row spreads a row's splits but lives only as long as
+// one row's loads; with thousands of rows (large batches, usually with few splits each)
+// the launch of those short CTAs, not their memory traffic, set the pass's time.  With
+// more splits per row the four warps' parallel loads win (1024 rows of 19 splits:
+// 41.8 us a step with four warps per row, 42.5 with one).
 constexpr int kRowWarps = 8;
+constexpr int kRowSplits = 8;
 constexpr int64_t kRowsPerWarpMin = 1024;   // rows from which the warp-per-row form runs
 
 template <int D>
@@ -134,12 +137,12 @@ __global__ void __launch_bounds__(kRowWarps * 32) fd_combine_rows_kernel(const _
   pdl_wait();
   const int64_t row = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   if (row >= (int64_t)p.B * p.Q * p.Hq) return;
-  merge_row<D, 8>(p, row, threadIdx.x & 31);
+  merge_row<D, kRowSplits>(p, row, threadIdx.x & 31);
 }
 
 cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool pdl) {
   const int64_t rows = (int64_t)p.B * p.Q * p.Hq;
-  const bool by_rows = rows >= kRowsPerWarpMin;
+  const bool by_rows = rows >= kRowsPerWarpMin && p.S <= kRowSplits;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(by_rows ? (rows + kRowWarps - 1) / kRowWarps : rows));
   cfg.blockDim = dim3(by_rows ? kRowWarps * 32 : 128);

@@ -29,7 +29,7 @@ __device__ __forceinline__ float lg2_approx(float x) {
 
 // Split epilogue for an empty (or aborted) split: LSE_i = -inf for the whole group.
 __device__ __forceinline__ void write_empty_split(const Params& p, const SplitInfo& si, int tid) {
-  if (tid < p.n_rows) p.lse_part[flat_row(p, si.b, si.g, tid) * p.S + si.split] = kNegInf;
+  if (tid < p.n_rows) put_empty_row(p, si.b, si.g, tid, si.split);
 }
 
 // Index of (warp w, row h, dim j) in the merge scratch macc [NCW][G][D].  The dims of
@@ -50,7 +50,7 @@ __device__ __forceinline__ int macc_index(int w, int h, int j) {
 // visible to all (it returns false if the threads could not meet; nothing more is
 // written then); every thread then forms 4 output dims at a time.  Returns sync's
 // answer.
-template <int G, int D, int NCW, class Sync>
+template <int G, int D, int NCW, bool DIRECT = true, class Sync>
 __device__ __forceinline__ bool merge_warps_and_store(const Params& p, const SplitInfo& si,
                                                       const float* macc, float* mm, float* ml,
                                                       int ctid, Sync&& sync) {
@@ -70,11 +70,32 @@ __device__ __forceinline__ bool merge_warps_and_store(const Params& p, const Spl
 #pragma unroll
     for (int w = 0; w < NCW; ++w) mm[w * G + h] = c[w] * inv;
     ml[h] = L;
-    const int64_t row = flat_row(p, si.b, si.g, h);
-    p.lse_part[row * p.S + si.split] = L > 0.f ? (M + lg2_approx(L)) * 0.6931471805599453f : kNegInf;
+    put_lse<DIRECT>(p, si.b, si.g, h, si.split,
+                    L > 0.f ? (M + lg2_approx(L)) * 0.6931471805599453f : kNegInf);
   }
   if (!sync()) return false;
   constexpr int D4 = D / 4;
+  if (DIRECT && p.direct) {
+    // A single split's result is the output: every row is written, zeros for a row
+    // without keys.
+    for (int idx = ctid; idx < p.n_rows * D4; idx += NCW * 32) {
+      const int h = idx / D4, j = (idx - h * D4) * 4;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ml[h] > 0.f) {
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+          const float f = mm[w * G + h];
+          const float4 a = *reinterpret_cast<const float4*>(macc + macc_index<G, D>(w, h, j));
+          o.x = fmaf(a.x, f, o.x);
+          o.y = fmaf(a.y, f, o.y);
+          o.z = fmaf(a.z, f, o.z);
+          o.w = fmaf(a.w, f, o.w);
+        }
+      }
+      put_o4<D>(p, si.b, si.g, h, si.split, j, o);
+    }
+    return true;
+  }
   for (int idx = ctid; idx < p.n_rows * D4; idx += NCW * 32) {
     const int h = idx / D4, j = (idx - h * D4) * 4;
     if (!(ml[h] > 0.f)) continue;                   // no key in the split: no O_i

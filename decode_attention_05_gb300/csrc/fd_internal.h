@@ -85,6 +85,9 @@ struct Params {
   int64_t out_sb, out_sj, out_sh;
   int32_t out_bf16;       // 1: bf16 out, 0: f32 out
   float* lse_out;         // [B, Q, Hq] or nullptr
+  // 1: a single split whose result is the output: the partial pass writes out and
+  // lse_out itself and no merge runs (put_* in fd_pipeline.cuh); 0: it writes partials
+  int32_t direct;
   float scale_log2;       // log2(e) / sqrt(d): scores are kept in base-2 units inside kernels
   // FP8 KV cache (E4M3 codes): per-kv-head dequantisation scales [Hkv] (nullptr = 1)
   int32_t kv_fp8;
@@ -101,6 +104,9 @@ cudaError_t launch_partial_tc(const Params& p, const CUtensorMap& tk, const CUte
                               cudaStream_t stream);
 cudaError_t launch_partial_simt(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                 int dtype, cudaStream_t stream);
+// Whether the mma.sync kernel launch_partial_mma picks for p writes a single split's
+// result as the output when p.direct is set (otherwise the host runs the merge).
+bool mma_writes_direct(const Params& p);
 cudaError_t launch_partial_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream);
 cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool pdl);

@@ -603,6 +603,11 @@ struct Consumer {
     }
   }
 
+  // Whether store_own can write a single split's result as the output (Params::direct):
+  // not for 16 rows per warp, where the head-group and wide kernels sit at their
+  // register cap (the direct branch made them spill); mma_writes_direct tells the host.
+  static constexpr bool kDirect = SH::G <= 8;
+
   // End of a split when this warp alone saw all of it (head-group tiles: one warp per kv
   // head): write O_i = acc / l and LSE_i = (m + log2 l) ln 2 of the warp's rows directly,
   // the single-warp case of merge_warps_and_store.
@@ -615,6 +620,31 @@ struct Consumer {
         l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
         l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
       }
+    constexpr bool PAIRED = SH::KV8 || SH::F32;
+    const int d0 = PAIRED ? 2 * qr : qr, d1 = PAIRED ? 2 * qr + 1 : qr + 8;
+    if constexpr (kDirect) {
+      if (p.direct) {               // the row of out; a row without keys gets zeros
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int h = row0 + nt * 8 + qc + e;
+            if (h >= p.n_rows) continue;
+            const float L = l[nt][e];
+            const int64_t o = out_elem(p, b, g, h);
+#pragma unroll
+            for (int mt = 0; mt < SH::MTILES; ++mt) {
+              put_out(p, o + mt * 16 + d0, L > 0.f ? acc[nt][mt][e] * vsc / L : 0.f);
+              put_out(p, o + mt * 16 + d1, L > 0.f ? acc[nt][mt][2 + e] * vsc / L : 0.f);
+            }
+            if (qr == 0)
+              put_lse(p, b, g, h, split,
+                      L > 0.f ? (m[nt][e] + lg2_approx(L)) * 0.6931471805599453f : kNegInf);
+          }
+        }
+        return;
+      }
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -627,8 +657,6 @@ struct Consumer {
           float* o = p.o_part + (row * p.S + split) * SH::D;
 #pragma unroll
           for (int mt = 0; mt < SH::MTILES; ++mt) {
-            constexpr bool PAIRED = SH::KV8 || SH::F32;
-            const int d0 = PAIRED ? 2 * qr : qr, d1 = PAIRED ? 2 * qr + 1 : qr + 8;
             o[mt * 16 + d0] = acc[nt][mt][e] * vsc / L;
             o[mt * 16 + d1] = acc[nt][mt][2 + e] * vsc / L;
           }
@@ -818,8 +846,7 @@ __global__ void __maxnreg__(200)
   pdl_trigger();
   if (aborted) {                    // this warp's rows of the split: weight 0
     const int h = warp * SH::G + lane;
-    if (lane < SH::G && h < p.n_rows)
-      p.lse_part[flat_row(p, si.b, si.g, h) * p.S + si.split] = kNegInf;
+    if (lane < SH::G && h < p.n_rows) put_empty_row<Consumer<SH>::kDirect>(p, si.b, si.g, h, si.split);
   } else {
     c.store_own(p, si.b, si.g, si.split, lane);
   }
@@ -844,8 +871,12 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
                 "one 16-token page slice per consumer warp");
   // (Not with 16 query rows per kv head: there its registers would spill.)
   if constexpr (SH::G <= 8) {
-    if (threadIdx.x == SH::NCW * 32)
-      prefetch_first_pages<TOK>(p, &tk, &tv, kPrefetchHeadTiles, (int)blockIdx.y * kHeadGroup);
+    if (threadIdx.x == SH::NCW * 32) {
+      if (p.block_table != nullptr)
+        prefetch_first_pages<TOK>(p, &tk, &tv, kPrefetchHeadTiles, (int)blockIdx.y * kHeadGroup);
+      else
+        prefetch_first_tiles<TOK>(p, &tk, &tv, kPrefetchHeadTiles, (int)blockIdx.y * kHeadGroup);
+    }
   }
   pdl_wait();                       // inputs of this step are visible
   SplitInfo si = split_info<TOK>(p);
@@ -857,7 +888,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (si.n_tiles == 0) {            // empty split for every head of the group
     for (int i = threadIdx.x; i < kHeadGroup * p.n_rows; i += blockDim.x)
-      p.lse_part[flat_row(p, si.b, si.g + i / p.n_rows, i % p.n_rows) * p.S + si.split] = kNegInf;
+      put_empty_row<Consumer<SH>::kDirect>(p, si.b, si.g + i / p.n_rows, i % p.n_rows, si.split);
     pdl_trigger();
     return;
   }
@@ -908,7 +939,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   }
   pdl_trigger();
   if (aborted || *reinterpret_cast<volatile int32_t*>(&ctl->abort)) {
-    if (lane < p.n_rows) p.lse_part[flat_row(p, si.b, g, lane) * p.S + si.split] = kNegInf;
+    if (lane < p.n_rows) put_empty_row<Consumer<SH>::kDirect>(p, si.b, g, lane, si.split);
     return;
   }
   c.store_own(p, si.b, g, si.split, lane);
@@ -926,6 +957,10 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
                               const __grid_constant__ CUtensorMap tv,
                               const __grid_constant__ Params p) {
   constexpr int G = SH::G, TT = SH::TT, STAGES = SH::STAGES;
+  // (Not with 16 query rows per kv head, whose registers are at the cap.)
+  if constexpr (G <= 8) {
+    if (threadIdx.x == SH::NCW * 32) prefetch_first_item<TT>(p, &tk, &tv, kPrefetchTiles);
+  }
   pdl_wait();                       // inputs of this step are visible
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>(
@@ -947,7 +982,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   if (warp == SH::NCW) {
     prefetch_tensormap(&tk);
     prefetch_tensormap(&tv);
-    produce_items<TT, STAGES>(p, &tk, &tv, stages, ctl, lane);
+    produce_items<TT, STAGES, (G <= 8)>(p, &tk, &tv, stages, ctl, lane);
     pdl_trigger();
     return;
   }
@@ -1006,7 +1041,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
       si.b = mt.b;
       si.g = mt.g;
       si.split = mt.split;
-      if (!merge_warps_and_store<G, SH::D, SH::NCW>(p, si, macc, ctl->mm, ctl->ml, threadIdx.x,
+      if (!merge_warps_and_store<G, SH::D, SH::NCW, (G <= 8)>(p, si, macc, ctl->mm, ctl->ml, threadIdx.x,
                                                     [&] { return meet(2); })) {
         give_up();
         break;
@@ -1112,6 +1147,16 @@ cudaError_t dispatch_kind(const Params& p, const CUtensorMap& tk, const CUtensor
 }
 
 }  // namespace
+
+// The kernels launch_partial_mma runs with 16 rows per warp -- head groups, the wide
+// kernel for 33 to 64 rows and the persistent schedule -- write partials only (their
+// Consumer<SH>::kDirect / DIRECT forms); every other instantiation also writes a single
+// split's result as the output.
+bool mma_writes_direct(const Params& p) {
+  const int r = rows_template(p.n_rows);
+  if (p.head_group || p.persistent) return r <= 8;
+  return r != 64;
+}
 
 cudaError_t launch_partial_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream) {

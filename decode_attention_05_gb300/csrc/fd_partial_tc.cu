@@ -666,9 +666,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int q = 0; q < NPART; ++q) mm[q * R + t] = c[q] * inv;
         lrow[t] = L;
-        const int64_t row = flat_row(p, si.b, si.g, t);
-        p.lse_part[row * p.S + si.split] =
-            L > 0.f ? (M + lg2_approx(L)) * 0.6931471805599453f : kNegInf;
+        put_lse(p, si.b, si.g, t, si.split,
+                L > 0.f ? (M + lg2_approx(L)) * 0.6931471805599453f : kNegInf);
       }
       named_bar_sync(1, kTcSoftThreads);
       // All 256 threads write O_i: thread t takes dims 4 (t mod 32) .. + 3 of the rows
@@ -681,8 +680,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int k = 0; k < R / 8; ++k) {
         const int hr = (t >> 5) + 8 * k;
-        if (hr < p.n_rows && lrow[hr] > 0.f) {        // no key in the split: no O_i
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (hr >= p.n_rows) continue;
+        const bool live = lrow[hr] > 0.f;
+        if (!live && !p.direct) continue;           // no key in the split: no O_i
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live) {
 #pragma unroll
           for (int q = 0; q < NPART; ++q) {
             const float f = mm[q * R + hr];
@@ -693,6 +695,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             acc.z = fmaf(a.z, f, acc.z);
             acc.w = fmaf(a.w, f, acc.w);
           }
+        }
+        if (p.direct) {
+          put_o4<kTcD>(p, si.b, si.g, hr, si.split, c4 * 4, acc);
+        } else {
           const int64_t row = ((int64_t)si.b * p.Q + (hr >> lgG)) * p.Hq +
                               (int64_t)si.g * p.G + (hr & (p.G - 1));
           *reinterpret_cast<float4*>(obase + row * ostride) = acc;

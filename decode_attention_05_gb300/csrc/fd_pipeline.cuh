@@ -147,6 +147,71 @@ __device__ __forceinline__ int64_t key_bound(const Params& p, int64_t L, int rho
   return L - p.Q + 1 + rho / p.G;
 }
 
+// ---------------------------------------------------------------- split results
+//
+// A split writes its normalised output O_i and LSE_i to the workspace partials -- except
+// when the call has one split and asks for the output (Params::direct).  The merge is
+// then the identity: the one weight is 2^(LSE_1 - LSE_1) = 1, so out = O_1 and
+// lse_out = LSE_1, and the partial pass writes out and lse_out itself (no O_i round trip
+// through memory, no merge launch).  A row that the split leaves without a key gets
+// out = 0 and lse_out = -inf there, as the merge would give it.
+__device__ __forceinline__ int64_t out_elem(const Params& p, int b, int g, int rho) {
+  const int j = rho / p.G, h = rho - j * p.G;
+  return (int64_t)b * p.out_sb + (int64_t)j * p.out_sj + ((int64_t)g * p.G + h) * p.out_sh;
+}
+__device__ __forceinline__ void put_out(const Params& p, int64_t e, float v) {
+  if (p.out_bf16) {
+    reinterpret_cast<__nv_bfloat16*>(p.out)[e] = __float2bfloat16_rn(v);
+  } else {
+    reinterpret_cast<float*>(p.out)[e] = v;
+  }
+}
+// LSE_i of row rho of group (b, g).  DIRECT = false: a kernel that never runs with
+// Params::direct (its partials-only form, for instantiations at their register cap).
+template <bool DIRECT = true>
+__device__ __forceinline__ void put_lse(const Params& p, int b, int g, int rho, int split, float v) {
+  const int64_t row = flat_row(p, b, g, rho);
+  if (!DIRECT || !p.direct) {
+    p.lse_part[row * p.S + split] = v;
+  } else if (p.lse_out != nullptr) {
+    p.lse_out[row] = v;
+  }
+}
+// Dims j .. j + 3 of O_i of row rho of group (b, g).
+template <int D>
+__device__ __forceinline__ void put_o4(const Params& p, int b, int g, int rho, int split, int j,
+                                       float4 o) {
+  if (!p.direct) {
+    *reinterpret_cast<float4*>(p.o_part + (flat_row(p, b, g, rho) * p.S + split) * D + j) = o;
+  } else {
+    const int64_t e = out_elem(p, b, g, rho) + j;
+    put_out(p, e, o.x);
+    put_out(p, e + 1, o.y);
+    put_out(p, e + 2, o.z);
+    put_out(p, e + 3, o.w);
+  }
+}
+// Dim j of O_i of row rho of group (b, g).
+template <int D>
+__device__ __forceinline__ void put_o1(const Params& p, int b, int g, int rho, int split, int j,
+                                       float v) {
+  if (!p.direct) {
+    p.o_part[(flat_row(p, b, g, rho) * p.S + split) * D + j] = v;
+  } else {
+    put_out(p, out_elem(p, b, g, rho) + j, v);
+  }
+}
+// Row rho of group (b, g) has no key in the split (or its split was abandoned): LSE_i =
+// -inf and no O_i -- weight 0 in the merge; with direct output, out = 0 and -inf.
+template <bool DIRECT = true>
+__device__ __forceinline__ void put_empty_row(const Params& p, int b, int g, int rho, int split) {
+  put_lse<DIRECT>(p, b, g, rho, split, kNegInf);
+  if (DIRECT && p.direct) {
+    const int64_t e = out_elem(p, b, g, rho);
+    for (int j = 0; j < p.d; ++j) put_out(p, e + j, 0.f);
+  }
+}
+
 // Take a ticket on an epoch-tagged counter word (the fused merge's per-group
 // arrivals).  A counter word holds
 // (epoch << 32 | arrivals).  Each call brings a fresh epoch, so the first arrival of a
@@ -207,10 +272,52 @@ struct PersistCtl {
   int32_t abort;
 };
 
+// Item x of the persistent schedule: its split, kv head and row.
+struct Item {
+  int split, g, b;
+};
+__device__ __forceinline__ Item item_of(const Params& p, int64_t x) {
+  const int64_t per_split = (int64_t)p.Hkv * p.B;
+  const int64_t r = x % per_split;
+  return Item{p.S - 1 - (int)(x / per_split), (int)(r % p.Hkv), (int)(r / p.Hkv)};
+}
+
+// The first `count` tiles of the CTA's first item (item blockIdx.x: the first item of
+// every CTA is its own, the queue hands out the rest) prefetched into L2 before the
+// kernel waits for the previous kernel of the stream: the row length and page ids are
+// read relaxed -- a hint only, the producer reads them again after the wait.  Pages
+// shorter than a tile are not prefetched.
+template <int TT>
+__device__ __forceinline__ void prefetch_first_item(const Params& p, const CUtensorMap* tk,
+                                                    const CUtensorMap* tv, int count) {
+  const Item it = item_of(p, (int64_t)blockIdx.x);
+  const int64_t L = min(max((int64_t)ld_relaxed_s32(p.seq_lens + it.b), (int64_t)0), p.L_cap);
+  const int64_t lo = (int64_t)it.split * p.split_len;
+  const int64_t hi = min(lo + p.split_len, L);
+  const int64_t T0 = lo / TT * TT;
+  const bool paged = p.block_table != nullptr;
+  if (paged && p.page_size < TT) return;
+#pragma unroll 1
+  for (int k = 0; k < count; ++k) {
+    const int64_t t0 = T0 + (int64_t)k * TT;
+    if (t0 >= hi) break;
+    if (!paged) {
+      tma_prefetch_5d(tk, 0, (int)t0, 0, it.g, it.b);
+      tma_prefetch_5d(tv, 0, (int)t0, 0, it.g, it.b);
+    } else {
+      const int32_t id = ld_relaxed_s32(p.block_table + (int64_t)it.b * p.bt_sb + (t0 >> p.log2_page));
+      if (id < 0 || (int64_t)id >= p.num_pages) continue;
+      const int slot = (int)(t0 & (p.page_size - 1));
+      tma_prefetch_5d(tk, 0, slot, 0, it.g, id);
+      tma_prefetch_5d(tv, 0, slot, 0, it.g, id);
+    }
+  }
+}
+
 // Producer warp of the persistent kernel: takes items from the queue and streams their
 // tiles into the ring without a break between items; publishes a kDone stage at the
 // end.  Empty items get their LSE_i = -inf written here and never reach the consumers.
-template <int TT, int STAGES>
+template <int TT, int STAGES, bool DIRECT>
 __device__ __forceinline__ void produce_items(const Params& p, const CUtensorMap* tk,
                                               const CUtensorMap* tv, uint8_t* stages,
                                               PersistCtl<STAGES>* ctl, int lane) {
@@ -237,20 +344,19 @@ __device__ __forceinline__ void produce_items(const Params& p, const CUtensorMap
     return ok != 0;
   };
 
-  // Items come from a plain fetch-and-add on the queue word (zero at launch: a fresh
-  // workspace header is zero and the last CTA of every launch puts it back).  The next
-  // item's ticket is taken when an item starts, so its latency hides behind the item.
-  unsigned long long ticket = 0;
-  if (lane == 0) ticket = atomicAdd(p.item_queue, 1ull);
+  // The CTA's first item is item blockIdx.x (the grid never has more CTAs than items);
+  // the others come from a plain fetch-and-add on the queue word, offset by the grid
+  // size (the word is zero at launch: a fresh workspace header is zero and the last CTA
+  // of every launch puts it back).  The next item's ticket is taken when an item starts,
+  // so its latency hides behind the item.
+  unsigned long long ticket = blockIdx.x;
   while (!aborted) {
     if (__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int32_t*>(&ctl->abort), 0)) break;
     const int64_t item = (int64_t)__shfl_sync(0xffffffffu, ticket, 0);
     if (item >= n_items) break;
-    if (lane == 0) ticket = atomicAdd(p.item_queue, 1ull);
-    const int64_t per_split = (int64_t)p.Hkv * p.B;
-    const int split = p.S - 1 - (int)(item / per_split);
-    const int g = (int)((item % per_split) % p.Hkv);
-    const int b = (int)((item % per_split) / p.Hkv);
+    if (lane == 0) ticket = gridDim.x + atomicAdd(p.item_queue, 1ull);
+    const Item it = item_of(p, item);
+    const int split = it.split, g = it.g, b = it.b;
     int64_t L = p.seq_lens[b];
     if (L < 0 || L > p.L_cap) {
       if (lane == 0) atomicOr(p.flags, FD_DEVFLAG_SEQ_LEN);
@@ -259,7 +365,7 @@ __device__ __forceinline__ void produce_items(const Params& p, const CUtensorMap
     const int64_t lo = (int64_t)split * p.split_len;
     const int64_t hi = min(lo + p.split_len, L);
     if (lo >= hi) {                 // empty split: weight 0 in the merge
-      if (lane < p.n_rows) p.lse_part[flat_row(p, b, g, lane) * p.S + split] = kNegInf;
+      if (lane < p.n_rows) put_empty_row<DIRECT>(p, b, g, lane, split);
       continue;
     }
     const int64_t T0 = lo / TT * TT;

@@ -125,7 +125,12 @@ typedef enum {
  *   page_size    0 for a contiguous cache; else a power of two in [8, 65536].
  *   num_splits   S >= 1, or 0 for the count fd_resolve_num_splits_q reports (the
  *                capacity heuristic; one CTA's worth per SM for more than 16 rows per
- *                kv head).  S <= 4096.
+ *                kv head).  S <= 4096.  With S = 1 the merge is the identity (the one
+ *                weight is 1): the partial pass then writes out and lse_out itself and
+ *                no merge kernel runs, whatever the merge mode -- except on the
+ *                16-rows-per-warp mma.sync kernels (head groups or the persistent
+ *                schedule with 9-16 rows, the wide kernel with 33-64 rows), which write
+ *                partials that the merge kernel then reads.
  *   out          device, q's shape, bf16 or f32 (bf16 is rounded to nearest even).
  *   lse_out      device f32 [B, Hq] or [B, Q, Hq] (contiguous), natural log; may be NULL.
  *   workspace    device scratch of at least fd_workspace_size(B, Q * Hq, Hkv, d, S) bytes,
@@ -376,10 +381,11 @@ FD_API int32_t fd_get_path(void);
  * header and stream their tiles back to back.  Same partials as FD_SCHEDULE_GRID, bit
  * for bit (the per-item arithmetic is shared).
  * FD_SCHEDULE_HEAD_GROUPS: one CTA per (split, group of 4 kv heads, row); a tile is 16
- * tokens of one page for all 4 heads, loaded as one 16 KB TMA box instead of four 4 KB
- * ones, and each consumer warp keeps one head's state.  For paged bf16 caches with
- * d = 128, 16- or 32-token pages and Hkv a multiple of 4; other calls run the grid
- * schedule.  Same results up to rounding order.
+ * tokens of a row (of one page) for all 4 heads, loaded as one 16 KB TMA box, and each
+ * consumer warp keeps one head's state (no cross-warp merge).  For bf16 caches with
+ * d = 128, Hkv a multiple of 4 and up to 16 query rows per kv head, contiguous or with
+ * pages of at least 16 tokens; other calls run the grid schedule.  Same results up to
+ * rounding order.
  * FD_SCHEDULE_TAIL_SHARING: the grid schedule, and a CTA that has finished its own
  * split goes on with tiles taken from the back of a split of the same (b, kv head)
  * that is still in progress (claim words in the workspace; each CTA's stream stays
@@ -389,7 +395,11 @@ FD_API int32_t fd_get_path(void);
  * run, so results are equal up to rounding order.  The tcgen05 kernel only; measured
  * slower than the grid schedule on GB300 (the owners' claims cost more than the tail
  * they recover), so it is never chosen automatically.
- * FD_SCHEDULE_AUTO (default): head groups where they apply, else grid.
+ * FD_SCHEDULE_AUTO (default): head groups where they apply with 16- or 32-token pages
+ * (one 16 KB box instead of four 4 KB ones), and for contiguous caches or larger pages
+ * when the batch holds at least 5 (b, kv head) pairs per SM (B x Hkv >= 5 x SMs) with up
+ * to 8 query rows per kv head (many short CTAs otherwise; measured 10-30% faster there);
+ * else grid.
  * The persistent and head-group schedules run only with FD_MERGE_KERNEL (or
  * fd_decode_partial) and on the mma.sync path; otherwise the grid schedule runs (with
  * tail sharing on the tcgen05 kernel under FD_SCHEDULE_TAIL_SHARING).
@@ -474,11 +484,14 @@ FD_API fd_status fd_selftest_stalled_decode(const fd_tensor* q, const fd_tensor*
 /*
  * Name of the partial-pass kernel a call would launch under the current process
  * settings (path, merge mode, schedule): "fd_partial_mma_kernel",
- * "fd_partial_heads_kernel", "fd_partial_wide_kernel", "fd_partial_persist_kernel" or
- * "fd_partial_simt_kernel".  dtype is q's fd_dtype, kv_dtype the cache's; page_size 0
- * for a contiguous cache; rows the query rows per kv head (Q x Hq / Hkv); with_output
- * 1 for fd_decode_attention, 0 for fd_decode_partial.  NULL for a
- * combination no entry point accepts.  Static string; host only.
+ * "fd_partial_heads_kernel", "fd_partial_wide_kernel", "fd_partial_persist_kernel",
+ * "fd_partial_tc_kernel" or "fd_partial_simt_kernel".  dtype is q's fd_dtype, kv_dtype
+ * the cache's; page_size 0 for a contiguous cache; rows the query rows per kv head
+ * (Q x Hq / Hkv); with_output 1 for fd_decode_attention, 0 for fd_decode_partial.  For
+ * a call of more than one split and fewer than 5 (b, kv head) pairs per SM: with one
+ * split FD_MERGE_IN_KERNEL does not apply (see num_splits above), and large batches may
+ * take head groups -- fd_partial_kernel_name_for answers for a call's exact sizes.  NULL
+ * for a combination no entry point accepts.  Static string; host only.
  */
 FD_API const char* fd_partial_kernel_name(int32_t dtype, int32_t kv_dtype, int32_t d, int32_t Hkv,
                                           int32_t page_size, int32_t rows, int32_t with_output);
@@ -488,6 +501,18 @@ FD_API const char* fd_partial_kernel_name_ex(const fd_options* options, int32_t 
                                              int32_t kv_dtype, int32_t d, int32_t Hkv,
                                              int32_t page_size, int32_t rows,
                                              int32_t with_output);
+/* The kernel of one call with these sizes exactly: B rows, Q query tokens, Hq query and
+ * Hkv kv heads, head dim d, page_size (0: contiguous), capacity L_cap and num_splits
+ * (0: the count fd_resolve_num_splits_q reports), under `options` (NULL = the
+ * process-wide settings).  Unlike fd_partial_kernel_name it sees the batch size (the
+ * automatic schedule takes head groups for large batches) and the split count (one
+ * split with an output never merges in-kernel).  Uses the current device's SM count.
+ * NULL for a combination no entry point accepts. */
+FD_API const char* fd_partial_kernel_name_for(const fd_options* options, int32_t dtype,
+                                              int32_t kv_dtype, int32_t B, int32_t Q,
+                                              int32_t Hq, int32_t Hkv, int32_t d,
+                                              int32_t page_size, int64_t L_cap,
+                                              int32_t num_splits, int32_t with_output);
 
 /* Split count a single-token call with these sizes and this num_splits argument would use. */
 FD_API int32_t fd_resolve_num_splits(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int64_t L_cap,

@@ -323,6 +323,33 @@ def test_validation(case, expected):
 
 # ---------------------------------------------------------------- per-call options
 
+def test_partial_kernel_name_for_sized_calls():
+    """The kernel of a call with exact sizes: one split with an output never merges
+    in-kernel (so small pages keep head groups under FD_MERGE_IN_KERNEL), forced head
+    groups take contiguous caches and large pages, and bad sizes give None.  (Without a
+    device the SM count is unknown and the large-batch rule never applies.)"""
+    import torch
+    bf = torch.bfloat16
+    name = fd.partial_kernel_name_for
+    inkernel = fd.options(merge_mode=fd.FD_MERGE_IN_KERNEL)
+    assert name(bf, bf, 4, 1, 32, 8, 128, 16, 4096, 1, options=inkernel) == "fd_partial_heads_kernel"
+    assert name(bf, bf, 4, 1, 32, 8, 128, 16, 4096, 4, options=inkernel) == "fd_partial_mma_kernel"
+    assert name(bf, bf, 4, 1, 32, 8, 128, 16, 4096, 4, with_output=False,
+                options=inkernel) == "fd_partial_heads_kernel"
+    heads = fd.options(schedule=fd.FD_SCHEDULE_HEAD_GROUPS)
+    assert name(bf, bf, 4, 1, 32, 8, 128, 0, 4096, 4, options=heads) == "fd_partial_heads_kernel"
+    assert name(bf, bf, 4, 1, 32, 8, 128, 64, 4096, 4, options=heads) == "fd_partial_heads_kernel"
+    assert name(bf, bf, 4, 1, 32, 8, 128, 8, 4096, 4, options=heads) == "fd_partial_mma_kernel"
+    assert name(bf, bf, 4, 1, 24, 6, 128, 0, 4096, 4, options=heads) == "fd_partial_mma_kernel"
+    assert name(bf, bf, 4, 4, 32, 8, 128, 0, 4096, 4) == "fd_partial_mma_kernel"     # 16 rows
+    assert name(bf, bf, 4, 8, 32, 8, 128, 0, 4096, 4) == "fd_partial_tc_kernel"      # 32 rows
+    for bad in ((0, 1, 32, 8), (4, 0, 32, 8), (4, 1, 30, 8), (4, 1, 32, 0), (4, 17, 32, 8)):
+        assert name(bf, bf, *bad, 128, 0, 4096, 4) is None
+    assert name(bf, bf, 4, 1, 32, 8, 128, 0, 0, 4) is None
+    assert name(bf, bf, 4, 1, 32, 8, 128, 0, 4096, -1) is None
+    assert name(bf, bf, 4, 1, 32, 8, 128, 0, 4096, 4, options=fd.options(path=9)) is None
+
+
 def test_options_choose_the_kernel_per_call():
     """fd_options override the process-wide settings for one query (and one call) and
     leave those settings as they were; FD_FROM_PROCESS fields follow them."""

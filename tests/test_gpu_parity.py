@@ -443,12 +443,13 @@ def test_sequence_sharded_merge(name, path):
 
 
 @pytest.mark.parametrize("d", [128, 64])
-@pytest.mark.parametrize("S", [0, 1, 3])
+@pytest.mark.parametrize("S", [0, 1, 2, 3, 8, 9])
 def test_large_batch_merge(d, S):
-    """Batches of 1024 query rows or more are merged one warp per row (not one CTA per
-    row): 48 rows x 32 heads of ragged lengths -- empty rows, one-key rows, rows that end
-    inside a split and splits with no key -- against the oracle, with the planner's split
-    count (one split here), one and three splits."""
+    """Batches of 1024 query rows or more with up to 8 splits are merged one warp per row
+    (not one CTA per row): 48 rows x 32 heads of ragged lengths -- empty rows, one-key
+    rows, rows that end inside a split and splits with no key -- against the oracle, with
+    the planner's split count, 2, 3 and 8 splits (one warp per row), 9 (one CTA per row)
+    and one split (no merge: the partial pass writes the output)."""
     import random
     rnd = random.Random(1000 + d)
     lens = [0, 1, 600, 599, 65] + [rnd.randint(0, 600) for _ in range(43)]

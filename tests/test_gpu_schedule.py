@@ -6,7 +6,7 @@ test_gpu_parity) and bit for bit against the grid schedule.  The queue in the wo
 header must also come back clean after each launch (several calls in a row, stale
 workspace contents, a replayed CUDA graph).
 
-Head groups: tiles of 16 tokens x 4 kv heads for small pages; checked against the
+Head groups: tiles of 16 tokens x 4 kv heads (small pages, contiguous caches); checked against the
 oracle and against the grid schedule up to rounding order.
 """
 import numpy as np
@@ -212,7 +212,7 @@ HEAD_LENS = [0, 1, 15, 16, 17, 37, 500, 2048]
 
 
 @pytest.mark.parametrize("ps,Hkv,G", [(16, 4, 1), (16, 4, 8), (16, 8, 4), (32, 8, 2),
-                                      (16, 12, 16), (32, 4, 16)])
+                                      (16, 12, 16), (32, 4, 16), (64, 8, 4), (256, 4, 2)])
 def test_head_groups_match_oracle_and_grid(ps, Hkv, G):
     """Tiles of 16 tokens x 4 kv heads (one TMA box), one consumer warp per head: against
     the oracle, and against the one-head-per-CTA grid schedule.  The outputs of the two
@@ -229,6 +229,72 @@ def test_head_groups_match_oracle_and_grid(ps, Hkv, G):
         assert torch.equal(torch.isneginf(lh), torch.isneginf(lg))
         fin = torch.isfinite(lg)
         assert torch.allclose(lh[fin], lg[fin], atol=1e-5, rtol=1e-6)
+
+
+@pytest.mark.parametrize("Hkv,G", [(4, 1), (8, 4), (12, 16), (4, 8)])
+def test_head_groups_contiguous(Hkv, G):
+    """Head-group tiles on a contiguous cache (16 tokens x 4 kv heads of a row, one TMA
+    box; stale slots past each length hold NaN; the last box of a row runs past the
+    capacity): against the oracle and the grid schedule's LSE, with 1, 5 and 33 splits."""
+    w = workloads.contiguous_case(len(HEAD_LENS), Hkv * G, Hkv, 128, 2050, HEAD_LENS,
+                                  seed=580 + Hkv + G, out_dtype=torch.float32)
+    ref_o, ref_l = ref_for(w)
+    wd = w.to("cuda")
+    for S in (1, 5, 33):
+        oh, lh = _run_sched(wd, w, S, fd.FD_SCHEDULE_HEAD_GROUPS)
+        check(w, oh.cpu().double().numpy(), lh.cpu().double().numpy(), ref_o, ref_l)
+        og, lg = _run_sched(wd, w, S, fd.FD_SCHEDULE_GRID)
+        assert torch.equal(torch.isneginf(lh), torch.isneginf(lg))
+        fin = torch.isfinite(lg)
+        assert torch.allclose(lh[fin], lg[fin], atol=1e-5, rtol=1e-6)
+
+
+def test_head_groups_contiguous_multi_token():
+    Q, G, Hkv, d = 2, 8, 8, 128
+    Hq = Hkv * G
+    lens = [1, 2, 65, 300, 1000]
+    w = workloads.contiguous_case(len(lens), Hq, Hkv, d, 1000, lens, seed=590,
+                                  out_dtype=torch.float32)
+    q4 = workloads.multi_token_queries(len(lens), Q, Hq, d, seed=591)
+    _, k, v, lens_np, bt, ps = w.oracle_arrays()
+    ref_o, ref_l = oracle.decode_causal(workloads.np_storage(q4), k, v, lens_np)
+    wd = w.to("cuda")
+    B = len(lens)
+    for S in (1, 3):
+        o, l = _run_sched(wd, w, S, fd.FD_SCHEDULE_HEAD_GROUPS, q=q4.cuda())
+        mw = workloads.Workload("mt", q4.reshape(B * Q, Hq, d), w.k, w.v, w.seq_lens)
+        check(mw, o.cpu().double().numpy().reshape(B * Q, Hq, d),
+              l.cpu().double().numpy().reshape(B * Q, Hq),
+              ref_o.reshape(B * Q, Hq, d), ref_l.reshape(B * Q, Hq))
+
+
+@pytest.mark.parametrize("paged", [0, 64])
+def test_head_groups_auto_for_large_batches(paged):
+    """The default schedule takes head groups on a contiguous cache (or 64-token pages)
+    once the batch holds 5 (b, kv head) pairs per SM, and the grid below that: a ragged
+    batch of that size against the oracle, and the kernel the sized name query reports
+    on both sides of the threshold."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Hkv, G = 8, 4
+    B = -(-5 * sms // Hkv)
+    import random
+    rnd = random.Random(600)
+    lens = [0, 1, 16, 17, 300] + [rnd.randint(1, 300) for _ in range(B - 5)]
+    if paged:
+        w = workloads.paged_case(B, Hkv * G, Hkv, 128, paged, 5, lens, seed=601,
+                                 out_dtype=torch.float32)
+    else:
+        w = workloads.contiguous_case(B, Hkv * G, Hkv, 128, 300, lens, seed=601,
+                                      out_dtype=torch.float32)
+    name = lambda b: fd.partial_kernel_name_for(torch.bfloat16, torch.bfloat16, b, 1, Hkv * G,
+                                                Hkv, 128, paged, w.L_cap)
+    assert name(B) == "fd_partial_heads_kernel"
+    assert name(B - 1) == "fd_partial_mma_kernel"
+    ref_o, ref_l = ref_for(w)
+    wd = w.to("cuda")
+    S = fd.resolve_num_splits(B, Hkv * G, Hkv, 128, w.L_cap, 0)
+    o, l = _run_sched(wd, w, S, fd.FD_SCHEDULE_AUTO)
+    check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
 
 
 def test_head_groups_bf16_out_and_auto_default():
@@ -301,13 +367,17 @@ def test_head_groups_partials_and_merge():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-@pytest.mark.parametrize("ps,Hkv", [(64, 4), (16, 2), (8, 4)])
+@pytest.mark.parametrize("ps,Hkv", [(16, 2), (8, 4), (0, 6)])
 def test_head_groups_fall_back_to_grid(ps, Hkv):
-    """Where head groups do not apply (pages of 64+ or 8 tokens, Hkv not a multiple of
-    4), the head-group setting runs the grid schedule: identical results."""
+    """Where head groups do not apply (8-token pages, Hkv not a multiple of 4), the
+    head-group setting runs the grid schedule: identical results."""
     lens = [700, 1, 129]
-    w = workloads.paged_case(3, Hkv * 4, Hkv, 128, ps, -(-1024 // ps), lens, seed=570 + ps,
-                             out_dtype=torch.float32)
+    if ps:
+        w = workloads.paged_case(3, Hkv * 4, Hkv, 128, ps, -(-1024 // ps), lens, seed=570 + ps,
+                                 out_dtype=torch.float32)
+    else:
+        w = workloads.contiguous_case(3, Hkv * 4, Hkv, 128, 1024, lens, seed=570,
+                                      out_dtype=torch.float32)
     wd = w.to("cuda")
     oh, lh = _run_sched(wd, w, 5, fd.FD_SCHEDULE_HEAD_GROUPS)
     og, lg = _run_sched(wd, w, 5, fd.FD_SCHEDULE_GRID)
