@@ -59,24 +59,33 @@ struct Schedule {
 // known -- the name-only queries).
 // f32 inputs on the tensor-core path run on the grid schedule only.
 //
-// Automatic head groups: always for 16- and 32-token pages (four 4 KB page boxes become
-// one 16 KB box); for contiguous caches and larger pages once the batch holds
-// kHeadsMinPairsPerSm (b, kv head) pairs per SM, with up to 8 query rows per kv head.
+// Automatic head groups: always for small pages (16 and 32 tokens bf16, 32 FP8: their
+// one-page boxes become one 16 KB box); for contiguous caches and larger pages once the
+// batch holds kHeadsMinPairsPerSm (b, kv head) pairs per SM, with up to 8 query rows per
+// kv head.
 // There one CTA streams four kv heads of a row without a cross-warp merge, and the grid
 // schedule's many short CTAs lose a start-up and an epilogue each.  Measured on GB300
 // (bf16, d = 128, 32 heads over 8 kv heads, one split, a step over 256-512 MiB of KV):
 // 128 rows of 512 tokens 50.0 -> 39.8 us, 256 x 512 92.1 -> 77.8, 512 x 256 101.6 ->
 // 84.8, 1024 x 128 127.7 -> 90.0, 96 x 1024 64.0 -> 60.1; below the threshold the grid
-// wins (64 x 1024: 42.0 against 49.6, whose 128 CTAs leave SMs idle).
+// wins (64 x 1024: 42.0 against 49.6, whose 128 CTAs leave SMs idle).  FP8 caches
+// (32-token tiles of 4 heads), same batches: 128 x 512 31.0 -> 22.8 us, 256 x 256 36.8
+// -> 26.3, 1024 x 128 102.5 -> 62.7; with 32-token pages 32 x 2048 41.7 -> 25.5.
 constexpr int64_t kHeadsMinPairsPerSm = 5;
 
 Schedule choose_schedule(int sched, int path, bool kv8, bool f32, int64_t d, int64_t Hkv,
                          int32_t page_size, bool fused, int64_t rows, int64_t pairs) {
   const bool narrow = rows <= fd::kMaxNarrowRows && !f32;
-  const bool head_ok = path == FD_PATH_MMA && !kv8 && d == 128 &&
-                       (page_size == 0 || page_size >= 16) &&
+  // A head-group tile holds head_tok tokens of each head (one 16 KB box of 4 heads): a
+  // page must hold at least that many.
+  const int32_t head_tok = kv8 ? 32 : 16;
+  const bool head_ok = path == FD_PATH_MMA && d == 128 &&
+                       (page_size == 0 || page_size >= head_tok) &&
                        Hkv % fd::kHeadGroup == 0 && !fused && narrow;
-  const bool small_pages = page_size == 16 || page_size == 32;
+  // Pages whose one-page boxes are small on the grid schedule: 16 and 32 tokens for bf16
+  // (4 and 8 KB), 32 for FP8 (4 KB).  (FP8 with 64-token pages keeps the grid for small
+  // batches: 32 rows of 2048 tokens 26.3 us on the grid, 51.2 with head groups.)
+  const bool small_pages = page_size == head_tok || (!kv8 && page_size == 2 * head_tok);
   const int sms = rows <= 8 && pairs > 0 ? fd::sm_count() : 0;   // 0: no device
   const bool big_batch = sms > 0 && pairs >= kHeadsMinPairsPerSm * sms;
   Schedule sc;
@@ -604,7 +613,8 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   // ---- tensor maps (box height: one tile, or one page when pages are shorter; with head
   // groups 16 rows of kHeadGroup heads)
   const int TT = fd::tile_tokens((int)d, es);
-  const uint32_t box_rows = heads ? 16u : (uint32_t)(paged && page_size < TT ? page_size : TT);
+  const uint32_t box_rows = heads ? (uint32_t)(TT / fd::kHeadGroup)     // 16 bf16, 32 FP8
+                                 : (uint32_t)(paged && page_size < TT ? page_size : TT);
   const uint32_t box_heads = heads ? (uint32_t)fd::kHeadGroup : 1u;
   fd_status st = make_kv_map(k_cache, box_rows, box_heads, &pr->tk);
   if (st != FD_OK) return st;

@@ -854,21 +854,24 @@ __global__ void __maxnreg__(200)
 }
 
 // ---------------------------------------------------------------- head-group tiles
-// One CTA per (split, group of kHeadGroup kv heads, row).  A tile is 16 tokens of one
-// page for the group's kHeadGroup heads: one TMA box of 16 rows x kHeadGroup heads
-// (16 KB) per K and V, laid out [head][line][row][128 B] -- the same shared-memory
-// layout as kHeadGroup page boxes of 16 rows, so the consumer's addressing is
-// unchanged: consumer warp w reads tile rows 16 w .. 16 w + 15, which are head
-// g0 + w's 16 tokens.  Each warp therefore sees every token of its own head in the
-// split and writes that head's partial itself; no cross-warp merge.
+// One CTA per (split, group of kHeadGroup kv heads, row).  A tile is TOK tokens (16 for
+// bf16, 32 for FP8) of the row -- of one page when paged -- for the group's kHeadGroup
+// heads: one TMA box of TOK rows x kHeadGroup heads (16 KB) per K and V, laid out
+// [head][line][row][128 B] -- the same shared-memory layout as kHeadGroup page boxes of
+// TOK rows, so the consumer's addressing is unchanged: consumer warp w reads tile rows
+// TOK w .. TOK w + TOK - 1, which are head g0 + w's TOK tokens.  Each warp therefore
+// sees every token of its own head in the split and writes that head's partial itself;
+// no cross-warp merge.
 template <class SH>
 __global__ void __launch_bounds__(SH::THREADS, 2)
     fd_partial_heads_kernel(const __grid_constant__ CUtensorMap tk,
                             const __grid_constant__ CUtensorMap tv,
                             const __grid_constant__ Params p) {
-  constexpr int STAGES = SH::STAGES, TOK = 16;
-  static_assert(SH::ROWS_PER_WARP == TOK && SH::CHUNKS == 1 && SH::NCW == kHeadGroup,
-                "one 16-token page slice per consumer warp");
+  // Tokens of one head in a tile: 16 (bf16) or 32 (FP8), so that the box of kHeadGroup
+  // heads is kTileBytes -- and exactly one consumer warp's rows of the tile.
+  constexpr int STAGES = SH::STAGES, TOK = SH::ROWS_PER_WARP;
+  static_assert(SH::NCW == kHeadGroup && TOK * kHeadGroup == SH::TT && !SH::WIDE && !SH::F32,
+                "one head's tokens per consumer warp");
   // (Not with 16 query rows per kv head: there its registers would spill.)
   if constexpr (SH::G <= 8) {
     if (threadIdx.x == SH::NCW * 32) {
@@ -1078,7 +1081,7 @@ cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap
     dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
     e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
   } else if (p.head_group) {
-    if constexpr (SH::D == 128 && !SH::KV8 && !SH::F32) {
+    if constexpr (SH::D == 128 && !SH::F32) {
       auto kernel = fd_partial_heads_kernel<SH>;
       static SmemOptIn opt_in;
       e = opt_in.apply(kernel, (int)SH::SMEM_BYTES);
@@ -1086,7 +1089,7 @@ cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap
       dim3 grid((unsigned)p.S, (unsigned)(p.Hkv / kHeadGroup), (unsigned)p.B);
       e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
     } else {
-      return cudaErrorInvalidValue;   // the host enables head groups for bf16 d = 128 only
+      return cudaErrorInvalidValue;   // the host enables head groups for d = 128 only
     }
   } else {
     auto kernel = fd_partial_mma_kernel<SH>;

@@ -381,11 +381,11 @@ FD_API int32_t fd_get_path(void);
  * header and stream their tiles back to back.  Same partials as FD_SCHEDULE_GRID, bit
  * for bit (the per-item arithmetic is shared).
  * FD_SCHEDULE_HEAD_GROUPS: one CTA per (split, group of 4 kv heads, row); a tile is 16
- * tokens of a row (of one page) for all 4 heads, loaded as one 16 KB TMA box, and each
- * consumer warp keeps one head's state (no cross-warp merge).  For bf16 caches with
- * d = 128, Hkv a multiple of 4 and up to 16 query rows per kv head, contiguous or with
- * pages of at least 16 tokens; other calls run the grid schedule.  Same results up to
- * rounding order.
+ * tokens (bf16; 32 for FP8 E4M3) of a row -- of one page -- for all 4 heads, loaded as
+ * one 16 KB TMA box, and each consumer warp keeps one head's state (no cross-warp
+ * merge).  For bf16 or FP8 caches with d = 128, Hkv a multiple of 4 and up to 16 query
+ * rows per kv head, contiguous or with pages of at least one tile's tokens; other calls
+ * run the grid schedule.  Same results up to rounding order.
  * FD_SCHEDULE_TAIL_SHARING: the grid schedule, and a CTA that has finished its own
  * split goes on with tiles taken from the back of a split of the same (b, kv head)
  * that is still in progress (claim words in the workspace; each CTA's stream stays
@@ -395,11 +395,11 @@ FD_API int32_t fd_get_path(void);
  * run, so results are equal up to rounding order.  The tcgen05 kernel only; measured
  * slower than the grid schedule on GB300 (the owners' claims cost more than the tail
  * they recover), so it is never chosen automatically.
- * FD_SCHEDULE_AUTO (default): head groups where they apply with 16- or 32-token pages
- * (one 16 KB box instead of four 4 KB ones), and for contiguous caches or larger pages
- * when the batch holds at least 5 (b, kv head) pairs per SM (B x Hkv >= 5 x SMs) with up
- * to 8 query rows per kv head (many short CTAs otherwise; measured 10-30% faster there);
- * else grid.
+ * FD_SCHEDULE_AUTO (default): head groups where they apply with small pages (16 or 32
+ * tokens bf16, 32 FP8: one 16 KB box instead of several 4-8 KB page boxes), and for
+ * contiguous caches or larger pages when the batch holds at least 5 (b, kv head) pairs
+ * per SM (B x Hkv >= 5 x SMs) with up to 8 query rows per kv head (many short CTAs
+ * otherwise; measured 10-40% faster there); else grid.
  * The persistent and head-group schedules run only with FD_MERGE_KERNEL (or
  * fd_decode_partial) and on the mma.sync path; otherwise the grid schedule runs (with
  * tail sharing on the tcgen05 kernel under FD_SCHEDULE_TAIL_SHARING).

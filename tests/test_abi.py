@@ -166,6 +166,8 @@ def test_partial_kernel_name_follows_settings():
         assert name(bf, bf, 128, 6, 16) == "fd_partial_mma_kernel"             # Hkv % 4
         assert name(bf, bf, 64, 8, 16) == "fd_partial_mma_kernel"              # d = 64
         assert name(bf, f8, 128, 8, 16) == "fd_partial_mma_kernel"             # FP8 KV
+        assert name(bf, f8, 128, 8, 32) == "fd_partial_heads_kernel"           # 32-token tiles
+        assert name(bf, f8, 128, 8, 64) == "fd_partial_mma_kernel"
         assert name(f32, f32, 128, 8) == "fd_partial_mma_kernel"               # 3xTF32
         assert name(f32, f32, 64, 8, 16, rows=4) == "fd_partial_mma_kernel"    # grid only
         assert name(f32, f32, 128, 8, rows=16) == "fd_partial_simt_kernel"     # > 8 rows

@@ -297,6 +297,88 @@ def test_head_groups_auto_for_large_batches(paged):
     check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
 
 
+def _fp8_views(codes):
+    return codes.view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("ps,Hkv,G", [(0, 8, 4), (32, 8, 4), (64, 4, 8), (0, 4, 16),
+                                      (32, 12, 2), (16, 8, 4)])
+def test_head_groups_fp8(ps, Hkv, G):
+    """FP8 E4M3 caches with head-group tiles of 32 tokens x 4 kv heads (one 16 KB box; a
+    warp per head, per-head scales) against the fp64 FP8 oracle, and the grid schedule's
+    LSE.  16-token pages cannot hold a 32-token tile: there the setting runs the grid
+    schedule, bit for bit."""
+    lens = HEAD_LENS
+    if ps:
+        w = workloads.paged_case(len(lens), Hkv * G, Hkv, 128, ps, -(-2048 // ps), lens,
+                                 seed=610 + ps + G, extra_pages=1, out_dtype=torch.float32)
+    else:
+        w = workloads.contiguous_case(len(lens), Hkv * G, Hkv, 128, 2050, lens, seed=610 + G,
+                                      out_dtype=torch.float32)
+    kc, vc, ks, vs = workloads.fp8_quantize(w)
+    q, _, _, lens_np, bt, ps_ = w.oracle_arrays()
+    ref_o, ref_l = oracle.decode_kv8(q, _fp8_views(kc), _fp8_views(vc), ks.numpy(), vs.numpy(),
+                                     lens_np, block_table=bt, page_size=ps_)
+    wd = w.to("cuda")
+    kcd, vcd, ksd, vsd = kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda()
+    B, Hq = w.B, w.Hq
+    expect = "fd_partial_mma_kernel" if ps == 16 else "fd_partial_heads_kernel"
+    assert fd.partial_kernel_name_for(torch.bfloat16, torch.float8_e4m3fn, B, 1, Hq, Hkv, 128,
+                                      ps, w.L_cap, 5, options=fd.options(
+                                          path=fd.FD_PATH_MMA,
+                                          schedule=fd.FD_SCHEDULE_HEAD_GROUPS)) == expect
+    fd.set_path(fd.FD_PATH_MMA)
+    for S in (1, 5, 33):
+        res = {}
+        for sched in (fd.FD_SCHEDULE_HEAD_GROUPS, fd.FD_SCHEDULE_GRID):
+            fd.set_schedule(sched)
+            ws = torch.zeros(fd.workspace_size(B, Hq, Hkv, 128, S), dtype=torch.uint8,
+                             device="cuda")
+            o, l = fd.decode_attention_fp8kv(wd.q, kcd, vcd, ksd, vsd, wd.seq_lens,
+                                             wd.block_table, ps, S, workspace=ws,
+                                             out_dtype=torch.float32)
+            torch.cuda.synchronize()
+            assert fd.read_device_error(ws) == 0
+            res[sched] = (o, l)
+        oh, lh = res[fd.FD_SCHEDULE_HEAD_GROUPS]
+        og, lg = res[fd.FD_SCHEDULE_GRID]
+        check(w, oh.cpu().double().numpy(), lh.cpu().double().numpy(), ref_o, ref_l)
+        if ps == 16:
+            assert torch.equal(oh, og) and torch.equal(lh, lg)
+        assert torch.equal(torch.isneginf(lh), torch.isneginf(lg))
+        fin = torch.isfinite(lg)
+        assert torch.allclose(lh[fin], lg[fin], atol=1e-5, rtol=1e-6)
+
+
+def test_head_groups_fp8_auto_for_large_batches():
+    """FP8 cache, contiguous: the default schedule takes head groups from 5 (b, kv head)
+    pairs per SM (and for 32-token pages at any batch); a ragged batch of that size
+    against the fp64 FP8 oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Hkv, G = 8, 4
+    B = -(-5 * sms // Hkv)
+    import random
+    rnd = random.Random(620)
+    lens = [0, 1, 32, 33, 300] + [rnd.randint(1, 300) for _ in range(B - 5)]
+    w = workloads.contiguous_case(B, Hkv * G, Hkv, 128, 300, lens, seed=621,
+                                  out_dtype=torch.float32)
+    name = lambda b, ps: fd.partial_kernel_name_for(torch.bfloat16, torch.float8_e4m3fn, b, 1,
+                                                    Hkv * G, Hkv, 128, ps, 320)
+    assert name(B, 0) == "fd_partial_heads_kernel"
+    assert name(B - 1, 0) == "fd_partial_mma_kernel"
+    assert name(1, 32) == "fd_partial_heads_kernel"
+    assert name(B - 1, 64) == "fd_partial_mma_kernel"
+    kc, vc, ks, vs = workloads.fp8_quantize(w)
+    q, _, _, lens_np, _, _ = w.oracle_arrays()
+    ref_o, ref_l = oracle.decode_kv8(q, _fp8_views(kc), _fp8_views(vc), ks.numpy(), vs.numpy(),
+                                     lens_np)
+    wd = w.to("cuda")
+    o, l = fd.decode_attention_fp8kv(wd.q, kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda(),
+                                     wd.seq_lens, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
+
+
 def test_head_groups_bf16_out_and_auto_default():
     """The default schedule takes head groups for a 16-token-page bf16 cache; bf16 out."""
     w = workloads.paged_case(4, 32, 8, 128, 16, 128, [2048, 1000, 1, 1500], seed=520)
