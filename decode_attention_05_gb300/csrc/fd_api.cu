@@ -55,8 +55,8 @@ struct Schedule {
 };
 
 // rows: query rows per (b, kv head) group (Q x G); groups above kMaxNarrowRows always
-// run the wide grid kernel.  pairs: the call's (b, kv head) pairs, B x Hkv (0: not
-// known -- the name-only queries).
+// run the wide grid kernel.  pairs: the call's (b, kv head) pairs, B x Hkv, and
+// split_len its tokens per split (0: not known -- the name-only queries).
 // f32 inputs on the tensor-core path run on the grid schedule only.
 //
 // Automatic head groups: always for small pages (16 and 32 tokens bf16, 32 FP8: their
@@ -72,9 +72,18 @@ struct Schedule {
 // (32-token tiles of 4 heads), same batches: 128 x 512 31.0 -> 22.8 us, 256 x 256 36.8
 // -> 26.3, 1024 x 128 102.5 -> 62.7; with 32-token pages 32 x 2048 41.7 -> 25.5.
 constexpr int64_t kHeadsMinPairsPerSm = 5;
+// ... and with head groups, the persistent schedule for items of at most
+// kPersistMaxItemTokens tokens (split_len): each short CTA of the head-group grid pays
+// ~2.5 us of start-up and pipeline fill for little streaming.  Measured on GB300 (Hq 32
+// over Hkv 8, one split), head groups -> persistent head groups: bf16 1024 rows x 128
+// tokens 90.6 -> 81.5 us, 512 x 256 84.8 -> 83.1; FP8 1024 x 128 62.7 -> 52.1, 512 x 256
+// 52.1 -> 50.5; 16-token pages 1024 x 128 94.8 -> 82.5.  From 512 tokens per item the
+// grid is ahead (bf16 256 x 512: 77.3 against 80.2; FP8 256 x 512: 44.4 against 47.7).
+constexpr int64_t kPersistMaxItemTokens = 256;
 
 Schedule choose_schedule(int sched, int path, bool kv8, bool f32, int64_t d, int64_t Hkv,
-                         int32_t page_size, bool fused, int64_t rows, int64_t pairs) {
+                         int32_t page_size, bool fused, int64_t rows, int64_t pairs,
+                         int64_t split_len) {
   const bool narrow = rows <= fd::kMaxNarrowRows && !f32;
   // A head-group tile holds head_tok tokens of each head (one 16 KB box of 4 heads): a
   // page must hold at least that many.
@@ -89,10 +98,15 @@ Schedule choose_schedule(int sched, int path, bool kv8, bool f32, int64_t d, int
   const int sms = rows <= 8 && pairs > 0 ? fd::sm_count() : 0;   // 0: no device
   const bool big_batch = sms > 0 && pairs >= kHeadsMinPairsPerSm * sms;
   Schedule sc;
-  sc.heads = head_ok && ((sched == FD_SCHEDULE_AUTO && (small_pages || big_batch)) ||
+  // The tiling: head groups where the automatic rule takes them (the persistent schedule
+  // follows it too), or everywhere they apply when asked for.
+  sc.heads = head_ok && (((sched == FD_SCHEDULE_AUTO || sched == FD_SCHEDULE_PERSISTENT) &&
+                          (small_pages || big_batch)) ||
                          sched == FD_SCHEDULE_HEAD_GROUPS);
-  sc.persistent = !sc.heads && path == FD_PATH_MMA && !fused && narrow &&
-                  sched == FD_SCHEDULE_PERSISTENT;
+  const bool short_items = split_len > 0 && split_len <= kPersistMaxItemTokens;
+  sc.persistent = path == FD_PATH_MMA && !fused && narrow &&
+                  (sched == FD_SCHEDULE_PERSISTENT ||
+                   (sched == FD_SCHEDULE_AUTO && sc.heads && big_batch && short_items));
   // Tail sharing: the tcgen05 kernel, when asked for (measured slower than the plain
   // grid on GB300: the owners' claim round trips cost more than the tail it recovers).
   sc.tail_share = path == FD_PATH_TCGEN05 && sched == FD_SCHEDULE_TAIL_SHARING;
@@ -121,7 +135,7 @@ int resolve_path(int path, int32_t q_dtype, bool kv8, int64_t d, int32_t page_si
 // the split count, or 0 when not known (then a call of few pairs and several splits).
 const char* kernel_name(const Settings& cfg, int32_t dtype, int32_t kv_dtype, int32_t d,
                         int32_t Hkv, int32_t page_size, int32_t rows, int32_t with_output,
-                        int64_t pairs, int32_t S) {
+                        int64_t pairs, int32_t S, int64_t split_len) {
   const bool kv8 = kv_dtype == FD_F8E4M3;
   if ((dtype != FD_BF16 && dtype != FD_F32) || (!kv8 && kv_dtype != dtype) ||
       (kv8 && dtype != FD_BF16) || d <= 0 || Hkv <= 0 || page_size < 0 || rows < 1 ||
@@ -139,8 +153,8 @@ const char* kernel_name(const Settings& cfg, int32_t dtype, int32_t kv_dtype, in
   // One split with an output writes the output from the partial pass: no in-kernel merge.
   const bool fused = with_output && S != 1 && cfg.merge == FD_MERGE_IN_KERNEL;
   const Schedule sc = choose_schedule(cfg.schedule, path, kv8, dtype == FD_F32, d, Hkv,
-                                      page_size, fused, rows, pairs);
-  if (sc.heads) return "fd_partial_heads_kernel";
+                                      page_size, fused, rows, pairs, split_len);
+  if (sc.heads) return sc.persistent ? "fd_partial_heads_persist_kernel" : "fd_partial_heads_kernel";
   if (sc.persistent) return "fd_partial_persist_kernel";
   return "fd_partial_mma_kernel";
 }
@@ -390,7 +404,7 @@ const char* fd_partial_kernel_name_ex(const fd_options* options, int32_t dtype,
                                       int32_t page_size, int32_t rows, int32_t with_output) {
   Settings cfg;
   if (!resolve_settings(options, &cfg)) return nullptr;
-  return kernel_name(cfg, dtype, kv_dtype, d, Hkv, page_size, rows, with_output, 0, 0);
+  return kernel_name(cfg, dtype, kv_dtype, d, Hkv, page_size, rows, with_output, 0, 0, 0);
 }
 
 const char* fd_partial_kernel_name_for(const fd_options* options, int32_t dtype,
@@ -405,7 +419,7 @@ const char* fd_partial_kernel_name_for(const fd_options* options, int32_t dtype,
   if (rows > fd::kMaxRows) return nullptr;
   const int32_t S = num_splits > 0 ? num_splits : heuristic_splits(B, Q, Hq, Hkv, d, L_cap);
   return kernel_name(cfg, dtype, kv_dtype, d, Hkv, page_size, (int32_t)rows, with_output,
-                     (int64_t)B * Hkv, S);
+                     (int64_t)B * Hkv, S, (L_cap + S - 1) / S);
 }
 
 size_t fd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_splits) {
@@ -607,7 +621,8 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   const bool direct = need_out && S == 1;
   const bool fused = need_out && !direct && cfg.merge == FD_MERGE_IN_KERNEL;
   const Schedule sc = choose_schedule(cfg.schedule, path, kv8, q->dtype == FD_F32, d, Hkv,
-                                     paged ? page_size : 0, fused, Q * G, B * Hkv);
+                                     paged ? page_size : 0, fused, Q * G, B * Hkv,
+                                     (L_cap + S - 1) / S);
   const bool heads = sc.heads, persistent = sc.persistent;
 
   // ---- tensor maps (box height: one tile, or one page when pages are shorter; with head

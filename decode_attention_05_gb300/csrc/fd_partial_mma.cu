@@ -962,7 +962,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   constexpr int G = SH::G, TT = SH::TT, STAGES = SH::STAGES;
   // (Not with 16 query rows per kv head, whose registers are at the cap.)
   if constexpr (G <= 8) {
-    if (threadIdx.x == SH::NCW * 32) prefetch_first_item<TT>(p, &tk, &tv, kPrefetchTiles);
+    if (threadIdx.x == SH::NCW * 32) prefetch_first_item<TT, 1>(p, &tk, &tv, kPrefetchTiles);
   }
   pdl_wait();                       // inputs of this step are visible
   extern __shared__ uint8_t smem_raw[];
@@ -1059,20 +1059,121 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   pdl_trigger();
 }
 
+// ---------------------------------------------------------------- persistent head groups
+// The persistent schedule over head-group tiles: items are (split, group of kHeadGroup
+// kv heads, row), taken from the queue as above, and each tile is one box of TOK tokens
+// x kHeadGroup heads.  Consumer warp w owns head g0 + w of every item, as in the
+// head-group kernel: it restarts its state at an item's first tile and writes its head's
+// partial at the item's last, with no cross-warp merge -- so the warps never wait for one
+// another, and the producer streams the next item while they finish the last one.  The
+// per-item arithmetic is the head-group kernel's, bit for bit.
+template <class SH>
+__global__ void __launch_bounds__(SH::THREADS, 2)
+    fd_partial_heads_persist_kernel(const __grid_constant__ CUtensorMap tk,
+                                    const __grid_constant__ CUtensorMap tv,
+                                    const __grid_constant__ Params p) {
+  constexpr int STAGES = SH::STAGES, TOK = SH::ROWS_PER_WARP;
+  static_assert(SH::NCW == kHeadGroup && TOK * kHeadGroup == SH::TT && !SH::WIDE && !SH::F32,
+                "one head's tokens per consumer warp");
+  if constexpr (SH::G <= 8) {
+    if (threadIdx.x == SH::NCW * 32)
+      prefetch_first_item<TOK, kHeadGroup>(p, &tk, &tv, kPrefetchHeadTiles);
+  }
+  pdl_wait();                       // inputs of this step are visible
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  auto* ctl = reinterpret_cast<PersistCtl<STAGES>*>(stages + SH::RING_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_addr(&ctl->full[s]), 1);
+      mbar_init(smem_addr(&ctl->empty[s]), SH::NCW);
+    }
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == SH::NCW) {
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+    produce_items<TOK, STAGES, Consumer<SH>::kDirect, kHeadGroup>(p, &tk, &tv, stages, ctl, lane);
+    pdl_trigger();
+    return;
+  }
+
+  Consumer<SH> c;
+  const int r0 = warp * TOK;
+  const uint32_t lb = (uint32_t)p.log2_box;
+  bool open = false;                // an item started and not yet written
+  TileMeta mt{};
+  for (int n = 0;; ++n) {
+    const int stage = n % STAGES;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(smem_addr(&ctl->full[stage]), (n / STAGES) & 1);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) {
+        ctl->abort = 1;
+        atomicOr(p.flags, kDevFlagTimeout);
+      }
+      break;
+    }
+    mt = ctl->meta[stage];
+    if (mt.flags & kMetaDone) break;
+    const int g = mt.g + warp;      // this warp's kv head
+    if (mt.flags & kMetaFirst) {
+      c.start(p, mt.b, g, mt.L, lane);
+      open = true;
+    }
+    uint8_t* kt = stages + (size_t)stage * 2 * kTileBytes;
+    // Row r0 + i of the tile is token t0 + i of head g: pass the row-0 token as t0 - r0.
+    c.tile(p, kt, kt + kTileBytes, mt.t0 - r0, mt.lo, mt.hi, mt.bad, warp, lane, lb, false);
+    if (mt.flags & kMetaLast) {
+      c.store_own(p, mt.b, g, mt.split, lane);
+      open = false;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
+  }
+  // An item left half done by a wait that ran out: weight 0 for this warp's head.
+  if (open && lane < p.n_rows)
+    put_empty_row<Consumer<SH>::kDirect>(p, mt.b, mt.g + warp, lane, mt.split);
+  pdl_trigger();
+}
+
 template <class SH>
 cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                        cudaStream_t stream) {
   cudaError_t e;
   if constexpr (SH::PERSIST) {
-    auto kernel = fd_partial_persist_kernel<SH>;
-    static SmemOptIn opt_in;
-    e = opt_in.apply(kernel, (int)SH::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const int64_t items = (int64_t)p.S * p.Hkv * p.B;
-    const unsigned grid = (unsigned)(items < 2 * sms ? items : 2 * sms);
-    e = launch_partial_kernel(kernel, dim3(grid), SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
+    if (p.head_group) {
+      if constexpr (SH::D == 128) {
+        auto kernel = fd_partial_heads_persist_kernel<SH>;
+        static SmemOptIn opt_in;
+        e = opt_in.apply(kernel, (int)SH::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        const int64_t items = (int64_t)p.S * (p.Hkv / kHeadGroup) * p.B;
+        const unsigned grid = (unsigned)(items < 2 * sms ? items : 2 * sms);
+        e = launch_partial_kernel(kernel, dim3(grid), SH::THREADS, SH::SMEM_BYTES, stream, tk,
+                                  tv, p);
+      } else {
+        return cudaErrorInvalidValue;   // the host enables head groups for d = 128 only
+      }
+    } else {
+      auto kernel = fd_partial_persist_kernel<SH>;
+      static SmemOptIn opt_in;
+      e = opt_in.apply(kernel, (int)SH::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      const int64_t items = (int64_t)p.S * p.Hkv * p.B;
+      const unsigned grid = (unsigned)(items < 2 * sms ? items : 2 * sms);
+      e = launch_partial_kernel(kernel, dim3(grid), SH::THREADS, SH::SMEM_BYTES, stream, tk, tv,
+                                p);
+    }
   } else if constexpr (SH::WIDE) {
     auto kernel = fd_partial_wide_kernel<SH>;
     static SmemOptIn opt_in;

@@ -272,14 +272,17 @@ struct PersistCtl {
   int32_t abort;
 };
 
-// Item x of the persistent schedule: its split, kv head and row.
+// Item x of the persistent schedule: its split, (first) kv head and row.  HG kv heads per
+// item: 1, or kHeadGroup with head-group tiles (then g is a multiple of kHeadGroup).
 struct Item {
   int split, g, b;
 };
+template <int HG>
 __device__ __forceinline__ Item item_of(const Params& p, int64_t x) {
-  const int64_t per_split = (int64_t)p.Hkv * p.B;
+  const int64_t groups = p.Hkv / HG;
+  const int64_t per_split = groups * p.B;
   const int64_t r = x % per_split;
-  return Item{p.S - 1 - (int)(x / per_split), (int)(r % p.Hkv), (int)(r / p.Hkv)};
+  return Item{p.S - 1 - (int)(x / per_split), (int)(r % groups) * HG, (int)(r / groups)};
 }
 
 // The first `count` tiles of the CTA's first item (item blockIdx.x: the first item of
@@ -287,10 +290,10 @@ __device__ __forceinline__ Item item_of(const Params& p, int64_t x) {
 // kernel waits for the previous kernel of the stream: the row length and page ids are
 // read relaxed -- a hint only, the producer reads them again after the wait.  Pages
 // shorter than a tile are not prefetched.
-template <int TT>
+template <int TT, int HG>
 __device__ __forceinline__ void prefetch_first_item(const Params& p, const CUtensorMap* tk,
                                                     const CUtensorMap* tv, int count) {
-  const Item it = item_of(p, (int64_t)blockIdx.x);
+  const Item it = item_of<HG>(p, (int64_t)blockIdx.x);
   const int64_t L = min(max((int64_t)ld_relaxed_s32(p.seq_lens + it.b), (int64_t)0), p.L_cap);
   const int64_t lo = (int64_t)it.split * p.split_len;
   const int64_t hi = min(lo + p.split_len, L);
@@ -317,7 +320,9 @@ __device__ __forceinline__ void prefetch_first_item(const Params& p, const CUten
 // Producer warp of the persistent kernel: takes items from the queue and streams their
 // tiles into the ring without a break between items; publishes a kDone stage at the
 // end.  Empty items get their LSE_i = -inf written here and never reach the consumers.
-template <int TT, int STAGES, bool DIRECT>
+// HG kv heads per item (1, or kHeadGroup with head-group tiles: TT is then one head's
+// tokens of a tile, and one box of TT rows x HG heads fills the stage).
+template <int TT, int STAGES, bool DIRECT, int HG = 1>
 __device__ __forceinline__ void produce_items(const Params& p, const CUtensorMap* tk,
                                               const CUtensorMap* tv, uint8_t* stages,
                                               PersistCtl<STAGES>* ctl, int lane) {
@@ -327,7 +332,7 @@ __device__ __forceinline__ void produce_items(const Params& p, const CUtensorMap
   const int pages_per_tile = paged ? (ps >= TT ? 1 : TT / ps) : 1;
   const int box_rows = paged ? (ps >= TT ? TT : ps) : TT;
   const uint32_t box_bytes = (uint32_t)(kTileBytes / TT) * box_rows;
-  const int64_t n_items = (int64_t)p.S * p.Hkv * p.B;
+  const int64_t n_items = (int64_t)p.S * (p.Hkv / HG) * p.B;
   int n = 0;                        // tiles published so far (ring position)
   bool aborted = false;
 
@@ -355,7 +360,7 @@ __device__ __forceinline__ void produce_items(const Params& p, const CUtensorMap
     const int64_t item = (int64_t)__shfl_sync(0xffffffffu, ticket, 0);
     if (item >= n_items) break;
     if (lane == 0) ticket = gridDim.x + atomicAdd(p.item_queue, 1ull);
-    const Item it = item_of(p, item);
+    const Item it = item_of<HG>(p, item);
     const int split = it.split, g = it.g, b = it.b;
     int64_t L = p.seq_lens[b];
     if (L < 0 || L > p.L_cap) {
@@ -365,7 +370,8 @@ __device__ __forceinline__ void produce_items(const Params& p, const CUtensorMap
     const int64_t lo = (int64_t)split * p.split_len;
     const int64_t hi = min(lo + p.split_len, L);
     if (lo >= hi) {                 // empty split: weight 0 in the merge
-      if (lane < p.n_rows) put_empty_row<DIRECT>(p, b, g, lane, split);
+      for (int i = lane; i < HG * p.n_rows; i += 32)
+        put_empty_row<DIRECT>(p, b, g + i / p.n_rows, i % p.n_rows, split);
       continue;
     }
     const int64_t T0 = lo / TT * TT;

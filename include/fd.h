@@ -378,8 +378,10 @@ FD_API int32_t fd_get_path(void);
  * FD_SCHEDULE_GRID: one CTA per item, two per SM; items beyond one wave wait for a
  * slot, and each CTA fills and drains its own copy pipeline.
  * FD_SCHEDULE_PERSISTENT: two CTAs per SM take items from a queue in the workspace
- * header and stream their tiles back to back.  Same partials as FD_SCHEDULE_GRID, bit
- * for bit (the per-item arithmetic is shared).
+ * header and stream their tiles back to back.  Items are those of the tiling the
+ * automatic schedule picks: one kv head (same partials as FD_SCHEDULE_GRID, bit for
+ * bit), or a group of 4 kv heads where FD_SCHEDULE_AUTO takes head groups (same
+ * partials as the head-group kernel, bit for bit).
  * FD_SCHEDULE_HEAD_GROUPS: one CTA per (split, group of 4 kv heads, row); a tile is 16
  * tokens (bf16; 32 for FP8 E4M3) of a row -- of one page -- for all 4 heads, loaded as
  * one 16 KB TMA box, and each consumer warp keeps one head's state (no cross-warp
@@ -399,7 +401,9 @@ FD_API int32_t fd_get_path(void);
  * tokens bf16, 32 FP8: one 16 KB box instead of several 4-8 KB page boxes), and for
  * contiguous caches or larger pages when the batch holds at least 5 (b, kv head) pairs
  * per SM (B x Hkv >= 5 x SMs) with up to 8 query rows per kv head (many short CTAs
- * otherwise; measured 10-40% faster there); else grid.
+ * otherwise; measured 10-40% faster there) -- such a batch with at most 256 tokens per
+ * split runs them on the persistent schedule (10-20% faster again on 128-token rows);
+ * else grid.
  * The persistent and head-group schedules run only with FD_MERGE_KERNEL (or
  * fd_decode_partial) and on the mma.sync path; otherwise the grid schedule runs (with
  * tail sharing on the tcgen05 kernel under FD_SCHEDULE_TAIL_SHARING).
@@ -485,7 +489,7 @@ FD_API fd_status fd_selftest_stalled_decode(const fd_tensor* q, const fd_tensor*
  * Name of the partial-pass kernel a call would launch under the current process
  * settings (path, merge mode, schedule): "fd_partial_mma_kernel",
  * "fd_partial_heads_kernel", "fd_partial_wide_kernel", "fd_partial_persist_kernel",
- * "fd_partial_tc_kernel" or "fd_partial_simt_kernel".  dtype is q's fd_dtype, kv_dtype
+ * "fd_partial_heads_persist_kernel", "fd_partial_tc_kernel" or "fd_partial_simt_kernel".  dtype is q's fd_dtype, kv_dtype
  * the cache's; page_size 0 for a contiguous cache; rows the query rows per kv head
  * (Q x Hq / Hkv); with_output 1 for fd_decode_attention, 0 for fd_decode_partial.  For
  * a call of more than one split and fewer than 5 (b, kv head) pairs per SM: with one

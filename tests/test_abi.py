@@ -188,7 +188,8 @@ def test_partial_kernel_name_follows_settings():
         fd.set_schedule(fd.FD_SCHEDULE_GRID)
         assert name(bf, bf, 128, 8, 16) == "fd_partial_mma_kernel"
         fd.set_schedule(fd.FD_SCHEDULE_PERSISTENT)
-        assert name(bf, bf, 128, 8, 16) == "fd_partial_persist_kernel"
+        assert name(bf, bf, 128, 8, 16) == "fd_partial_heads_persist_kernel"   # its tiling
+        assert name(bf, bf, 128, 8, 64) == "fd_partial_persist_kernel"
         assert name(bf, bf, 128, 8) == "fd_partial_persist_kernel"
         assert name(f32, f32, 128, 8) == "fd_partial_mma_kernel"
         fd.set_path(fd.FD_PATH_MMA)

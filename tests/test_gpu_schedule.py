@@ -1,10 +1,11 @@
 """GPU parity of the alternative schedules of the tensor-core partial pass.
 
-Persistent: the same per-item arithmetic as the grid kernel, only assigned differently
-to CTAs, so every case is checked twice: against the fp64 oracle (the tolerances of
-test_gpu_parity) and bit for bit against the grid schedule.  The queue in the workspace
-header must also come back clean after each launch (several calls in a row, stale
-workspace contents, a replayed CUDA graph).
+Persistent: the same per-item arithmetic as the non-persistent kernel of the same tiling
+(the grid kernel, or the head-group kernel where the automatic rule takes head groups),
+only assigned differently to CTAs, so every case is checked twice: against the fp64
+oracle (the tolerances of test_gpu_parity) and bit for bit against that kernel.  The
+queue in the workspace header must also come back clean after each launch (several
+calls in a row, stale workspace contents, a replayed CUDA graph).
 
 Head groups: tiles of 16 tokens x 4 kv heads (small pages, contiguous caches); checked against the
 oracle and against the grid schedule up to rounding order.
@@ -46,13 +47,14 @@ def _decode(wd, w, S, ws=None, q=None):
 
 
 def _both(wd, w, S, q=None):
+    """Persistent schedule and the automatic one (the same tiling), bit for bit."""
     fd.set_path(fd.FD_PATH_MMA)
-    fd.set_schedule(fd.FD_SCHEDULE_GRID)
+    fd.set_schedule(fd.FD_SCHEDULE_AUTO)
     og, lg = _decode(wd, w, S, q=q)
     fd.set_schedule(fd.FD_SCHEDULE_PERSISTENT)
     op, lp = _decode(wd, w, S, q=q)
-    assert torch.equal(og, op), "persistent and grid outputs differ"
-    assert torch.equal(lg, lp), "persistent and grid LSE differ"
+    assert torch.equal(og, op), "persistent and non-persistent outputs differ"
+    assert torch.equal(lg, lp), "persistent and non-persistent LSE differ"
     return op, lp
 
 
@@ -130,6 +132,69 @@ def test_persistent_fp8_kv():
         check(w, o.float().cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
         res.append((o, l))
     assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+
+
+@pytest.mark.parametrize("kind", ["paged16", "contiguous-large-batch", "fp8-paged32"])
+def test_persistent_head_groups(kind):
+    """The persistent schedule over head-group tiles (where the automatic rule takes
+    them): items of 4 kv heads from the queue, a warp per head.  Against the oracle and,
+    bit for bit, the head-group kernel, for 1 to 37 splits.  A large batch of short rows
+    (at most 256 tokens per split) takes it by default."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Hkv, G = 8, 4
+    name = lambda B, ps, kv, S: fd.partial_kernel_name_for(
+        torch.bfloat16, kv, B, 1, Hkv * G, Hkv, 128, ps, 2048, S,
+        options=fd.options(path=fd.FD_PATH_MMA, schedule=fd.FD_SCHEDULE_PERSISTENT))
+    if kind == "contiguous-large-batch":
+        B = -(-5 * sms // Hkv)
+        import random
+        rnd = random.Random(460)
+        lens = [0, 1, 16, 17, 200] + [rnd.randint(1, 200) for _ in range(B - 5)]
+        w = workloads.contiguous_case(B, Hkv * G, Hkv, 128, 200, lens, seed=461,
+                                      out_dtype=torch.float32)
+        assert name(B, 0, torch.bfloat16, 1) == "fd_partial_heads_persist_kernel"
+        assert name(B - 1, 0, torch.bfloat16, 1) == "fd_partial_persist_kernel"
+        splits = (1, 3)
+    else:
+        ps = 16 if kind == "paged16" else 32
+        w = workloads.paged_case(len(HEAD_LENS), Hkv * G, Hkv, 128, ps, -(-2048 // ps),
+                                 HEAD_LENS, seed=462 + ps, extra_pages=1,
+                                 out_dtype=torch.float32)
+        splits = (1, 6, 37)
+    if kind != "fp8-paged32":
+        if kind == "paged16":
+            assert name(8, 16, torch.bfloat16, 6) == "fd_partial_heads_persist_kernel"
+        ref_o, ref_l = ref_for(w)
+        wd = w.to("cuda")
+        for S in splits:
+            oh, lh = _run_sched(wd, w, S, fd.FD_SCHEDULE_HEAD_GROUPS)
+            op, lp = _run_sched(wd, w, S, fd.FD_SCHEDULE_PERSISTENT)
+            check(w, op.cpu().double().numpy(), lp.cpu().double().numpy(), ref_o, ref_l)
+            assert torch.equal(oh, op) and torch.equal(lh, lp)
+            if kind == "contiguous-large-batch":      # the automatic choice (200 tokens)
+                oa, la = _run_sched(wd, w, S, fd.FD_SCHEDULE_AUTO)
+                assert torch.equal(oa, op) and torch.equal(la, lp)
+        return
+    assert name(8, 32, torch.float8_e4m3fn, 6) == "fd_partial_heads_persist_kernel"
+    kc, vc, ks, vs = workloads.fp8_quantize(w)
+    q, _, _, lens, bt, ps_ = w.oracle_arrays()
+    ref_o, ref_l = oracle.decode_kv8(q, kc.view(torch.uint8).numpy(), vc.view(torch.uint8).numpy(),
+                                     ks.numpy(), vs.numpy(), lens, block_table=bt, page_size=ps_)
+    wd = w.to("cuda")
+    args = (wd.q, kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda(), wd.seq_lens, wd.block_table, 32)
+    fd.set_path(fd.FD_PATH_MMA)
+    for S in splits:
+        res = []
+        for sched in (fd.FD_SCHEDULE_HEAD_GROUPS, fd.FD_SCHEDULE_PERSISTENT):
+            fd.set_schedule(sched)
+            ws = torch.zeros(fd.workspace_size(w.B, 32, 8, 128, S), dtype=torch.uint8,
+                             device="cuda")
+            o, l = fd.decode_attention_fp8kv(*args, S, workspace=ws, out_dtype=torch.float32)
+            torch.cuda.synchronize()
+            assert fd.read_device_error(ws) == 0
+            check(w, o.cpu().double().numpy(), l.cpu().double().numpy(), ref_o, ref_l)
+            res.append((o, l))
+        assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
 
 
 def test_persistent_back_to_back_and_stale_workspace():
@@ -288,8 +353,13 @@ def test_head_groups_auto_for_large_batches(paged):
                                       out_dtype=torch.float32)
     name = lambda b: fd.partial_kernel_name_for(torch.bfloat16, torch.bfloat16, b, 1, Hkv * G,
                                                 Hkv, 128, paged, w.L_cap)
-    assert name(B) == "fd_partial_heads_kernel"
+    assert name(B) == "fd_partial_heads_kernel"              # 300 tokens a split
     assert name(B - 1) == "fd_partial_mma_kernel"
+    short = lambda b, L: fd.partial_kernel_name_for(torch.bfloat16, torch.bfloat16, b, 1,
+                                                    Hkv * G, Hkv, 128, paged, L, 1)
+    assert short(B, 256) == "fd_partial_heads_persist_kernel"
+    assert short(B, 320) == "fd_partial_heads_kernel"
+    assert short(B - 1, 128) == "fd_partial_mma_kernel"
     ref_o, ref_l = ref_for(w)
     wd = w.to("cuda")
     S = fd.resolve_num_splits(B, Hkv * G, Hkv, 128, w.L_cap, 0)
