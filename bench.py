@@ -73,7 +73,20 @@ def parse_args():
                          "tokens per row over the same cache, causal inside the split")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue every timed call from Python instead of replaying CUDA graphs")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="with --context: a large-batch serving workload of B full rows "
+                         "(Hq 32, Hkv 8, d 128) instead of --config")
+    ap.add_argument("--context", type=int, default=0, help="tokens per row for --batch")
     return ap.parse_args()
+
+
+def base_workload(args):
+    """The workload the arms run: --config N, or a serving batch (--batch, --context)."""
+    if args.batch or args.context:
+        if args.batch <= 0 or args.context <= 0:
+            raise SystemExit("--batch and --context go together, both > 0")
+        return workloads.serving_case(args.batch, args.context)
+    return workloads.CONFIGS[args.config]()
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -113,6 +126,8 @@ KERNEL_SOURCES = {
                                 "fd_device.cuh", "fd_internal.h"],
     "fd_partial_persist_kernel": ["fd_partial_mma.cu", "fd_pipeline.cuh", "fd_epilogue.cuh",
                                   "fd_device.cuh", "fd_internal.h"],
+    "fd_partial_heads_persist_kernel": ["fd_partial_mma.cu", "fd_pipeline.cuh",
+                                        "fd_epilogue.cuh", "fd_device.cuh", "fd_internal.h"],
     "fd_partial_simt_kernel": ["fd_partial_simt.cu", "fd_partial_simt.cuh", "fd_pipeline.cuh",
                                "fd_epilogue.cuh", "fd_device.cuh", "fd_internal.h"],
     "fd_partial_wide_kernel": ["fd_partial_mma.cu", "fd_pipeline.cuh", "fd_epilogue.cuh",
@@ -315,7 +330,7 @@ def run_reference(args):
     world, rank, _ = dist_info()
     if rank != 0:
         return 0
-    w = with_query_tokens(workloads.CONFIGS[args.config](), args.query_tokens)
+    w = with_query_tokens(base_workload(args), args.query_tokens)
     scales = None
     if args.kv == "fp8":
         w, ks, vs = fp8_variant(w)
@@ -384,7 +399,7 @@ def run_fd(args):
     fd.set_path({"auto": fd.FD_PATH_AUTO, "simt": fd.FD_PATH_SIMT, "mma": fd.FD_PATH_MMA,
                  "tcgen05": fd.FD_PATH_TCGEN05}[args.path])
 
-    w_cpu = with_query_tokens(workloads.CONFIGS[args.config](), args.query_tokens)
+    w_cpu = with_query_tokens(base_workload(args), args.query_tokens)
     scales_cpu = None
     if args.kv == "fp8":
         if w_cpu.Q > 1:
@@ -406,6 +421,10 @@ def run_fd(args):
         wide = kernel in ("fd_partial_tc_kernel", "fd_partial_wide_kernel")
         S = fd.num_splits_for_lengths(B, Hq, Hkv, d, w.L_cap, w_cpu.seq_lens,
                                       sms // 2 if wide else sms, page_size=w.page_size)
+    # The kernel this call runs, now that the batch and the split count are known (large
+    # batches take head groups, short rows the persistent schedule).
+    kernel = fd.partial_kernel_name_for(w.q.dtype, w.k.dtype, B, Qt, Hq, Hkv, d, w.page_size,
+                                        w.L_cap, S) or kernel
     ws = torch.zeros(fd.workspace_size(B, Qt * Hq, Hkv, d, S), dtype=torch.uint8,
                      device="cuda")
     out = torch.empty(tuple(w.q.shape), dtype=w.out_dtype, device="cuda")
@@ -540,19 +559,21 @@ def run_fd(args):
     e3.record(stream)
     e3.synchronize()
     partial_ms = e2.elapsed_time(e3) / args.steps
-    lse_part, o_part = fd.workspace_partials(ws, B * Qt, Hq, d, S)
-    dout = tensor_desc(out.view(B * Qt, Hq, d))
-    merge_call = lambda s: checked(L.fd_merge_partials(B * Qt, Hq, d, S, lse_part.data_ptr(),
-                                                       o_part.data_ptr(), ctypes.byref(dout),
-                                                       lse.data_ptr(), s))
-    merge_graph = make_graph(merge_call, chunk)
-    barrier()
-    e4, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e4.record(stream)
-    issue(merge_call, merge_graph, args.steps)
-    e5.record(stream)
-    e5.synchronize()
-    merge_ms = e4.elapsed_time(e5) / args.steps
+    merge_ms = 0.0          # one split: the step's partial pass writes the output itself
+    if S > 1:
+        lse_part, o_part = fd.workspace_partials(ws, B * Qt, Hq, d, S)
+        dout = tensor_desc(out.view(B * Qt, Hq, d))
+        merge_call = lambda s: checked(L.fd_merge_partials(B * Qt, Hq, d, S, lse_part.data_ptr(),
+                                                           o_part.data_ptr(), ctypes.byref(dout),
+                                                           lse.data_ptr(), s))
+        merge_graph = make_graph(merge_call, chunk)
+        barrier()
+        e4, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e4.record(stream)
+        issue(merge_call, merge_graph, args.steps)
+        e5.record(stream)
+        e5.synchronize()
+        merge_ms = e4.elapsed_time(e5) / args.steps
     peak, peak_src = measured_peak()
     achieved = kv_bytes / (partial_ms * 1e-3) / 1e9
     path_name = {"fd_partial_simt_kernel": "simt", "fd_partial_tc_kernel": "tcgen05"}.get(kernel, "mma")
@@ -562,6 +583,9 @@ def run_fd(args):
                 "algorithmic_bytes_per_launch": kv_bytes,
                 "partial_us": round(partial_ms * 1e3, 2), "merge_us": round(merge_ms * 1e3, 2),
                 "launch": launch_label(args.steps)}
+    if S == 1:
+        roofline["merge"] = ("none in the step: with one split the partial pass writes the "
+                             "output; partial_us times the partials-only pass")
 
     # ---- end to end through the public API, host buffers, copies inside the timed region
     pin = lambda t: t.pin_memory()

@@ -233,6 +233,14 @@ def config4() -> Workload:
                       name="ragged paged GQA bf16 B16 Hq32 Hkv8 d128 ps16 L<=32768")
 
 
+def serving_case(B: int, L: int, Hq: int = 32, Hkv: int = 8, d: int = 128) -> Workload:
+    """A large-batch serving step: B rows of L tokens each (every row full), bf16,
+    N(0,1), contiguous cache; seed 2000 + B.  Not one of the five workloads: a shape for
+    the many-short-rows regime (bench.py --batch/--context)."""
+    return contiguous_case(B, Hq, Hkv, d, L, seed=2000 + B, poison_tail=False,
+                           name="serving bf16 B%d Hq%d Hkv%d d%d L%d" % (B, Hq, Hkv, d, L))
+
+
 def config5(num_splits: int = 8) -> Workload:
     B, Hq, Hkv, d, L = 8, 32, 8, 128, 16384
     G = Hq // Hkv
