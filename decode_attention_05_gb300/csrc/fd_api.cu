@@ -55,8 +55,8 @@ struct Schedule {
 };
 
 // rows: query rows per (b, kv head) group (Q x G); groups above kMaxNarrowRows always
-// run the wide grid kernel.  pairs: the call's (b, kv head) pairs, B x Hkv, and
-// split_len its tokens per split (0: not known -- the name-only queries).
+// run the wide grid kernel.  pairs: the call's (b, kv head) pairs, B x Hkv, S its split
+// count and split_len its tokens per split (0: not known -- the name-only queries).
 // f32 inputs on the tensor-core path run on the grid schedule only.
 //
 // Automatic head groups: always for small pages (16 and 32 tokens bf16, 32 FP8: their
@@ -73,17 +73,20 @@ struct Schedule {
 // -> 26.3, 1024 x 128 102.5 -> 62.7; with 32-token pages 32 x 2048 41.7 -> 25.5.
 constexpr int64_t kHeadsMinPairsPerSm = 5;
 // ... and with head groups, the persistent schedule for items of at most
-// kPersistMaxItemTokens tokens (split_len): each short CTA of the head-group grid pays
-// ~2.5 us of start-up and pipeline fill for little streaming.  Measured on GB300 (Hq 32
-// over Hkv 8, one split), head groups -> persistent head groups: bf16 1024 rows x 128
-// tokens 90.6 -> 81.5 us, 512 x 256 84.8 -> 83.1; FP8 1024 x 128 62.7 -> 52.1, 512 x 256
-// 52.1 -> 50.5; 16-token pages 1024 x 128 94.8 -> 82.5.  From 512 tokens per item the
-// grid is ahead (bf16 256 x 512: 77.3 against 80.2; FP8 256 x 512: 44.4 against 47.7).
+// kPersistMaxItemTokens tokens (split_len), kPersistMinItemsPerSm of them per SM or
+// more: each short CTA of the head-group grid pays ~2.5 us of start-up and pipeline fill
+// for little streaming.  Measured on GB300 (Hq 32 over Hkv 8, one split), head groups ->
+// persistent head groups: bf16 1024 rows x 128 tokens 90.6 -> 81.5 us, 512 x 256 84.8 ->
+// 83.1; FP8 1024 x 128 62.7 -> 52.1, 512 x 256 52.1 -> 50.5; 16-token pages 1024 x 128
+// 94.8 -> 82.5.  With fewer items a CTA's last one is a large share of its work (256 x
+// 256, 3.4 items per SM: bf16 42.2 against 43.9, FP8 26.3 against 28.9), and from 512
+// tokens per item the grid is ahead (bf16 256 x 512: 77.3 against 80.2).
 constexpr int64_t kPersistMaxItemTokens = 256;
+constexpr int64_t kPersistMinItemsPerSm = 6;
 
 Schedule choose_schedule(int sched, int path, bool kv8, bool f32, int64_t d, int64_t Hkv,
                          int32_t page_size, bool fused, int64_t rows, int64_t pairs,
-                         int64_t split_len) {
+                         int64_t S, int64_t split_len) {
   const bool narrow = rows <= fd::kMaxNarrowRows && !f32;
   // A head-group tile holds head_tok tokens of each head (one 16 KB box of 4 heads): a
   // page must hold at least that many.
@@ -103,7 +106,8 @@ Schedule choose_schedule(int sched, int path, bool kv8, bool f32, int64_t d, int
   sc.heads = head_ok && (((sched == FD_SCHEDULE_AUTO || sched == FD_SCHEDULE_PERSISTENT) &&
                           (small_pages || big_batch)) ||
                          sched == FD_SCHEDULE_HEAD_GROUPS);
-  const bool short_items = split_len > 0 && split_len <= kPersistMaxItemTokens;
+  const bool short_items = split_len > 0 && split_len <= kPersistMaxItemTokens &&
+                           pairs / fd::kHeadGroup * S >= kPersistMinItemsPerSm * sms;
   sc.persistent = path == FD_PATH_MMA && !fused && narrow &&
                   (sched == FD_SCHEDULE_PERSISTENT ||
                    (sched == FD_SCHEDULE_AUTO && sc.heads && big_batch && short_items));
@@ -153,7 +157,7 @@ const char* kernel_name(const Settings& cfg, int32_t dtype, int32_t kv_dtype, in
   // One split with an output writes the output from the partial pass: no in-kernel merge.
   const bool fused = with_output && S != 1 && cfg.merge == FD_MERGE_IN_KERNEL;
   const Schedule sc = choose_schedule(cfg.schedule, path, kv8, dtype == FD_F32, d, Hkv,
-                                      page_size, fused, rows, pairs, split_len);
+                                      page_size, fused, rows, pairs, S, split_len);
   if (sc.heads) return sc.persistent ? "fd_partial_heads_persist_kernel" : "fd_partial_heads_kernel";
   if (sc.persistent) return "fd_partial_persist_kernel";
   return "fd_partial_mma_kernel";
@@ -621,7 +625,7 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   const bool direct = need_out && S == 1;
   const bool fused = need_out && !direct && cfg.merge == FD_MERGE_IN_KERNEL;
   const Schedule sc = choose_schedule(cfg.schedule, path, kv8, q->dtype == FD_F32, d, Hkv,
-                                     paged ? page_size : 0, fused, Q * G, B * Hkv,
+                                     paged ? page_size : 0, fused, Q * G, B * Hkv, S,
                                      (L_cap + S - 1) / S);
   const bool heads = sc.heads, persistent = sc.persistent;
 

@@ -402,8 +402,8 @@ FD_API int32_t fd_get_path(void);
  * contiguous caches or larger pages when the batch holds at least 5 (b, kv head) pairs
  * per SM (B x Hkv >= 5 x SMs) with up to 8 query rows per kv head (many short CTAs
  * otherwise; measured 10-40% faster there) -- such a batch with at most 256 tokens per
- * split runs them on the persistent schedule (10-20% faster again on 128-token rows);
- * else grid.
+ * split and at least 6 head-group items per SM runs them on the persistent schedule
+ * (10-20% faster again on 128-token rows); else grid.
  * The persistent and head-group schedules run only with FD_MERGE_KERNEL (or
  * fd_decode_partial) and on the mma.sync path; otherwise the grid schedule runs (with
  * tail sharing on the tcgen05 kernel under FD_SCHEDULE_TAIL_SHARING).

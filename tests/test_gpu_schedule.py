@@ -146,14 +146,14 @@ def test_persistent_head_groups(kind):
         torch.bfloat16, kv, B, 1, Hkv * G, Hkv, 128, ps, 2048, S,
         options=fd.options(path=fd.FD_PATH_MMA, schedule=fd.FD_SCHEDULE_PERSISTENT))
     if kind == "contiguous-large-batch":
-        B = -(-5 * sms // Hkv)
+        B = -(-6 * sms * 4 // Hkv)              # 6 head-group items per SM at one split
         import random
         rnd = random.Random(460)
         lens = [0, 1, 16, 17, 200] + [rnd.randint(1, 200) for _ in range(B - 5)]
         w = workloads.contiguous_case(B, Hkv * G, Hkv, 128, 200, lens, seed=461,
                                       out_dtype=torch.float32)
         assert name(B, 0, torch.bfloat16, 1) == "fd_partial_heads_persist_kernel"
-        assert name(B - 1, 0, torch.bfloat16, 1) == "fd_partial_persist_kernel"
+        assert name(-(-5 * sms // Hkv) - 1, 0, torch.bfloat16, 1) == "fd_partial_persist_kernel"
         splits = (1, 3)
     else:
         ps = 16 if kind == "paged16" else 32
@@ -357,8 +357,11 @@ def test_head_groups_auto_for_large_batches(paged):
     assert name(B - 1) == "fd_partial_mma_kernel"
     short = lambda b, L: fd.partial_kernel_name_for(torch.bfloat16, torch.bfloat16, b, 1,
                                                     Hkv * G, Hkv, 128, paged, L, 1)
-    assert short(B, 256) == "fd_partial_heads_persist_kernel"
-    assert short(B, 320) == "fd_partial_heads_kernel"
+    B6 = -(-6 * sms * 4 // Hkv)                 # 6 head-group items per SM
+    assert short(B6, 256) == "fd_partial_heads_persist_kernel"
+    assert short(B6, 320) == "fd_partial_heads_kernel"
+    assert short(B6 - 1, 256) == "fd_partial_heads_kernel"
+    assert short(B, 256) == "fd_partial_heads_kernel"
     assert short(B - 1, 128) == "fd_partial_mma_kernel"
     ref_o, ref_l = ref_for(w)
     wd = w.to("cuda")
