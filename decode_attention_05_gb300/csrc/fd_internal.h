@@ -88,6 +88,10 @@ struct Params {
   // 1: a single split whose result is the output: the partial pass writes out and
   // lse_out itself and no merge runs (put_* in fd_pipeline.cuh); 0: it writes partials
   int32_t direct;
+  // CTAs of the grid resident at once (set by a launcher whose CTAs prefetch the first
+  // tiles of the CTA `wave` places later once they have issued their own, which then
+  // finds them in L2 when it starts; 0: no such prefetch)
+  int32_t wave;
   float scale_log2;       // log2(e) / sqrt(d): scores are kept in base-2 units inside kernels
   // FP8 KV cache (E4M3 codes): per-kv-head dequantisation scales [Hkv] (nullptr = 1)
   int32_t kv_fp8;

@@ -909,7 +909,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   if (warp == SH::NCW) {            // producer: one 16-row box of the group per K and V
     prefetch_tensormap(&tk);
     prefetch_tensormap(&tv);
-    produce_tiles<TOK, STAGES>(p, si, &tk, &tv, stages, ctl, lane);
+    produce_tiles<TOK, STAGES, kHeadGroup>(p, si, &tk, &tv, stages, ctl, lane);
     pdl_trigger();
     return;
   }
@@ -1188,7 +1188,9 @@ cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap
       e = opt_in.apply(kernel, (int)SH::SMEM_BYTES);
       if (e != cudaSuccess) return e;
       dim3 grid((unsigned)p.S, (unsigned)(p.Hkv / kHeadGroup), (unsigned)p.B);
-      e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
+      Params q = p;
+      q.wave = 2 * sm_count();      // two CTAs per SM
+      e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, q);
     } else {
       return cudaErrorInvalidValue;   // the host enables head groups for d = 128 only
     }
@@ -1198,7 +1200,9 @@ cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap
     e = opt_in.apply(kernel, (int)SH::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
-    e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
+    Params q = p;
+    q.wave = 2 * sm_count();        // two CTAs per SM
+    e = launch_partial_kernel(kernel, grid, SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, q);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -723,7 +723,9 @@ cudaError_t launch_tc(const Params& p, const CUtensorMap& tk, const CUtensorMap&
   cudaError_t e = opt_in.apply(kernel, (int)kTcSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.S, (unsigned)p.Hkv, (unsigned)p.B);
-  e = launch_partial_kernel(kernel, grid, kTcThreads, kTcSmemBytes, stream, tk, tv, p);
+  Params q = p;
+  q.wave = sm_count();              // one CTA per SM
+  e = launch_partial_kernel(kernel, grid, kTcThreads, kTcSmemBytes, stream, tk, tv, q);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -85,13 +85,13 @@ __device__ __forceinline__ int32_t ld_relaxed_s32(const int32_t* a) {
   return v;
 }
 template <int TT>
-__device__ __forceinline__ void prefetch_first_tiles(const Params& p, const CUtensorMap* tk,
-                                                     const CUtensorMap* tv, int count, int head) {
+__device__ __forceinline__ void prefetch_tiles_of(const Params& p, const CUtensorMap* tk,
+                                                  const CUtensorMap* tv, int count, int split,
+                                                  int head, int b) {
   if (p.block_table != nullptr) return;       // paged caches: prefetch_first_pages
-  const int b = (int)blockIdx.z;
-  const int64_t L = min((int64_t)ld_relaxed_s32(p.seq_lens + b), p.L_cap);
+  const int64_t L = min(max((int64_t)ld_relaxed_s32(p.seq_lens + b), (int64_t)0), p.L_cap);
   int64_t lo, hi;
-  split_range<TT>(p, (int)blockIdx.x, L, lo, hi);
+  split_range<TT>(p, split, L, lo, hi);
   const int64_t T0 = lo / TT * TT;
 #pragma unroll 1
   for (int k = 0; k < count; ++k) {
@@ -100,6 +100,29 @@ __device__ __forceinline__ void prefetch_first_tiles(const Params& p, const CUte
     tma_prefetch_5d(tk, 0, (int)t0, 0, head, b);
     tma_prefetch_5d(tv, 0, (int)t0, 0, head, b);
   }
+}
+template <int TT>
+__device__ __forceinline__ void prefetch_first_tiles(const Params& p, const CUtensorMap* tk,
+                                                     const CUtensorMap* tv, int count, int head) {
+  prefetch_tiles_of<TT>(p, tk, tv, count, (int)blockIdx.x, head, (int)blockIdx.z);
+}
+
+// The next wave (contiguous caches, grid (S, Hkv / HPC, B) of HPC kv heads per CTA):
+// once a CTA has issued its own tiles, the first `count` tiles of the CTA p.wave launch
+// places later -- the one that will take a freed slot about when this one ends -- go to
+// L2, so that CTA's first loads hit L2 instead of waiting on HBM.  A hint only: the
+// lengths are read relaxed and a wrong guess costs bandwidth, not correctness.
+template <int TT, int HPC = 1>
+__device__ __forceinline__ void prefetch_next_wave(const Params& p, const CUtensorMap* tk,
+                                                   const CUtensorMap* tv, int count) {
+  if (p.wave <= 0 || p.block_table != nullptr) return;
+  const int64_t linear = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
+  const int64_t target = linear + p.wave;
+  if (target >= (int64_t)gridDim.x * gridDim.y * gridDim.z) return;
+  const int split = (int)(target % gridDim.x);
+  const int64_t rest = target / gridDim.x;
+  prefetch_tiles_of<TT>(p, tk, tv, count, split, (int)(rest % gridDim.y) * HPC,
+                        (int)(rest / gridDim.y));
 }
 
 // The same for a paged cache whose boxes are TT rows of one page (TT <= page_size; the
@@ -581,7 +604,8 @@ __device__ __forceinline__ bool selftest_stops(const Params& p, int n) {
 
 // Producer warp: streams tiles 0..n_tiles-1 of the split.  All 32 lanes run the loop
 // (they share the page-id window); lane 0 issues the copies.
-template <int TT, int STAGES>
+// HPC: kv heads per CTA of the grid (1, or kHeadGroup for head-group tiles).
+template <int TT, int STAGES, int HPC = 1>
 __device__ __forceinline__ void produce_tiles(const Params& p, const SplitInfo& si,
                                               const CUtensorMap* tk, const CUtensorMap* tv,
                                               uint8_t* stages, PipeCtl<STAGES>* ctl,
@@ -597,6 +621,7 @@ __device__ __forceinline__ void produce_tiles(const Params& p, const SplitInfo& 
                            win, pol, lane);
     __syncwarp();
   }
+  if (n == si.n_tiles && lane == 0) prefetch_next_wave<TT, HPC>(p, tk, tv, STAGES);
   drain_ring(p, ctl, n, lane);
 }
 
@@ -786,6 +811,7 @@ __device__ __forceinline__ void produce_tiles_shared(const Params& p, const Spli
     ++n;
   }
   const int n_total = n;
+  if (!aborted && lane == 0) prefetch_next_wave<TT>(p, tk, tv, STAGES);
   if (!aborted) {
     for (int k = 0; k < 2; ++k) {            // the end, for each tile parity
       if (!acquire_slot(p, ctl, n, lane)) break;
