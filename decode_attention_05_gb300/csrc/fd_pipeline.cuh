@@ -273,6 +273,13 @@ struct PipeCtl {
   int32_t last;             // this CTA drew its group's last ticket (fused merge)
 };
 
+// Failure-path self-test (Params::selftest_stall): whether the producer of this CTA stops
+// before its ring slot n.  Never true outside fd_selftest_stalled_decode.
+__device__ __forceinline__ bool selftest_stops(const Params& p, int n) {
+  return p.selftest_stall > 0 && n == p.selftest_stall - 1 && blockIdx.x == 0 &&
+         blockIdx.y == 0 && blockIdx.z == 0;
+}
+
 // ---------------------------------------------------------------- persistent schedule
 //
 // Work item x (0 .. S * Hkv * B - 1) is split S - 1 - x / (Hkv * B) of kv head
@@ -403,7 +410,7 @@ __device__ __forceinline__ void produce_items(const Params& p, const CUtensorMap
     int64_t cache_base = -64;
     int32_t cache = -2;
     for (int t = 0; t < n_tiles; ++t, ++n) {
-      if (!acquire(n)) {
+      if (selftest_stops(p, n) || !acquire(n)) {
         aborted = true;
         break;
       }
@@ -593,13 +600,6 @@ __device__ __forceinline__ void drain_ring(const Params& p, PipeCtl<STAGES>* ctl
       }
     }
   }
-}
-
-// Failure-path self-test (Params::selftest_stall): whether the producer of this CTA stops
-// before its ring slot n.  Never true outside fd_selftest_stalled_decode.
-__device__ __forceinline__ bool selftest_stops(const Params& p, int n) {
-  return p.selftest_stall > 0 && n == p.selftest_stall - 1 && blockIdx.x == 0 &&
-         blockIdx.y == 0 && blockIdx.z == 0;
 }
 
 // Producer warp: streams tiles 0..n_tiles-1 of the split.  All 32 lanes run the loop

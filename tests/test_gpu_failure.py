@@ -80,12 +80,32 @@ def _stalled_case(kind):
         w = workloads.contiguous_case(2, 16, 2, 64, 4096, [4096, 2000], seed=816,
                                       out_dtype=torch.float32)
         Q, S, stall = 4, 4, 1
+    elif kind == "persist":
+        w = workloads.contiguous_case(2, 16, 2, 128, 4096, [4096, 2000], seed=817,
+                                      out_dtype=torch.float32)
+        S, stall = 4, 3
+        opts = fd.options(path=fd.FD_PATH_MMA, schedule=fd.FD_SCHEDULE_PERSISTENT)
+    elif kind == "heads_persist":
+        w = workloads.paged_case(2, 16, 4, 128, 16, 256, [4096, 1000], seed=818,
+                                 out_dtype=torch.float32)
+        S, stall = 4, 5
+        opts = fd.options(schedule=fd.FD_SCHEDULE_PERSISTENT)
+    elif kind == "heads_contiguous":
+        w = workloads.contiguous_case(2, 16, 4, 128, 4096, [4096, 1000], seed=819,
+                                      out_dtype=torch.float32)
+        S, stall = 4, 1
+        opts = fd.options(schedule=fd.FD_SCHEDULE_HEAD_GROUPS)
+    elif kind == "direct":                   # one split: out written by the partial pass
+        w = workloads.contiguous_case(2, 16, 2, 128, 4096, [4096, 2000], seed=821,
+                                      out_dtype=torch.float32)
+        S, stall = 1, 2
     else:
         raise ValueError(kind)
     return w, Q, S, stall, opts
 
 
-@pytest.mark.parametrize("kind", ["mma", "mma_fused", "heads", "simt", "tc", "tc_shared", "wide"])
+@pytest.mark.parametrize("kind", ["mma", "mma_fused", "heads", "simt", "tc", "tc_shared", "wide",
+                                  "persist", "heads_persist", "heads_contiguous", "direct"])
 def test_real_kernel_wait_runs_out_and_context_survives(kind):
     import numpy as np
     import oracle
@@ -97,9 +117,12 @@ def test_real_kernel_wait_runs_out_and_context_survives(kind):
     expected = {"mma": "fd_partial_mma_kernel", "mma_fused": "fd_partial_mma_kernel",
                 "heads": "fd_partial_heads_kernel", "simt": "fd_partial_simt_kernel",
                 "tc": "fd_partial_tc_kernel", "tc_shared": "fd_partial_tc_kernel",
-                "wide": "fd_partial_wide_kernel"}[kind]
-    assert fd.partial_kernel_name(torch.bfloat16, torch.bfloat16, w.d, w.Hkv, w.page_size,
-                                  rows=Q * (w.Hq // w.Hkv), options=opts) == expected
+                "wide": "fd_partial_wide_kernel", "persist": "fd_partial_persist_kernel",
+                "heads_persist": "fd_partial_heads_persist_kernel",
+                "heads_contiguous": "fd_partial_heads_kernel",
+                "direct": "fd_partial_mma_kernel"}[kind]
+    assert fd.partial_kernel_name_for(torch.bfloat16, torch.bfloat16, w.B, Q, w.Hq, w.Hkv, w.d,
+                                      w.page_size, w.L_cap, S, options=opts) == expected
     ws = torch.zeros(fd.workspace_size(w.B, Q * w.Hq, w.Hkv, w.d, S), dtype=torch.uint8,
                      device="cuda")
     out = torch.empty(tuple(q.shape), dtype=torch.float32, device="cuda")
