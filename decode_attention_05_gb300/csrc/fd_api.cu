@@ -630,7 +630,7 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
   const bool heads = sc.heads, persistent = sc.persistent;
 
   // ---- tensor maps (box height: one tile, or one page when pages are shorter; with head
-  // groups 16 rows of kHeadGroup heads)
+  // groups a quarter tile -- 16 bf16 or 32 FP8 rows -- of kHeadGroup heads)
   const int TT = fd::tile_tokens((int)d, es);
   const uint32_t box_rows = heads ? (uint32_t)(TT / fd::kHeadGroup)     // 16 bf16, 32 FP8
                                  : (uint32_t)(paged && page_size < TT ? page_size : TT);

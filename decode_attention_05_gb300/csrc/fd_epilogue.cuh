@@ -92,7 +92,7 @@ __device__ __forceinline__ bool merge_warps_and_store(const Params& p, const Spl
           o.w = fmaf(a.w, f, o.w);
         }
       }
-      put_o4<D>(p, si.b, si.g, h, si.split, j, o);
+      put_out4(p, si.b, si.g, h, j, o);
     }
     return true;
   }

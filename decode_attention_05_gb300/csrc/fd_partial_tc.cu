@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (p.direct) {
-          put_o4<kTcD>(p, si.b, si.g, hr, si.split, c4 * 4, acc);
+          put_out4(p, si.b, si.g, hr, c4 * 4, acc);
         } else {
           const int64_t row = ((int64_t)si.b * p.Q + (hr >> lgG)) * p.Hq +
                               (int64_t)si.g * p.G + (hr & (p.G - 1));

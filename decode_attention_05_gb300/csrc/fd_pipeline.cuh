@@ -200,29 +200,13 @@ __device__ __forceinline__ void put_lse(const Params& p, int b, int g, int rho, 
     p.lse_out[row] = v;
   }
 }
-// Dims j .. j + 3 of O_i of row rho of group (b, g).
-template <int D>
-__device__ __forceinline__ void put_o4(const Params& p, int b, int g, int rho, int split, int j,
-                                       float4 o) {
-  if (!p.direct) {
-    *reinterpret_cast<float4*>(p.o_part + (flat_row(p, b, g, rho) * p.S + split) * D + j) = o;
-  } else {
-    const int64_t e = out_elem(p, b, g, rho) + j;
-    put_out(p, e, o.x);
-    put_out(p, e + 1, o.y);
-    put_out(p, e + 2, o.z);
-    put_out(p, e + 3, o.w);
-  }
-}
-// Dim j of O_i of row rho of group (b, g).
-template <int D>
-__device__ __forceinline__ void put_o1(const Params& p, int b, int g, int rho, int split, int j,
-                                       float v) {
-  if (!p.direct) {
-    p.o_part[(flat_row(p, b, g, rho) * p.S + split) * D + j] = v;
-  } else {
-    put_out(p, out_elem(p, b, g, rho) + j, v);
-  }
+// Direct output: dims j .. j + 3 of out for row rho of group (b, g).
+__device__ __forceinline__ void put_out4(const Params& p, int b, int g, int rho, int j, float4 o) {
+  const int64_t e = out_elem(p, b, g, rho) + j;
+  put_out(p, e, o.x);
+  put_out(p, e + 1, o.y);
+  put_out(p, e + 2, o.z);
+  put_out(p, e + 3, o.w);
 }
 // Row rho of group (b, g) has no key in the split (or its split was abandoned): LSE_i =
 // -inf and no O_i -- weight 0 in the merge; with direct output, out = 0 and -inf.
