@@ -4,6 +4,7 @@
  * A plain C99 program that includes fd.h, allocates device buffers with the CUDA runtime,
  * runs one decode step three ways -- fd_decode_attention, fd_decode_attention_ex with
  * per-call options (the mma.sync path) and a plan (fd_plan_create / fd_plan_decode) --
+ * asks fd_partial_kernel_name_for which kernel two calls would run,
  * and checks every output element against the fp64 oracle (oracle/fd_oracle.c, test
  * infrastructure, linked into this test only) with the parity tolerances of the Python
  * tests:  out |got - ref| <= 4e-3 + 8e-3 |ref|,  lse |got - ref| <= 1e-4 + 1e-5 |ref|.
@@ -175,6 +176,25 @@ int main(void) {
       return 1;
     }
     bad += check(name, out_h, lse_h, ref_o, ref_l);
+  }
+  {
+    /* The kernel a call of these sizes runs: a 1-split call over 16-token pages takes head
+     * groups even under the single-launch merge (one split never merges in-kernel). */
+    fd_options inkernel;
+    const char* k;
+    inkernel.path = FD_FROM_PROCESS;
+    inkernel.merge_mode = FD_MERGE_IN_KERNEL;
+    inkernel.schedule = FD_FROM_PROCESS;
+    k = fd_partial_kernel_name_for(&inkernel, FD_BF16, FD_BF16, B, 1, HQ, HKV, D, 0, LCAP, S, 1);
+    if (!k || strcmp(k, "fd_partial_mma_kernel") != 0) {
+      fprintf(stderr, "fd_partial_kernel_name_for: %s\n", k ? k : "(null)");
+      return 1;
+    }
+    k = fd_partial_kernel_name_for(&inkernel, FD_BF16, FD_BF16, 4, 1, 32, 8, D, 16, 4096, 1, 1);
+    if (!k || strcmp(k, "fd_partial_heads_kernel") != 0) {
+      fprintf(stderr, "fd_partial_kernel_name_for (pages): %s\n", k ? k : "(null)");
+      return 1;
+    }
   }
   fd_plan_destroy(plan);
   cudaFree(dq);
