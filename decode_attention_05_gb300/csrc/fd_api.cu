@@ -126,11 +126,22 @@ bool tc_takes(int32_t q_dtype, bool kv8, int64_t d, int32_t page_size, int64_t r
 
 // Automatic choice: groups of kTcAutoMinRows rows or more go to the tcgen05 kernel where
 // it applies; otherwise the mma.sync path for bf16 and for f32 groups of up to
-// kMaxF32MmaRows rows, and the CUDA-core path for larger f32 groups.
+// kMaxF32MmaRows rows, and the CUDA-core path for larger f32 groups.  Exception: groups
+// of up to 32 rows whose splits hold at most kTcMinSplitTokens tokens (split_len; 0: not
+// known) take the mma.sync wide kernel.  The tcgen05 kernel holds one CTA per SM and pays
+// its start-up and epilogue (~7.5 us) once per split with nothing to overlap them, so
+// short splits of large batches run faster two CTAs per SM.  Measured on GB300 (Hq 64
+// over Hkv 8, 4 query tokens = 32 rows, one split), tcgen05 -> mma.sync: 256 rows x 256
+// tokens 140.1 -> 122.3 us, 512 x 128 239.2 -> 163.0, 128 x 256 69.2 -> 62.2; with 512
+// tokens a split the tcgen05 kernel is ahead (128 x 512: 91.1 against 106.5), and with
+// 64 rows at any length (256 x 256, 8 query tokens: 153.9 against 253.2).
+constexpr int64_t kTcMinSplitTokens = 257;
+
 int resolve_path(int path, int32_t q_dtype, bool kv8, int64_t d, int32_t page_size,
-                 int64_t rows) {
+                 int64_t rows, int64_t split_len) {
   if (path != FD_PATH_AUTO) return path;
-  if (rows >= fd::kTcAutoMinRows && tc_takes(q_dtype, kv8, d, page_size, rows))
+  const bool short_splits = rows <= 32 && split_len > 0 && split_len < kTcMinSplitTokens;
+  if (rows >= fd::kTcAutoMinRows && tc_takes(q_dtype, kv8, d, page_size, rows) && !short_splits)
     return FD_PATH_TCGEN05;
   return q_dtype == FD_BF16 || rows <= fd::kMaxF32MmaRows ? FD_PATH_MMA : FD_PATH_SIMT;
 }
@@ -145,7 +156,7 @@ const char* kernel_name(const Settings& cfg, int32_t dtype, int32_t kv_dtype, in
       (kv8 && dtype != FD_BF16) || d <= 0 || Hkv <= 0 || page_size < 0 || rows < 1 ||
       rows > fd::kMaxRows)
     return nullptr;
-  const int path = resolve_path(cfg.path, dtype, kv8, d, page_size, rows);
+  const int path = resolve_path(cfg.path, dtype, kv8, d, page_size, rows, split_len);
   if ((path == FD_PATH_MMA && dtype == FD_F32 && rows > fd::kMaxF32MmaRows) ||
       (kv8 && path != FD_PATH_MMA))
     return nullptr;
@@ -603,7 +614,8 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
     return fail(FD_ERR_UNSUPPORTED, "grid too large");
 
   // ---- path
-  const int path = resolve_path(cfg.path, q->dtype, kv8, d, paged ? page_size : 0, Q * G);
+  const int path = resolve_path(cfg.path, q->dtype, kv8, d, paged ? page_size : 0, Q * G,
+                                (L_cap + S - 1) / S);
   if (path == FD_PATH_TCGEN05 && !tc_takes(q->dtype, kv8, d, paged ? page_size : 0, Q * G))
     return fail(FD_ERR_UNSUPPORTED,
                 "the tcgen05 kernel takes bf16 q/K/V with d = 128, up to %d query rows per kv "

@@ -88,9 +88,10 @@ typedef struct {
 /* Kernel path selection for the partial pass (process-wide setting). */
 typedef enum {
   FD_PATH_AUTO = 0,    /* the fastest kernel for the call: FD_PATH_TCGEN05 for bf16 groups
-                          of 17 to 64 query rows per kv head that it takes, FD_PATH_MMA
-                          for other bf16 groups and f32 groups of up to 8 rows, CUDA
-                          cores otherwise                                                */
+                          of 17 to 64 query rows per kv head that it takes (but groups of
+                          up to 32 rows with at most 256 tokens a split: FD_PATH_MMA),
+                          FD_PATH_MMA for other bf16 groups and f32 groups of up to 8
+                          rows, CUDA cores otherwise                                     */
   FD_PATH_SIMT = 1,    /* CUDA-core dot products for every dtype                         */
   FD_PATH_MMA = 2,     /* mma.sync tensor-core tiles: bf16 (up to 64 rows), f32 (3xTF32,
                           up to 8 rows); FD_ERR_UNSUPPORTED otherwise                    */

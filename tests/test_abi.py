@@ -346,6 +346,10 @@ def test_partial_kernel_name_for_sized_calls():
     assert name(bf, bf, 4, 1, 24, 6, 128, 0, 4096, 4, options=heads) == "fd_partial_mma_kernel"
     assert name(bf, bf, 4, 4, 32, 8, 128, 0, 4096, 4) == "fd_partial_mma_kernel"     # 16 rows
     assert name(bf, bf, 4, 8, 32, 8, 128, 0, 4096, 4) == "fd_partial_tc_kernel"      # 32 rows
+    # up to 32 rows with at most 256 tokens a split: the mma.sync wide kernel
+    assert name(bf, bf, 4, 8, 32, 8, 128, 0, 1024, 4) == "fd_partial_wide_kernel"
+    assert name(bf, bf, 4, 8, 32, 8, 128, 0, 1028, 4) == "fd_partial_tc_kernel"     # 257 a split
+    assert name(bf, bf, 4, 8, 64, 8, 128, 0, 1024, 4) == "fd_partial_tc_kernel"     # 64 rows
     for bad in ((0, 1, 32, 8), (4, 0, 32, 8), (4, 1, 30, 8), (4, 1, 32, 0), (4, 17, 32, 8)):
         assert name(bf, bf, *bad, 128, 0, 4096, 4) is None
     assert name(bf, bf, 4, 1, 32, 8, 128, 0, 0, 4) is None
