@@ -83,6 +83,9 @@ constexpr int64_t kHeadsMinPairsPerSm = 5;
 // tokens per item the grid is ahead (bf16 256 x 512: 77.3 against 80.2).
 constexpr int64_t kPersistMaxItemTokens = 256;
 constexpr int64_t kPersistMinItemsPerSm = 6;
+// Splits of fewer tokens than this, with 17 to 32 query rows per kv head, run the
+// persistent wide kernel rather than the tcgen05 kernel (resolve_path).
+constexpr int64_t kTcMinSplitTokens = 513;
 
 Schedule choose_schedule(int sched, int path, bool kv8, bool f32, int64_t d, int64_t Hkv,
                          int32_t page_size, bool fused, int64_t rows, int64_t pairs,
@@ -108,9 +111,15 @@ Schedule choose_schedule(int sched, int path, bool kv8, bool f32, int64_t d, int
                          sched == FD_SCHEDULE_HEAD_GROUPS);
   const bool short_items = split_len > 0 && split_len <= kPersistMaxItemTokens &&
                            pairs / fd::kHeadGroup * S >= kPersistMinItemsPerSm * sms;
-  sc.persistent = path == FD_PATH_MMA && !fused && narrow &&
+  // Wide groups of up to 32 rows (the mma.sync wide kernel, 8 rows a warp) have a
+  // persistent form too, taken automatically for the short splits that resolve_path
+  // gives them (fewer than kTcMinSplitTokens tokens).
+  const bool wide32 = rows > fd::kMaxNarrowRows && rows <= 32 && !f32 && !kv8;
+  const bool short_wide = wide32 && split_len > 0 && split_len < kTcMinSplitTokens;
+  sc.persistent = path == FD_PATH_MMA && !fused && (narrow || wide32) &&
                   (sched == FD_SCHEDULE_PERSISTENT ||
-                   (sched == FD_SCHEDULE_AUTO && sc.heads && big_batch && short_items));
+                   (sched == FD_SCHEDULE_AUTO &&
+                    ((sc.heads && big_batch && short_items) || short_wide)));
   // Tail sharing: the tcgen05 kernel, when asked for (measured slower than the plain
   // grid on GB300: the owners' claim round trips cost more than the tail it recovers).
   sc.tail_share = path == FD_PATH_TCGEN05 && sched == FD_SCHEDULE_TAIL_SHARING;
@@ -127,15 +136,15 @@ bool tc_takes(int32_t q_dtype, bool kv8, int64_t d, int32_t page_size, int64_t r
 // Automatic choice: groups of kTcAutoMinRows rows or more go to the tcgen05 kernel where
 // it applies; otherwise the mma.sync path for bf16 and for f32 groups of up to
 // kMaxF32MmaRows rows, and the CUDA-core path for larger f32 groups.  Exception: groups
-// of up to 32 rows whose splits hold at most kTcMinSplitTokens tokens (split_len; 0: not
-// known) take the mma.sync wide kernel.  The tcgen05 kernel holds one CTA per SM and pays
-// its start-up and epilogue (~7.5 us) once per split with nothing to overlap them, so
-// short splits of large batches run faster two CTAs per SM.  Measured on GB300 (Hq 64
-// over Hkv 8, 4 query tokens = 32 rows, one split), tcgen05 -> mma.sync: 256 rows x 256
-// tokens 140.1 -> 122.3 us, 512 x 128 239.2 -> 163.0, 128 x 256 69.2 -> 62.2; with 512
-// tokens a split the tcgen05 kernel is ahead (128 x 512: 91.1 against 106.5), and with
-// 64 rows at any length (256 x 256, 8 query tokens: 153.9 against 253.2).
-constexpr int64_t kTcMinSplitTokens = 257;
+// of up to 32 rows whose splits hold fewer than kTcMinSplitTokens tokens (split_len; 0:
+// not known) take the mma.sync wide kernel on the persistent schedule (choose_schedule).
+// The tcgen05 kernel holds one CTA per SM and pays its start-up and epilogue (~7.5 us)
+// once per split with nothing to overlap them; the persistent wide kernel streams its
+// items back to back, two CTAs per SM.  Measured on GB300 (Hq 64 over Hkv 8, 4 query
+// tokens = 32 rows, one split), tcgen05 -> persistent wide: 256 rows x 256 tokens 140.0
+// -> 78.0 us, 512 x 128 238.8 -> 94.2, 128 x 512 91.0 -> 77.7, 64 x 512 49.1 -> 43.4;
+// from 1024 tokens a split the tcgen05 kernel is ahead (64 x 1024: 69.8 against 74.2,
+// 32 x 2048: 54.4 against 71.6), and with 64 rows at any length.
 
 int resolve_path(int path, int32_t q_dtype, bool kv8, int64_t d, int32_t page_size,
                  int64_t rows, int64_t split_len) {
@@ -164,11 +173,12 @@ const char* kernel_name(const Settings& cfg, int32_t dtype, int32_t kv_dtype, in
     return tc_takes(dtype, kv8, d, page_size, rows) ? "fd_partial_tc_kernel" : nullptr;
   if (rows > fd::kMaxNarrowRows && (path != FD_PATH_MMA || kv8)) return nullptr;
   if (path == FD_PATH_SIMT) return "fd_partial_simt_kernel";
-  if (rows > fd::kMaxNarrowRows) return "fd_partial_wide_kernel";
   // One split with an output writes the output from the partial pass: no in-kernel merge.
   const bool fused = with_output && S != 1 && cfg.merge == FD_MERGE_IN_KERNEL;
   const Schedule sc = choose_schedule(cfg.schedule, path, kv8, dtype == FD_F32, d, Hkv,
                                       page_size, fused, rows, pairs, S, split_len);
+  if (rows > fd::kMaxNarrowRows)
+    return sc.persistent ? "fd_partial_wide_persist_kernel" : "fd_partial_wide_kernel";
   if (sc.heads) return sc.persistent ? "fd_partial_heads_persist_kernel" : "fd_partial_heads_kernel";
   if (sc.persistent) return "fd_partial_persist_kernel";
   return "fd_partial_mma_kernel";

@@ -57,7 +57,7 @@ struct MmaShape {
   static constexpr bool KV8 = KV8_;                        // K/V stored as FP8 E4M3 codes
   static constexpr bool WIDE = WIDE_;
   static constexpr bool F32 = F32_;
-  static_assert(!(WIDE && (KV8 || PERSIST_)), "wide groups: bf16 grid schedule only");
+  static_assert(!(WIDE && KV8), "wide groups: bf16 only");
   static_assert(!(F32 && (KV8 || PERSIST_ || WIDE_ || G_ > 8)),
                 "f32 inputs: grid schedule, up to 8 rows");
   static constexpr int NT = G > 8 ? 2 : 1;                 // n-tiles of 8 heads
@@ -1144,11 +1144,100 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   pdl_trigger();
 }
 
+// ---------------------------------------------------------------- persistent wide groups
+// The persistent schedule over the wide kernel's items (split, kv head, row) of 17 to 32
+// query rows: consumer warp w keeps rows 8 w .. 8 w + 7 of every item over each whole
+// tile, restarts them at an item's first tile and writes their partial at its last, so
+// the warps never wait for one another and the producer streams the next item while
+// they finish.  Per item, the arithmetic is the wide kernel's, bit for bit.
+template <class SH>
+__global__ void __launch_bounds__(SH::THREADS, 2)
+    fd_partial_wide_persist_kernel(const __grid_constant__ CUtensorMap tk,
+                                   const __grid_constant__ CUtensorMap tv,
+                                   const __grid_constant__ Params p) {
+  constexpr int TT = SH::TT, STAGES = SH::STAGES;
+  static_assert(SH::WIDE && SH::PERSIST && SH::G == 8, "wide groups of up to 32 rows");
+  if (threadIdx.x == SH::NCW * 32) prefetch_first_item<TT, 1>(p, &tk, &tv, kPrefetchTiles);
+  pdl_wait();                       // inputs of this step are visible
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  auto* ctl = reinterpret_cast<PersistCtl<STAGES>*>(stages + SH::RING_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_addr(&ctl->full[s]), 1);
+      mbar_init(smem_addr(&ctl->empty[s]), SH::NCW);
+    }
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == SH::NCW) {
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+    produce_items<TT, STAGES, Consumer<SH>::kDirect, 1>(p, &tk, &tv, stages, ctl, lane);
+    pdl_trigger();
+    return;
+  }
+
+  Consumer<SH> c;
+  const bool multi_page = p.page_size > 0 && p.page_size < TT;
+  const uint32_t lb = (uint32_t)p.log2_box;
+  bool open = false;                // an item started and not yet written
+  TileMeta mt{};
+  for (int n = 0;; ++n) {
+    const int stage = n % STAGES;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(smem_addr(&ctl->full[stage]), (n / STAGES) & 1);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) {
+        ctl->abort = 1;
+        atomicOr(p.flags, kDevFlagTimeout);
+      }
+      break;
+    }
+    mt = ctl->meta[stage];
+    if (mt.flags & kMetaDone) break;
+    if (mt.flags & kMetaFirst) {
+      c.start(p, mt.b, mt.g, mt.L, lane, warp * SH::G);
+      open = true;
+    }
+    uint8_t* kt = stages + (size_t)stage * 2 * kTileBytes;
+    c.tile(p, kt, kt + kTileBytes, mt.t0, mt.lo, mt.hi, mt.bad, warp, lane, lb, multi_page);
+    if (mt.flags & kMetaLast) {
+      c.store_own(p, mt.b, mt.g, mt.split, lane);
+      open = false;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
+  }
+  // An item left half done by a wait that ran out: weight 0 for this warp's rows.
+  if (open) {
+    const int h = warp * SH::G + lane;
+    if (lane < SH::G && h < p.n_rows) put_empty_row<Consumer<SH>::kDirect>(p, mt.b, mt.g, h, mt.split);
+  }
+  pdl_trigger();
+}
+
 template <class SH>
 cudaError_t launch_mma(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv,
                        cudaStream_t stream) {
   cudaError_t e;
-  if constexpr (SH::PERSIST) {
+  if constexpr (SH::PERSIST && SH::WIDE) {
+    auto kernel = fd_partial_wide_persist_kernel<SH>;
+    static SmemOptIn opt_in;
+    e = opt_in.apply(kernel, (int)SH::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int64_t items = (int64_t)p.S * p.Hkv * p.B;
+    const unsigned grid = (unsigned)(items < 2 * sms ? items : 2 * sms);
+    e = launch_partial_kernel(kernel, dim3(grid), SH::THREADS, SH::SMEM_BYTES, stream, tk, tv, p);
+  } else if constexpr (SH::PERSIST) {
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     if (p.head_group) {
@@ -1218,7 +1307,7 @@ cudaError_t dispatch_g(const Params& p, const CUtensorMap& tk, const CUtensorMap
     case 8: return launch_mma<MmaShape<D, 8, KV8, PERSIST>>(p, tk, tv, stream);
     case 16: return launch_mma<MmaShape<D, 16, KV8, PERSIST>>(p, tk, tv, stream);
     case 32:   // wide groups: four warps of 8 rows
-      if constexpr (!KV8 && !PERSIST) return launch_mma<MmaShape<D, 8, false, false, true>>(p, tk, tv, stream);
+      if constexpr (!KV8) return launch_mma<MmaShape<D, 8, false, PERSIST, true>>(p, tk, tv, stream);
       else return cudaErrorInvalidValue;
     case 64:   // four warps of 16 rows
       if constexpr (!KV8 && !PERSIST) return launch_mma<MmaShape<D, 16, false, false, true>>(p, tk, tv, stream);
@@ -1262,6 +1351,7 @@ cudaError_t dispatch_kind(const Params& p, const CUtensorMap& tk, const CUtensor
 // split's result as the output.
 bool mma_writes_direct(const Params& p) {
   const int r = rows_template(p.n_rows);
+  if (r == 32) return true;         // wide groups, 8 rows a warp (grid or persistent)
   if (p.head_group || p.persistent) return r <= 8;
   return r != 64;
 }

@@ -89,7 +89,8 @@ typedef struct {
 typedef enum {
   FD_PATH_AUTO = 0,    /* the fastest kernel for the call: FD_PATH_TCGEN05 for bf16 groups
                           of 17 to 64 query rows per kv head that it takes (but groups of
-                          up to 32 rows with at most 256 tokens a split: FD_PATH_MMA),
+                          up to 32 rows with at most 512 tokens a split: FD_PATH_MMA, on
+                          the persistent schedule),
                           FD_PATH_MMA for other bf16 groups and f32 groups of up to 8
                           rows, CUDA cores otherwise                                     */
   FD_PATH_SIMT = 1,    /* CUDA-core dot products for every dtype                         */
@@ -381,8 +382,10 @@ FD_API int32_t fd_get_path(void);
  * FD_SCHEDULE_PERSISTENT: two CTAs per SM take items from a queue in the workspace
  * header and stream their tiles back to back.  Items are those of the tiling the
  * automatic schedule picks: one kv head (same partials as FD_SCHEDULE_GRID, bit for
- * bit), or a group of 4 kv heads where FD_SCHEDULE_AUTO takes head groups (same
- * partials as the head-group kernel, bit for bit).
+ * bit; also for 17 to 32 query rows per kv head on the wide kernel), or a group of 4 kv
+ * heads where FD_SCHEDULE_AUTO takes head groups (same partials as the head-group
+ * kernel, bit for bit).  The automatic schedule itself runs it for large batches of
+ * short rows (head groups) and for short splits of 17 to 32 rows.
  * FD_SCHEDULE_HEAD_GROUPS: one CTA per (split, group of 4 kv heads, row); a tile is 16
  * tokens (bf16; 32 for FP8 E4M3) of a row -- of one page -- for all 4 heads, loaded as
  * one 16 KB TMA box, and each consumer warp keeps one head's state (no cross-warp
@@ -490,7 +493,8 @@ FD_API fd_status fd_selftest_stalled_decode(const fd_tensor* q, const fd_tensor*
  * Name of the partial-pass kernel a call would launch under the current process
  * settings (path, merge mode, schedule): "fd_partial_mma_kernel",
  * "fd_partial_heads_kernel", "fd_partial_wide_kernel", "fd_partial_persist_kernel",
- * "fd_partial_heads_persist_kernel", "fd_partial_tc_kernel" or "fd_partial_simt_kernel".  dtype is q's fd_dtype, kv_dtype
+ * "fd_partial_heads_persist_kernel", "fd_partial_wide_persist_kernel",
+ * "fd_partial_tc_kernel" or "fd_partial_simt_kernel".  dtype is q's fd_dtype, kv_dtype
  * the cache's; page_size 0 for a contiguous cache; rows the query rows per kv head
  * (Q x Hq / Hkv); with_output 1 for fd_decode_attention, 0 for fd_decode_partial.  For
  * a call of more than one split and fewer than 5 (b, kv head) pairs per SM: with one

@@ -194,7 +194,8 @@ def test_partial_kernel_name_follows_settings():
         assert name(f32, f32, 128, 8) == "fd_partial_mma_kernel"
         fd.set_path(fd.FD_PATH_MMA)
         assert name(f32, f32, 128, 8, rows=16) is None
-        assert name(bf, bf, 128, 8, rows=32) == "fd_partial_wide_kernel"
+        assert name(bf, bf, 128, 8, rows=32) == "fd_partial_wide_persist_kernel"  # 8 a warp
+        assert name(bf, bf, 128, 8, rows=64) == "fd_partial_wide_kernel"          # 16 a warp
         fd.set_path(fd.FD_PATH_TCGEN05)
         assert name(bf, bf, 128, 8) == "fd_partial_tc_kernel"                 # any group size
         assert name(bf, bf, 128, 8, 32, rows=64) == "fd_partial_tc_kernel"
@@ -346,10 +347,12 @@ def test_partial_kernel_name_for_sized_calls():
     assert name(bf, bf, 4, 1, 24, 6, 128, 0, 4096, 4, options=heads) == "fd_partial_mma_kernel"
     assert name(bf, bf, 4, 4, 32, 8, 128, 0, 4096, 4) == "fd_partial_mma_kernel"     # 16 rows
     assert name(bf, bf, 4, 8, 32, 8, 128, 0, 4096, 4) == "fd_partial_tc_kernel"      # 32 rows
-    # up to 32 rows with at most 256 tokens a split: the mma.sync wide kernel
-    assert name(bf, bf, 4, 8, 32, 8, 128, 0, 1024, 4) == "fd_partial_wide_kernel"
-    assert name(bf, bf, 4, 8, 32, 8, 128, 0, 1028, 4) == "fd_partial_tc_kernel"     # 257 a split
+    # up to 32 rows with at most 512 tokens a split: the persistent mma.sync wide kernel
+    assert name(bf, bf, 4, 8, 32, 8, 128, 0, 2048, 4) == "fd_partial_wide_persist_kernel"
+    assert name(bf, bf, 4, 8, 32, 8, 128, 0, 2052, 4) == "fd_partial_tc_kernel"     # 513 a split
     assert name(bf, bf, 4, 8, 64, 8, 128, 0, 1024, 4) == "fd_partial_tc_kernel"     # 64 rows
+    grid = fd.options(schedule=fd.FD_SCHEDULE_GRID)
+    assert name(bf, bf, 4, 8, 32, 8, 128, 0, 2048, 4, options=grid) == "fd_partial_wide_kernel"
     for bad in ((0, 1, 32, 8), (4, 0, 32, 8), (4, 1, 30, 8), (4, 1, 32, 0), (4, 17, 32, 8)):
         assert name(bf, bf, *bad, 128, 0, 4096, 4) is None
     assert name(bf, bf, 4, 1, 32, 8, 128, 0, 0, 4) is None

@@ -95,6 +95,11 @@ def _stalled_case(kind):
                                       out_dtype=torch.float32)
         S, stall = 4, 1
         opts = fd.options(schedule=fd.FD_SCHEDULE_HEAD_GROUPS)
+    elif kind == "wide_persist":             # 32 rows per kv head, persistent
+        w = workloads.contiguous_case(2, 16, 2, 128, 4096, [4096, 2000], seed=822,
+                                      out_dtype=torch.float32)
+        Q, S, stall = 4, 4, 2
+        opts = fd.options(path=fd.FD_PATH_MMA, schedule=fd.FD_SCHEDULE_PERSISTENT)
     elif kind == "direct":                   # one split: out written by the partial pass
         w = workloads.contiguous_case(2, 16, 2, 128, 4096, [4096, 2000], seed=821,
                                       out_dtype=torch.float32)
@@ -105,7 +110,8 @@ def _stalled_case(kind):
 
 
 @pytest.mark.parametrize("kind", ["mma", "mma_fused", "heads", "simt", "tc", "tc_shared", "wide",
-                                  "persist", "heads_persist", "heads_contiguous", "direct"])
+                                  "persist", "heads_persist", "heads_contiguous", "direct",
+                                  "wide_persist"])
 def test_real_kernel_wait_runs_out_and_context_survives(kind):
     import numpy as np
     import oracle
@@ -120,6 +126,7 @@ def test_real_kernel_wait_runs_out_and_context_survives(kind):
                 "wide": "fd_partial_wide_kernel", "persist": "fd_partial_persist_kernel",
                 "heads_persist": "fd_partial_heads_persist_kernel",
                 "heads_contiguous": "fd_partial_heads_kernel",
+                "wide_persist": "fd_partial_wide_persist_kernel",
                 "direct": "fd_partial_mma_kernel"}[kind]
     assert fd.partial_kernel_name_for(torch.bfloat16, torch.bfloat16, w.B, Q, w.Hq, w.Hkv, w.d,
                                       w.page_size, w.L_cap, S, options=opts) == expected

@@ -197,6 +197,43 @@ def test_persistent_head_groups(kind):
         assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
 
 
+@pytest.mark.parametrize("d,paged", [(128, 0), (128, 16), (64, 0), (64, 8)])
+def test_persistent_wide_groups(d, paged):
+    """The persistent schedule over wide groups (4 query tokens x G 8 = 32 rows per kv
+    head, 8 rows a warp): against the multi-token oracle and, bit for bit, the wide
+    kernel on the grid, for 1, 3 and 9 splits; rows shorter than the query count leave
+    their first queries without keys."""
+    Q, G, Hkv = 4, 8, 2
+    Hq = Hkv * G
+    lens = [1, 3, 65, 300, 1000, 0]
+    if paged:
+        w = workloads.paged_case(len(lens), Hq, Hkv, d, paged, -(-1024 // paged), lens,
+                                 seed=470 + d + paged, out_dtype=torch.float32)
+    else:
+        w = workloads.contiguous_case(len(lens), Hq, Hkv, d, 1024, lens, seed=470 + d,
+                                      out_dtype=torch.float32)
+    q4 = workloads.multi_token_queries(len(lens), Q, Hq, d, seed=480 + d)
+    _, k, v, lens_np, bt, ps = w.oracle_arrays()
+    ref_o, ref_l = oracle.decode_causal(workloads.np_storage(q4), k, v, lens_np,
+                                        block_table=bt, page_size=ps)
+    B = len(lens)
+    assert fd.partial_kernel_name_for(torch.bfloat16, torch.bfloat16, B, Q, Hq, Hkv, d, paged,
+                                      w.L_cap, 3, options=fd.options(
+                                          path=fd.FD_PATH_MMA,
+                                          schedule=fd.FD_SCHEDULE_PERSISTENT)) == \
+        "fd_partial_wide_persist_kernel"
+    wd = w.to("cuda")
+    qd = q4.cuda()
+    for S in (1, 3, 9):
+        og, lg = _run_sched(wd, w, S, fd.FD_SCHEDULE_GRID, q=qd)
+        op, lp = _run_sched(wd, w, S, fd.FD_SCHEDULE_PERSISTENT, q=qd)
+        assert torch.equal(og, op) and torch.equal(lg, lp)
+        mw = workloads.Workload("mt", q4.reshape(B * Q, Hq, d), w.k, w.v, w.seq_lens)
+        check(mw, op.cpu().double().numpy().reshape(B * Q, Hq, d),
+              lp.cpu().double().numpy().reshape(B * Q, Hq),
+              ref_o.reshape(B * Q, Hq, d), ref_l.reshape(B * Q, Hq))
+
+
 def test_persistent_back_to_back_and_stale_workspace():
     """Calls in a row on one stream with no host sync between them, in a workspace whose
     partial regions start as random bytes: each launch must find a clean queue."""
