@@ -606,7 +606,7 @@ struct Consumer {
   // Whether store_own can write a single split's result as the output (Params::direct):
   // not for 16 rows per warp, where the head-group and wide kernels sit at their
   // register cap (the direct branch made them spill); mma_writes_direct tells the host.
-  static constexpr bool kDirect = SH::G <= 8;
+  __host__ __device__ static constexpr bool direct_ok() { return SH::G <= 8; }
 
   // End of a split when this warp alone saw all of it (head-group tiles: one warp per kv
   // head): write O_i = acc / l and LSE_i = (m + log2 l) ln 2 of the warp's rows directly,
@@ -622,7 +622,7 @@ struct Consumer {
       }
     constexpr bool PAIRED = SH::KV8 || SH::F32;
     const int d0 = PAIRED ? 2 * qr : qr, d1 = PAIRED ? 2 * qr + 1 : qr + 8;
-    if constexpr (kDirect) {
+    if constexpr (direct_ok()) {
       if (p.direct) {               // the row of out; a row without keys gets zeros
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -846,7 +846,7 @@ __global__ void __maxnreg__(200)
   pdl_trigger();
   if (aborted) {                    // this warp's rows of the split: weight 0
     const int h = warp * SH::G + lane;
-    if (lane < SH::G && h < p.n_rows) put_empty_row<Consumer<SH>::kDirect>(p, si.b, si.g, h, si.split);
+    if (lane < SH::G && h < p.n_rows) put_empty_row<Consumer<SH>::direct_ok()>(p, si.b, si.g, h, si.split);
   } else {
     c.store_own(p, si.b, si.g, si.split, lane);
   }
@@ -891,7 +891,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (si.n_tiles == 0) {            // empty split for every head of the group
     for (int i = threadIdx.x; i < kHeadGroup * p.n_rows; i += blockDim.x)
-      put_empty_row<Consumer<SH>::kDirect>(p, si.b, si.g + i / p.n_rows, i % p.n_rows, si.split);
+      put_empty_row<Consumer<SH>::direct_ok()>(p, si.b, si.g + i / p.n_rows, i % p.n_rows, si.split);
     pdl_trigger();
     return;
   }
@@ -942,7 +942,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   }
   pdl_trigger();
   if (aborted || *reinterpret_cast<volatile int32_t*>(&ctl->abort)) {
-    if (lane < p.n_rows) put_empty_row<Consumer<SH>::kDirect>(p, si.b, g, lane, si.split);
+    if (lane < p.n_rows) put_empty_row<Consumer<SH>::direct_ok()>(p, si.b, g, lane, si.split);
     return;
   }
   c.store_own(p, si.b, g, si.split, lane);
@@ -1099,7 +1099,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   if (warp == SH::NCW) {
     prefetch_tensormap(&tk);
     prefetch_tensormap(&tv);
-    produce_items<TOK, STAGES, Consumer<SH>::kDirect, kHeadGroup>(p, &tk, &tv, stages, ctl, lane);
+    produce_items<TOK, STAGES, Consumer<SH>::direct_ok(), kHeadGroup>(p, &tk, &tv, stages, ctl, lane);
     pdl_trigger();
     return;
   }
@@ -1140,7 +1140,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   }
   // An item left half done by a wait that ran out: weight 0 for this warp's head.
   if (open && lane < p.n_rows)
-    put_empty_row<Consumer<SH>::kDirect>(p, mt.b, mt.g + warp, lane, mt.split);
+    put_empty_row<Consumer<SH>::direct_ok()>(p, mt.b, mt.g + warp, lane, mt.split);
   pdl_trigger();
 }
 
@@ -1178,7 +1178,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   if (warp == SH::NCW) {
     prefetch_tensormap(&tk);
     prefetch_tensormap(&tv);
-    produce_items<TT, STAGES, Consumer<SH>::kDirect, 1>(p, &tk, &tv, stages, ctl, lane);
+    produce_items<TT, STAGES, Consumer<SH>::direct_ok(), 1>(p, &tk, &tv, stages, ctl, lane);
     pdl_trigger();
     return;
   }
@@ -1218,7 +1218,7 @@ __global__ void __launch_bounds__(SH::THREADS, 2)
   // An item left half done by a wait that ran out: weight 0 for this warp's rows.
   if (open) {
     const int h = warp * SH::G + lane;
-    if (lane < SH::G && h < p.n_rows) put_empty_row<Consumer<SH>::kDirect>(p, mt.b, mt.g, h, mt.split);
+    if (lane < SH::G && h < p.n_rows) put_empty_row<Consumer<SH>::direct_ok()>(p, mt.b, mt.g, h, mt.split);
   }
   pdl_trigger();
 }
@@ -1347,7 +1347,7 @@ cudaError_t dispatch_kind(const Params& p, const CUtensorMap& tk, const CUtensor
 
 // The kernels launch_partial_mma runs with 16 rows per warp -- head groups, the wide
 // kernel for 33 to 64 rows and the persistent schedule -- write partials only (their
-// Consumer<SH>::kDirect / DIRECT forms); every other instantiation also writes a single
+// Consumer<SH>::direct_ok() / DIRECT forms); every other instantiation also writes a single
 // split's result as the output.
 bool mma_writes_direct(const Params& p) {
   const int r = rows_template(p.n_rows);
