@@ -20,7 +20,10 @@
 // the last CTA of a group pays for the merge -- and picks the split count with the
 // shortest simulated step.  It plans for the default schedule: where head-group tiles
 // apply (d = 128 with 16- or 32-token pages and Hkv a multiple of 4) a CTA streams one
-// split of four kv heads in 16-token tiles, one 16 KB box per K and V.
+// split of four kv heads in 16-token tiles, one 16 KB box per K and V.  (The automatic
+// schedule also takes head groups -- and, for short rows, their persistent form -- for
+// batches of at least 5 (b, kv head) pairs per SM on any cache; both planners already
+// give those one split, since one wave of one-head CTAs is full without splitting.)
 #include <cuda_runtime.h>
 
 #include <algorithm>
