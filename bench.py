@@ -128,6 +128,8 @@ KERNEL_SOURCES = {
                                   "fd_device.cuh", "fd_internal.h"],
     "fd_partial_heads_persist_kernel": ["fd_partial_mma.cu", "fd_pipeline.cuh",
                                         "fd_epilogue.cuh", "fd_device.cuh", "fd_internal.h"],
+    "fd_partial_wide_persist_kernel": ["fd_partial_mma.cu", "fd_pipeline.cuh",
+                                       "fd_epilogue.cuh", "fd_device.cuh", "fd_internal.h"],
     "fd_partial_simt_kernel": ["fd_partial_simt.cu", "fd_partial_simt.cuh", "fd_pipeline.cuh",
                                "fd_epilogue.cuh", "fd_device.cuh", "fd_internal.h"],
     "fd_partial_wide_kernel": ["fd_partial_mma.cu", "fd_pipeline.cuh", "fd_epilogue.cuh",
