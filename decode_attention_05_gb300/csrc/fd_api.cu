@@ -114,7 +114,7 @@ Schedule choose_schedule(int sched, int path, bool kv8, bool f32, int64_t d, int
   // Wide groups of up to 32 rows (the mma.sync wide kernel, 8 rows a warp) have a
   // persistent form too, taken automatically for the short splits that resolve_path
   // gives them (fewer than kTcMinSplitTokens tokens).
-  const bool wide32 = rows > fd::kMaxNarrowRows && rows <= 32 && !f32 && !kv8;
+  const bool wide32 = rows > fd::kMaxNarrowRows && rows <= 32 && !f32;
   const bool short_wide = wide32 && split_len > 0 && split_len < kTcMinSplitTokens;
   sc.persistent = path == FD_PATH_MMA && !fused && (narrow || wide32) &&
                   (sched == FD_SCHEDULE_PERSISTENT ||
@@ -171,7 +171,8 @@ const char* kernel_name(const Settings& cfg, int32_t dtype, int32_t kv_dtype, in
     return nullptr;
   if (path == FD_PATH_TCGEN05)
     return tc_takes(dtype, kv8, d, page_size, rows) ? "fd_partial_tc_kernel" : nullptr;
-  if (rows > fd::kMaxNarrowRows && (path != FD_PATH_MMA || kv8)) return nullptr;
+  if (rows > fd::kMaxNarrowRows && (path != FD_PATH_MMA || (kv8 && rows > fd::kMaxFp8Rows)))
+    return nullptr;
   if (path == FD_PATH_SIMT) return "fd_partial_simt_kernel";
   // One split with an output writes the output from the partial pass: no in-kernel merge.
   const bool fused = with_output && S != 1 && cfg.merge == FD_MERGE_IN_KERNEL;
@@ -637,10 +638,14 @@ fd_status prepare(const fd_tensor* q, const fd_tensor* k_cache, const fd_tensor*
                 fd::kMaxF32MmaRows);
   if (kv8 && path != FD_PATH_MMA)
     return fail(FD_ERR_UNSUPPORTED, "the FP8 KV cache runs on the tensor-core path only");
-  if (Q * G > fd::kMaxNarrowRows && (path == FD_PATH_SIMT || kv8))
+  if (Q * G > fd::kMaxNarrowRows && path == FD_PATH_SIMT)
     return fail(FD_ERR_UNSUPPORTED,
-                "more than %d query rows per kv head (%lld) run on the bf16 tensor-core paths only",
+                "more than %d query rows per kv head (%lld) run on the tensor-core paths only",
                 fd::kMaxNarrowRows, (long long)(Q * G));
+  if (kv8 && Q * G > fd::kMaxFp8Rows)
+    return fail(FD_ERR_UNSUPPORTED,
+                "an FP8 KV cache takes up to %d query rows per kv head, not %lld",
+                fd::kMaxFp8Rows, (long long)(Q * G));
 
   // ---- schedule (fd_set_schedule or the call's options).  One split with an output:
   // the partial pass writes the output itself (Params::direct) and nothing merges.

@@ -163,6 +163,9 @@ struct SmemOptIn {
 // up to kMaxRows (groups above kMaxNarrowRows run the wide tensor-core kernel only).
 constexpr int kMaxNarrowRows = 16;
 constexpr int kMaxRows = 64;
+// FP8 KV caches take up to kMaxFp8Rows query rows per kv head (the wide kernel with 8
+// rows a warp above kMaxNarrowRows).
+constexpr int kMaxFp8Rows = 32;
 // The automatic path sends groups of at least this many rows to the tcgen05 kernel
 // (where it applies).  GQA 128K cache, one CTA's worth of splits per SM: 32 rows 91 us
 // (tcgen05) vs 132 us (mma.sync wide kernel), 64 rows 93 us vs 228 us; up to 16 rows the

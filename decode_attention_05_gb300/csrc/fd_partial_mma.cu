@@ -57,7 +57,7 @@ struct MmaShape {
   static constexpr bool KV8 = KV8_;                        // K/V stored as FP8 E4M3 codes
   static constexpr bool WIDE = WIDE_;
   static constexpr bool F32 = F32_;
-  static_assert(!(WIDE && KV8), "wide groups: bf16 only");
+  static_assert(!(WIDE && KV8 && G_ > 8), "wide groups: FP8 up to 8 rows a warp");
   static_assert(!(F32 && (KV8 || PERSIST_ || WIDE_ || G_ > 8)),
                 "f32 inputs: grid schedule, up to 8 rows");
   static constexpr int NT = G > 8 ? 2 : 1;                 // n-tiles of 8 heads
@@ -509,6 +509,25 @@ struct Consumer {
         // gives the A fragment of V^T with m-row qr <-> dim 2 qr and m-row qr + 8 <->
         // dim 2 qr + 1 of the 16-dim tile (undone when the output is written).
         const int vtok_addr = rb + lr + (lm & 1) * 8;
+        // WIDE: every warp reads every row, so V rows outside [lo, hi) or on an invalid
+        // page are masked in registers (after widening: their codes may be NaN).  a[0],
+        // a[1] hold tokens 2c, 2c + 1 of the chunk (low, high half), a[2], a[3] tokens
+        // 2c + 8, 2c + 9, c = lane % 4 -- as in the bf16 branch below.
+        uint32_t vmask[2] = {0xffffffffu, 0xffffffffu};
+        if (SH::WIDE && !clean) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t mk = 0u;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int row = rb + 8 * hh + 2 * (lane & 3) + u;
+              const int64_t tok = t0 + row;
+              const int pslot = multi_page ? (row >> p.log2_page) : 0;
+              if (tok >= lo && tok < hi && !((bad >> pslot) & 1u)) mk |= 0xffffu << (16 * u);
+            }
+            vmask[hh] = mk;
+          }
+        }
 #pragma unroll
         for (int mt = 0; mt < SH::MTILES; mt += 2) {
           const int c16 = mt + (lm >> 1);
@@ -518,8 +537,14 @@ struct Consumer {
           for (int u = 0; u < 2; ++u) {
             const uint32_t x0 = byte_perm(r[2 * u], 0u, 0x3120u);       // tokens 0-7
             const uint32_t x1 = byte_perm(r[2 * u + 1], 0u, 0x3120u);   // tokens 8-15
-            const uint32_t a[4] = {e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x0 >> 16),
-                                   e4m3x2_to_f16x2(x1), e4m3x2_to_f16x2(x1 >> 16)};
+            uint32_t a[4] = {e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x0 >> 16),
+                             e4m3x2_to_f16x2(x1), e4m3x2_to_f16x2(x1 >> 16)};
+            if (SH::WIDE && !clean) {
+              a[0] &= vmask[0];
+              a[1] &= vmask[0];
+              a[2] &= vmask[1];
+              a[3] &= vmask[1];
+            }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma_f16(acc[nt][mt + u], a, pb[ch][nt][0], pb[ch][nt][1]);
@@ -1306,9 +1331,8 @@ cudaError_t dispatch_g(const Params& p, const CUtensorMap& tk, const CUtensorMap
     case 4: return launch_mma<MmaShape<D, 4, KV8, PERSIST>>(p, tk, tv, stream);
     case 8: return launch_mma<MmaShape<D, 8, KV8, PERSIST>>(p, tk, tv, stream);
     case 16: return launch_mma<MmaShape<D, 16, KV8, PERSIST>>(p, tk, tv, stream);
-    case 32:   // wide groups: four warps of 8 rows
-      if constexpr (!KV8) return launch_mma<MmaShape<D, 8, false, PERSIST, true>>(p, tk, tv, stream);
-      else return cudaErrorInvalidValue;
+    case 32:   // wide groups: four warps of 8 rows (bf16 or FP8 KV)
+      return launch_mma<MmaShape<D, 8, KV8, PERSIST, true>>(p, tk, tv, stream);
     case 64:   // four warps of 16 rows
       if constexpr (!KV8 && !PERSIST) return launch_mma<MmaShape<D, 16, false, false, true>>(p, tk, tv, stream);
       else return cudaErrorInvalidValue;

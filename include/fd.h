@@ -110,7 +110,7 @@ typedef enum {
  *                query j (0-based) attends to the keys t <= L_b - Q + j (the causal mask
  *                of [AI-Infra] 2.5 applied inside each split); a query that sees no key
  *                gets out = 0, lse_out = -inf.  Q * G <= 64 (above 16 rows per kv
- *                head: bf16 on the tensor-core paths only).
+ *                head: the tensor-core paths only; FP8 caches up to 32 rows).
  *   k_cache      device, same dtype as q.  Contiguous: [B, Hkv, L_cap, d] (block_table
  *                NULL).  Paged: [num_pages, Hkv, page_size, d]; logical token t of row
  *                b is slot t % page_size of page block_table[b][t / page_size] -- the
@@ -146,8 +146,8 @@ typedef enum {
  *   stream       cudaStream_t (as void*), NULL = legacy default stream.
  *
  * Supported: d in {64, 128}; G = Hq / Hkv in {1, 2, 4, 8, 16, 32, 64} with Q * G <= 64
- * (more than 16 rows per kv head: bf16 on the tensor-core paths only; f32 on the
- * tensor cores up to 8 rows, on CUDA cores up to 16); (q, k, v) all bf16 with out bf16
+ * (more than 16 rows per kv head: bf16 on the tensor-core paths only -- FP8 caches up
+ * to 32 rows; f32 on the tensor cores up to 8 rows, on CUDA cores up to 16); (q, k, v) all bf16 with out bf16
  * or f32, or all f32 with out f32.  B >= 1, L_cap >= 1.
  * Errors: FD_ERR_INVALID_ARG for rank/shape/stride/alignment mismatches, Hq % Hkv != 0,
  * NULL required pointers, num_splits < 0, page_size invalid with a block table;
@@ -167,9 +167,11 @@ FD_API fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cach
  * among the KV-cache optimisations); the format read here: each kv head g has one fp32
  * dequantisation scale for K and one for V, and an element's value is code * scale.
  *   k_scale, v_scale  device f32 [Hkv] (4-byte aligned), or NULL for 1.0.
- *   q bf16 [B, Hq, 128] or [B, Q, Hq, 128]; out bf16 or f32; head dim 128 only; runs on
- *   the tensor-core path (FP8 pairs widened exactly to f16, q converted to f16, P fed as
- *   f16, f32 accumulation).  Everything else as fd_decode_attention, merge mode included.
+ *   q bf16 [B, Hq, 128] or [B, Q, Hq, 128], up to 32 query rows per kv head (Q x Hq /
+ *   Hkv; above 16 the mma.sync wide kernel, 8 rows a warp); out bf16 or f32; head dim
+ *   128 only; runs on the tensor-core path (FP8 pairs widened exactly to f16, q converted
+ *   to f16, P fed as f16, f32 accumulation).  Everything else as fd_decode_attention,
+ *   merge mode included.
  */
 FD_API fd_status fd_decode_attention_fp8kv(const fd_tensor* q, const fd_tensor* k_cache,
                                            const fd_tensor* v_cache, const float* k_scale,

@@ -178,7 +178,8 @@ def test_partial_kernel_name_follows_settings():
         assert name(bf, bf, 128, 8, 16, rows=64) == "fd_partial_tc_kernel"
         assert name(bf, bf, 128, 8, 8, rows=64) == "fd_partial_wide_kernel"   # 8-token pages
         assert name(bf, bf, 64, 8, rows=32) == "fd_partial_wide_kernel"       # d = 64
-        assert name(bf, f8, 128, 8, rows=32) is None                          # bf16 only
+        assert name(bf, f8, 128, 8, rows=32) == "fd_partial_wide_kernel"      # FP8 <= 32
+        assert name(bf, f8, 128, 8, rows=33) is None
         assert name(f32, f32, 128, 8, rows=32) is None
         assert name(bf, bf, 128, 8, rows=65) is None
         fd.set_merge_mode(fd.FD_MERGE_IN_KERNEL)                              # single launch

@@ -522,8 +522,8 @@ def test_multi_token_decode(name, path, Q, G, paged):
 
 
 def test_multi_token_limits():
-    """Up to 64 query rows per kv head on the bf16 tensor-core path; more rows, or more
-    than 16 on the CUDA-core path or with an FP8 cache, are refused on the host."""
+    """Up to 64 query rows per kv head on the bf16 tensor-core path, 32 with an FP8
+    cache; more rows, or more than 16 on the CUDA-core path, are refused on the host."""
     seq = torch.tensor([64], dtype=torch.int32, device="cuda")
     k = torch.zeros(1, 1, 64, 128, dtype=torch.bfloat16, device="cuda")
     q = torch.zeros(1, 5, 16, 128, dtype=torch.bfloat16, device="cuda")     # 5 x 16 = 80 rows
@@ -535,9 +535,13 @@ def test_multi_token_limits():
         fd.decode_attention(q, k, k, seq, num_splits=1)
     fd.set_path(fd.FD_PATH_AUTO)
     k8 = k.float().to(torch.float8_e4m3fn)
+    q40 = torch.zeros(1, 5, 8, 128, dtype=torch.bfloat16, device="cuda")    # 40 rows
     with pytest.raises(fd.FdError):
-        fd.decode_attention_fp8kv(q, k8, k8, None, None, seq, num_splits=1)
+        fd.decode_attention_fp8kv(q40, k8, k8, None, None, seq, num_splits=1)
+    o8, _ = fd.decode_attention_fp8kv(q, k8, k8, None, None, seq, num_splits=1)  # 24: accepted
     o, l = fd.decode_attention(q, k, k, seq, num_splits=1)                   # accepted
+    torch.cuda.synchronize()
+    assert o8.shape == (1, 3, 8, 128)
     torch.cuda.synchronize()
     assert o.shape == (1, 3, 8, 128)
 
@@ -632,6 +636,55 @@ def test_fp8_kv_multi_token():
     mw = workloads.Workload("mt8", q4.reshape(3 * Q, 32, 128), w.k, w.v, w.seq_lens)
     check(mw, o.cpu().double().numpy().reshape(3 * Q, 32, 128), l.cpu().double().numpy().reshape(3 * Q, 32),
           ref_o.reshape(3 * Q, 32, 128), ref_l.reshape(3 * Q, 32))
+
+
+@pytest.mark.parametrize("Q,G,paged,sched", [(4, 8, 0, "auto"), (3, 8, 32, "auto"),
+                                             (4, 8, 64, "grid"), (2, 16, 0, "persistent"),
+                                             (4, 8, 16, "persistent")])
+def test_fp8_kv_wide_groups(Q, G, paged, sched):
+    """FP8 cache with 17 to 32 query rows per kv head: the mma.sync wide kernel (8 rows a
+    warp), on the grid and the persistent schedule, against the fp64 multi-token oracle
+    over the dequantised cache (power-of-two scales make it exact in fp32); the
+    persistent and grid results agree bit for bit."""
+    Hkv = 2
+    Hq = Hkv * G
+    lens = [1, Q - 1, 65, 300, 1000, 0]
+    if paged:
+        w = workloads.paged_case(len(lens), Hq, Hkv, 128, paged, -(-1024 // paged), lens,
+                                 seed=330 + Q + G + paged, out_dtype=torch.float32)
+    else:
+        w = workloads.contiguous_case(len(lens), Hq, Hkv, 128, 1024, lens, seed=330 + Q + G,
+                                      out_dtype=torch.float32)
+    kc, vc, ks, vs = workloads.fp8_quantize(w, power_of_two_scales=True)
+    deq = lambda c, s: (c.float() * s.view(1, -1, 1, 1)).numpy()
+    q4 = workloads.multi_token_queries(len(lens), Q, Hq, 128, seed=340 + Q + G)
+    _, _, _, lens_np, bt, ps = w.oracle_arrays()
+    ref_o, ref_l = oracle.decode_causal(q4.float().numpy(), deq(kc, ks), deq(vc, vs), lens_np,
+                                        block_table=bt, page_size=ps)
+    B = len(lens)
+    wd = w.to("cuda")
+    kcd, vcd, ksd, vsd, qd = kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda(), q4.cuda()
+    schedule = {"auto": fd.FD_SCHEDULE_AUTO, "grid": fd.FD_SCHEDULE_GRID,
+                "persistent": fd.FD_SCHEDULE_PERSISTENT}[sched]
+    res = {}
+    for S in (1, 5):
+        for sc in {schedule, fd.FD_SCHEDULE_GRID}:
+            fd.set_schedule(sc)
+            ws = torch.zeros(fd.workspace_size(B, Q * Hq, Hkv, 128, S), dtype=torch.uint8,
+                             device="cuda")
+            o, l = fd.decode_attention_fp8kv(qd, kcd, vcd, ksd, vsd, wd.seq_lens, wd.block_table,
+                                             paged, S, workspace=ws, out_dtype=torch.float32)
+            torch.cuda.synchronize()
+            assert fd.read_device_error(ws) == 0
+            mw = workloads.Workload("mt8", q4.reshape(B * Q, Hq, 128), w.k, w.v, w.seq_lens)
+            check(mw, o.cpu().double().numpy().reshape(B * Q, Hq, 128),
+                  l.cpu().double().numpy().reshape(B * Q, Hq),
+                  ref_o.reshape(B * Q, Hq, 128), ref_l.reshape(B * Q, Hq))
+            res[(S, sc)] = (o, l)
+        if schedule == fd.FD_SCHEDULE_PERSISTENT:
+            a, b = res[(S, schedule)], res[(S, fd.FD_SCHEDULE_GRID)]
+            assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    fd.set_schedule(fd.FD_SCHEDULE_AUTO)
 
 
 def test_fp8_kv_is_refused_by_the_bf16_entry_point():
