@@ -259,6 +259,23 @@ def good():
             desc([2, 8, 128]))
 
 
+def test_fp8_row_limit_on_the_host():
+    """An FP8 cache takes up to 32 query rows per kv head: 40 (5 query tokens x G 8) are
+    refused before anything touches the device."""
+    lib = fd.lib()
+    r = ctypes.byref
+    for Qn, ok in ((5, False), (4, True)):
+        q, out = desc([2, Qn, 16, 128]), desc([2, Qn, 16, 128])
+        k, v = desc([2, 2, 1024, 128], dtype=3), desc([2, 2, 1024, 128], dtype=3)
+        st = lib.fd_decode_attention_fp8kv(r(q), r(k), r(v), None, None, FAKE, None, 0, 4,
+                                           r(out), FAKE, FAKE, 1 << 28, None)
+        msg = lib.fd_last_error().decode()
+        if not ok:
+            assert st == UNSUPPORTED and "32 query rows" in msg, msg
+        else:
+            assert "query rows" not in msg, msg
+
+
 @pytest.mark.parametrize("case,expected", [
     ("null_q", INVALID), ("null_seq", INVALID), ("null_ws", INVALID), ("rank", INVALID),
     ("hq_not_multiple", INVALID), ("kv_shape_mismatch", INVALID), ("dtype_mix", INVALID),
