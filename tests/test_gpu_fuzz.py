@@ -35,8 +35,9 @@ def draw(i, medium=False):
     fp8 = d == 128 and r.random() < 0.2
     f32 = not fp8 and r.random() < 0.15
     Q = r.choice([1, 1, 1, 2, 3, 4, 8])
-    wide_ok = not fp8 and not f32          # above 16 rows: bf16 tensor-core path only
-    G = r.choice([g for g in (1, 2, 4, 8, 16, 32, 64) if Q * g <= (64 if wide_ok else 16)])
+    # above 16 rows: the tensor-core paths only (bf16 up to 64 rows, FP8 up to 32)
+    max_rows = 16 if f32 else (32 if fp8 else 64)
+    G = r.choice([g for g in (1, 2, 4, 8, 16, 32, 64) if Q * g <= max_rows])
     Hkv = r.choice([1, 2, 3, 4, 8])
     B = r.randint(1, 5)
     paged = r.random() < 0.5
